@@ -32,8 +32,10 @@ h // (Hq/Hkv); scale 1/sqrt(head_dim); SwiGLU silu(gate)*up; greedy =
 lowest index among maxima; sampling = Gumbel-max over the top-k of
 logits/T, ordered (value desc, index asc), lowest index on ties.
 
-Everything is float32 (the precision the task fixes for this oracle);
-weights are the exact f32 values of their bf16 / Q8_0 storage.
+Everything is float32 (the precision the task fixes for this oracle).
+Weights are the exact f32 values of their bf16 storage; Q8_0 weights are
+d*q rounded once to f16, the value the tensor cores multiply by (the
+comparison is to run on the same rounded weights as the GPU).
 """
 from __future__ import annotations
 
@@ -86,14 +88,24 @@ def quant_q8_0(w: np.ndarray) -> np.ndarray:
     return out.reshape(rows, nb * 34)
 
 
-def weights_to_f32(raw) -> Dict[str, np.ndarray]:
-    """Map ``{name: synthetic.RawTensor}`` to ``{name: f32 array}``."""
+def round_to_f16(w: np.ndarray) -> np.ndarray:
+    """f32 -> nearest f16 (ties to even) -> f32."""
+    return w.astype(np.float16).astype(np.float32)
+
+
+def weights_to_f32(raw, q8_0_operand: str = "f16") -> Dict[str, np.ndarray]:
+    """Map ``{name: synthetic.RawTensor}`` to ``{name: f32 array}``.
+
+    Q8_0 matrices: the predictor computes with the dequantised weights as
+    rounded for its tensor-core operands, so ``q8_0_operand='f16'`` (the
+    default) gives f16(d*q); ``'exact'`` gives d*q itself."""
     out = {}
     for name, t in raw.items():
         if t.dtype == "bf16":
             out[name] = bf16_to_f32(t.data).reshape(t.shape)
         elif t.dtype == "q8_0":
-            out[name] = dequant_q8_0(t.data, t.shape[0], t.shape[1])
+            w = dequant_q8_0(t.data, t.shape[0], t.shape[1])
+            out[name] = round_to_f16(w) if q8_0_operand == "f16" else w
         elif t.dtype == "f16":
             out[name] = t.data.astype(np.float32).reshape(t.shape)
         elif t.dtype == "f32":
@@ -191,8 +203,8 @@ class Predictor:
         self.e0 = W["talker.codec_embd.weight"]
 
     @classmethod
-    def from_raw(cls, g, raw):
-        return cls(g, weights_to_f32(raw))
+    def from_raw(cls, g, raw, q8_0_operand: str = "f16"):
+        return cls(g, weights_to_f32(raw, q8_0_operand))
 
     # -- one decoder layer applied to one new position of every row ---------
     def layer_step(self, l: int, x: np.ndarray, pos: int, cache_k: list, cache_v: list) -> np.ndarray:

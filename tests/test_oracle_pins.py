@@ -511,3 +511,19 @@ def test_mutant_without_cache_append_is_caught():
         O.Predictor.layer_step = orig
     b = O.predict_frames_bruteforce(P, H, q0, forced=a["codes"])
     assert not np.allclose(a["logits"], b["logits"], rtol=1e-5, atol=1e-5)
+
+
+def test_q8_0_operand_rounding_is_nearest_f16():
+    """The f16 operand of a dequantised weight is d*q rounded to nearest-even,
+    which numpy's float16 conversion (a library routine) also gives; values
+    already on the f16 grid pass unchanged."""
+    rng = np.random.default_rng(14)
+    qq = rng.integers(-127, 128, size=(3, 64)).astype(np.int8)
+    dd = rng.uniform(1e-4, 2e-3, size=(3, 2)).astype(np.float16)
+    raw = {"m": S.RawTensor("m", S.Q8_0, (3, 64), S.pack_q8_0(qq, dd))}
+    exact = O.weights_to_f32(raw, "exact")["m"]
+    got = O.weights_to_f32(raw)["m"]
+    np.testing.assert_array_equal(got, exact.astype(np.float16).astype(np.float32))
+    assert np.abs(got - exact).max() <= np.abs(exact).max() * 2.0 ** -11
+    on_grid = np.float16([0.5, -0.25, 1.5e-3]).astype(np.float32)
+    np.testing.assert_array_equal(O.round_to_f16(on_grid), on_grid)
