@@ -1,0 +1,350 @@
+#!/usr/bin/env python3
+"""Throughput of the Code Predictor frame loop on GB300.
+
+One step = one qp_predict_frames call: the whole 15-step loop for a batch of
+B frames whose inputs are already resident in HBM.  Prints ONE JSON line
+(rank 0).  ``--impl reference`` times the CPU oracle instead, on the same
+workload and metric.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--config C] [--impl ours|reference]
+
+Configs (B frames): 1 = B1 greedy, 2 = B32 greedy (default), 3 = B128 greedy,
+4 = B256 top-k 50 sampling, 5 = B1024 greedy with Q8_0 weights.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "code-predictor frames/s (15 steps each) at batch B on 1 GB300; µs/step at B=1"
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# algorithmic work of one call ("Roofline")
+# ---------------------------------------------------------------------------
+
+def work_of(g, B: int, gemm_format: str, sampling: bool):
+    """(bytes, flops) one call must move / compute at minimum."""
+    d, qw, kvw, F, V, th = g.hidden, g.n_q_heads * g.head_dim, g.n_kv_heads * g.head_dim, g.ffn, g.vocab, g.talker_hidden
+    layer_params = (qw + 2 * kvw) * d + d * qw + 2 * F * d + d * F
+    head_params = V * d
+    proj_params = d * th
+    wb = 2.0 if gemm_format == "bf16" else 34.0 / 32.0
+    weight_bytes = wb * (g.n_steps * (g.layers * layer_params + head_params) + proj_params)
+    io = B * (th * 4 + 4 + g.n_steps * 4          # H, q0, codes
+              + th * 2 + (g.n_steps - 1) * d * 2)  # E0 row and the code-embedding rows gathered
+    if sampling:
+        io += B * g.n_steps * V * 4
+    positions = g.n_steps + 1
+    flops = B * (2 * positions * g.layers * layer_params + 2 * g.n_steps * head_params + 2 * 2 * proj_params)
+    for p in range(positions):   # attention: q.k and p.v over p+1 keys, every q head
+        flops += B * g.layers * g.n_q_heads * (p + 1) * g.head_dim * 4
+    return weight_bytes + io, float(flops)
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for f in sorted(glob.glob(os.path.join(ROOT, "codebook_rvq_code_gb300", "csrc", "*"))):
+        h.update(open(f, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(config_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current sources."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(config_name)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n and n[0]:
+            return int(n[0])
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+def time_oracle(g, raw, w, frames: int, budget_s: float):
+    """Run the oracle on the first `frames` frames of the workload until
+    about budget_s seconds have passed; frames/s."""
+    import oracle as O
+    P = O.Predictor.from_raw(g, raw)
+    H, q0 = w.H[:frames], w.q0[:frames]
+    gum = None if w.gumbel is None else w.gumbel[:frames]
+    done, t0 = 0, time.perf_counter()
+    while True:
+        O.predict_frames(P, H, q0, w.temperature, w.top_k, gum)
+        done += frames
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return done / el, done, el
+
+
+def reference_arm(args, g, raw, w):
+    import oracle as O
+    P = O.Predictor.from_raw(g, raw)
+    frames = min(w.B, 8)
+    H, q0 = w.H[:frames], w.q0[:frames]
+    gum = None if w.gumbel is None else w.gumbel[:frames]
+    for _ in range(args.warmup):
+        O.predict_frames(P, H, q0, w.temperature, w.top_k, gum)
+    times = []
+    for _ in range(args.steps):
+        t = time.perf_counter()
+        O.predict_frames(P, H, q0, w.temperature, w.top_k, gum)
+        times.append(time.perf_counter() - t)
+    sec = sum(times)
+    fps = frames * args.steps / sec
+    cores = oracle_threads()
+    sample = f"first {frames} of the {w.B} frames of {w.name}, full 15-step loop, per step"
+    return {
+        "impl": "reference", "metric": METRIC, "value": fps, "unit": "frames/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "frames_per_step": frames},
+        "cpu_baseline": {"value": fps, "unit": "frames/s", "cores": cores, "kind": "oracle", "sample": sample},
+        "e2e": {"value": fps, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# ---------------------------------------------------------------------------
+
+def main():
+    args = parse()
+    import numpy as np
+    import synthetic as S
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    g = S.Geometry()
+    w = S.make_workload(args.config, g)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        raw = S.workload_weights(w, g)
+        print(json.dumps(reference_arm(args, g, raw, w)), flush=True)
+        return
+
+    import torch
+    import torch.distributed as dist
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+
+    from codebook_rvq_code_gb300 import build as qb
+    qb.build()
+    import codebook_rvq_code_gb300 as qpk
+
+    raw = S.workload_weights(w, g)
+    cp = qpk.CodePredictor(g, max_batch=w.B)
+    cp.load_raw_weights(raw, device=dev)
+    B = w.B
+    H = torch.from_numpy(w.H).to(dev)
+    q0 = torch.from_numpy(w.q0).to(dev)
+    codes = torch.empty((B, g.n_steps), dtype=torch.int32, device=dev)
+    samp = None
+    if w.gumbel is not None:
+        samp = (w.temperature, w.top_k, torch.from_numpy(w.gumbel).to(dev))
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def call():
+        cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    if cp.device_status() != 0:
+        raise RuntimeError("device status set during warm-up")
+    if world > 1:
+        dist.barrier()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            flush.fill_(float(i))          # evict the previous call's lines from L2
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * B * args.steps / (total_ms / 1e3)
+    launches = cp.launches_per_call(B, samp is not None) * args.steps
+
+    # end to end through the host-buffer entry point: pinned H/q0 in, codes out
+    e2e = None
+    if not args.no_e2e:
+        Hh = torch.from_numpy(w.H).pin_memory()
+        qh = torch.from_numpy(w.q0).pin_memory()
+        ch = torch.empty((B, g.n_steps), dtype=torch.int32).pin_memory()
+        for _ in range(2):
+            cp.predict_host(Hh, qh, ch, sampling=samp, stream=stream)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            cp.predict_host(Hh, qh, ch, sampling=samp, stream=stream)
+        el = time.perf_counter() - t0
+        e2e = {"value": world * B * args.steps / el, "unit": "frames/s",
+               "h2d_bytes_per_step": int(Hh.numel() * 4 + qh.numel() * 4),
+               "d2h_bytes_per_step": int(ch.numel() * 4)}
+
+    if rank != 0:
+        cp.close()
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    hbm, tf_burst, tf_sust, peak_src = peaks()
+    nbytes, flops = work_of(g, B, w.gemm_format, samp is not None)
+    sec = ms_per_step / 1e3
+    t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tf_sust * 1e12)
+    if t_hbm >= t_tc:
+        roof = {"bound": "hbm", "achieved": nbytes / sec / 1e9, "peak": hbm, "unit": "GB/s"}
+    else:
+        roof = {"bound": "tensor", "achieved": flops / sec / 1e12, "peak": tf_sust, "unit": "TFLOP/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
+    roof["algorithmic_bytes_per_launch"] = nbytes
+    roof["algorithmic_flops_per_launch"] = flops
+    roof["traffic"] = recorded_traffic(w.name)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16" if w.gemm_format == "bf16" else "q8_0",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "steps_per_frame": g.n_steps,
+                   "l2": f"flushed between timed iterations ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "us_per_step": 1e3 * ms_per_step / g.n_steps,
+        "roofline": roof,
+        "gpu_launches": launches,
+        "clocks": clk.summary(),
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline:
+        fps, done, el = time_oracle(g, raw, w, min(B, 8), 10.0)
+        line["cpu_baseline"] = {"value": fps, "unit": "frames/s", "cores": oracle_threads(), "kind": "oracle",
+                                "sample": f"{done} frames ({min(B, 8)} per pass) of {w.name} in {el:.1f} s"}
+    cp.close()
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,211 @@
+"""Python binding of libqp, the GB300 Code Predictor library.
+
+Argument marshalling only: every step of the frame loop runs in the CUDA
+kernels of ``libqp.so`` behind the C ABI declared in ``include/qp.h``.
+Importing this package loads the library and fails loudly if it has not
+been built (``codebook_rvq_code_gb300.build.build()``); there is no CPU path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Dict, Optional
+
+from .build import LIB_PATH
+
+QP_OK = 0
+STATUS_NAMES = {
+    0: "QP_OK", 1: "QP_ERR_ARG", 2: "QP_ERR_STATE", 3: "QP_ERR_WEIGHT_MISSING", 4: "QP_ERR_WEIGHT_SHAPE",
+    5: "QP_ERR_WEIGHT_DTYPE", 6: "QP_ERR_CUDA", 7: "QP_ERR_TIMEOUT", 8: "QP_ERR_BAD_TOKEN", 9: "QP_ERR_OOM",
+    10: "QP_ERR_UNKNOWN_WEIGHT", 11: "QP_ERR_DUPLICATE_WEIGHT",
+}
+DTYPES = {"bf16": 0, "f16": 1, "f32": 2, "q8_0": 3}
+
+# every symbol include/qp.h declares
+EXPORTED = [
+    "qp_abi_version", "qp_status_string", "qp_default_geometry", "qp_create", "qp_load_weights",
+    "qp_predict_frames", "qp_predict_frames_ex", "qp_predict_frames_host", "qp_get_device_status",
+    "qp_launches_per_call", "qp_destroy",
+]
+
+
+class QpGeometry(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("hidden", "layers", "n_q_heads", "n_kv_heads", "head_dim", "ffn",
+                                             "vocab", "n_steps", "talker_hidden", "code_embed_dim", "q0_vocab")] + \
+               [("rms_eps", ctypes.c_float), ("rope_theta", ctypes.c_float)]
+
+
+class QpWeight(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("dtype", ctypes.c_int), ("dev_ptr", ctypes.c_void_p),
+                ("shape", ctypes.c_int64 * 2)]
+
+
+class QpSampling(ctypes.Structure):
+    _fields_ = [("temperature", ctypes.c_float), ("top_k", ctypes.c_int), ("gumbel", ctypes.c_void_p)]
+
+
+class QpError(RuntimeError):
+    def __init__(self, where: str, code: int):
+        super().__init__(f"{where}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise ImportError(f"libqp.so not built at {path}; run codebook_rvq_code_gb300.build.build()")
+    lib = ctypes.CDLL(path)
+    vp, i32, cp = ctypes.c_void_p, ctypes.c_int, ctypes.c_char_p
+    lib.qp_abi_version.restype = i32
+    lib.qp_status_string.restype = cp
+    lib.qp_status_string.argtypes = [i32]
+    lib.qp_default_geometry.restype = i32
+    lib.qp_default_geometry.argtypes = [ctypes.POINTER(QpGeometry)]
+    lib.qp_create.restype = i32
+    lib.qp_create.argtypes = [ctypes.POINTER(QpGeometry), i32, ctypes.POINTER(vp)]
+    lib.qp_load_weights.restype = i32
+    lib.qp_load_weights.argtypes = [vp, ctypes.POINTER(QpWeight), i32, vp]
+    lib.qp_predict_frames.restype = i32
+    lib.qp_predict_frames.argtypes = [vp, i32, vp, vp, vp, vp, vp]
+    lib.qp_predict_frames_ex.restype = i32
+    lib.qp_predict_frames_ex.argtypes = [vp, i32, vp, vp, vp, vp, ctypes.POINTER(QpSampling), vp, vp]
+    lib.qp_predict_frames_host.restype = i32
+    lib.qp_predict_frames_host.argtypes = [vp, i32, vp, vp, vp, ctypes.POINTER(QpSampling), vp]
+    lib.qp_get_device_status.restype = i32
+    lib.qp_get_device_status.argtypes = [vp, vp]
+    lib.qp_launches_per_call.restype = i32
+    lib.qp_launches_per_call.argtypes = [vp, i32, i32]
+    lib.qp_destroy.restype = None
+    lib.qp_destroy.argtypes = [vp]
+    return lib
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def lib() -> ctypes.CDLL:
+    global _LIB
+    if _LIB is None:
+        _LIB = load_library()
+    return _LIB
+
+
+def default_geometry() -> QpGeometry:
+    g = QpGeometry()
+    _check("qp_default_geometry", lib().qp_default_geometry(ctypes.byref(g)))
+    return g
+
+
+def geometry_from(obj) -> QpGeometry:
+    """A QpGeometry from any object with the same field names."""
+    g = QpGeometry()
+    for name, _ in QpGeometry._fields_:
+        setattr(g, name, getattr(obj, name))
+    return g
+
+
+def _check(where: str, code: int):
+    if code != QP_OK:
+        raise QpError(where, code)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else int(t.data_ptr())
+
+
+def _stream_ptr(stream) -> Optional[int]:
+    import torch
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream) or None
+
+
+class CodePredictor:
+    """One qp_handle: weights plus scratch for batches of up to max_batch frames."""
+
+    def __init__(self, geometry=None, max_batch: int = 1):
+        self._lib = lib()
+        self.geometry = default_geometry() if geometry is None else (
+            geometry if isinstance(geometry, QpGeometry) else geometry_from(geometry))
+        self.max_batch = max_batch
+        h = ctypes.c_void_p()
+        _check("qp_create", self._lib.qp_create(ctypes.byref(self.geometry), max_batch, ctypes.byref(h)))
+        self._h = h
+        self._keep = []
+
+    # -- weights -------------------------------------------------------------
+    def load_weights(self, tensors: Dict[str, tuple], stream=None):
+        """tensors: name -> (dtype tag, device tensor, shape); see qp_weight."""
+        arr = (QpWeight * len(tensors))()
+        names = []
+        for i, (name, (dt, t, shape)) in enumerate(tensors.items()):
+            nb = name.encode()
+            names.append(nb)
+            arr[i].name = nb
+            arr[i].dtype = DTYPES[dt]
+            arr[i].dev_ptr = int(t.data_ptr())
+            arr[i].shape[0] = int(shape[0])
+            arr[i].shape[1] = int(shape[1]) if len(shape) > 1 else 0
+        _check("qp_load_weights", self._lib.qp_load_weights(self._h, arr, len(tensors), _stream_ptr(stream)))
+
+    def load_raw_weights(self, raw, device="cuda", stream=None):
+        """Upload storage-format tensors (objects with .name .dtype .shape .data
+        numpy arrays) and hand them to qp_load_weights."""
+        import torch
+        up = {}
+        for name, t in raw.items():
+            data = torch.from_numpy(t.data.view("uint8").reshape(-1).copy()).to(device)
+            up[name] = (t.dtype, data, t.shape)
+        self.load_weights(up, stream=stream)
+        torch.cuda.synchronize()
+        return up
+
+    # -- prediction ----------------------------------------------------------
+    def predict(self, H, q0, out_codes=None, out_logits=None, sampling=None, forced=None, stream=None):
+        """H [B, talker_hidden] f32 cuda, q0 [B] int32 cuda.  sampling: None
+        or (temperature, top_k, gumbel [B, n_steps, vocab] f32 cuda).
+        Returns out_codes [B, n_steps] int32 (allocated if not given)."""
+        import torch
+        B = int(H.shape[0])
+        n = self.geometry.n_steps
+        if out_codes is None:
+            out_codes = torch.empty((B, n), dtype=torch.int32, device=H.device)
+        samp = None
+        if sampling is not None:
+            T, k, gum = sampling
+            samp = QpSampling(float(T), int(k), _ptr(gum))
+        _check("qp_predict_frames_ex", self._lib.qp_predict_frames_ex(
+            self._h, B, _ptr(H), _ptr(q0), _ptr(out_codes), _ptr(out_logits),
+            ctypes.byref(samp) if samp is not None else None, _ptr(forced), _stream_ptr(stream)))
+        return out_codes
+
+    def predict_host(self, H_host, q0_host, codes_host, sampling=None, stream=None):
+        """Host buffers (numpy or CPU tensors): copies in, predicts, copies the
+        codes back and synchronises, all inside the library call."""
+        samp = None
+        if sampling is not None:
+            T, k, gum = sampling
+            samp = QpSampling(float(T), int(k), _ptr(gum))
+
+        def hp(a):
+            return a.ctypes.data if hasattr(a, "ctypes") else int(a.data_ptr())
+        B = int(H_host.shape[0])
+        _check("qp_predict_frames_host", self._lib.qp_predict_frames_host(
+            self._h, B, hp(H_host), hp(q0_host), hp(codes_host),
+            ctypes.byref(samp) if samp is not None else None, _stream_ptr(stream)))
+        return codes_host
+
+    def device_status(self, stream=None) -> int:
+        return int(self._lib.qp_get_device_status(self._h, _stream_ptr(stream)))
+
+    def launches_per_call(self, B: int, sampling: bool = False) -> int:
+        return int(self._lib.qp_launches_per_call(self._h, B, int(sampling)))
+
+    def close(self):
+        if getattr(self, "_h", None):
+            self._lib.qp_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

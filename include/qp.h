@@ -1,0 +1,179 @@
+/*
+ * qp.h -- C ABI of the GB300 Code Predictor library (libqp.so).
+ *
+ * The library runs the per-frame Code Predictor loop of Qwen3-TTS: for every
+ * audio frame, given the Talker's hidden state H and first-codebook token q0,
+ * a 5-layer causal transformer takes 15 autoregressive steps and emits the
+ * residual-codebook tokens q1..q15 (16 codebooks with q0).  Frames from many
+ * requests are batched into one call.
+ *
+ *   - 15 fixed steps per frame, a preallocated KV cache, the whole frame loop
+ *     run as one fixed GPU program instead of a host-driven sequence:
+ *     "テキスト音声合成モデルを50ミリ秒未満で応答させる方法", section
+ *     "Qwen3-TTSの最適化方法", item 3.
+ *   - The predictor is a stateless batched step whose inputs are the frame's
+ *     H (and q0) and whose outputs are the residual codes:
+ *     "拆解 Qwen3-TTS：OpenVINO 移植过程中的图分离与调度实践", sections 1, 2.2.
+ *   - Geometry, tensor names and shapes, Q8_0 storage, and the rule that a
+ *     loader fails on missing or unmapped tensors: "rightkit-qts 0.2.3 -
+ *     Qwen3-TTS 1.7B -> QTS GGUF", sections "Loader contract", "Expected
+ *     verification shapes", "Upstream differences & verification scope".
+ *   - Sampling stays caller-controlled (same page, "Usage"): the caller
+ *     passes temperature, top-k and the Gumbel noise itself.
+ *
+ * Conventions for every entry point:
+ *   - Device pointers are CUDA device addresses on the handle's device,
+ *     owned by the caller, read/written asynchronously on the given stream.
+ *   - qp_stream is a cudaStream_t passed as void*; NULL means the legacy
+ *     default stream.
+ *   - A call that returns anything but QP_OK enqueued nothing.
+ *   - Errors the GPU detects (an out-of-range token, a stalled grid barrier)
+ *     are latched in a device status word; qp_get_device_status reads and
+ *     clears it.  Kernels never trap: a bad token is clamped for addressing
+ *     and reported.
+ *   - A handle may be used from one host thread at a time.
+ */
+#ifndef QP_H
+#define QP_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define QP_ABI_VERSION 1
+
+typedef enum qp_status {
+  QP_OK = 0,
+  QP_ERR_ARG = 1,            /* null pointer, B out of range, bad geometry  */
+  QP_ERR_STATE = 2,          /* weights not loaded / already loaded          */
+  QP_ERR_WEIGHT_MISSING = 3, /* a required tensor was not supplied           */
+  QP_ERR_WEIGHT_SHAPE = 4,   /* shape differs from the geometry              */
+  QP_ERR_WEIGHT_DTYPE = 5,   /* storage type not accepted for that tensor    */
+  QP_ERR_CUDA = 6,           /* a CUDA runtime call failed                   */
+  QP_ERR_TIMEOUT = 7,        /* device: a grid barrier gave up waiting       */
+  QP_ERR_BAD_TOKEN = 8,      /* device: q0 or a forced code out of range     */
+  QP_ERR_OOM = 9,            /* device allocation failed in create/load      */
+  QP_ERR_UNKNOWN_WEIGHT = 10,/* a supplied name is not a predictor tensor    */
+  QP_ERR_DUPLICATE_WEIGHT = 11
+} qp_status;
+
+/* Storage types of weight tensors. */
+typedef enum qp_dtype {
+  QP_BF16 = 0,
+  QP_F16 = 1,
+  QP_F32 = 2,
+  QP_Q8_0 = 3   /* blocks of 32 along the input dim: {f16 d; int8 q[32]},
+                   34 bytes, value = d * q (GGUF Q8_0)                        */
+} qp_dtype;
+
+/* Predictor geometry.  qp_default_geometry fills the 1.7B Code Predictor:
+ * hidden 1024, 5 layers, 16 q-heads / 8 kv-heads of 128, FFN 3072, 2048-entry
+ * codebooks, 15 steps, Talker width 2048, 1024-wide code embeddings that
+ * enter unprojected, 2048-entry q0 table, RMSNorm eps 1e-6, RoPE theta 1e6.
+ * Supported: head_dim 128; n_q_heads a multiple of n_kv_heads;
+ * code_embed_dim == hidden; hidden, ffn, talker_hidden and vocab multiples
+ * of 128; 1 <= n_steps <= 15. */
+typedef struct qp_geometry {
+  int hidden, layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_steps;
+  int talker_hidden, code_embed_dim, q0_vocab;
+  float rms_eps, rope_theta;
+} qp_geometry;
+
+/* One weight tensor handed to qp_load_weights.
+ * name:   the predictor-file name, e.g. "code_pred.blk.3.ffn_up.weight",
+ *         "code_pred.small_to_mtp_projection.bias",
+ *         "code_pred.codec_embd.7.weight", "code_pred.lm_head.0.weight",
+ *         or "talker.codec_embd.weight" (the q0 table).
+ * dtype:  matrices (projection weight, attn_q/k/v/output, ffn_gate/up/down,
+ *         lm_head.*) accept QP_BF16 or QP_Q8_0 -- all of them the same one;
+ *         embedding tables accept QP_BF16; vectors (norms, bias) QP_F32.
+ * dev_ptr: device memory, row-major HF layout [shape[0], shape[1]]; a Q8_0
+ *         tensor is its raw block stream, shape[0] rows of shape[1]/32
+ *         blocks.  Vectors use shape = {n, 0}. */
+typedef struct qp_weight {
+  const char* name;
+  qp_dtype dtype;
+  const void* dev_ptr;
+  int64_t shape[2];
+} qp_weight;
+
+/* Sampling: z = logits / temperature; the top_k largest z (ties by lower
+ * index) form the candidate set; the code is argmax over it of
+ * z + gumbel[b, step, i], lowest index on ties.  gumbel is a device array
+ * [B, n_steps, vocab] f32 of standard Gumbel noise supplied by the caller. */
+typedef struct qp_sampling {
+  float temperature;   /* > 0 */
+  int top_k;           /* 1 .. vocab */
+  const float* gumbel; /* device, [B, n_steps, vocab] */
+} qp_sampling;
+
+typedef struct qp_handle qp_handle;
+typedef void* qp_stream;
+
+/* Library ABI version (QP_ABI_VERSION). */
+int qp_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* qp_status_string(qp_status s);
+
+/* Fill *g with the default geometry.  QP_ERR_ARG if g is NULL. */
+qp_status qp_default_geometry(qp_geometry* g);
+
+/* Create a handle on the current CUDA device for batches of up to
+ * max_batch frames (1 <= max_batch <= 65536).  Allocates the library-owned
+ * scratch (activations, KV cache, status word) sized for max_batch.  On
+ * error *out is set to NULL. */
+qp_status qp_create(const qp_geometry* g, int max_batch, qp_handle** out);
+
+/* Copy and repack the n weight tensors into library-owned device memory, on
+ * stream s.  All 89 tensors must be supplied exactly once (the 88 of the
+ * predictor file plus talker.codec_embd.weight); a missing, duplicate,
+ * unknown, mis-shaped or wrongly typed tensor fails the whole load and
+ * nothing is enqueued.  The caller may free its buffers once s has reached
+ * this point.  May be called again to replace all weights. */
+qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream s);
+
+/* Greedy prediction for B frames (1 <= B <= max_batch), enqueued on s.
+ *   H          device, [B, talker_hidden] f32, row-major
+ *   q0         device, [B] int32 in [0, q0_vocab)
+ *   out_codes  device, [B, n_steps] int32: q1..q15 per frame
+ *   out_logits device, [B, n_steps, vocab] f32, or NULL to skip */
+qp_status qp_predict_frames(qp_handle* h, int B, const float* H, const int32_t* q0,
+                            int32_t* out_codes, float* out_logits, qp_stream s);
+
+/* As qp_predict_frames, plus:
+ *   samp          NULL for greedy, else Gumbel top-k sampling (above)
+ *   forced_codes  NULL, or device [B, n_steps] int32: teacher forcing.  The
+ *                 input of step k+1 embeds forced_codes[b, k-1] instead of
+ *                 the decided code; out_codes still holds the decisions. */
+qp_status qp_predict_frames_ex(qp_handle* h, int B, const float* H, const int32_t* q0,
+                               int32_t* out_codes, float* out_logits,
+                               const qp_sampling* samp, const int32_t* forced_codes,
+                               qp_stream s);
+
+/* Host-buffer variant: H_host [B, talker_hidden] f32, q0_host [B] int32 and
+ * codes_host [B, n_steps] int32 are host memory (pinned or pageable).
+ * Copies the inputs to library-owned device buffers, predicts (greedy, or
+ * sampling with a DEVICE gumbel array when samp is not NULL), copies the
+ * codes back and synchronises s before returning. */
+qp_status qp_predict_frames_host(qp_handle* h, int B, const float* H_host,
+                                 const int32_t* q0_host, int32_t* codes_host,
+                                 const qp_sampling* samp, qp_stream s);
+
+/* Synchronise s, read and clear the device status word: QP_OK, or the
+ * first device-detected error since the last read. */
+qp_status qp_get_device_status(qp_handle* h, qp_stream s);
+
+/* Number of GPU kernel launches one qp_predict_frames_ex call with these
+ * arguments enqueues (for launch accounting); -1 on bad arguments. */
+int qp_launches_per_call(qp_handle* h, int B, int sampling);
+
+/* Free everything the handle owns (synchronises the device first). */
+void qp_destroy(qp_handle* h);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* QP_H */
