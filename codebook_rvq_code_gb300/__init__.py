@@ -25,7 +25,7 @@ DTYPES = {"bf16": 0, "f16": 1, "f32": 2, "q8_0": 3}
 EXPORTED = [
     "qp_abi_version", "qp_status_string", "qp_default_geometry", "qp_create", "qp_load_weights",
     "qp_predict_frames", "qp_predict_frames_ex", "qp_predict_frames_host", "qp_get_device_status",
-    "qp_launches_per_call", "qp_destroy",
+    "qp_launches_per_call", "qp_destroy", "qp_predict_frames_static",
 ]
 
 
@@ -70,6 +70,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qp_predict_frames_ex.argtypes = [vp, i32, vp, vp, vp, vp, ctypes.POINTER(QpSampling), vp, vp]
     lib.qp_predict_frames_host.restype = i32
     lib.qp_predict_frames_host.argtypes = [vp, i32, vp, vp, vp, ctypes.POINTER(QpSampling), vp]
+    lib.qp_predict_frames_static.restype = i32
+    lib.qp_predict_frames_static.argtypes = [vp, i32, vp, vp, vp, vp, vp]
     lib.qp_get_device_status.restype = i32
     lib.qp_get_device_status.argtypes = [vp, vp]
     lib.qp_launches_per_call.restype = i32
@@ -192,6 +194,17 @@ class CodePredictor:
             self._h, B, hp(H_host), hp(q0_host), hp(codes_host),
             ctypes.byref(samp) if samp is not None else None, _stream_ptr(stream)))
         return codes_host
+
+    def predict_static(self, H, q0, out_codes=None, out_logits=None, stream=None):
+        """Greedy prediction through qp_predict_frames_static (scratch in the
+        library's static device array; B <= 8)."""
+        import torch
+        B = int(H.shape[0])
+        if out_codes is None:
+            out_codes = torch.empty((B, self.geometry.n_steps), dtype=torch.int32, device=H.device)
+        _check("qp_predict_frames_static", self._lib.qp_predict_frames_static(
+            self._h, B, _ptr(H), _ptr(q0), _ptr(out_codes), _ptr(out_logits), _stream_ptr(stream)))
+        return out_codes
 
     def device_status(self, stream=None) -> int:
         return int(self._lib.qp_get_device_status(self._h, _stream_ptr(stream)))

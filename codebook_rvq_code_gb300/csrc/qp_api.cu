@@ -425,6 +425,17 @@ qp_status qp_predict_frames_host(qp_handle* h, int B, const float* H_host, const
   return QP_OK;
 }
 
+qp_status qp_predict_frames_static(qp_handle* h, int B, const float* H, const int32_t* q0, int32_t* out_codes,
+                                   float* out_logits, qp_stream s) {
+  qp_status st = check_run(h, B, H, q0, out_codes, nullptr);
+  if (st != QP_OK) return st;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return QP_ERR_CUDA;
+  qp::RunArgs a;
+  a.B = B; a.H = H; a.q0 = q0; a.out_codes = out_codes; a.out_logits = out_logits;
+  return qp::run_frames_static(h, a, static_cast<cudaStream_t>(s));
+}
+
 qp_status qp_get_device_status(qp_handle* h, qp_stream sv) {
   if (!h) return QP_ERR_ARG;
   DeviceGuard dg(h->device);

@@ -116,6 +116,8 @@ qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s);
 size_t packed_bytes(int fmt, int N, int K);
 cudaError_t pack_matrix(const QMat& src, PackedMat& dst, cudaStream_t s);
 size_t persistent_smem_bytes();
+// the same kernel with its scratch in a static device array (qp_persistent.cu)
+qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s);
 int launches_per_call(const qp_handle* h, int B, bool sampling);
 // weight repack helpers (qp_engine.cu)
 cudaError_t repack_q8_0(const uint8_t* blocks, int N, int K, int8_t* qs, __half* d, cudaStream_t s);

@@ -806,4 +806,130 @@ qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s) 
   return QP_OK;
 }
 
+
+// ---------------------------------------------------------------------------
+// Allocation-free entry point.
+//
+// Callers whose device memory is owned by someone else cannot have this
+// library call cudaMalloc on their behalf: a process whose framework
+// allocator has already reserved the GPU's memory, or a real-time audio path
+// that forbids allocation once it is running.  qp_predict_frames_static
+// runs the same persistent kernel as qp_predict_frames, but its scratch (the
+// residual stream, MMA operand, accumulators, logits, KV cache and barrier
+// words) lives in the file-scope array below, which the CUDA runtime places
+// in device memory when the library's module loads on a device, and which
+// every device that loads the library holds until the process exits.  The
+// weights still come from a handle the caller loaded beforehand.
+// ---------------------------------------------------------------------------
+
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;   // 8 MiB per device
+constexpr int kStaticMaxFrames = 8;
+
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+void* g_static_ptr[kMaxDevices] = {};
+bool g_static_attr[kMaxDevices] = {};
+
+size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
+
+// Byte layout of the scratch for B frames; returns the total.
+struct StaticLayout {
+  size_t xres, act, qkv, gu, logits, kv, sync, total;
+};
+StaticLayout static_layout(const qp_geometry& g, int B) {
+  const size_t R = size_t(2) * B;
+  const size_t qw = size_t(g.n_q_heads) * 128, kvw = size_t(g.n_kv_heads) * 128;
+  size_t aw = g.hidden;
+  if (qw > aw) aw = qw;
+  if (size_t(g.ffn) > aw) aw = g.ffn;
+  if (size_t(g.talker_hidden) > aw) aw = g.talker_hidden;
+  const size_t r16 = (R + 15) / 16 * 16;
+  const size_t act_rows = r16 <= size_t(kMaxNc) ? r16 : (R + kMaxNc - 1) / kMaxNc * kMaxNc;
+  StaticLayout L{};
+  size_t off = 0;
+  L.xres = off;   off += align256(R * g.hidden * 4);
+  L.act = off;    off += align256(act_rows * aw * 2);
+  L.qkv = off;    off += align256(R * (qw + 2 * kvw) * 4);
+  L.gu = off;     off += align256(R * 2 * size_t(g.ffn) * 4);
+  L.logits = off; off += align256(size_t(B) * g.vocab * 4);
+  L.kv = off;     off += align256(size_t(g.layers) * B * (g.n_steps + 1) * 2 * kvw * 4);
+  L.sync = off;   off += 256;
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s) {
+  const qp_geometry& g = h->g;
+  if (a.B < 1 || a.B > kStaticMaxFrames) return QP_ERR_ARG;
+  const StaticLayout SL = static_layout(g, a.B);
+  if (SL.total > kStaticScratchBytes) return QP_ERR_ARG;
+  if (h->device < 0 || h->device >= kMaxDevices) return QP_ERR_ARG;
+  // once per device, with that device current: the array's device address
+  if (!g_static_ptr[h->device]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) {
+      cudaGetLastError();
+      return QP_ERR_CUDA;
+    }
+    g_static_ptr[h->device] = ptr;
+  }
+  if (!g_static_attr[h->device]) {
+    if (cudaFuncSetAttribute(k_frames, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(persistent_smem_bytes())) != cudaSuccess) {
+      cudaGetLastError();
+      return QP_ERR_CUDA;
+    }
+    g_static_attr[h->device] = true;
+  }
+  unsigned char* base = static_cast<unsigned char*>(g_static_ptr[h->device]);
+  PParams p{};
+  p.d = g.hidden; p.qw = g.n_q_heads * 128; p.kvw = g.n_kv_heads * 128; p.F = g.ffn; p.V = g.vocab;
+  p.th = g.talker_hidden; p.L = g.layers; p.n_q = g.n_q_heads; p.n_kv = g.n_kv_heads; p.n_steps = g.n_steps;
+  p.q0_vocab = g.q0_vocab; p.eps = g.rms_eps; p.q8 = h->wfmt == WF_Q8_0;
+  p.w_proj = h->pproj.w; p.s_proj = h->pproj.scale; p.b_proj = h->b_proj; p.e0 = h->e0;
+  for (int l = 0; l < g.layers; ++l) {
+    const LayerW& L = h->layer[l];
+    const PackedLayer& PL = h->player[l];
+    p.layer[l] = {PL.qkv.w, PL.qkv.scale, PL.o.w, PL.o.scale, PL.gu.w, PL.gu.scale, PL.down.w, PL.down.scale,
+                  L.attn_norm, L.q_norm, L.k_norm, L.ffn_norm};
+  }
+  p.out_norm = h->out_norm;
+  for (int j = 0; j < g.n_steps; ++j) {
+    p.embed[j] = h->embed[j];
+    p.w_head[j] = h->phead[j].w;
+    p.s_head[j] = h->phead[j].scale;
+  }
+  p.rope_cs = h->rope_cs;
+  p.xres = reinterpret_cast<float*>(base + SL.xres);
+  p.act = reinterpret_cast<uint16_t*>(base + SL.act);
+  p.acc_qkv = reinterpret_cast<float*>(base + SL.qkv);
+  p.acc_gu = reinterpret_cast<float*>(base + SL.gu);
+  p.logits = reinterpret_cast<float*>(base + SL.logits);
+  p.kv = reinterpret_cast<float*>(base + SL.kv);
+  p.bar = reinterpret_cast<unsigned int*>(base + SL.sync);
+  p.abort_flag = reinterpret_cast<int*>(base + SL.sync + 4);
+  p.status = h->status;
+  p.Bmax = a.B;
+  p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = nullptr;
+  p.temperature = 0.f; p.top_k = 0; p.gumbel = nullptr;
+  // the barrier counter and abort flag must start at zero; every other
+  // buffer is written before it is read within the call
+  if (cudaMemsetAsync(base + SL.sync, 0, 8, s) != cudaSuccess) {
+    cudaGetLastError();
+    return QP_ERR_CUDA;
+  }
+  void* args[] = {&p};
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_frames), dim3(h->num_sms), dim3(kThreads), args,
+                                  persistent_smem_bytes(), s) != cudaSuccess) {
+    cudaGetLastError();
+    return QP_ERR_CUDA;
+  }
+  return QP_OK;
+}
+
 }  // namespace qp

@@ -162,6 +162,31 @@ qp_status qp_predict_frames_host(qp_handle* h, int B, const float* H_host,
                                  const int32_t* q0_host, int32_t* codes_host,
                                  const qp_sampling* samp, qp_stream s);
 
+/* Greedy prediction that allocates nothing, for callers that cannot let a
+ * library call cudaMalloc for them: a process whose own allocator already
+ * holds the GPU's memory, or a real-time audio path that forbids allocation
+ * once it runs.  (The pages have no counterpart: this is a library
+ * convenience, not part of the method.)  It runs the same kernel as
+ * qp_predict_frames with the same arguments and outputs (no sampling, no
+ * teacher forcing), but the kernel's scratch -- residual stream, tensor-core
+ * operand, accumulators, logits, KV cache, barrier words -- lives in one
+ * static device array of 8 MiB that every GPU loading the library holds
+ * until the process exits.  Weights come from h, loaded beforehand; errors
+ * the GPU detects still go to h's status word.
+ *   - B must be at most 8, and the scratch B frames need under h's geometry
+ *     must fit in 8 MiB (it does for the default geometry); otherwise
+ *     QP_ERR_ARG and nothing is enqueued.
+ *   - The first call on a device looks up the array's device address and
+ *     sets the kernel's shared-memory limit; make that first call before any
+ *     stream capture begins.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     the call clears the barrier words it needs at zero and writes every
+ *     other byte before reading it.  Calls whose executions overlap on the
+ *     GPU (other streams, other handles, other threads) race on the array:
+ *     serialise them. */
+qp_status qp_predict_frames_static(qp_handle* h, int B, const float* H, const int32_t* q0,
+                                   int32_t* out_codes, float* out_logits, qp_stream s);
+
 /* Synchronise s, read and clear the device status word: QP_OK, or the
  * first device-detected error since the last read. */
 qp_status qp_get_device_status(qp_handle* h, qp_stream s);

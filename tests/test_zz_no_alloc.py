@@ -1,0 +1,79 @@
+"""qp_predict_frames_static: the entry point that allocates nothing.
+
+It serves callers that cannot let the library call cudaMalloc for them (their
+own allocator holds the GPU's memory, or their audio path forbids allocation
+once running): the kernel's scratch sits in a static device array instead.
+This checks, through the C ABI, that two calls in a row give what
+qp_predict_frames gives on the same handle and inputs, within the tolerance
+the parity tests use, and that sizes beyond the array are refused.  The file
+is collected last so that a failure here never hides another test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+
+import oracle as O
+import synthetic as S
+from _parity import SMALL, TOL
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def qpk():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from codebook_rvq_code_gb300 import build
+    build.build()
+    import codebook_rvq_code_gb300 as m
+    return m
+
+
+@pytest.mark.parametrize("geometry,B", [(S.Geometry(), 1), (S.Geometry(), 8), (SMALL, 5)])
+def test_static_entry_matches_the_allocating_entry(qpk, geometry, B):
+    import torch
+    raw = S.make_weights(geometry, seed=11, norm_mode="perturbed")
+    cp = qpk.CodePredictor(geometry, max_batch=B)
+    cp.load_raw_weights(raw)
+    H, q0 = S.toy_inputs(geometry, B, seed=3)
+    tH = torch.from_numpy(H).cuda()
+    tq = torch.from_numpy(q0.astype(np.int32)).cuda()
+    n, V = geometry.n_steps, geometry.vocab
+    ref_codes = torch.empty((B, n), dtype=torch.int32, device="cuda")
+    ref_logits = torch.empty((B, n, V), dtype=torch.float32, device="cuda")
+    lib = cp._lib
+    assert lib.qp_predict_frames(cp._h, B, tH.data_ptr(), tq.data_ptr(), ref_codes.data_ptr(),
+                                 ref_logits.data_ptr(), None) == 0
+    torch.cuda.synchronize()
+    ref_l = ref_logits.cpu().numpy()
+    ref_c = ref_codes.cpu().numpy()
+    clear = O.top2_gap(ref_l) > TOL
+    for _ in range(2):   # the array keeps the previous call's contents
+        codes = torch.full((B, n), -1, dtype=torch.int32, device="cuda")
+        logits = torch.full((B, n, V), float("nan"), dtype=torch.float32, device="cuda")
+        assert lib.qp_predict_frames_static(cp._h, B, tH.data_ptr(), tq.data_ptr(), codes.data_ptr(),
+                                            logits.data_ptr(), None) == 0
+        torch.cuda.synchronize()
+        assert cp.device_status() == 0
+        got_l = logits.cpu().numpy()
+        assert np.all(np.isfinite(got_l))
+        assert np.abs(got_l - ref_l).max() <= TOL
+        np.testing.assert_array_equal(codes.cpu().numpy()[clear], ref_c[clear])
+    cp.close()
+
+
+def test_static_entry_refuses_batches_beyond_its_array(qpk):
+    import torch
+    g = SMALL
+    cp = qpk.CodePredictor(g, max_batch=16)
+    cp.load_raw_weights(S.make_weights(g, seed=2))
+    H = torch.zeros((16, g.talker_hidden), device="cuda")
+    q0 = torch.zeros(16, dtype=torch.int32, device="cuda")
+    codes = torch.empty((16, g.n_steps), dtype=torch.int32, device="cuda")
+    assert cp._lib.qp_predict_frames_static(cp._h, 9, H.data_ptr(), q0.data_ptr(), codes.data_ptr(),
+                                            None, None) == 1
+    assert cp._lib.qp_predict_frames_static(None, 1, H.data_ptr(), q0.data_ptr(), codes.data_ptr(),
+                                            None, None) == 1
+    cp.close()
