@@ -26,6 +26,7 @@ EXPORTED = [
     "qp_abi_version", "qp_status_string", "qp_default_geometry", "qp_create", "qp_load_weights",
     "qp_predict_frames", "qp_predict_frames_ex", "qp_predict_frames_host", "qp_get_device_status",
     "qp_launches_per_call", "qp_destroy", "qp_predict_frames_static",
+    "qp_trace_enable", "qp_trace_read",   # include/qp_debug.h
 ]
 
 
@@ -78,6 +79,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qp_launches_per_call.argtypes = [vp, i32, i32]
     lib.qp_destroy.restype = None
     lib.qp_destroy.argtypes = [vp]
+    lib.qp_trace_enable.restype = i32
+    lib.qp_trace_enable.argtypes = [vp, i32]
+    lib.qp_trace_read.restype = i32
+    lib.qp_trace_read.argtypes = [vp, vp, i32, ctypes.POINTER(ctypes.c_int)]
     return lib
 
 
@@ -205,6 +210,20 @@ class CodePredictor:
         _check("qp_predict_frames_static", self._lib.qp_predict_frames_static(
             self._h, B, _ptr(H), _ptr(q0), _ptr(out_codes), _ptr(out_logits), _stream_ptr(stream)))
         return out_codes
+
+    def trace(self, enable: bool = True):
+        """Turn the phase trace of include/qp_debug.h on or off."""
+        _check("qp_trace_enable", self._lib.qp_trace_enable(self._h, int(enable)))
+
+    def read_trace(self, phases: int):
+        """The last call's stamps as a numpy array [phases, n_cta, 2] (ns)."""
+        import numpy as np
+        n_sm = ctypes.c_int(0)
+        buf = np.zeros(phases * 1024 * 2, dtype=np.uint64)
+        got = self._lib.qp_trace_read(self._h, buf.ctypes.data, phases, ctypes.byref(n_sm))
+        if got < 0:
+            raise QpError("qp_trace_read", QP_ERR_STATE)
+        return buf[: got * n_sm.value * 2].reshape(got, n_sm.value, 2)
 
     def device_status(self, stream=None) -> int:
         return int(self._lib.qp_get_device_status(self._h, _stream_ptr(stream)))

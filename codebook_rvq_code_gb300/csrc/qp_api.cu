@@ -1,4 +1,4 @@
-// C ABI of libqp: handle life cycle, weight validation and repacking, and the
+// C ABI of libqp: handle life cycle, weight validation and packing, and the
 // argument checks in front of the frame loop.  See include/qp.h.
 #include <cmath>
 #include <cstdio>
@@ -9,8 +9,7 @@
 #include <vector>
 
 #include "qp_internal.h"
-
-using qp::QMat;
+#include "../../include/qp_debug.h"
 
 namespace {
 
@@ -50,50 +49,46 @@ T* carve(char*& p, size_t count) {
 template <typename T>
 size_t carve_size(size_t count) { return (count * sizeof(T) + 255) & ~size_t(255); }
 
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
 // What a tensor name maps to, and the shape it must have.
 struct Slot {
   enum Kind { MATRIX, EMBED, VECTOR } kind;
   int64_t rows, cols;   // cols = 0 for vectors
-  int role;             // see Role
-  int layer, index;
-};
-enum Role {
-  R_PROJ_W, R_PROJ_B, R_OUT_NORM, R_E0, R_EMBED, R_HEAD,
-  R_ATTN_NORM, R_Q, R_K, R_V, R_O, R_QN, R_KN, R_FFN_NORM, R_GATE, R_UP, R_DOWN
 };
 
 std::unordered_map<std::string, Slot> build_slots(const qp_geometry& g) {
   std::unordered_map<std::string, Slot> m;
   const int64_t d = g.hidden, qw = int64_t(g.n_q_heads) * g.head_dim,
                 kvw = int64_t(g.n_kv_heads) * g.head_dim;
-  m["code_pred.small_to_mtp_projection.weight"] = {Slot::MATRIX, d, g.talker_hidden, R_PROJ_W, -1, -1};
-  m["code_pred.small_to_mtp_projection.bias"] = {Slot::VECTOR, d, 0, R_PROJ_B, -1, -1};
-  m["code_pred.output_norm.weight"] = {Slot::VECTOR, d, 0, R_OUT_NORM, -1, -1};
-  m["talker.codec_embd.weight"] = {Slot::EMBED, g.q0_vocab, g.talker_hidden, R_E0, -1, -1};
+  m["code_pred.small_to_mtp_projection.weight"] = {Slot::MATRIX, d, g.talker_hidden};
+  m["code_pred.small_to_mtp_projection.bias"] = {Slot::VECTOR, d, 0};
+  m["code_pred.output_norm.weight"] = {Slot::VECTOR, d, 0};
+  m["talker.codec_embd.weight"] = {Slot::EMBED, g.q0_vocab, g.talker_hidden};
   for (int j = 0; j < g.n_steps; ++j) {
-    m["code_pred.codec_embd." + std::to_string(j) + ".weight"] = {Slot::EMBED, g.vocab, g.code_embed_dim, R_EMBED, -1, j};
-    m["code_pred.lm_head." + std::to_string(j) + ".weight"] = {Slot::MATRIX, g.vocab, d, R_HEAD, -1, j};
+    m["code_pred.codec_embd." + std::to_string(j) + ".weight"] = {Slot::EMBED, g.vocab, g.code_embed_dim};
+    m["code_pred.lm_head." + std::to_string(j) + ".weight"] = {Slot::MATRIX, g.vocab, d};
   }
   for (int l = 0; l < g.layers; ++l) {
     std::string p = "code_pred.blk." + std::to_string(l) + ".";
-    m[p + "attn_norm.weight"] = {Slot::VECTOR, d, 0, R_ATTN_NORM, l, -1};
-    m[p + "attn_q.weight"] = {Slot::MATRIX, qw, d, R_Q, l, -1};
-    m[p + "attn_k.weight"] = {Slot::MATRIX, kvw, d, R_K, l, -1};
-    m[p + "attn_v.weight"] = {Slot::MATRIX, kvw, d, R_V, l, -1};
-    m[p + "attn_output.weight"] = {Slot::MATRIX, d, qw, R_O, l, -1};
-    m[p + "attn_q_norm.weight"] = {Slot::VECTOR, g.head_dim, 0, R_QN, l, -1};
-    m[p + "attn_k_norm.weight"] = {Slot::VECTOR, g.head_dim, 0, R_KN, l, -1};
-    m[p + "ffn_norm.weight"] = {Slot::VECTOR, d, 0, R_FFN_NORM, l, -1};
-    m[p + "ffn_gate.weight"] = {Slot::MATRIX, g.ffn, d, R_GATE, l, -1};
-    m[p + "ffn_up.weight"] = {Slot::MATRIX, g.ffn, d, R_UP, l, -1};
-    m[p + "ffn_down.weight"] = {Slot::MATRIX, d, g.ffn, R_DOWN, l, -1};
+    m[p + "attn_norm.weight"] = {Slot::VECTOR, d, 0};
+    m[p + "attn_q.weight"] = {Slot::MATRIX, qw, d};
+    m[p + "attn_k.weight"] = {Slot::MATRIX, kvw, d};
+    m[p + "attn_v.weight"] = {Slot::MATRIX, kvw, d};
+    m[p + "attn_output.weight"] = {Slot::MATRIX, d, qw};
+    m[p + "attn_q_norm.weight"] = {Slot::VECTOR, g.head_dim, 0};
+    m[p + "attn_k_norm.weight"] = {Slot::VECTOR, g.head_dim, 0};
+    m[p + "ffn_norm.weight"] = {Slot::VECTOR, d, 0};
+    m[p + "ffn_gate.weight"] = {Slot::MATRIX, g.ffn, d};
+    m[p + "ffn_up.weight"] = {Slot::MATRIX, g.ffn, d};
+    m[p + "ffn_down.weight"] = {Slot::MATRIX, d, g.ffn};
   }
   return m;
 }
 
 size_t matrix_bytes(int fmt, int64_t N, int64_t K) {
-  if (fmt == qp::WF_BF16) return carve_size<uint16_t>(size_t(N) * K);
-  return carve_size<int8_t>(size_t(N) * K) + carve_size<__half>(size_t(N) * (K / 32));
+  return fmt == qp::WF_BF16 ? carve_size<uint8_t>(size_t(N) * K * 2)
+                            : carve_size<uint8_t>(size_t(N) * K) + carve_size<__half>(size_t(N) * (K / 32));
 }
 
 }  // namespace
@@ -111,7 +106,7 @@ const char* qp_status_string(qp_status s) {
     case QP_ERR_WEIGHT_SHAPE: return "weight tensor has the wrong shape";
     case QP_ERR_WEIGHT_DTYPE: return "weight tensor has an unsupported storage type";
     case QP_ERR_CUDA: return "CUDA runtime error";
-    case QP_ERR_TIMEOUT: return "device barrier timed out";
+    case QP_ERR_TIMEOUT: return "device wait timed out";
     case QP_ERR_BAD_TOKEN: return "token out of range";
     case QP_ERR_OOM: return "device out of memory";
     case QP_ERR_UNKNOWN_WEIGHT: return "unknown weight tensor name";
@@ -144,62 +139,45 @@ qp_status qp_create(const qp_geometry* gp, int max_batch, qp_handle** out) {
     delete h;
     return QP_ERR_CUDA;
   }
-  const size_t R = size_t(2) * max_batch;
-  const int qw = g.n_q_heads * g.head_dim, kvw = g.n_kv_heads * g.head_dim;
-  int aw = g.hidden;
-  if (qw > aw) aw = qw;
-  if (g.ffn > aw) aw = g.ffn;
-  if (g.talker_hidden > aw) aw = g.talker_hidden;
-  h->act_width = aw;
-  const int ctx = g.n_steps + 1;
-  size_t bytes = 0;
-  bytes += carve_size<float>(R * g.hidden);
-  bytes += carve_size<uint16_t>(R * aw);
-  bytes += carve_size<float>(R * (qw + 2 * kvw));
-  bytes += carve_size<float>(R * 2 * g.ffn);
-  bytes += carve_size<float>(size_t(g.layers) * max_batch * ctx * 2 * kvw);
-  bytes += carve_size<float>(size_t(max_batch) * g.vocab);
-  bytes += carve_size<int>(64);
-  bytes += carve_size<float2>(size_t(ctx) * (g.head_dim / 2));
-  bytes += carve_size<float>(size_t(max_batch) * g.talker_hidden);
-  bytes += carve_size<int32_t>(max_batch);
-  bytes += carve_size<int32_t>(size_t(max_batch) * g.n_steps);
-  const size_t Rpad = (R + 127) / 128 * 128;
-  bytes += carve_size<uint16_t>(Rpad * aw);
-  bytes += carve_size<unsigned int>(64);
-  if (cudaMalloc(&h->sarena, bytes) != cudaSuccess) {
+  // the persistent kernel's scratch, plus its per-call synchronisation region
+  h->scr = qp::scratch_layout(g, max_batch);
+  if (cudaMalloc(&h->sarena, h->scr.total) != cudaSuccess) {
     cudaGetLastError();
     delete h;
     return QP_ERR_OOM;
   }
-  h->sarena_bytes = bytes;
-  char* p = static_cast<char*>(h->sarena);
-  h->X = carve<float>(p, R * g.hidden);
-  h->act = carve<uint16_t>(p, R * aw);
-  h->qkv = carve<float>(p, R * (qw + 2 * kvw));
-  h->gu = carve<float>(p, R * 2 * g.ffn);
-  h->kv = carve<float>(p, size_t(g.layers) * max_batch * ctx * 2 * kvw);
-  h->logits = carve<float>(p, size_t(max_batch) * g.vocab);
+  h->sarena_bytes = h->scr.total;
+  // small fixed buffers: status word, RoPE table, host-entry staging
+  const int ctx = g.n_steps + 1;
+  const size_t fbytes = carve_size<int>(64) + carve_size<float2>(size_t(ctx) * 64) +
+                        carve_size<float>(size_t(max_batch) * g.talker_hidden) + carve_size<int32_t>(max_batch) +
+                        carve_size<int32_t>(size_t(max_batch) * g.n_steps);
+  if (cudaMalloc(&h->farena, fbytes) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->sarena);
+    delete h;
+    return QP_ERR_OOM;
+  }
+  char* p = static_cast<char*>(h->farena);
   h->status = carve<int>(p, 64);
-  h->rope_cs = carve<float2>(p, size_t(ctx) * (g.head_dim / 2));
+  h->rope_cs = carve<float2>(p, size_t(ctx) * 64);
   h->H_stage = carve<float>(p, size_t(max_batch) * g.talker_hidden);
   h->q0_stage = carve<int32_t>(p, max_batch);
   h->codes_stage = carve<int32_t>(p, size_t(max_batch) * g.n_steps);
-  h->pact = carve<uint16_t>(p, Rpad * aw);
-  h->sync_words = carve<unsigned int>(p, 64);
 
-  // RoPE table: angle p * theta^(-2i/head_dim) formed in double, rounded once.
-  std::vector<float2> cs(size_t(ctx) * (g.head_dim / 2));
+  // RoPE table: angle pos * theta^(-2i/head_dim) formed in double, rounded once.
+  std::vector<float2> cs(size_t(ctx) * 64);
   for (int pos = 0; pos < ctx; ++pos)
-    for (int i = 0; i < g.head_dim / 2; ++i) {
-      double ang = pos * std::pow(double(g.rope_theta), -2.0 * i / g.head_dim);
-      cs[size_t(pos) * (g.head_dim / 2) + i] = make_float2(float(std::cos(ang)), float(std::sin(ang)));
+    for (int i = 0; i < 64; ++i) {
+      const double ang = pos * std::pow(double(g.rope_theta), -2.0 * i / g.head_dim);
+      cs[size_t(pos) * 64 + i] = make_float2(float(std::cos(ang)), float(std::sin(ang)));
     }
-  if (cudaMemcpy(h->rope_cs, cs.data(), cs.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemset(h->status, 0, 64 * sizeof(int)) != cudaSuccess ||
-      cudaMemset(h->pact, 0, Rpad * aw * sizeof(uint16_t)) != cudaSuccess ||
-      cudaMemset(h->sync_words, 0, 64 * sizeof(unsigned int)) != cudaSuccess) {
+  if (cudaMemset(h->sarena, 0, h->scr.total) != cudaSuccess ||
+      cudaMemcpy(h->rope_cs, cs.data(), cs.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(h->status, 0, 64 * sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
     cudaFree(h->sarena);
+    cudaFree(h->farena);
     delete h;
     return QP_ERR_CUDA;
   }
@@ -229,28 +207,24 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
     if (sl.kind == Slot::EMBED && w[i].dtype != QP_BF16) return QP_ERR_WEIGHT_DTYPE;
     if (sl.kind == Slot::MATRIX) {
       if (w[i].dtype != QP_BF16 && w[i].dtype != QP_Q8_0) return QP_ERR_WEIGHT_DTYPE;
-      int f = w[i].dtype == QP_BF16 ? qp::WF_BF16 : qp::WF_Q8_0;
+      const int f = w[i].dtype == QP_BF16 ? qp::WF_BF16 : qp::WF_Q8_0;
       if (fmt >= 0 && f != fmt) return QP_ERR_WEIGHT_DTYPE;   // one format for all matrices
       fmt = f;
     }
+    if (w[i].dtype == QP_BF16 && !aligned16(w[i].dev_ptr)) return QP_ERR_ARG;
+    if (w[i].dtype == QP_F32 && (reinterpret_cast<uintptr_t>(w[i].dev_ptr) & 3)) return QP_ERR_ARG;
   }
   for (auto& kv : slots)
     if (!seen.count(kv.first)) return QP_ERR_WEIGHT_MISSING;
 
-  // Size the arena.
-  const int64_t d = g.hidden, qw = int64_t(g.n_q_heads) * g.head_dim, kvw = int64_t(g.n_kv_heads) * g.head_dim;
+  const int64_t d = g.hidden, qw = int64_t(g.n_q_heads) * 128, kvw = int64_t(g.n_kv_heads) * 128;
   size_t bytes = matrix_bytes(fmt, d, g.talker_hidden) + carve_size<float>(d) +
                  carve_size<uint16_t>(size_t(g.q0_vocab) * g.talker_hidden) + carve_size<float>(d);
   for (int l = 0; l < g.layers; ++l)
     bytes += matrix_bytes(fmt, qw + 2 * kvw, d) + matrix_bytes(fmt, d, qw) + matrix_bytes(fmt, 2 * g.ffn, d) +
-             matrix_bytes(fmt, d, g.ffn) + 2 * carve_size<float>(d) + 2 * carve_size<float>(g.head_dim);
+             matrix_bytes(fmt, d, g.ffn) + 2 * carve_size<float>(d) + 2 * carve_size<float>(128);
   for (int j = 0; j < g.n_steps; ++j)
-    bytes += carve_size<uint16_t>(size_t(g.vocab) * d) + matrix_bytes(fmt, g.vocab, d);
-  // packed copies for the tensor-core engine
-  auto pk = [&](int64_t N, int64_t K) { return matrix_bytes(fmt, N, K); };
-  bytes += pk(d, g.talker_hidden);
-  for (int l = 0; l < g.layers; ++l) bytes += pk(qw + 2 * kvw, d) + pk(d, qw) + pk(2 * g.ffn, d) + pk(d, g.ffn);
-  for (int j = 0; j < g.n_steps; ++j) bytes += pk(g.vocab, d);
+    bytes += carve_size<uint16_t>(size_t(g.vocab) * d) + carve_size<float>(g.vocab) + matrix_bytes(fmt, g.vocab, d);
 
   if (h->warena) {
     cudaDeviceSynchronize();
@@ -265,32 +239,24 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
   h->warena_bytes = bytes;
   h->wfmt = fmt;
   char* p = static_cast<char*>(h->warena);
-
+  cudaError_t err = cudaSuccess;
+  auto chk = [&](cudaError_t e) { if (e != cudaSuccess && err == cudaSuccess) err = e; };
+  auto get = [&](const std::string& name) -> const qp_weight& { return w[seen[name]]; };
   auto alloc_mat = [&](int64_t N, int64_t K) {
-    QMat m;
-    m.N = int(N); m.K = int(K); m.fmt = fmt;
+    qp::PackedMat m;
+    m.N = int(N); m.K = int(K);
     if (fmt == qp::WF_BF16) {
-      m.w = carve<uint16_t>(p, size_t(N) * K);
+      m.w = carve<uint8_t>(p, size_t(N) * K * 2);
     } else {
-      m.w = carve<int8_t>(p, size_t(N) * K);
+      m.w = carve<uint8_t>(p, size_t(N) * K);
       m.scale = carve<__half>(p, size_t(N) * (K / 32));
     }
     return m;
   };
-  // Copy rows [row0, row0 + rows) of matrix m from a caller tensor.
-  auto put_rows = [&](const QMat& m, int64_t row0, const qp_weight& src) -> cudaError_t {
-    const int64_t rows = src.shape[0], K = src.shape[1];
-    if (fmt == qp::WF_BF16) {
-      return cudaMemcpyAsync(static_cast<uint16_t*>(const_cast<void*>(m.w)) + row0 * K, src.dev_ptr,
-                             size_t(rows) * K * 2, cudaMemcpyDeviceToDevice, s);
-    }
-    return qp::repack_q8_0(static_cast<const uint8_t*>(src.dev_ptr), int(rows), int(K),
-                           static_cast<int8_t*>(const_cast<void*>(m.w)) + row0 * K,
-                           const_cast<__half*>(m.scale) + row0 * (K / 32), s);
+  auto put = [&](const qp::PackedMat& m, int row0, const std::string& name) {
+    const qp_weight& src = get(name);
+    chk(qp::pack_rows(src.dev_ptr, fmt, int(src.shape[0]), int(src.shape[1]), m, row0, s));
   };
-  auto get = [&](const std::string& name) -> const qp_weight& { return w[seen[name]]; };
-  cudaError_t err = cudaSuccess;
-  auto chk = [&](cudaError_t e) { if (e != cudaSuccess && err == cudaSuccess) err = e; };
   auto put_vec = [&](const std::string& name, int64_t count) {
     float* dst = carve<float>(p, count);
     chk(cudaMemcpyAsync(dst, get(name).dev_ptr, size_t(count) * 4, cudaMemcpyDeviceToDevice, s));
@@ -298,7 +264,7 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
   };
 
   h->proj = alloc_mat(d, g.talker_hidden);
-  chk(put_rows(h->proj, 0, get("code_pred.small_to_mtp_projection.weight")));
+  put(h->proj, 0, "code_pred.small_to_mtp_projection.weight");
   h->b_proj = put_vec("code_pred.small_to_mtp_projection.bias", d);
   {
     uint16_t* e0 = carve<uint16_t>(p, size_t(g.q0_vocab) * g.talker_hidden);
@@ -308,51 +274,35 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
   }
   h->out_norm = put_vec("code_pred.output_norm.weight", d);
   for (int l = 0; l < g.layers; ++l) {
-    std::string pre = "code_pred.blk." + std::to_string(l) + ".";
+    const std::string pre = "code_pred.blk." + std::to_string(l) + ".";
     qp::LayerW& L = h->layer[l];
     L.qkv = alloc_mat(qw + 2 * kvw, d);
-    chk(put_rows(L.qkv, 0, get(pre + "attn_q.weight")));
-    chk(put_rows(L.qkv, qw, get(pre + "attn_k.weight")));
-    chk(put_rows(L.qkv, qw + kvw, get(pre + "attn_v.weight")));
+    put(L.qkv, 0, pre + "attn_q.weight");
+    put(L.qkv, int(qw), pre + "attn_k.weight");
+    put(L.qkv, int(qw + kvw), pre + "attn_v.weight");
     L.o = alloc_mat(d, qw);
-    chk(put_rows(L.o, 0, get(pre + "attn_output.weight")));
+    put(L.o, 0, pre + "attn_output.weight");
     L.gu = alloc_mat(2 * g.ffn, d);
-    chk(put_rows(L.gu, 0, get(pre + "ffn_gate.weight")));
-    chk(put_rows(L.gu, g.ffn, get(pre + "ffn_up.weight")));
+    put(L.gu, 0, pre + "ffn_gate.weight");
+    put(L.gu, g.ffn, pre + "ffn_up.weight");
     L.down = alloc_mat(d, g.ffn);
-    chk(put_rows(L.down, 0, get(pre + "ffn_down.weight")));
+    put(L.down, 0, pre + "ffn_down.weight");
     L.attn_norm = put_vec(pre + "attn_norm.weight", d);
     L.ffn_norm = put_vec(pre + "ffn_norm.weight", d);
-    L.q_norm = put_vec(pre + "attn_q_norm.weight", g.head_dim);
-    L.k_norm = put_vec(pre + "attn_k_norm.weight", g.head_dim);
+    L.q_norm = put_vec(pre + "attn_q_norm.weight", 128);
+    L.k_norm = put_vec(pre + "attn_k_norm.weight", 128);
   }
   for (int j = 0; j < g.n_steps; ++j) {
     uint16_t* e = carve<uint16_t>(p, size_t(g.vocab) * d);
     chk(cudaMemcpyAsync(e, get("code_pred.codec_embd." + std::to_string(j) + ".weight").dev_ptr,
                         size_t(g.vocab) * d * 2, cudaMemcpyDeviceToDevice, s));
     h->embed[j] = e;
+    float* ss = carve<float>(p, g.vocab);
+    chk(qp::row_sumsq_bf16(e, g.vocab, int(d), ss, s));
+    h->embed_ss[j] = ss;
     h->head[j] = alloc_mat(g.vocab, d);
-    chk(put_rows(h->head[j], 0, get("code_pred.lm_head." + std::to_string(j) + ".weight")));
+    put(h->head[j], 0, "code_pred.lm_head." + std::to_string(j) + ".weight");
   }
-  auto pack = [&](const QMat& m) {
-    qp::PackedMat pm;
-    if (fmt == qp::WF_BF16) {
-      pm.w = carve<uint8_t>(p, size_t(m.N) * m.K * 2);
-    } else {
-      pm.w = carve<uint8_t>(p, size_t(m.N) * m.K);
-      pm.scale = carve<__half>(p, size_t(m.N) * (m.K / 32));
-    }
-    chk(qp::pack_matrix(m, pm, s));
-    return pm;
-  };
-  h->pproj = pack(h->proj);
-  for (int l = 0; l < g.layers; ++l) {
-    h->player[l].qkv = pack(h->layer[l].qkv);
-    h->player[l].o = pack(h->layer[l].o);
-    h->player[l].gu = pack(h->layer[l].gu);
-    h->player[l].down = pack(h->layer[l].down);
-  }
-  for (int j = 0; j < g.n_steps; ++j) h->phead[j] = pack(h->head[j]);
   if (err != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;
@@ -362,36 +312,31 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
 }
 
 static qp_status check_run(qp_handle* h, int B, const float* H, const int32_t* q0, int32_t* out_codes,
-                           const qp_sampling* samp) {
+                           const qp_sampling* samp, bool device_ptrs) {
   if (!h) return QP_ERR_ARG;
   if (!h->loaded) return QP_ERR_STATE;
   if (B < 1 || B > h->max_batch || !H || !q0 || !out_codes) return QP_ERR_ARG;
+  if (device_ptrs && !aligned16(H)) return QP_ERR_ARG;
   if (samp) {
     if (!(samp->temperature > 0.f) || !std::isfinite(samp->temperature)) return QP_ERR_ARG;
     if (samp->top_k < 1 || samp->top_k > h->g.vocab || !samp->gumbel) return QP_ERR_ARG;
+    if (h->g.vocab > qp::kMaxVocab) return QP_ERR_ARG;
   }
   return QP_OK;
-}
-
-// The persistent tensor-core engine runs every call; QP_ENGINE=layers selects
-// the per-operation kernels (kept while the persistent engine is brought up).
-static qp_status dispatch(qp_handle* h, const qp::RunArgs& a, cudaStream_t s) {
-  static const char* eng = std::getenv("QP_ENGINE");
-  if (eng && std::strcmp(eng, "layers") == 0) return qp::run_frames(h, a, s);
-  return qp::run_frames_persistent(h, a, s);
 }
 
 qp_status qp_predict_frames_ex(qp_handle* h, int B, const float* H, const int32_t* q0, int32_t* out_codes,
                                float* out_logits, const qp_sampling* samp, const int32_t* forced_codes,
                                qp_stream s) {
-  qp_status st = check_run(h, B, H, q0, out_codes, samp);
+  qp_status st = check_run(h, B, H, q0, out_codes, samp, true);
   if (st != QP_OK) return st;
+  if (out_logits && !aligned16(out_logits)) return QP_ERR_ARG;
   DeviceGuard dg(h->device);
   if (!dg.ok) return QP_ERR_CUDA;
   qp::RunArgs a;
   a.B = B; a.H = H; a.q0 = q0; a.out_codes = out_codes; a.out_logits = out_logits; a.forced = forced_codes;
   if (samp) { a.temperature = samp->temperature; a.top_k = samp->top_k; a.gumbel = samp->gumbel; }
-  return dispatch(h, a, static_cast<cudaStream_t>(s));
+  return qp::run_frames_persistent(h, a, static_cast<cudaStream_t>(s));
 }
 
 qp_status qp_predict_frames(qp_handle* h, int B, const float* H, const int32_t* q0, int32_t* out_codes,
@@ -401,7 +346,7 @@ qp_status qp_predict_frames(qp_handle* h, int B, const float* H, const int32_t* 
 
 qp_status qp_predict_frames_host(qp_handle* h, int B, const float* H_host, const int32_t* q0_host,
                                  int32_t* codes_host, const qp_sampling* samp, qp_stream sv) {
-  qp_status st = check_run(h, B, H_host, q0_host, codes_host, samp);
+  qp_status st = check_run(h, B, H_host, q0_host, codes_host, samp, false);
   if (st != QP_OK) return st;
   DeviceGuard dg(h->device);
   if (!dg.ok) return QP_ERR_CUDA;
@@ -415,7 +360,7 @@ qp_status qp_predict_frames_host(qp_handle* h, int B, const float* H_host, const
   qp::RunArgs a;
   a.B = B; a.H = h->H_stage; a.q0 = h->q0_stage; a.out_codes = h->codes_stage;
   if (samp) { a.temperature = samp->temperature; a.top_k = samp->top_k; a.gumbel = samp->gumbel; }
-  st = dispatch(h, a, s);
+  st = qp::run_frames_persistent(h, a, s);
   if (st != QP_OK) return st;
   if (cudaMemcpyAsync(codes_host, h->codes_stage, size_t(B) * g.n_steps * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
@@ -427,8 +372,9 @@ qp_status qp_predict_frames_host(qp_handle* h, int B, const float* H_host, const
 
 qp_status qp_predict_frames_static(qp_handle* h, int B, const float* H, const int32_t* q0, int32_t* out_codes,
                                    float* out_logits, qp_stream s) {
-  qp_status st = check_run(h, B, H, q0, out_codes, nullptr);
+  qp_status st = check_run(h, B, H, q0, out_codes, nullptr, true);
   if (st != QP_OK) return st;
+  if (out_logits && !aligned16(out_logits)) return QP_ERR_ARG;
   DeviceGuard dg(h->device);
   if (!dg.ok) return QP_ERR_CUDA;
   qp::RunArgs a;
@@ -450,11 +396,49 @@ qp_status qp_get_device_status(qp_handle* h, qp_stream sv) {
   return static_cast<qp_status>(v);
 }
 
-int qp_launches_per_call(qp_handle* h, int B, int sampling) {
+int qp_launches_per_call(qp_handle* h, int B, int /*sampling*/) {
   if (!h || B < 1 || B > h->max_batch) return -1;
-  static const char* eng = std::getenv("QP_ENGINE");
-  if (eng && std::strcmp(eng, "layers") == 0) return qp::launches_per_call(h, B, sampling != 0);
   return 1;   // one persistent kernel per call
+}
+
+qp_status qp_trace_enable(qp_handle* h, int enable) {
+  if (!h) return QP_ERR_ARG;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return QP_ERR_CUDA;
+  cudaDeviceSynchronize();
+  if (h->trace) {
+    cudaFree(h->trace);
+    h->trace = nullptr;
+    h->trace_phases = 0;
+  }
+  if (!enable) return QP_OK;
+  const int phases = 8192;
+  // section stamps [phases][cta][2], then a 16384-word event log per CTA
+  const size_t bytes = (size_t(phases) * h->num_sms * 2 + size_t(h->num_sms) * 16384) * sizeof(unsigned long long);
+  if (cudaMalloc(&h->trace, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    h->trace = nullptr;
+    return QP_ERR_OOM;
+  }
+  cudaMemset(h->trace, 0, bytes);
+  h->trace_phases = phases;
+  return QP_OK;
+}
+
+int qp_trace_read(qp_handle* h, uint64_t* host, int phases, int* n_cta) {
+  if (!h || !host || phases < 0 || !h->trace) return -1;
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return -1;
+  if (phases > h->trace_phases) phases = h->trace_phases;
+  if (n_cta) *n_cta = h->num_sms;
+  size_t words = size_t(phases) * h->num_sms * 2;
+  if (phases == h->trace_phases) words += size_t(h->num_sms) * 16384;   // and the event logs
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(host, h->trace, words * sizeof(uint64_t), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  return phases;
 }
 
 void qp_destroy(qp_handle* h) {
@@ -462,8 +446,10 @@ void qp_destroy(qp_handle* h) {
   {
     DeviceGuard dg(h->device);
     cudaDeviceSynchronize();
+    if (h->trace) cudaFree(h->trace);
     if (h->warena) cudaFree(h->warena);
     if (h->sarena) cudaFree(h->sarena);
+    if (h->farena) cudaFree(h->farena);
   }
   delete h;
 }

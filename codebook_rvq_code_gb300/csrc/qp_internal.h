@@ -14,36 +14,28 @@ constexpr int kMaxLayers = 16;
 constexpr int kMaxSteps = 15;
 constexpr int kMaxCtx = kMaxSteps + 1;   // positions 0..n_steps
 constexpr int kHeadDim = 128;
+constexpr int kTileM = 128;              // weight rows per MMA tile
+constexpr int kKs = 128;                 // K per slice
+constexpr int kMaxNc = 128;              // frames (rows) per MMA N chunk
+constexpr int kMaxVocab = 4096;
 
 enum WFmt { WF_BF16 = 0, WF_Q8_0 = 1 };
 
-// A weight matrix [N, K] (HF [out, in]) in the library's own layout.
-//   WF_BF16: w = bf16 bits, row-major [N, K]
-//   WF_Q8_0: w = int8 values row-major [N, K]; scale = f16 [N, K/32]
-struct QMat {
-  const void* w = nullptr;
-  const __half* scale = nullptr;
-  int N = 0, K = 0;
-  int fmt = WF_BF16;
-};
-
 // A weight matrix packed for the tensor cores: 128-row tiles, each the
-// K-major core-matrix image [K/8][16][8 rows][8 k] of f16 (WF_BF16 input)
-// or int8 (WF_Q8_0 input, with f16 scales [tile][K/128][4][128]).
+// K-major core-matrix image [K/8][16][8 rows][8 k] of f16 (bf16 input,
+// converted) or of int8 (Q8_0 input, with f16 scales [tile][K/128][4][128]).
+// One 128-row x 128-K slice is contiguous: 32 KB (f16) or 16 KB + 1 KB.
 struct PackedMat {
   uint8_t* w = nullptr;
   __half* scale = nullptr;
-};
-
-struct PackedLayer {
-  PackedMat qkv, o, gu, down;
+  int N = 0, K = 0;
 };
 
 struct LayerW {
-  QMat qkv;   // [q_width + 2*kv_width, hidden]: q rows, then k rows, then v rows
-  QMat o;     // [hidden, q_width]
-  QMat gu;    // [2*ffn, hidden]: gate rows, then up rows
-  QMat down;  // [hidden, ffn]
+  PackedMat qkv;   // [q_width + 2*kv_width, hidden]: q rows, then k rows, then v rows
+  PackedMat o;     // [hidden, q_width]
+  PackedMat gu;    // [2*ffn, hidden]: gate rows, then up rows
+  PackedMat down;  // [hidden, ffn]
   const float* attn_norm = nullptr;
   const float* q_norm = nullptr;
   const float* k_norm = nullptr;
@@ -63,6 +55,27 @@ struct RunArgs {
   const float* gumbel = nullptr;
 };
 
+// Rows of the MMA operand buffer for R activation rows (chunks of <= 128).
+inline size_t operand_rows(size_t R) {
+  const size_t r16 = (R + 15) / 16 * 16;
+  return r16 <= size_t(kMaxNc) ? r16 : (R + kMaxNc - 1) / kMaxNc * kMaxNc;
+}
+
+// Byte offsets of the kernel's scratch for batches of up to `bmax` frames.
+struct Scratch {
+  size_t x1, xk;                         // residual streams: step 1 [2B, d], later steps [B, d]
+  size_t a1[5], ak[4], ahead;            // f16 operands: step 1 proj/qkv/o/gu/down, later qkv/o/gu/down, head
+  size_t acc1_qkv, acck_qkv, acc1_gu, acck_gu, logits;
+  size_t kv;                             // [layer][frame][pos][k|v][kv_width] f32
+  size_t sync;                           // start of the zeroed-per-call region
+  size_t total;                          // sync + the largest sync region (B = bmax)
+};
+Scratch scratch_layout(const qp_geometry& g, int bmax);
+// Bytes of the synchronisation region a call with B frames uses (zeroed at
+// the start of every call): counters, sums of squares, argmax words,
+// decisions, abort flag.
+size_t sync_bytes(const qp_geometry& g, int B);
+
 }  // namespace qp
 
 struct qp_handle {
@@ -76,49 +89,40 @@ struct qp_handle {
   // weights (library-owned arena)
   void* warena = nullptr;
   size_t warena_bytes = 0;
-  qp::QMat proj;
+  qp::PackedMat proj;
   const float* b_proj = nullptr;
-  const uint16_t* e0 = nullptr;            // [q0_vocab, talker_hidden] bf16
+  const uint16_t* e0 = nullptr;                 // [q0_vocab, talker_hidden] bf16
   qp::LayerW layer[qp::kMaxLayers];
   const float* out_norm = nullptr;
-  const uint16_t* embed[qp::kMaxSteps] = {};  // [vocab, hidden] bf16
-  qp::QMat head[qp::kMaxSteps];            // [vocab, hidden]
-  // the same matrices packed for the persistent tensor-core engine
-  qp::PackedMat pproj;
-  qp::PackedLayer player[qp::kMaxLayers];
-  qp::PackedMat phead[qp::kMaxSteps];
+  const uint16_t* embed[qp::kMaxSteps] = {};    // [vocab, hidden] bf16
+  const float* embed_ss[qp::kMaxSteps] = {};    // [vocab]: sum of squares of each row
+  qp::PackedMat head[qp::kMaxSteps];            // [vocab, hidden]
 
-  // scratch (sized for max_batch)
+  // scratch: persistent buffers then the per-call sync region
   void* sarena = nullptr;
   size_t sarena_bytes = 0;
-  float* X = nullptr;          // [2*max_batch, hidden] residual stream
-  uint16_t* act = nullptr;     // [2*max_batch, act_width] f16 GEMM operand
-  int act_width = 0;
-  float* qkv = nullptr;        // [2*max_batch, q_width + 2*kv_width]
-  float* gu = nullptr;         // [2*max_batch, 2*ffn]
-  float* kv = nullptr;         // [layers][max_batch][ctx][2][n_kv][128]
-  float* logits = nullptr;     // [max_batch, vocab]
-  int* status = nullptr;       // device status word
-  uint16_t* pact = nullptr;    // f16 MMA operand, [chunk][K/8][Nc/8][8][8]
-  unsigned int* sync_words = nullptr;  // grid-barrier counter, abort flag
-  float2* rope_cs = nullptr;   // [ctx][64] (cos, sin)
-  // staging for the host-buffer entry point
-  float* H_stage = nullptr;
+  qp::Scratch scr;
+  // small fixed buffers
+  void* farena = nullptr;
+  int* status = nullptr;                        // device status word
+  float2* rope_cs = nullptr;                    // [ctx][64] (cos, sin)
+  float* H_stage = nullptr;                     // host-buffer entry point staging
   int32_t* q0_stage = nullptr;
   int32_t* codes_stage = nullptr;
+  unsigned long long* trace = nullptr;          // optional phase trace (qp_debug.h)
+  int trace_phases = 0;
 };
 
 namespace qp {
-// engine entry (qp_engine.cu): enqueue the whole frame loop on s
-qp_status run_frames(qp_handle* h, const RunArgs& a, cudaStream_t s);
 // persistent engine (qp_persistent.cu)
 qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s);
-size_t packed_bytes(int fmt, int N, int K);
-cudaError_t pack_matrix(const QMat& src, PackedMat& dst, cudaStream_t s);
-size_t persistent_smem_bytes();
-// the same kernel with its scratch in a static device array (qp_persistent.cu)
 qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s);
-int launches_per_call(const qp_handle* h, int B, bool sampling);
-// weight repack helpers (qp_engine.cu)
-cudaError_t repack_q8_0(const uint8_t* blocks, int N, int K, int8_t* qs, __half* d, cudaStream_t s);
+size_t persistent_smem_bytes();
+// load-time weight preparation (qp_weights.cu)
+size_t packed_bytes(int fmt, int N, int K);
+// Pack `rows` rows of a caller matrix [rows, K] (bf16, or a Q8_0 block
+// stream) into rows [row0, row0 + rows) of the packed matrix dst.
+cudaError_t pack_rows(const void* src, int fmt, int rows, int K, const PackedMat& dst, int row0, cudaStream_t s);
+// out[r] = sum_i E[r, i]^2 (f32) for a [rows, cols] bf16 table.
+cudaError_t row_sumsq_bf16(const uint16_t* E, int rows, int cols, float* out, cudaStream_t s);
 }  // namespace qp

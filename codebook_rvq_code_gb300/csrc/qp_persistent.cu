@@ -1,26 +1,41 @@
-// The Code Predictor frame loop as ONE persistent cooperative kernel.
+// The Code Predictor frame loop as ONE persistent cooperative kernel,
+// scheduled as a dataflow over tiles.
 //
-// The whole 15-step loop of a batch of frames ("テキスト音声合成モデルを50ミリ秒未満で
-// 応答させる方法", "Qwen3-TTSの最適化方法" item 3: a fixed GPU program in place
-// of a host-driven sequence, with a preallocated KV cache) runs as a list of
-// phases separated by grid barriers.  Every weight contraction is a GEMM
-// phase on the tcgen05 tensor cores:
+// For a batch of B frames the call runs the whole 15-step loop
+// ("テキスト音声合成モデルを50ミリ秒未満で応答させる方法", "Qwen3-TTSの最適化方法"
+// item 3: a fixed GPU program instead of a host-driven sequence, over a
+// preallocated KV cache):
+//   step 1: rows 2b = small_to_mtp(H_b), 2b+1 = small_to_mtp(E0[q0_b]);
+//   step k >= 2: row b = E[k-2][q_{k-1}];
+//   5 layers per step: RMSNorm -> QKV -> per-head QK-norm + RoPE -> causal
+//   GQA attention -> O + residual -> RMSNorm -> gate/up -> SwiGLU -> down +
+//   residual; then output RMSNorm, lm_head[k-1] and the decision.
 //
-//   D[128 weight rows, Nc rows of frames] += W[128, K-slice] * act[Nc, K-slice]^T
+// Every weight contraction runs on the tcgen05 tensor cores as
+//   D[128 weight rows, Nc activation rows] += W[128, 128-K slice] * act^T
+// with f16 operands and f32 accumulators in TMEM.  Weights arrive packed in
+// the MMA's shared-memory image (qp_weights.cu), one bulk copy per slice.
 //
-// with f16 operands and an f32 accumulator in TMEM.  Weights are packed at
-// load time into exactly the shared-memory image the MMA descriptors read
-// (K-major 8x16-byte core matrices, no swizzle), so one K-slice of one
-// 128-row tile is one contiguous cp.async.bulk.  A producer warp streams the
-// CTA's weight slices for all phases, in order, through a ring of shared
-// memory slots; it never waits on the grid, so weight traffic runs ahead
-// across phase boundaries.  GEMM slices are dealt out to CTAs in equal
-// contiguous runs (stream-K style); each run's partial tile is added into an
-// f32 accumulator in global memory with red.add.  Elementwise phases (RMSNorm,
-// QK-norm + RoPE + attention, SwiGLU, the decision) run on the same CTAs.
-#include <cooperative_groups.h>
-#include <cstdio>
-
+// Roles inside each CTA (one CTA per SM, all co-resident):
+//   producer warp  streams the CTA's weight slices for the whole call through
+//                  a ring of shared-memory slots;
+//   dequant warps  (Q8_0 only) turn int8 slices into f16 operand slots;
+//   MMA warp       waits until a slice's activation operand is published,
+//                  bulk-copies it, issues the MMAs into one of two TMEM
+//                  accumulators and commits;
+//   consumer warps drain accumulators into f32 buffers (red.add, so slices
+//                  of one tile may come from several CTAs), and run the
+//                  elementwise work.
+// There are no grid-wide barriers.  Each output tile carries a counter; the
+// CTA whose contribution completes a tile (the "last arriver") finishes it:
+// an x tile becomes the next GEMM's operand f16(x * w_norm) plus partial
+// sums of squares (the next GEMM scales its output by 1/rms), a gate/up tile
+// pair becomes the down operand silu(g)*u, a logits tile feeds the greedy
+// argmax.  Attention runs one warp per (frame, kv head) as soon as that
+// head's q/k/v tiles are complete.  Consumers wait only on work earlier in
+// the one program order every CTA follows, so the earliest pending item can
+// always run: no deadlock.  Every wait is bounded; one that runs out latches
+// QP_ERR_TIMEOUT and sets an abort flag that every other wait honours.
 #include "qp_common.cuh"
 #include "qp_internal.h"
 #include "qp_ptx.cuh"
@@ -29,25 +44,57 @@ namespace qp {
 
 namespace {
 
-constexpr int kConsumers = 256;             // 8 consumer warps
-constexpr int kThreads = kConsumers + 32;   // + 1 producer warp
-constexpr int kNSlot = 4;                   // weight ring slots
-constexpr int kKs = 128;                    // K per slice
-constexpr int kTileM = 128;                 // weight rows per MMA tile
-constexpr int kMaxNc = 128;                 // frames per MMA (N)
-constexpr uint32_t kSlotBytes = kTileM * kKs * 2;          // 32 KB f16
-constexpr uint32_t kQ8Bytes = kTileM * kKs;                // 16 KB int8
-constexpr uint32_t kQ8ScaleBytes = (kKs / 32) * kTileM * 2;  // 1 KB f16
-constexpr uint32_t kActBytes = kKs * kMaxNc * 2;           // 32 KB
-constexpr uint32_t kTmemCols = 128;
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kProducerWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kDeqWarp0 = 10;
+constexpr int kDeqThreads = 4 * 32;
+constexpr int kThreads = (kConsumerWarps + 2 + 4) * 32;   // 448
 
-enum { BAR_ALL = 1, BAR_H0 = 2, BAR_H1 = 3 };
+constexpr uint32_t kSlotBytes = kTileM * kKs * 2;              // 32 KB f16 slice
+constexpr uint32_t kQ8Bytes = kTileM * kKs;                    // 16 KB int8 slice
+constexpr uint32_t kQ8ScaleBytes = (kKs / 32) * kTileM * 2;    // 1 KB of scales
+constexpr uint32_t kQ8SlotBytes = kQ8Bytes + kQ8ScaleBytes;
+constexpr int kNSlotF16 = 4, kNSlotQ8 = 3, kNDeq = 2, kNAct = 2;
+constexpr uint32_t kActBytes = kKs * kMaxNc * 2;               // 32 KB operand slice
+constexpr uint32_t kTmemCols = 256;                            // two 128-column accumulators
+
+// shared memory map (offsets from a 1 KB aligned base)
+constexpr uint32_t kOffRing = 0;                               // f16 slots, or Q8_0 raw slots
+constexpr uint32_t kOffDeq = 53248;                            // Q8_0: dequantised slots
+constexpr uint32_t kOffAct = 131072;                           // activation operand slots
+constexpr uint32_t kOffKeys = kOffAct + kNAct * kActBytes;     // top-k keys
+constexpr uint32_t kOffMisc = kOffKeys + kMaxVocab * 4;
+static_assert(kNSlotQ8 * kQ8SlotBytes <= kOffDeq, "raw Q8_0 slots overlap the dequantised ones");
+static_assert(kOffDeq + kNDeq * kSlotBytes <= kOffAct, "dequantised slots overlap the operand slots");
+static_assert(kNSlotF16 * kSlotBytes <= kOffAct, "f16 slots overlap the operand slots");
+
+enum { BAR_CONS = 1, BAR_DEQ = 2 };
+enum { G_PROJ = 0, G_QKV, G_O, G_GU, G_DOWN, G_HEAD };
+
+struct Misc {
+  uint64_t wfull[kNSlotF16], wempty[kNSlotF16];
+  uint64_t dfull[kNDeq], dempty[kNDeq];
+  uint64_t afull[kNAct], aempty[kNAct];
+  uint64_t accfull[2], accempty[2];
+  uint64_t mmadone;
+  uint32_t tmem_base;
+  int flag[4];
+  int fail;       // a consumer wait gave up: every consumer warp leaves at the next section end
+  unsigned evc;   // next slot of this CTA's consumer event log (tracing only)
+  int deq_ok;     // broadcast of the dequant leader's waits
+  float red[8];
+  unsigned long long redu[8];
+  int sel[2];
+  int hist[256];
+  int chunk_cnt[kConsumers];
+  float inv[kMaxNc];
+};
 
 struct PLayer {
-  const uint8_t* w_qkv; const __half* s_qkv;
-  const uint8_t* w_o; const __half* s_o;
-  const uint8_t* w_gu; const __half* s_gu;
-  const uint8_t* w_d; const __half* s_d;
+  const uint8_t* w[4];     // qkv, o, gu, down (packed)
+  const __half* s[4];
   const float* attn_norm; const float* q_norm; const float* k_norm; const float* ffn_norm;
 };
 
@@ -55,458 +102,251 @@ struct PParams {
   int d, qw, kvw, F, V, th, L, n_q, n_kv, n_steps, q0_vocab;
   float eps;
   int q8;
-  const uint8_t* w_proj; const __half* s_proj; const float* b_proj;
-  const uint16_t* e0;
+  const uint8_t* w_proj; const __half* s_proj; const float* b_proj; const uint16_t* e0;
   PLayer layer[kMaxLayers];
   const float* out_norm;
-  const uint16_t* embed[kMaxSteps];
+  const uint16_t* embed[kMaxSteps]; const float* embed_ss[kMaxSteps];
   const uint8_t* w_head[kMaxSteps]; const __half* s_head[kMaxSteps];
   const float2* rope_cs;
-  float* xres; uint16_t* act; float* acc_qkv; float* acc_gu; float* logits; float* kv;
-  unsigned int* bar; int* abort_flag; int* status;
+  // scratch
+  float* x1; float* xk; uint16_t* a1[5]; uint16_t* ak[4]; uint16_t* ahead;
+  float* acc1_qkv; float* acck_qkv; float* acc1_gu; float* acck_gu; float* logits; float* kv;
   int Bmax;
+  // per-call synchronisation (zeroed before the launch)
+  unsigned* tile_cnt; unsigned* ready; unsigned* ss_cnt; float* ss; unsigned* pair; unsigned* head_done;
+  unsigned long long* codepk; unsigned* decided; int* abort_flag; int* status;
+  int NCH, MT, KS, NGEMM;
+  unsigned long long* trace; int trace_n;
+  // the call
   int B; const float* H; const int32_t* q0; int32_t* out_codes; float* out_logits; const int32_t* forced;
   float temperature; int top_k; const float* gumbel;
 };
 
-struct Smem {
-  alignas(1024) uint8_t slot[kNSlot][kSlotBytes];
-  alignas(1024) uint8_t actb[kActBytes];
-  union {   // the Q8_0 operand in GEMM phases, the top-k keys in the decision
-    alignas(1024) uint8_t deq[kSlotBytes];
-    uint32_t keys[8192];
-  };
-  alignas(8) uint64_t full[kNSlot];
-  alignas(8) uint64_t empty[kNSlot];
-  alignas(8) uint64_t actbar;
-  alignas(8) uint64_t mmabar;
-  uint32_t tmem_base;
-  float red[2][8];
-  float xs[2][128];
-  float sc[2][kMaxCtx];
-  unsigned long long redu[8];
-  int sh_int[8];
-  int hist[256];
-  int chunk_cnt[kConsumers];
+// ------------------------------------------------------------ event log
+// With tracing on, each CTA also keeps an event log after the section stamps:
+// consumer events in [0, 8192), MMA-warp events in [8192, 16384) of its
+// region; one word = (globaltimer ns mod 2^48) << 16 | code << 12 | gemm.
+enum {
+  EV_READY = 1, EV_LANDED, EV_COMMIT,            // MMA warp, per slice / segment
+  EV_ACC = 4, EV_REDS, EV_COUNTED, EV_LASTDONE,   // consumer epilogue, per segment
+  EV_ATT_READY = 8, EV_ATT_DONE                   // attention warp, per item
 };
-
-// N-chunking of R rows for the MMA: chunks of Nc (multiple of 16, <= 128).
-struct Chunking { int Nc, n_chunks; };
-__device__ __forceinline__ Chunking chunking(int R) {
-  const int r16 = (R + 15) & ~15;
-  if (r16 <= kMaxNc) return {r16, 1};
-  return {kMaxNc, (R + kMaxNc - 1) / kMaxNc};
+__device__ __forceinline__ unsigned long long* ev_base(const PParams& p) {
+  return p.trace ? p.trace + size_t(p.trace_n) * gridDim.x * 2 + size_t(blockIdx.x) * 16384 : nullptr;
 }
-
-// Element offset of (row n, feature k) in the activation operand layout
-// [chunk][K/8][Nc/8][8 rows][8 k] for reduction length Kdim.
-__device__ __forceinline__ size_t act_off(int n, int k, int Kdim, Chunking c) {
-  const int ch = n / c.Nc, nn = n - ch * c.Nc;
-  return size_t(ch) * Kdim * c.Nc + (size_t((k >> 3) * (c.Nc >> 3) + (nn >> 3)) << 6) + ((nn & 7) << 3) + (k & 7);
+__device__ __forceinline__ unsigned long long ev_word(int code, int gi) {
+  return ((globaltimer_ns() & 0xFFFFFFFFFFFFull) << 16) | (unsigned long long)(code & 15) << 12 | unsigned(gi & 4095);
 }
-
-struct Gemm {
-  const uint8_t* w; const __half* s;
-  int n_mt, n_ks;       // 128-row tiles, 128-wide K slices
-  int Kdim;
-  float* acc; int ld;   // acc[row][feature]
-  int R;
-};
-
-// The CTA's contiguous run [beg, end) of the phase's slices.
-__device__ __forceinline__ void my_slices(int total, int gemm_idx, int& beg, int& end) {
-  const int G = gridDim.x;
-  const int g = (blockIdx.x + gemm_idx * 37) % G;
-  beg = int((long long)total * g / G);
-  end = int((long long)total * (g + 1) / G);
+__device__ __forceinline__ void ev_mma(const PParams& p, unsigned& idx, int code, int gi) {
+  unsigned long long* b = ev_base(p);
+  if (b && idx < 8192) b[8192 + idx++] = ev_word(code, gi);
 }
-
-// ---------------------------------------------------------------------------
-// The phase program.  Producer and consumers walk the same sequence of GEMM
-// phases; this builds the i-th one (call order) for both.
-// ---------------------------------------------------------------------------
-struct Prog {
-  const PParams& p;
-  __device__ Prog(const PParams& pp) : p(pp) {}
-  __device__ int num_gemms() const { return 1 + p.n_steps * (p.L * 4 + 1); }
-  __device__ Gemm gemm(int i) const {
-    Gemm g;
-    const int B = p.B;
-    if (i == 0) {   // small_to_mtp projection of step 1 (2 rows per frame)
-      g.w = p.w_proj; g.s = p.s_proj; g.n_mt = p.d / kTileM; g.Kdim = p.th; g.acc = p.xres; g.ld = p.d; g.R = 2 * B;
-    } else {
-      const int j = i - 1, per_step = p.L * 4 + 1, step = j / per_step + 1, r = j % per_step;
-      const int R = step == 1 ? 2 * B : B;
-      if (r == p.L * 4) {   // lm_head[step-1]
-        g.w = p.w_head[step - 1]; g.s = p.s_head[step - 1]; g.n_mt = p.V / kTileM; g.Kdim = p.d;
-        g.acc = p.logits; g.ld = p.V; g.R = B;
-      } else {
-        const PLayer& L = p.layer[r / 4];
-        switch (r % 4) {
-          case 0: g.w = L.w_qkv; g.s = L.s_qkv; g.n_mt = (p.qw + 2 * p.kvw) / kTileM; g.Kdim = p.d;
-                  g.acc = p.acc_qkv; g.ld = p.qw + 2 * p.kvw; break;
-          case 1: g.w = L.w_o; g.s = L.s_o; g.n_mt = p.d / kTileM; g.Kdim = p.qw; g.acc = p.xres; g.ld = p.d; break;
-          case 2: g.w = L.w_gu; g.s = L.s_gu; g.n_mt = 2 * p.F / kTileM; g.Kdim = p.d; g.acc = p.acc_gu;
-                  g.ld = 2 * p.F; break;
-          default: g.w = L.w_d; g.s = L.s_d; g.n_mt = p.d / kTileM; g.Kdim = p.F; g.acc = p.xres; g.ld = p.d; break;
-        }
-        g.R = R;
-      }
-    }
-    g.n_ks = g.Kdim / kKs;
-    return g;
+__device__ __forceinline__ void ev_cons(const PParams& p, unsigned* evc, int code, int gi) {
+  unsigned long long* b = ev_base(p);
+  if (b) {
+    const unsigned i = atomicAdd(evc, 1u);
+    if (i < 8192) b[i] = ev_word(code, gi);
   }
-};
-
-// ---------------------------------------------------------------------------
-// grid barrier (consumer threads only)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ bool grid_barrier(const PParams& p, unsigned int target) {
-  named_bar(BAR_ALL, kConsumers);
-  __shared__ int s_abort;
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(p.bar, 1u);
-    int ab = 0;
-    if (ld_acquire_u32(p.bar) < target) {
-      const long long t0 = clock64();
-      while (ld_acquire_u32(p.bar) < target) {
-        if (*(volatile int*)p.abort_flag) { ab = 1; break; }
-        if (clock64() - t0 > kSpinLimit) {
-          set_status(p.status, QP_ERR_TIMEOUT);
-          atomicExch(p.abort_flag, 1);
-          ab = 1;
-          break;
-        }
-      }
-    }
-    __threadfence();
-    s_abort = ab;
-  }
-  named_bar(BAR_ALL, kConsumers);
-  return s_abort == 0;
 }
 
+// ------------------------------------------------------------------ waits
 __device__ __forceinline__ void abort_all(const PParams& p) {
   set_status(p.status, QP_ERR_TIMEOUT);
   atomicExch(p.abort_flag, 1);
 }
+__device__ __forceinline__ bool aborted(const PParams& p) { return *(volatile int*)p.abort_flag != 0; }
 
-// Sum over the 128 threads of one half (4 warps) of the consumers.
-__device__ __forceinline__ float half_sum(float v, float* red4, int half) {
-  const int lane = threadIdx.x & 31, w = (threadIdx.x >> 5) & 3;
-  v = warp_sum(v);
-  if (lane == 0) red4[w] = v;
-  named_bar(BAR_H0 + half, 128);
-  const float s = red4[0] + red4[1] + red4[2] + red4[3];
-  named_bar(BAR_H0 + half, 128);
-  return s;
-}
-
-// Sum / max over all 256 consumer threads.
-__device__ __forceinline__ float all_sum(float v, Smem& sm) {
-  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
-  v = warp_sum(v);
-  if (lane == 0) sm.red[0][w] = v;
-  named_bar(BAR_ALL, kConsumers);
-  float s = 0.f;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) s += sm.red[0][i];
-  named_bar(BAR_ALL, kConsumers);
-  return s;
-}
-
-// ---------------------------------------------------------------------------
-// elementwise phases
-// ---------------------------------------------------------------------------
-
-// Step 1 inputs: act rows 2b = f16(H[b]) and 2b+1 = f16(E0[q0[b]]) in the
-// projection's operand layout; residual rows start at the projection bias.
-__device__ void phase_prep(const PParams& p) {
-  const int R = 2 * p.B;
-  const Chunking c = chunking(R);
-  for (int r = blockIdx.x; r < R; r += gridDim.x) {
-    const int b = r >> 1;
-    int q = 0;
-    if (r & 1) {
-      q = p.q0[b];
-      if (q < 0 || q >= p.q0_vocab) {
-        if (threadIdx.x == 0) set_status(p.status, QP_ERR_BAD_TOKEN);
-        q = q < 0 ? 0 : p.q0_vocab - 1;
-      }
-    }
-    for (int k = threadIdx.x * 4; k < p.th; k += kConsumers * 4) {
-      float v[4];
-      if (r & 1) {
-        const uint2 e = *reinterpret_cast<const uint2*>(p.e0 + size_t(q) * p.th + k);
-        v[0] = bf16_bits_to_f32(e.x & 0xffff); v[1] = bf16_bits_to_f32(e.x >> 16);
-        v[2] = bf16_bits_to_f32(e.y & 0xffff); v[3] = bf16_bits_to_f32(e.y >> 16);
-      } else {
-        const float4 h = *reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k);
-        v[0] = h.x; v[1] = h.y; v[2] = h.z; v[3] = h.w;
-      }
-      uint2 o;
-      o.x = uint32_t(f32_to_f16_bits(v[0])) | (uint32_t(f32_to_f16_bits(v[1])) << 16);
-      o.y = uint32_t(f32_to_f16_bits(v[2])) | (uint32_t(f32_to_f16_bits(v[3])) << 16);
-      *reinterpret_cast<uint2*>(p.act + act_off(r, k, p.th, c)) = o;
-    }
-    for (int k = threadIdx.x; k < p.d; k += kConsumers) p.xres[size_t(r) * p.d + k] = p.b_proj[k];
-  }
-}
-
-// act = f16(RMSNorm(xres[src row]) * w) in the layout for R rows; zero the
-// next GEMM's accumulator rows.
-__device__ void phase_norm(const PParams& p, Smem& sm, int R, int src_stride, int src_off, const float* w,
-                           float* zero_acc, int zero_ld) {
-  const Chunking c = chunking(R);
-  for (int r = blockIdx.x; r < R; r += gridDim.x) {
-    const float* x = p.xres + (size_t(r) * src_stride + src_off) * p.d;
-    float v[4][4];
-    float ss = 0.f;
-    int n = 0;
-    for (int k = threadIdx.x * 4; k < p.d; k += kConsumers * 4, ++n) {
-      const float4 t = __ldcg(reinterpret_cast<const float4*>(x + k));
-      v[n][0] = t.x; v[n][1] = t.y; v[n][2] = t.z; v[n][3] = t.w;
-      ss += t.x * t.x + t.y * t.y + t.z * t.z + t.w * t.w;
-    }
-    ss = all_sum(ss, sm);
-    const float inv = rsqrtf(ss / float(p.d) + p.eps);
-    n = 0;
-    for (int k = threadIdx.x * 4; k < p.d; k += kConsumers * 4, ++n) {
-      uint2 o;
-      o.x = uint32_t(f32_to_f16_bits(v[n][0] * inv * w[k])) | (uint32_t(f32_to_f16_bits(v[n][1] * inv * w[k + 1])) << 16);
-      o.y = uint32_t(f32_to_f16_bits(v[n][2] * inv * w[k + 2])) | (uint32_t(f32_to_f16_bits(v[n][3] * inv * w[k + 3])) << 16);
-      *reinterpret_cast<uint2*>(p.act + act_off(r, k, p.d, c)) = o;
-    }
-    if (zero_acc)
-      for (int k = threadIdx.x * 4; k < zero_ld; k += kConsumers * 4)
-        *reinterpret_cast<float4*>(zero_acc + size_t(r) * zero_ld + k) = make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-}
-
-// Per-head RMSNorm then rotate-half RoPE of a 128-vector held one element
-// per thread of a half.
-__device__ __forceinline__ float head_norm_rope(float v, const float* nw, float eps, const float2* cs_row,
-                                                Smem& sm, int half) {
-  const int t = threadIdx.x & 127;
-  const float ss = half_sum(v * v, sm.red[half], half);
-  const float n = v * rsqrtf(ss / 128.f + eps) * nw[t];
-  sm.xs[half][t] = n;
-  named_bar(BAR_H0 + half, 128);
-  const float2 cs = cs_row[t & 63];
-  const float r = t < 64 ? n * cs.x - sm.xs[half][t + 64] * cs.y : n * cs.x + sm.xs[half][t - 64] * cs.y;
-  named_bar(BAR_H0 + half, 128);
-  return r;
-}
-
-// Attention of one (frame, kv head): per-head norms and RoPE of the new
-// position(s), KV cache append, causal softmax over positions 0..pos for
-// every q head of the group; output into the O-proj operand.
-__device__ void phase_attn(const PParams& p, Smem& sm, int l, int P, int pos0) {
-  const int B = p.B, R = B * P, ctx = p.n_steps + 1, grp = p.n_q / p.n_kv;
-  const int qkvw = p.qw + 2 * p.kvw;
-  const Chunking c = chunking(R);
-  const int half = threadIdx.x >> 7, t = threadIdx.x & 127, lane = threadIdx.x & 31, wq = (threadIdx.x >> 5) & 3;
-  const PLayer& L = p.layer[l];
-  float* kv_l = p.kv + size_t(l) * p.Bmax * ctx * 2 * p.kvw;
-  for (int item = blockIdx.x; item < B * p.n_kv; item += gridDim.x) {
-    const int b = item / p.n_kv, j = item % p.n_kv;
-    float* kvb = kv_l + size_t(b) * ctx * 2 * p.kvw;
-    for (int pp = 0; pp < P; ++pp) {
-      const int r = b * P + pp, pos = pos0 + pp;
-      if (half == 0) {
-        const float kr = __ldcg(p.acc_qkv + size_t(r) * qkvw + p.qw + j * 128 + t);
-        const float ko = head_norm_rope(kr, L.k_norm, p.eps, p.rope_cs + pos * 64, sm, 0);
-        kvb[(size_t(pos) * 2 + 0) * p.kvw + j * 128 + t] = ko;
-      } else {
-        kvb[(size_t(pos) * 2 + 1) * p.kvw + j * 128 + t] =
-            __ldcg(p.acc_qkv + size_t(r) * qkvw + p.qw + p.kvw + j * 128 + t);
-      }
-    }
-    named_bar(BAR_ALL, kConsumers);
-    const float scale = rsqrtf(128.f);
-    for (int pp = 0; pp < P; ++pp) {
-      const int r = b * P + pp, pos = pos0 + pp;
-      for (int gi = half; gi < grp; gi += 2) {
-        const int hq = j * grp + gi;
-        const float qr = __ldcg(p.acc_qkv + size_t(r) * qkvw + hq * 128 + t);
-        const float qo = head_norm_rope(qr, L.q_norm, p.eps, p.rope_cs + pos * 64, sm, half);
-        sm.xs[half][t] = qo;
-        named_bar(BAR_H0 + half, 128);
-        for (int i = wq; i <= pos; i += 4) {
-          const float* kr = kvb + (size_t(i) * 2 + 0) * p.kvw + j * 128;
-          const float4 kk = __ldcg(reinterpret_cast<const float4*>(kr + lane * 4));
-          float s = sm.xs[half][lane * 4] * kk.x + sm.xs[half][lane * 4 + 1] * kk.y +
-                    sm.xs[half][lane * 4 + 2] * kk.z + sm.xs[half][lane * 4 + 3] * kk.w;
-          s = warp_sum(s);
-          if (lane == 0) sm.sc[half][i] = s * scale;
-        }
-        named_bar(BAR_H0 + half, 128);
-        float mx = -INFINITY;
-        for (int i = 0; i <= pos; ++i) mx = fmaxf(mx, sm.sc[half][i]);
-        float den = 0.f, o = 0.f;
-        for (int i = 0; i <= pos; ++i) {
-          const float e = expf(sm.sc[half][i] - mx);
-          den += e;
-          o += e * __ldcg(kvb + (size_t(i) * 2 + 1) * p.kvw + j * 128 + t);
-        }
-        p.act[act_off(r, hq * 128 + t, p.qw, c)] = f32_to_f16_bits(o / den);
-        named_bar(BAR_H0 + half, 128);
-      }
-    }
-    named_bar(BAR_ALL, kConsumers);
-  }
-}
-
-// act = f16(silu(gate) * up) for R rows.
-__device__ void phase_swiglu(const PParams& p, int R) {
-  const Chunking c = chunking(R);
-  const int F = p.F;
-  for (int r = blockIdx.x; r < R; r += gridDim.x) {
-    const float* gu = p.acc_gu + size_t(r) * 2 * F;
-    for (int k = threadIdx.x * 4; k < F; k += kConsumers * 4) {
-      const float4 g = __ldcg(reinterpret_cast<const float4*>(gu + k));
-      const float4 u = __ldcg(reinterpret_cast<const float4*>(gu + F + k));
-      uint2 o;
-      o.x = uint32_t(f32_to_f16_bits(silu_f(g.x) * u.x)) | (uint32_t(f32_to_f16_bits(silu_f(g.y) * u.y)) << 16);
-      o.y = uint32_t(f32_to_f16_bits(silu_f(g.z) * u.z)) | (uint32_t(f32_to_f16_bits(silu_f(g.w) * u.w)) << 16);
-      *reinterpret_cast<uint2*>(p.act + act_off(r, k, F, c)) = o;
+// Until *ctr >= want (acquire), bounded.
+__device__ bool poll_geq(const PParams& p, const unsigned* ctr, unsigned want) {
+  if (ld_acquire_u32(ctr) >= want) return true;
+  const long long t0 = clock64();
+  for (unsigned it = 1;; ++it) {
+    if (ld_acquire_u32(ctr) >= want) return true;
+    if ((it & 63) == 0) {
+      if (aborted(p)) return false;
+      if (clock64() - t0 > kSpinLimit) { abort_all(p); return false; }
     }
   }
 }
 
-// Decision of step `step` for each frame: greedy argmax, or Gumbel-max over
-// the top-k of logits / T.  Writes the code, the logits if asked, and the
-// next position's residual row E[step-1][code].
-__device__ void phase_decide(const PParams& p, Smem& sm, int step) {
-  const int V = p.V, t = threadIdx.x, lane = t & 31, w = t >> 5;
-  for (int b = blockIdx.x; b < p.B; b += gridDim.x) {
-    const float* l = p.logits + size_t(b) * V;
-    if (p.out_logits) {
-      float* o = p.out_logits + (size_t(b) * p.n_steps + (step - 1)) * V;
-      for (int i = t; i < V; i += kConsumers) o[i] = __ldcg(l + i);
+// mbarrier phase wait, bounded, abandoning when the grid aborts.
+__device__ bool mwait(const PParams& p, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (unsigned it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255) == 0) {
+      if (aborted(p)) return false;
+      if (clock64() - t0 > kSpinLimit) { abort_all(p); return false; }
     }
-    unsigned long long best = 0ull;
-    if (p.temperature <= 0.f) {
-      for (int i = t; i < V; i += kConsumers) {
-        const unsigned long long pk = pack_argmax(__ldcg(l + i), i);
-        best = pk > best ? pk : best;
-      }
+  }
+}
+
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Fetch-and-add with acquire-release semantics at GPU scope: publishes this
+// CTA's earlier writes (ordered before it by bar.sync) and, for the caller
+// that completes a count, makes every earlier contributor's writes visible.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// ----------------------------------------------------------- the program
+struct Ck { int Nc, n; };
+__device__ __forceinline__ Ck chunking(int R) {
+  const int r16 = (R + 15) & ~15;
+  if (r16 <= kMaxNc) return {r16, 1};
+  return {kMaxNc, (R + kMaxNc - 1) / kMaxNc};
+}
+__device__ __forceinline__ int rows_in(int R, Ck c, int ch) { return min(c.Nc, R - ch * c.Nc); }
+
+// Element offset of (row n, feature k) in an operand buffer laid out
+// [chunk][K/8][Nc/8][8 rows][8 k] for reduction length Kdim.
+__device__ __forceinline__ size_t act_off(int n, int k, int Kdim, Ck c) {
+  const int ch = n / c.Nc, nn = n - ch * c.Nc;
+  return size_t(ch) * Kdim * c.Nc + (size_t((k >> 3) * (c.Nc >> 3) + (nn >> 3)) << 6) + ((nn & 7) << 3) + (k & 7);
+}
+
+struct GI {
+  int kind, k, l, R, n_mt, n_ks, Kdim, ld;
+  const uint8_t* w; const __half* s; const uint16_t* act; float* acc;
+};
+
+__device__ __forceinline__ int gi_of(const PParams& p, int k, int l, int t) { return 1 + (k - 1) * (4 * p.L + 1) + 4 * l + t; }
+__device__ __forceinline__ int gi_head(const PParams& p, int k) { return 1 + (k - 1) * (4 * p.L + 1) + 4 * p.L; }
+
+__device__ GI gemm_inst(const PParams& p, int gi) {
+  GI g;
+  const int B = p.B;
+  if (gi == 0) {
+    g.kind = G_PROJ; g.k = 1; g.l = 0; g.R = 2 * B; g.n_mt = p.d / kTileM; g.Kdim = p.th;
+    g.w = p.w_proj; g.s = p.s_proj; g.act = p.a1[0]; g.acc = p.x1; g.ld = p.d;
+  } else {
+    const int j = gi - 1, per = 4 * p.L + 1, r = j % per;
+    g.k = j / per + 1;
+    const bool s1 = g.k == 1;
+    if (r == 4 * p.L) {
+      g.kind = G_HEAD; g.l = p.L - 1; g.R = B; g.n_mt = p.V / kTileM; g.Kdim = p.d;
+      g.w = p.w_head[g.k - 1]; g.s = p.s_head[g.k - 1]; g.act = p.ahead; g.acc = p.logits; g.ld = p.V;
     } else {
-      const float T = p.temperature;
-      for (int i = t; i < V; i += kConsumers) sm.keys[i] = f32_order_key(__ldcg(l + i) / T);
-      uint32_t prefix = 0, mask = 0;
-      int remaining = p.top_k;
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        sm.hist[t] = 0;
-        named_bar(BAR_ALL, kConsumers);
-        for (int i = t; i < V; i += kConsumers) {
-          const uint32_t k = sm.keys[i];
-          if ((k & mask) == prefix) atomicAdd(&sm.hist[(k >> shift) & 255], 1);
-        }
-        named_bar(BAR_ALL, kConsumers);
-        if (t == 0) {
-          int cum = 0, sel = 0;
-          for (int dg = 255; dg >= 0; --dg) {
-            if (cum + sm.hist[dg] >= remaining) { sel = dg; break; }
-            cum += sm.hist[dg];
-          }
-          sm.sh_int[0] = sel;
-          sm.sh_int[1] = remaining - cum;
-        }
-        named_bar(BAR_ALL, kConsumers);
-        prefix |= uint32_t(sm.sh_int[0]) << shift;
-        mask |= 255u << shift;
-        remaining = sm.sh_int[1];
-        named_bar(BAR_ALL, kConsumers);
-      }
-      const uint32_t kth = prefix;
-      const int per = (V + kConsumers - 1) / kConsumers;
-      const int lo = t * per, hi = min(V, lo + per);
-      int cnt = 0;
-      for (int i = lo; i < hi; ++i) cnt += sm.keys[i] == kth;
-      sm.chunk_cnt[t] = cnt;
-      named_bar(BAR_ALL, kConsumers);
-      if (t == 0) {
-        int run = 0;
-        for (int i = 0; i < kConsumers; ++i) { const int cc = sm.chunk_cnt[i]; sm.chunk_cnt[i] = run; run += cc; }
-      }
-      named_bar(BAR_ALL, kConsumers);
-      int eq_rank = sm.chunk_cnt[t];
-      const float* gb = p.gumbel + (size_t(b) * p.n_steps + (step - 1)) * V;
-      for (int i = lo; i < hi; ++i) {
-        const uint32_t k = sm.keys[i];
-        bool in = k > kth;
-        if (k == kth) { in = eq_rank < remaining; ++eq_rank; }
-        if (in) {
-          const float z = __ldcg(l + i) / T;
-          const unsigned long long pk = pack_argmax(z + gb[i], i);
-          best = pk > best ? pk : best;
-        }
+      g.l = r / 4;
+      g.R = s1 ? 2 * B : B;
+      const PLayer& L = p.layer[g.l];
+      const int t = r % 4;
+      g.w = L.w[t]; g.s = L.s[t];
+      switch (t) {
+        case 0: g.kind = G_QKV; g.n_mt = (p.qw + 2 * p.kvw) / kTileM; g.Kdim = p.d;
+                g.act = s1 ? p.a1[1] : p.ak[0]; g.acc = s1 ? p.acc1_qkv : p.acck_qkv; g.ld = p.qw + 2 * p.kvw; break;
+        case 1: g.kind = G_O; g.n_mt = p.d / kTileM; g.Kdim = p.qw;
+                g.act = s1 ? p.a1[2] : p.ak[1]; g.acc = s1 ? p.x1 : p.xk; g.ld = p.d; break;
+        case 2: g.kind = G_GU; g.n_mt = 2 * p.F / kTileM; g.Kdim = p.d;
+                g.act = s1 ? p.a1[3] : p.ak[2]; g.acc = s1 ? p.acc1_gu : p.acck_gu; g.ld = 2 * p.F; break;
+        default: g.kind = G_DOWN; g.n_mt = p.d / kTileM; g.Kdim = p.F;
+                 g.act = s1 ? p.a1[4] : p.ak[3]; g.acc = s1 ? p.x1 : p.xk; g.ld = p.d; break;
       }
     }
-    best = warp_max_u64(best);
-    if (lane == 0) sm.redu[w] = best;
-    named_bar(BAR_ALL, kConsumers);
-    if (t == 0) {
-      unsigned long long v = sm.redu[0];
-      for (int i = 1; i < 8; ++i) v = sm.redu[i] > v ? sm.redu[i] : v;
-      const int code = unpack_argmax_index(v);
-      p.out_codes[size_t(b) * p.n_steps + (step - 1)] = code;
-      int nc = p.forced ? p.forced[size_t(b) * p.n_steps + (step - 1)] : code;
-      if (nc < 0 || nc >= V) {
-        set_status(p.status, QP_ERR_BAD_TOKEN);
-        nc = nc < 0 ? 0 : V - 1;
-      }
-      sm.sh_int[2] = nc;
-    }
-    named_bar(BAR_ALL, kConsumers);
-    if (step < p.n_steps) {
-      const uint16_t* e = p.embed[step - 1] + size_t(sm.sh_int[2]) * p.d;
-      for (int i = t; i < p.d; i += kConsumers) p.xres[size_t(b) * p.d + i] = bf16_bits_to_f32(e[i]);
-    }
-    named_bar(BAR_ALL, kConsumers);
   }
+  g.n_ks = g.Kdim / kKs;
+  return g;
 }
 
-// ---------------------------------------------------------------------------
-// GEMM phase, consumer side
-// ---------------------------------------------------------------------------
-__device__ bool phase_gemm(const PParams& p, Smem& sm, const Gemm& g, int gemm_idx, uint32_t& slot_it,
-                           uint32_t& act_it, uint32_t& mma_it) {
-  const Chunking c = chunking(g.R);
-  const int total = c.n_chunks * g.n_mt * g.n_ks;
-  int beg, end;
-  my_slices(total, gemm_idx, beg, end);
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  const uint32_t idesc = idesc_f16(kTileM, c.Nc);
-  const uint32_t act_bytes = uint32_t(kKs) * c.Nc * 2;
-  int* failed = &sm.sh_int[3];   // a wait ran out: unwind the whole grid
-  if (t == 0) {
-    *failed = 0;
-    if (beg < end) fence_proxy_async_global();
-  }
-  named_bar(BAR_ALL, kConsumers);
-  for (int s = beg; s < end; ++s) {
-    const int ks = s % g.n_ks, tt = s / g.n_ks, mt = tt % g.n_mt, ch = tt / g.n_mt;
-    const bool first = (s == beg) || ks == 0;
-    const bool last = (s == end - 1) || ks == g.n_ks - 1;
-    const uint32_t slot = slot_it % kNSlot, spar = (slot_it / kNSlot) & 1;
-    ++slot_it;
-    if (t == 0) {
-      const uint16_t* src = p.act + size_t(ch) * g.Kdim * c.Nc + size_t(ks) * kKs * c.Nc;
-      mbar_expect_tx(&sm.actbar, act_bytes);
-      bulk_g2s(sm.actb, src, act_bytes, &sm.actbar);
+// This CTA's contiguous run [beg, end) of a GEMM's slices.  Slices are
+// ordered (chunk, 128-row tile, K slice); runs rotate with the GEMM index.
+__device__ __forceinline__ void my_run(int total, int gi, int& beg, int& end) {
+  const int G = gridDim.x, g = (blockIdx.x + gi * 37) % G;
+  beg = int((long long)total * g / G);
+  end = int((long long)total * (g + 1) / G);
+}
+
+// sync-region accessors
+__device__ __forceinline__ unsigned* tile_cnt(const PParams& p, int gi, int ch, int mt) {
+  return p.tile_cnt + (size_t(gi) * p.NCH + ch) * p.MT + mt;
+}
+__device__ __forceinline__ unsigned* ready_cnt(const PParams& p, int gi, int ch, int ks) {
+  return p.ready + (size_t(gi) * p.NCH + ch) * p.KS + ks;
+}
+__device__ __forceinline__ unsigned* ss_cnt(const PParams& p, int gi, int ch) { return p.ss_cnt + size_t(gi) * p.NCH + ch; }
+__device__ __forceinline__ float* ss_at(const PParams& p, int gi, int row) { return p.ss + size_t(gi) * 2 * p.B + row; }
+__device__ __forceinline__ unsigned* pair_cnt(const PParams& p, int k, int l, int ch, int kd) {
+  return p.pair + ((size_t(k - 1) * p.L + l) * p.NCH + ch) * (p.F / kTileM) + kd;
+}
+__device__ __forceinline__ unsigned* head_done(const PParams& p, int k, int ch) {
+  return p.head_done + size_t(k - 1) * p.NCH + ch;
+}
+
+__device__ __forceinline__ uint2 pack4_f16(float a, float b, float c, float d) {
+  return make_uint2(uint32_t(f32_to_f16_bits(a)) | (uint32_t(f32_to_f16_bits(b)) << 16),
+                    uint32_t(f32_to_f16_bits(c)) | (uint32_t(f32_to_f16_bits(d)) << 16));
+}
+
+// ---------------------------------------------------------------- producer
+__device__ void producer_role(const PParams& p, Misc& ms, uint8_t* smem) {
+  const int nslot = p.q8 ? kNSlotQ8 : kNSlotF16;
+  const uint32_t stride = p.q8 ? kQ8SlotBytes : kSlotBytes;
+  const uint64_t pol = policy_evict_first();
+  uint32_t it = 0;
+  for (int gi = 0; gi < p.NGEMM; ++gi) {
+    const GI G = gemm_inst(p, gi);
+    const Ck c = chunking(G.R);
+    int beg, end;
+    my_run(c.n * G.n_mt * G.n_ks, gi, beg, end);
+    for (int s = beg; s < end; ++s) {
+      const int ks = s % G.n_ks, mt = (s / G.n_ks) % G.n_mt;
+      const uint32_t slot = it % nslot, u = it / nslot;
+      if (u > 0 && !mwait(p, &ms.wempty[slot], (u - 1) & 1)) goto drain;
+      {
+        const size_t tile = size_t(mt) * G.n_ks + ks;
+        uint8_t* dst = smem + kOffRing + slot * stride;
+        if (p.q8) {
+          mbar_expect_tx(&ms.wfull[slot], kQ8SlotBytes);
+          bulk_g2s_stream(dst, G.w + tile * kQ8Bytes, kQ8Bytes, &ms.wfull[slot], pol);
+          bulk_g2s_stream(dst + kQ8Bytes, reinterpret_cast<const uint8_t*>(G.s) + tile * kQ8ScaleBytes, kQ8ScaleBytes,
+                          &ms.wfull[slot], pol);
+        } else {
+          mbar_expect_tx(&ms.wfull[slot], kSlotBytes);
+          bulk_g2s_stream(dst, G.w + tile * kSlotBytes, kSlotBytes, &ms.wfull[slot], pol);
+        }
+      }
+      ++it;
     }
-    const uint8_t* a_src = sm.slot[slot];
-    if (p.q8) {
-      if (!mbar_wait(&sm.full[slot], spar)) atomicOr(failed, 1);
-      // dequantise the int8 slice into the f16 operand buffer (same order)
-      const int8_t* qv = reinterpret_cast<const int8_t*>(sm.slot[slot]);
-      const __half* sc = reinterpret_cast<const __half*>(sm.slot[slot] + kQ8Bytes);
-      uint16_t* dq = reinterpret_cast<uint16_t*>(sm.deq);
-      for (int e = t * 16; e < kTileM * kKs; e += kConsumers * 16) {
-        // e indexes [k8][m8][8 rows][8 k]; 16 values = 2 rows of one core matrix
+  }
+drain:
+  // every copy issued into this CTA's shared memory lands before it exits
+  for (uint32_t k = it > uint32_t(nslot) ? it - nslot : 0; k < it; ++k) mbar_wait(&ms.wfull[k % nslot], (k / nslot) & 1);
+}
+
+// --------------------------------------------------------- Q8_0 dequant
+__device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
+  const int t = threadIdx.x - kDeqWarp0 * 32;
+  uint32_t it = 0;
+  for (int gi = 0; gi < p.NGEMM; ++gi) {
+    const GI G = gemm_inst(p, gi);
+    const Ck c = chunking(G.R);
+    int beg, end;
+    my_run(c.n * G.n_mt * G.n_ks, gi, beg, end);
+    for (int s = beg; s < end; ++s, ++it) {
+      const uint32_t rs = it % kNSlotQ8, ru = it / kNSlotQ8, ds = it % kNDeq, du = it / kNDeq;
+      if (t == 0) {   // the leader waits for every dequant thread, then broadcasts
+        bool w = mwait(p, &ms.wfull[rs], ru & 1);
+        if (w && du > 0) w = mwait(p, &ms.dempty[ds], (du - 1) & 1);
+        ms.deq_ok = w;
+      }
+      named_bar(BAR_DEQ, kDeqThreads);
+      if (!ms.deq_ok) return;
+      const uint8_t* src = smem + kOffRing + rs * kQ8SlotBytes;
+      const int8_t* qv = reinterpret_cast<const int8_t*>(src);
+      const __half* sc = reinterpret_cast<const __half*>(src + kQ8Bytes);
+      uint16_t* dq = reinterpret_cast<uint16_t*>(smem + kOffDeq + ds * kSlotBytes);
+      for (int e = t * 16; e < kTileM * kKs; e += kDeqThreads * 16) {
+        // e walks [k8][m8][8 rows][8 k]; 16 values are two rows of one core matrix
         const int4 raw = *reinterpret_cast<const int4*>(qv + e);
         const int8_t* q = reinterpret_cast<const int8_t*>(&raw);
         uint32_t out[8];
@@ -524,288 +364,841 @@ __device__ bool phase_gemm(const PParams& p, Smem& sm, const Gemm& g, int gemm_i
         *reinterpret_cast<uint4*>(dq + e + 8) = make_uint4(out[4], out[5], out[6], out[7]);
       }
       fence_proxy_async_shared();
-      named_bar(BAR_ALL, kConsumers);
-      if (t == 0) mbar_arrive(&sm.empty[slot]);
-      a_src = sm.deq;
+      named_bar(BAR_DEQ, kDeqThreads);
+      if (t == 0) {
+        mbar_arrive(&ms.wempty[rs]);
+        mbar_arrive(&ms.dfull[ds]);
+      }
     }
-    if (t == 0) {
-      if (!p.q8 && !mbar_wait(&sm.full[slot], spar)) *failed = 1;
-      if (!mbar_wait(&sm.actbar, act_it & 1)) *failed = 1;
-    }
-    if (t == 0 && !*failed) {
+  }
+}
+
+// --------------------------------------------------------------- MMA warp
+__device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
+  uint32_t wit = 0, ait = 0, seg = 0;
+  unsigned evi = 0;
+  bool ok = true;
+  for (int gi = 0; gi < p.NGEMM && ok; ++gi) {
+    const GI G = gemm_inst(p, gi);
+    const Ck c = chunking(G.R);
+    int beg, end;
+    my_run(c.n * G.n_mt * G.n_ks, gi, beg, end);
+    const uint32_t idesc = idesc_f16(kTileM, c.Nc);
+    const uint32_t abytes = uint32_t(kKs) * c.Nc * 2;
+    for (int s = beg; s < end; ++s) {
+      const int ks = s % G.n_ks, tt = s / G.n_ks, ch = tt / G.n_mt;
+      const bool first = s == beg || ks == 0;
+      const bool last = s == end - 1 || ks == G.n_ks - 1;
+      if (!poll_geq(p, ready_cnt(p, gi, ch, ks), unsigned(rows_in(G.R, c, ch)))) { ok = false; break; }
+      ev_mma(p, evi, EV_READY, gi);
+      const uint32_t a = ait % kNAct, au = ait / kNAct;
+      if (au > 0 && !mwait(p, &ms.aempty[a], (au - 1) & 1)) { ok = false; break; }
+      uint8_t* abuf = smem + kOffAct + a * kActBytes;
+      fence_proxy_async_global();
+      mbar_expect_tx(&ms.afull[a], abytes);
+      bulk_g2s(abuf, G.act + size_t(ch) * G.Kdim * c.Nc + size_t(ks) * kKs * c.Nc, abytes, &ms.afull[a]);
+      const uint8_t* A;
+      uint64_t* wfree;
+      if (p.q8) {
+        const uint32_t ds = wit % kNDeq;
+        if (!mwait(p, &ms.dfull[ds], (wit / kNDeq) & 1)) { ok = false; break; }
+        A = smem + kOffDeq + ds * kSlotBytes;
+        wfree = &ms.dempty[ds];
+      } else {
+        const uint32_t ws = wit % kNSlotF16;
+        if (!mwait(p, &ms.wfull[ws], (wit / kNSlotF16) & 1)) { ok = false; break; }
+        A = smem + kOffRing + ws * kSlotBytes;
+        wfree = &ms.wempty[ws];
+      }
+      const uint32_t tb = seg & 1;
+      if (first && seg >= 2 && !mwait(p, &ms.accempty[tb], ((seg >> 1) - 1) & 1)) { ok = false; break; }
+      if (!mwait(p, &ms.afull[a], au & 1)) { ok = false; break; }
+      ev_mma(p, evi, EV_LANDED, gi);
       tc_fence_after();
-      const uint32_t a0 = smem_u32(a_src), b0 = smem_u32(sm.actb);
+      const uint32_t a0 = smem_u32(A), b0 = smem_u32(abuf), d = ms.tmem_base + tb * 128;
 #pragma unroll
       for (int j = 0; j < kKs / 16; ++j) {
         const uint64_t ad = smem_desc(a0 + j * 2 * (kTileM / 8) * 128, (kTileM / 8) * 128, 128);
         const uint64_t bd = smem_desc(b0 + j * 2 * (c.Nc / 8) * 128, (c.Nc / 8) * 128, 128);
-        mma_f16(sm.tmem_base, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
+        mma_f16(d, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
       }
-      if (!p.q8) mma_commit(&sm.empty[slot]);
-      mma_commit(&sm.mmabar);
-      if (!mbar_wait(&sm.mmabar, mma_it & 1)) *failed = 1;
-      tc_fence_before();
-    }
-    ++act_it;
-    ++mma_it;
-    named_bar(BAR_ALL, kConsumers);
-    if (*failed) {
-      if (t == 0) {
-        abort_all(p);
-        mbar_wait(&sm.actbar, (act_it - 1) & 1);   // the operand copy may still be landing
+      mma_commit(wfree);
+      mma_commit(&ms.aempty[a]);
+      if (last) {
+        mma_commit(&ms.accfull[tb]);
+        // second arrival, by this thread: releases (CTA scope) what its
+        // acquires of the operand counters saw to the consumers' epilogue
+        mbar_arrive(&ms.accfull[tb]);
+        ev_mma(p, evi, EV_COMMIT, gi);
+        ++seg;
       }
-      return false;
+      ++wit;
+      ++ait;
     }
-    if (last) {
-      tc_fence_after();
-      const int quarter = warp & 3, halfc = warp >> 2;
-      const int m = mt * kTileM + quarter * 32 + lane;
-      const int cols = c.Nc / 2;
-      for (int col = halfc * cols; col < (halfc + 1) * cols; col += 8) {
-        float v[8];
-        tmem_ld8(sm.tmem_base + (uint32_t(quarter * 32) << 16) + uint32_t(col), v);
+  }
+  // every MMA retires before TMEM is released
+  mma_commit(&ms.mmadone);
+  mbar_wait(&ms.mmadone, 0);
+}
+
+// ------------------------------------------------------ consumer helpers
+// RMSNorm of a 128-vector held as 4 values per lane, then rotate-half RoPE
+// at position pos (pairs (i, i+64) sit in lanes l and l^16).
+__device__ __forceinline__ float4 norm_rope(float4 x, const float* nw, float eps, const float2* cs, int lane) {
+  const float ss = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
+  const float r = rsqrtf(ss / 128.f + eps);
+  const float4 w = *reinterpret_cast<const float4*>(nw + lane * 4);
+  float v[4] = {x.x * r * w.x, x.y * r * w.y, x.z * r * w.z, x.w * r * w.w};
+  float o[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const int n = ch * c.Nc + col + i;
-          if (n < g.R) red_add_f32(g.acc + size_t(n) * g.ld + m, v[i]);
-        }
+  for (int e = 0; e < 4; ++e) {
+    const float partner = __shfl_xor_sync(0xffffffffu, v[e], 16);
+    const float2 c = cs[(lane * 4 + e) & 63];
+    o[e] = lane < 16 ? v[e] * c.x - partner * c.y : v[e] * c.x + partner * c.y;
+  }
+  return make_float4(o[0], o[1], o[2], o[3]);
+}
+
+// Step-1 inputs, one warp per row r < 2B: operand rows 2b = f16(H_b),
+// 2b+1 = f16(E0[q0_b]); residual rows start at the projection bias.
+__device__ bool prep1_items(const PParams& p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = gridDim.x;
+  const int R = 2 * p.B;
+  const Ck c = chunking(R);
+  for (int r = blockIdx.x + warp * G; r < R; r += kConsumerWarps * G) {
+    const int b = r >> 1, ch = r / c.Nc;
+    if ((r & 1) == 0) {
+      for (int kk = lane * 4; kk < p.th; kk += 128) {
+        const float4 h = *reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + kk);
+        *reinterpret_cast<uint2*>(p.a1[0] + act_off(r, kk, p.th, c)) = pack4_f16(h.x, h.y, h.z, h.w);
       }
-      tc_fence_before();
-      named_bar(BAR_ALL, kConsumers);
+    } else {
+      int q = p.q0[b];
+      if (q < 0 || q >= p.q0_vocab) {
+        if (lane == 0) set_status(p.status, QP_ERR_BAD_TOKEN);
+        q = q < 0 ? 0 : p.q0_vocab - 1;
+      }
+      for (int kk = lane * 4; kk < p.th; kk += 128) {
+        const uint2 e = *reinterpret_cast<const uint2*>(p.e0 + size_t(q) * p.th + kk);
+        *reinterpret_cast<uint2*>(p.a1[0] + act_off(r, kk, p.th, c)) =
+            pack4_f16(bf16_bits_to_f32(e.x & 0xffff), bf16_bits_to_f32(e.x >> 16), bf16_bits_to_f32(e.y & 0xffff),
+                      bf16_bits_to_f32(e.y >> 16));
+      }
+    }
+    for (int kk = lane * 4; kk < p.d; kk += 128)
+      *reinterpret_cast<float4*>(p.x1 + size_t(r) * p.d + kk) = *reinterpret_cast<const float4*>(p.b_proj + kk);
+    __syncwarp();
+    if (lane == 0)
+      for (int ks = 0; ks < p.th / kKs; ++ks) red_release_add(ready_cnt(p, 0, ch, ks), 1);
+  }
+  return true;
+}
+
+// The code of step `step` for frame b (lane 0 only): waits for the argmax or
+// the sampled decision.  Returns -1 if the grid aborted.
+__device__ int wait_code(const PParams& p, int step, int b) {
+  const Ck c = chunking(p.B);
+  if (p.temperature > 0.f) {
+    unsigned* dp = p.decided + size_t(step - 1) * p.B + b;
+    if (!poll_geq(p, dp, 1u)) return -1;
+    return int(ld_acquire_u32(dp)) - 1;
+  }
+  if (!poll_geq(p, head_done(p, step, b / c.Nc), unsigned(p.V / kTileM))) return -1;
+  return unpack_argmax_index(ld_acquire_u64(p.codepk + size_t(step - 1) * p.B + b));
+}
+
+// Step k >= 2 inputs, one warp per frame: report the previous step's code,
+// embed the next input (teacher-forced if asked) as residual row b and as
+// the layer-0 QKV operand f16(E * w_attn_norm); its squared norm comes from
+// the table precomputed at load.
+__device__ bool prepk_items(const PParams& p, int k) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = gridDim.x;
+  const Ck c = chunking(p.B);
+  const int gi = gi_of(p, k, 0, 0);
+  const float* wn = p.layer[0].attn_norm;
+  for (int b = (blockIdx.x + k * 11) % G + warp * G; b < p.B; b += kConsumerWarps * G) {
+    int nc = 0;
+    if (lane == 0) {
+      const int code = wait_code(p, k - 1, b);
+      if (code >= 0) {
+        p.out_codes[size_t(b) * p.n_steps + (k - 2)] = code;
+        nc = p.forced ? p.forced[size_t(b) * p.n_steps + (k - 2)] : code;
+        if (nc < 0 || nc >= p.V) {
+          set_status(p.status, QP_ERR_BAD_TOKEN);
+          nc = nc < 0 ? 0 : p.V - 1;
+        }
+      } else {
+        nc = -1;
+      }
+    }
+    nc = __shfl_sync(0xffffffffu, nc, 0);
+    if (nc < 0) return false;
+    __syncwarp();   // the writes below follow lane 0's acquire
+    const uint16_t* e = p.embed[k - 2] + size_t(nc) * p.d;
+    for (int kk = lane * 4; kk < p.d; kk += 128) {
+      const uint2 ev = *reinterpret_cast<const uint2*>(e + kk);
+      const float v0 = bf16_bits_to_f32(ev.x & 0xffff), v1 = bf16_bits_to_f32(ev.x >> 16);
+      const float v2 = bf16_bits_to_f32(ev.y & 0xffff), v3 = bf16_bits_to_f32(ev.y >> 16);
+      *reinterpret_cast<float4*>(p.xk + size_t(b) * p.d + kk) = make_float4(v0, v1, v2, v3);
+      const float4 w = *reinterpret_cast<const float4*>(wn + kk);
+      *reinterpret_cast<uint2*>(p.ak[0] + act_off(b, kk, p.d, c)) = pack4_f16(v0 * w.x, v1 * w.y, v2 * w.z, v3 * w.w);
+    }
+    if (lane == 0) *ss_at(p, gi, b) = p.embed_ss[k - 2][nc];
+    __syncwarp();
+    if (lane == 0) {
+      const int ch = b / c.Nc;
+      for (int ks = 0; ks < p.d / kKs; ++ks) red_release_add(ready_cnt(p, gi, ch, ks), 1);
+      red_release_add(ss_cnt(p, gi, ch), unsigned(p.d / kTileM));
     }
   }
   return true;
 }
 
-// ---------------------------------------------------------------------------
-// producer warp: stream this CTA's weight slices for every GEMM phase
-// ---------------------------------------------------------------------------
-__device__ void producer(const PParams& p, Smem& sm) {
-  const Prog prog(p);
-  const int ng = prog.num_gemms();
-  const uint64_t pol = policy_evict_first();
-  uint32_t it = 0;
-  for (int gi = 0; gi < ng; ++gi) {
-    const Gemm g = prog.gemm(gi);
-    const Chunking c = chunking(g.R);
-    const int total = c.n_chunks * g.n_mt * g.n_ks;
-    int beg, end;
-    my_slices(total, gi, beg, end);
-    for (int s = beg; s < end; ++s) {
-      const int ks = s % g.n_ks, mt = (s / g.n_ks) % g.n_mt;
-      const uint32_t slot = it % kNSlot, u = it / kNSlot;
-      if (u > 0) {
-        bool done = false;
-        const long long t0 = clock64();
-        while (!(done = mbar_try_wait(&sm.empty[slot], (u - 1) & 1))) {
-          if (*(volatile int*)p.abort_flag || clock64() - t0 > kSpinLimit) break;
-        }
-        if (!done) {
-          abort_all(p);
-          // drain copies still in flight into this CTA's shared memory
-          for (uint32_t k = (it >= kNSlot ? it - kNSlot : 0); k < it; ++k)
-            mbar_wait(&sm.full[k % kNSlot], (k / kNSlot) & 1);
-          return;
-        }
-      }
-      const size_t tile = size_t(mt) * g.n_ks + ks;
-      if (p.q8) {
-        mbar_expect_tx(&sm.full[slot], kQ8Bytes + kQ8ScaleBytes);
-        bulk_g2s_stream(sm.slot[slot], g.w + tile * kQ8Bytes, kQ8Bytes, &sm.full[slot], pol);
-        bulk_g2s_stream(sm.slot[slot] + kQ8Bytes, reinterpret_cast<const uint8_t*>(g.s) + tile * kQ8ScaleBytes,
-                        kQ8ScaleBytes, &sm.full[slot], pol);
-      } else {
-        mbar_expect_tx(&sm.full[slot], kSlotBytes);
-        bulk_g2s_stream(sm.slot[slot], g.w + tile * kSlotBytes, kSlotBytes, &sm.full[slot], pol);
-      }
-      ++it;
+__device__ bool final_items(const PParams& p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = gridDim.x;
+  for (int b = (blockIdx.x + 5) % G + warp * G; b < p.B; b += kConsumerWarps * G) {
+    int code = 0;
+    if (lane == 0) {
+      code = wait_code(p, p.n_steps, b);
+      if (code >= 0) p.out_codes[size_t(b) * p.n_steps + (p.n_steps - 1)] = code;
+    }
+    code = __shfl_sync(0xffffffffu, code, 0);
+    if (code < 0) return false;
+  }
+  return true;
+}
+
+// Attention of one (frame, kv head) per warp at layer l of step k: per-head
+// norms and RoPE of the new position(s), KV append, causal softmax over
+// positions 0..pos for the group's q heads; output into the O operand.
+// Lane l holds dims 4l..4l+3 of every 128-vector.  Scores of two q heads x
+// 16 positions are 32 partial dot products per lane, summed across the warp
+// by one reduce-scatter that leaves score (head l/16, position l%16) in lane l.
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
-  // every slot the consumers did not take (abort path) must land before exit
-  for (uint32_t k = (it >= kNSlot ? it - kNSlot : 0); k < it; ++k) mbar_wait(&sm.full[k % kNSlot], (k / kNSlot) & 1);
+  return v[0];
+}
+
+__device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = gridDim.x;
+  const int P = k == 1 ? 2 : 1, pos0 = k == 1 ? 0 : k, R = p.B * P;
+  const Ck c = chunking(R);
+  const int gi_q = gi_of(p, k, l, 0), gi_o = gi_q + 1;
+  const int qkvw = p.qw + 2 * p.kvw, grp = p.n_q / p.n_kv, ctx = p.n_steps + 1;
+  float* acc = k == 1 ? p.acc1_qkv : p.acck_qkv;
+  uint16_t* act_o = k == 1 ? p.a1[2] : p.ak[1];
+  const PLayer& L = p.layer[l];
+  const int n_items = p.B * p.n_kv, nks = p.d / kKs;
+  const float scale = rsqrtf(128.f);
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  float* kvl = p.kv + size_t(l) * p.Bmax * ctx * 2 * p.kvw;
+  for (int i = (blockIdx.x + gi_q * 13) % G + warp * G; i < n_items; i += kConsumerWarps * G) {
+    const int b = i / p.n_kv, j = i % p.n_kv, r0 = b * P, ch = r0 / c.Nc;
+    // the group's q tiles, its k tile and its v tile: one lane polls each
+    int okl = 1;
+    if (lane < grp + 2) {
+      const int tile = lane < grp ? j * grp + lane
+                                  : (lane == grp ? p.qw / kTileM + j : (p.qw + p.kvw) / kTileM + j);
+      okl = poll_geq(p, tile_cnt(p, gi_q, ch, tile), unsigned(nks));
+    }
+    if (!__all_sync(0xffffffffu, okl)) return false;
+    __syncwarp();   // order every lane's reads after the acquires
+    if (lane == 0) ev_cons(p, &ms.evc, EV_ATT_READY, gi_q);
+    float* kvb = kvl + size_t(b) * ctx * 2 * p.kvw + j * 128 + lane * 4;   // + (pos*2 + {0,1}) * kvw
+    for (int pp = 0; pp < P; ++pp) {
+      const int r = r0 + pp, pos = pos0 + pp;
+      float* row = acc + size_t(r) * qkvw;
+      float* kr = row + p.qw + j * 128 + lane * 4;
+      float* vr = row + p.qw + p.kvw + j * 128 + lane * 4;
+      const float4 kraw = __ldcg(reinterpret_cast<const float4*>(kr));
+      const float4 vnew = __ldcg(reinterpret_cast<const float4*>(vr));
+      const float4 knew = norm_rope(kraw, L.k_norm, p.eps, p.rope_cs + pos * 64, lane);
+      *reinterpret_cast<float4*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = knew;
+      *reinterpret_cast<float4*>(kvb + (size_t(pos) * 2 + 1) * p.kvw) = vnew;
+      *reinterpret_cast<float4*>(kr) = z4;
+      *reinterpret_cast<float4*>(vr) = z4;
+      __syncwarp();
+      // keys and values of positions 0..pos (the newest from registers)
+      float4 kk[kMaxCtx];
+#pragma unroll
+      for (int t = 0; t < kMaxCtx; ++t)
+        kk[t] = t < pos ? __ldcg(reinterpret_cast<const float4*>(kvb + (size_t(t) * 2 + 0) * p.kvw))
+                        : (t == pos ? knew : z4);
+      for (int g0 = 0; g0 < grp; g0 += 2) {
+        const int nh = min(2, grp - g0);
+        float4 qn[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          qn[hh] = z4;
+          if (hh < nh) {
+            float* qr = row + (j * grp + g0 + hh) * 128 + lane * 4;
+            qn[hh] = norm_rope(__ldcg(reinterpret_cast<const float4*>(qr)), L.q_norm, p.eps, p.rope_cs + pos * 64,
+                               lane);
+            *reinterpret_cast<float4*>(qr) = z4;
+          }
+        }
+        float part[32];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+          for (int t = 0; t < kMaxCtx; ++t)
+            part[hh * 16 + t] = qn[hh].x * kk[t].x + qn[hh].y * kk[t].y + qn[hh].z * kk[t].z + qn[hh].w * kk[t].w;
+        // lane l: score of head (l >> 4), position (l & 15)
+        const bool valid = (lane >> 4) < nh && (lane & 15) <= pos;
+        const float rsum = reduce_scatter32(part, lane);   // all 32 lanes take part
+        const float sc = valid ? rsum * scale : -INFINITY;
+        float mx = sc;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float e = valid ? expf(sc - mx) : 0.f;
+        float den = e;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        const float pr = den > 0.f ? e / den : 0.f;
+        float4 o2[2] = {z4, z4};
+#pragma unroll
+        for (int t = 0; t < kMaxCtx; ++t) {
+          const float4 vv = t < pos ? __ldcg(reinterpret_cast<const float4*>(kvb + (size_t(t) * 2 + 1) * p.kvw))
+                                    : (t == pos ? vnew : z4);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float w = __shfl_sync(0xffffffffu, pr, hh * 16 + t);
+            o2[hh].x += w * vv.x; o2[hh].y += w * vv.y; o2[hh].z += w * vv.z; o2[hh].w += w * vv.w;
+          }
+        }
+        for (int hh = 0; hh < nh; ++hh)
+          *reinterpret_cast<uint2*>(act_o + act_off(r, (j * grp + g0 + hh) * 128 + lane * 4, p.qw, c)) =
+              pack4_f16(o2[hh].x, o2[hh].y, o2[hh].z, o2[hh].w);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) {
+      for (int g2 = 0; g2 < grp; ++g2) red_release_add(ready_cnt(p, gi_o, ch, j * grp + g2), unsigned(P));
+      ev_cons(p, &ms.evc, EV_ATT_DONE, gi_q);
+    }
+  }
+  return true;
+}
+
+// Finishing work of a completed tile, by the CTA whose contribution
+// completed it (all consumer threads).  Each warp takes rows warp, warp + 8,
+// ...; the loads of up to four of its rows are issued together.
+__device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, int ch, int mt, Ck c) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (G.kind == G_QKV) return true;
+  if (G.kind == G_PROJ || G.kind == G_O || G.kind == G_DOWN) {
+    const int rows = rows_in(G.R, c, ch);
+    const float* X = G.acc;
+    const int feat = mt * kTileM + lane * 4;
+    bool to_head = false;
+    int gi_n;
+    const float* w;
+    uint16_t* act_n;
+    if (G.kind == G_PROJ) {
+      gi_n = gi_of(p, 1, 0, 0); w = p.layer[0].attn_norm; act_n = p.a1[1];
+    } else if (G.kind == G_O) {
+      gi_n = gi + 1; w = p.layer[G.l].ffn_norm; act_n = G.k == 1 ? p.a1[3] : p.ak[2];
+    } else if (G.l + 1 < p.L) {
+      gi_n = gi + 1; w = p.layer[G.l + 1].attn_norm; act_n = G.k == 1 ? p.a1[1] : p.ak[0];
+    } else {
+      to_head = true; gi_n = gi_head(p, G.k); w = p.out_norm; act_n = p.ahead;
+    }
+    const float4 wv = *reinterpret_cast<const float4*>(w + feat);
+    const int P = G.k == 1 ? 2 : 1;
+    const Ck ch_h = chunking(p.B);
+    for (int r0 = warp; r0 < rows; r0 += 4 * kConsumerWarps) {
+      float4 xv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = r0 + u * kConsumerWarps, n = ch * c.Nc + row;
+        const bool use = row < rows && (!to_head || (n % P) == P - 1);
+        xv[u] = use ? __ldcg(reinterpret_cast<const float4*>(X + size_t(n) * p.d + feat)) : z4;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = r0 + u * kConsumerWarps, n = ch * c.Nc + row;
+        if (row >= rows || (to_head && (n % P) != P - 1)) continue;
+        const float4 x = xv[u];
+        const float sq = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
+        const int nr = to_head ? n / P : n;
+        if (lane == 0) red_add_f32(ss_at(p, gi_n, nr), sq);
+        *reinterpret_cast<uint2*>(act_n + act_off(nr, feat, p.d, to_head ? ch_h : c)) =
+            pack4_f16(x.x * wv.x, x.y * wv.y, x.z * wv.z, x.w * wv.w);
+      }
+    }
+    named_bar(BAR_CONS, kConsumers);
+    if (t == 0) {
+      // release: the bar.sync above orders every consumer thread's writes first
+      if (!to_head) {
+        red_release_add(ready_cnt(p, gi_n, ch, mt), unsigned(rows));
+        red_release_add(ss_cnt(p, gi_n, ch), unsigned(rows));
+      } else {
+        // frames whose last position lies in this chunk: [nlo/P, nhi/P)
+        const int f0 = (ch * c.Nc) / P, f1 = (ch * c.Nc + rows) / P;
+        for (int hc = f0 / ch_h.Nc; f1 > f0 && hc <= (f1 - 1) / ch_h.Nc; ++hc) {
+          const int lo = max(f0, hc * ch_h.Nc), hi = min(f1, (hc + 1) * ch_h.Nc);
+          red_release_add(ready_cnt(p, gi_n, hc, mt), unsigned(hi - lo));
+          red_release_add(ss_cnt(p, gi_n, hc), unsigned(hi - lo));
+        }
+      }
+    }
+    return true;
+  }
+  if (G.kind == G_GU) {
+    const int nkd = p.F / kTileM, kd = mt % nkd;
+    if (t == 0) ms.flag[2] = atom_add_acq_rel(pair_cnt(p, G.k, G.l, ch, kd), 1u) == 1u;
+    named_bar(BAR_CONS, kConsumers);
+    if (!ms.flag[2]) return true;
+    const int rows = rows_in(G.R, c, ch);
+    uint16_t* act_d = G.k == 1 ? p.a1[4] : p.ak[3];
+    const int feat = kd * kTileM + lane * 4;
+    for (int r0 = warp; r0 < rows; r0 += 4 * kConsumerWarps) {
+      float4 gv[4], uv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = r0 + u * kConsumerWarps;
+        const float* gp = G.acc + size_t(ch * c.Nc + row) * 2 * p.F + feat;
+        gv[u] = row < rows ? __ldcg(reinterpret_cast<const float4*>(gp)) : z4;
+        uv[u] = row < rows ? __ldcg(reinterpret_cast<const float4*>(gp + p.F)) : z4;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = r0 + u * kConsumerWarps, n = ch * c.Nc + row;
+        if (row >= rows) continue;
+        float* gp = G.acc + size_t(n) * 2 * p.F + feat;
+        const float4 g = gv[u], uu = uv[u];
+        *reinterpret_cast<uint2*>(act_d + act_off(n, feat, p.F, c)) =
+            pack4_f16(silu_f(g.x) * uu.x, silu_f(g.y) * uu.y, silu_f(g.z) * uu.z, silu_f(g.w) * uu.w);
+        *reinterpret_cast<float4*>(gp) = z4;
+        *reinterpret_cast<float4*>(gp + p.F) = z4;
+      }
+    }
+    named_bar(BAR_CONS, kConsumers);
+    if (t == 0) red_release_add(ready_cnt(p, gi + 1, ch, kd), unsigned(rows));
+    return true;
+  }
+  // G_HEAD: final logits of 128 codebook entries for the chunk's frames
+  {
+    const int rows = rows_in(p.B, c, ch);
+    const int col = mt * kTileM + lane * 4;
+    const bool greedy = p.temperature <= 0.f;
+    for (int r0 = warp; r0 < rows; r0 += 4 * kConsumerWarps) {
+      float4 lv[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = r0 + u * kConsumerWarps;
+        lv[u] = row < rows ? __ldcg(reinterpret_cast<const float4*>(p.logits + size_t(ch * c.Nc + row) * p.V + col)) : z4;
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int row = r0 + u * kConsumerWarps, b = ch * c.Nc + row;
+        if (row >= rows) continue;
+        const float4 lg = lv[u];
+        if (p.out_logits)
+          *reinterpret_cast<float4*>(p.out_logits + (size_t(b) * p.n_steps + (G.k - 1)) * p.V + col) = lg;
+        if (greedy) {
+          unsigned long long best = pack_argmax(lg.x, col);
+          const unsigned long long c1 = pack_argmax(lg.y, col + 1), c2 = pack_argmax(lg.z, col + 2),
+                                   c3 = pack_argmax(lg.w, col + 3);
+          best = c1 > best ? c1 : best;
+          best = c2 > best ? c2 : best;
+          best = c3 > best ? c3 : best;
+          best = warp_max_u64(best);
+          if (lane == 0) atomicMax(p.codepk + size_t(G.k - 1) * p.B + b, best);
+          *reinterpret_cast<float4*>(p.logits + size_t(b) * p.V + col) = z4;
+        }
+      }
+    }
+    named_bar(BAR_CONS, kConsumers);
+    if (t == 0) red_release_add(head_done(p, G.k, ch), 1u);
+    return true;
+  }
+}
+
+// Drain this CTA's accumulator segments of GEMM gi.
+__device__ bool epilogues(const PParams& p, Misc& ms, int gi, uint32_t& seg) {
+  const GI G = gemm_inst(p, gi);
+  const Ck c = chunking(G.R);
+  int beg, end;
+  my_run(c.n * G.n_mt * G.n_ks, gi, beg, end);
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const bool scaled = G.kind == G_QKV || G.kind == G_GU || G.kind == G_HEAD;
+  int s = beg;
+  while (s < end) {
+    const int ks = s % G.n_ks, tt = s / G.n_ks, mt = tt % G.n_mt, ch = tt / G.n_mt;
+    const int seg_end = min(end, s + (G.n_ks - ks)), nsl = seg_end - s;
+    const uint32_t tb = seg & 1;
+    const int rows = rows_in(G.R, c, ch);
+    // consumer-wide waits are taken by thread 0 and broadcast, so that every
+    // consumer thread leaves (or stays) together.  The norm statistics of a
+    // scaled GEMM are gathered first, while the MMAs may still run.
+    if (scaled) {
+      if (t == 0) ms.flag[1] = poll_geq(p, ss_cnt(p, gi, ch), unsigned(rows * (p.d / kTileM)));
+      named_bar(BAR_CONS, kConsumers);
+      if (!ms.flag[1]) return false;
+      for (int col = t; col < c.Nc; col += kConsumers) {
+        const int n = ch * c.Nc + col;
+        ms.inv[col] = n < G.R ? rsqrtf(__ldcg(ss_at(p, gi, n)) / float(p.d) + p.eps) : 0.f;
+      }
+    }
+    if (t == 0) ms.flag[1] = mwait(p, &ms.accfull[tb], (seg >> 1) & 1);
+    named_bar(BAR_CONS, kConsumers);
+    if (!ms.flag[1]) return false;
+    if (t == 0) ev_cons(p, &ms.evc, EV_ACC, gi);
+    tc_fence_after();
+    const int quarter = warp & 3, half = warp >> 2, cols = c.Nc / 2;
+    const int m = mt * kTileM + quarter * 32 + lane;
+    for (int col = half * cols; col < (half + 1) * cols; col += 8) {
+      float v[8];
+      tmem_ld8(ms.tmem_base + tb * 128 + (uint32_t(quarter * 32) << 16) + uint32_t(col), v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int n = ch * c.Nc + col + i;
+        if (n < G.R) red_add_f32(G.acc + size_t(n) * G.ld + m, scaled ? v[i] * ms.inv[col + i] : v[i]);
+      }
+    }
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&ms.accempty[tb]);
+    named_bar(BAR_CONS, kConsumers);
+    if (t == 0) {
+      ev_cons(p, &ms.evc, EV_REDS, gi);
+      const unsigned old = atom_add_acq_rel(tile_cnt(p, gi, ch, mt), unsigned(nsl));
+      ms.flag[0] = old + unsigned(nsl) == unsigned(G.n_ks);
+      ev_cons(p, &ms.evc, EV_COUNTED, gi);
+    }
+    named_bar(BAR_CONS, kConsumers);
+    if (ms.flag[0]) {
+      if (!last_arriver(p, ms, G, gi, ch, mt, c)) return false;
+      if (t == 0) ev_cons(p, &ms.evc, EV_LASTDONE, gi);
+    }
+    ++seg;
+    s = seg_end;
+  }
+  return true;
+}
+
+// Gumbel top-k decisions of step k, one frame per CTA pass (all consumers).
+__device__ bool decide_items(const PParams& p, Misc& ms, uint32_t* keys, int k) {
+  const int V = p.V, t = threadIdx.x, lane = t & 31, w = t >> 5, G = gridDim.x;
+  const Ck c = chunking(p.B);
+  const float T = p.temperature;
+  for (int b = (blockIdx.x + k * 7) % G; b < p.B; b += G) {
+    if (t == 0) ms.flag[3] = poll_geq(p, head_done(p, k, b / c.Nc), unsigned(V / kTileM));
+    named_bar(BAR_CONS, kConsumers);
+    if (!ms.flag[3]) return false;
+    float* l = p.logits + size_t(b) * V;
+    for (int i = t; i < V; i += kConsumers) keys[i] = f32_order_key(__ldcg(l + i) / T);
+    uint32_t prefix = 0, mask = 0;
+    int remaining = p.top_k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      ms.hist[t] = 0;
+      named_bar(BAR_CONS, kConsumers);
+      for (int i = t; i < V; i += kConsumers) {
+        const uint32_t kk = keys[i];
+        if ((kk & mask) == prefix) atomicAdd(&ms.hist[(kk >> shift) & 255], 1);
+      }
+      named_bar(BAR_CONS, kConsumers);
+      if (t == 0) {
+        int cum = 0, sel = 0;
+        for (int dg = 255; dg >= 0; --dg) {
+          if (cum + ms.hist[dg] >= remaining) { sel = dg; break; }
+          cum += ms.hist[dg];
+        }
+        ms.sel[0] = sel;
+        ms.sel[1] = remaining - cum;
+      }
+      named_bar(BAR_CONS, kConsumers);
+      prefix |= uint32_t(ms.sel[0]) << shift;
+      mask |= 255u << shift;
+      remaining = ms.sel[1];
+      named_bar(BAR_CONS, kConsumers);
+    }
+    const uint32_t kth = prefix;
+    const int per = (V + kConsumers - 1) / kConsumers, lo = t * per, hi = min(V, lo + per);
+    int cnt = 0;
+    for (int i = lo; i < hi; ++i) cnt += keys[i] == kth;
+    ms.chunk_cnt[t] = cnt;
+    named_bar(BAR_CONS, kConsumers);
+    if (t == 0) {
+      int run = 0;
+      for (int i = 0; i < kConsumers; ++i) { const int cc = ms.chunk_cnt[i]; ms.chunk_cnt[i] = run; run += cc; }
+    }
+    named_bar(BAR_CONS, kConsumers);
+    int eq_rank = ms.chunk_cnt[t];
+    const float* gb = p.gumbel + (size_t(b) * p.n_steps + (k - 1)) * V;
+    unsigned long long best = 0ull;
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t kk = keys[i];
+      bool in = kk > kth;
+      if (kk == kth) { in = eq_rank < remaining; ++eq_rank; }
+      if (in) {
+        const unsigned long long pk = pack_argmax(__ldcg(l + i) / T + gb[i], i);
+        best = pk > best ? pk : best;
+      }
+    }
+    best = warp_max_u64(best);
+    if (lane == 0) ms.redu[w] = best;
+    named_bar(BAR_CONS, kConsumers);
+    for (int i = t; i < V; i += kConsumers) l[i] = 0.f;   // the buffer is reused next step
+    named_bar(BAR_CONS, kConsumers);
+    if (t == 0) {
+      unsigned long long v = ms.redu[0];
+      for (int i = 1; i < kConsumerWarps; ++i) v = ms.redu[i] > v ? ms.redu[i] : v;
+      __threadfence();
+      atomicExch(p.decided + size_t(k - 1) * p.B + b, unsigned(unpack_argmax_index(v) + 1));
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void trace_mark(const PParams& p, int sec, int which) {
+  if (p.trace && threadIdx.x == 0 && sec < p.trace_n)
+    p.trace[(size_t(sec) * gridDim.x + blockIdx.x) * 2 + which] = globaltimer_ns();
+}
+
+__device__ void consumer_role(const PParams& p, Misc& ms, uint8_t* smem) {
+  uint32_t seg = 0;
+  int sec = 0;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kOffKeys);
+  // A section ends with one consumer-wide barrier; a failed wait in any warp
+  // makes every consumer warp leave there together.
+#define QP_SECTION(expr)                      \
+  {                                           \
+    trace_mark(p, sec, 0);                    \
+    const bool ok_ = (expr);                  \
+    if (!ok_) ms.fail = 1;                    \
+    named_bar(BAR_CONS, kConsumers);          \
+    trace_mark(p, sec, 1);                    \
+    ++sec;                                    \
+    if (ms.fail) return;                      \
+  }
+  QP_SECTION(prep1_items(p));
+  QP_SECTION(epilogues(p, ms, 0, seg));
+  for (int k = 1; k <= p.n_steps; ++k) {
+    if (k > 1) QP_SECTION(prepk_items(p, k));
+    for (int l = 0; l < p.L; ++l) {
+      QP_SECTION(epilogues(p, ms, gi_of(p, k, l, 0), seg));
+      QP_SECTION(attn_items(p, ms, k, l));
+      QP_SECTION(epilogues(p, ms, gi_of(p, k, l, 1), seg));
+      QP_SECTION(epilogues(p, ms, gi_of(p, k, l, 2), seg));
+      QP_SECTION(epilogues(p, ms, gi_of(p, k, l, 3), seg));
+    }
+    QP_SECTION(epilogues(p, ms, gi_head(p, k), seg));
+    if (p.temperature > 0.f) QP_SECTION(decide_items(p, ms, keys, k));
+  }
+  QP_SECTION(final_items(p));
+#undef QP_SECTION
 }
 
 __global__ void __launch_bounds__(kThreads, 1) k_frames(const PParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
   const int t = threadIdx.x, warp = t >> 5;
   if (t == 0) {
-    for (int i = 0; i < kNSlot; ++i) { mbar_init(&sm.full[i], 1); mbar_init(&sm.empty[i], 1); }
-    mbar_init(&sm.actbar, 1);
-    mbar_init(&sm.mmabar, 1);
+    for (int i = 0; i < kNSlotF16; ++i) { mbar_init(&ms.wfull[i], 1); mbar_init(&ms.wempty[i], 1); }
+    for (int i = 0; i < kNDeq; ++i) { mbar_init(&ms.dfull[i], 1); mbar_init(&ms.dempty[i], 1); }
+    for (int i = 0; i < kNAct; ++i) { mbar_init(&ms.afull[i], 1); mbar_init(&ms.aempty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&ms.accfull[i], 2); mbar_init(&ms.accempty[i], kConsumerWarps); }
+    mbar_init(&ms.mmadone, 1);
+    ms.fail = 0;
+    ms.deq_ok = 1;
+    ms.evc = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) tmem_alloc(&sm.tmem_base, kTmemCols);
+  if (warp == 0) tmem_alloc(&ms.tmem_base, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
 
-  if (warp == kConsumers / 32) {
-    if ((t & 31) == 0) producer(p, sm);
-    return;
+  if (warp < kConsumerWarps) {
+    consumer_role(p, ms, smem);
+  } else if (warp == kProducerWarp) {
+    if ((t & 31) == 0) producer_role(p, ms, smem);
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    if ((t & 31) == 0) mma_role(p, ms, smem);
+    __syncwarp();
+  } else if (p.q8) {
+    dequant_role(p, ms, smem);
   }
-
-  const Prog prog(p);
-  uint32_t slot_it = 0, act_it = 0, mma_it = 0, phase = 0;
-  int gemm_idx = 0;
-  const unsigned G = gridDim.x;
-  bool alive = true;
-  auto barrier = [&]() {
-    ++phase;
-    alive = grid_barrier(p, phase * G);
-    return alive;
-  };
-  auto gemm = [&]() {
-    phase_gemm(p, sm, prog.gemm(gemm_idx), gemm_idx, slot_it, act_it, mma_it);
-    ++gemm_idx;
-    return barrier();
-  };
-  const int B = p.B, qkvw = p.qw + 2 * p.kvw;
-
-  do {
-    phase_prep(p);
-    if (!barrier()) break;
-    if (!gemm()) break;   // projection into xres
-    for (int step = 1; step <= p.n_steps && alive; ++step) {
-      const int P = step == 1 ? 2 : 1, R = B * P, pos0 = step == 1 ? 0 : step;
-      for (int l = 0; l < p.L && alive; ++l) {
-        const PLayer& L = p.layer[l];
-        phase_norm(p, sm, R, 1, 0, L.attn_norm, p.acc_qkv, qkvw);
-        if (!barrier()) break;
-        if (!gemm()) break;                 // QKV
-        phase_attn(p, sm, l, P, pos0);
-        if (!barrier()) break;
-        if (!gemm()) break;                 // O-proj into xres
-        phase_norm(p, sm, R, 1, 0, L.ffn_norm, p.acc_gu, 2 * p.F);
-        if (!barrier()) break;
-        if (!gemm()) break;                 // gate/up
-        phase_swiglu(p, R);
-        if (!barrier()) break;
-        if (!gemm()) break;                 // down into xres
-      }
-      if (!alive) break;
-      phase_norm(p, sm, B, P, P - 1, p.out_norm, p.logits, p.V);
-      if (!barrier()) break;
-      if (!gemm()) break;                   // lm_head
-      phase_decide(p, sm, step);
-      if (!barrier()) break;
-    }
-  } while (false);
-
-  // all tcgen05 work of this CTA is complete (every MMA was waited on)
   tc_fence_before();
-  named_bar(BAR_ALL, kConsumers);
+  __syncthreads();
   tc_fence_after();
-  if (warp == 0) tmem_dealloc(sm.tmem_base, kTmemCols);
+  if (warp == 0) tmem_dealloc(ms.tmem_base, kTmemCols);
 }
 
-// ---------------------------------------------------------------------------
-// weight packing (load time)
-// ---------------------------------------------------------------------------
+// ----------------------------------------------------------------- host
+size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
-// bf16 row-major [N, K] -> f16 packed tiles [N/128][K/8][16][8][8].
-__global__ void k_pack_f16(const uint16_t* __restrict__ src, int N, int K, uint16_t* __restrict__ dst) {
-  const size_t total = size_t(N) * (K / 8);
-  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
-    const int n = int(i / (K / 8)), k8 = int(i % (K / 8));
-    const int mt = n / kTileM, r = n % kTileM;
-    const uint4 v = *reinterpret_cast<const uint4*>(src + size_t(n) * K + k8 * 8);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float lo = bf16_bits_to_f32(w[j] & 0xffff), hi = bf16_bits_to_f32(w[j] >> 16);
-      o[j] = uint32_t(f32_to_f16_bits(lo)) | (uint32_t(f32_to_f16_bits(hi)) << 16);
-    }
-    const size_t off = size_t(mt) * K * kTileM + size_t(k8) * (kTileM * 8) + (r >> 3) * 64 + (r & 7) * 8;
-    *reinterpret_cast<uint4*>(dst + off) = make_uint4(o[0], o[1], o[2], o[3]);
-  }
+struct SyncLayout {
+  size_t tile_cnt, ready, ss_cnt, ss, pair, head_done, codepk, decided, abort_flag, total;
+  int NCH, MT, KS, NGEMM;
+};
+
+SyncLayout sync_layout(const qp_geometry& g, int B) {
+  SyncLayout S{};
+  const size_t R1 = size_t(2) * B;
+  S.NCH = int(R1 <= size_t(kMaxNc) ? 1 : (R1 + kMaxNc - 1) / kMaxNc);
+  const int qkvw = (g.n_q_heads + 2 * g.n_kv_heads) * 128;
+  int mt = g.hidden;
+  if (qkvw > mt) mt = qkvw;
+  if (2 * g.ffn > mt) mt = 2 * g.ffn;
+  if (g.vocab > mt) mt = g.vocab;
+  S.MT = mt / kTileM;
+  int ks = g.hidden;
+  if (g.talker_hidden > ks) ks = g.talker_hidden;
+  if (g.n_q_heads * 128 > ks) ks = g.n_q_heads * 128;
+  if (g.ffn > ks) ks = g.ffn;
+  S.KS = ks / kKs;
+  S.NGEMM = 1 + g.n_steps * (4 * g.layers + 1);
+  size_t o = 0;
+  S.tile_cnt = o; o += al256(size_t(S.NGEMM) * S.NCH * S.MT * 4);
+  S.ready = o;    o += al256(size_t(S.NGEMM) * S.NCH * S.KS * 4);
+  S.ss_cnt = o;   o += al256(size_t(S.NGEMM) * S.NCH * 4);
+  S.ss = o;       o += al256(size_t(S.NGEMM) * R1 * 4);
+  S.pair = o;     o += al256(size_t(g.n_steps) * g.layers * S.NCH * (g.ffn / kTileM) * 4);
+  S.head_done = o; o += al256(size_t(g.n_steps) * S.NCH * 4);
+  S.codepk = o;   o += al256(size_t(g.n_steps) * B * 8);
+  S.decided = o;  o += al256(size_t(g.n_steps) * B * 4);
+  S.abort_flag = o; o += 256;
+  S.total = o;
+  return S;
 }
 
-// Q8_0 (int8 [N, K] + f16 scales [N, K/32]) -> packed int8 tiles in the same
-// element order, and scales [N/128][K/128][4][128].
-__global__ void k_pack_q8(const int8_t* __restrict__ qs, const __half* __restrict__ d, int N, int K,
-                          int8_t* __restrict__ dq, __half* __restrict__ ds) {
-  const size_t total = size_t(N) * (K / 8);
-  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
-    const int n = int(i / (K / 8)), k8 = int(i % (K / 8));
-    const int mt = n / kTileM, r = n % kTileM;
-    const uint2 v = *reinterpret_cast<const uint2*>(qs + size_t(n) * K + k8 * 8);
-    const size_t off = size_t(mt) * K * kTileM + size_t(k8) * (kTileM * 8) + (r >> 3) * 64 + (r & 7) * 8;
-    *reinterpret_cast<uint2*>(dq + off) = v;
-    if ((k8 & 3) == 0) {
-      const int k = k8 * 8, ks = k / kKs, kb = (k % kKs) / 32;
-      ds[(size_t(mt) * (K / kKs) + ks) * (kKs / 32) * kTileM + kb * kTileM + r] = d[size_t(n) * (K / 32) + k / 32];
-    }
-  }
-}
-
-}  // namespace
-
-size_t packed_bytes(int fmt, int N, int K) {
-  if (fmt == WF_BF16) return size_t(N) * K * 2;
-  return size_t(N) * K + size_t(N) * (K / 32) * 2;
-}
-
-cudaError_t pack_matrix(const QMat& src, PackedMat& dst, cudaStream_t s) {
-  const size_t total = size_t(src.N) * (src.K / 8);
-  const int grid = int(total / 256 + 1 < 8192 ? total / 256 + 1 : 8192);
-  if (src.fmt == WF_BF16) {
-    k_pack_f16<<<grid, 256, 0, s>>>(static_cast<const uint16_t*>(src.w), src.N, src.K,
-                                    reinterpret_cast<uint16_t*>(dst.w));
-  } else {
-    k_pack_q8<<<grid, 256, 0, s>>>(static_cast<const int8_t*>(src.w), src.scale, src.N, src.K,
-                                   reinterpret_cast<int8_t*>(dst.w), dst.scale);
-  }
-  return cudaGetLastError();
-}
-
-size_t persistent_smem_bytes() { return sizeof(Smem) + 1024; }
-
-qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s) {
+void fill_params(PParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L,
+                 uint8_t* sync, const SyncLayout& S, int bmax) {
   const qp_geometry& g = h->g;
-  if (a.temperature > 0.f && g.vocab > 8192) return QP_ERR_ARG;
-  PParams p{};
   p.d = g.hidden; p.qw = g.n_q_heads * 128; p.kvw = g.n_kv_heads * 128; p.F = g.ffn; p.V = g.vocab;
   p.th = g.talker_hidden; p.L = g.layers; p.n_q = g.n_q_heads; p.n_kv = g.n_kv_heads; p.n_steps = g.n_steps;
   p.q0_vocab = g.q0_vocab; p.eps = g.rms_eps; p.q8 = h->wfmt == WF_Q8_0;
-  p.w_proj = h->pproj.w; p.s_proj = h->pproj.scale; p.b_proj = h->b_proj; p.e0 = h->e0;
+  p.w_proj = h->proj.w; p.s_proj = h->proj.scale; p.b_proj = h->b_proj; p.e0 = h->e0;
   for (int l = 0; l < g.layers; ++l) {
-    const LayerW& L = h->layer[l];
-    const PackedLayer& PL = h->player[l];
-    p.layer[l] = {PL.qkv.w, PL.qkv.scale, PL.o.w, PL.o.scale, PL.gu.w, PL.gu.scale, PL.down.w, PL.down.scale,
-                  L.attn_norm, L.q_norm, L.k_norm, L.ffn_norm};
+    const LayerW& Lw = h->layer[l];
+    const PackedMat* m[4] = {&Lw.qkv, &Lw.o, &Lw.gu, &Lw.down};
+    for (int i = 0; i < 4; ++i) { p.layer[l].w[i] = m[i]->w; p.layer[l].s[i] = m[i]->scale; }
+    p.layer[l].attn_norm = Lw.attn_norm; p.layer[l].q_norm = Lw.q_norm;
+    p.layer[l].k_norm = Lw.k_norm; p.layer[l].ffn_norm = Lw.ffn_norm;
   }
   p.out_norm = h->out_norm;
   for (int j = 0; j < g.n_steps; ++j) {
-    p.embed[j] = h->embed[j];
-    p.w_head[j] = h->phead[j].w;
-    p.s_head[j] = h->phead[j].scale;
+    p.embed[j] = h->embed[j]; p.embed_ss[j] = h->embed_ss[j];
+    p.w_head[j] = h->head[j].w; p.s_head[j] = h->head[j].scale;
   }
   p.rope_cs = h->rope_cs;
-  p.xres = h->X; p.act = h->pact; p.acc_qkv = h->qkv; p.acc_gu = h->gu; p.logits = h->logits; p.kv = h->kv;
-  p.bar = h->sync_words; p.abort_flag = reinterpret_cast<int*>(h->sync_words + 1); p.status = h->status;
-  p.Bmax = h->max_batch;
+  p.x1 = reinterpret_cast<float*>(scratch + L.x1);
+  p.xk = reinterpret_cast<float*>(scratch + L.xk);
+  for (int i = 0; i < 5; ++i) p.a1[i] = reinterpret_cast<uint16_t*>(scratch + L.a1[i]);
+  for (int i = 0; i < 4; ++i) p.ak[i] = reinterpret_cast<uint16_t*>(scratch + L.ak[i]);
+  p.ahead = reinterpret_cast<uint16_t*>(scratch + L.ahead);
+  p.acc1_qkv = reinterpret_cast<float*>(scratch + L.acc1_qkv);
+  p.acck_qkv = reinterpret_cast<float*>(scratch + L.acck_qkv);
+  p.acc1_gu = reinterpret_cast<float*>(scratch + L.acc1_gu);
+  p.acck_gu = reinterpret_cast<float*>(scratch + L.acck_gu);
+  p.logits = reinterpret_cast<float*>(scratch + L.logits);
+  p.kv = reinterpret_cast<float*>(scratch + L.kv);
+  p.Bmax = bmax;
+  p.tile_cnt = reinterpret_cast<unsigned*>(sync + S.tile_cnt);
+  p.ready = reinterpret_cast<unsigned*>(sync + S.ready);
+  p.ss_cnt = reinterpret_cast<unsigned*>(sync + S.ss_cnt);
+  p.ss = reinterpret_cast<float*>(sync + S.ss);
+  p.pair = reinterpret_cast<unsigned*>(sync + S.pair);
+  p.head_done = reinterpret_cast<unsigned*>(sync + S.head_done);
+  p.codepk = reinterpret_cast<unsigned long long*>(sync + S.codepk);
+  p.decided = reinterpret_cast<unsigned*>(sync + S.decided);
+  p.abort_flag = reinterpret_cast<int*>(sync + S.abort_flag);
+  p.status = h->status;
+  p.NCH = S.NCH; p.MT = S.MT; p.KS = S.KS; p.NGEMM = S.NGEMM;
+  p.trace = h->trace; p.trace_n = h->trace_phases;
   p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;
   p.temperature = a.temperature; p.top_k = a.top_k; p.gumbel = a.gumbel;
+}
 
-  static bool attr_done[64] = {};
-  const size_t smem = persistent_smem_bytes();
-  if (h->device < 64 && !attr_done[h->device]) {
-    if (cudaFuncSetAttribute(k_frames, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
+// Zero what must start at zero, then launch.
+qp_status launch(qp_handle* h, PParams& p, uint8_t* scratch, const Scratch& L, uint8_t* sync, const SyncLayout& S,
+                 cudaStream_t s, bool* attr_done) {
+  const qp_geometry& g = h->g;
+  if (!*attr_done) {
+    if (cudaFuncSetAttribute(k_frames, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(persistent_smem_bytes())) != cudaSuccess) {
+      cudaGetLastError();
       return QP_ERR_CUDA;
-    attr_done[h->device] = true;
+    }
+    *attr_done = true;
   }
-  if (cudaMemsetAsync(h->sync_words, 0, 2 * sizeof(unsigned int), s) != cudaSuccess) return QP_ERR_CUDA;
+  const size_t B = size_t(p.B), qkvw = size_t(g.n_q_heads + 2 * g.n_kv_heads) * 128, F2 = size_t(2) * g.ffn;
+  cudaError_t e = cudaMemsetAsync(sync, 0, S.total, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch + L.acc1_qkv, 0, 2 * B * qkvw * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch + L.acck_qkv, 0, B * qkvw * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch + L.acc1_gu, 0, 2 * B * F2 * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch + L.acck_gu, 0, B * F2 * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(scratch + L.logits, 0, B * size_t(g.vocab) * 4, s);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return QP_ERR_CUDA;
+  }
   void* args[] = {&p};
-  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_frames), dim3(h->num_sms), dim3(kThreads), args, smem,
-                                  s) != cudaSuccess) {
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_frames), dim3(h->num_sms), dim3(kThreads), args,
+                                  persistent_smem_bytes(), s) != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;
   }
   return QP_OK;
 }
 
+bool g_attr_done[64] = {};
+
+}  // namespace
+
+size_t persistent_smem_bytes() { return kOffMisc + sizeof(Misc) + 1024; }
+
+Scratch scratch_layout(const qp_geometry& g, int bmax) {
+  Scratch L{};
+  const size_t R1 = size_t(2) * bmax, RK = size_t(bmax), o1 = operand_rows(R1), ok = operand_rows(RK);
+  const size_t d = g.hidden, qw = size_t(g.n_q_heads) * 128, kvw = size_t(g.n_kv_heads) * 128, F = g.ffn;
+  const size_t qkvw = qw + 2 * kvw, th = g.talker_hidden, V = g.vocab;
+  size_t o = 0;
+  L.x1 = o; o += al256(R1 * d * 4);
+  L.xk = o; o += al256(RK * d * 4);
+  const size_t k1[5] = {th, d, qw, d, F};
+  for (int i = 0; i < 5; ++i) { L.a1[i] = o; o += al256(o1 * k1[i] * 2); }
+  const size_t kk[4] = {d, qw, d, F};
+  for (int i = 0; i < 4; ++i) { L.ak[i] = o; o += al256(ok * kk[i] * 2); }
+  L.ahead = o; o += al256(ok * d * 2);
+  L.acc1_qkv = o; o += al256(R1 * qkvw * 4);
+  L.acck_qkv = o; o += al256(RK * qkvw * 4);
+  L.acc1_gu = o;  o += al256(R1 * 2 * F * 4);
+  L.acck_gu = o;  o += al256(RK * 2 * F * 4);
+  L.logits = o;   o += al256(RK * V * 4);
+  L.kv = o;       o += al256(size_t(g.layers) * RK * (g.n_steps + 1) * 2 * kvw * 4);
+  L.sync = o;
+  L.total = o + sync_layout(g, bmax).total;
+  return L;
+}
+
+size_t sync_bytes(const qp_geometry& g, int B) { return sync_layout(g, B).total; }
+
+qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s) {
+  if (a.temperature > 0.f && h->g.vocab > kMaxVocab) return QP_ERR_ARG;
+  uint8_t* scratch = static_cast<uint8_t*>(h->sarena);
+  const SyncLayout S = sync_layout(h->g, a.B);
+  PParams p{};
+  fill_params(p, h, a, scratch, h->scr, scratch + h->scr.sync, S, h->max_batch);
+  bool* done = h->device >= 0 && h->device < 64 ? &g_attr_done[h->device] : nullptr;
+  bool local = false;
+  return launch(h, p, scratch, h->scr, scratch + h->scr.sync, S, s, done ? done : &local);
+}
 
 // ---------------------------------------------------------------------------
 // Allocation-free entry point.
@@ -814,8 +1207,8 @@ qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s) 
 // library call cudaMalloc on their behalf: a process whose framework
 // allocator has already reserved the GPU's memory, or a real-time audio path
 // that forbids allocation once it is running.  qp_predict_frames_static
-// runs the same persistent kernel as qp_predict_frames, but its scratch (the
-// residual stream, MMA operand, accumulators, logits, KV cache and barrier
+// runs the same kernel as qp_predict_frames, but its scratch (residual
+// streams, operands, accumulators, logits, KV cache and synchronisation
 // words) lives in the file-scope array below, which the CUDA runtime places
 // in device memory when the library's module loads on a device, and which
 // every device that loads the library holds until the process exits.  The
@@ -828,46 +1221,16 @@ constexpr int kStaticMaxFrames = 8;
 static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
 namespace {
-
 constexpr int kMaxDevices = 64;
 void* g_static_ptr[kMaxDevices] = {};
 bool g_static_attr[kMaxDevices] = {};
-
-size_t align256(size_t b) { return (b + 255) & ~size_t(255); }
-
-// Byte layout of the scratch for B frames; returns the total.
-struct StaticLayout {
-  size_t xres, act, qkv, gu, logits, kv, sync, total;
-};
-StaticLayout static_layout(const qp_geometry& g, int B) {
-  const size_t R = size_t(2) * B;
-  const size_t qw = size_t(g.n_q_heads) * 128, kvw = size_t(g.n_kv_heads) * 128;
-  size_t aw = g.hidden;
-  if (qw > aw) aw = qw;
-  if (size_t(g.ffn) > aw) aw = g.ffn;
-  if (size_t(g.talker_hidden) > aw) aw = g.talker_hidden;
-  const size_t r16 = (R + 15) / 16 * 16;
-  const size_t act_rows = r16 <= size_t(kMaxNc) ? r16 : (R + kMaxNc - 1) / kMaxNc * kMaxNc;
-  StaticLayout L{};
-  size_t off = 0;
-  L.xres = off;   off += align256(R * g.hidden * 4);
-  L.act = off;    off += align256(act_rows * aw * 2);
-  L.qkv = off;    off += align256(R * (qw + 2 * kvw) * 4);
-  L.gu = off;     off += align256(R * 2 * size_t(g.ffn) * 4);
-  L.logits = off; off += align256(size_t(B) * g.vocab * 4);
-  L.kv = off;     off += align256(size_t(g.layers) * B * (g.n_steps + 1) * 2 * kvw * 4);
-  L.sync = off;   off += 256;
-  L.total = off;
-  return L;
-}
-
 }  // namespace
 
 qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   const qp_geometry& g = h->g;
   if (a.B < 1 || a.B > kStaticMaxFrames) return QP_ERR_ARG;
-  const StaticLayout SL = static_layout(g, a.B);
-  if (SL.total > kStaticScratchBytes) return QP_ERR_ARG;
+  const Scratch L = scratch_layout(g, a.B);
+  if (L.total > kStaticScratchBytes) return QP_ERR_ARG;
   if (h->device < 0 || h->device >= kMaxDevices) return QP_ERR_ARG;
   // once per device, with that device current: the array's device address
   if (!g_static_ptr[h->device]) {
@@ -878,58 +1241,16 @@ qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s) {
     }
     g_static_ptr[h->device] = ptr;
   }
-  if (!g_static_attr[h->device]) {
-    if (cudaFuncSetAttribute(k_frames, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(persistent_smem_bytes())) != cudaSuccess) {
-      cudaGetLastError();
-      return QP_ERR_CUDA;
-    }
-    g_static_attr[h->device] = true;
-  }
-  unsigned char* base = static_cast<unsigned char*>(g_static_ptr[h->device]);
+  uint8_t* base = static_cast<uint8_t*>(g_static_ptr[h->device]);
+  const SyncLayout S = sync_layout(g, a.B);
+  RunArgs ga = a;
+  ga.forced = nullptr;
+  ga.temperature = 0.f; ga.top_k = 0; ga.gumbel = nullptr;
   PParams p{};
-  p.d = g.hidden; p.qw = g.n_q_heads * 128; p.kvw = g.n_kv_heads * 128; p.F = g.ffn; p.V = g.vocab;
-  p.th = g.talker_hidden; p.L = g.layers; p.n_q = g.n_q_heads; p.n_kv = g.n_kv_heads; p.n_steps = g.n_steps;
-  p.q0_vocab = g.q0_vocab; p.eps = g.rms_eps; p.q8 = h->wfmt == WF_Q8_0;
-  p.w_proj = h->pproj.w; p.s_proj = h->pproj.scale; p.b_proj = h->b_proj; p.e0 = h->e0;
-  for (int l = 0; l < g.layers; ++l) {
-    const LayerW& L = h->layer[l];
-    const PackedLayer& PL = h->player[l];
-    p.layer[l] = {PL.qkv.w, PL.qkv.scale, PL.o.w, PL.o.scale, PL.gu.w, PL.gu.scale, PL.down.w, PL.down.scale,
-                  L.attn_norm, L.q_norm, L.k_norm, L.ffn_norm};
-  }
-  p.out_norm = h->out_norm;
-  for (int j = 0; j < g.n_steps; ++j) {
-    p.embed[j] = h->embed[j];
-    p.w_head[j] = h->phead[j].w;
-    p.s_head[j] = h->phead[j].scale;
-  }
-  p.rope_cs = h->rope_cs;
-  p.xres = reinterpret_cast<float*>(base + SL.xres);
-  p.act = reinterpret_cast<uint16_t*>(base + SL.act);
-  p.acc_qkv = reinterpret_cast<float*>(base + SL.qkv);
-  p.acc_gu = reinterpret_cast<float*>(base + SL.gu);
-  p.logits = reinterpret_cast<float*>(base + SL.logits);
-  p.kv = reinterpret_cast<float*>(base + SL.kv);
-  p.bar = reinterpret_cast<unsigned int*>(base + SL.sync);
-  p.abort_flag = reinterpret_cast<int*>(base + SL.sync + 4);
-  p.status = h->status;
-  p.Bmax = a.B;
-  p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = nullptr;
-  p.temperature = 0.f; p.top_k = 0; p.gumbel = nullptr;
-  // the barrier counter and abort flag must start at zero; every other
-  // buffer is written before it is read within the call
-  if (cudaMemsetAsync(base + SL.sync, 0, 8, s) != cudaSuccess) {
-    cudaGetLastError();
-    return QP_ERR_CUDA;
-  }
-  void* args[] = {&p};
-  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_frames), dim3(h->num_sms), dim3(kThreads), args,
-                                  persistent_smem_bytes(), s) != cudaSuccess) {
-    cudaGetLastError();
-    return QP_ERR_CUDA;
-  }
-  return QP_OK;
+  fill_params(p, h, ga, base, L, base + L.sync, S, a.B);
+  // the launch zeroes the synchronisation words and accumulators; every
+  // other byte is written before it is read within the call
+  return launch(h, p, base, L, base + L.sync, S, s, &g_static_attr[h->device]);
 }
 
 }  // namespace qp

@@ -154,4 +154,10 @@ __device__ __forceinline__ uint32_t ld_acquire_u32(const unsigned int* p) {
 }
 __device__ __forceinline__ float ld_cg_f32(const float* p) { return __ldcg(p); }
 
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 }  // namespace qp

@@ -1,0 +1,105 @@
+// Load-time weight preparation: pack caller matrices into the tensor-core
+// slice layout, and precompute the squared norm of every embedding row.
+//
+// Packed layout of a matrix [N, K] (N, K multiples of 128): 128-row tiles;
+// inside a tile the element (row r, column k) sits at
+//   (k / 8) * 1024 + (r / 8) * 64 + (r % 8) * 8 + (k % 8)
+// i.e. K-major core matrices of 8 rows x 8 values (16 bytes as f16), the
+// image a no-swizzle tcgen05 shared-memory descriptor reads with a leading
+// (K) byte offset of 16 * 128 and a stride (M) byte offset of 128.  One
+// 128-row x 128-column slice is therefore a contiguous run.  Q8_0 keeps the
+// same element order with one byte per value; its f16 scales are stored
+// [tile][K/128][4 blocks of 32][128 rows].
+#include "qp_common.cuh"
+#include "qp_internal.h"
+
+namespace qp {
+
+namespace {
+
+__device__ __forceinline__ size_t packed_off(int n, int k, int K) {
+  const int mt = n / kTileM, r = n % kTileM;
+  return size_t(mt) * K * kTileM + size_t(k >> 3) * (kTileM * 8) + (r >> 3) * 64 + (r & 7) * 8 + (k & 7);
+}
+
+// bf16 rows -> f16 packed (exact for values in f16's normal range).
+__global__ void k_pack_bf16(const uint16_t* __restrict__ src, int rows, int K, uint16_t* __restrict__ dst,
+                            int row0) {
+  const size_t total = size_t(rows) * (K / 8);
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
+    const int r = int(i / (K / 8)), k8 = int(i % (K / 8));
+    const uint4 v = *reinterpret_cast<const uint4*>(src + size_t(r) * K + k8 * 8);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      o[j] = uint32_t(f32_to_f16_bits(bf16_bits_to_f32(w[j] & 0xffff))) |
+             (uint32_t(f32_to_f16_bits(bf16_bits_to_f32(w[j] >> 16))) << 16);
+    *reinterpret_cast<uint4*>(dst + packed_off(row0 + r, k8 * 8, K)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// Q8_0 block stream rows ({f16 d; int8 q[32]} per 32 values) -> packed int8
+// values plus packed scales.  One thread per block.
+__global__ void k_pack_q8(const uint8_t* __restrict__ src, int rows, int K, int8_t* __restrict__ dq,
+                          __half* __restrict__ ds, int row0) {
+  const int nb = K / 32;
+  const size_t total = size_t(rows) * nb;
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
+    const int r = int(i / nb), kb = int(i % nb);
+    const uint8_t* b = src + i * 34;
+    const int n = row0 + r;
+    const int mt = n / kTileM, rr = n % kTileM, k = kb * 32;
+    ds[(size_t(mt) * (K / kKs) + k / kKs) * (kKs / 32) * kTileM + ((k % kKs) / 32) * kTileM + rr] =
+        __ushort_as_half(static_cast<unsigned short>(b[0] | (b[1] << 8)));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t lo = 0, hi = 0;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        lo |= uint32_t(b[2 + j * 8 + e]) << (8 * e);
+        hi |= uint32_t(b[2 + j * 8 + 4 + e]) << (8 * e);
+      }
+      *reinterpret_cast<uint2*>(dq + packed_off(n, k + j * 8, K)) = make_uint2(lo, hi);
+    }
+  }
+}
+
+__global__ void k_row_sumsq(const uint16_t* __restrict__ E, int cols, float* __restrict__ out) {
+  __shared__ float red[32];
+  const uint16_t* row = E + size_t(blockIdx.x) * cols;
+  float s = 0.f;
+  for (int i = threadIdx.x; i < cols; i += blockDim.x) {
+    const float v = bf16_bits_to_f32(row[i]);
+    s += v * v;
+  }
+  s = block_sum(s, red);
+  if (threadIdx.x == 0) out[blockIdx.x] = s;
+}
+
+int grid_for(size_t total) { return int(total / 256 + 1 < 8192 ? total / 256 + 1 : 8192); }
+
+}  // namespace
+
+size_t packed_bytes(int fmt, int N, int K) {
+  if (fmt == WF_BF16) return size_t(N) * K * 2;
+  return size_t(N) * K + size_t(N) * (K / 32) * 2;
+}
+
+cudaError_t pack_rows(const void* src, int fmt, int rows, int K, const PackedMat& dst, int row0, cudaStream_t s) {
+  if (fmt == WF_BF16) {
+    k_pack_bf16<<<grid_for(size_t(rows) * (K / 8)), 256, 0, s>>>(static_cast<const uint16_t*>(src), rows, K,
+                                                                  reinterpret_cast<uint16_t*>(dst.w), row0);
+  } else {
+    k_pack_q8<<<grid_for(size_t(rows) * (K / 32)), 256, 0, s>>>(static_cast<const uint8_t*>(src), rows, K,
+                                                                 reinterpret_cast<int8_t*>(dst.w), dst.scale, row0);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t row_sumsq_bf16(const uint16_t* E, int rows, int cols, float* out, cudaStream_t s) {
+  k_row_sumsq<<<rows, 256, 0, s>>>(E, cols, out);
+  return cudaGetLastError();
+}
+
+}  // namespace qp

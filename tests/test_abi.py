@@ -4,6 +4,7 @@ These run without a GPU: only calls that fail argument checks before any
 CUDA call are made.
 """
 import ctypes
+import glob
 import os
 import re
 
@@ -22,9 +23,11 @@ def lib():
 
 
 def declared_functions():
-    src = open(os.path.join(ROOT, "include", "qp.h")).read()
-    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(qp_[a-z_0-9]+)\s*\(", src)))
+    names = set()
+    for h in sorted(glob.glob(os.path.join(ROOT, "include", "*.h"))):
+        src = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        names |= set(re.findall(r"\b(qp_[a-z_0-9]+)\s*\(", src))
+    return sorted(names)
 
 
 def test_header_declares_the_binding_symbols():
