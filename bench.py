@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the per-configuration summary")
     return ap.parse_args()
 
 
@@ -208,6 +209,58 @@ def reference_arm(args, g, raw, w):
     }
 
 
+def roofline_of(g, B, gemm_format, sampling, ms_per_call, hbm, tf):
+    nbytes, flops = work_of(g, B, gemm_format, sampling)
+    sec = ms_per_call / 1e3
+    if nbytes / (hbm * 1e9) >= flops / (tf * 1e12):
+        ach, peak, unit, bound = nbytes / sec / 1e9, hbm, "GB/s", "hbm"
+    else:
+        ach, peak, unit, bound = flops / sec / 1e12, tf, "TFLOP/s", "tensor"
+    return {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak}
+
+
+def sweep(g, dev, stream, steps, hbm, tf):
+    """Every batch configuration once more: ms per call, frames/s, us/step
+    and roofline fraction (each call a full 15-step loop, L2 flushed)."""
+    import torch
+    import synthetic as S
+    import codebook_rvq_code_gb300 as qpk
+    out = {}
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    raw_cache = {}
+    for cfg in (1, 2, 3, 4, 5):
+        w = S.make_workload(cfg, g)
+        if w.gemm_format not in raw_cache:
+            raw_cache[w.gemm_format] = S.workload_weights(w, g)
+        cp = qpk.CodePredictor(g, max_batch=w.B)
+        cp.load_raw_weights(raw_cache[w.gemm_format], device=dev)
+        H = torch.from_numpy(w.H).to(dev)
+        q0 = torch.from_numpy(w.q0).to(dev)
+        samp = None if w.gumbel is None else (w.temperature, w.top_k, torch.from_numpy(w.gumbel).to(dev))
+        codes = torch.empty((w.B, g.n_steps), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream)
+        torch.cuda.synchronize()
+        tot = 0.0
+        for i in range(steps):
+            flush.fill_(float(i))
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        ms = tot / steps
+        st = cp.device_status()
+        cp.close()
+        roof = roofline_of(g, w.B, w.gemm_format, samp is not None, ms, hbm, tf)
+        out[w.name] = {"B": w.B, "ms_per_call": ms, "frames_per_s": w.B / (ms / 1e3),
+                       "us_per_step": 1e3 * ms / g.n_steps, "roofline_bound": roof["bound"],
+                       "roofline_frac": roof["frac"], "device_status": st}
+    return out
+
+
 # ---------------------------------------------------------------------------
 
 def main():
@@ -336,6 +389,8 @@ def main():
     }
     if e2e:
         line["e2e"] = e2e
+    if not args.no_sweep and world == 1:
+        line["per_config"] = sweep(g, dev, stream, max(5, min(args.steps, 20)), hbm, tf_sust)
     if not args.no_cpu_baseline:
         fps, done, el = time_oracle(g, raw, w, min(B, 8), 10.0)
         line["cpu_baseline"] = {"value": fps, "unit": "frames/s", "cores": oracle_threads(), "kind": "oracle",

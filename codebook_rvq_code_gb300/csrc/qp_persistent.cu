@@ -110,7 +110,8 @@ struct PParams {
   const float2* rope_cs;
   // scratch
   float* x1; float* xk; uint16_t* a1[5]; uint16_t* ak[4]; uint16_t* ahead;
-  float* acc1_qkv; float* acck_qkv; float* acc1_gu; float* acck_gu; float* logits; float* kv;
+  float* acc1_qkv; float* acck_qkv; float* acc1_gu; float* acck_gu; float* logits;
+  uint16_t* kv;   // f16 [layer][frame][pos][k|v][kv_width]
   int Bmax;
   // per-call synchronisation (zeroed before the launch)
   unsigned* tile_cnt; unsigned* ready; unsigned* ss_cnt; float* ss; unsigned* pair; unsigned* head_done;
@@ -129,7 +130,8 @@ struct PParams {
 enum {
   EV_READY = 1, EV_LANDED, EV_COMMIT,            // MMA warp, per slice / segment
   EV_ACC = 4, EV_REDS, EV_COUNTED, EV_LASTDONE,   // consumer epilogue, per segment
-  EV_ATT_READY = 8, EV_ATT_DONE                   // attention warp, per item
+  EV_ATT_READY = 8, EV_ATT_DONE,                  // attention warp, per item
+  EV_WEIGHTS = 10                                 // MMA warp: the slice's weights are in shared memory
 };
 __device__ __forceinline__ unsigned long long* ev_base(const PParams& p) {
   return p.trace ? p.trace + size_t(p.trace_n) * gridDim.x * 2 + size_t(blockIdx.x) * 16384 : nullptr;
@@ -182,6 +184,12 @@ __device__ bool mwait(const PParams& p, uint64_t* bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -286,6 +294,11 @@ __device__ __forceinline__ uint2 pack4_f16(float a, float b, float c, float d) {
   return make_uint2(uint32_t(f32_to_f16_bits(a)) | (uint32_t(f32_to_f16_bits(b)) << 16),
                     uint32_t(f32_to_f16_bits(c)) | (uint32_t(f32_to_f16_bits(d)) << 16));
 }
+__device__ __forceinline__ float4 unpack4_f16(uint2 v) {
+  return make_float4(f16_bits_to_f32(v.x & 0xffff), f16_bits_to_f32(v.x >> 16), f16_bits_to_f32(v.y & 0xffff),
+                     f16_bits_to_f32(v.y >> 16));
+}
+
 
 // ---------------------------------------------------------------- producer
 __device__ void producer_role(const PParams& p, Misc& ms, uint8_t* smem) {
@@ -324,6 +337,21 @@ drain:
 }
 
 // --------------------------------------------------------- Q8_0 dequant
+// Four int8 values (one 32-bit word, little-endian) times an f16 scale, as
+// four f16: q is made exact in f16 as (1024 + (q + 128)) - 1152 -- the
+// mantissa of an f16 in [1024, 2048) holds the integer -- and the product
+// d * q is one correctly rounded f16 multiply, i.e. d * q rounded to the
+// nearest f16.
+__device__ __forceinline__ uint2 q8x4_to_f16x4(uint32_t w, __half2 d2) {
+  const uint32_t u = w ^ 0x80808080u;                 // q + 128 in each byte
+  const uint32_t lo = __byte_perm(u, 0x64646464u, 0x5150);   // bytes 0,1 -> f16 0x64xx
+  const uint32_t hi = __byte_perm(u, 0x64646464u, 0x5352);   // bytes 2,3
+  const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+  const __half2 a = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), bias), d2);
+  const __half2 b = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), bias), d2);
+  return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
+
 __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
   const int t = threadIdx.x - kDeqWarp0 * 32;
   uint32_t it = 0;
@@ -347,18 +375,20 @@ __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
       uint16_t* dq = reinterpret_cast<uint16_t*>(smem + kOffDeq + ds * kSlotBytes);
       for (int e = t * 16; e < kTileM * kKs; e += kDeqThreads * 16) {
         // e walks [k8][m8][8 rows][8 k]; 16 values are two rows of one core matrix
-        const int4 raw = *reinterpret_cast<const int4*>(qv + e);
-        const int8_t* q = reinterpret_cast<const int8_t*>(&raw);
+        const uint4 raw = *reinterpret_cast<const uint4*>(qv + e);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
         uint32_t out[8];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const int ee = e + h2 * 8;
           const int k8 = ee >> 10, m = ((ee >> 6) & 15) * 8 + ((ee >> 3) & 7);
-          const float dsc = __half2float(sc[(k8 >> 2) * kTileM + m]);
+          const __half2 d2 = __half2half2(sc[(k8 >> 2) * kTileM + m]);
 #pragma unroll
-          for (int i = 0; i < 4; ++i)
-            out[h2 * 4 + i] = uint32_t(f32_to_f16_bits(q8_0_operand(dsc, q[h2 * 8 + 2 * i]))) |
-                              (uint32_t(f32_to_f16_bits(q8_0_operand(dsc, q[h2 * 8 + 2 * i + 1]))) << 16);
+          for (int i = 0; i < 2; ++i) {
+            const uint2 pr = q8x4_to_f16x4(w4[h2 * 2 + i], d2);
+            out[h2 * 4 + i * 2] = pr.x;
+            out[h2 * 4 + i * 2 + 1] = pr.y;
+          }
         }
         *reinterpret_cast<uint4*>(dq + e) = make_uint4(out[0], out[1], out[2], out[3]);
         *reinterpret_cast<uint4*>(dq + e + 8) = make_uint4(out[4], out[5], out[6], out[7]);
@@ -374,8 +404,11 @@ __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
 }
 
 // --------------------------------------------------------------- MMA warp
+// Two-stage software pipeline over the CTA's slices: the operand copy of
+// slice s+1 is issued (after its readiness counter is satisfied) before the
+// MMAs of slice s, so operand latency overlaps tensor-core work.
 __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
-  uint32_t wit = 0, ait = 0, seg = 0;
+  uint32_t wit = 0, a_issue = 0, a_comp = 0, seg = 0;
   unsigned evi = 0;
   bool ok = true;
   for (int gi = 0; gi < p.NGEMM && ok; ++gi) {
@@ -385,18 +418,43 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
     my_run(c.n * G.n_mt * G.n_ks, gi, beg, end);
     const uint32_t idesc = idesc_f16(kTileM, c.Nc);
     const uint32_t abytes = uint32_t(kKs) * c.Nc * 2;
-    for (int s = beg; s < end; ++s) {
-      const int ks = s % G.n_ks, tt = s / G.n_ks, ch = tt / G.n_mt;
-      const bool first = s == beg || ks == 0;
-      const bool last = s == end - 1 || ks == G.n_ks - 1;
-      if (!poll_geq(p, ready_cnt(p, gi, ch, ks), unsigned(rows_in(G.R, c, ch)))) { ok = false; break; }
+    // Readiness of the run's operand slices: one batch of relaxed loads and a
+    // single acquire fence up front, instead of an acquire round trip per slice.
+    const int ch_lo = beg < end ? beg / G.n_ks / G.n_mt : 0;
+    uint64_t seen = 0;
+    if (beg < end) {
+      const int ch_hi = (end - 1) / G.n_ks / G.n_mt;
+      for (int ch = ch_lo; ch <= ch_hi; ++ch)
+        for (int ks = 0; ks < G.n_ks; ++ks) {
+          const int bit = (ch - ch_lo) * G.n_ks + ks;
+          if (bit < 64 && ld_relaxed_u32(ready_cnt(p, gi, ch, ks)) >= unsigned(rows_in(G.R, c, ch)))
+            seen |= 1ull << bit;
+        }
+      fence_acq_rel_gpu();
+    }
+    auto issue = [&](int s) -> bool {
+      const int ks = s % G.n_ks, ch = s / G.n_ks / G.n_mt, bit = (ch - ch_lo) * G.n_ks + ks;
+      if (!(bit < 64 && ((seen >> bit) & 1ull))) {
+        if (!poll_geq(p, ready_cnt(p, gi, ch, ks), unsigned(rows_in(G.R, c, ch)))) return false;
+        if (bit < 64) seen |= 1ull << bit;
+      }
       ev_mma(p, evi, EV_READY, gi);
-      const uint32_t a = ait % kNAct, au = ait / kNAct;
-      if (au > 0 && !mwait(p, &ms.aempty[a], (au - 1) & 1)) { ok = false; break; }
-      uint8_t* abuf = smem + kOffAct + a * kActBytes;
+      const uint32_t a = a_issue % kNAct, au = a_issue / kNAct;
+      if (au > 0 && !mwait(p, &ms.aempty[a], (au - 1) & 1)) return false;
       fence_proxy_async_global();
       mbar_expect_tx(&ms.afull[a], abytes);
-      bulk_g2s(abuf, G.act + size_t(ch) * G.Kdim * c.Nc + size_t(ks) * kKs * c.Nc, abytes, &ms.afull[a]);
+      bulk_g2s(smem + kOffAct + a * kActBytes, G.act + size_t(ch) * G.Kdim * c.Nc + size_t(ks) * kKs * c.Nc, abytes,
+               &ms.afull[a]);
+      ++a_issue;
+      return true;
+    };
+    if (beg < end && !issue(beg)) { ok = false; break; }
+    for (int s = beg; s < end; ++s) {
+      if (s + 1 < end && !issue(s + 1)) { ok = false; break; }
+      const int ks = s % G.n_ks;
+      const bool first = s == beg || ks == 0;
+      const bool last = s == end - 1 || ks == G.n_ks - 1;
+      const uint32_t a = a_comp % kNAct, au = a_comp / kNAct;
       const uint8_t* A;
       uint64_t* wfree;
       if (p.q8) {
@@ -410,12 +468,13 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
         A = smem + kOffRing + ws * kSlotBytes;
         wfree = &ms.wempty[ws];
       }
+      ev_mma(p, evi, EV_WEIGHTS, gi);
       const uint32_t tb = seg & 1;
       if (first && seg >= 2 && !mwait(p, &ms.accempty[tb], ((seg >> 1) - 1) & 1)) { ok = false; break; }
       if (!mwait(p, &ms.afull[a], au & 1)) { ok = false; break; }
       ev_mma(p, evi, EV_LANDED, gi);
       tc_fence_after();
-      const uint32_t a0 = smem_u32(A), b0 = smem_u32(abuf), d = ms.tmem_base + tb * 128;
+      const uint32_t a0 = smem_u32(A), b0 = smem_u32(smem + kOffAct + a * kActBytes), d = ms.tmem_base + tb * 128;
 #pragma unroll
       for (int j = 0; j < kKs / 16; ++j) {
         const uint64_t ad = smem_desc(a0 + j * 2 * (kTileM / 8) * 128, (kTileM / 8) * 128, 128);
@@ -433,12 +492,14 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
         ++seg;
       }
       ++wit;
-      ++ait;
+      ++a_comp;
     }
   }
-  // every MMA retires before TMEM is released
+  // every MMA retires, and every operand copy lands, before TMEM and shared
+  // memory are released
   mma_commit(&ms.mmadone);
   mbar_wait(&ms.mmadone, 0);
+  for (uint32_t k = a_comp; k < a_issue; ++k) mbar_wait(&ms.afull[k % kNAct], (k / kNAct) & 1);
 }
 
 // ------------------------------------------------------ consumer helpers
@@ -600,7 +661,7 @@ __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
   const int n_items = p.B * p.n_kv, nks = p.d / kKs;
   const float scale = rsqrtf(128.f);
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  float* kvl = p.kv + size_t(l) * p.Bmax * ctx * 2 * p.kvw;
+  uint16_t* kvl = p.kv + size_t(l) * p.Bmax * ctx * 2 * p.kvw;
   for (int i = (blockIdx.x + gi_q * 13) % G + warp * G; i < n_items; i += kConsumerWarps * G) {
     const int b = i / p.n_kv, j = i % p.n_kv, r0 = b * P, ch = r0 / c.Nc;
     // the group's q tiles, its k tile and its v tile: one lane polls each
@@ -613,26 +674,31 @@ __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
     if (!__all_sync(0xffffffffu, okl)) return false;
     __syncwarp();   // order every lane's reads after the acquires
     if (lane == 0) ev_cons(p, &ms.evc, EV_ATT_READY, gi_q);
-    float* kvb = kvl + size_t(b) * ctx * 2 * p.kvw + j * 128 + lane * 4;   // + (pos*2 + {0,1}) * kvw
+    uint16_t* kvb = kvl + size_t(b) * ctx * 2 * p.kvw + j * 128 + lane * 4;   // + (pos*2 + {0,1}) * kvw
     for (int pp = 0; pp < P; ++pp) {
       const int r = r0 + pp, pos = pos0 + pp;
       float* row = acc + size_t(r) * qkvw;
       float* kr = row + p.qw + j * 128 + lane * 4;
       float* vr = row + p.qw + p.kvw + j * 128 + lane * 4;
+      // every load of the item that does not depend on another is issued first:
+      // the new k, v and the first two q heads, then the cached keys and values
       const float4 kraw = __ldcg(reinterpret_cast<const float4*>(kr));
       const float4 vnew = __ldcg(reinterpret_cast<const float4*>(vr));
+      float4 qraw[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        qraw[hh] = hh < grp ? __ldcg(reinterpret_cast<const float4*>(row + (j * grp + hh) * 128 + lane * 4)) : z4;
+      uint2 kh[kMaxCtx], vh[kMaxCtx];
+#pragma unroll
+      for (int t = 0; t < kMaxCtx; ++t) {
+        kh[t] = t < pos ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 0) * p.kvw)) : make_uint2(0, 0);
+        vh[t] = t < pos ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 1) * p.kvw)) : make_uint2(0, 0);
+      }
       const float4 knew = norm_rope(kraw, L.k_norm, p.eps, p.rope_cs + pos * 64, lane);
-      *reinterpret_cast<float4*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = knew;
-      *reinterpret_cast<float4*>(kvb + (size_t(pos) * 2 + 1) * p.kvw) = vnew;
+      *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = pack4_f16(knew.x, knew.y, knew.z, knew.w);
+      *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 1) * p.kvw) = pack4_f16(vnew.x, vnew.y, vnew.z, vnew.w);
       *reinterpret_cast<float4*>(kr) = z4;
       *reinterpret_cast<float4*>(vr) = z4;
-      __syncwarp();
-      // keys and values of positions 0..pos (the newest from registers)
-      float4 kk[kMaxCtx];
-#pragma unroll
-      for (int t = 0; t < kMaxCtx; ++t)
-        kk[t] = t < pos ? __ldcg(reinterpret_cast<const float4*>(kvb + (size_t(t) * 2 + 0) * p.kvw))
-                        : (t == pos ? knew : z4);
       for (int g0 = 0; g0 < grp; g0 += 2) {
         const int nh = min(2, grp - g0);
         float4 qn[2];
@@ -641,17 +707,19 @@ __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
           qn[hh] = z4;
           if (hh < nh) {
             float* qr = row + (j * grp + g0 + hh) * 128 + lane * 4;
-            qn[hh] = norm_rope(__ldcg(reinterpret_cast<const float4*>(qr)), L.q_norm, p.eps, p.rope_cs + pos * 64,
-                               lane);
+            const float4 q = g0 == 0 ? qraw[hh] : __ldcg(reinterpret_cast<const float4*>(qr));
+            qn[hh] = norm_rope(q, L.q_norm, p.eps, p.rope_cs + pos * 64, lane);
             *reinterpret_cast<float4*>(qr) = z4;
           }
         }
         float part[32];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh)
+        for (int t = 0; t < kMaxCtx; ++t) {
+          const float4 kk = t < pos ? unpack4_f16(kh[t]) : (t == pos ? knew : z4);
 #pragma unroll
-          for (int t = 0; t < kMaxCtx; ++t)
-            part[hh * 16 + t] = qn[hh].x * kk[t].x + qn[hh].y * kk[t].y + qn[hh].z * kk[t].z + qn[hh].w * kk[t].w;
+          for (int hh = 0; hh < 2; ++hh)
+            part[hh * 16 + t] = qn[hh].x * kk.x + qn[hh].y * kk.y + qn[hh].z * kk.z + qn[hh].w * kk.w;
+        }
         // lane l: score of head (l >> 4), position (l & 15)
         const bool valid = (lane >> 4) < nh && (lane & 15) <= pos;
         const float rsum = reduce_scatter32(part, lane);   // all 32 lanes take part
@@ -667,8 +735,7 @@ __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
         float4 o2[2] = {z4, z4};
 #pragma unroll
         for (int t = 0; t < kMaxCtx; ++t) {
-          const float4 vv = t < pos ? __ldcg(reinterpret_cast<const float4*>(kvb + (size_t(t) * 2 + 1) * p.kvw))
-                                    : (t == pos ? vnew : z4);
+          const float4 vv = t < pos ? unpack4_f16(vh[t]) : (t == pos ? vnew : z4);
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const float w = __shfl_sync(0xffffffffu, pr, hh * 16 + t);
@@ -679,6 +746,7 @@ __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
           *reinterpret_cast<uint2*>(act_o + act_off(r, (j * grp + g0 + hh) * 128 + lane * 4, p.qw, c)) =
               pack4_f16(o2[hh].x, o2[hh].y, o2[hh].z, o2[hh].w);
       }
+      __syncwarp();   // the next position of this frame reads what was stored here
     }
     __syncwarp();
     if (lane == 0) {
@@ -691,7 +759,7 @@ __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
 
 // Finishing work of a completed tile, by the CTA whose contribution
 // completed it (all consumer threads).  Each warp takes rows warp, warp + 8,
-// ...; the loads of up to four of its rows are issued together.
+// ...; the loads of several of its rows are issued together.
 __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, int ch, int mt, Ck c) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -716,16 +784,16 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
     const float4 wv = *reinterpret_cast<const float4*>(w + feat);
     const int P = G.k == 1 ? 2 : 1;
     const Ck ch_h = chunking(p.B);
-    for (int r0 = warp; r0 < rows; r0 += 4 * kConsumerWarps) {
-      float4 xv[4];
+    for (int r0 = warp; r0 < rows; r0 += 8 * kConsumerWarps) {
+      float4 xv[8];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const int row = r0 + u * kConsumerWarps, n = ch * c.Nc + row;
         const bool use = row < rows && (!to_head || (n % P) == P - 1);
         xv[u] = use ? __ldcg(reinterpret_cast<const float4*>(X + size_t(n) * p.d + feat)) : z4;
       }
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
+      for (int u = 0; u < 8; ++u) {
         const int row = r0 + u * kConsumerWarps, n = ch * c.Nc + row;
         if (row >= rows || (to_head && (n % P) != P - 1)) continue;
         const float4 x = xv[u];
@@ -826,7 +894,7 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
 }
 
 // Drain this CTA's accumulator segments of GEMM gi.
-__device__ bool epilogues(const PParams& p, Misc& ms, int gi, uint32_t& seg) {
+__device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, uint32_t& seg) {
   const GI G = gemm_inst(p, gi);
   const Ck c = chunking(G.R);
   int beg, end;
@@ -856,16 +924,31 @@ __device__ bool epilogues(const PParams& p, Misc& ms, int gi, uint32_t& seg) {
     if (!ms.flag[1]) return false;
     if (t == 0) ev_cons(p, &ms.evc, EV_ACC, gi);
     tc_fence_after();
+    // Each warp drains 32 accumulator rows (features) x 8 columns (frames) at
+    // a time, transposes them through its 1 KB of shared memory, and adds 4
+    // consecutive features per thread with one vector reduction.
     const int quarter = warp & 3, half = warp >> 2, cols = c.Nc / 2;
-    const int m = mt * kTileM + quarter * 32 + lane;
+    const int m0 = mt * kTileM + quarter * 32;
+    float* tp = reinterpret_cast<float*>(keys) + warp * 256;   // [8 frames][32 features]
     for (int col = half * cols; col < (half + 1) * cols; col += 8) {
       float v[8];
       tmem_ld8(ms.tmem_base + tb * 128 + (uint32_t(quarter * 32) << 16) + uint32_t(col), v);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int n = ch * c.Nc + col + i;
-        if (n < G.R) red_add_f32(G.acc + size_t(n) * G.ld + m, scaled ? v[i] * ms.inv[col + i] : v[i]);
+      for (int i = 0; i < 8; ++i) tp[i * 32 + lane] = v[i];
+      __syncwarp();
+#pragma unroll
+      for (int pass = 0; pass < 2; ++pass) {
+        const int f = pass * 4 + (lane >> 3), k4 = (lane & 7) * 4, n = ch * c.Nc + col + f;
+        if (n < G.R) {
+          float4 x = *reinterpret_cast<const float4*>(tp + f * 32 + k4);
+          if (scaled) {
+            const float s = ms.inv[col + f];
+            x.x *= s; x.y *= s; x.z *= s; x.w *= s;
+          }
+          red_add_v4_f32(G.acc + size_t(n) * G.ld + m0 + k4, x);
+        }
       }
+      __syncwarp();
     }
     tc_fence_before();
     __syncwarp();
@@ -984,17 +1067,17 @@ __device__ void consumer_role(const PParams& p, Misc& ms, uint8_t* smem) {
     if (ms.fail) return;                      \
   }
   QP_SECTION(prep1_items(p));
-  QP_SECTION(epilogues(p, ms, 0, seg));
+  QP_SECTION(epilogues(p, ms, keys, 0, seg));
   for (int k = 1; k <= p.n_steps; ++k) {
     if (k > 1) QP_SECTION(prepk_items(p, k));
     for (int l = 0; l < p.L; ++l) {
-      QP_SECTION(epilogues(p, ms, gi_of(p, k, l, 0), seg));
+      QP_SECTION(epilogues(p, ms, keys, gi_of(p, k, l, 0), seg));
       QP_SECTION(attn_items(p, ms, k, l));
-      QP_SECTION(epilogues(p, ms, gi_of(p, k, l, 1), seg));
-      QP_SECTION(epilogues(p, ms, gi_of(p, k, l, 2), seg));
-      QP_SECTION(epilogues(p, ms, gi_of(p, k, l, 3), seg));
+      QP_SECTION(epilogues(p, ms, keys, gi_of(p, k, l, 1), seg));
+      QP_SECTION(epilogues(p, ms, keys, gi_of(p, k, l, 2), seg));
+      QP_SECTION(epilogues(p, ms, keys, gi_of(p, k, l, 3), seg));
     }
-    QP_SECTION(epilogues(p, ms, gi_head(p, k), seg));
+    QP_SECTION(epilogues(p, ms, keys, gi_head(p, k), seg));
     if (p.temperature > 0.f) QP_SECTION(decide_items(p, ms, keys, k));
   }
   QP_SECTION(final_items(p));
@@ -1107,7 +1190,7 @@ void fill_params(PParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scra
   p.acc1_gu = reinterpret_cast<float*>(scratch + L.acc1_gu);
   p.acck_gu = reinterpret_cast<float*>(scratch + L.acck_gu);
   p.logits = reinterpret_cast<float*>(scratch + L.logits);
-  p.kv = reinterpret_cast<float*>(scratch + L.kv);
+  p.kv = reinterpret_cast<uint16_t*>(scratch + L.kv);
   p.Bmax = bmax;
   p.tile_cnt = reinterpret_cast<unsigned*>(sync + S.tile_cnt);
   p.ready = reinterpret_cast<unsigned*>(sync + S.ready);
@@ -1181,7 +1264,7 @@ Scratch scratch_layout(const qp_geometry& g, int bmax) {
   L.acc1_gu = o;  o += al256(R1 * 2 * F * 4);
   L.acck_gu = o;  o += al256(RK * 2 * F * 4);
   L.logits = o;   o += al256(RK * V * 4);
-  L.kv = o;       o += al256(size_t(g.layers) * RK * (g.n_steps + 1) * 2 * kvw * 4);
+  L.kv = o;       o += al256(size_t(g.layers) * RK * (g.n_steps + 1) * 2 * kvw * 2);
   L.sync = o;
   L.total = o + sync_layout(g, bmax).total;
   return L;
