@@ -1,0 +1,116 @@
+// Device helpers shared by the frame-loop kernels: bounded waits that honour
+// a grid-wide abort flag, counter atomics with explicit memory order, f16
+// packing, and the per-warp RMSNorm + RoPE and score reduction of attention.
+// A params type passed to the waits has int* members abort_flag and status.
+#pragma once
+
+#include "qp_common.cuh"
+#include "qp_internal.h"
+#include "qp_ptx.cuh"
+
+namespace qp {
+namespace {
+
+// ------------------------------------------------------------------ waits
+template <class Par>
+__device__ __forceinline__ void abort_all(const Par& p) {
+  set_status(p.status, QP_ERR_TIMEOUT);
+  atomicExch(p.abort_flag, 1);
+}
+template <class Par>
+__device__ __forceinline__ bool aborted(const Par& p) { return *(volatile int*)p.abort_flag != 0; }
+
+// Until *ctr >= want (acquire), bounded.
+template <class Par>
+__device__ bool poll_geq(const Par& p, const unsigned* ctr, unsigned want) {
+  if (ld_acquire_u32(ctr) >= want) return true;
+  const long long t0 = clock64();
+  for (unsigned it = 1;; ++it) {
+    if (ld_acquire_u32(ctr) >= want) return true;
+    if ((it & 63) == 0) {
+      if (aborted(p)) return false;
+      if (clock64() - t0 > kSpinLimit) { abort_all(p); return false; }
+    }
+  }
+}
+
+// mbarrier phase wait, bounded, abandoning when the grid aborts.
+template <class Par>
+__device__ bool mwait(const Par& p, uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (unsigned it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255) == 0) {
+      if (aborted(p)) return false;
+      if (clock64() - t0 > kSpinLimit) { abort_all(p); return false; }
+    }
+  }
+}
+
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Fetch-and-add with acquire-release semantics at GPU scope: publishes this
+// CTA's earlier writes (ordered before it by bar.sync) and, for the caller
+// that completes a count, makes every earlier contributor's writes visible.
+__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint2 pack4_f16(float a, float b, float c, float d) {
+  return make_uint2(uint32_t(f32_to_f16_bits(a)) | (uint32_t(f32_to_f16_bits(b)) << 16),
+                    uint32_t(f32_to_f16_bits(c)) | (uint32_t(f32_to_f16_bits(d)) << 16));
+}
+__device__ __forceinline__ float4 unpack4_f16(uint2 v) {
+  return make_float4(f16_bits_to_f32(v.x & 0xffff), f16_bits_to_f32(v.x >> 16), f16_bits_to_f32(v.y & 0xffff),
+                     f16_bits_to_f32(v.y >> 16));
+}
+
+
+// RMSNorm of a 128-vector held as 4 values per lane, then rotate-half RoPE
+// at position pos (pairs (i, i+64) sit in lanes l and l^16).
+__device__ __forceinline__ float4 norm_rope(float4 x, const float* nw, float eps, const float2* cs, int lane) {
+  const float ss = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
+  const float r = rsqrtf(ss / 128.f + eps);
+  const float4 w = *reinterpret_cast<const float4*>(nw + lane * 4);
+  float v[4] = {x.x * r * w.x, x.y * r * w.y, x.z * r * w.z, x.w * r * w.w};
+  float o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float partner = __shfl_xor_sync(0xffffffffu, v[e], 16);
+    const float2 c = cs[(lane * 4 + e) & 63];
+    o[e] = lane < 16 ? v[e] * c.x - partner * c.y : v[e] * c.x + partner * c.y;
+  }
+  return make_float4(o[0], o[1], o[2], o[3]);
+}
+
+__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0];
+}
+
+}  // namespace
+}  // namespace qp

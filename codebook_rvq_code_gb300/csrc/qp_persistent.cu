@@ -36,9 +36,7 @@
 // the one program order every CTA follows, so the earliest pending item can
 // always run: no deadlock.  Every wait is bounded; one that runs out latches
 // QP_ERR_TIMEOUT and sets an abort flag that every other wait honours.
-#include "qp_common.cuh"
-#include "qp_internal.h"
-#include "qp_ptx.cuh"
+#include "qp_device.cuh"
 
 namespace qp {
 
@@ -151,62 +149,6 @@ __device__ __forceinline__ void ev_cons(const PParams& p, unsigned* evc, int cod
   }
 }
 
-// ------------------------------------------------------------------ waits
-__device__ __forceinline__ void abort_all(const PParams& p) {
-  set_status(p.status, QP_ERR_TIMEOUT);
-  atomicExch(p.abort_flag, 1);
-}
-__device__ __forceinline__ bool aborted(const PParams& p) { return *(volatile int*)p.abort_flag != 0; }
-
-// Until *ctr >= want (acquire), bounded.
-__device__ bool poll_geq(const PParams& p, const unsigned* ctr, unsigned want) {
-  if (ld_acquire_u32(ctr) >= want) return true;
-  const long long t0 = clock64();
-  for (unsigned it = 1;; ++it) {
-    if (ld_acquire_u32(ctr) >= want) return true;
-    if ((it & 63) == 0) {
-      if (aborted(p)) return false;
-      if (clock64() - t0 > kSpinLimit) { abort_all(p); return false; }
-    }
-  }
-}
-
-// mbarrier phase wait, bounded, abandoning when the grid aborts.
-__device__ bool mwait(const PParams& p, uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const long long t0 = clock64();
-  for (unsigned it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 255) == 0) {
-      if (aborted(p)) return false;
-      if (clock64() - t0 > kSpinLimit) { abort_all(p); return false; }
-    }
-  }
-}
-
-__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Fetch-and-add with acquire-release semantics at GPU scope: publishes this
-// CTA's earlier writes (ordered before it by bar.sync) and, for the caller
-// that completes a count, makes every earlier contributor's writes visible.
-__device__ __forceinline__ unsigned atom_add_acq_rel(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
-  return old;
-}
-__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
 // ----------------------------------------------------------- the program
 struct Ck { int Nc, n; };
 __device__ __forceinline__ Ck chunking(int R) {
@@ -289,16 +231,6 @@ __device__ __forceinline__ unsigned* pair_cnt(const PParams& p, int k, int l, in
 __device__ __forceinline__ unsigned* head_done(const PParams& p, int k, int ch) {
   return p.head_done + size_t(k - 1) * p.NCH + ch;
 }
-
-__device__ __forceinline__ uint2 pack4_f16(float a, float b, float c, float d) {
-  return make_uint2(uint32_t(f32_to_f16_bits(a)) | (uint32_t(f32_to_f16_bits(b)) << 16),
-                    uint32_t(f32_to_f16_bits(c)) | (uint32_t(f32_to_f16_bits(d)) << 16));
-}
-__device__ __forceinline__ float4 unpack4_f16(uint2 v) {
-  return make_float4(f16_bits_to_f32(v.x & 0xffff), f16_bits_to_f32(v.x >> 16), f16_bits_to_f32(v.y & 0xffff),
-                     f16_bits_to_f32(v.y >> 16));
-}
-
 
 // ---------------------------------------------------------------- producer
 __device__ void producer_role(const PParams& p, Misc& ms, uint8_t* smem) {
@@ -503,23 +435,6 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
 }
 
 // ------------------------------------------------------ consumer helpers
-// RMSNorm of a 128-vector held as 4 values per lane, then rotate-half RoPE
-// at position pos (pairs (i, i+64) sit in lanes l and l^16).
-__device__ __forceinline__ float4 norm_rope(float4 x, const float* nw, float eps, const float2* cs, int lane) {
-  const float ss = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
-  const float r = rsqrtf(ss / 128.f + eps);
-  const float4 w = *reinterpret_cast<const float4*>(nw + lane * 4);
-  float v[4] = {x.x * r * w.x, x.y * r * w.y, x.z * r * w.z, x.w * r * w.w};
-  float o[4];
-#pragma unroll
-  for (int e = 0; e < 4; ++e) {
-    const float partner = __shfl_xor_sync(0xffffffffu, v[e], 16);
-    const float2 c = cs[(lane * 4 + e) & 63];
-    o[e] = lane < 16 ? v[e] * c.x - partner * c.y : v[e] * c.x + partner * c.y;
-  }
-  return make_float4(o[0], o[1], o[2], o[3]);
-}
-
 // Step-1 inputs, one warp per row r < 2B: operand rows 2b = f16(H_b),
 // 2b+1 = f16(E0[q0_b]); residual rows start at the projection bias.
 __device__ bool prep1_items(const PParams& p) {
@@ -635,20 +550,6 @@ __device__ bool final_items(const PParams& p) {
 // Lane l holds dims 4l..4l+3 of every 128-vector.  Scores of two q heads x
 // 16 positions are 32 partial dot products per lane, summed across the warp
 // by one reduce-scatter that leaves score (head l/16, position l%16) in lane l.
-__device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < o; ++i) {
-      const float send = upper ? v[i] : v[i + o];
-      const float keep = upper ? v[i + o] : v[i];
-      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
-  }
-  return v[0];
-}
-
 __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = gridDim.x;
   const int P = k == 1 ? 2 : 1, pos0 = k == 1 ? 0 : k, R = p.B * P;
