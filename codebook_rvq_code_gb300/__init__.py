@@ -26,7 +26,7 @@ EXPORTED = [
     "qp_abi_version", "qp_status_string", "qp_default_geometry", "qp_create", "qp_load_weights",
     "qp_predict_frames", "qp_predict_frames_ex", "qp_predict_frames_host", "qp_get_device_status",
     "qp_launches_per_call", "qp_destroy", "qp_predict_frames_static",
-    "qp_trace_enable", "qp_trace_read",   # include/qp_debug.h
+    "qp_set_engine", "qp_trace_enable", "qp_trace_read",   # include/qp_debug.h
 ]
 
 
@@ -79,6 +79,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qp_launches_per_call.argtypes = [vp, i32, i32]
     lib.qp_destroy.restype = None
     lib.qp_destroy.argtypes = [vp]
+    lib.qp_set_engine.restype = i32
+    lib.qp_set_engine.argtypes = [vp, i32]
     lib.qp_trace_enable.restype = i32
     lib.qp_trace_enable.argtypes = [vp, i32]
     lib.qp_trace_read.restype = i32
@@ -210,6 +212,13 @@ class CodePredictor:
         _check("qp_predict_frames_static", self._lib.qp_predict_frames_static(
             self._h, B, _ptr(H), _ptr(q0), _ptr(out_codes), _ptr(out_logits), _stream_ptr(stream)))
         return out_codes
+
+    ENGINES = {"auto": 0, "tile": 1, "small": 2}
+
+    def set_engine(self, engine: str):
+        """Schedule for later calls (include/qp_debug.h): "auto", "tile" or
+        "small"."""
+        _check("qp_set_engine", self._lib.qp_set_engine(self._h, self.ENGINES[engine]))
 
     def trace(self, enable: bool = True):
         """Turn the phase trace of include/qp_debug.h on or off."""

@@ -91,6 +91,15 @@ size_t matrix_bytes(int fmt, int64_t N, int64_t K) {
                             : carve_size<uint8_t>(size_t(N) * K) + carve_size<__half>(size_t(N) * (K / 32));
 }
 
+// The engine that serves a call (qp_debug.h, qp_engine).
+qp_status run(qp_handle* h, const qp::RunArgs& a, cudaStream_t s) {
+  const bool sm = qp::small_supported(h, a);
+  if (h->engine == QP_ENGINE_SMALL && !sm) return QP_ERR_ARG;
+  if (sm && h->engine != QP_ENGINE_TILE)
+    return qp::run_frames_small(h, a, static_cast<uint8_t*>(h->sarena), h->scr, h->max_batch, s);
+  return qp::run_frames_persistent(h, a, s);
+}
+
 }  // namespace
 
 extern "C" {
@@ -336,7 +345,7 @@ qp_status qp_predict_frames_ex(qp_handle* h, int B, const float* H, const int32_
   qp::RunArgs a;
   a.B = B; a.H = H; a.q0 = q0; a.out_codes = out_codes; a.out_logits = out_logits; a.forced = forced_codes;
   if (samp) { a.temperature = samp->temperature; a.top_k = samp->top_k; a.gumbel = samp->gumbel; }
-  return qp::run_frames_persistent(h, a, static_cast<cudaStream_t>(s));
+  return run(h, a, static_cast<cudaStream_t>(s));
 }
 
 qp_status qp_predict_frames(qp_handle* h, int B, const float* H, const int32_t* q0, int32_t* out_codes,
@@ -360,7 +369,7 @@ qp_status qp_predict_frames_host(qp_handle* h, int B, const float* H_host, const
   qp::RunArgs a;
   a.B = B; a.H = h->H_stage; a.q0 = h->q0_stage; a.out_codes = h->codes_stage;
   if (samp) { a.temperature = samp->temperature; a.top_k = samp->top_k; a.gumbel = samp->gumbel; }
-  st = qp::run_frames_persistent(h, a, s);
+  st = run(h, a, s);
   if (st != QP_OK) return st;
   if (cudaMemcpyAsync(codes_host, h->codes_stage, size_t(B) * g.n_steps * 4, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
       cudaStreamSynchronize(s) != cudaSuccess) {
@@ -399,6 +408,12 @@ qp_status qp_get_device_status(qp_handle* h, qp_stream sv) {
 int qp_launches_per_call(qp_handle* h, int B, int /*sampling*/) {
   if (!h || B < 1 || B > h->max_batch) return -1;
   return 1;   // one persistent kernel per call
+}
+
+qp_status qp_set_engine(qp_handle* h, int engine) {
+  if (!h || engine < QP_ENGINE_AUTO || engine > QP_ENGINE_SMALL) return QP_ERR_ARG;
+  h->engine = engine;
+  return QP_OK;
 }
 
 qp_status qp_trace_enable(qp_handle* h, int enable) {

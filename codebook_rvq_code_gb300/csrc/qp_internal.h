@@ -76,6 +76,10 @@ Scratch scratch_layout(const qp_geometry& g, int bmax);
 // decisions, abort flag.
 size_t sync_bytes(const qp_geometry& g, int B);
 
+// Largest batch the small-batch engine serves (2B <= 128 activation rows at
+// step 1: one tensor-core N chunk).
+constexpr int kSmallMaxFrames = 64;
+
 }  // namespace qp
 
 struct qp_handle {
@@ -111,6 +115,8 @@ struct qp_handle {
   int32_t* codes_stage = nullptr;
   unsigned long long* trace = nullptr;          // optional phase trace (qp_debug.h)
   int trace_phases = 0;
+
+  int engine = 0;                               // qp_engine (qp_debug.h)
 };
 
 namespace qp {
@@ -118,6 +124,11 @@ namespace qp {
 qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s);
 qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s);
 size_t persistent_smem_bytes();
+// small-batch engine (qp_small.cu): bf16 weights, at most kSmallMaxFrames
+bool small_supported(const qp_handle* h, const RunArgs& a);
+qp_status run_frames_small(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
+                           cudaStream_t s);
+size_t small_smem_bytes();
 // load-time weight preparation (qp_weights.cu)
 size_t packed_bytes(int fmt, int N, int K);
 // Pack `rows` rows of a caller matrix [rows, K] (bf16, or a Q8_0 block

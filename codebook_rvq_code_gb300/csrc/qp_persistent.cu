@@ -37,6 +37,7 @@
 // always run: no deadlock.  Every wait is bounded; one that runs out latches
 // QP_ERR_TIMEOUT and sets an abort flag that every other wait honours.
 #include "qp_device.cuh"
+#include "../../include/qp_debug.h"
 
 namespace qp {
 
@@ -1230,6 +1231,9 @@ qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   RunArgs ga = a;
   ga.forced = nullptr;
   ga.temperature = 0.f; ga.top_k = 0; ga.gumbel = nullptr;
+  const bool sm = small_supported(h, ga);
+  if (h->engine == QP_ENGINE_SMALL && !sm) return QP_ERR_ARG;
+  if (sm && h->engine != QP_ENGINE_TILE) return run_frames_small(h, ga, base, L, a.B, s);
   PParams p{};
   fill_params(p, h, ga, base, L, base + L.sync, S, a.B);
   // the launch zeroes the synchronisation words and accumulators; every

@@ -1,0 +1,1055 @@
+// The Code Predictor frame loop for small batches (at most 64 frames): one
+// persistent kernel, scheduled for latency.
+//
+// It computes what qp_persistent.cu computes (the whole frame loop as one
+// fixed GPU program over a preallocated KV cache: "テキスト音声合成モデルを50
+// ミリ秒未満で応答させる方法", section "Qwen3-TTSの最適化方法", item 3).  The
+// contractions use the same tensor-core shape -- 128 weight rows on M, the
+// activation rows on N (16..128), f16 operands, f32 accumulators in TMEM --
+// and K is split across the SMs in 128-column slices so that every SM streams
+// an equal share of each weight matrix.  What differs is how a dependent step
+// completes:
+//
+//   * each (128-row tile, K slice) unit adds its f32 partial product straight
+//     into the destination (the residual stream for projection, O and down;
+//     the q|k|v, gate|up and logit accumulators otherwise) and counts itself
+//     done; a GEMM waits for one counter to reach the previous GEMM's unit
+//     count.  There is no finishing pass over a completed tile;
+//   * the consumer warps of the CTA that runs a unit build its operand slice
+//     in shared memory from those f32 sources: x * w_norm, silu(g) * u, the
+//     f16 conversion -- the work the tile engine's finishing pass does once;
+//   * a GEMM whose input is RMS-normalised computes the rows' scale itself
+//     (from the complete residual rows) and applies it to its partials before
+//     they are added, so every accumulator holds final values.
+//
+// Roles per CTA (one CTA per SM): warps 0-7 consume (operand builds,
+// accumulator drains, attention, step inputs, decisions), warp 8 streams
+// weights, warp 9 issues the MMAs.  Every wait is bounded and honours a
+// grid-wide abort flag; each role walks the program in one order and waits
+// only on work earlier in that order, and all CTAs are co-resident
+// (cooperative launch).
+#include "qp_device.cuh"
+
+namespace qp {
+
+namespace {
+
+constexpr int kSmConsumerWarps = 8;
+constexpr int kSmConsumers = kSmConsumerWarps * 32;
+constexpr int kSmProducerWarp = 8;
+constexpr int kSmMmaWarp = 9;
+constexpr int kSmThreads = 10 * 32;
+
+constexpr uint32_t kSmWSlot = kTileM * kKs * 2;      // one 128 x 128 f16 weight slice
+constexpr int kSmNW = 5;                             // weight ring slots
+constexpr uint32_t kSmOpBytes = 32768;               // operand slices, 128 K x N rows f16 each
+constexpr int kSmMaxOp = 8;
+constexpr uint32_t kSmOffW = 0;
+constexpr uint32_t kSmOffOp = kSmNW * kSmWSlot;
+constexpr uint32_t kSmOffKeys = kSmOffOp + kSmOpBytes;   // top-k keys, or the drain's transpose buffer
+constexpr uint32_t kSmOffMisc = kSmOffKeys + kMaxVocab * 4;
+constexpr uint32_t kSmTmemCols = 256;                // two accumulators of up to 128 columns
+
+enum { SBAR_CONS = 1 };
+enum { S_PROJ = 0, S_QKV, S_O, S_GU, S_DOWN, S_HEAD };
+
+struct SMisc {
+  uint64_t wfull[kSmNW], wempty[kSmNW];
+  uint64_t ofull[kSmMaxOp], oempty[kSmMaxOp];
+  uint64_t accfull[2], accempty[2];
+  uint64_t mmadone;
+  uint32_t tmem_base;
+  int flag[4];
+  int fail;
+  unsigned evc;
+  unsigned long long redu[kSmConsumerWarps];
+  int sel[2];
+  int hist[256];
+  int chunk_cnt[kSmConsumers];
+  float inv[kMaxNc];
+  float ssp[kSmConsumerWarps][kMaxNc];   // per-warp partial sums of squares
+  int bcast;
+};
+
+struct SLayer {
+  const uint16_t* w[4];    // qkv, o, gu, down: tile-packed f16 (qp_weights.cu)
+  const float* attn_norm; const float* q_norm; const float* k_norm; const float* ffn_norm;
+};
+
+struct SParams {
+  int d, qw, kvw, F, V, th, L, n_q, n_kv, n_steps, q0_vocab;
+  float eps;
+  const uint16_t* w_proj; const float* b_proj; const uint16_t* e0;
+  SLayer layer[kMaxLayers];
+  const float* out_norm;
+  const uint16_t* embed[kMaxSteps];
+  const uint16_t* w_head[kMaxSteps];
+  const float2* rope_cs;
+  // scratch (rows: 2B at step 1, B later)
+  float* x;                // residual stream [row][d]
+  uint16_t* a_o;           // attention output, f16 [row][q_width]
+  float* acc_qkv;          // [row][q_width + 2 kv_width], scaled by the row's RMS
+  float* acc_gu;           // [row][2 ffn]: gate then up, scaled by the row's RMS
+  float* logits;           // [frame][vocab]
+  uint16_t* kv;            // f16 [layer][frame][pos][k|v][kv_width]
+  int Bmax;                // frame stride of the KV cache
+  // per-call synchronisation (zeroed before the launch)
+  unsigned* done;          // [gemm]: units finished
+  unsigned* qkv_tile;      // [step][layer][128-row tile of q|k|v]: K slices finished
+  unsigned* att;           // [step][layer]: attention items finished
+  unsigned* prep;          // [step]: input rows finished
+  unsigned* decided;       // [step][frame]: sampled code + 1
+  int* abort_flag; int* status;
+  int NGEMM, NHT;
+  int op_slot_bytes, n_op;      // operand ring: slot size for the call's widest N, slot count
+  unsigned long long* trace; int trace_n;
+  // the call
+  int B; const float* H; const int32_t* q0; int32_t* out_codes; float* out_logits; const int32_t* forced;
+  float temperature; int top_k; const float* gumbel;
+};
+
+// One GEMM of the program: n_mt tiles of 128 weight rows x n_ks slices of K.
+struct SG {
+  int kind, k, l, R, N, n_mt, n_ks, ld;
+  bool scaled;
+  const uint16_t* w; float* out;
+};
+__device__ __forceinline__ int sgi_of(const SParams& p, int k, int l, int t) { return 1 + (k - 1) * (4 * p.L + 1) + 4 * l + t; }
+__device__ __forceinline__ int sgi_head(const SParams& p, int k) { return 1 + (k - 1) * (4 * p.L + 1) + 4 * p.L; }
+__device__ __forceinline__ int sm_cols(int R) { return (R + 15) & ~15; }
+
+__device__ SG sgemm(const SParams& p, int gi) {
+  SG g;
+  g.scaled = false;
+  if (gi == 0) {
+    g.kind = S_PROJ; g.k = 1; g.l = 0; g.R = 2 * p.B; g.n_mt = p.d / kTileM; g.n_ks = p.th / kKs;
+    g.w = p.w_proj; g.out = p.x; g.ld = p.d;
+  } else {
+    const int j = gi - 1, per = 4 * p.L + 1, r = j % per;
+    g.k = j / per + 1;
+    g.R = g.k == 1 ? 2 * p.B : p.B;
+    if (r == 4 * p.L) {
+      g.kind = S_HEAD; g.l = p.L - 1; g.R = p.B; g.n_mt = p.V / kTileM; g.n_ks = p.d / kKs;
+      g.w = p.w_head[g.k - 1]; g.out = p.logits; g.ld = p.V; g.scaled = true;
+    } else {
+      g.l = r / 4;
+      const SLayer& L = p.layer[g.l];
+      switch (r % 4) {
+        case 0: g.kind = S_QKV; g.n_mt = (p.qw + 2 * p.kvw) / kTileM; g.n_ks = p.d / kKs; g.w = L.w[0];
+                g.out = p.acc_qkv; g.ld = p.qw + 2 * p.kvw; g.scaled = true; break;
+        case 1: g.kind = S_O; g.n_mt = p.d / kTileM; g.n_ks = p.qw / kKs; g.w = L.w[1]; g.out = p.x; g.ld = p.d; break;
+        case 2: g.kind = S_GU; g.n_mt = 2 * p.F / kTileM; g.n_ks = p.d / kKs; g.w = L.w[2];
+                g.out = p.acc_gu; g.ld = 2 * p.F; g.scaled = true; break;
+        default: g.kind = S_DOWN; g.n_mt = p.d / kTileM; g.n_ks = p.F / kKs; g.w = L.w[3]; g.out = p.x; g.ld = p.d; break;
+      }
+    }
+  }
+  g.N = sm_cols(g.R);
+  return g;
+}
+
+// This CTA's contiguous run [beg, end) of a GEMM's units, ordered (tile, K
+// slice); the runs rotate with the GEMM index so that the CTAs with the
+// larger share change from one GEMM to the next.
+__device__ __forceinline__ void sm_run(const SG& g, int gi, int& beg, int& end) {
+  const int G = gridDim.x, c = int((unsigned(blockIdx.x) + unsigned(gi) * 37u) % unsigned(G));
+  const int total = g.n_mt * g.n_ks;
+  beg = int((long long)total * c / G);
+  end = int((long long)total * (c + 1) / G);
+}
+
+// sync-region accessors
+__device__ __forceinline__ unsigned* sm_done(const SParams& p, int gi) { return p.done + gi; }
+__device__ __forceinline__ unsigned* sm_qkv_tile(const SParams& p, int k, int l, int t) {
+  return p.qkv_tile + (size_t(k - 1) * p.L + l) * p.NHT + t;
+}
+__device__ __forceinline__ unsigned* sm_att(const SParams& p, int k, int l) { return p.att + (k - 1) * p.L + l; }
+__device__ __forceinline__ unsigned* sm_prep(const SParams& p, int k) { return p.prep + (k - 1); }
+
+// The counter a GEMM's operand depends on and the value that completes it.
+__device__ void sm_ready(const SParams& p, int gi, const unsigned*& ctr, unsigned& want) {
+  const SG g = sgemm(p, gi);
+  auto all_of = [&](int gp) { const SG q = sgemm(p, gp); ctr = sm_done(p, gp); want = unsigned(q.n_mt * q.n_ks); };
+  switch (g.kind) {
+    case S_PROJ: ctr = sm_prep(p, 1); want = unsigned(2 * p.B); return;
+    case S_QKV:
+      if (g.l > 0) { all_of(gi - 1); return; }          // the previous layer's down projection
+      if (g.k == 1) { all_of(0); return; }              // the input projection
+      ctr = sm_prep(p, g.k); want = unsigned(p.B); return;   // the step's input rows
+    case S_O: ctr = sm_att(p, g.k, g.l); want = unsigned(p.B * p.n_kv); return;
+    default: all_of(gi - 1); return;                     // GU: O; DOWN: GU; HEAD: the last DOWN
+  }
+}
+
+// ------------------------------------------------------------ tracing
+// Section stamps [section][cta][start, end], then a per-CTA event log:
+// consumer events in [0, 8192), MMA-warp events in [8192, 16384); one word =
+// (globaltimer ns mod 2^48) << 16 | code << 12 | gemm.
+enum {
+  SEV_READY = 1, SEV_BUILT = 2, SEV_COMMIT = 3,   // consumers: readiness seen, operands built; MMA: segment committed
+  SEV_ACC = 4, SEV_PUBLISHED = 6,                 // consumers: accumulator seen, units released
+  SEV_ATT_READY = 8, SEV_ATT_DONE = 9,            // attention warp, per item
+  SEV_WEIGHTS = 10, SEV_ISSUE = 11,               // MMA: waited for a weight slice; producer: copy issued
+  SEV_WEIGHTS_READY = 12                          // MMA: the weight slice was already there
+};
+__device__ __forceinline__ unsigned long long* sm_ev_base(const SParams& p) {
+  return p.trace ? p.trace + size_t(p.trace_n) * gridDim.x * 2 + size_t(blockIdx.x) * 16384 : nullptr;
+}
+__device__ __forceinline__ unsigned long long sm_ev_word(int code, int gi) {
+  return ((globaltimer_ns() & 0xFFFFFFFFFFFFull) << 16) | (unsigned long long)(code & 15) << 12 | unsigned(gi & 4095);
+}
+__device__ __forceinline__ void sm_ev_mma(const SParams& p, unsigned& idx, int code, int gi) {
+  unsigned long long* b = sm_ev_base(p);
+  if (b && idx < 8192) b[8192 + idx++] = sm_ev_word(code, gi);
+}
+__device__ __forceinline__ void sm_ev(const SParams& p, unsigned* cnt, int code, int gi) {
+  unsigned long long* b = sm_ev_base(p);
+  if (b) {
+    const unsigned i = atomicAdd(cnt, 1u);
+    if (i < 8192) b[i] = sm_ev_word(code, gi);
+  }
+}
+__device__ __forceinline__ void sm_trace_mark(const SParams& p, int sec, int which) {
+  if (p.trace && threadIdx.x == 0 && sec < p.trace_n)
+    p.trace[(size_t(sec) * gridDim.x + blockIdx.x) * 2 + which] = globaltimer_ns();
+}
+
+// ---------------------------------------------------------------- producer
+// Streams the weight slices of this CTA's units, in program order, through
+// the ring; it depends on nothing, so it runs ahead by the ring's depth.
+__device__ void sm_producer(const SParams& p, SMisc& ms, uint8_t* smem) {
+  const uint64_t pol = policy_evict_first();
+  uint32_t it = 0;
+  for (int gi = 0; gi < p.NGEMM; ++gi) {
+    const SG g = sgemm(p, gi);
+    int beg, end;
+    sm_run(g, gi, beg, end);
+    for (int s = beg; s < end; ++s) {
+      const uint32_t slot = it % kSmNW, u = it / kSmNW;
+      if (u > 0 && !mwait(p, &ms.wempty[slot], (u - 1) & 1)) goto drain;
+      sm_ev(p, &ms.evc, SEV_ISSUE, gi);
+      mbar_expect_tx(&ms.wfull[slot], kSmWSlot);
+      // tile mt, slice ks of the tile-packed matrix: one contiguous 32 KB run
+      bulk_g2s_stream(smem + kSmOffW + slot * kSmWSlot, reinterpret_cast<const uint8_t*>(g.w) + size_t(s) * kSmWSlot,
+                      kSmWSlot, &ms.wfull[slot], pol);
+      ++it;
+    }
+  }
+drain:
+  for (uint32_t k = it > uint32_t(kSmNW) ? it - kSmNW : 0; k < it; ++k) mbar_wait(&ms.wfull[k % kSmNW], (k / kSmNW) & 1);
+}
+
+// --------------------------------------------------------------- MMA warp
+// Per unit: the weight slice (A, 128 rows) and the operand slice the
+// consumers built (B, N rows), 8 MMAs of K = 16 into the accumulator of the
+// unit's segment (a run of consecutive K slices of one tile).
+__device__ void sm_mma(const SParams& p, SMisc& ms, uint8_t* smem) {
+  uint32_t wit = 0, oit = 0, seg = 0;
+  unsigned evi = 0;
+  const uint32_t nop = uint32_t(p.n_op);
+  for (int gi = 0; gi < p.NGEMM; ++gi) {
+    const SG g = sgemm(p, gi);
+    int beg, end;
+    sm_run(g, gi, beg, end);
+    const uint32_t idesc = idesc_f16(kTileM, g.N);
+    const uint32_t blb = uint32_t(g.N / 8) * 128;   // operand K-direction core-matrix stride
+    for (int s = beg; s < end; ++s) {
+      const int ks = s % g.n_ks;
+      const bool first = s == beg || ks == 0;
+      const bool last = s == end - 1 || ks == g.n_ks - 1;
+      const uint32_t ws = wit % kSmNW, os = oit % nop, tb = seg & 1;
+      if (mbar_try_wait(&ms.wfull[ws], (wit / kSmNW) & 1)) {
+        sm_ev_mma(p, evi, SEV_WEIGHTS_READY, gi);
+      } else {
+        if (!mwait(p, &ms.wfull[ws], (wit / kSmNW) & 1)) goto out;
+        sm_ev_mma(p, evi, SEV_WEIGHTS, gi);
+      }
+      if (!mwait(p, &ms.ofull[os], (oit / nop) & 1)) goto out;
+      if (first && seg >= 2 && !mwait(p, &ms.accempty[tb], ((seg >> 1) - 1) & 1)) goto out;
+      tc_fence_after();
+      {
+        const uint32_t a0 = smem_u32(smem + kSmOffW + ws * kSmWSlot);
+        const uint32_t b0 = smem_u32(smem + kSmOffOp + os * uint32_t(p.op_slot_bytes));
+        const uint32_t d = ms.tmem_base + tb * 128;
+#pragma unroll
+        for (int j = 0; j < kKs / 16; ++j) {
+          const uint64_t ad = smem_desc(a0 + uint32_t(j) * 2 * (kTileM / 8) * 128, (kTileM / 8) * 128, 128);
+          const uint64_t bd = smem_desc(b0 + uint32_t(j) * 2 * blb, blb, 128);
+          mma_f16(d, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
+        }
+      }
+      mma_commit(&ms.wempty[ws]);
+      mma_commit(&ms.oempty[os]);
+      if (last) {
+        mma_commit(&ms.accfull[tb]);
+        sm_ev_mma(p, evi, SEV_COMMIT, gi);
+        ++seg;
+      }
+      ++wit;
+      ++oit;
+    }
+  }
+out:
+  // every MMA retires before TMEM and shared memory are released
+  mma_commit(&ms.mmadone);
+  mbar_wait(&ms.mmadone, 0);
+}
+
+// ------------------------------------------------------ consumer helpers
+__device__ __forceinline__ void ld8f(const float* src, float (&v)[8]) {
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(src)), b = __ldcg(reinterpret_cast<const float4*>(src + 4));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ uint4 pack8h(const float (&v)[8]) {
+  const uint2 a = pack4_f16(v[0], v[1], v[2], v[3]), b = pack4_f16(v[4], v[5], v[6], v[7]);
+  return make_uint4(a.x, a.y, b.x, b.y);
+}
+
+// The operand slices of units u0 .. u0+nu-1 (K slice u % n_ks: columns
+// ks*128 .. +127) for the GEMM's R activation rows, each written to its ring
+// slot as the K-major core-matrix image [16 k groups][N/8 row groups][8 rows]
+// [8 k] of f16 (all consumer threads; one thread per 8 consecutive columns
+// of a row, so global reads coalesce, and every unit's loads in one pass).
+__device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, uint32_t oit, uint8_t* smem) {
+  const int n8 = g.N / 8, per = g.R * 16;
+  const uint32_t nop = uint32_t(p.n_op);
+  for (int it = threadIdx.x; it < nu * per; it += kSmConsumers) {
+    const int ui = it / per, rem = it - ui * per;
+    const int n = rem >> 4, k8 = rem & 15, k = ((u0 + ui) % g.n_ks) * kKs + k8 * 8;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(smem + kSmOffOp + ((oit + ui) % nop) * uint32_t(p.op_slot_bytes));
+    uint4 h;
+    if (g.kind == S_O) {
+      h = __ldcg(reinterpret_cast<const uint4*>(p.a_o + size_t(n) * p.qw + k));
+    } else {
+      float v[8];
+      if (g.kind == S_PROJ) {
+        // rows 2b, 2b+1: the Talker state H_b and the embedding of q0_b,
+        // the first two positions of frame b ("Qwen3-TTS Technical Report",
+        // section 2.3)
+        const int b = n >> 1;
+        if ((n & 1) == 0) {
+          const float4 a = __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k));
+          const float4 c = __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k + 4));
+          v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
+        } else {
+          int q = p.q0[b];
+          q = q < 0 ? 0 : (q >= p.q0_vocab ? p.q0_vocab - 1 : q);   // reported by the step-1 input pass
+          const uint4 e = __ldg(reinterpret_cast<const uint4*>(p.e0 + size_t(q) * p.th + k));
+          const uint32_t w[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) { v[2 * i] = bf16_bits_to_f32(w[i] & 0xffff); v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16); }
+        }
+      } else if (g.kind == S_DOWN) {
+        float u[8];
+        ld8f(p.acc_gu + size_t(n) * 2 * p.F + k, v);
+        ld8f(p.acc_gu + size_t(n) * 2 * p.F + p.F + k, u);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = silu_f(v[i]) * u[i];
+      } else {
+        // x * w_norm of an RMS-normalised input; the row scale is applied to
+        // the GEMM's partial products instead
+        const float* wn;
+        int row = n;
+        if (g.kind == S_QKV) wn = p.layer[g.l].attn_norm;
+        else if (g.kind == S_GU) wn = p.layer[g.l].ffn_norm;
+        else { wn = p.out_norm; row = g.k == 1 ? 2 * n + 1 : n; }   // head: each frame's last position
+        float w[8];
+        ld8f(p.x + size_t(row) * p.d + k, v);
+        ld8f(wn + k, w);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] *= w[i];
+      }
+      h = pack8h(v);
+    }
+    *reinterpret_cast<uint4*>(dst + (size_t(k8 * n8 + (n >> 3)) << 6) + ((n & 7) << 3)) = h;
+  }
+}
+
+// inv[n] = 1 / RMS of the GEMM's input row n, from the complete residual row
+// (all consumer threads: each thread sums its columns of eight rows at a
+// time with all eight loads in flight, the warps' partials meet in shared
+// memory).  The caller's next barrier publishes ms.inv.
+__device__ void sm_inv(const SParams& p, const SG& g, SMisc& ms) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nc = p.d / 4;
+  for (int r0 = 0; r0 < g.R; r0 += 8) {
+    float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int c = t; c < nc; c += kSmConsumers) {
+      float4 a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int n = r0 + u, row = (g.kind == S_HEAD && g.k == 1) ? 2 * n + 1 : n;
+        a[u] = n < g.R ? __ldcg(reinterpret_cast<const float4*>(p.x + size_t(row) * p.d) + c)
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) s8[u] += a[u].x * a[u].x + a[u].y * a[u].y + a[u].z * a[u].z + a[u].w * a[u].w;
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const float v = warp_sum(s8[u]);
+      if (lane == 0 && r0 + u < g.R) ms.ssp[warp][r0 + u] = v;
+    }
+  }
+  named_bar(SBAR_CONS, kSmConsumers);
+  if (t < g.R) {
+    float ss = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSmConsumerWarps; ++w) ss += ms.ssp[w][t];
+    ms.inv[t] = rsqrtf(ss / float(p.d) + p.eps);
+  }
+}
+
+// Add one segment's accumulator (tile mt, nsl K slices) into the GEMM's
+// destination, scaled by the rows' inv for a normalised input.  Each warp
+// drains 32 accumulator rows (output features) x 8 columns (activation rows)
+// at a time, transposes them through its 1 KB of shared memory and adds 4
+// consecutive features per thread with one vector reduction.
+__device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g, int gi, int mt, int nsl,
+                         uint32_t& seg, bool publish) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const uint32_t tb = seg & 1;
+  if (t == 0) ms.flag[1] = mwait(p, &ms.accfull[tb], (seg >> 1) & 1);
+  named_bar(SBAR_CONS, kSmConsumers);
+  if (!ms.flag[1]) return false;
+  if (t == 0) sm_ev(p, &ms.evc, SEV_ACC, gi);
+  tc_fence_after();
+  const int quarter = warp & 3, half = warp >> 2, cols = g.N / 2;
+  const int m0 = mt * kTileM + quarter * 32;
+  float* tp = reinterpret_cast<float*>(smem + kSmOffKeys) + warp * 256;   // [8 rows][32 features]
+  for (int col = half * cols; col < (half + 1) * cols && col < g.R; col += 8) {   // warp-uniform bounds
+    float v[8];
+    tmem_ld8(ms.tmem_base + tb * 128 + (uint32_t(quarter * 32) << 16) + uint32_t(col), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tp[i * 32 + lane] = v[i];
+    __syncwarp();
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int f = pass * 4 + (lane >> 3), k4 = (lane & 7) * 4, n = col + f;
+      if (n < g.R) {
+        float4 x = *reinterpret_cast<const float4*>(tp + f * 32 + k4);
+        if (g.scaled) {
+          const float s = ms.inv[n];
+          x.x *= s; x.y *= s; x.z *= s; x.w *= s;
+        }
+        red_add_v4_f32(g.out + size_t(n) * g.ld + m0 + k4, x);
+      }
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&ms.accempty[tb]);
+  ++seg;
+  if (publish) {
+    named_bar(SBAR_CONS, kSmConsumers);
+    if (t == 0) {
+      // release: the bar.sync above orders every consumer thread's reductions first
+      if (g.kind == S_QKV) red_release_add(sm_qkv_tile(p, g.k, g.l, mt), unsigned(nsl));
+      red_release_add(sm_done(p, gi), unsigned(nsl));
+      sm_ev(p, &ms.evc, SEV_PUBLISHED, gi);
+    }
+  }
+  return true;
+}
+
+// This CTA's units of GEMM gi (all consumer threads): wait for the operand's
+// source, build the operand slices, drain the accumulators.
+//
+// When the whole run fits in the operand ring (the usual case) every unit is
+// built in one pass, so the MMAs of all segments start together, and the
+// drained segments are released with one counter update.  Otherwise each
+// segment is built and then the previous one drained, so that a segment's
+// MMAs wait only for drains two segments back, which precede the builds they
+// follow, and the ring's waits are for MMAs of units built earlier: neither
+// can wait on work that comes later in this order.
+__device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint32_t& seg, uint32_t& oit) {
+  const SG g = sgemm(p, gi);
+  int beg, end;
+  sm_run(g, gi, beg, end);
+  if (beg >= end) return true;
+  const int t = threadIdx.x;
+  if (t == 0) {
+    const unsigned* ctr;
+    unsigned want;
+    sm_ready(p, gi, ctr, want);
+    ms.flag[2] = poll_geq(p, ctr, want);
+  }
+  named_bar(SBAR_CONS, kSmConsumers);
+  if (!ms.flag[2]) return false;
+  if (t == 0) sm_ev(p, &ms.evc, SEV_READY, gi);
+  const uint32_t nop = uint32_t(p.n_op);
+  // builds units [u, u_end) in passes of at most one ring
+  auto build = [&](int u, int u_end) -> bool {
+    while (u < u_end) {
+      const int nu = min(u_end - u, int(nop));
+      if (t == 0) {
+        // a slot is free once the MMAs of the unit that used it last completed
+        bool ok = true;
+        for (int i = 0; i < nu && ok; ++i) {
+          const uint32_t o = oit + uint32_t(i);
+          if (o >= nop) ok = mwait(p, &ms.oempty[o % nop], ((o / nop) - 1) & 1);
+        }
+        ms.flag[3] = ok;
+      }
+      named_bar(SBAR_CONS, kSmConsumers);
+      if (!ms.flag[3]) return false;
+      sm_build(p, g, u, nu, oit, smem);
+      fence_proxy_async_shared();   // the tensor cores read what these generic stores wrote
+      named_bar(SBAR_CONS, kSmConsumers);
+      if (t == 0)
+        for (int i = 0; i < nu; ++i) mbar_arrive(&ms.ofull[(oit + uint32_t(i)) % nop]);
+      oit += uint32_t(nu);
+      u += nu;
+    }
+    if (t == 0) sm_ev(p, &ms.evc, SEV_BUILT, gi);
+    return true;
+  };
+  auto scale = [&]() {
+    if (g.scaled) {
+      sm_inv(p, g, ms);
+      named_bar(SBAR_CONS, kSmConsumers);
+    }
+  };
+  if (end - beg <= int(nop)) {
+    if (!build(beg, end)) return false;
+    scale();
+    for (int s = beg; s < end;) {
+      const int ks0 = s % g.n_ks, seg_end = min(end, s + (g.n_ks - ks0));
+      if (!sm_drain(p, ms, smem, g, gi, s / g.n_ks, seg_end - s, seg, false)) return false;
+      s = seg_end;
+    }
+    named_bar(SBAR_CONS, kSmConsumers);
+    if (t == 0) {
+      // release: the bar.sync above orders every consumer thread's reductions first
+      if (g.kind == S_QKV)
+        for (int s = beg; s < end;) {
+          const int ks0 = s % g.n_ks, seg_end = min(end, s + (g.n_ks - ks0));
+          red_release_add(sm_qkv_tile(p, g.k, g.l, s / g.n_ks), unsigned(seg_end - s));
+          s = seg_end;
+        }
+      red_release_add(sm_done(p, gi), unsigned(end - beg));
+      sm_ev(p, &ms.evc, SEV_PUBLISHED, gi);
+    }
+    return true;
+  }
+  int s = beg, si = 0, prev_mt = -1, prev_nsl = 0;
+  while (s < end) {
+    const int ks0 = s % g.n_ks, mt = s / g.n_ks;
+    const int seg_end = min(end, s + (g.n_ks - ks0)), nsl = seg_end - s;
+    if (!build(s, seg_end)) return false;
+    if (si == 0) scale();
+    if (si > 0 && !sm_drain(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true)) return false;
+    prev_mt = mt;
+    prev_nsl = nsl;
+    ++si;
+    s = seg_end;
+  }
+  return sm_drain(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true);
+}
+
+// Step-1 setup, one warp per row r < 2B: the residual row starts at the
+// projection bias (the projection's partials are added to it); the q|k|v
+// accumulator row and the frame's logit row start at zero; out-of-range
+// first codes are reported.
+__device__ bool sm_prep1(const SParams& p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = gridDim.x;
+  const int qkvw = p.qw + 2 * p.kvw;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r = blockIdx.x + warp * G; r < 2 * p.B; r += kSmConsumerWarps * G) {
+    for (int f = lane * 4; f < p.d; f += 128)
+      *reinterpret_cast<float4*>(p.x + size_t(r) * p.d + f) = *reinterpret_cast<const float4*>(p.b_proj + f);
+    for (int f = lane * 4; f < qkvw; f += 128) *reinterpret_cast<float4*>(p.acc_qkv + size_t(r) * qkvw + f) = z4;
+    if (r < p.B)
+      for (int f = lane * 4; f < p.V; f += 128) *reinterpret_cast<float4*>(p.logits + size_t(r) * p.V + f) = z4;
+    if ((r & 1) && lane == 0) {
+      const int q = p.q0[r >> 1];
+      if (q < 0 || q >= p.q0_vocab) set_status(p.status, QP_ERR_BAD_TOKEN);
+    }
+    __syncwarp();
+    if (lane == 0) red_release_add(sm_prep(p, 1), 1u);
+  }
+  return true;
+}
+
+// The code of step `step` for frame b, computed by the whole CTA (all
+// consumer threads; the same value, or -1 if the grid aborted, in every
+// thread).  Greedy: the argmax of the frame's complete logit row (lowest
+// index on ties), which is copied out if asked and zeroed for the next
+// step's accumulation.  Sampling: the decision the sampling pass published.
+__device__ int sm_code(const SParams& p, SMisc& ms, int step, int b) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  if (p.temperature > 0.f) {
+    if (t == 0) {
+      unsigned* dp = p.decided + size_t(step - 1) * p.B + b;
+      ms.bcast = poll_geq(p, dp, 1u) ? int(ld_acquire_u32(dp)) - 1 : -1;
+    }
+    named_bar(SBAR_CONS, kSmConsumers);
+    const int code = ms.bcast;
+    named_bar(SBAR_CONS, kSmConsumers);
+    return code;
+  }
+  if (t == 0) {
+    const SG h = sgemm(p, sgi_head(p, step));
+    ms.bcast = poll_geq(p, sm_done(p, sgi_head(p, step)), unsigned(h.n_mt * h.n_ks)) ? 0 : -1;
+  }
+  named_bar(SBAR_CONS, kSmConsumers);
+  if (ms.bcast < 0) return -1;
+  float* row = p.logits + size_t(b) * p.V;
+  float* dst = p.out_logits ? p.out_logits + (size_t(b) * p.n_steps + (step - 1)) * p.V : nullptr;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  unsigned long long best = 0ull;
+  for (int f0 = t * 4; f0 < p.V; f0 += 2 * 4 * kSmConsumers) {
+    float4 v[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int f = f0 + i * 4 * kSmConsumers;
+      v[i] = f < p.V ? __ldcg(reinterpret_cast<const float4*>(row + f)) : z4;
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int f = f0 + i * 4 * kSmConsumers;
+      if (f >= p.V) continue;
+      if (dst) *reinterpret_cast<float4*>(dst + f) = v[i];
+      *reinterpret_cast<float4*>(row + f) = z4;
+      unsigned long long c = pack_argmax(v[i].x, f);
+      const unsigned long long c1 = pack_argmax(v[i].y, f + 1), c2 = pack_argmax(v[i].z, f + 2),
+                               c3 = pack_argmax(v[i].w, f + 3);
+      c = c1 > c ? c1 : c;
+      c = c2 > c ? c2 : c;
+      c = c3 > c ? c3 : c;
+      best = c > best ? c : best;
+    }
+  }
+  best = warp_max_u64(best);
+  if (lane == 0) ms.redu[warp] = best;
+  named_bar(SBAR_CONS, kSmConsumers);
+  unsigned long long v = ms.redu[0];
+#pragma unroll
+  for (int i = 1; i < kSmConsumerWarps; ++i) v = ms.redu[i] > v ? ms.redu[i] : v;
+  named_bar(SBAR_CONS, kSmConsumers);   // ms.redu and ms.bcast are reused
+  return unpack_argmax_index(v);
+}
+
+// Step k >= 2 inputs, one frame per CTA: report the previous step's code,
+// embed the next input (teacher-forced if asked) as residual row b.
+__device__ bool sm_prepk(const SParams& p, SMisc& ms, int k) {
+  const int t = threadIdx.x, G = gridDim.x;
+  for (int b = (blockIdx.x + k * 11) % G; b < p.B; b += G) {
+    const int code = sm_code(p, ms, k - 1, b);
+    if (code < 0) return false;
+    if (t == 0) {
+      p.out_codes[size_t(b) * p.n_steps + (k - 2)] = code;
+      int nc = p.forced ? p.forced[size_t(b) * p.n_steps + (k - 2)] : code;
+      if (nc < 0 || nc >= p.V) {
+        set_status(p.status, QP_ERR_BAD_TOKEN);
+        nc = nc < 0 ? 0 : p.V - 1;
+      }
+      ms.bcast = nc;
+    }
+    named_bar(SBAR_CONS, kSmConsumers);
+    const uint16_t* e = p.embed[k - 2] + size_t(ms.bcast) * p.d;
+    for (int f = t * 4; f < p.d; f += 4 * kSmConsumers) {
+      const uint2 ev = *reinterpret_cast<const uint2*>(e + f);
+      *reinterpret_cast<float4*>(p.x + size_t(b) * p.d + f) =
+          make_float4(bf16_bits_to_f32(ev.x & 0xffff), bf16_bits_to_f32(ev.x >> 16), bf16_bits_to_f32(ev.y & 0xffff),
+                      bf16_bits_to_f32(ev.y >> 16));
+    }
+    named_bar(SBAR_CONS, kSmConsumers);
+    if (t == 0) red_release_add(sm_prep(p, k), 1u);
+  }
+  return true;
+}
+
+__device__ bool sm_final(const SParams& p, SMisc& ms) {
+  const int G = gridDim.x;
+  for (int b = (blockIdx.x + 5) % G; b < p.B; b += G) {
+    const int code = sm_code(p, ms, p.n_steps, b);
+    if (code < 0) return false;
+    if (threadIdx.x == 0) p.out_codes[size_t(b) * p.n_steps + (p.n_steps - 1)] = code;
+  }
+  return true;
+}
+
+// Attention of one (frame, kv head) per warp at layer l of step k: per-head
+// RMSNorm and RoPE of the new position(s), KV append, causal softmax over
+// positions 0..pos for the group's q heads, output into the O operand rows.
+// Lane l holds dims 4l..4l+3 of every 128-vector; the scores of two q heads x
+// 16 positions are 32 partial dot products per lane, summed across the warp
+// by one reduce-scatter that leaves score (head l/16, position l%16) in lane
+// l.  The item then zeroes what it read of the q|k|v accumulator and its
+// share of the frame's gate|up accumulator rows, which this layer's GEMMs
+// accumulate into next.
+__device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = gridDim.x;
+  const int P = k == 1 ? 2 : 1, pos0 = k == 1 ? 0 : k;
+  const int gi_q = sgi_of(p, k, l, 0);
+  const int qkvw = p.qw + 2 * p.kvw, grp = p.n_q / p.n_kv, ctx = p.n_steps + 1;
+  const SLayer& L = p.layer[l];
+  const int n_items = p.B * p.n_kv;
+  const unsigned slices = unsigned(p.d / kKs);
+  const int guw = ((2 * p.F + p.n_kv - 1) / p.n_kv + 3) & ~3;   // gate|up columns zeroed per item
+  const float scale = rsqrtf(float(kHeadDim));
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  uint16_t* kvl = p.kv + size_t(l) * p.Bmax * ctx * 2 * p.kvw;
+  for (int i = (blockIdx.x + gi_q * 13) % G + warp * G; i < n_items; i += kSmConsumerWarps * G) {
+    const int b = i / p.n_kv, j = i % p.n_kv, r0 = b * P;
+    // the group's q head tiles, its k tile and its v tile: one lane polls each
+    int okl = 1;
+    if (lane < grp + 2) {
+      const int tile = lane < grp ? j * grp + lane : (lane == grp ? p.qw / kHeadDim + j : (p.qw + p.kvw) / kHeadDim + j);
+      okl = poll_geq(p, sm_qkv_tile(p, k, l, tile), slices);
+    }
+    if (!__all_sync(0xffffffffu, okl)) return false;
+    __syncwarp();   // every lane's reads follow the acquires
+    if (lane == 0) sm_ev(p, &ms.evc, SEV_ATT_READY, gi_q);
+    uint16_t* kvb = kvl + size_t(b) * ctx * 2 * p.kvw + j * kHeadDim + lane * 4;   // + (pos*2 + {0,1}) * kvw
+    for (int pp = 0; pp < P; ++pp) {
+      const int r = r0 + pp, pos = pos0 + pp;
+      float* row = p.acc_qkv + size_t(r) * qkvw;
+      float* kr = row + p.qw + j * kHeadDim + lane * 4;
+      float* vr = row + p.qw + p.kvw + j * kHeadDim + lane * 4;
+      // independent loads first: new k, v, the first two q heads, then the cache
+      const float4 kraw = __ldcg(reinterpret_cast<const float4*>(kr));
+      const float4 vnew = __ldcg(reinterpret_cast<const float4*>(vr));
+      float4 qraw[2];
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh)
+        qraw[hh] = hh < grp ? __ldcg(reinterpret_cast<const float4*>(row + (j * grp + hh) * kHeadDim + lane * 4)) : z4;
+      uint2 kh[kMaxCtx], vh[kMaxCtx];
+#pragma unroll
+      for (int t = 0; t < kMaxCtx; ++t) {
+        kh[t] = t < pos ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 0) * p.kvw)) : make_uint2(0, 0);
+        vh[t] = t < pos ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 1) * p.kvw)) : make_uint2(0, 0);
+      }
+      const float4 knew = norm_rope(kraw, L.k_norm, p.eps, p.rope_cs + pos * 64, lane);
+      *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = pack4_f16(knew.x, knew.y, knew.z, knew.w);
+      *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 1) * p.kvw) = pack4_f16(vnew.x, vnew.y, vnew.z, vnew.w);
+      *reinterpret_cast<float4*>(kr) = z4;
+      *reinterpret_cast<float4*>(vr) = z4;
+      for (int g0 = 0; g0 < grp; g0 += 2) {
+        const int nh = min(2, grp - g0);
+        float4 qn[2];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          qn[hh] = z4;
+          if (hh < nh) {
+            float* qr = row + (j * grp + g0 + hh) * kHeadDim + lane * 4;
+            const float4 q = g0 == 0 ? qraw[hh] : __ldcg(reinterpret_cast<const float4*>(qr));
+            qn[hh] = norm_rope(q, L.q_norm, p.eps, p.rope_cs + pos * 64, lane);
+            *reinterpret_cast<float4*>(qr) = z4;
+          }
+        }
+        float part[32];
+#pragma unroll
+        for (int t = 0; t < kMaxCtx; ++t) {
+          const float4 kk = t < pos ? unpack4_f16(kh[t]) : (t == pos ? knew : z4);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh)
+            part[hh * 16 + t] = qn[hh].x * kk.x + qn[hh].y * kk.y + qn[hh].z * kk.z + qn[hh].w * kk.w;
+        }
+        const bool valid = (lane >> 4) < nh && (lane & 15) <= pos;
+        const float rsum = reduce_scatter32(part, lane);   // all 32 lanes take part
+        const float sc = valid ? rsum * scale : -INFINITY;
+        float mx = sc;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        const float e = valid ? expf(sc - mx) : 0.f;
+        float den = e;
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+        const float pr = den > 0.f ? e / den : 0.f;
+        float4 o2[2] = {z4, z4};
+#pragma unroll
+        for (int t = 0; t < kMaxCtx; ++t) {
+          const float4 vv = t < pos ? unpack4_f16(vh[t]) : (t == pos ? vnew : z4);
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const float w = __shfl_sync(0xffffffffu, pr, hh * 16 + t);
+            o2[hh].x += w * vv.x; o2[hh].y += w * vv.y; o2[hh].z += w * vv.z; o2[hh].w += w * vv.w;
+          }
+        }
+        for (int hh = 0; hh < nh; ++hh)
+          *reinterpret_cast<uint2*>(p.a_o + size_t(r) * p.qw + (j * grp + g0 + hh) * kHeadDim + lane * 4) =
+              pack4_f16(o2[hh].x, o2[hh].y, o2[hh].z, o2[hh].w);
+      }
+      for (int f = j * guw + lane * 4; f < min(2 * p.F, (j + 1) * guw); f += 128)
+        *reinterpret_cast<float4*>(p.acc_gu + size_t(r) * 2 * p.F + f) = z4;
+      __syncwarp();   // the next position of this frame reads what was stored here
+    }
+    __syncwarp();
+    if (lane == 0) {
+      red_release_add(sm_att(p, k, l), 1u);
+      sm_ev(p, &ms.evc, SEV_ATT_DONE, gi_q);
+    }
+  }
+  return true;
+}
+
+// Gumbel top-k decisions of step k, one frame per CTA pass (all consumers):
+// radix select of the k-th largest logit / T, then the argmax of
+// logit / T + g over the kept set (ties at the threshold kept lowest index
+// first).  The logit row is copied out if asked and zeroed for the next step.
+__device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
+  const int V = p.V, t = threadIdx.x, lane = t & 31, w = t >> 5, G = gridDim.x;
+  const float T = p.temperature;
+  const SG h = sgemm(p, sgi_head(p, k));
+  for (int b = (blockIdx.x + k * 7) % G; b < p.B; b += G) {
+    if (t == 0) ms.flag[3] = poll_geq(p, sm_done(p, sgi_head(p, k)), unsigned(h.n_mt * h.n_ks));
+    named_bar(SBAR_CONS, kSmConsumers);
+    if (!ms.flag[3]) return false;
+    float* l = p.logits + size_t(b) * V;
+    for (int i = t; i < V; i += kSmConsumers) keys[i] = f32_order_key(__ldcg(l + i) / T);
+    uint32_t prefix = 0, mask = 0;
+    int remaining = p.top_k;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      ms.hist[t] = 0;
+      named_bar(SBAR_CONS, kSmConsumers);
+      for (int i = t; i < V; i += kSmConsumers) {
+        const uint32_t kk = keys[i];
+        if ((kk & mask) == prefix) atomicAdd(&ms.hist[(kk >> shift) & 255], 1);
+      }
+      named_bar(SBAR_CONS, kSmConsumers);
+      if (t == 0) {
+        int cum = 0, sel = 0;
+        for (int dg = 255; dg >= 0; --dg) {
+          if (cum + ms.hist[dg] >= remaining) { sel = dg; break; }
+          cum += ms.hist[dg];
+        }
+        ms.sel[0] = sel;
+        ms.sel[1] = remaining - cum;
+      }
+      named_bar(SBAR_CONS, kSmConsumers);
+      prefix |= uint32_t(ms.sel[0]) << shift;
+      mask |= 255u << shift;
+      remaining = ms.sel[1];
+      named_bar(SBAR_CONS, kSmConsumers);
+    }
+    const uint32_t kth = prefix;
+    const int per = (V + kSmConsumers - 1) / kSmConsumers, lo = t * per, hi = min(V, lo + per);
+    int cnt = 0;
+    for (int i = lo; i < hi; ++i) cnt += keys[i] == kth;
+    ms.chunk_cnt[t] = cnt;
+    named_bar(SBAR_CONS, kSmConsumers);
+    if (t == 0) {
+      int run = 0;
+      for (int i = 0; i < kSmConsumers; ++i) { const int cc = ms.chunk_cnt[i]; ms.chunk_cnt[i] = run; run += cc; }
+    }
+    named_bar(SBAR_CONS, kSmConsumers);
+    int eq_rank = ms.chunk_cnt[t];
+    const float* gb = p.gumbel + (size_t(b) * p.n_steps + (k - 1)) * V;
+    unsigned long long best = 0ull;
+    for (int i = lo; i < hi; ++i) {
+      const uint32_t kk = keys[i];
+      bool in = kk > kth;
+      if (kk == kth) { in = eq_rank < remaining; ++eq_rank; }
+      if (in) {
+        const unsigned long long pk = pack_argmax(__ldcg(l + i) / T + gb[i], i);
+        best = pk > best ? pk : best;
+      }
+    }
+    best = warp_max_u64(best);
+    if (lane == 0) ms.redu[w] = best;
+    named_bar(SBAR_CONS, kSmConsumers);
+    float* dst = p.out_logits ? p.out_logits + (size_t(b) * p.n_steps + (k - 1)) * V : nullptr;
+    for (int i = t; i < V; i += kSmConsumers) {
+      if (dst) dst[i] = __ldcg(l + i);
+      l[i] = 0.f;
+    }
+    named_bar(SBAR_CONS, kSmConsumers);
+    if (t == 0) {
+      unsigned long long v = ms.redu[0];
+      for (int i = 1; i < kSmConsumerWarps; ++i) v = ms.redu[i] > v ? ms.redu[i] : v;
+      __threadfence();
+      atomicExch(p.decided + size_t(k - 1) * p.B + b, unsigned(unpack_argmax_index(v) + 1));
+    }
+    named_bar(SBAR_CONS, kSmConsumers);   // keys and ms.redu are reused by the next frame
+  }
+  return true;
+}
+
+__device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
+  uint32_t seg = 0, oit = 0;
+  int sec = 0;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kSmOffKeys);
+  // A section ends with one consumer-wide barrier; a failed wait in any warp
+  // makes every consumer warp leave there together.
+#define SM_SECTION(expr)                      \
+  {                                           \
+    sm_trace_mark(p, sec, 0);                 \
+    const bool ok_ = (expr);                  \
+    if (!ok_) ms.fail = 1;                    \
+    named_bar(SBAR_CONS, kSmConsumers);       \
+    sm_trace_mark(p, sec, 1);                 \
+    ++sec;                                    \
+    if (ms.fail) return;                      \
+  }
+  SM_SECTION(sm_prep1(p));
+  SM_SECTION(sm_gemm(p, ms, smem, 0, seg, oit));
+  for (int k = 1; k <= p.n_steps; ++k) {
+    if (k > 1) SM_SECTION(sm_prepk(p, ms, k));
+    for (int l = 0; l < p.L; ++l) {
+      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 0), seg, oit));
+      SM_SECTION(sm_attn(p, ms, k, l));
+      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 1), seg, oit));
+      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 2), seg, oit));
+      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 3), seg, oit));
+    }
+    SM_SECTION(sm_gemm(p, ms, smem, sgi_head(p, k), seg, oit));
+    if (p.temperature > 0.f) SM_SECTION(sm_decide(p, ms, keys, k));
+  }
+  SM_SECTION(sm_final(p, ms));
+#undef SM_SECTION
+}
+
+__global__ void __launch_bounds__(kSmThreads, 1) k_frames_small(const SParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  SMisc& ms = *reinterpret_cast<SMisc*>(smem + kSmOffMisc);
+  const int t = threadIdx.x, warp = t >> 5;
+  if (t == 0) {
+    for (int i = 0; i < kSmNW; ++i) { mbar_init(&ms.wfull[i], 1); mbar_init(&ms.wempty[i], 1); }
+    for (int i = 0; i < kSmMaxOp; ++i) { mbar_init(&ms.ofull[i], 1); mbar_init(&ms.oempty[i], 1); }
+    for (int i = 0; i < 2; ++i) { mbar_init(&ms.accfull[i], 1); mbar_init(&ms.accempty[i], kSmConsumerWarps); }
+    mbar_init(&ms.mmadone, 1);
+    ms.fail = 0;
+    ms.evc = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(&ms.tmem_base, kSmTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+
+  if (warp < kSmConsumerWarps) {
+    sm_consumer(p, ms, smem);
+  } else if (warp == kSmProducerWarp) {
+    if ((t & 31) == 0) sm_producer(p, ms, smem);
+    __syncwarp();
+  } else if (warp == kSmMmaWarp) {
+    if ((t & 31) == 0) sm_mma(p, ms, smem);
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(ms.tmem_base, kSmTmemCols);
+}
+
+// ----------------------------------------------------------------- host
+size_t sm_al256(size_t b) { return (b + 255) & ~size_t(255); }
+
+struct SmSync {
+  size_t done, qkv_tile, att, prep, decided, abort_flag, total;
+  int NGEMM, NHT;
+};
+
+SmSync sm_sync_layout(const qp_geometry& g, int B) {
+  SmSync S{};
+  S.NGEMM = 1 + g.n_steps * (4 * g.layers + 1);
+  S.NHT = g.n_q_heads + 2 * g.n_kv_heads;   // 128-row tiles of q|k|v (head_dim 128)
+  const size_t steps = size_t(g.n_steps);
+  size_t o = 0;
+  S.done = o;       o += sm_al256(size_t(S.NGEMM) * 4);
+  S.qkv_tile = o;   o += sm_al256(steps * g.layers * S.NHT * 4);
+  S.att = o;        o += sm_al256(steps * g.layers * 4);
+  S.prep = o;       o += sm_al256(steps * 4);
+  S.decided = o;    o += sm_al256(steps * B * 4);
+  S.abort_flag = o; o += 256;
+  S.total = o;
+  return S;
+}
+
+void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, uint8_t* sync,
+             const SmSync& S, int bmax) {
+  const qp_geometry& g = h->g;
+  p.d = g.hidden; p.qw = g.n_q_heads * kHeadDim; p.kvw = g.n_kv_heads * kHeadDim; p.F = g.ffn; p.V = g.vocab;
+  p.th = g.talker_hidden; p.L = g.layers; p.n_q = g.n_q_heads; p.n_kv = g.n_kv_heads; p.n_steps = g.n_steps;
+  p.q0_vocab = g.q0_vocab; p.eps = g.rms_eps;
+  p.w_proj = reinterpret_cast<const uint16_t*>(h->proj.w); p.b_proj = h->b_proj; p.e0 = h->e0;
+  for (int l = 0; l < g.layers; ++l) {
+    const LayerW& Lw = h->layer[l];
+    p.layer[l].w[0] = reinterpret_cast<const uint16_t*>(Lw.qkv.w);
+    p.layer[l].w[1] = reinterpret_cast<const uint16_t*>(Lw.o.w);
+    p.layer[l].w[2] = reinterpret_cast<const uint16_t*>(Lw.gu.w);
+    p.layer[l].w[3] = reinterpret_cast<const uint16_t*>(Lw.down.w);
+    p.layer[l].attn_norm = Lw.attn_norm; p.layer[l].q_norm = Lw.q_norm;
+    p.layer[l].k_norm = Lw.k_norm; p.layer[l].ffn_norm = Lw.ffn_norm;
+  }
+  p.out_norm = h->out_norm;
+  for (int j = 0; j < g.n_steps; ++j) {
+    p.embed[j] = h->embed[j];
+    p.w_head[j] = reinterpret_cast<const uint16_t*>(h->head[j].w);
+  }
+  p.rope_cs = h->rope_cs;
+  // the tile engine's buffers, each at least as large as this schedule needs
+  p.x = reinterpret_cast<float*>(scratch + L.x1);
+  p.a_o = reinterpret_cast<uint16_t*>(scratch + L.a1[2]);
+  p.acc_qkv = reinterpret_cast<float*>(scratch + L.acc1_qkv);
+  p.acc_gu = reinterpret_cast<float*>(scratch + L.acc1_gu);
+  p.logits = reinterpret_cast<float*>(scratch + L.logits);
+  p.kv = reinterpret_cast<uint16_t*>(scratch + L.kv);
+  p.Bmax = bmax;
+  p.done = reinterpret_cast<unsigned*>(sync + S.done);
+  p.qkv_tile = reinterpret_cast<unsigned*>(sync + S.qkv_tile);
+  p.att = reinterpret_cast<unsigned*>(sync + S.att);
+  p.prep = reinterpret_cast<unsigned*>(sync + S.prep);
+  p.decided = reinterpret_cast<unsigned*>(sync + S.decided);
+  p.abort_flag = reinterpret_cast<int*>(sync + S.abort_flag);
+  p.status = h->status;
+  p.NGEMM = S.NGEMM; p.NHT = S.NHT;
+  // operand slots sized for the widest GEMM of the call (2B rows at step 1)
+  p.op_slot_bytes = ((2 * a.B + 15) / 16 * 16) * kKs * 2;
+  p.n_op = int(kSmOpBytes / uint32_t(p.op_slot_bytes));
+  if (p.n_op > kSmMaxOp) p.n_op = kSmMaxOp;
+  p.trace = h->trace; p.trace_n = h->trace_phases;
+  p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;
+  p.temperature = a.temperature; p.top_k = a.top_k; p.gumbel = a.gumbel;
+}
+
+constexpr int kSmMaxDevices = 64;
+bool g_sm_attr[kSmMaxDevices] = {};
+
+}  // namespace
+
+size_t small_smem_bytes() { return kSmOffMisc + sizeof(SMisc) + 1024; }
+
+bool small_supported(const qp_handle* h, const RunArgs& a) {
+  if (h->wfmt != WF_BF16) return false;
+  if (a.B < 1 || a.B > kSmallMaxFrames) return false;
+  if (a.temperature > 0.f && h->g.vocab > kMaxVocab) return false;
+  return true;
+}
+
+qp_status run_frames_small(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
+                           cudaStream_t s) {
+  if (!small_supported(h, a) || a.B > bmax) return QP_ERR_ARG;
+  const SmSync S = sm_sync_layout(h->g, a.B);
+  if (L.total - L.sync < S.total) return QP_ERR_ARG;
+  uint8_t* sync = scratch + L.sync;
+  SParams p{};
+  sm_fill(p, h, a, scratch, L, sync, S, bmax);
+  const int dev = h->device;
+  bool local = false;
+  bool* attr = dev >= 0 && dev < kSmMaxDevices ? &g_sm_attr[dev] : &local;
+  if (!*attr) {
+    if (cudaFuncSetAttribute(k_frames_small, cudaFuncAttributeMaxDynamicSharedMemorySize, int(small_smem_bytes())) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return QP_ERR_CUDA;
+    }
+    *attr = true;
+  }
+  if (cudaMemsetAsync(sync, 0, S.total, s) != cudaSuccess) {
+    cudaGetLastError();
+    return QP_ERR_CUDA;
+  }
+  void* args[] = {&p};
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_frames_small), dim3(h->num_sms), dim3(kSmThreads), args,
+                                  small_smem_bytes(), s) != cudaSuccess) {
+    cudaGetLastError();
+    return QP_ERR_CUDA;
+  }
+  return QP_OK;
+}
+
+}  // namespace qp

@@ -1,5 +1,6 @@
 /*
- * qp_debug.h -- phase tracing of libqp's persistent kernel (profiling aid).
+ * qp_debug.h -- engine selection and phase tracing of libqp's persistent
+ * kernels (profiling and testing aids; not part of the method).
  *
  * With tracing on, thread 0 of every CTA stamps the GPU global timer (ns)
  * when its consumer warps start and finish each section of the program (the
@@ -18,6 +19,26 @@
 #ifdef __cplusplus
 extern "C" {
 #endif
+
+/* The frame loop has two schedules of the same computation, both splitting
+ * every weight matrix into (128-row tile, 128-column K slice) units spread
+ * over all SMs.  The tile engine serves any batch and both weight formats: a
+ * completed tile is finished (residual, norm, SwiGLU, f16 operand) once by
+ * the CTA whose partial completed it.  The small-batch engine serves bf16
+ * weights with at most 64 frames per call: partials go straight into their
+ * destination and each consumer builds its operand slice from it, which
+ * removes one dependent global round trip per GEMM.  QP_ENGINE_AUTO (the
+ * default) takes the small-batch engine wherever it can serve a call. */
+typedef enum {
+  QP_ENGINE_AUTO = 0,
+  QP_ENGINE_TILE = 1,
+  QP_ENGINE_SMALL = 2
+} qp_engine;
+
+/* Select the engine for later calls on h.  With QP_ENGINE_SMALL a call the
+ * small-batch engine cannot serve (Q8_0 weights, more than 64 frames)
+ * returns QP_ERR_ARG.  QP_ERR_ARG for a null handle or an unknown engine. */
+qp_status qp_set_engine(qp_handle* h, int engine);
 
 /* enable != 0: allocate a device buffer for up to 8192 sections x the SM count
  * and record every later call into it (each call overwrites the last);
