@@ -95,8 +95,8 @@ size_t matrix_bytes(int fmt, int64_t N, int64_t K) {
 qp_status run(qp_handle* h, const qp::RunArgs& a, cudaStream_t s) {
   const bool sm = qp::small_supported(h, a);
   if (h->engine == QP_ENGINE_SMALL && !sm) return QP_ERR_ARG;
-  if (sm && h->engine != QP_ENGINE_TILE)
-    return qp::run_frames_small(h, a, static_cast<uint8_t*>(h->sarena), h->scr, h->max_batch, s);
+  const bool pick = h->engine == QP_ENGINE_SMALL || (h->engine == QP_ENGINE_AUTO && a.B <= qp::kSmallAutoFrames);
+  if (sm && pick) return qp::run_frames_small(h, a, static_cast<uint8_t*>(h->sarena), h->scr, h->max_batch, s);
   return qp::run_frames_persistent(h, a, s);
 }
 

@@ -1233,7 +1233,8 @@ qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   ga.temperature = 0.f; ga.top_k = 0; ga.gumbel = nullptr;
   const bool sm = small_supported(h, ga);
   if (h->engine == QP_ENGINE_SMALL && !sm) return QP_ERR_ARG;
-  if (sm && h->engine != QP_ENGINE_TILE) return run_frames_small(h, ga, base, L, a.B, s);
+  const bool pick = h->engine == QP_ENGINE_SMALL || (h->engine == QP_ENGINE_AUTO && a.B <= kSmallAutoFrames);
+  if (sm && pick) return run_frames_small(h, ga, base, L, a.B, s);
   PParams p{};
   fill_params(p, h, ga, base, L, base + L.sync, S, a.B);
   // the launch zeroes the synchronisation words and accumulators; every

@@ -353,9 +353,11 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, uint32_t
         if (g.kind == S_QKV) wn = p.layer[g.l].attn_norm;
         else if (g.kind == S_GU) wn = p.layer[g.l].ffn_norm;
         else { wn = p.out_norm; row = g.k == 1 ? 2 * n + 1 : n; }   // head: each frame's last position
-        float w[8];
+        // both loads in flight together
+        const float4 w0 = __ldg(reinterpret_cast<const float4*>(wn + k));
+        const float4 w1 = __ldg(reinterpret_cast<const float4*>(wn + k + 4));
         ld8f(p.x + size_t(row) * p.d + k, v);
-        ld8f(wn + k, w);
+        const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] *= w[i];
       }
@@ -477,17 +479,19 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
   named_bar(SBAR_CONS, kSmConsumers);
   if (!ms.flag[2]) return false;
   if (t == 0) sm_ev(p, &ms.evc, SEV_READY, gi);
-  const uint32_t nop = uint32_t(p.n_op);
+  const uint32_t nop = uint32_t(p.n_op), oit0 = oit;
   // builds units [u, u_end) in passes of at most one ring
   auto build = [&](int u, int u_end) -> bool {
     while (u < u_end) {
       const int nu = min(u_end - u, int(nop));
       if (t == 0) {
-        // a slot is free once the MMAs of the unit that used it last completed
+        // A slot is free once the MMAs of the unit that used it last have
+        // completed.  For a unit of an earlier GEMM that is already known:
+        // this CTA drained its accumulator, which the MMAs' commit gates.
         bool ok = true;
         for (int i = 0; i < nu && ok; ++i) {
           const uint32_t o = oit + uint32_t(i);
-          if (o >= nop) ok = mwait(p, &ms.oempty[o % nop], ((o / nop) - 1) & 1);
+          if (o >= nop && o - nop >= oit0) ok = mwait(p, &ms.oempty[o % nop], ((o / nop) - 1) & 1);
         }
         ms.flag[3] = ok;
       }
