@@ -219,6 +219,28 @@ def roofline_of(g, B, gemm_format, sampling, ms_per_call, hbm, tf):
     return {"bound": bound, "achieved": ach, "peak": peak, "unit": unit, "frac": ach / peak}
 
 
+def whole_job(local_ms: float, frames_per_step: int, steps: int, world: int, device=None):
+    """The job's time and throughput over all ranks: each rank timed its own
+    `steps` calls of `frames_per_step` frames (weak scaling, no collective on
+    the data path); the job took as long as the slowest rank, and processed
+    every rank's frames.  With world > 1 the max is taken with one all_reduce
+    on `device` (the rank's GPU under NCCL, the CPU under gloo)."""
+    total_ms = float(local_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms, world * frames_per_step * steps / (total_ms / 1e3)
+
+
+def engine_of(B: int, gemm_format: str) -> str:
+    """The schedule QP_ENGINE_AUTO picks (include/qp_debug.h): the small-batch
+    engine for bf16 calls of at most 16 frames, the tile engine otherwise."""
+    return "small" if gemm_format == "bf16" and B <= 16 else "tile"
+
+
 def sweep(g, dev, stream, steps, hbm, tf):
     """Every batch configuration once more: ms per call, frames/s, us/step
     and roofline fraction (each call a full 15-step loop, L2 flushed)."""
@@ -255,7 +277,8 @@ def sweep(g, dev, stream, steps, hbm, tf):
         st = cp.device_status()
         cp.close()
         roof = roofline_of(g, w.B, w.gemm_format, samp is not None, ms, hbm, tf)
-        out[w.name] = {"B": w.B, "ms_per_call": ms, "frames_per_s": w.B / (ms / 1e3),
+        out[w.name] = {"B": w.B, "engine": engine_of(w.B, w.gemm_format), "ms_per_call": ms,
+                       "frames_per_s": w.B / (ms / 1e3),
                        "us_per_step": 1e3 * ms / g.n_steps, "roofline_bound": roof["bound"],
                        "roofline_frac": roof["frac"], "device_status": st}
     return out
@@ -329,13 +352,8 @@ def main():
     if world > 1:
         dist.barrier()
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms, value = whole_job(sum(step_ms), B, args.steps, world, dev if world > 1 else None)
     ms_per_step = total_ms / args.steps
-    value = world * B * args.steps / (total_ms / 1e3)
     launches = cp.launches_per_call(B, samp is not None) * args.steps
 
     # end to end through the host-buffer entry point: pinned H/q0 in, codes out
@@ -379,7 +397,7 @@ def main():
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.gemm_format == "bf16" else "q8_0",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": B, "steps_per_frame": g.n_steps,
+        "config": {"workload": w.name, "B": B, "steps_per_frame": g.n_steps, "engine": engine_of(B, w.gemm_format),
                    "l2": f"flushed between timed iterations ({L2_FLUSH_BYTES >> 20} MB write)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "us_per_step": 1e3 * ms_per_step / g.n_steps,
