@@ -211,10 +211,19 @@ __device__ GI gemm_inst(const PParams& p, int gi) {
 
 // This CTA's contiguous run [beg, end) of a GEMM's slices.  Slices are
 // ordered (chunk, 128-row tile, K slice); runs rotate with the GEMM index.
-__device__ __forceinline__ void my_run(int total, int gi, int& beg, int& end) {
+// The GEMM's slices are ordered (chunk, 128-row tile, K slice) and cut into
+// pieces: each tile's K range is split into S parts, S = the fewest that
+// still gives every CTA a piece (1 once the tiles outnumber the CTAs), so a
+// tile's partial sums pass through the f32 accumulator as few times as the
+// grid allows.  This CTA takes a contiguous run of pieces -- a contiguous
+// run [beg, end) of slices -- rotated with the GEMM index.
+__device__ __forceinline__ void my_run(int tiles, int n_ks, int gi, int& beg, int& end) {
   const int G = gridDim.x, g = (blockIdx.x + gi * 37) % G;
-  beg = int((long long)total * g / G);
-  end = int((long long)total * (g + 1) / G);
+  const int S = max(1, min(n_ks, G / tiles));
+  const long long P = (long long)tiles * S;
+  const int p0 = int(P * g / G), p1 = int(P * (g + 1) / G);
+  beg = (p0 / S) * n_ks + ((p0 % S) * n_ks) / S;
+  end = (p1 / S) * n_ks + ((p1 % S) * n_ks) / S;
 }
 
 // sync-region accessors
@@ -243,7 +252,7 @@ __device__ void producer_role(const PParams& p, Misc& ms, uint8_t* smem) {
     const GI G = gemm_inst(p, gi);
     const Ck c = chunking(G.R);
     int beg, end;
-    my_run(c.n * G.n_mt * G.n_ks, gi, beg, end);
+    my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
     for (int s = beg; s < end; ++s) {
       const int ks = s % G.n_ks, mt = (s / G.n_ks) % G.n_mt;
       const uint32_t slot = it % nslot, u = it / nslot;
@@ -292,7 +301,7 @@ __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
     const GI G = gemm_inst(p, gi);
     const Ck c = chunking(G.R);
     int beg, end;
-    my_run(c.n * G.n_mt * G.n_ks, gi, beg, end);
+    my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
     for (int s = beg; s < end; ++s, ++it) {
       const uint32_t rs = it % kNSlotQ8, ru = it / kNSlotQ8, ds = it % kNDeq, du = it / kNDeq;
       if (t == 0) {   // the leader waits for every dequant thread, then broadcasts
@@ -348,7 +357,7 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
     const GI G = gemm_inst(p, gi);
     const Ck c = chunking(G.R);
     int beg, end;
-    my_run(c.n * G.n_mt * G.n_ks, gi, beg, end);
+    my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
     const uint32_t idesc = idesc_f16(kTileM, c.Nc);
     const uint32_t abytes = uint32_t(kKs) * c.Nc * 2;
     // Readiness of the run's operand slices: one batch of relaxed loads and a
@@ -800,7 +809,7 @@ __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, ui
   const GI G = gemm_inst(p, gi);
   const Ck c = chunking(G.R);
   int beg, end;
-  my_run(c.n * G.n_mt * G.n_ks, gi, beg, end);
+  my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const bool scaled = G.kind == G_QKV || G.kind == G_GU || G.kind == G_HEAD;
   int s = beg;
