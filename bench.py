@@ -284,6 +284,56 @@ def sweep(g, dev, stream, steps, hbm, tf):
     return out
 
 
+def rvq_rows(dev, stream, steps, hbm):
+    """The RVQ codebook kernels (include/qp_rvq.h) on a codec-sized workload:
+    16 EMA codebooks of 2048 x 512 and 16384 frames' codes.  The codec's
+    codebook width is not on the pages; 512 is this measurement's choice.
+    Roofline: HBM, with the unique bytes each call must move (the decode
+    gathers 16 rows per frame, but from a 64 MB table that stays in L2)."""
+    import numpy as np
+    import torch
+    import codebook_rvq_code_gb300 as qpk
+    Q, K, D, N = 16, 2048, 512, 16384
+    rng = np.random.default_rng(5)
+    usage = torch.from_numpy(rng.uniform(0.0, 50.0, size=(Q, K)).astype(np.float32)).to(dev)
+    es = torch.from_numpy(rng.standard_normal((Q, K, D)).astype(np.float32)).to(dev) * usage[:, :, None]
+    codes = torch.from_numpy(rng.integers(0, K, size=(N, Q), dtype=np.int32)).to(dev)
+    cbs = torch.empty_like(es)
+    out = torch.empty((N, D), dtype=torch.float32, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for i in range(steps):
+            flush.fill_(float(i))
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / steps
+
+    ms_n = timed(lambda: qpk.rvq_normalize(es, usage, out=cbs, stream=stream))
+    ms_d = timed(lambda: qpk.rvq_decode(cbs, codes, out=out, stream=stream))
+    nb = 2 * Q * K * D * 4 + Q * K * 4
+    db = Q * K * D * 4 + N * Q * 4 + N * D * 4
+    return {
+        "rvq_normalize": {"workload": f"{Q} EMA codebooks x {K} x {D} f32", "ms": ms_n,
+                          "roofline": {"bound": "hbm", "achieved": nb / (ms_n / 1e3) / 1e9, "peak": hbm,
+                                       "unit": "GB/s", "frac": nb / (ms_n / 1e3) / 1e9 / hbm, "bytes": nb}},
+        "rvq_decode": {"workload": f"{N} frames x {Q} codes into {K} x {D} f32 codebooks", "ms": ms_d,
+                       "frames_per_s": N / (ms_d / 1e3),
+                       "gathered_GB_per_s": N * Q * D * 4 / (ms_d / 1e3) / 1e9,
+                       "roofline": {"bound": "hbm", "achieved": db / (ms_d / 1e3) / 1e9, "peak": hbm,
+                                    "unit": "GB/s", "frac": db / (ms_d / 1e3) / 1e9 / hbm, "bytes": db}},
+    }
+
+
 # ---------------------------------------------------------------------------
 
 def main():
@@ -409,6 +459,7 @@ def main():
         line["e2e"] = e2e
     if not args.no_sweep and world == 1:
         line["per_config"] = sweep(g, dev, stream, max(5, min(args.steps, 20)), hbm, tf_sust)
+        line["next_rows"] = rvq_rows(dev, stream, max(5, min(args.steps, 20)), hbm)
     if not args.no_cpu_baseline:
         fps, done, el = time_oracle(g, raw, w, min(B, 8), 10.0)
         line["cpu_baseline"] = {"value": fps, "unit": "frames/s", "cores": oracle_threads(), "kind": "oracle",

@@ -27,6 +27,7 @@ EXPORTED = [
     "qp_predict_frames", "qp_predict_frames_ex", "qp_predict_frames_host", "qp_get_device_status",
     "qp_launches_per_call", "qp_destroy", "qp_predict_frames_static",
     "qp_set_engine", "qp_trace_enable", "qp_trace_read",   # include/qp_debug.h
+    "qp_rvq_normalize", "qp_rvq_decode",                   # include/qp_rvq.h
 ]
 
 
@@ -85,6 +86,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qp_trace_enable.argtypes = [vp, i32]
     lib.qp_trace_read.restype = i32
     lib.qp_trace_read.argtypes = [vp, vp, i32, ctypes.POINTER(ctypes.c_int)]
+    lib.qp_rvq_normalize.restype = i32
+    lib.qp_rvq_normalize.argtypes = [vp, vp, i32, i32, i32, vp, vp]
+    lib.qp_rvq_decode.restype = i32
+    lib.qp_rvq_decode.argtypes = [vp, i32, i32, i32, vp, i32, vp, vp, vp]
     return lib
 
 
@@ -125,6 +130,31 @@ def _stream_ptr(stream) -> Optional[int]:
     import torch
     s = stream if stream is not None else torch.cuda.current_stream()
     return int(s.cuda_stream) or None
+
+
+def rvq_normalize(embedding_sum, cluster_usage, out=None, stream=None):
+    """EMA codebooks -> codebooks (include/qp_rvq.h): f32 CUDA tensors
+    [Q, K, D] and [Q, K]; returns the [Q, K, D] codebooks."""
+    import torch
+    Q, K, D = (int(x) for x in embedding_sum.shape)
+    if out is None:
+        out = torch.empty_like(embedding_sum)
+    _check("qp_rvq_normalize", lib().qp_rvq_normalize(_ptr(embedding_sum), _ptr(cluster_usage), Q, K, D, _ptr(out),
+                                                      _stream_ptr(stream)))
+    return out
+
+
+def rvq_decode(codebooks, codes, out=None, status=None, stream=None):
+    """sum_i codebooks[i][codes[:, i]] (include/qp_rvq.h): f32 [Q, K, D] and
+    int32 [N, Q] CUDA tensors; returns the [N, D] sums."""
+    import torch
+    Q, K, D = (int(x) for x in codebooks.shape)
+    N = int(codes.shape[0])
+    if out is None:
+        out = torch.empty((N, D), dtype=torch.float32, device=codebooks.device)
+    _check("qp_rvq_decode", lib().qp_rvq_decode(_ptr(codebooks), Q, K, D, _ptr(codes), N, _ptr(out), _ptr(status),
+                                                _stream_ptr(stream)))
+    return out
 
 
 class CodePredictor:
