@@ -318,11 +318,28 @@ def rvq_rows(dev, stream, steps, hbm):
             tot += a.elapsed_time(b)
         return tot / steps
 
+    # frame-feedback embeddings (qp_code_embeddings) of configuration 5's batch:
+    # 1024 frames x 15 codes, bf16 rows in, f32 rows out
+    import synthetic as S
+    g = S.Geometry()
+    Bf = 1024
+    cp = qpk.CodePredictor(g, max_batch=1)
+    cp.load_raw_weights(S.make_weights(g, seed=0), device=dev)
+    fcodes = torch.from_numpy(rng.integers(0, g.vocab, size=(Bf, g.n_steps), dtype=np.int32)).to(dev)
+    fout = torch.empty((Bf, g.n_steps, g.hidden), dtype=torch.float32, device=dev)
+    ms_f = timed(lambda: cp.code_embeddings(fcodes, out=fout, stream=stream))
+    fst = cp.device_status()
+    cp.close()
+    fb = Bf * g.n_steps * (g.hidden * 2 + g.hidden * 4 + 4)
     ms_n = timed(lambda: qpk.rvq_normalize(es, usage, out=cbs, stream=stream))
     ms_d = timed(lambda: qpk.rvq_decode(cbs, codes, out=out, stream=stream))
     nb = 2 * Q * K * D * 4 + Q * K * 4
     db = Q * K * D * 4 + N * Q * 4 + N * D * 4
     return {
+        "code_embeddings": {"workload": f"{Bf} frames x {g.n_steps} codes, {g.hidden}-wide bf16 tables -> f32",
+                            "ms": ms_f, "frames_per_s": Bf / (ms_f / 1e3), "device_status": fst,
+                            "roofline": {"bound": "hbm", "achieved": fb / (ms_f / 1e3) / 1e9, "peak": hbm,
+                                         "unit": "GB/s", "frac": fb / (ms_f / 1e3) / 1e9 / hbm, "bytes": fb}},
         "rvq_normalize": {"workload": f"{Q} EMA codebooks x {K} x {D} f32", "ms": ms_n,
                           "roofline": {"bound": "hbm", "achieved": nb / (ms_n / 1e3) / 1e9, "peak": hbm,
                                        "unit": "GB/s", "frac": nb / (ms_n / 1e3) / 1e9 / hbm, "bytes": nb}},

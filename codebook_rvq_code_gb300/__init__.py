@@ -25,7 +25,7 @@ DTYPES = {"bf16": 0, "f16": 1, "f32": 2, "q8_0": 3}
 EXPORTED = [
     "qp_abi_version", "qp_status_string", "qp_default_geometry", "qp_create", "qp_load_weights",
     "qp_predict_frames", "qp_predict_frames_ex", "qp_predict_frames_host", "qp_get_device_status",
-    "qp_launches_per_call", "qp_destroy", "qp_predict_frames_static",
+    "qp_launches_per_call", "qp_destroy", "qp_predict_frames_static", "qp_code_embeddings",
     "qp_set_engine", "qp_trace_enable", "qp_trace_read",   # include/qp_debug.h
     "qp_rvq_normalize", "qp_rvq_decode",                   # include/qp_rvq.h
 ]
@@ -78,6 +78,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qp_get_device_status.argtypes = [vp, vp]
     lib.qp_launches_per_call.restype = i32
     lib.qp_launches_per_call.argtypes = [vp, i32, i32]
+    lib.qp_code_embeddings.restype = i32
+    lib.qp_code_embeddings.argtypes = [vp, i32, vp, vp, vp]
     lib.qp_destroy.restype = None
     lib.qp_destroy.argtypes = [vp]
     lib.qp_set_engine.restype = i32
@@ -242,6 +244,19 @@ class CodePredictor:
         _check("qp_predict_frames_static", self._lib.qp_predict_frames_static(
             self._h, B, _ptr(H), _ptr(q0), _ptr(out_codes), _ptr(out_logits), _stream_ptr(stream)))
         return out_codes
+
+    def code_embeddings(self, codes, out=None, stream=None):
+        """E_j[codes[:, j]] for j < n_steps as f32 [B, n_steps, hidden]
+        (qp_code_embeddings): the frame's residual codes in the predictor's
+        embedding space."""
+        import torch
+        B = int(codes.shape[0])
+        g = self.geometry
+        if out is None:
+            out = torch.empty((B, g.n_steps, g.hidden), dtype=torch.float32, device=codes.device)
+        _check("qp_code_embeddings", self._lib.qp_code_embeddings(self._h, B, _ptr(codes), _ptr(out),
+                                                                  _stream_ptr(stream)))
+        return out
 
     ENGINES = {"auto": 0, "tile": 1, "small": 2}
 

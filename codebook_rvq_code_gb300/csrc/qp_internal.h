@@ -117,6 +117,7 @@ struct qp_handle {
   float* H_stage = nullptr;                     // host-buffer entry point staging
   int32_t* q0_stage = nullptr;
   int32_t* codes_stage = nullptr;
+  const uint16_t** embed_dev = nullptr;         // device copy of embed[] (qp_code_embeddings)
   unsigned long long* trace = nullptr;          // optional phase trace (qp_debug.h)
   int trace_phases = 0;
 
@@ -138,6 +139,10 @@ size_t packed_bytes(int fmt, int N, int K);
 // Pack `rows` rows of a caller matrix [rows, K] (bf16, or a Q8_0 block
 // stream) into rows [row0, row0 + rows) of the packed matrix dst.
 cudaError_t pack_rows(const void* src, int fmt, int rows, int K, const PackedMat& dst, int row0, cudaStream_t s);
+// out[b][j] = tables[j][codes[b][j]] as f32 for b < B, j < n_tables
+// (tables_dev: a device array of n_tables device pointers to [V, d] bf16).
+cudaError_t code_embeddings(const uint16_t* const* tables_dev, int n_tables, int V, int d, const int32_t* codes,
+                            int B, float* out, int* status, cudaStream_t s);
 // out[r] = sum_i E[r, i]^2 (f32) for a [rows, cols] bf16 table.
 cudaError_t row_sumsq_bf16(const uint16_t* E, int rows, int cols, float* out, cudaStream_t s);
 }  // namespace qp

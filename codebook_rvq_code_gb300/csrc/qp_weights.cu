@@ -77,6 +77,28 @@ __global__ void k_row_sumsq(const uint16_t* __restrict__ E, int cols, float* __r
   if (threadIdx.x == 0) out[blockIdx.x] = s;
 }
 
+// out[b][j][:] = E_j[codes[b][j]][:] (bf16 -> f32, exact), 4 values a thread.
+__global__ void k_code_embeddings(const uint16_t* const* __restrict__ tables, int n_tables, int V, int d,
+                                  const int32_t* __restrict__ codes, long long B, float* __restrict__ out,
+                                  int* status) {
+  const int d4 = d / 4;
+  const long long total = B * n_tables * d4;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
+       i += (long long)gridDim.x * blockDim.x) {
+    const long long row = i / d4;                 // b * n_tables + j
+    const int j = int(row % n_tables), c4 = int(i % d4);
+    int code = codes[row];
+    if (code < 0 || code >= V) {
+      if (c4 == 0) set_status(status, QP_ERR_BAD_TOKEN);
+      code = code < 0 ? 0 : V - 1;
+    }
+    const uint2 e = *reinterpret_cast<const uint2*>(tables[j] + size_t(code) * d + c4 * 4);
+    *reinterpret_cast<float4*>(out + row * d + c4 * 4) =
+        make_float4(bf16_bits_to_f32(e.x & 0xffff), bf16_bits_to_f32(e.x >> 16), bf16_bits_to_f32(e.y & 0xffff),
+                    bf16_bits_to_f32(e.y >> 16));
+  }
+}
+
 int grid_for(size_t total) { return int(total / 256 + 1 < 8192 ? total / 256 + 1 : 8192); }
 
 }  // namespace
@@ -94,6 +116,13 @@ cudaError_t pack_rows(const void* src, int fmt, int rows, int K, const PackedMat
     k_pack_q8<<<grid_for(size_t(rows) * (K / 32)), 256, 0, s>>>(static_cast<const uint8_t*>(src), rows, K,
                                                                  reinterpret_cast<int8_t*>(dst.w), dst.scale, row0);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t code_embeddings(const uint16_t* const* tables_dev, int n_tables, int V, int d, const int32_t* codes,
+                            int B, float* out, int* status, cudaStream_t s) {
+  const size_t total = size_t(B) * n_tables * (d / 4);
+  k_code_embeddings<<<grid_for(total), 256, 0, s>>>(tables_dev, n_tables, V, d, codes, B, out, status);
   return cudaGetLastError();
 }
 

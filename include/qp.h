@@ -195,6 +195,20 @@ qp_status qp_get_device_status(qp_handle* h, qp_stream s);
  * arguments enqueues (for launch accounting); -1 on bad arguments. */
 int qp_launches_per_call(qp_handle* h, int B, int sampling);
 
+/* Frame-feedback embeddings: out[b][j] = E_j[codes[b][j]] as f32, for j =
+ * 0 .. n_steps-1, where E_j is the loaded table code_pred.codec_embd.j
+ * (bf16, converted exactly) and codes[b][j] is the frame's code q_{j+1} as
+ * qp_predict_frames returns it ([B][n_steps] int32, device).  These are the
+ * vectors of a frame's residual codes in the predictor's own embedding
+ * space, table n_steps-1 included, which the loop itself never reads
+ * (reading: the pages name the tables but not this use; it is inferred from
+ * table 14's existence, "rightkit-qts 0.2.3", section "Loader contract").
+ * out is [B][n_steps][hidden] f32, device, 16-byte aligned.  A code outside
+ * [0, vocab) is clamped for addressing and latches QP_ERR_BAD_TOKEN in the
+ * device status word.  QP_ERR_STATE if no weights are loaded, QP_ERR_ARG for
+ * B < 0, null or misaligned pointers; B == 0 enqueues nothing. */
+qp_status qp_code_embeddings(qp_handle* h, int B, const int32_t* codes, float* out, qp_stream s);
+
 /* Free everything the handle owns (synchronises the device first). */
 void qp_destroy(qp_handle* h);
 

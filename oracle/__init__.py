@@ -3,7 +3,7 @@
 Only the tests, the smoke check and bench.py's CPU-baseline / reference legs
 may import this package.  It shares no code with the CUDA library.
 """
-from .predictor import (Predictor, attend, bf16_to_f32, dequant_q8_0, forward_sequence,
+from .predictor import (Predictor, attend, bf16_to_f32, code_embeddings, dequant_q8_0, forward_sequence,
                         greedy_code, gumbel_topk_code, predict_frames,
                         predict_frames_bruteforce, quant_q8_0, rms_norm, rope,
                         rope_angles, round_to_f16, sampling_decidable, silu, top2_gap, topk_set,

@@ -403,3 +403,18 @@ def predict_frames_bruteforce(P: Predictor, H: np.ndarray, q0: np.ndarray,
             nxt = forced[:, k - 1] if forced is not None else codes[:, k - 1]
             seq.append(P.embed[k - 1][np.asarray(nxt)].astype(F32))
     return {"codes": codes, "logits": logits}
+
+
+def code_embeddings(P: Predictor, codes: np.ndarray) -> np.ndarray:
+    """Frame-feedback embeddings: out[b, j] = E_j[codes[b, j]] for j < n_steps,
+    where codes[b, j] is the frame's code q_{j+1} and E_j the predictor's
+    code-embedding table j ("rightkit-qts 0.2.3 -- Qwen3-TTS 1.7B -> QTS GGUF",
+    section "Loader contract": code_pred.codec_embd.{0..14}).  The loop reads
+    tables 0..n_steps-2 for its own inputs; table n_steps-1 is included here
+    (reading: the pages name the tables but not their use outside the loop).
+    f32, from the bf16 tables."""
+    codes = np.asarray(codes)
+    out = np.zeros((codes.shape[0], P.g.n_steps, P.g.hidden), dtype=F32)
+    for j in range(P.g.n_steps):
+        out[:, j] = P.embed[j][codes[:, j]]
+    return out

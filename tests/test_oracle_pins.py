@@ -527,3 +527,24 @@ def test_q8_0_operand_rounding_is_nearest_f16():
     assert np.abs(got - exact).max() <= np.abs(exact).max() * 2.0 ** -11
     on_grid = np.float16([0.5, -0.25, 1.5e-3]).astype(np.float32)
     np.testing.assert_array_equal(O.round_to_f16(on_grid), on_grid)
+
+
+def test_code_embeddings_take_table_j_for_code_j():
+    """Table j answers code j: with column 0 of E_j holding j and column 1 the
+    row index c, every output row names its own table and code, so a shifted
+    table or a wrong code column fails."""
+    import dataclasses
+    g = dataclasses.replace(S.TOY, n_steps=5)
+    raw = S.make_weights(g, seed=1)
+    P = O.Predictor.from_raw(g, raw)
+    for j in range(g.n_steps):
+        P.embed[j] = np.zeros_like(P.embed[j])
+        P.embed[j][:, 0] = j
+        P.embed[j][:, 1] = np.arange(P.embed[j].shape[0])
+    rng = np.random.default_rng(2)
+    codes = rng.integers(0, g.vocab, size=(7, g.n_steps))
+    out = O.code_embeddings(P, codes)
+    assert out.shape == (7, g.n_steps, g.hidden)
+    for j in range(g.n_steps):
+        np.testing.assert_array_equal(out[:, j, 0], j)
+        np.testing.assert_array_equal(out[:, j, 1], codes[:, j])
