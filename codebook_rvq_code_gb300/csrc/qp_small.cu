@@ -69,6 +69,8 @@ struct SMisc {
   float inv[kMaxNc];
   float ssp[kSmConsumerWarps][kMaxNc];   // per-warp partial sums of squares
   int bcast;
+  uint32_t ouse[kSmMaxOp];   // consumers (thread 0): fills of each operand slot so far
+  uint32_t ouse_m[kSmMaxOp]; // MMA thread: fills of each operand slot consumed so far
 };
 
 struct SLayer {
@@ -101,7 +103,6 @@ struct SParams {
   unsigned* decided;       // [step][frame]: sampled code + 1
   int* abort_flag; int* status;
   int NGEMM, NHT;
-  int op_slot_bytes, n_op;      // operand ring: slot size for the call's widest N, slot count
   unsigned long long* trace; int trace_n;
   // the call
   int B; const float* H; const int32_t* q0; int32_t* out_codes; float* out_logits; const int32_t* forced;
@@ -146,6 +147,14 @@ __device__ SG sgemm(const SParams& p, int gi) {
   }
   g.N = sm_cols(g.R);
   return g;
+}
+
+// The operand ring of a GEMM: slots of N x 128 f16 (the GEMM's own width),
+// as many as fit the region.  A CTA's unit i of the GEMM uses slot i % n.
+__device__ __forceinline__ uint32_t sm_op_bytes(const SG& g) { return uint32_t(g.N) * kKs * 2; }
+__device__ __forceinline__ uint32_t sm_op_slots(const SG& g) {
+  const uint32_t n = kSmOpBytes / sm_op_bytes(g);
+  return n < uint32_t(kSmMaxOp) ? n : uint32_t(kSmMaxOp);
 }
 
 // This CTA's contiguous run [beg, end) of a GEMM's units, ordered (tile, K
@@ -244,32 +253,33 @@ drain:
 // consumers built (B, N rows), 8 MMAs of K = 16 into the accumulator of the
 // unit's segment (a run of consecutive K slices of one tile).
 __device__ void sm_mma(const SParams& p, SMisc& ms, uint8_t* smem) {
-  uint32_t wit = 0, oit = 0, seg = 0;
+  uint32_t wit = 0, seg = 0;
+  uint32_t* ouse = ms.ouse_m;
   unsigned evi = 0;
-  const uint32_t nop = uint32_t(p.n_op);
   for (int gi = 0; gi < p.NGEMM; ++gi) {
     const SG g = sgemm(p, gi);
     int beg, end;
     sm_run(g, gi, beg, end);
     const uint32_t idesc = idesc_f16(kTileM, g.N);
     const uint32_t blb = uint32_t(g.N / 8) * 128;   // operand K-direction core-matrix stride
+    const uint32_t nop = sm_op_slots(g), obytes = sm_op_bytes(g);
     for (int s = beg; s < end; ++s) {
       const int ks = s % g.n_ks;
       const bool first = s == beg || ks == 0;
       const bool last = s == end - 1 || ks == g.n_ks - 1;
-      const uint32_t ws = wit % kSmNW, os = oit % nop, tb = seg & 1;
+      const uint32_t ws = wit % kSmNW, os = uint32_t(s - beg) % nop, tb = seg & 1;
       if (mbar_try_wait(&ms.wfull[ws], (wit / kSmNW) & 1)) {
         sm_ev_mma(p, evi, SEV_WEIGHTS_READY, gi);
       } else {
         if (!mwait(p, &ms.wfull[ws], (wit / kSmNW) & 1)) goto out;
         sm_ev_mma(p, evi, SEV_WEIGHTS, gi);
       }
-      if (!mwait(p, &ms.ofull[os], (oit / nop) & 1)) goto out;
+      if (!mwait(p, &ms.ofull[os], ouse[os] & 1)) goto out;
       if (first && seg >= 2 && !mwait(p, &ms.accempty[tb], ((seg >> 1) - 1) & 1)) goto out;
       tc_fence_after();
       {
         const uint32_t a0 = smem_u32(smem + kSmOffW + ws * kSmWSlot);
-        const uint32_t b0 = smem_u32(smem + kSmOffOp + os * uint32_t(p.op_slot_bytes));
+        const uint32_t b0 = smem_u32(smem + kSmOffOp + os * obytes);
         const uint32_t d = ms.tmem_base + tb * 128;
 #pragma unroll
         for (int j = 0; j < kKs / 16; ++j) {
@@ -286,7 +296,7 @@ __device__ void sm_mma(const SParams& p, SMisc& ms, uint8_t* smem) {
         ++seg;
       }
       ++wit;
-      ++oit;
+      ++ouse[os];
     }
   }
 out:
@@ -310,13 +320,14 @@ __device__ __forceinline__ uint4 pack8h(const float (&v)[8]) {
 // slot as the K-major core-matrix image [16 k groups][N/8 row groups][8 rows]
 // [8 k] of f16 (all consumer threads; one thread per 8 consecutive columns
 // of a row, so global reads coalesce, and every unit's loads in one pass).
-__device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, uint32_t oit, uint8_t* smem) {
+// i0: the run index of unit u0 (its operand goes to slot (i0 + ui) % slots).
+__device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, uint8_t* smem) {
   const int n8 = g.N / 8, per = g.R * 16;
-  const uint32_t nop = uint32_t(p.n_op);
+  const uint32_t nop = sm_op_slots(g), obytes = sm_op_bytes(g);
   for (int it = threadIdx.x; it < nu * per; it += kSmConsumers) {
     const int ui = it / per, rem = it - ui * per;
     const int n = rem >> 4, k8 = rem & 15, k = ((u0 + ui) % g.n_ks) * kKs + k8 * 8;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(smem + kSmOffOp + ((oit + ui) % nop) * uint32_t(p.op_slot_bytes));
+    uint16_t* dst = reinterpret_cast<uint16_t*>(smem + kSmOffOp + (uint32_t(i0 + ui) % nop) * obytes);
     uint4 h;
     if (g.kind == S_O) {
       h = __ldcg(reinterpret_cast<const uint4*>(p.a_o + size_t(n) * p.qw + k));
@@ -464,7 +475,7 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
 // MMAs wait only for drains two segments back, which precede the builds they
 // follow, and the ring's waits are for MMAs of units built earlier: neither
 // can wait on work that comes later in this order.
-__device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint32_t& seg, uint32_t& oit) {
+__device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint32_t& seg) {
   const SG g = sgemm(p, gi);
   int beg, end;
   sm_run(g, gi, beg, end);
@@ -479,7 +490,7 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
   named_bar(SBAR_CONS, kSmConsumers);
   if (!ms.flag[2]) return false;
   if (t == 0) sm_ev(p, &ms.evc, SEV_READY, gi);
-  const uint32_t nop = uint32_t(p.n_op), oit0 = oit;
+  const uint32_t nop = sm_op_slots(g);
   // builds units [u, u_end) in passes of at most one ring
   auto build = [&](int u, int u_end) -> bool {
     while (u < u_end) {
@@ -488,21 +499,25 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
         // A slot is free once the MMAs of the unit that used it last have
         // completed.  For a unit of an earlier GEMM that is already known:
         // this CTA drained its accumulator, which the MMAs' commit gates.
+        // Within this run, wait for the unit one ring earlier.
         bool ok = true;
         for (int i = 0; i < nu && ok; ++i) {
-          const uint32_t o = oit + uint32_t(i);
-          if (o >= nop && o - nop >= oit0) ok = mwait(p, &ms.oempty[o % nop], ((o / nop) - 1) & 1);
+          const uint32_t ri = uint32_t(u + i - beg), os = ri % nop;
+          if (ri >= nop) ok = mwait(p, &ms.oempty[os], (ms.ouse[os] - 1) & 1);
         }
         ms.flag[3] = ok;
       }
       named_bar(SBAR_CONS, kSmConsumers);
       if (!ms.flag[3]) return false;
-      sm_build(p, g, u, nu, oit, smem);
+      sm_build(p, g, u, nu, u - beg, smem);
       fence_proxy_async_shared();   // the tensor cores read what these generic stores wrote
       named_bar(SBAR_CONS, kSmConsumers);
       if (t == 0)
-        for (int i = 0; i < nu; ++i) mbar_arrive(&ms.ofull[(oit + uint32_t(i)) % nop]);
-      oit += uint32_t(nu);
+        for (int i = 0; i < nu; ++i) {
+          const uint32_t os = uint32_t(u + i - beg) % nop;
+          mbar_arrive(&ms.ofull[os]);
+          ++ms.ouse[os];
+        }
       u += nu;
     }
     if (t == 0) sm_ev(p, &ms.evc, SEV_BUILT, gi);
@@ -872,7 +887,7 @@ __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
 }
 
 __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
-  uint32_t seg = 0, oit = 0;
+  uint32_t seg = 0;
   int sec = 0;
   uint32_t* keys = reinterpret_cast<uint32_t*>(smem + kSmOffKeys);
   // A section ends with one consumer-wide barrier; a failed wait in any warp
@@ -888,17 +903,17 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
     if (ms.fail) return;                      \
   }
   SM_SECTION(sm_prep1(p));
-  SM_SECTION(sm_gemm(p, ms, smem, 0, seg, oit));
+  SM_SECTION(sm_gemm(p, ms, smem, 0, seg));
   for (int k = 1; k <= p.n_steps; ++k) {
     if (k > 1) SM_SECTION(sm_prepk(p, ms, k));
     for (int l = 0; l < p.L; ++l) {
-      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 0), seg, oit));
+      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 0), seg));
       SM_SECTION(sm_attn(p, ms, k, l));
-      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 1), seg, oit));
-      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 2), seg, oit));
-      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 3), seg, oit));
+      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 1), seg));
+      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 2), seg));
+      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 3), seg));
     }
-    SM_SECTION(sm_gemm(p, ms, smem, sgi_head(p, k), seg, oit));
+    SM_SECTION(sm_gemm(p, ms, smem, sgi_head(p, k), seg));
     if (p.temperature > 0.f) SM_SECTION(sm_decide(p, ms, keys, k));
   }
   SM_SECTION(sm_final(p, ms));
@@ -917,6 +932,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) k_frames_small(const SParams p)
     mbar_init(&ms.mmadone, 1);
     ms.fail = 0;
     ms.evc = 0;
+    for (int i = 0; i < kSmMaxOp; ++i) { ms.ouse[i] = 0; ms.ouse_m[i] = 0; }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tmem_alloc(&ms.tmem_base, kSmTmemCols);
@@ -1001,10 +1017,6 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   p.abort_flag = reinterpret_cast<int*>(sync + S.abort_flag);
   p.status = h->status;
   p.NGEMM = S.NGEMM; p.NHT = S.NHT;
-  // operand slots sized for the widest GEMM of the call (2B rows at step 1)
-  p.op_slot_bytes = ((2 * a.B + 15) / 16 * 16) * kKs * 2;
-  p.n_op = int(kSmOpBytes / uint32_t(p.op_slot_bytes));
-  if (p.n_op > kSmMaxOp) p.n_op = kSmMaxOp;
   p.trace = h->trace; p.trace_n = h->trace_phases;
   p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;
   p.temperature = a.temperature; p.top_k = a.top_k; p.gumbel = a.gumbel;
