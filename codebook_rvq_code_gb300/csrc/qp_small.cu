@@ -41,8 +41,8 @@ constexpr int kSmMmaWarp = 9;
 constexpr int kSmThreads = 10 * 32;
 
 constexpr uint32_t kSmWSlot = kTileM * kKs * 2;      // one 128 x 128 f16 weight slice
-constexpr int kSmNW = 5;                             // weight ring slots
-constexpr uint32_t kSmOpBytes = 32768;               // operand slices, 128 K x N rows f16 each
+constexpr int kSmNW = 4;                             // weight ring slots
+constexpr uint32_t kSmOpBytes = 65536;               // operand slices, 128 K x N rows f16 each
 constexpr int kSmMaxOp = 8;
 constexpr uint32_t kSmOffW = 0;
 constexpr uint32_t kSmOffOp = kSmNW * kSmWSlot;
