@@ -79,10 +79,10 @@ size_t sync_bytes(const qp_geometry& g, int B);
 // Largest batch the small-batch engine serves (2B <= 128 activation rows at
 // step 1: one tensor-core N chunk), and the largest it is chosen for
 // automatically: its operand slices are built from f32 sources by every CTA
-// that uses them, which beyond 16 frames costs more per step on GB300 than
-// the tile engine's one finishing pass (measured crossover between 16 and 32).
+// that uses them, which beyond 32 frames costs more per step on GB300 than
+// the tile engine's one finishing pass (measured crossover between 32 and 64).
 constexpr int kSmallMaxFrames = 64;
-constexpr int kSmallAutoFrames = 16;
+constexpr int kSmallAutoFrames = 32;
 
 }  // namespace qp
 

@@ -149,6 +149,10 @@ __device__ SG sgemm(const SParams& p, int gi) {
   return g;
 }
 
+// GEMMs whose input is RMS-normalised (their partials are scaled by the row's 1/RMS)
+template <int KIND>
+constexpr bool kScaled = KIND == S_QKV || KIND == S_GU || KIND == S_HEAD;
+
 // The operand ring of a GEMM: slots of N x 128 f16 (the GEMM's own width),
 // as many as fit the region.  A CTA's unit i of the GEMM uses slot i % n.
 __device__ __forceinline__ uint32_t sm_op_bytes(const SG& g) { return uint32_t(g.N) * kKs * 2; }
@@ -321,6 +325,7 @@ __device__ __forceinline__ uint4 pack8h(const float (&v)[8]) {
 // [8 k] of f16 (all consumer threads; one thread per 8 consecutive columns
 // of a row, so global reads coalesce, and every unit's loads in one pass).
 // i0: the run index of unit u0 (its operand goes to slot (i0 + ui) % slots).
+template <int KIND>
 __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, uint8_t* smem) {
   const int n8 = g.N / 8, per = g.R * 16;
   const uint32_t nop = sm_op_slots(g), obytes = sm_op_bytes(g);
@@ -329,11 +334,11 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
     const int n = rem >> 4, k8 = rem & 15, k = ((u0 + ui) % g.n_ks) * kKs + k8 * 8;
     uint16_t* dst = reinterpret_cast<uint16_t*>(smem + kSmOffOp + (uint32_t(i0 + ui) % nop) * obytes);
     uint4 h;
-    if (g.kind == S_O) {
+    if (KIND == S_O) {
       h = __ldcg(reinterpret_cast<const uint4*>(p.a_o + size_t(n) * p.qw + k));
     } else {
       float v[8];
-      if (g.kind == S_PROJ) {
+      if (KIND == S_PROJ) {
         // rows 2b, 2b+1: the Talker state H_b and the embedding of q0_b,
         // the first two positions of frame b ("Qwen3-TTS Technical Report",
         // section 2.3)
@@ -350,7 +355,7 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
 #pragma unroll
           for (int i = 0; i < 4; ++i) { v[2 * i] = bf16_bits_to_f32(w[i] & 0xffff); v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16); }
         }
-      } else if (g.kind == S_DOWN) {
+      } else if (KIND == S_DOWN) {
         float u[8];
         ld8f(p.acc_gu + size_t(n) * 2 * p.F + k, v);
         ld8f(p.acc_gu + size_t(n) * 2 * p.F + p.F + k, u);
@@ -361,8 +366,8 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
         // the GEMM's partial products instead
         const float* wn;
         int row = n;
-        if (g.kind == S_QKV) wn = p.layer[g.l].attn_norm;
-        else if (g.kind == S_GU) wn = p.layer[g.l].ffn_norm;
+        if (KIND == S_QKV) wn = p.layer[g.l].attn_norm;
+        else if (KIND == S_GU) wn = p.layer[g.l].ffn_norm;
         else { wn = p.out_norm; row = g.k == 1 ? 2 * n + 1 : n; }   // head: each frame's last position
         // both loads in flight together
         const float4 w0 = __ldg(reinterpret_cast<const float4*>(wn + k));
@@ -382,6 +387,7 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
 // (all consumer threads: each thread sums its columns of eight rows at a
 // time with all eight loads in flight, the warps' partials meet in shared
 // memory).  The caller's next barrier publishes ms.inv.
+template <int KIND>
 __device__ void sm_inv(const SParams& p, const SG& g, SMisc& ms) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nc = p.d / 4;
   for (int r0 = 0; r0 < g.R; r0 += 8) {
@@ -390,7 +396,7 @@ __device__ void sm_inv(const SParams& p, const SG& g, SMisc& ms) {
       float4 a[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
-        const int n = r0 + u, row = (g.kind == S_HEAD && g.k == 1) ? 2 * n + 1 : n;
+        const int n = r0 + u, row = (KIND == S_HEAD && g.k == 1) ? 2 * n + 1 : n;
         a[u] = n < g.R ? __ldcg(reinterpret_cast<const float4*>(p.x + size_t(row) * p.d) + c)
                        : make_float4(0.f, 0.f, 0.f, 0.f);
       }
@@ -417,6 +423,7 @@ __device__ void sm_inv(const SParams& p, const SG& g, SMisc& ms) {
 // drains 32 accumulator rows (output features) x 8 columns (activation rows)
 // at a time, transposes them through its 1 KB of shared memory and adds 4
 // consecutive features per thread with one vector reduction.
+template <int KIND>
 __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g, int gi, int mt, int nsl,
                          uint32_t& seg, bool publish) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
@@ -440,7 +447,7 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
       const int f = pass * 4 + (lane >> 3), k4 = (lane & 7) * 4, n = col + f;
       if (n < g.R) {
         float4 x = *reinterpret_cast<const float4*>(tp + f * 32 + k4);
-        if (g.scaled) {
+        if (kScaled<KIND>) {
           const float s = ms.inv[n];
           x.x *= s; x.y *= s; x.z *= s; x.w *= s;
         }
@@ -457,7 +464,7 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
     named_bar(SBAR_CONS, kSmConsumers);
     if (t == 0) {
       // release: the bar.sync above orders every consumer thread's reductions first
-      if (g.kind == S_QKV) red_release_add(sm_qkv_tile(p, g.k, g.l, mt), unsigned(nsl));
+      if (KIND == S_QKV) red_release_add(sm_qkv_tile(p, g.k, g.l, mt), unsigned(nsl));
       red_release_add(sm_done(p, gi), unsigned(nsl));
       sm_ev(p, &ms.evc, SEV_PUBLISHED, gi);
     }
@@ -475,6 +482,7 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
 // MMAs wait only for drains two segments back, which precede the builds they
 // follow, and the ring's waits are for MMAs of units built earlier: neither
 // can wait on work that comes later in this order.
+template <int KIND>
 __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint32_t& seg) {
   const SG g = sgemm(p, gi);
   int beg, end;
@@ -509,7 +517,7 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
       }
       named_bar(SBAR_CONS, kSmConsumers);
       if (!ms.flag[3]) return false;
-      sm_build(p, g, u, nu, u - beg, smem);
+      sm_build<KIND>(p, g, u, nu, u - beg, smem);
       fence_proxy_async_shared();   // the tensor cores read what these generic stores wrote
       named_bar(SBAR_CONS, kSmConsumers);
       if (t == 0)
@@ -524,8 +532,8 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
     return true;
   };
   auto scale = [&]() {
-    if (g.scaled) {
-      sm_inv(p, g, ms);
+    if (kScaled<KIND>) {
+      sm_inv<KIND>(p, g, ms);
       named_bar(SBAR_CONS, kSmConsumers);
     }
   };
@@ -534,13 +542,13 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
     scale();
     for (int s = beg; s < end;) {
       const int ks0 = s % g.n_ks, seg_end = min(end, s + (g.n_ks - ks0));
-      if (!sm_drain(p, ms, smem, g, gi, s / g.n_ks, seg_end - s, seg, false)) return false;
+      if (!sm_drain<KIND>(p, ms, smem, g, gi, s / g.n_ks, seg_end - s, seg, false)) return false;
       s = seg_end;
     }
     named_bar(SBAR_CONS, kSmConsumers);
     if (t == 0) {
       // release: the bar.sync above orders every consumer thread's reductions first
-      if (g.kind == S_QKV)
+      if (KIND == S_QKV)
         for (int s = beg; s < end;) {
           const int ks0 = s % g.n_ks, seg_end = min(end, s + (g.n_ks - ks0));
           red_release_add(sm_qkv_tile(p, g.k, g.l, s / g.n_ks), unsigned(seg_end - s));
@@ -557,13 +565,13 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
     const int seg_end = min(end, s + (g.n_ks - ks0)), nsl = seg_end - s;
     if (!build(s, seg_end)) return false;
     if (si == 0) scale();
-    if (si > 0 && !sm_drain(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true)) return false;
+    if (si > 0 && !sm_drain<KIND>(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true)) return false;
     prev_mt = mt;
     prev_nsl = nsl;
     ++si;
     s = seg_end;
   }
-  return sm_drain(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true);
+  return sm_drain<KIND>(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true);
 }
 
 // Step-1 setup, one warp per row r < 2B: the residual row starts at the
@@ -903,17 +911,17 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
     if (ms.fail) return;                      \
   }
   SM_SECTION(sm_prep1(p));
-  SM_SECTION(sm_gemm(p, ms, smem, 0, seg));
+  SM_SECTION(sm_gemm<S_PROJ>(p, ms, smem, 0, seg));
   for (int k = 1; k <= p.n_steps; ++k) {
     if (k > 1) SM_SECTION(sm_prepk(p, ms, k));
     for (int l = 0; l < p.L; ++l) {
-      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 0), seg));
+      SM_SECTION(sm_gemm<S_QKV>(p, ms, smem, sgi_of(p, k, l, 0), seg));
       SM_SECTION(sm_attn(p, ms, k, l));
-      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 1), seg));
-      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 2), seg));
-      SM_SECTION(sm_gemm(p, ms, smem, sgi_of(p, k, l, 3), seg));
+      SM_SECTION(sm_gemm<S_O>(p, ms, smem, sgi_of(p, k, l, 1), seg));
+      SM_SECTION(sm_gemm<S_GU>(p, ms, smem, sgi_of(p, k, l, 2), seg));
+      SM_SECTION(sm_gemm<S_DOWN>(p, ms, smem, sgi_of(p, k, l, 3), seg));
     }
-    SM_SECTION(sm_gemm(p, ms, smem, sgi_head(p, k), seg));
+    SM_SECTION(sm_gemm<S_HEAD>(p, ms, smem, sgi_head(p, k), seg));
     if (p.temperature > 0.f) SM_SECTION(sm_decide(p, ms, keys, k));
   }
   SM_SECTION(sm_final(p, ms));
