@@ -671,11 +671,12 @@ __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
 // Finishing work of a completed tile, by the CTA whose contribution
 // completed it (all consumer threads).  Each warp takes rows warp, warp + 8,
 // ...; the loads of several of its rows are issued together.
+template <int KIND>
 __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, int ch, int mt, Ck c) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (G.kind == G_QKV) return true;
-  if (G.kind == G_PROJ || G.kind == G_O || G.kind == G_DOWN) {
+  if (KIND == G_QKV) return true;
+  if (KIND == G_PROJ || KIND == G_O || KIND == G_DOWN) {
     const int rows = rows_in(G.R, c, ch);
     const float* X = G.acc;
     const int feat = mt * kTileM + lane * 4;
@@ -683,9 +684,9 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
     int gi_n;
     const float* w;
     uint16_t* act_n;
-    if (G.kind == G_PROJ) {
+    if (KIND == G_PROJ) {
       gi_n = gi_of(p, 1, 0, 0); w = p.layer[0].attn_norm; act_n = p.a1[1];
-    } else if (G.kind == G_O) {
+    } else if (KIND == G_O) {
       gi_n = gi + 1; w = p.layer[G.l].ffn_norm; act_n = G.k == 1 ? p.a1[3] : p.ak[2];
     } else if (G.l + 1 < p.L) {
       gi_n = gi + 1; w = p.layer[G.l + 1].attn_norm; act_n = G.k == 1 ? p.a1[1] : p.ak[0];
@@ -733,7 +734,7 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
     }
     return true;
   }
-  if (G.kind == G_GU) {
+  if (KIND == G_GU) {
     const int nkd = p.F / kTileM, kd = mt % nkd;
     if (t == 0) ms.flag[2] = atom_add_acq_rel(pair_cnt(p, G.k, G.l, ch, kd), 1u) == 1u;
     named_bar(BAR_CONS, kConsumers);
@@ -805,13 +806,14 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
 }
 
 // Drain this CTA's accumulator segments of GEMM gi.
+template <int KIND>
 __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, uint32_t& seg) {
   const GI G = gemm_inst(p, gi);
   const Ck c = chunking(G.R);
   int beg, end;
   my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const bool scaled = G.kind == G_QKV || G.kind == G_GU || G.kind == G_HEAD;
+  const bool scaled = KIND == G_QKV || KIND == G_GU || KIND == G_HEAD;
   int s = beg;
   while (s < end) {
     const int ks = s % G.n_ks, tt = s / G.n_ks, mt = tt % G.n_mt, ch = tt / G.n_mt;
@@ -873,7 +875,7 @@ __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, ui
     }
     named_bar(BAR_CONS, kConsumers);
     if (ms.flag[0]) {
-      if (!last_arriver(p, ms, G, gi, ch, mt, c)) return false;
+      if (!last_arriver<KIND>(p, ms, G, gi, ch, mt, c)) return false;
       if (t == 0) ev_cons(p, &ms.evc, EV_LASTDONE, gi);
     }
     ++seg;
@@ -978,17 +980,17 @@ __device__ void consumer_role(const PParams& p, Misc& ms, uint8_t* smem) {
     if (ms.fail) return;                      \
   }
   QP_SECTION(prep1_items(p));
-  QP_SECTION(epilogues(p, ms, keys, 0, seg));
+  QP_SECTION(epilogues<G_PROJ>(p, ms, keys, 0, seg));
   for (int k = 1; k <= p.n_steps; ++k) {
     if (k > 1) QP_SECTION(prepk_items(p, k));
     for (int l = 0; l < p.L; ++l) {
-      QP_SECTION(epilogues(p, ms, keys, gi_of(p, k, l, 0), seg));
+      QP_SECTION(epilogues<G_QKV>(p, ms, keys, gi_of(p, k, l, 0), seg));
       QP_SECTION(attn_items(p, ms, k, l));
-      QP_SECTION(epilogues(p, ms, keys, gi_of(p, k, l, 1), seg));
-      QP_SECTION(epilogues(p, ms, keys, gi_of(p, k, l, 2), seg));
-      QP_SECTION(epilogues(p, ms, keys, gi_of(p, k, l, 3), seg));
+      QP_SECTION(epilogues<G_O>(p, ms, keys, gi_of(p, k, l, 1), seg));
+      QP_SECTION(epilogues<G_GU>(p, ms, keys, gi_of(p, k, l, 2), seg));
+      QP_SECTION(epilogues<G_DOWN>(p, ms, keys, gi_of(p, k, l, 3), seg));
     }
-    QP_SECTION(epilogues(p, ms, keys, gi_head(p, k), seg));
+    QP_SECTION(epilogues<G_HEAD>(p, ms, keys, gi_head(p, k), seg));
     if (p.temperature > 0.f) QP_SECTION(decide_items(p, ms, keys, k));
   }
   QP_SECTION(final_items(p));
