@@ -22,6 +22,8 @@ LIB_PATH = os.path.join(HERE, "libqp.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-I", INCLUDE, "-I", CSRC]
+if os.environ.get("QP_TRACE") == "1":   # compile the phase-trace hooks in (include/qp_debug.h)
+    NVCC_FLAGS.append("-DQP_TRACE=1")
 
 
 def nvcc_path() -> str:
@@ -43,9 +45,17 @@ def _deps():
                                + glob.glob(os.path.join(INCLUDE, "*.h")))
 
 
-def up_to_date() -> bool:
+FLAGS_STAMP = os.path.join(BUILD_DIR, "flags.txt")
+
+
+def up_to_date(flags=None) -> bool:
+    """The library exists, is newer than every source and header, and was
+    built with the same compiler flags."""
     if not os.path.exists(LIB_PATH):
         return False
+    if flags is not None:
+        if not os.path.exists(FLAGS_STAMP) or open(FLAGS_STAMP).read() != " ".join(flags):
+            return False
     t = os.path.getmtime(LIB_PATH)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
@@ -59,11 +69,11 @@ def _run(cmd):
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     """Compile every CUDA source and link libqp.so; returns its path."""
-    if not force and up_to_date():
+    flags = NVCC_FLAGS + list(extra_flags or [])
+    if not force and up_to_date(flags):
         return LIB_PATH
     nvcc = nvcc_path()
     os.makedirs(BUILD_DIR, exist_ok=True)
-    flags = NVCC_FLAGS + list(extra_flags or [])
     jobs = []
     for src in _sources():
         obj = os.path.join(BUILD_DIR, os.path.basename(src) + ".o")
@@ -77,6 +87,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     tmp = LIB_PATH + ".tmp"
     _run([nvcc] + ARCH + ["-shared", "-o", tmp] + [j[1] for j in jobs])
     os.replace(tmp, LIB_PATH)
+    with open(FLAGS_STAMP, "w") as f:
+        f.write(" ".join(flags))
     return LIB_PATH
 
 

@@ -423,6 +423,9 @@ qp_status qp_set_engine(qp_handle* h, int engine) {
 
 qp_status qp_trace_enable(qp_handle* h, int enable) {
   if (!h) return QP_ERR_ARG;
+#ifndef QP_TRACE
+  if (enable) return QP_ERR_STATE;   // the kernels were built without the trace hooks
+#endif
   DeviceGuard dg(h->device);
   if (!dg.ok) return QP_ERR_CUDA;
   cudaDeviceSynchronize();

@@ -138,6 +138,9 @@ __device__ __forceinline__ unsigned long long* ev_base(const PParams& p) {
 __device__ __forceinline__ unsigned long long ev_word(int code, int gi) {
   return ((globaltimer_ns() & 0xFFFFFFFFFFFFull) << 16) | (unsigned long long)(code & 15) << 12 | unsigned(gi & 4095);
 }
+// Compiled in only with QP_TRACE (qp_debug.h): the hooks sit on the loop's
+// critical path, where even untaken branches cost instruction fetch.
+#ifdef QP_TRACE
 __device__ __forceinline__ void ev_mma(const PParams& p, unsigned& idx, int code, int gi) {
   unsigned long long* b = ev_base(p);
   if (b && idx < 8192) b[8192 + idx++] = ev_word(code, gi);
@@ -149,6 +152,10 @@ __device__ __forceinline__ void ev_cons(const PParams& p, unsigned* evc, int cod
     if (i < 8192) b[i] = ev_word(code, gi);
   }
 }
+#else
+__device__ __forceinline__ void ev_mma(const PParams&, unsigned&, int, int) {}
+__device__ __forceinline__ void ev_cons(const PParams&, unsigned*, int, int) {}
+#endif
 
 // ----------------------------------------------------------- the program
 struct Ck { int Nc, n; };
@@ -958,10 +965,14 @@ __device__ bool decide_items(const PParams& p, Misc& ms, uint32_t* keys, int k) 
   return true;
 }
 
+#ifdef QP_TRACE
 __device__ __forceinline__ void trace_mark(const PParams& p, int sec, int which) {
   if (p.trace && threadIdx.x == 0 && sec < p.trace_n)
     p.trace[(size_t(sec) * gridDim.x + blockIdx.x) * 2 + which] = globaltimer_ns();
 }
+#else
+__device__ __forceinline__ void trace_mark(const PParams&, int, int) {}
+#endif
 
 __device__ void consumer_role(const PParams& p, Misc& ms, uint8_t* smem) {
   uint32_t seg = 0;

@@ -211,6 +211,9 @@ __device__ __forceinline__ unsigned long long* sm_ev_base(const SParams& p) {
 __device__ __forceinline__ unsigned long long sm_ev_word(int code, int gi) {
   return ((globaltimer_ns() & 0xFFFFFFFFFFFFull) << 16) | (unsigned long long)(code & 15) << 12 | unsigned(gi & 4095);
 }
+// Compiled in only with QP_TRACE (qp_debug.h): the hooks sit on the loop's
+// critical path, where even untaken branches cost instruction fetch.
+#ifdef QP_TRACE
 __device__ __forceinline__ void sm_ev_mma(const SParams& p, unsigned& idx, int code, int gi) {
   unsigned long long* b = sm_ev_base(p);
   if (b && idx < 8192) b[8192 + idx++] = sm_ev_word(code, gi);
@@ -226,6 +229,11 @@ __device__ __forceinline__ void sm_trace_mark(const SParams& p, int sec, int whi
   if (p.trace && threadIdx.x == 0 && sec < p.trace_n)
     p.trace[(size_t(sec) * gridDim.x + blockIdx.x) * 2 + which] = globaltimer_ns();
 }
+#else
+__device__ __forceinline__ void sm_ev_mma(const SParams&, unsigned&, int, int) {}
+__device__ __forceinline__ void sm_ev(const SParams&, unsigned*, int, int) {}
+__device__ __forceinline__ void sm_trace_mark(const SParams&, int, int) {}
+#endif
 
 // ---------------------------------------------------------------- producer
 // Streams the weight slices of this CTA's units, in program order, through

@@ -41,7 +41,11 @@ typedef enum {
  * returns QP_ERR_ARG.  QP_ERR_ARG for a null handle or an unknown engine. */
 qp_status qp_set_engine(qp_handle* h, int engine);
 
-/* enable != 0: allocate a device buffer for up to 8192 sections x the SM count
+/* Tracing is compiled in only when libqp is built with QP_TRACE=1 in the
+ * environment (codebook_rvq_code_gb300/build.py): the hooks sit on the
+ * loop's critical path.  Without them, enable != 0 returns QP_ERR_STATE.
+ *
+ * enable != 0: allocate a device buffer for up to 8192 sections x the SM count
  * and record every later call into it (each call overwrites the last);
  * enable == 0: stop recording and free it.  Synchronises the device. */
 qp_status qp_trace_enable(qp_handle* h, int enable);
