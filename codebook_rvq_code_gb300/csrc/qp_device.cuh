@@ -112,5 +112,23 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
   return v[0];
 }
 
+// Sixteen warp-wide sums: lane l ends with the total over all 32 lanes of
+// v[(l >> 1) & 15] (lanes 2i and 2i + 1 both hold sum i).  Four halving
+// exchanges, then the lane pairs meet.
+__device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 2; o >>= 1) {
+    const int c = o >> 1;
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < c; ++i) {
+      const float send = upper ? v[i] : v[i + c];
+      const float keep = upper ? v[i + c] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  return v[0] + __shfl_xor_sync(0xffffffffu, v[0], 1);
+}
+
 }  // namespace
 }  // namespace qp

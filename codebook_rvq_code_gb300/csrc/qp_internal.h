@@ -66,6 +66,7 @@ struct Scratch {
   size_t x1, xk;                         // residual streams: step 1 [2B, d], later steps [B, d]
   size_t a1[5], ak[4], ahead;            // f16 operands: step 1 proj/qkv/o/gu/down, later qkv/o/gu/down, head
   size_t acc1_qkv, acck_qkv, acc1_gu, acck_gu, logits;
+  size_t acc_qkv_b;                      // a second [2B, q|k|v] accumulator (small-batch engine)
   size_t kv;                             // [layer][frame][pos][k|v][kv_width] f16
   size_t sync;                           // start of the zeroed-per-call region
   size_t total;                          // sync + the largest sync region (B = bmax)

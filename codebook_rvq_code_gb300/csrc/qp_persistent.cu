@@ -1188,6 +1188,7 @@ Scratch scratch_layout(const qp_geometry& g, int bmax) {
   L.acc1_gu = o;  o += al256(R1 * 2 * F * 4);
   L.acck_gu = o;  o += al256(RK * 2 * F * 4);
   L.logits = o;   o += al256(RK * V * 4);
+  L.acc_qkv_b = o; o += al256(R1 * qkvw * 4);
   L.kv = o;       o += al256(size_t(g.layers) * RK * (g.n_steps + 1) * 2 * kvw * 2);
   L.sync = o;
   L.total = o + sync_layout(g, bmax).total;

@@ -49,9 +49,16 @@ constexpr uint32_t kSmOffOp = kSmNW * kSmWSlot;
 constexpr uint32_t kSmOffKeys = kSmOffOp + kSmOpBytes;   // top-k keys, or the drain's transpose buffer
 constexpr uint32_t kSmOffMisc = kSmOffKeys + kMaxVocab * 4;
 constexpr uint32_t kSmTmemCols = 256;                // two accumulators of up to 128 columns
+// Largest batch whose attention runs inside the O projection's operand build
+// (each of the O projection's units then computes its q head for every
+// frame); larger batches run attention as a section of its own.
+constexpr int kSmFuseFrames = 8;
 
 enum { SBAR_CONS = 1 };
 enum { S_PROJ = 0, S_QKV, S_O, S_GU, S_DOWN, S_HEAD };
+// The O projection with attention folded into its operand build (a code
+// path of the S_O GEMM, not a GEMM of its own).
+constexpr int S_OA = 6;
 
 struct SMisc {
   uint64_t wfull[kSmNW], wempty[kSmNW];
@@ -90,7 +97,7 @@ struct SParams {
   // scratch (rows: 2B at step 1, B later)
   float* x;                // residual stream [row][d]
   uint16_t* a_o;           // attention output, f16 [row][q_width]
-  float* acc_qkv;          // [row][q_width + 2 kv_width], scaled by the row's RMS
+  float* acc_qkv[2];       // [row][q_width + 2 kv_width], scaled by the row's RMS; layers alternate
   float* acc_gu;           // [row][2 ffn]: gate then up, scaled by the row's RMS
   float* logits;           // [frame][vocab]
   uint16_t* kv;            // f16 [layer][frame][pos][k|v][kv_width]
@@ -105,6 +112,7 @@ struct SParams {
   int NGEMM, NHT;
   unsigned long long* trace; int trace_n;
   // the call
+  int fuse;                // attention inside the O projection's operand build
   int B; const float* H; const int32_t* q0; int32_t* out_codes; float* out_logits; const int32_t* forced;
   float temperature; int top_k; const float* gumbel;
 };
@@ -137,7 +145,7 @@ __device__ SG sgemm(const SParams& p, int gi) {
       const SLayer& L = p.layer[g.l];
       switch (r % 4) {
         case 0: g.kind = S_QKV; g.n_mt = (p.qw + 2 * p.kvw) / kTileM; g.n_ks = p.d / kKs; g.w = L.w[0];
-                g.out = p.acc_qkv; g.ld = p.qw + 2 * p.kvw; g.scaled = true; break;
+                g.out = p.acc_qkv[((g.k - 1) * p.L + g.l) & 1]; g.ld = p.qw + 2 * p.kvw; g.scaled = true; break;
         case 1: g.kind = S_O; g.n_mt = p.d / kTileM; g.n_ks = p.qw / kKs; g.w = L.w[1]; g.out = p.x; g.ld = p.d; break;
         case 2: g.kind = S_GU; g.n_mt = 2 * p.F / kTileM; g.n_ks = p.d / kKs; g.w = L.w[2];
                 g.out = p.acc_gu; g.ld = 2 * p.F; g.scaled = true; break;
@@ -333,6 +341,97 @@ __device__ __forceinline__ uint4 pack8h(const float (&v)[8]) {
 // [8 k] of f16 (all consumer threads; one thread per 8 consecutive columns
 // of a row, so global reads coalesce, and every unit's loads in one pass).
 // i0: the run index of unit u0 (its operand goes to slot (i0 + ui) % slots).
+// Attention of q head h for activation row n at layer l of step k (one warp;
+// lane l holds dims 4l..4l+3 of every 128-vector), stored as row n of the O
+// projection's operand slice for K slice h.  Per-head RMSNorm and RoPE of q
+// and of the frame's new key(s) (the step's positions come from the q|k|v
+// accumulator, earlier positions from the KV cache), causal softmax over
+// positions 0..pos, weighted sum of the values.  The per-head q/k norm
+// tensors and the 16 q / 8 kv heads of 128 are those of "rightkit-qts 0.2.3
+// - Qwen3-TTS 1.7B -> QTS GGUF", section "Loader contract"; where the norm
+// sits, the head grouping h / 2 and the 1/sqrt(128) scale are readings of
+// that geometry.  If `append`, the row's own key and value are stored in the
+// cache for the later steps.
+static_assert(kMaxCtx == 16, "sm_attn_row holds one score per position in a 16-way reduce-scatter");
+__device__ void sm_attn_row(const SParams& p, const float* acc, int k, int l, int h, int n, bool append,
+                            uint16_t* dst, int n8) {
+  const int lane = threadIdx.x & 31;
+  const int P = k == 1 ? 2 : 1, pos0 = k == 1 ? 0 : k;
+  const int b = n / P, pos = pos0 + (n - b * P);
+  const int qkvw = p.qw + 2 * p.kvw, j = h / (p.n_q / p.n_kv), ctx = p.n_steps + 1;
+  const SLayer& L = p.layer[l];
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  uint16_t* kvb = p.kv + (size_t(l) * p.Bmax + b) * ctx * 2 * p.kvw + j * kHeadDim + lane * 4;
+  const float* fr = acc + size_t(b) * P * qkvw;   // the frame's rows of this step
+  // independent loads first: q, the step's keys and values, then the cache
+  const float4 qraw = __ldcg(reinterpret_cast<const float4*>(acc + size_t(n) * qkvw + h * kHeadDim + lane * 4));
+  float4 kraw[2], vnew[2];
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp) {
+    kraw[pp] = pp < P ? __ldcg(reinterpret_cast<const float4*>(fr + pp * qkvw + p.qw + j * kHeadDim + lane * 4)) : z4;
+    vnew[pp] = pp < P ? __ldcg(reinterpret_cast<const float4*>(fr + pp * qkvw + p.qw + p.kvw + j * kHeadDim + lane * 4))
+                      : z4;
+  }
+  uint2 kh[kMaxCtx], vh[kMaxCtx];
+#pragma unroll
+  for (int t = 0; t < kMaxCtx; ++t) {
+    kh[t] = t < pos0 ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 0) * p.kvw)) : make_uint2(0, 0);
+    vh[t] = t < pos0 ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 1) * p.kvw)) : make_uint2(0, 0);
+  }
+  const float4 qn = norm_rope(qraw, L.q_norm, p.eps, p.rope_cs + pos * 64, lane);
+  float4 knew[2];
+#pragma unroll
+  for (int pp = 0; pp < 2; ++pp)
+    knew[pp] = pp < P ? norm_rope(kraw[pp], L.k_norm, p.eps, p.rope_cs + (pos0 + pp) * 64, lane) : z4;
+  if (append) {
+    const bool second = pos != pos0;
+    const float4 kk = second ? knew[1] : knew[0], vv = second ? vnew[1] : vnew[0];
+    *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = pack4_f16(kk.x, kk.y, kk.z, kk.w);
+    *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 1) * p.kvw) = pack4_f16(vv.x, vv.y, vv.z, vv.w);
+  }
+  float part[kMaxCtx];
+#pragma unroll
+  for (int t = 0; t < kMaxCtx; ++t) {
+    const float4 kk = t < pos0 ? unpack4_f16(kh[t]) : (t == pos0 ? knew[0] : (t == pos0 + 1 ? knew[1] : z4));
+    part[t] = qn.x * kk.x + qn.y * kk.y + qn.z * kk.z + qn.w * kk.w;
+  }
+  const int tl = lane >> 1;                           // the position whose score this lane holds
+  const float rsum = reduce_scatter16(part, lane);    // all 32 lanes take part
+  const bool valid = tl <= pos;
+  const float sc = valid ? rsum * rsqrtf(float(kHeadDim)) : -INFINITY;
+  float mx = sc;
+#pragma unroll
+  for (int o = 16; o >= 2; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  const float e = valid ? expf(sc - mx) : 0.f;
+  float den = e;
+#pragma unroll
+  for (int o = 16; o >= 2; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+  const float pr = e / den;                           // den >= 1: position 0 is always valid
+  float4 o4 = z4;
+#pragma unroll
+  for (int t = 0; t < kMaxCtx; ++t) {
+    const float4 vv = t < pos0 ? unpack4_f16(vh[t]) : (t == pos0 ? vnew[0] : (t == pos0 + 1 ? vnew[1] : z4));
+    const float w = __shfl_sync(0xffffffffu, pr, 2 * t);
+    o4.x += w * vv.x; o4.y += w * vv.y; o4.z += w * vv.z; o4.w += w * vv.w;
+  }
+  *reinterpret_cast<uint2*>(dst + (size_t((lane >> 1) * n8 + (n >> 3)) << 6) + ((n & 7) << 3) + (lane & 1) * 4) =
+      pack4_f16(o4.x, o4.y, o4.z, o4.w);
+}
+
+// The O projection's operand slices with attention folded in: one warp per
+// (unit, row); the unit's K slice is its q head.
+__device__ void sm_build_oa(const SParams& p, const SG& g, int u0, int nu, int i0, uint8_t* smem) {
+  const int n8 = g.N / 8, warp = threadIdx.x >> 5, grp = p.n_q / p.n_kv;
+  const uint32_t nop = sm_op_slots(g), obytes = sm_op_bytes(g);
+  const float* acc = p.acc_qkv[((g.k - 1) * p.L + g.l) & 1];
+  for (int it = warp; it < nu * g.R; it += kSmConsumerWarps) {
+    const int ui = it / g.R, n = it - ui * g.R, u = u0 + ui, h = u % g.n_ks;
+    uint16_t* dst = reinterpret_cast<uint16_t*>(smem + kSmOffOp + (uint32_t(i0 + ui) % nop) * obytes);
+    // the first tile's unit of each group's first q head appends the group's keys and values
+    sm_attn_row(p, acc, g.k, g.l, h, n, u < g.n_ks && h % grp == 0, dst, n8);
+  }
+}
+
 template <int KIND>
 __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, uint8_t* smem) {
   const int n8 = g.N / 8, per = g.R * 16;
@@ -347,9 +446,10 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
     } else {
       float v[8];
       if (KIND == S_PROJ) {
-        // rows 2b, 2b+1: the Talker state H_b and the embedding of q0_b,
-        // the first two positions of frame b ("Qwen3-TTS Technical Report",
-        // section 2.3)
+        // rows 2b, 2b+1: the Talker state H_b and the embedding of q0_b, the
+        // first two positions of frame b (H and q0 feed the residual loop:
+        // "拆解 Qwen3-TTS：OpenVINO 移植过程中的图分离与调度实践", section 1;
+        // their order is a reading)
         const int b = n >> 1;
         if ((n & 1) == 0) {
           const float4 a = __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k));
@@ -391,31 +491,53 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
   }
 }
 
+// Per-warp sums of squares of rows r0 .. r0+ROWS-1 (those below R) of the
+// GEMM's input into ms.ssp[warp]: each thread sums its columns of all ROWS
+// rows with all of those loads in flight.  Up to 8 rows, one warp reduction
+// per row present; 16 rows meet in one reduce-scatter across the warp.
+template <int KIND, int ROWS>
+__device__ __forceinline__ void sm_ssq(const SParams& p, const SG& g, SMisc& ms, int r0) {
+  static_assert(ROWS == 8 || ROWS == 16, "8 rows reduce per row, 16 by reduce_scatter16");
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nc = p.d / 4;
+  float sq[ROWS];
+#pragma unroll
+  for (int u = 0; u < ROWS; ++u) sq[u] = 0.f;
+  for (int c = t; c < nc; c += kSmConsumers) {
+    float4 a[ROWS];
+#pragma unroll
+    for (int u = 0; u < ROWS; ++u) {
+      const int n = r0 + u, row = (KIND == S_HEAD && g.k == 1) ? 2 * n + 1 : n;
+      a[u] = n < g.R ? __ldcg(reinterpret_cast<const float4*>(p.x + size_t(row) * p.d) + c)
+                     : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < ROWS; ++u) sq[u] += a[u].x * a[u].x + a[u].y * a[u].y + a[u].z * a[u].z + a[u].w * a[u].w;
+  }
+  if constexpr (ROWS == 16) {
+    // lanes 2i and 2i + 1 end with row r0 + i's warp total
+    const float v = reduce_scatter16(sq, lane);
+    if ((lane & 1) == 0 && r0 + (lane >> 1) < g.R) ms.ssp[warp][r0 + (lane >> 1)] = v;
+  } else {
+#pragma unroll
+    for (int u = 0; u < ROWS; ++u) {
+      if (r0 + u < g.R) {   // warp-uniform
+        const float v = warp_sum(sq[u]);
+        if (lane == 0) ms.ssp[warp][r0 + u] = v;
+      }
+    }
+  }
+}
+
 // inv[n] = 1 / RMS of the GEMM's input row n, from the complete residual row
-// (all consumer threads: each thread sums its columns of eight rows at a
-// time with all eight loads in flight, the warps' partials meet in shared
-// memory).  The caller's next barrier publishes ms.inv.
+// (all consumer threads; the warps' partial sums meet in shared memory).  The
+// caller's next barrier publishes ms.inv.
 template <int KIND>
 __device__ void sm_inv(const SParams& p, const SG& g, SMisc& ms) {
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, nc = p.d / 4;
-  for (int r0 = 0; r0 < g.R; r0 += 8) {
-    float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int c = t; c < nc; c += kSmConsumers) {
-      float4 a[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int n = r0 + u, row = (KIND == S_HEAD && g.k == 1) ? 2 * n + 1 : n;
-        a[u] = n < g.R ? __ldcg(reinterpret_cast<const float4*>(p.x + size_t(row) * p.d) + c)
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) s8[u] += a[u].x * a[u].x + a[u].y * a[u].y + a[u].z * a[u].z + a[u].w * a[u].w;
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) {
-      const float v = warp_sum(s8[u]);
-      if (lane == 0 && r0 + u < g.R) ms.ssp[warp][r0 + u] = v;
-    }
+  const int t = threadIdx.x;
+  if (g.R <= 8) {
+    sm_ssq<KIND, 8>(p, g, ms, 0);
+  } else {
+    for (int r0 = 0; r0 < g.R; r0 += 16) sm_ssq<KIND, 16>(p, g, ms, r0);
   }
   named_bar(SBAR_CONS, kSmConsumers);
   if (t < g.R) {
@@ -480,6 +602,30 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
   return true;
 }
 
+// With attention inside the O projection, the q|k|v accumulator of layer n
+// is read by many units, so nothing zeroes it as it is read.  Instead the
+// layers alternate between two accumulators, and the O projection's units of
+// layer n clear, in equal shares by unit index: the gate|up accumulator that
+// layer n's GU projection adds into next (last read by layer n-1's down
+// projection), and the other q|k|v accumulator, which layer n+1's QKV
+// projection adds into (last read by layer n-1's O projection).  Both
+// earlier readers precede layer n's QKV projection, whose tiles these units
+// acquired; both later writers follow the O projection's completion count,
+// which these units release after the stores.
+__device__ void sm_zero_oa(const SParams& p, const SG& g, int beg, int end) {
+  const long long U = (long long)g.n_mt * g.n_ks;
+  const int n = (g.k - 1) * p.L + g.l;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  const long long zg = (long long)g.R * (2 * p.F) / 4;
+  float4* gu = reinterpret_cast<float4*>(p.acc_gu);
+  for (long long i = zg * beg / U + threadIdx.x; i < zg * end / U; i += kSmConsumers) gu[i] = z4;
+  if (n + 1 < p.n_steps * p.L) {
+    const long long zq = (long long)g.R * (p.qw + 2 * p.kvw) / 4;
+    float4* q = reinterpret_cast<float4*>(p.acc_qkv[(n + 1) & 1]);
+    for (long long i = zq * beg / U + threadIdx.x; i < zq * end / U; i += kSmConsumers) q[i] = z4;
+  }
+}
+
 // This CTA's units of GEMM gi (all consumer threads): wait for the operand's
 // source, build the operand slices, drain the accumulators.
 //
@@ -497,7 +643,20 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
   sm_run(g, gi, beg, end);
   if (beg >= end) return true;
   const int t = threadIdx.x;
-  if (t == 0) {
+  if (KIND == S_OA) {
+    // each unit's head needs its q tile and its group's k and v tiles
+    if (t < 32) {
+      const int grp = p.n_q / p.n_kv;
+      int ok = 1;
+      for (int i = t; i < 3 * (end - beg) && ok; i += 32) {
+        const int h = (beg + i / 3) % g.n_ks, j = h / grp, w = i % 3;
+        const int tile = w == 0 ? h : (w == 1 ? p.qw / kHeadDim + j : (p.qw + p.kvw) / kHeadDim + j);
+        ok = poll_geq(p, sm_qkv_tile(p, g.k, g.l, tile), unsigned(p.d / kKs));
+      }
+      ok = __all_sync(0xffffffffu, ok);
+      if (t == 0) ms.flag[2] = ok;
+    }
+  } else if (t == 0) {
     const unsigned* ctr;
     unsigned want;
     sm_ready(p, gi, ctr, want);
@@ -525,7 +684,8 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
       }
       named_bar(SBAR_CONS, kSmConsumers);
       if (!ms.flag[3]) return false;
-      sm_build<KIND>(p, g, u, nu, u - beg, smem);
+      if constexpr (KIND == S_OA) sm_build_oa(p, g, u, nu, u - beg, smem);
+      else sm_build<KIND>(p, g, u, nu, u - beg, smem);
       fence_proxy_async_shared();   // the tensor cores read what these generic stores wrote
       named_bar(SBAR_CONS, kSmConsumers);
       if (t == 0)
@@ -547,6 +707,7 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
   };
   if (end - beg <= int(nop)) {
     if (!build(beg, end)) return false;
+    if (KIND == S_OA) sm_zero_oa(p, g, beg, end);
     scale();
     for (int s = beg; s < end;) {
       const int ks0 = s % g.n_ks, seg_end = min(end, s + (g.n_ks - ks0));
@@ -572,7 +733,10 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
     const int ks0 = s % g.n_ks, mt = s / g.n_ks;
     const int seg_end = min(end, s + (g.n_ks - ks0)), nsl = seg_end - s;
     if (!build(s, seg_end)) return false;
-    if (si == 0) scale();
+    if (si == 0) {
+      if (KIND == S_OA) sm_zero_oa(p, g, beg, end);
+      scale();
+    }
     if (si > 0 && !sm_drain<KIND>(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true)) return false;
     prev_mt = mt;
     prev_nsl = nsl;
@@ -583,9 +747,9 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
 }
 
 // Step-1 setup, one warp per row r < 2B: the residual row starts at the
-// projection bias (the projection's partials are added to it); the q|k|v
-// accumulator row and the frame's logit row start at zero; out-of-range
-// first codes are reported.
+// projection bias (the projection's partials are added to it); the row of
+// both q|k|v accumulators and the frame's logit row start at zero;
+// out-of-range first codes are reported.
 __device__ bool sm_prep1(const SParams& p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = gridDim.x;
   const int qkvw = p.qw + 2 * p.kvw;
@@ -593,7 +757,10 @@ __device__ bool sm_prep1(const SParams& p) {
   for (int r = blockIdx.x + warp * G; r < 2 * p.B; r += kSmConsumerWarps * G) {
     for (int f = lane * 4; f < p.d; f += 128)
       *reinterpret_cast<float4*>(p.x + size_t(r) * p.d + f) = *reinterpret_cast<const float4*>(p.b_proj + f);
-    for (int f = lane * 4; f < qkvw; f += 128) *reinterpret_cast<float4*>(p.acc_qkv + size_t(r) * qkvw + f) = z4;
+    for (int f = lane * 4; f < qkvw; f += 128) {
+      *reinterpret_cast<float4*>(p.acc_qkv[0] + size_t(r) * qkvw + f) = z4;
+      *reinterpret_cast<float4*>(p.acc_qkv[1] + size_t(r) * qkvw + f) = z4;
+    }
     if (r < p.B)
       for (int f = lane * 4; f < p.V; f += 128) *reinterpret_cast<float4*>(p.logits + size_t(r) * p.V + f) = z4;
     if ((r & 1) && lane == 0) {
@@ -740,7 +907,7 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
     uint16_t* kvb = kvl + size_t(b) * ctx * 2 * p.kvw + j * kHeadDim + lane * 4;   // + (pos*2 + {0,1}) * kvw
     for (int pp = 0; pp < P; ++pp) {
       const int r = r0 + pp, pos = pos0 + pp;
-      float* row = p.acc_qkv + size_t(r) * qkvw;
+      float* row = p.acc_qkv[((k - 1) * p.L + l) & 1] + size_t(r) * qkvw;
       float* kr = row + p.qw + j * kHeadDim + lane * 4;
       float* vr = row + p.qw + p.kvw + j * kHeadDim + lane * 4;
       // independent loads first: new k, v, the first two q heads, then the cache
@@ -924,8 +1091,12 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
     if (k > 1) SM_SECTION(sm_prepk(p, ms, k));
     for (int l = 0; l < p.L; ++l) {
       SM_SECTION(sm_gemm<S_QKV>(p, ms, smem, sgi_of(p, k, l, 0), seg));
-      SM_SECTION(sm_attn(p, ms, k, l));
-      SM_SECTION(sm_gemm<S_O>(p, ms, smem, sgi_of(p, k, l, 1), seg));
+      if (p.fuse) {
+        SM_SECTION(sm_gemm<S_OA>(p, ms, smem, sgi_of(p, k, l, 1), seg));
+      } else {
+        SM_SECTION(sm_attn(p, ms, k, l));
+        SM_SECTION(sm_gemm<S_O>(p, ms, smem, sgi_of(p, k, l, 1), seg));
+      }
       SM_SECTION(sm_gemm<S_GU>(p, ms, smem, sgi_of(p, k, l, 2), seg));
       SM_SECTION(sm_gemm<S_DOWN>(p, ms, smem, sgi_of(p, k, l, 3), seg));
     }
@@ -1020,7 +1191,8 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   // the tile engine's buffers, each at least as large as this schedule needs
   p.x = reinterpret_cast<float*>(scratch + L.x1);
   p.a_o = reinterpret_cast<uint16_t*>(scratch + L.a1[2]);
-  p.acc_qkv = reinterpret_cast<float*>(scratch + L.acc1_qkv);
+  p.acc_qkv[0] = reinterpret_cast<float*>(scratch + L.acc1_qkv);
+  p.acc_qkv[1] = reinterpret_cast<float*>(scratch + L.acc_qkv_b);
   p.acc_gu = reinterpret_cast<float*>(scratch + L.acc1_gu);
   p.logits = reinterpret_cast<float*>(scratch + L.logits);
   p.kv = reinterpret_cast<uint16_t*>(scratch + L.kv);
@@ -1036,6 +1208,7 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   p.trace = h->trace; p.trace_n = h->trace_phases;
   p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;
   p.temperature = a.temperature; p.top_k = a.top_k; p.gumbel = a.gumbel;
+  p.fuse = a.B <= kSmFuseFrames;
 }
 
 constexpr int kSmMaxDevices = 64;
