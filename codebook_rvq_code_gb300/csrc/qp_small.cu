@@ -59,6 +59,10 @@ enum { S_PROJ = 0, S_QKV, S_O, S_GU, S_DOWN, S_HEAD };
 // The O projection with attention folded into its operand build (a code
 // path of the S_O GEMM, not a GEMM of its own).
 constexpr int S_OA = 6;
+// The QKV projection without the row scale (a code path of the S_QKV GEMM):
+// when attention runs as a section of its own, each attention item scales
+// its frame's q, k and v itself, so the GEMM needs no row-scale pass.
+constexpr int S_QKVU = 7;
 
 struct SMisc {
   uint64_t wfull[kSmNW], wempty[kSmNW];
@@ -157,9 +161,18 @@ __device__ SG sgemm(const SParams& p, int gi) {
   return g;
 }
 
-// GEMMs whose input is RMS-normalised (their partials are scaled by the row's 1/RMS)
+// GEMMs whose partials are scaled by the input row's 1/RMS.  From step 2 on
+// the head's logits are added unscaled: a positive row scale does not move
+// the argmax, and the frame's decision applies it where values are copied
+// out or sampled, from the frame's residual row, which only that decision's
+// CTA overwrites afterwards.  (At step 1 the head's rows are 2b+1, which the
+// next step's inputs overwrite from other CTAs, so there the GEMM scales.)
 template <int KIND>
-constexpr bool kScaled = KIND == S_QKV || KIND == S_GU || KIND == S_HEAD;
+constexpr bool kScaled = KIND == S_QKV || KIND == S_GU;
+template <int KIND>
+__device__ __forceinline__ bool sm_scaled(const SG& g) { return kScaled<KIND> || (KIND == S_HEAD && g.k == 1); }
+template <int KIND>
+constexpr bool kQkv = KIND == S_QKV || KIND == S_QKVU;
 
 // The operand ring of a GEMM: slots of N x 128 f16 (the GEMM's own width),
 // as many as fit the region.  A CTA's unit i of the GEMM uses slot i % n.
@@ -474,7 +487,7 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
         // the GEMM's partial products instead
         const float* wn;
         int row = n;
-        if (KIND == S_QKV) wn = p.layer[g.l].attn_norm;
+        if (kQkv<KIND>) wn = p.layer[g.l].attn_norm;
         else if (KIND == S_GU) wn = p.layer[g.l].ffn_norm;
         else { wn = p.out_norm; row = g.k == 1 ? 2 * n + 1 : n; }   // head: each frame's last position
         // both loads in flight together
@@ -577,7 +590,7 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
       const int f = pass * 4 + (lane >> 3), k4 = (lane & 7) * 4, n = col + f;
       if (n < g.R) {
         float4 x = *reinterpret_cast<const float4*>(tp + f * 32 + k4);
-        if (kScaled<KIND>) {
+        if (sm_scaled<KIND>(g)) {
           const float s = ms.inv[n];
           x.x *= s; x.y *= s; x.z *= s; x.w *= s;
         }
@@ -594,7 +607,7 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
     named_bar(SBAR_CONS, kSmConsumers);
     if (t == 0) {
       // release: the bar.sync above orders every consumer thread's reductions first
-      if (KIND == S_QKV) red_release_add(sm_qkv_tile(p, g.k, g.l, mt), unsigned(nsl));
+      if (kQkv<KIND>) red_release_add(sm_qkv_tile(p, g.k, g.l, mt), unsigned(nsl));
       red_release_add(sm_done(p, gi), unsigned(nsl));
       sm_ev(p, &ms.evc, SEV_PUBLISHED, gi);
     }
@@ -700,7 +713,7 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
     return true;
   };
   auto scale = [&]() {
-    if (kScaled<KIND>) {
+    if (sm_scaled<KIND>(g)) {
       sm_inv<KIND>(p, g, ms);
       named_bar(SBAR_CONS, kSmConsumers);
     }
@@ -717,7 +730,7 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
     named_bar(SBAR_CONS, kSmConsumers);
     if (t == 0) {
       // release: the bar.sync above orders every consumer thread's reductions first
-      if (KIND == S_QKV)
+      if (kQkv<KIND>)
         for (int s = beg; s < end;) {
           const int ks0 = s % g.n_ks, seg_end = min(end, s + (g.n_ks - ks0));
           red_release_add(sm_qkv_tile(p, g.k, g.l, s / g.n_ks), unsigned(seg_end - s));
@@ -773,11 +786,32 @@ __device__ bool sm_prep1(const SParams& p) {
   return true;
 }
 
+// 1/RMS of residual row `row` (all consumer threads; the same value in
+// every thread).  ms.ssp[*][0] holds the warps' partial sums until the
+// caller's next consumer barrier.
+__device__ float sm_row_inv(const SParams& p, SMisc& ms, int row) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  float ss = 0.f;
+  for (int c = t * 4; c < p.d; c += 4 * kSmConsumers) {
+    const float4 v = __ldcg(reinterpret_cast<const float4*>(p.x + size_t(row) * p.d + c));
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = warp_sum(ss);
+  if (lane == 0) ms.ssp[warp][0] = ss;
+  named_bar(SBAR_CONS, kSmConsumers);
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kSmConsumerWarps; ++w) tot += ms.ssp[w][0];
+  return rsqrtf(tot / float(p.d) + p.eps);
+}
+
 // The code of step `step` for frame b, computed by the whole CTA (all
 // consumer threads; the same value, or -1 if the grid aborted, in every
 // thread).  Greedy: the argmax of the frame's complete logit row (lowest
-// index on ties), which is copied out if asked and zeroed for the next
-// step's accumulation.  Sampling: the decision the sampling pass published.
+// index on ties; from step 2 on the row holds the logits before the row
+// scale), which is copied out, scaled, if asked and zeroed for the next
+// step's accumulation.
+// Sampling: the decision the sampling pass published.
 __device__ int sm_code(const SParams& p, SMisc& ms, int step, int b) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   if (p.temperature > 0.f) {
@@ -798,6 +832,7 @@ __device__ int sm_code(const SParams& p, SMisc& ms, int step, int b) {
   if (ms.bcast < 0) return -1;
   float* row = p.logits + size_t(b) * p.V;
   float* dst = p.out_logits ? p.out_logits + (size_t(b) * p.n_steps + (step - 1)) * p.V : nullptr;
+  const float rs = dst && step > 1 ? sm_row_inv(p, ms, b) : 1.f;   // the head's input row
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   unsigned long long best = 0ull;
   for (int f0 = t * 4; f0 < p.V; f0 += 2 * 4 * kSmConsumers) {
@@ -811,7 +846,7 @@ __device__ int sm_code(const SParams& p, SMisc& ms, int step, int b) {
     for (int i = 0; i < 2; ++i) {
       const int f = f0 + i * 4 * kSmConsumers;
       if (f >= p.V) continue;
-      if (dst) *reinterpret_cast<float4*>(dst + f) = v[i];
+      if (dst) *reinterpret_cast<float4*>(dst + f) = make_float4(v[i].x * rs, v[i].y * rs, v[i].z * rs, v[i].w * rs);
       *reinterpret_cast<float4*>(row + f) = z4;
       unsigned long long c = pack_argmax(v[i].x, f);
       const unsigned long long c1 = pack_argmax(v[i].y, f + 1), c2 = pack_argmax(v[i].z, f + 2),
@@ -872,9 +907,12 @@ __device__ bool sm_final(const SParams& p, SMisc& ms) {
   return true;
 }
 
-// Attention of one (frame, kv head) per warp at layer l of step k: per-head
-// RMSNorm and RoPE of the new position(s), KV append, causal softmax over
-// positions 0..pos for the group's q heads, output into the O operand rows.
+// Attention of one (frame, kv head) per warp at layer l of step k: the row
+// scale 1/RMS of the layer's input row (the QKV projection's partials are
+// added unscaled; the residual row is unchanged until the O projection,
+// which waits for every item), per-head RMSNorm and RoPE of the new
+// position(s), KV append, causal softmax over positions 0..pos for the
+// group's q heads, output into the O operand rows.
 // Lane l holds dims 4l..4l+3 of every 128-vector; the scores of two q heads x
 // 16 positions are 32 partial dot products per lane, summed across the warp
 // by one reduce-scatter that leaves score (head l/16, position l%16) in lane
@@ -910,13 +948,22 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
       float* row = p.acc_qkv[((k - 1) * p.L + l) & 1] + size_t(r) * qkvw;
       float* kr = row + p.qw + j * kHeadDim + lane * 4;
       float* vr = row + p.qw + p.kvw + j * kHeadDim + lane * 4;
-      // independent loads first: new k, v, the first two q heads, then the cache
-      const float4 kraw = __ldcg(reinterpret_cast<const float4*>(kr));
-      const float4 vnew = __ldcg(reinterpret_cast<const float4*>(vr));
+      // independent loads first: the input row, new k, v, the first two q heads, then the cache
+      float ss = 0.f;
+#pragma unroll 8
+      for (int c = lane * 4; c < p.d; c += 128) {
+        const float4 xv = __ldcg(reinterpret_cast<const float4*>(p.x + size_t(r) * p.d + c));
+        ss += xv.x * xv.x + xv.y * xv.y + xv.z * xv.z + xv.w * xv.w;
+      }
+      float4 kraw = __ldcg(reinterpret_cast<const float4*>(kr));
+      float4 vnew = __ldcg(reinterpret_cast<const float4*>(vr));
       float4 qraw[2];
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh)
         qraw[hh] = hh < grp ? __ldcg(reinterpret_cast<const float4*>(row + (j * grp + hh) * kHeadDim + lane * 4)) : z4;
+      const float rs = rsqrtf(warp_sum(ss) / float(p.d) + p.eps);
+      kraw.x *= rs; kraw.y *= rs; kraw.z *= rs; kraw.w *= rs;
+      vnew.x *= rs; vnew.y *= rs; vnew.z *= rs; vnew.w *= rs;
       uint2 kh[kMaxCtx], vh[kMaxCtx];
 #pragma unroll
       for (int t = 0; t < kMaxCtx; ++t) {
@@ -936,7 +983,8 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
           qn[hh] = z4;
           if (hh < nh) {
             float* qr = row + (j * grp + g0 + hh) * kHeadDim + lane * 4;
-            const float4 q = g0 == 0 ? qraw[hh] : __ldcg(reinterpret_cast<const float4*>(qr));
+            float4 q = g0 == 0 ? qraw[hh] : __ldcg(reinterpret_cast<const float4*>(qr));
+            q.x *= rs; q.y *= rs; q.z *= rs; q.w *= rs;
             qn[hh] = norm_rope(q, L.q_norm, p.eps, p.rope_cs + pos * 64, lane);
             *reinterpret_cast<float4*>(qr) = z4;
           }
@@ -988,7 +1036,8 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
 }
 
 // Gumbel top-k decisions of step k, one frame per CTA pass (all consumers):
-// radix select of the k-th largest logit / T, then the argmax of
+// the row's logits are the accumulated ones, times the head input row's
+// scale from step 2 on; radix select of the k-th largest logit / T, then the argmax of
 // logit / T + g over the kept set (ties at the threshold kept lowest index
 // first).  The logit row is copied out if asked and zeroed for the next step.
 __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
@@ -1000,7 +1049,8 @@ __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
     named_bar(SBAR_CONS, kSmConsumers);
     if (!ms.flag[3]) return false;
     float* l = p.logits + size_t(b) * V;
-    for (int i = t; i < V; i += kSmConsumers) keys[i] = f32_order_key(__ldcg(l + i) / T);
+    const float rs = k > 1 ? sm_row_inv(p, ms, b) : 1.f;
+    for (int i = t; i < V; i += kSmConsumers) keys[i] = f32_order_key(__ldcg(l + i) * rs / T);
     uint32_t prefix = 0, mask = 0;
     int remaining = p.top_k;
     for (int shift = 24; shift >= 0; shift -= 8) {
@@ -1045,7 +1095,7 @@ __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
       bool in = kk > kth;
       if (kk == kth) { in = eq_rank < remaining; ++eq_rank; }
       if (in) {
-        const unsigned long long pk = pack_argmax(__ldcg(l + i) / T + gb[i], i);
+        const unsigned long long pk = pack_argmax(__ldcg(l + i) * rs / T + gb[i], i);
         best = pk > best ? pk : best;
       }
     }
@@ -1054,7 +1104,7 @@ __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
     named_bar(SBAR_CONS, kSmConsumers);
     float* dst = p.out_logits ? p.out_logits + (size_t(b) * p.n_steps + (k - 1)) * V : nullptr;
     for (int i = t; i < V; i += kSmConsumers) {
-      if (dst) dst[i] = __ldcg(l + i);
+      if (dst) dst[i] = __ldcg(l + i) * rs;
       l[i] = 0.f;
     }
     named_bar(SBAR_CONS, kSmConsumers);
@@ -1090,10 +1140,11 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
   for (int k = 1; k <= p.n_steps; ++k) {
     if (k > 1) SM_SECTION(sm_prepk(p, ms, k));
     for (int l = 0; l < p.L; ++l) {
-      SM_SECTION(sm_gemm<S_QKV>(p, ms, smem, sgi_of(p, k, l, 0), seg));
       if (p.fuse) {
+        SM_SECTION(sm_gemm<S_QKV>(p, ms, smem, sgi_of(p, k, l, 0), seg));
         SM_SECTION(sm_gemm<S_OA>(p, ms, smem, sgi_of(p, k, l, 1), seg));
       } else {
+        SM_SECTION(sm_gemm<S_QKVU>(p, ms, smem, sgi_of(p, k, l, 0), seg));
         SM_SECTION(sm_attn(p, ms, k, l));
         SM_SECTION(sm_gemm<S_O>(p, ms, smem, sgi_of(p, k, l, 1), seg));
       }

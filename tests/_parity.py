@@ -88,3 +88,19 @@ def assert_parity(stats: ParityStats):
     assert stats.forced_mismatch == 0, stats
     assert stats.free_prefix_mismatch == 0, stats
     assert stats.decidable_steps > 0, stats
+
+
+def decided_prefix(*logit_sets, tol: float = TOL):
+    """What two free-running calls on the same inputs must agree on.
+
+    A greedy decision whose top-2 gap is within the tolerance may go either
+    way between calls (split-K partial sums meet in f32 atomics, in no fixed
+    order), and every later step of that frame follows the choice.  So each
+    frame agrees up to its first such step, taken over all the given logit
+    arrays [B, steps, vocab]: codes before it, logits up to it.  Returns the
+    two [B, steps] masks (codes, logits)."""
+    clear = np.logical_and.reduce([O.top2_gap(l) > tol for l in logit_sets])
+    n = clear.shape[1]
+    first = np.where(clear.all(axis=1), n, np.argmin(clear, axis=1))
+    steps = np.arange(n)[None, :]
+    return steps < first[:, None], steps <= first[:, None]

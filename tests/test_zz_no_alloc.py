@@ -15,7 +15,7 @@ import pytest
 
 import oracle as O
 import synthetic as S
-from _parity import SMALL, TOL
+from _parity import SMALL, TOL, decided_prefix
 
 pytestmark = pytest.mark.gpu
 
@@ -49,7 +49,6 @@ def test_static_entry_matches_the_allocating_entry(qpk, geometry, B):
     torch.cuda.synchronize()
     ref_l = ref_logits.cpu().numpy()
     ref_c = ref_codes.cpu().numpy()
-    clear = O.top2_gap(ref_l) > TOL
     for _ in range(2):   # the array keeps the previous call's contents
         codes = torch.full((B, n), -1, dtype=torch.int32, device="cuda")
         logits = torch.full((B, n, V), float("nan"), dtype=torch.float32, device="cuda")
@@ -59,8 +58,9 @@ def test_static_entry_matches_the_allocating_entry(qpk, geometry, B):
         assert cp.device_status() == 0
         got_l = logits.cpu().numpy()
         assert np.all(np.isfinite(got_l))
-        assert np.abs(got_l - ref_l).max() <= TOL
-        np.testing.assert_array_equal(codes.cpu().numpy()[clear], ref_c[clear])
+        code_mask, logit_mask = decided_prefix(ref_l, got_l)   # near-ties may go either way
+        assert np.abs(got_l - ref_l)[logit_mask].max() <= TOL
+        np.testing.assert_array_equal(codes.cpu().numpy()[code_mask], ref_c[code_mask])
     cp.close()
 
 
