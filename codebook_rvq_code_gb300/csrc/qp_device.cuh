@@ -112,6 +112,78 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
   return v[0];
 }
 
+// ------------------------------------------------------ top-k selection
+// The top_k-th largest of the order keys keys[0..V) in shared memory, by a
+// most-significant-digit radix select over four 8-bit digits (all NT
+// consumer threads of the CTA, which meet at named barrier `bar`; hist has
+// 256 entries, sel 2).  Returns that key; `remaining` says how many keys
+// equal to it belong to the top_k (the first ones in index order).  Each
+// digit is chosen by one warp: lane l holds the 8 bins 255-8l .. 248-8l, a
+// shuffle prefix sum gives every lane the count above its bins, and the lane
+// whose range reaches `remaining` picks the digit.
+template <int NT>
+__device__ uint32_t topk_kth_key(const uint32_t* keys, int V, int top_k, int* hist, int* sel, int bar,
+                                 int& remaining) {
+  const int t = threadIdx.x, lane = t & 31;
+  uint32_t prefix = 0, mask = 0;
+  remaining = top_k;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = t; i < 256; i += NT) hist[i] = 0;
+    named_bar(bar, NT);
+    for (int i = t; i < V; i += NT) {
+      const uint32_t kk = keys[i];
+      if ((kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255], 1);
+    }
+    named_bar(bar, NT);
+    if (t < 32) {
+      int c[8], s = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) { c[i] = hist[255 - 8 * lane - i]; s += c[i]; }
+      int incl = s;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const int excl = incl - s;
+      if (excl < remaining && remaining <= incl) {   // exactly one lane
+        int cum = excl;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (cum + c[i] >= remaining) { sel[0] = 255 - 8 * lane - i; sel[1] = remaining - cum; break; }
+          cum += c[i];
+        }
+      }
+      if (lane == 31 && incl < remaining) { sel[0] = 0; sel[1] = remaining - incl; }   // not reached for top_k <= V
+    }
+    named_bar(bar, NT);
+    prefix |= uint32_t(sel[0]) << shift;
+    mask |= 255u << shift;
+    remaining = sel[1];
+    named_bar(bar, NT);   // sel and hist are rewritten by the next digit
+  }
+  return prefix;
+}
+
+// Exclusive prefix sum of v over the NT threads in thread order (CTA-wide;
+// wtot holds NT / 32 ints).  Ends with the barrier that publishes the warp
+// totals; the caller's next barrier must come before wtot is rewritten.
+template <int NT>
+__device__ int block_exclusive_scan(int v, int* wtot, int bar) {
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) wtot[warp] = incl;
+  named_bar(bar, NT);
+  int off = 0;
+  for (int w = 0; w < warp; ++w) off += wtot[w];
+  return off + incl - v;
+}
+
 // Sixteen warp-wide sums: lane l ends with the total over all 32 lanes of
 // v[(l >> 1) & 15] (lanes 2i and 2i + 1 both hold sum i).  Four halving
 // exchanges, then the lane pairs meet.

@@ -76,7 +76,6 @@ struct SMisc {
   unsigned long long redu[kSmConsumerWarps];
   int sel[2];
   int hist[256];
-  int chunk_cnt[kSmConsumers];
   float inv[kMaxNc];
   float ssp[kSmConsumerWarps][kMaxNc];   // per-warp partial sums of squares
   int bcast;
@@ -1051,43 +1050,14 @@ __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
     float* l = p.logits + size_t(b) * V;
     const float rs = k > 1 ? sm_row_inv(p, ms, b) : 1.f;
     for (int i = t; i < V; i += kSmConsumers) keys[i] = f32_order_key(__ldcg(l + i) * rs / T);
-    uint32_t prefix = 0, mask = 0;
-    int remaining = p.top_k;
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      ms.hist[t] = 0;
-      named_bar(SBAR_CONS, kSmConsumers);
-      for (int i = t; i < V; i += kSmConsumers) {
-        const uint32_t kk = keys[i];
-        if ((kk & mask) == prefix) atomicAdd(&ms.hist[(kk >> shift) & 255], 1);
-      }
-      named_bar(SBAR_CONS, kSmConsumers);
-      if (t == 0) {
-        int cum = 0, sel = 0;
-        for (int dg = 255; dg >= 0; --dg) {
-          if (cum + ms.hist[dg] >= remaining) { sel = dg; break; }
-          cum += ms.hist[dg];
-        }
-        ms.sel[0] = sel;
-        ms.sel[1] = remaining - cum;
-      }
-      named_bar(SBAR_CONS, kSmConsumers);
-      prefix |= uint32_t(ms.sel[0]) << shift;
-      mask |= 255u << shift;
-      remaining = ms.sel[1];
-      named_bar(SBAR_CONS, kSmConsumers);
-    }
-    const uint32_t kth = prefix;
+    int remaining;
+    const uint32_t kth = topk_kth_key<kSmConsumers>(keys, V, p.top_k, ms.hist, ms.sel, SBAR_CONS, remaining);
     const int per = (V + kSmConsumers - 1) / kSmConsumers, lo = t * per, hi = min(V, lo + per);
     int cnt = 0;
     for (int i = lo; i < hi; ++i) cnt += keys[i] == kth;
-    ms.chunk_cnt[t] = cnt;
-    named_bar(SBAR_CONS, kSmConsumers);
-    if (t == 0) {
-      int run = 0;
-      for (int i = 0; i < kSmConsumers; ++i) { const int cc = ms.chunk_cnt[i]; ms.chunk_cnt[i] = run; run += cc; }
-    }
-    named_bar(SBAR_CONS, kSmConsumers);
-    int eq_rank = ms.chunk_cnt[t];
+    // keys equal to the threshold are kept lowest index first: this thread's
+    // first one has rank (number of equal keys in earlier threads' chunks)
+    int eq_rank = block_exclusive_scan<kSmConsumers>(cnt, ms.hist, SBAR_CONS);
     const float* gb = p.gumbel + (size_t(b) * p.n_steps + (k - 1)) * V;
     unsigned long long best = 0ull;
     for (int i = lo; i < hi; ++i) {
