@@ -579,17 +579,34 @@ __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
   const float scale = rsqrtf(128.f);
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   uint16_t* kvl = p.kv + size_t(l) * p.Bmax * ctx * 2 * p.kvw;
-  for (int i = (blockIdx.x + gi_q * 13) % G + warp * G; i < n_items; i += kConsumerWarps * G) {
-    const int b = i / p.n_kv, j = i % p.n_kv, r0 = b * P, ch = r0 / c.Nc;
-    // the group's q tiles, its k tile and its v tile: one lane polls each
-    int okl = 1;
-    if (lane < grp + 2) {
-      const int tile = lane < grp ? j * grp + lane
-                                  : (lane == grp ? p.qw / kTileM + j : (p.qw + p.kvw) / kTileM + j);
-      okl = poll_geq(p, tile_cnt(p, gi_q, ch, tile), unsigned(nks));
+  // Each warp takes a contiguous range of items in (kv head, frame) order, so
+  // that consecutive items of one kv head and one 128-row chunk form a group:
+  // one readiness poll before the group, one release of its rows after it.
+  const int gw = warp * G + (blockIdx.x + gi_q * 13) % G, W = kConsumerWarps * G;
+  const int i_beg = int((long long)n_items * gw / W), i_end = int((long long)n_items * (gw + 1) / W);
+  int g_j = -1, g_ch = -1, g_rows = 0;   // the open group
+  auto close_group = [&]() {
+    __syncwarp();   // every lane's writes precede lane 0's release
+    if (lane == 0 && g_rows > 0)
+      for (int g2 = 0; g2 < grp; ++g2) red_release_add(ready_cnt(p, gi_o, g_ch, g_j * grp + g2), unsigned(g_rows));
+    g_rows = 0;
+  };
+  for (int i = i_beg; i < i_end; ++i) {
+    const int j = i / p.B, b = i % p.B, r0 = b * P, ch = r0 / c.Nc;
+    if (j != g_j || ch != g_ch) {
+      close_group();
+      g_j = j;
+      g_ch = ch;
+      // the group's q tiles, its k tile and its v tile: one lane polls each
+      int okl = 1;
+      if (lane < grp + 2) {
+        const int tile = lane < grp ? j * grp + lane
+                                    : (lane == grp ? p.qw / kTileM + j : (p.qw + p.kvw) / kTileM + j);
+        okl = poll_geq(p, tile_cnt(p, gi_q, ch, tile), unsigned(nks));
+      }
+      if (!__all_sync(0xffffffffu, okl)) return false;
+      __syncwarp();   // order every lane's reads after the acquires
     }
-    if (!__all_sync(0xffffffffu, okl)) return false;
-    __syncwarp();   // order every lane's reads after the acquires
     if (lane == 0) ev_cons(p, &ms.evc, EV_ATT_READY, gi_q);
     uint16_t* kvb = kvl + size_t(b) * ctx * 2 * p.kvw + j * 128 + lane * 4;   // + (pos*2 + {0,1}) * kvw
     for (int pp = 0; pp < P; ++pp) {
@@ -665,12 +682,10 @@ __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
       }
       __syncwarp();   // the next position of this frame reads what was stored here
     }
-    __syncwarp();
-    if (lane == 0) {
-      for (int g2 = 0; g2 < grp; ++g2) red_release_add(ready_cnt(p, gi_o, ch, j * grp + g2), unsigned(P));
-      ev_cons(p, &ms.evc, EV_ATT_DONE, gi_q);
-    }
+    g_rows += P;
+    if (lane == 0) ev_cons(p, &ms.evc, EV_ATT_DONE, gi_q);
   }
+  close_group();
   return true;
 }
 
