@@ -26,7 +26,8 @@ What it computes, and where the pages say so:
 
 Readings taken where the pages are silent (each is listed in the design doc):
 positions 0 = small_to_mtp(H), 1 = small_to_mtp(E0[q0]), k+1 = E[k-1][q_k]
-for k = 1..14 (1024-wide tables enter unprojected); RMSNorm x*rsqrt(mean
+for k = 1..14 (hidden-wide tables enter unprojected; Talker-wide tables,
+2048 x 2048 in the exporter page's shapes, pass through small_to_mtp); RMSNorm x*rsqrt(mean
 x^2 + eps)*w; per-head q/k RMSNorm before RoPE; q head h reads kv head
 h // (Hq/Hkv); scale 1/sqrt(head_dim); SwiGLU silu(gate)*up; greedy =
 lowest index among maxima; sampling = Gumbel-max over the top-k of
@@ -233,6 +234,19 @@ class Predictor:
         """small_to_mtp: Linear talker_hidden -> hidden with bias."""
         return (v.astype(F32) @ self.w_proj.T + self.b_proj).astype(F32)
 
+    def step_input(self, k: int, codes: np.ndarray) -> np.ndarray:
+        """The input row of step k >= 2: the code embedding E[k-2][q_{k-1}].
+
+        Tables as wide as the hidden stream enter it unprojected.  Tables as
+        wide as the Talker state (2048 x 2048 in "rightkit-qts 0.2.3 --
+        Qwen3-TTS 1.7B -> QTS GGUF", section "Expected verification shapes")
+        can only enter the 1024-wide stream through small_to_mtp, which the
+        same page lists as the predictor's projection: they are projected
+        like H and E0[q0] (reading; the page gives the shapes, not the
+        wiring)."""
+        e = self.embed[k - 2][np.asarray(codes)].astype(F32)
+        return self.project(e) if self.g.code_embed_dim != self.g.hidden else e
+
     def logits(self, step: int, x_last: np.ndarray) -> np.ndarray:
         """lm_head[step-1] applied to the output-normed final stream."""
         y = rms_norm(x_last, self.out_norm, self.g.rms_eps)
@@ -331,7 +345,7 @@ def predict_frames(P: Predictor, H: np.ndarray, q0: np.ndarray,
     for k in range(1, n + 1):
         if k > 1:
             prev = forced[:, k - 2] if forced is not None else codes[:, k - 2]
-            x = run_position(P.embed[k - 2][np.asarray(prev)].astype(F32), k)
+            x = run_position(P.step_input(k, prev), k)
         lg = P.logits(k, x)
         logits[:, k - 1] = lg
         if gumbel is None:
@@ -401,7 +415,7 @@ def predict_frames_bruteforce(P: Predictor, H: np.ndarray, q0: np.ndarray,
         codes[:, k - 1] = greedy_code(lg)
         if k < g.n_steps:
             nxt = forced[:, k - 1] if forced is not None else codes[:, k - 1]
-            seq.append(P.embed[k - 1][np.asarray(nxt)].astype(F32))
+            seq.append(P.step_input(k + 1, nxt))
     return {"codes": codes, "logits": logits}
 
 
@@ -414,7 +428,7 @@ def code_embeddings(P: Predictor, codes: np.ndarray) -> np.ndarray:
     (reading: the pages name the tables but not their use outside the loop).
     f32, from the bf16 tables."""
     codes = np.asarray(codes)
-    out = np.zeros((codes.shape[0], P.g.n_steps, P.g.hidden), dtype=F32)
+    out = np.zeros((codes.shape[0], P.g.n_steps, P.g.code_embed_dim), dtype=F32)
     for j in range(P.g.n_steps):
         out[:, j] = P.embed[j][codes[:, j]]
     return out

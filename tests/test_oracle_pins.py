@@ -548,3 +548,61 @@ def test_code_embeddings_take_table_j_for_code_j():
     for j in range(g.n_steps):
         np.testing.assert_array_equal(out[:, j, 0], j)
         np.testing.assert_array_equal(out[:, j, 1], codes[:, j])
+
+
+# ---------------------------------------------------------------------------
+# Talker-wide code embeddings (projected step inputs)
+# ---------------------------------------------------------------------------
+
+def _wide_pair(seed=5):
+    """Two toy geometries that differ only in how step inputs enter: A has
+    Talker-wide (80) code tables that pass through small_to_mtp, B has
+    hidden-wide (64) tables that enter unprojected.  A's projection is
+    [I | 0] with bias c, and B's tables are A's first 64 columns plus c, so
+    every input row is the same in both."""
+    import dataclasses
+    ga = dataclasses.replace(S.TOY, talker_hidden=80, code_embed_dim=80)
+    gb = dataclasses.replace(S.TOY, talker_hidden=80, code_embed_dim=64)
+    wa = O.weights_to_f32(S.make_weights(ga, seed=seed, norm_mode="perturbed"))
+    rng = np.random.default_rng(seed + 1)
+    wp = np.zeros((ga.hidden, ga.talker_hidden), np.float32)
+    wp[:, :ga.hidden] = np.eye(ga.hidden, dtype=np.float32)
+    c = (0.1 * rng.standard_normal(ga.hidden)).astype(np.float32)
+    wa["code_pred.small_to_mtp_projection.weight"] = wp
+    wa["code_pred.small_to_mtp_projection.bias"] = c
+    wb = dict(wa)
+    for j in range(ga.n_steps):
+        t = wa[f"code_pred.codec_embd.{j}.weight"]
+        wb[f"code_pred.codec_embd.{j}.weight"] = (t[:, :ga.hidden] + c).astype(np.float32)
+    return ga, gb, O.Predictor(ga, wa), O.Predictor(gb, wb)
+
+
+def test_wide_code_tables_are_projected():
+    """With the projection [I | 0] + c, Talker-wide tables through
+    small_to_mtp give exactly the run of hidden-wide tables holding the
+    first columns plus c: the step inputs pass through the projection, its
+    bias included, from the right table."""
+    ga, gb, PA, PB = _wide_pair()
+    H, q0 = S.toy_inputs(ga, 4, seed=9)
+    a = O.predict_frames(PA, H, q0)
+    b = O.predict_frames(PB, H, q0)
+    np.testing.assert_array_equal(a["codes"], b["codes"])
+    np.testing.assert_allclose(a["logits"], b["logits"], rtol=0, atol=1e-6)
+    # and the wide tables do change the result when the projection is not the identity
+    rng = np.random.default_rng(11)
+    W = dict(PA.W)
+    W["code_pred.small_to_mtp_projection.weight"] = (0.1 * rng.standard_normal(
+        W["code_pred.small_to_mtp_projection.weight"].shape)).astype(np.float32)
+    c = O.predict_frames(O.Predictor(ga, W), H, q0)
+    assert np.abs(c["logits"][:, 1:] - a["logits"][:, 1:]).max() > 1e-3
+
+
+def test_wide_code_tables_cache_equals_full_prefix_recompute():
+    import dataclasses
+    g = dataclasses.replace(S.TOY, talker_hidden=80, code_embed_dim=80)
+    P = O.Predictor.from_raw(g, S.make_weights(g, seed=4, norm_mode="perturbed"))
+    H, q0 = S.toy_inputs(g, 3, seed=2)
+    a = O.predict_frames(P, H, q0)
+    b = O.predict_frames_bruteforce(P, H, q0)
+    np.testing.assert_array_equal(a["codes"], b["codes"])
+    np.testing.assert_allclose(a["logits"], b["logits"], rtol=1e-5, atol=1e-5)
