@@ -246,14 +246,14 @@ class CodePredictor:
         return out_codes
 
     def code_embeddings(self, codes, out=None, stream=None):
-        """E_j[codes[:, j]] for j < n_steps as f32 [B, n_steps, hidden]
+        """E_j[codes[:, j]] for j < n_steps as f32 [B, n_steps, code_embed_dim]
         (qp_code_embeddings): the frame's residual codes in the predictor's
         embedding space."""
         import torch
         B = int(codes.shape[0])
         g = self.geometry
         if out is None:
-            out = torch.empty((B, g.n_steps, g.hidden), dtype=torch.float32, device=codes.device)
+            out = torch.empty((B, g.n_steps, g.code_embed_dim), dtype=torch.float32, device=codes.device)
         _check("qp_code_embeddings", self._lib.qp_code_embeddings(self._h, B, _ptr(codes), _ptr(out),
                                                                   _stream_ptr(stream)))
         return out

@@ -31,7 +31,9 @@ bool geometry_supported(const qp_geometry& g) {
   if (g.head_dim != qp::kHeadDim) return false;
   if (g.n_kv_heads <= 0 || g.n_q_heads <= 0 || g.n_q_heads % g.n_kv_heads) return false;
   if (g.n_steps < 1 || g.n_steps > qp::kMaxSteps) return false;
-  if (g.code_embed_dim != g.hidden) return false;
+  // code tables as wide as the stream (unprojected) or as the Talker state
+  // (each step's input then passes through small_to_mtp)
+  if (g.code_embed_dim != g.hidden && g.code_embed_dim != g.talker_hidden) return false;
   if (g.hidden % 128 || g.ffn % 128 || g.talker_hidden % 128 || g.vocab % 128) return false;
   if (g.hidden > 4096 || g.vocab > 8192) return false;
   if (g.ffn <= 0 || g.vocab <= 0 || g.talker_hidden <= 0 || g.q0_vocab <= 0) return false;
@@ -235,7 +237,8 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
     bytes += matrix_bytes(fmt, qw + 2 * kvw, d) + matrix_bytes(fmt, d, qw) + matrix_bytes(fmt, 2 * g.ffn, d) +
              matrix_bytes(fmt, d, g.ffn) + 2 * carve_size<float>(d) + 2 * carve_size<float>(128);
   for (int j = 0; j < g.n_steps; ++j)
-    bytes += carve_size<uint16_t>(size_t(g.vocab) * d) + carve_size<float>(g.vocab) + matrix_bytes(fmt, g.vocab, d);
+    bytes += carve_size<uint16_t>(size_t(g.vocab) * g.code_embed_dim) + carve_size<float>(g.vocab) +
+             matrix_bytes(fmt, g.vocab, d);
 
   if (h->warena) {
     cudaDeviceSynchronize();
@@ -304,12 +307,13 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
     L.k_norm = put_vec(pre + "attn_k_norm.weight", 128);
   }
   for (int j = 0; j < g.n_steps; ++j) {
-    uint16_t* e = carve<uint16_t>(p, size_t(g.vocab) * d);
+    const size_t ce = size_t(g.code_embed_dim);
+    uint16_t* e = carve<uint16_t>(p, size_t(g.vocab) * ce);
     chk(cudaMemcpyAsync(e, get("code_pred.codec_embd." + std::to_string(j) + ".weight").dev_ptr,
-                        size_t(g.vocab) * d * 2, cudaMemcpyDeviceToDevice, s));
+                        size_t(g.vocab) * ce * 2, cudaMemcpyDeviceToDevice, s));
     h->embed[j] = e;
     float* ss = carve<float>(p, g.vocab);
-    chk(qp::row_sumsq_bf16(e, g.vocab, int(d), ss, s));
+    chk(qp::row_sumsq_bf16(e, g.vocab, int(ce), ss, s));
     h->embed_ss[j] = ss;
     h->head[j] = alloc_mat(g.vocab, d);
     put(h->head[j], 0, "code_pred.lm_head." + std::to_string(j) + ".weight");
@@ -473,7 +477,7 @@ qp_status qp_code_embeddings(qp_handle* h, int B, const int32_t* codes, float* o
   DeviceGuard dg(h->device);
   if (!dg.ok) return QP_ERR_CUDA;
   const qp_geometry& g = h->g;
-  if (qp::code_embeddings(h->embed_dev, g.n_steps, g.vocab, g.hidden, codes, B, out, h->status,
+  if (qp::code_embeddings(h->embed_dev, g.n_steps, g.vocab, g.code_embed_dim, codes, B, out, h->status,
                           static_cast<cudaStream_t>(sv)) != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;

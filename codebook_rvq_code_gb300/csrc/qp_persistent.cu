@@ -1183,6 +1183,7 @@ Scratch scratch_layout(const qp_geometry& g, int bmax) {
 size_t sync_bytes(const qp_geometry& g, int B) { return sync_layout(g, B).total; }
 
 qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s) {
+  if (h->g.code_embed_dim != h->g.hidden) return QP_ERR_ARG;   // Talker-wide code tables: small-batch engine only
   if (a.temperature > 0.f && h->g.vocab > kMaxVocab) return QP_ERR_ARG;
   uint8_t* scratch = static_cast<uint8_t*>(h->sarena);
   const SyncLayout S = sync_layout(h->g, a.B);

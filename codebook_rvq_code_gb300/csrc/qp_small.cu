@@ -116,6 +116,8 @@ struct SParams {
   unsigned long long* trace; int trace_n;
   // the call
   int fuse;                // attention inside the O projection's operand build
+  int proj_in;             // code tables are Talker-wide: each step's input passes through small_to_mtp
+  int32_t* in_code;        // [step][frame]: the code whose embedding is step k's input (proj_in)
   int B; const float* H; const int32_t* q0; int32_t* out_codes; float* out_logits; const int32_t* forced;
   float temperature; int top_k; const float* gumbel;
 };
@@ -126,20 +128,37 @@ struct SG {
   bool scaled;
   const uint16_t* w; float* out;
 };
-__device__ __forceinline__ int sgi_of(const SParams& p, int k, int l, int t) { return 1 + (k - 1) * (4 * p.L + 1) + 4 * l + t; }
-__device__ __forceinline__ int sgi_head(const SParams& p, int k) { return 1 + (k - 1) * (4 * p.L + 1) + 4 * p.L; }
+// The program: GEMM 0 is step 1's projection (rows H_b, E0[q0_b]); step k
+// then has, with Talker-wide code tables and k >= 2, the projection of its
+// input rows, then 4 GEMMs per layer (QKV, O, GU, down) and the head.
+__device__ __forceinline__ int sgi_base(const SParams& p, int k) {
+  return 1 + (k - 1) * (4 * p.L + 1) + p.proj_in * (k - 1);
+}
+__device__ __forceinline__ int sgi_of(const SParams& p, int k, int l, int t) { return sgi_base(p, k) + 4 * l + t; }
+__device__ __forceinline__ int sgi_head(const SParams& p, int k) { return sgi_base(p, k) + 4 * p.L; }
+__device__ __forceinline__ int sgi_proj(const SParams& p, int k) { return k == 1 ? 0 : sgi_base(p, k) - 1; }
 __device__ __forceinline__ int sm_cols(int R) { return (R + 15) & ~15; }
 
 __device__ SG sgemm(const SParams& p, int gi) {
   SG g;
   g.scaled = false;
+  int r = -1;   // the GEMM's place in its step: -1 the projection, 4L the head
   if (gi == 0) {
-    g.kind = S_PROJ; g.k = 1; g.l = 0; g.R = 2 * p.B; g.n_mt = p.d / kTileM; g.n_ks = p.th / kKs;
+    g.k = 1;
+  } else {
+    const int per1 = 4 * p.L + 1, perk = per1 + p.proj_in;
+    if (gi <= per1) {
+      g.k = 1; r = gi - 1;
+    } else {
+      const int j = gi - 1 - per1;
+      g.k = j / perk + 2; r = j % perk - p.proj_in;
+    }
+  }
+  g.R = g.k == 1 ? 2 * p.B : p.B;
+  if (r < 0) {
+    g.kind = S_PROJ; g.l = 0; g.n_mt = p.d / kTileM; g.n_ks = p.th / kKs;
     g.w = p.w_proj; g.out = p.x; g.ld = p.d;
   } else {
-    const int j = gi - 1, per = 4 * p.L + 1, r = j % per;
-    g.k = j / per + 1;
-    g.R = g.k == 1 ? 2 * p.B : p.B;
     if (r == 4 * p.L) {
       g.kind = S_HEAD; g.l = p.L - 1; g.R = p.B; g.n_mt = p.V / kTileM; g.n_ks = p.d / kKs;
       g.w = p.w_head[g.k - 1]; g.out = p.logits; g.ld = p.V; g.scaled = true;
@@ -204,9 +223,9 @@ __device__ void sm_ready(const SParams& p, int gi, const unsigned*& ctr, unsigne
   const SG g = sgemm(p, gi);
   auto all_of = [&](int gp) { const SG q = sgemm(p, gp); ctr = sm_done(p, gp); want = unsigned(q.n_mt * q.n_ks); };
   switch (g.kind) {
-    case S_PROJ: ctr = sm_prep(p, 1); want = unsigned(2 * p.B); return;
+    case S_PROJ: ctr = sm_prep(p, g.k); want = unsigned(g.R); return;   // the step's input rows
     case S_QKV:
-      if (g.l > 0) { all_of(gi - 1); return; }          // the previous layer's down projection
+      if (g.l > 0 || (g.k > 1 && p.proj_in)) { all_of(gi - 1); return; }   // previous down, or the projection
       if (g.k == 1) { all_of(0); return; }              // the input projection
       ctr = sm_prep(p, g.k); want = unsigned(p.B); return;   // the step's input rows
     case S_O: ctr = sm_att(p, g.k, g.l); want = unsigned(p.B * p.n_kv); return;
@@ -463,7 +482,14 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
         // "拆解 Qwen3-TTS：OpenVINO 移植过程中的图分离与调度实践", section 1;
         // their order is a reading)
         const int b = n >> 1;
-        if ((n & 1) == 0) {
+        if (g.k > 1) {
+          // step k >= 2 with Talker-wide code tables: row n is E[k-2][the frame's input code]
+          const int32_t c = p.in_code[size_t(g.k - 1) * p.B + n];
+          const uint4 e = *reinterpret_cast<const uint4*>(p.embed[g.k - 2] + size_t(c) * p.th + k);
+          const uint32_t w[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) { v[2 * i] = bf16_bits_to_f32(w[i] & 0xffff); v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16); }
+        } else if ((n & 1) == 0) {
           const float4 a = __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k));
           const float4 c = __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k + 4));
           v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
@@ -867,7 +893,9 @@ __device__ int sm_code(const SParams& p, SMisc& ms, int step, int b) {
 }
 
 // Step k >= 2 inputs, one frame per CTA: report the previous step's code,
-// embed the next input (teacher-forced if asked) as residual row b.
+// embed the next input (teacher-forced if asked) as residual row b.  With
+// Talker-wide code tables the row starts at the projection's bias instead
+// and the code is recorded for the projection's operand build.
 __device__ bool sm_prepk(const SParams& p, SMisc& ms, int k) {
   const int t = threadIdx.x, G = gridDim.x;
   for (int b = (blockIdx.x + k * 11) % G; b < p.B; b += G) {
@@ -883,6 +911,14 @@ __device__ bool sm_prepk(const SParams& p, SMisc& ms, int k) {
       ms.bcast = nc;
     }
     named_bar(SBAR_CONS, kSmConsumers);
+    if (p.proj_in) {
+      if (t == 0) p.in_code[size_t(k - 1) * p.B + b] = ms.bcast;
+      for (int f = t * 4; f < p.d; f += 4 * kSmConsumers)
+        *reinterpret_cast<float4*>(p.x + size_t(b) * p.d + f) = *reinterpret_cast<const float4*>(p.b_proj + f);
+      named_bar(SBAR_CONS, kSmConsumers);
+      if (t == 0) red_release_add(sm_prep(p, k), 1u);
+      continue;
+    }
     const uint16_t* e = p.embed[k - 2] + size_t(ms.bcast) * p.d;
     for (int f = t * 4; f < p.d; f += 4 * kSmConsumers) {
       const uint2 ev = *reinterpret_cast<const uint2*>(e + f);
@@ -1109,6 +1145,7 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
   SM_SECTION(sm_gemm<S_PROJ>(p, ms, smem, 0, seg));
   for (int k = 1; k <= p.n_steps; ++k) {
     if (k > 1) SM_SECTION(sm_prepk(p, ms, k));
+    if (k > 1 && p.proj_in) SM_SECTION(sm_gemm<S_PROJ>(p, ms, smem, sgi_proj(p, k), seg));
     for (int l = 0; l < p.L; ++l) {
       if (p.fuse) {
         SM_SECTION(sm_gemm<S_QKV>(p, ms, smem, sgi_of(p, k, l, 0), seg));
@@ -1167,13 +1204,14 @@ __global__ void __launch_bounds__(kSmThreads, 1) k_frames_small(const SParams p)
 size_t sm_al256(size_t b) { return (b + 255) & ~size_t(255); }
 
 struct SmSync {
-  size_t done, qkv_tile, att, prep, decided, abort_flag, total;
+  size_t done, qkv_tile, att, prep, decided, in_code, abort_flag, total;
   int NGEMM, NHT;
 };
 
 SmSync sm_sync_layout(const qp_geometry& g, int B) {
   SmSync S{};
-  S.NGEMM = 1 + g.n_steps * (4 * g.layers + 1);
+  const int proj_in = g.code_embed_dim != g.hidden;   // a projection GEMM per step k >= 2
+  S.NGEMM = 1 + g.n_steps * (4 * g.layers + 1) + proj_in * (g.n_steps - 1);
   S.NHT = g.n_q_heads + 2 * g.n_kv_heads;   // 128-row tiles of q|k|v (head_dim 128)
   const size_t steps = size_t(g.n_steps);
   size_t o = 0;
@@ -1182,6 +1220,7 @@ SmSync sm_sync_layout(const qp_geometry& g, int B) {
   S.att = o;        o += sm_al256(steps * g.layers * 4);
   S.prep = o;       o += sm_al256(steps * 4);
   S.decided = o;    o += sm_al256(steps * B * 4);
+  S.in_code = o;    o += sm_al256(steps * B * 4);
   S.abort_flag = o; o += 256;
   S.total = o;
   return S;
@@ -1223,6 +1262,8 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   p.att = reinterpret_cast<unsigned*>(sync + S.att);
   p.prep = reinterpret_cast<unsigned*>(sync + S.prep);
   p.decided = reinterpret_cast<unsigned*>(sync + S.decided);
+  p.in_code = reinterpret_cast<int32_t*>(sync + S.in_code);
+  p.proj_in = g.code_embed_dim != g.hidden;
   p.abort_flag = reinterpret_cast<int*>(sync + S.abort_flag);
   p.status = h->status;
   p.NGEMM = S.NGEMM; p.NHT = S.NHT;

@@ -73,8 +73,13 @@ typedef enum qp_dtype {
  * codebooks, 15 steps, Talker width 2048, 1024-wide code embeddings that
  * enter unprojected, 2048-entry q0 table, RMSNorm eps 1e-6, RoPE theta 1e6.
  * Supported: head_dim 128; n_q_heads a multiple of n_kv_heads;
- * code_embed_dim == hidden; hidden, ffn, talker_hidden and vocab multiples
- * of 128; 1 <= n_steps <= 15. */
+ * code_embed_dim == hidden (code embeddings enter the stream unprojected) or
+ * code_embed_dim == talker_hidden (Talker-wide tables, 2048 x 2048 in
+ * "rightkit-qts 0.2.3 - Qwen3-TTS 1.7B -> QTS GGUF", section "Expected
+ * verification shapes": each step's input then passes through
+ * small_to_mtp like H and E0[q0]; served by the small-batch engine, bf16
+ * weights, B <= 64, and refused with QP_ERR_ARG otherwise); hidden, ffn,
+ * talker_hidden and vocab multiples of 128; 1 <= n_steps <= 15. */
 typedef struct qp_geometry {
   int hidden, layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_steps;
   int talker_hidden, code_embed_dim, q0_vocab;
@@ -203,7 +208,7 @@ int qp_launches_per_call(qp_handle* h, int B, int sampling);
  * space, table n_steps-1 included, which the loop itself never reads
  * (reading: the pages name the tables but not this use; it is inferred from
  * table 14's existence, "rightkit-qts 0.2.3", section "Loader contract").
- * out is [B][n_steps][hidden] f32, device, 16-byte aligned.  A code outside
+ * out is [B][n_steps][code_embed_dim] f32, device, 16-byte aligned.  A code outside
  * [0, vocab) is clamped for addressing and latches QP_ERR_BAD_TOKEN in the
  * device status word.  QP_ERR_STATE if no weights are loaded, QP_ERR_ARG for
  * B < 0, null or misaligned pointers; B == 0 enqueues nothing. */

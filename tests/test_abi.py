@@ -61,7 +61,7 @@ def test_create_rejects_bad_arguments_before_touching_cuda(lib):
     assert lib.qp_create(ctypes.byref(g), 0, ctypes.byref(h)) == 1
     assert lib.qp_create(ctypes.byref(g), 1 << 20, ctypes.byref(h)) == 1
     for field, bad in (("head_dim", 64), ("n_q_heads", 12), ("hidden", 1000), ("n_steps", 16),
-                       ("code_embed_dim", 2048), ("vocab", 100)):
+                       ("code_embed_dim", 1536), ("vocab", 100)):
         gg = qpk.default_geometry()
         setattr(gg, field, bad)
         assert lib.qp_create(ctypes.byref(gg), 1, ctypes.byref(h)) == 1, field
