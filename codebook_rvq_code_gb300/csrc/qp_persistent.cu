@@ -100,6 +100,7 @@ struct PParams {
   int d, qw, kvw, F, V, th, L, n_q, n_kv, n_steps, q0_vocab;
   float eps;
   int q8;
+  int proj_in;   // code tables are Talker-wide: each step's input passes through small_to_mtp
   const uint8_t* w_proj; const __half* s_proj; const float* b_proj; const uint16_t* e0;
   PLayer layer[kMaxLayers];
   const float* out_norm;
@@ -177,18 +178,36 @@ struct GI {
   const uint8_t* w; const __half* s; const uint16_t* act; float* acc;
 };
 
-__device__ __forceinline__ int gi_of(const PParams& p, int k, int l, int t) { return 1 + (k - 1) * (4 * p.L + 1) + 4 * l + t; }
-__device__ __forceinline__ int gi_head(const PParams& p, int k) { return 1 + (k - 1) * (4 * p.L + 1) + 4 * p.L; }
+// The program: GEMM 0 is step 1's projection (rows H_b, E0[q0_b]); step k
+// then has, with Talker-wide code tables and k >= 2, the projection of its
+// input rows, then 4 GEMMs per layer (QKV, O, GU, down) and the head.
+__device__ __forceinline__ int gi_base(const PParams& p, int k) {
+  return 1 + (k - 1) * (4 * p.L + 1) + p.proj_in * (k - 1);
+}
+__device__ __forceinline__ int gi_of(const PParams& p, int k, int l, int t) { return gi_base(p, k) + 4 * l + t; }
+__device__ __forceinline__ int gi_head(const PParams& p, int k) { return gi_base(p, k) + 4 * p.L; }
+__device__ __forceinline__ int gi_proj(const PParams& p, int k) { return k == 1 ? 0 : gi_base(p, k) - 1; }
 
 __device__ GI gemm_inst(const PParams& p, int gi) {
   GI g;
   const int B = p.B;
+  int r = -1;   // the GEMM's place in its step: -1 the projection, 4L the head
   if (gi == 0) {
-    g.kind = G_PROJ; g.k = 1; g.l = 0; g.R = 2 * B; g.n_mt = p.d / kTileM; g.Kdim = p.th;
-    g.w = p.w_proj; g.s = p.s_proj; g.act = p.a1[0]; g.acc = p.x1; g.ld = p.d;
+    g.k = 1;
   } else {
-    const int j = gi - 1, per = 4 * p.L + 1, r = j % per;
-    g.k = j / per + 1;
+    const int per1 = 4 * p.L + 1, perk = per1 + p.proj_in;
+    if (gi <= per1) {
+      g.k = 1; r = gi - 1;
+    } else {
+      const int j = gi - 1 - per1;
+      g.k = j / perk + 2; r = j % perk - p.proj_in;
+    }
+  }
+  if (r < 0) {
+    // step 1: rows H_b, E0[q0_b] into x1; step k >= 2: rows E[k-2][code_b] into xk
+    g.kind = G_PROJ; g.l = 0; g.R = g.k == 1 ? 2 * B : B; g.n_mt = p.d / kTileM; g.Kdim = p.th;
+    g.w = p.w_proj; g.s = p.s_proj; g.act = p.a1[0]; g.acc = g.k == 1 ? p.x1 : p.xk; g.ld = p.d;
+  } else {
     const bool s1 = g.k == 1;
     if (r == 4 * p.L) {
       g.kind = G_HEAD; g.l = p.L - 1; g.R = B; g.n_mt = p.V / kTileM; g.Kdim = p.d;
@@ -526,6 +545,26 @@ __device__ bool prepk_items(const PParams& p, int k) {
     nc = __shfl_sync(0xffffffffu, nc, 0);
     if (nc < 0) return false;
     __syncwarp();   // the writes below follow lane 0's acquire
+    if (p.proj_in) {
+      // Talker-wide table: row b of the step's projection operand is
+      // f16(E[k-2][nc]); the residual row starts at the projection's bias
+      const int gp = gi_proj(p, k);
+      const uint16_t* e = p.embed[k - 2] + size_t(nc) * p.th;
+      for (int kk = lane * 4; kk < p.th; kk += 128) {
+        const uint2 ev = *reinterpret_cast<const uint2*>(e + kk);
+        *reinterpret_cast<uint2*>(p.a1[0] + act_off(b, kk, p.th, c)) =
+            pack4_f16(bf16_bits_to_f32(ev.x & 0xffff), bf16_bits_to_f32(ev.x >> 16), bf16_bits_to_f32(ev.y & 0xffff),
+                      bf16_bits_to_f32(ev.y >> 16));
+      }
+      for (int kk = lane * 4; kk < p.d; kk += 128)
+        *reinterpret_cast<float4*>(p.xk + size_t(b) * p.d + kk) = *reinterpret_cast<const float4*>(p.b_proj + kk);
+      __syncwarp();
+      if (lane == 0) {
+        const int ch = b / c.Nc;
+        for (int ks = 0; ks < p.th / kKs; ++ks) red_release_add(ready_cnt(p, gp, ch, ks), 1);
+      }
+      continue;
+    }
     const uint16_t* e = p.embed[k - 2] + size_t(nc) * p.d;
     for (int kk = lane * 4; kk < p.d; kk += 128) {
       const uint2 ev = *reinterpret_cast<const uint2*>(e + kk);
@@ -706,7 +745,7 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
     const float* w;
     uint16_t* act_n;
     if (KIND == G_PROJ) {
-      gi_n = gi_of(p, 1, 0, 0); w = p.layer[0].attn_norm; act_n = p.a1[1];
+      gi_n = gi_of(p, G.k, 0, 0); w = p.layer[0].attn_norm; act_n = G.k == 1 ? p.a1[1] : p.ak[0];
     } else if (KIND == G_O) {
       gi_n = gi + 1; w = p.layer[G.l].ffn_norm; act_n = G.k == 1 ? p.a1[3] : p.ak[2];
     } else if (G.l + 1 < p.L) {
@@ -979,6 +1018,7 @@ __device__ void consumer_role(const PParams& p, Misc& ms, uint8_t* smem) {
   QP_SECTION(epilogues<G_PROJ>(p, ms, keys, 0, seg));
   for (int k = 1; k <= p.n_steps; ++k) {
     if (k > 1) QP_SECTION(prepk_items(p, k));
+    if (k > 1 && p.proj_in) QP_SECTION(epilogues<G_PROJ>(p, ms, keys, gi_proj(p, k), seg));
     for (int l = 0; l < p.L; ++l) {
       QP_SECTION(epilogues<G_QKV>(p, ms, keys, gi_of(p, k, l, 0), seg));
       QP_SECTION(attn_items(p, ms, k, l));
@@ -1054,7 +1094,7 @@ SyncLayout sync_layout(const qp_geometry& g, int B) {
   if (g.n_q_heads * 128 > ks) ks = g.n_q_heads * 128;
   if (g.ffn > ks) ks = g.ffn;
   S.KS = ks / kKs;
-  S.NGEMM = 1 + g.n_steps * (4 * g.layers + 1);
+  S.NGEMM = 1 + g.n_steps * (4 * g.layers + 1) + (g.code_embed_dim != g.hidden) * (g.n_steps - 1);
   size_t o = 0;
   S.tile_cnt = o; o += al256(size_t(S.NGEMM) * S.NCH * S.MT * 4);
   S.ready = o;    o += al256(size_t(S.NGEMM) * S.NCH * S.KS * 4);
@@ -1075,6 +1115,7 @@ void fill_params(PParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scra
   p.d = g.hidden; p.qw = g.n_q_heads * 128; p.kvw = g.n_kv_heads * 128; p.F = g.ffn; p.V = g.vocab;
   p.th = g.talker_hidden; p.L = g.layers; p.n_q = g.n_q_heads; p.n_kv = g.n_kv_heads; p.n_steps = g.n_steps;
   p.q0_vocab = g.q0_vocab; p.eps = g.rms_eps; p.q8 = h->wfmt == WF_Q8_0;
+  p.proj_in = g.code_embed_dim != g.hidden;
   p.w_proj = h->proj.w; p.s_proj = h->proj.scale; p.b_proj = h->b_proj; p.e0 = h->e0;
   for (int l = 0; l < g.layers; ++l) {
     const LayerW& Lw = h->layer[l];
@@ -1183,7 +1224,6 @@ Scratch scratch_layout(const qp_geometry& g, int bmax) {
 size_t sync_bytes(const qp_geometry& g, int B) { return sync_layout(g, B).total; }
 
 qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s) {
-  if (h->g.code_embed_dim != h->g.hidden) return QP_ERR_ARG;   // Talker-wide code tables: small-batch engine only
   if (a.temperature > 0.f && h->g.vocab > kMaxVocab) return QP_ERR_ARG;
   uint8_t* scratch = static_cast<uint8_t*>(h->sarena);
   const SyncLayout S = sync_layout(h->g, a.B);

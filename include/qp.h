@@ -77,8 +77,7 @@ typedef enum qp_dtype {
  * code_embed_dim == talker_hidden (Talker-wide tables, 2048 x 2048 in
  * "rightkit-qts 0.2.3 - Qwen3-TTS 1.7B -> QTS GGUF", section "Expected
  * verification shapes": each step's input then passes through
- * small_to_mtp like H and E0[q0]; served by the small-batch engine, bf16
- * weights, B <= 64, and refused with QP_ERR_ARG otherwise); hidden, ffn,
+ * small_to_mtp like H and E0[q0], one more projection GEMM per step); hidden, ffn,
  * talker_hidden and vocab multiples of 128; 1 <= n_steps <= 15. */
 typedef struct qp_geometry {
   int hidden, layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, n_steps;

@@ -4,8 +4,8 @@ The exporter page gives the predictor's 15 code-embedding tables as
 2048 x 2048 ("rightkit-qts 0.2.3 - Qwen3-TTS 1.7B -> QTS GGUF", section
 "Expected verification shapes"), twice the stream's width, so a step's input
 E[k-2][q_{k-1}] is projected like H and E0[q0] (the oracle's reading,
-pinned in test_oracle_pins.py).  The small-batch engine serves this geometry
-with a projection GEMM per step; the tile engine refuses it.
+pinned in test_oracle_pins.py).  Both engines serve this geometry with a
+projection GEMM per step.
 """
 import dataclasses
 
@@ -14,7 +14,7 @@ import pytest
 
 import oracle as O
 import synthetic as S
-from _parity import SMALL, TOL, assert_parity, check_parity, decided_prefix, run_gpu
+from _parity import SMALL, assert_parity, check_parity
 
 pytestmark = pytest.mark.gpu
 
@@ -42,10 +42,11 @@ def wide(qpk):
     cp.close()
 
 
+@pytest.mark.parametrize("engine", ["small", "tile"])
 @pytest.mark.parametrize("B", [1, 2, 5, 8, 9, 32, 64])
-def test_wide_tables_match_the_oracle(wide, B):
+def test_wide_tables_match_the_oracle(wide, engine, B):
     raw, P, cp = wide
-    cp.set_engine("small")
+    cp.set_engine(engine)
     try:
         H, q0 = S.toy_inputs(WIDE_SMALL, B, seed=300 + B)
         assert_parity(check_parity(cp, P, H, q0, np.arange(B)))
@@ -61,15 +62,18 @@ def test_wide_tables_sampling(wide):
     assert_parity(check_parity(cp, P, H, q0, np.arange(B), T, k, gum))
 
 
-def test_wide_tables_refused_by_the_tile_engine(wide, qpk):
-    raw, P, cp = wide
-    H, q0 = S.toy_inputs(WIDE_SMALL, 2, seed=1)
-    cp.set_engine("tile")
+def test_wide_tables_q8_0_and_more_frames(qpk):
+    """Q8_0 matrices (the exporter's format for eligible matrices) and 150
+    frames (two 128-row chunks): the tile engine."""
+    raw = S.make_weights(WIDE_SMALL, seed=7, gemm_format="q8_0", norm_mode="perturbed")
+    cp = qpk.CodePredictor(WIDE_SMALL, max_batch=150)
     try:
-        with pytest.raises(qpk.QpError):
-            run_gpu(cp, H, q0)
+        cp.load_raw_weights(raw)
+        H, q0 = S.toy_inputs(WIDE_SMALL, 150, seed=17)
+        rows = np.arange(0, 150, 7)
+        assert_parity(check_parity(cp, O.Predictor.from_raw(WIDE_SMALL, raw), H, q0, rows))
     finally:
-        cp.set_engine("auto")
+        cp.close()
 
 
 def test_wide_tables_feedback_embeddings(wide):
@@ -88,6 +92,9 @@ def test_wide_tables_full_geometry(qpk):
     try:
         cp.load_raw_weights(raw)
         H, q0 = S.toy_inputs(WIDE_FULL, 4, seed=8)
-        assert_parity(check_parity(cp, O.Predictor.from_raw(WIDE_FULL, raw), H, q0, np.arange(4)))
+        P = O.Predictor.from_raw(WIDE_FULL, raw)
+        for engine in ("small", "tile"):
+            cp.set_engine(engine)
+            assert_parity(check_parity(cp, P, H, q0, np.arange(4)))
     finally:
         cp.close()
