@@ -206,7 +206,10 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
   const qp_geometry& g = h->g;
   auto slots = build_slots(g);
   std::unordered_map<std::string, int> seen;
-  int fmt = -1;
+  // one format for the projection and layer matrices, one for the lm-heads
+  // (16-bit sources, f16 or bf16, pack to the same f16 operand format), one
+  // 16-bit encoding for all embedding tables
+  int fmt = -1, hfmt = -1, efmt = -1;
   for (int i = 0; i < n; ++i) {
     if (!w[i].name) return QP_ERR_ARG;
     auto it = slots.find(w[i].name);
@@ -217,18 +220,26 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
     if (!w[i].dev_ptr) return QP_ERR_ARG;
     if (w[i].shape[0] != sl.rows || w[i].shape[1] != sl.cols) return QP_ERR_WEIGHT_SHAPE;
     if (sl.kind == Slot::VECTOR && w[i].dtype != QP_F32) return QP_ERR_WEIGHT_DTYPE;
-    if (sl.kind == Slot::EMBED && w[i].dtype != QP_BF16) return QP_ERR_WEIGHT_DTYPE;
-    if (sl.kind == Slot::MATRIX) {
-      if (w[i].dtype != QP_BF16 && w[i].dtype != QP_Q8_0) return QP_ERR_WEIGHT_DTYPE;
-      const int f = w[i].dtype == QP_BF16 ? qp::WF_BF16 : qp::WF_Q8_0;
-      if (fmt >= 0 && f != fmt) return QP_ERR_WEIGHT_DTYPE;   // one format for all matrices
-      fmt = f;
+    if (sl.kind == Slot::EMBED) {
+      if (w[i].dtype != QP_BF16 && w[i].dtype != QP_F16) return QP_ERR_WEIGHT_DTYPE;
+      if (efmt >= 0 && int(w[i].dtype) != efmt) return QP_ERR_WEIGHT_DTYPE;   // one encoding for all tables
+      efmt = int(w[i].dtype);
     }
-    if (w[i].dtype == QP_BF16 && !aligned16(w[i].dev_ptr)) return QP_ERR_ARG;
+    if (sl.kind == Slot::MATRIX) {
+      if (w[i].dtype != QP_BF16 && w[i].dtype != QP_F16 && w[i].dtype != QP_Q8_0) return QP_ERR_WEIGHT_DTYPE;
+      const int f = w[i].dtype == QP_Q8_0 ? qp::WF_Q8_0 : qp::WF_BF16;
+      int& slot_fmt = std::strncmp(w[i].name, "code_pred.lm_head.", 18) == 0 ? hfmt : fmt;
+      if (slot_fmt >= 0 && f != slot_fmt) return QP_ERR_WEIGHT_DTYPE;
+      slot_fmt = f;
+    }
+    if ((w[i].dtype == QP_BF16 || w[i].dtype == QP_F16) && !aligned16(w[i].dev_ptr)) return QP_ERR_ARG;
     if (w[i].dtype == QP_F32 && (reinterpret_cast<uintptr_t>(w[i].dev_ptr) & 3)) return QP_ERR_ARG;
   }
   for (auto& kv : slots)
     if (!seen.count(kv.first)) return QP_ERR_WEIGHT_MISSING;
+  // 16-bit heads over Q8_0 matrices (the exporter's layout) are served;
+  // Q8_0 heads need Q8_0 matrices
+  if (hfmt == qp::WF_Q8_0 && fmt != qp::WF_Q8_0) return QP_ERR_WEIGHT_DTYPE;
 
   const int64_t d = g.hidden, qw = int64_t(g.n_q_heads) * 128, kvw = int64_t(g.n_kv_heads) * 128;
   size_t bytes = matrix_bytes(fmt, d, g.talker_hidden) + carve_size<float>(d) +
@@ -238,7 +249,7 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
              matrix_bytes(fmt, d, g.ffn) + 2 * carve_size<float>(d) + 2 * carve_size<float>(128);
   for (int j = 0; j < g.n_steps; ++j)
     bytes += carve_size<uint16_t>(size_t(g.vocab) * g.code_embed_dim) + carve_size<float>(g.vocab) +
-             matrix_bytes(fmt, g.vocab, d);
+             matrix_bytes(hfmt, g.vocab, d);
 
   if (h->warena) {
     cudaDeviceSynchronize();
@@ -252,14 +263,16 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
   }
   h->warena_bytes = bytes;
   h->wfmt = fmt;
+  h->hfmt = hfmt;
+  h->embed_f16 = efmt == QP_F16;
   char* p = static_cast<char*>(h->warena);
   cudaError_t err = cudaSuccess;
   auto chk = [&](cudaError_t e) { if (e != cudaSuccess && err == cudaSuccess) err = e; };
   auto get = [&](const std::string& name) -> const qp_weight& { return w[seen[name]]; };
-  auto alloc_mat = [&](int64_t N, int64_t K) {
+  auto alloc_mat = [&](int64_t N, int64_t K, int mfmt) {
     qp::PackedMat m;
-    m.N = int(N); m.K = int(K);
-    if (fmt == qp::WF_BF16) {
+    m.N = int(N); m.K = int(K); m.fmt = mfmt;
+    if (mfmt == qp::WF_BF16) {
       m.w = carve<uint8_t>(p, size_t(N) * K * 2);
     } else {
       m.w = carve<uint8_t>(p, size_t(N) * K);
@@ -269,7 +282,7 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
   };
   auto put = [&](const qp::PackedMat& m, int row0, const std::string& name) {
     const qp_weight& src = get(name);
-    chk(qp::pack_rows(src.dev_ptr, fmt, int(src.shape[0]), int(src.shape[1]), m, row0, s));
+    chk(qp::pack_rows(src.dev_ptr, m.fmt, src.dtype == QP_F16, int(src.shape[0]), int(src.shape[1]), m, row0, s));
   };
   auto put_vec = [&](const std::string& name, int64_t count) {
     float* dst = carve<float>(p, count);
@@ -277,7 +290,7 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
     return static_cast<const float*>(dst);
   };
 
-  h->proj = alloc_mat(d, g.talker_hidden);
+  h->proj = alloc_mat(d, g.talker_hidden, fmt);
   put(h->proj, 0, "code_pred.small_to_mtp_projection.weight");
   h->b_proj = put_vec("code_pred.small_to_mtp_projection.bias", d);
   {
@@ -290,16 +303,16 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
   for (int l = 0; l < g.layers; ++l) {
     const std::string pre = "code_pred.blk." + std::to_string(l) + ".";
     qp::LayerW& L = h->layer[l];
-    L.qkv = alloc_mat(qw + 2 * kvw, d);
+    L.qkv = alloc_mat(qw + 2 * kvw, d, fmt);
     put(L.qkv, 0, pre + "attn_q.weight");
     put(L.qkv, int(qw), pre + "attn_k.weight");
     put(L.qkv, int(qw + kvw), pre + "attn_v.weight");
-    L.o = alloc_mat(d, qw);
+    L.o = alloc_mat(d, qw, fmt);
     put(L.o, 0, pre + "attn_output.weight");
-    L.gu = alloc_mat(2 * g.ffn, d);
+    L.gu = alloc_mat(2 * g.ffn, d, fmt);
     put(L.gu, 0, pre + "ffn_gate.weight");
     put(L.gu, g.ffn, pre + "ffn_up.weight");
-    L.down = alloc_mat(d, g.ffn);
+    L.down = alloc_mat(d, g.ffn, fmt);
     put(L.down, 0, pre + "ffn_down.weight");
     L.attn_norm = put_vec(pre + "attn_norm.weight", d);
     L.ffn_norm = put_vec(pre + "ffn_norm.weight", d);
@@ -313,9 +326,9 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
                         size_t(g.vocab) * ce * 2, cudaMemcpyDeviceToDevice, s));
     h->embed[j] = e;
     float* ss = carve<float>(p, g.vocab);
-    chk(qp::row_sumsq_bf16(e, g.vocab, int(ce), ss, s));
+    chk(qp::row_sumsq_e16(e, g.vocab, int(ce), h->embed_f16, ss, s));
     h->embed_ss[j] = ss;
-    h->head[j] = alloc_mat(g.vocab, d);
+    h->head[j] = alloc_mat(g.vocab, d, hfmt);
     put(h->head[j], 0, "code_pred.lm_head." + std::to_string(j) + ".weight");
   }
   // the tables' device addresses, for qp_code_embeddings (from the handle's
@@ -477,7 +490,7 @@ qp_status qp_code_embeddings(qp_handle* h, int B, const int32_t* codes, float* o
   DeviceGuard dg(h->device);
   if (!dg.ok) return QP_ERR_CUDA;
   const qp_geometry& g = h->g;
-  if (qp::code_embeddings(h->embed_dev, g.n_steps, g.vocab, g.code_embed_dim, codes, B, out, h->status,
+  if (qp::code_embeddings(h->embed_dev, g.n_steps, g.vocab, g.code_embed_dim, codes, B, out, h->status, h->embed_f16,
                           static_cast<cudaStream_t>(sv)) != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;

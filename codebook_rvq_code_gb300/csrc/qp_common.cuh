@@ -18,6 +18,10 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
 __device__ __forceinline__ float f16_bits_to_f32(uint16_t b) { return __half2float(__ushort_as_half(b)); }
 
 __device__ __forceinline__ uint16_t f32_to_f16_bits(float f) { return __half_as_ushort(__float2half_rn(f)); }
+// One element of a 16-bit embedding table, stored as f16 or as bf16 (low 16 bits of b).
+__device__ __forceinline__ float e16_to_f32(uint32_t b, bool f16) {
+  return f16 ? f16_bits_to_f32(uint16_t(b & 0xffff)) : bf16_bits_to_f32(b & 0xffff);
+}
 
 // The f16 tensor-core operand of a Q8_0 weight: d * q rounded once to f16.
 __device__ __forceinline__ float q8_0_operand(float d, int q) { return __half2float(__float2half_rn(d * float(q))); }

@@ -29,6 +29,7 @@ struct PackedMat {
   uint8_t* w = nullptr;
   __half* scale = nullptr;
   int N = 0, K = 0;
+  int fmt = 0;    // WF_BF16 (16-bit source, packed as f16) or WF_Q8_0
 };
 
 struct LayerW {
@@ -93,17 +94,19 @@ struct qp_handle {
   int device = 0;
   int num_sms = 0;
   bool loaded = false;
-  int wfmt = qp::WF_BF16;
+  int wfmt = qp::WF_BF16;       // projection and layer matrices
+  int hfmt = qp::WF_BF16;       // lm-heads
+  bool embed_f16 = false;       // the embedding tables (q0 and code tables) are f16, else bf16
 
   // weights (library-owned arena)
   void* warena = nullptr;
   size_t warena_bytes = 0;
   qp::PackedMat proj;
   const float* b_proj = nullptr;
-  const uint16_t* e0 = nullptr;                 // [q0_vocab, talker_hidden] bf16
+  const uint16_t* e0 = nullptr;                 // [q0_vocab, talker_hidden] 16-bit (embed_f16)
   qp::LayerW layer[qp::kMaxLayers];
   const float* out_norm = nullptr;
-  const uint16_t* embed[qp::kMaxSteps] = {};    // [vocab, hidden] bf16
+  const uint16_t* embed[qp::kMaxSteps] = {};    // [vocab, code_embed_dim] 16-bit (embed_f16)
   const float* embed_ss[qp::kMaxSteps] = {};    // [vocab]: sum of squares of each row
   qp::PackedMat head[qp::kMaxSteps];            // [vocab, hidden]
 
@@ -137,13 +140,16 @@ qp_status run_frames_small(qp_handle* h, const RunArgs& a, uint8_t* scratch, con
 size_t small_smem_bytes();
 // load-time weight preparation (qp_weights.cu)
 size_t packed_bytes(int fmt, int N, int K);
-// Pack `rows` rows of a caller matrix [rows, K] (bf16, or a Q8_0 block
-// stream) into rows [row0, row0 + rows) of the packed matrix dst.
-cudaError_t pack_rows(const void* src, int fmt, int rows, int K, const PackedMat& dst, int row0, cudaStream_t s);
+// Pack `rows` rows of a caller matrix [rows, K] (16-bit -- f16 if src_f16,
+// else bf16 -- or a Q8_0 block stream) into rows [row0, row0 + rows) of the
+// packed matrix dst.
+cudaError_t pack_rows(const void* src, int fmt, bool src_f16, int rows, int K, const PackedMat& dst, int row0,
+                      cudaStream_t s);
 // out[b][j] = tables[j][codes[b][j]] as f32 for b < B, j < n_tables
-// (tables_dev: a device array of n_tables device pointers to [V, d] bf16).
+// (tables_dev: a device array of n_tables device pointers to [V, d] tables,
+// f16 if f16, else bf16).
 cudaError_t code_embeddings(const uint16_t* const* tables_dev, int n_tables, int V, int d, const int32_t* codes,
-                            int B, float* out, int* status, cudaStream_t s);
-// out[r] = sum_i E[r, i]^2 (f32) for a [rows, cols] bf16 table.
-cudaError_t row_sumsq_bf16(const uint16_t* E, int rows, int cols, float* out, cudaStream_t s);
+                            int B, float* out, int* status, bool f16, cudaStream_t s);
+// out[r] = sum_i E[r, i]^2 (f32) for a [rows, cols] 16-bit table (f16 if f16, else bf16).
+cudaError_t row_sumsq_e16(const uint16_t* E, int rows, int cols, bool f16, float* out, cudaStream_t s);
 }  // namespace qp

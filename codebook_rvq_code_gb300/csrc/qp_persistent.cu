@@ -66,6 +66,7 @@ constexpr uint32_t kOffAct = 131072;                           // activation ope
 constexpr uint32_t kOffKeys = kOffAct + kNAct * kActBytes;     // top-k keys
 constexpr uint32_t kOffMisc = kOffKeys + kMaxVocab * 4;
 static_assert(kNSlotQ8 * kQ8SlotBytes <= kOffDeq, "raw Q8_0 slots overlap the dequantised ones");
+static_assert(kSlotBytes / 2 <= kQ8SlotBytes && kNSlotQ8 >= 2, "a 16-bit slice takes two raw slots");
 static_assert(kOffDeq + kNDeq * kSlotBytes <= kOffAct, "dequantised slots overlap the operand slots");
 static_assert(kNSlotF16 * kSlotBytes <= kOffAct, "f16 slots overlap the operand slots");
 
@@ -99,7 +100,9 @@ struct PLayer {
 struct PParams {
   int d, qw, kvw, F, V, th, L, n_q, n_kv, n_steps, q0_vocab;
   float eps;
-  int q8;
+  int q8;        // projection and layer matrices are Q8_0
+  int q8_head;   // lm-heads are Q8_0 (else 16-bit, served from the dequantised slots when q8)
+  bool embed_f16;   // embedding tables are f16, else bf16
   int proj_in;   // code tables are Talker-wide: each step's input passes through small_to_mtp
   const uint8_t* w_proj; const __half* s_proj; const float* b_proj; const uint16_t* e0;
   PLayer layer[kMaxLayers];
@@ -268,18 +271,39 @@ __device__ __forceinline__ unsigned* head_done(const PParams& p, int k, int ch) 
 }
 
 // ---------------------------------------------------------------- producer
+// With Q8_0 matrices and 16-bit heads, a head slice (32 KB of f16) arrives
+// as two 16 KB halves in two consecutive raw slots, and the dequantising
+// warps copy it unchanged into the dequantised slot the MMA warp reads.
+// Every slice thus takes the same path in program order: each mbarrier's
+// waiters stay within one phase of it, which parity waits require.
+__device__ __forceinline__ bool slice_is_q8(const PParams& p, const GI& G) {
+  return p.q8 && (G.kind != G_HEAD || p.q8_head);
+}
+
 __device__ void producer_role(const PParams& p, Misc& ms, uint8_t* smem) {
   const int nslot = p.q8 ? kNSlotQ8 : kNSlotF16;
   const uint32_t stride = p.q8 ? kQ8SlotBytes : kSlotBytes;
   const uint64_t pol = policy_evict_first();
-  uint32_t it = 0;
+  uint32_t it = 0;      // raw-slot copies issued
   for (int gi = 0; gi < p.NGEMM; ++gi) {
     const GI G = gemm_inst(p, gi);
     const Ck c = chunking(G.R);
+    const bool q8g = slice_is_q8(p, G);
     int beg, end;
     my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
     for (int s = beg; s < end; ++s) {
       const int ks = s % G.n_ks, mt = (s / G.n_ks) % G.n_mt;
+      if (p.q8 && !q8g) {
+        const size_t tile = size_t(mt) * G.n_ks + ks;
+        for (int h = 0; h < 2; ++h, ++it) {
+          const uint32_t slot = it % nslot, u = it / nslot;
+          if (u > 0 && !mwait(p, &ms.wempty[slot], (u - 1) & 1)) goto drain;
+          mbar_expect_tx(&ms.wfull[slot], kSlotBytes / 2);
+          bulk_g2s_stream(smem + kOffRing + slot * stride, G.w + tile * kSlotBytes + h * (kSlotBytes / 2),
+                          kSlotBytes / 2, &ms.wfull[slot], pol);
+        }
+        continue;
+      }
       const uint32_t slot = it % nslot, u = it / nslot;
       if (u > 0 && !mwait(p, &ms.wempty[slot], (u - 1) & 1)) goto drain;
       {
@@ -321,21 +345,40 @@ __device__ __forceinline__ uint2 q8x4_to_f16x4(uint32_t w, __half2 d2) {
 
 __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
   const int t = threadIdx.x - kDeqWarp0 * 32;
-  uint32_t it = 0;
+  uint32_t it = 0, rit = 0;   // dequantised-slot sequence; raw slots
   for (int gi = 0; gi < p.NGEMM; ++gi) {
     const GI G = gemm_inst(p, gi);
     const Ck c = chunking(G.R);
+    const bool q8g = slice_is_q8(p, G);
     int beg, end;
     my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
-    for (int s = beg; s < end; ++s, ++it) {
-      const uint32_t rs = it % kNSlotQ8, ru = it / kNSlotQ8, ds = it % kNDeq, du = it / kNDeq;
+    for (int s = beg; s < end; ++s, ++it, rit += q8g ? 1 : 2) {
+      const uint32_t rs = rit % kNSlotQ8, ru = rit / kNSlotQ8, ds = it % kNDeq, du = it / kNDeq;
+      const uint32_t rs2 = (rit + 1) % kNSlotQ8, ru2 = (rit + 1) / kNSlotQ8;
       if (t == 0) {   // the leader waits for every dequant thread, then broadcasts
         bool w = mwait(p, &ms.wfull[rs], ru & 1);
+        if (w && !q8g) w = mwait(p, &ms.wfull[rs2], ru2 & 1);
         if (w && du > 0) w = mwait(p, &ms.dempty[ds], (du - 1) & 1);
         ms.deq_ok = w;
       }
       named_bar(BAR_DEQ, kDeqThreads);
       if (!ms.deq_ok) return;
+      if (!q8g) {
+        // a 16-bit slice: its two halves, unchanged
+        uint4* dq4 = reinterpret_cast<uint4*>(smem + kOffDeq + ds * kSlotBytes);
+        const uint4* h0 = reinterpret_cast<const uint4*>(smem + kOffRing + rs * kQ8SlotBytes);
+        const uint4* h1 = reinterpret_cast<const uint4*>(smem + kOffRing + rs2 * kQ8SlotBytes);
+        constexpr int kHalf4 = int(kSlotBytes / 2 / 16);
+        for (int e = t; e < 2 * kHalf4; e += kDeqThreads) dq4[e] = e < kHalf4 ? h0[e] : h1[e - kHalf4];
+        fence_proxy_async_shared();
+        named_bar(BAR_DEQ, kDeqThreads);
+        if (t == 0) {
+          mbar_arrive(&ms.wempty[rs]);
+          mbar_arrive(&ms.wempty[rs2]);
+          mbar_arrive(&ms.dfull[ds]);
+        }
+        continue;
+      }
       const uint8_t* src = smem + kOffRing + rs * kQ8SlotBytes;
       const int8_t* qv = reinterpret_cast<const int8_t*>(src);
       const __half* sc = reinterpret_cast<const __half*>(src + kQ8Bytes);
@@ -492,8 +535,8 @@ __device__ bool prep1_items(const PParams& p) {
       for (int kk = lane * 4; kk < p.th; kk += 128) {
         const uint2 e = *reinterpret_cast<const uint2*>(p.e0 + size_t(q) * p.th + kk);
         *reinterpret_cast<uint2*>(p.a1[0] + act_off(r, kk, p.th, c)) =
-            pack4_f16(bf16_bits_to_f32(e.x & 0xffff), bf16_bits_to_f32(e.x >> 16), bf16_bits_to_f32(e.y & 0xffff),
-                      bf16_bits_to_f32(e.y >> 16));
+            pack4_f16(e16_to_f32(e.x, p.embed_f16), e16_to_f32(e.x >> 16, p.embed_f16), e16_to_f32(e.y, p.embed_f16),
+                      e16_to_f32(e.y >> 16, p.embed_f16));
       }
     }
     for (int kk = lane * 4; kk < p.d; kk += 128)
@@ -553,8 +596,8 @@ __device__ bool prepk_items(const PParams& p, int k) {
       for (int kk = lane * 4; kk < p.th; kk += 128) {
         const uint2 ev = *reinterpret_cast<const uint2*>(e + kk);
         *reinterpret_cast<uint2*>(p.a1[0] + act_off(b, kk, p.th, c)) =
-            pack4_f16(bf16_bits_to_f32(ev.x & 0xffff), bf16_bits_to_f32(ev.x >> 16), bf16_bits_to_f32(ev.y & 0xffff),
-                      bf16_bits_to_f32(ev.y >> 16));
+            pack4_f16(e16_to_f32(ev.x, p.embed_f16), e16_to_f32(ev.x >> 16, p.embed_f16),
+                      e16_to_f32(ev.y, p.embed_f16), e16_to_f32(ev.y >> 16, p.embed_f16));
       }
       for (int kk = lane * 4; kk < p.d; kk += 128)
         *reinterpret_cast<float4*>(p.xk + size_t(b) * p.d + kk) = *reinterpret_cast<const float4*>(p.b_proj + kk);
@@ -568,8 +611,8 @@ __device__ bool prepk_items(const PParams& p, int k) {
     const uint16_t* e = p.embed[k - 2] + size_t(nc) * p.d;
     for (int kk = lane * 4; kk < p.d; kk += 128) {
       const uint2 ev = *reinterpret_cast<const uint2*>(e + kk);
-      const float v0 = bf16_bits_to_f32(ev.x & 0xffff), v1 = bf16_bits_to_f32(ev.x >> 16);
-      const float v2 = bf16_bits_to_f32(ev.y & 0xffff), v3 = bf16_bits_to_f32(ev.y >> 16);
+      const float v0 = e16_to_f32(ev.x, p.embed_f16), v1 = e16_to_f32(ev.x >> 16, p.embed_f16);
+      const float v2 = e16_to_f32(ev.y, p.embed_f16), v3 = e16_to_f32(ev.y >> 16, p.embed_f16);
       *reinterpret_cast<float4*>(p.xk + size_t(b) * p.d + kk) = make_float4(v0, v1, v2, v3);
       const float4 w = *reinterpret_cast<const float4*>(wn + kk);
       *reinterpret_cast<uint2*>(p.ak[0] + act_off(b, kk, p.d, c)) = pack4_f16(v0 * w.x, v1 * w.y, v2 * w.z, v3 * w.w);
@@ -1114,7 +1157,8 @@ void fill_params(PParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scra
   const qp_geometry& g = h->g;
   p.d = g.hidden; p.qw = g.n_q_heads * 128; p.kvw = g.n_kv_heads * 128; p.F = g.ffn; p.V = g.vocab;
   p.th = g.talker_hidden; p.L = g.layers; p.n_q = g.n_q_heads; p.n_kv = g.n_kv_heads; p.n_steps = g.n_steps;
-  p.q0_vocab = g.q0_vocab; p.eps = g.rms_eps; p.q8 = h->wfmt == WF_Q8_0;
+  p.q0_vocab = g.q0_vocab; p.eps = g.rms_eps; p.q8 = h->wfmt == WF_Q8_0; p.q8_head = h->hfmt == WF_Q8_0;
+  p.embed_f16 = h->embed_f16;
   p.proj_in = g.code_embed_dim != g.hidden;
   p.w_proj = h->proj.w; p.s_proj = h->proj.scale; p.b_proj = h->b_proj; p.e0 = h->e0;
   for (int l = 0; l < g.layers; ++l) {

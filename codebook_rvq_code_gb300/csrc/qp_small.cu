@@ -117,6 +117,7 @@ struct SParams {
   // the call
   int fuse;                // attention inside the O projection's operand build
   int proj_in;             // code tables are Talker-wide: each step's input passes through small_to_mtp
+  bool embed_f16;          // embedding tables are f16, else bf16
   int32_t* in_code;        // [step][frame]: the code whose embedding is step k's input (proj_in)
   int B; const float* H; const int32_t* q0; int32_t* out_codes; float* out_logits; const int32_t* forced;
   float temperature; int top_k; const float* gumbel;
@@ -488,7 +489,7 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
           const uint4 e = *reinterpret_cast<const uint4*>(p.embed[g.k - 2] + size_t(c) * p.th + k);
           const uint32_t w[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) { v[2 * i] = bf16_bits_to_f32(w[i] & 0xffff); v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16); }
+          for (int i = 0; i < 4; ++i) { v[2 * i] = e16_to_f32(w[i], p.embed_f16); v[2 * i + 1] = e16_to_f32(w[i] >> 16, p.embed_f16); }
         } else if ((n & 1) == 0) {
           const float4 a = __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k));
           const float4 c = __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k + 4));
@@ -499,7 +500,7 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
           const uint4 e = __ldg(reinterpret_cast<const uint4*>(p.e0 + size_t(q) * p.th + k));
           const uint32_t w[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) { v[2 * i] = bf16_bits_to_f32(w[i] & 0xffff); v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16); }
+          for (int i = 0; i < 4; ++i) { v[2 * i] = e16_to_f32(w[i], p.embed_f16); v[2 * i + 1] = e16_to_f32(w[i] >> 16, p.embed_f16); }
         }
       } else if (KIND == S_DOWN) {
         float u[8];
@@ -923,8 +924,8 @@ __device__ bool sm_prepk(const SParams& p, SMisc& ms, int k) {
     for (int f = t * 4; f < p.d; f += 4 * kSmConsumers) {
       const uint2 ev = *reinterpret_cast<const uint2*>(e + f);
       *reinterpret_cast<float4*>(p.x + size_t(b) * p.d + f) =
-          make_float4(bf16_bits_to_f32(ev.x & 0xffff), bf16_bits_to_f32(ev.x >> 16), bf16_bits_to_f32(ev.y & 0xffff),
-                      bf16_bits_to_f32(ev.y >> 16));
+          make_float4(e16_to_f32(ev.x, p.embed_f16), e16_to_f32(ev.x >> 16, p.embed_f16), e16_to_f32(ev.y, p.embed_f16),
+                      e16_to_f32(ev.y >> 16, p.embed_f16));
     }
     named_bar(SBAR_CONS, kSmConsumers);
     if (t == 0) red_release_add(sm_prep(p, k), 1u);
@@ -1233,6 +1234,7 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   p.th = g.talker_hidden; p.L = g.layers; p.n_q = g.n_q_heads; p.n_kv = g.n_kv_heads; p.n_steps = g.n_steps;
   p.q0_vocab = g.q0_vocab; p.eps = g.rms_eps;
   p.w_proj = reinterpret_cast<const uint16_t*>(h->proj.w); p.b_proj = h->b_proj; p.e0 = h->e0;
+  p.embed_f16 = h->embed_f16;
   for (int l = 0; l < g.layers; ++l) {
     const LayerW& Lw = h->layer[l];
     p.layer[l].w[0] = reinterpret_cast<const uint16_t*>(Lw.qkv.w);
@@ -1281,7 +1283,7 @@ bool g_sm_attr[kSmMaxDevices] = {};
 size_t small_smem_bytes() { return kSmOffMisc + sizeof(SMisc) + 1024; }
 
 bool small_supported(const qp_handle* h, const RunArgs& a) {
-  if (h->wfmt != WF_BF16) return false;
+  if (h->wfmt != WF_BF16 || h->hfmt != WF_BF16) return false;
   if (a.B < 1 || a.B > kSmallMaxFrames) return false;
   if (a.temperature > 0.f && h->g.vocab > kMaxVocab) return false;
   return true;

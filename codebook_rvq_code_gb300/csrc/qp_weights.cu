@@ -22,9 +22,10 @@ __device__ __forceinline__ size_t packed_off(int n, int k, int K) {
   return size_t(mt) * K * kTileM + size_t(k >> 3) * (kTileM * 8) + (r >> 3) * 64 + (r & 7) * 8 + (k & 7);
 }
 
-// bf16 rows -> f16 packed (exact for values in f16's normal range).
+// 16-bit rows -> f16 packed: f16 sources are copied, bf16 sources
+// converted (exact for values in f16's normal range).
 __global__ void k_pack_bf16(const uint16_t* __restrict__ src, int rows, int K, uint16_t* __restrict__ dst,
-                            int row0) {
+                            int row0, bool src_f16) {
   const size_t total = size_t(rows) * (K / 8);
   for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
     const int r = int(i / (K / 8)), k8 = int(i % (K / 8));
@@ -33,8 +34,9 @@ __global__ void k_pack_bf16(const uint16_t* __restrict__ src, int rows, int K, u
     uint32_t o[4];
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      o[j] = uint32_t(f32_to_f16_bits(bf16_bits_to_f32(w[j] & 0xffff))) |
-             (uint32_t(f32_to_f16_bits(bf16_bits_to_f32(w[j] >> 16))) << 16);
+      o[j] = src_f16 ? w[j]
+                     : uint32_t(f32_to_f16_bits(bf16_bits_to_f32(w[j] & 0xffff))) |
+                           (uint32_t(f32_to_f16_bits(bf16_bits_to_f32(w[j] >> 16))) << 16);
     *reinterpret_cast<uint4*>(dst + packed_off(row0 + r, k8 * 8, K)) = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
@@ -65,22 +67,22 @@ __global__ void k_pack_q8(const uint8_t* __restrict__ src, int rows, int K, int8
   }
 }
 
-__global__ void k_row_sumsq(const uint16_t* __restrict__ E, int cols, float* __restrict__ out) {
+__global__ void k_row_sumsq(const uint16_t* __restrict__ E, int cols, float* __restrict__ out, bool f16) {
   __shared__ float red[32];
   const uint16_t* row = E + size_t(blockIdx.x) * cols;
   float s = 0.f;
   for (int i = threadIdx.x; i < cols; i += blockDim.x) {
-    const float v = bf16_bits_to_f32(row[i]);
+    const float v = e16_to_f32(row[i], f16);
     s += v * v;
   }
   s = block_sum(s, red);
   if (threadIdx.x == 0) out[blockIdx.x] = s;
 }
 
-// out[b][j][:] = E_j[codes[b][j]][:] (bf16 -> f32, exact), 4 values a thread.
+// out[b][j][:] = E_j[codes[b][j]][:] (f16 or bf16 -> f32, exact), 4 values a thread.
 __global__ void k_code_embeddings(const uint16_t* const* __restrict__ tables, int n_tables, int V, int d,
                                   const int32_t* __restrict__ codes, long long B, float* __restrict__ out,
-                                  int* status) {
+                                  int* status, bool f16) {
   const int d4 = d / 4;
   const long long total = B * n_tables * d4;
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
@@ -94,8 +96,7 @@ __global__ void k_code_embeddings(const uint16_t* const* __restrict__ tables, in
     }
     const uint2 e = *reinterpret_cast<const uint2*>(tables[j] + size_t(code) * d + c4 * 4);
     *reinterpret_cast<float4*>(out + row * d + c4 * 4) =
-        make_float4(bf16_bits_to_f32(e.x & 0xffff), bf16_bits_to_f32(e.x >> 16), bf16_bits_to_f32(e.y & 0xffff),
-                    bf16_bits_to_f32(e.y >> 16));
+        make_float4(e16_to_f32(e.x, f16), e16_to_f32(e.x >> 16, f16), e16_to_f32(e.y, f16), e16_to_f32(e.y >> 16, f16));
   }
 }
 
@@ -108,10 +109,11 @@ size_t packed_bytes(int fmt, int N, int K) {
   return size_t(N) * K + size_t(N) * (K / 32) * 2;
 }
 
-cudaError_t pack_rows(const void* src, int fmt, int rows, int K, const PackedMat& dst, int row0, cudaStream_t s) {
+cudaError_t pack_rows(const void* src, int fmt, bool src_f16, int rows, int K, const PackedMat& dst, int row0,
+                      cudaStream_t s) {
   if (fmt == WF_BF16) {
     k_pack_bf16<<<grid_for(size_t(rows) * (K / 8)), 256, 0, s>>>(static_cast<const uint16_t*>(src), rows, K,
-                                                                  reinterpret_cast<uint16_t*>(dst.w), row0);
+                                                                  reinterpret_cast<uint16_t*>(dst.w), row0, src_f16);
   } else {
     k_pack_q8<<<grid_for(size_t(rows) * (K / 32)), 256, 0, s>>>(static_cast<const uint8_t*>(src), rows, K,
                                                                  reinterpret_cast<int8_t*>(dst.w), dst.scale, row0);
@@ -120,14 +122,14 @@ cudaError_t pack_rows(const void* src, int fmt, int rows, int K, const PackedMat
 }
 
 cudaError_t code_embeddings(const uint16_t* const* tables_dev, int n_tables, int V, int d, const int32_t* codes,
-                            int B, float* out, int* status, cudaStream_t s) {
+                            int B, float* out, int* status, bool f16, cudaStream_t s) {
   const size_t total = size_t(B) * n_tables * (d / 4);
-  k_code_embeddings<<<grid_for(total), 256, 0, s>>>(tables_dev, n_tables, V, d, codes, B, out, status);
+  k_code_embeddings<<<grid_for(total), 256, 0, s>>>(tables_dev, n_tables, V, d, codes, B, out, status, f16);
   return cudaGetLastError();
 }
 
-cudaError_t row_sumsq_bf16(const uint16_t* E, int rows, int cols, float* out, cudaStream_t s) {
-  k_row_sumsq<<<rows, 256, 0, s>>>(E, cols, out);
+cudaError_t row_sumsq_e16(const uint16_t* E, int rows, int cols, bool f16, float* out, cudaStream_t s) {
+  k_row_sumsq<<<rows, 256, 0, s>>>(E, cols, out, f16);
   return cudaGetLastError();
 }
 

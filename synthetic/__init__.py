@@ -140,13 +140,16 @@ def pack_q8_0(qs: np.ndarray, d: np.ndarray) -> np.ndarray:
 
 def make_weights(g: Geometry = Geometry(), seed: int = 0, gemm_format: str = BF16,
                  norm_mode: str = "ones", std: float = 0.02,
-                 head_format: Optional[str] = None) -> "OrderedDict[str, RawTensor]":
+                 head_format: Optional[str] = None,
+                 embed_format: str = BF16) -> "OrderedDict[str, RawTensor]":
     """Random-init predictor weights in storage format.
 
-    * gemm weights: N(0, std) -> bf16, or (gemm_format == 'q8_0') int8 values
-      uniform on {-127..127} with one f16 scale ~ U[1e-4, 2e-3] per 32-block;
+    * gemm weights: N(0, std) -> bf16 (or f16 with gemm_format == 'f16'), or
+      (gemm_format == 'q8_0') int8 values uniform on {-127..127} with one f16
+      scale ~ U[1e-4, 2e-3] per 32-block;
     * lm-heads: like gemm weights unless ``head_format`` says otherwise;
-    * embeddings: N(0, std) -> bf16;
+    * embeddings: N(0, std) -> bf16, or f16 with embed_format == 'f16' (the
+      exporter's layout: f16 embeddings and heads over Q8_0 matrices);
     * bias: N(0, std) f32;  norm vectors: 1.0 ('ones') or 1 + N(0, 0.1)
       ('perturbed', so that a dropped norm-weight multiply is visible).
     Everything is drawn from one ``numpy.random.default_rng(seed)`` in the
@@ -164,7 +167,9 @@ def make_weights(g: Geometry = Geometry(), seed: int = 0, gemm_format: str = BF1
             out[name] = RawTensor(name, Q8_0, shape, pack_q8_0(qs, d))
         elif role in ("gemm", "head", "embed"):
             w = rng.standard_normal(shape, dtype=np.float32) * np.float32(std)
-            out[name] = RawTensor(name, BF16, shape, to_bf16_bits(w))
+            f16 = (embed_format if role == "embed" else fmt) == F16
+            out[name] = (RawTensor(name, F16, shape, w.astype(np.float16)) if f16
+                         else RawTensor(name, BF16, shape, to_bf16_bits(w)))
         elif role == "bias":
             w = rng.standard_normal(shape, dtype=np.float32) * np.float32(std)
             out[name] = RawTensor(name, F32, shape, w.astype(np.float32))
