@@ -28,6 +28,8 @@ EXPORTED = [
     "qp_launches_per_call", "qp_destroy", "qp_predict_frames_static", "qp_code_embeddings",
     "qp_set_engine", "qp_trace_enable", "qp_trace_read",   # include/qp_debug.h
     "qp_rvq_normalize", "qp_rvq_decode",                   # include/qp_rvq.h
+    "qp_gguf_open", "qp_gguf_close", "qp_gguf_tensor_count", "qp_gguf_tensor_info",   # include/qp_gguf.h
+    "qp_gguf_geometry", "qp_gguf_load_weights",
 ]
 
 
@@ -92,6 +94,19 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qp_rvq_normalize.argtypes = [vp, vp, i32, i32, i32, vp, vp]
     lib.qp_rvq_decode.restype = i32
     lib.qp_rvq_decode.argtypes = [vp, i32, i32, i32, vp, i32, vp, vp, vp]
+    lib.qp_gguf_open.restype = i32
+    lib.qp_gguf_open.argtypes = [ctypes.c_char_p, ctypes.POINTER(vp)]
+    lib.qp_gguf_close.restype = None
+    lib.qp_gguf_close.argtypes = [vp]
+    lib.qp_gguf_tensor_count.restype = i32
+    lib.qp_gguf_tensor_count.argtypes = [vp]
+    lib.qp_gguf_tensor_info.restype = i32
+    lib.qp_gguf_tensor_info.argtypes = [vp, i32, ctypes.POINTER(cp), ctypes.POINTER(ctypes.c_int),
+                                        ctypes.POINTER(ctypes.c_int64)]
+    lib.qp_gguf_geometry.restype = i32
+    lib.qp_gguf_geometry.argtypes = [vp, vp, ctypes.POINTER(QpGeometry)]
+    lib.qp_gguf_load_weights.restype = i32
+    lib.qp_gguf_load_weights.argtypes = [vp, ctypes.POINTER(vp), i32, vp]
     return lib
 
 
@@ -103,6 +118,52 @@ def lib() -> ctypes.CDLL:
     if _LIB is None:
         _LIB = load_library()
     return _LIB
+
+
+class GgufFile:
+    """A parsed GGUF file (qp_gguf_open): its tensor table and metadata stay
+    on the host until a CodePredictor loads weights from it."""
+
+    def __init__(self, path: str):
+        self._lib = lib()
+        self._f = vp_t()
+        _check("qp_gguf_open", self._lib.qp_gguf_open(str(path).encode(), ctypes.byref(self._f)))
+        self.path = str(path)
+
+    def tensors(self):
+        """[(name, dtype tag or None, (out, in))] in file order (HF shapes)."""
+        out = []
+        names = {v: k for k, v in DTYPES.items()}
+        for i in range(self._lib.qp_gguf_tensor_count(self._f)):
+            name = ctypes.c_char_p()
+            dt = ctypes.c_int()
+            shape = (ctypes.c_int64 * 2)()
+            _check("qp_gguf_tensor_info", self._lib.qp_gguf_tensor_info(self._f, i, ctypes.byref(name),
+                                                                        ctypes.byref(dt), shape))
+            out.append((name.value.decode(), names.get(dt.value), (int(shape[0]), int(shape[1]))))
+        return out
+
+    def geometry(self, talker: "Optional[GgufFile]" = None) -> QpGeometry:
+        """Predictor geometry from this file's keys and tensor shapes; the q0
+        table may come from the Talker's file (qp_gguf_geometry)."""
+        g = QpGeometry()
+        _check("qp_gguf_geometry", self._lib.qp_gguf_geometry(self._f, talker._f if talker else None,
+                                                                ctypes.byref(g)))
+        return g
+
+    def close(self):
+        if getattr(self, "_f", None):
+            self._lib.qp_gguf_close(self._f)
+            self._f = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+vp_t = ctypes.c_void_p
 
 
 def default_geometry() -> QpGeometry:
@@ -284,6 +345,14 @@ class CodePredictor:
 
     def launches_per_call(self, B: int, sampling: bool = False) -> int:
         return int(self._lib.qp_launches_per_call(self._h, B, int(sampling)))
+
+    def load_gguf(self, *files, stream=None):
+        """Load the predictor's tensors from GgufFile objects or paths
+        (predictor file first, then the Talker's for the q0 table)."""
+        opened = [f if isinstance(f, GgufFile) else GgufFile(f) for f in files]
+        arr = (vp_t * len(opened))(*[f._f for f in opened])
+        _check("qp_gguf_load_weights", self._lib.qp_gguf_load_weights(self._h, arr, len(opened),
+                                                                      _stream_ptr(stream)))
 
     def close(self):
         if getattr(self, "_h", None):

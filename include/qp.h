@@ -90,9 +90,15 @@ typedef struct qp_geometry {
  *         "code_pred.small_to_mtp_projection.bias",
  *         "code_pred.codec_embd.7.weight", "code_pred.lm_head.0.weight",
  *         or "talker.codec_embd.weight" (the q0 table).
- * dtype:  matrices (projection weight, attn_q/k/v/output, ffn_gate/up/down,
- *         lm_head.*) accept QP_BF16 or QP_Q8_0 -- all of them the same one;
- *         embedding tables accept QP_BF16; vectors (norms, bias) QP_F32.
+ * dtype:  matrices accept QP_BF16, QP_F16 or QP_Q8_0.  The projection and
+ *         layer matrices (attn_q/k/v/output, ffn_gate/up/down) share one
+ *         format, 16-bit (f16 and bf16 may mix) or Q8_0; the lm-heads share
+ *         one, which may be 16-bit over Q8_0 matrices (the exporter's
+ *         layout) but not Q8_0 over 16-bit ones.  Embedding tables (the
+ *         code tables and the q0 table) accept QP_BF16 or QP_F16, one
+ *         encoding for all of them; vectors (norms, bias) QP_F32.  A
+ *         combination outside these is QP_ERR_WEIGHT_DTYPE.  Q8_0 layers
+ *         are served by the tile engine only.
  * dev_ptr: device memory, row-major HF layout [shape[0], shape[1]]; a Q8_0
  *         tensor is its raw block stream, shape[0] rows of shape[1]/32
  *         blocks.  Vectors use shape = {n, 0}. */
