@@ -284,6 +284,69 @@ def sweep(g, dev, stream, steps, hbm, tf):
     return out
 
 
+def work_exporter(g, B: int):
+    """(bytes, flops) of one call in the exporter's model layout: Talker-wide
+    code tables projected at every step, Q8_0 projection and layer matrices
+    (34 B per 32 weights), f16 heads and tables."""
+    d, qw, kvw, F, V, th = g.hidden, g.n_q_heads * g.head_dim, g.n_kv_heads * g.head_dim, g.ffn, g.vocab, g.talker_hidden
+    layer_params = (qw + 2 * kvw) * d + d * qw + 2 * F * d + d * F
+    head_params, proj_params = V * d, d * th
+    weight_bytes = 34.0 / 32.0 * g.n_steps * (g.layers * layer_params + proj_params) + 2.0 * g.n_steps * head_params
+    io = B * (th * 4 + 4 + g.n_steps * 4 + th * 2 + (g.n_steps - 1) * g.code_embed_dim * 2)
+    positions = g.n_steps + 1
+    flops = B * (2 * positions * g.layers * layer_params + 2 * g.n_steps * head_params + 2 * positions * proj_params)
+    for p_ in range(positions):
+        flops += B * g.layers * g.n_q_heads * (p_ + 1) * g.head_dim * 4
+    return weight_bytes + io, float(flops)
+
+
+def exporter_rows(dev, stream, steps, hbm, tc):
+    """The exporter's model layout (2048-wide code tables through small_to_mtp,
+    Q8_0 matrices, f16 heads and tables), random weights, greedy, at one frame
+    and at 256 frames (tile engine: Q8_0 layers)."""
+    import dataclasses
+    import torch
+    import codebook_rvq_code_gb300 as qpk
+    import synthetic as S
+    g = dataclasses.replace(S.Geometry(), code_embed_dim=S.Geometry().talker_hidden)
+    raw = S.make_weights(g, seed=0, gemm_format="q8_0", head_format="f16", embed_format="f16")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    out = {}
+    for B in (1, 256):
+        cp = qpk.CodePredictor(g, max_batch=B)
+        cp.load_raw_weights(raw, device=dev)
+        H, q0 = S.toy_inputs(g, B, seed=100 + B)
+        tH = torch.from_numpy(H).to(dev)
+        tq = torch.from_numpy(q0).to(dev)
+        codes = torch.empty((B, g.n_steps), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            cp.predict(tH, tq, out_codes=codes, stream=stream)
+        torch.cuda.synchronize()
+        tot = 0.0
+        for i in range(steps):
+            flush.fill_(float(i))
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            cp.predict(tH, tq, out_codes=codes, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        ms = tot / steps
+        nbytes, flops = work_exporter(g, B)
+        t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tc * 1e12)
+        bound = "hbm" if t_hbm >= t_tc else "tensor"
+        out[f"exporter_layout_B{B}"] = {
+            "workload": f"{B} frames, 1.7B geometry, 2048-wide code tables projected each step, "
+                        "Q8_0 matrices, f16 heads and tables, greedy",
+            "ms_per_call": ms, "us_per_step": 1e3 * ms / g.n_steps, "frames_per_s": B / (ms / 1e3),
+            "device_status": cp.device_status(),
+            "roofline": {"bound": bound, "frac": (t_hbm if bound == "hbm" else t_tc) / (ms / 1e3),
+                         "algorithmic_bytes": nbytes, "algorithmic_flops": flops}}
+        cp.close()
+    return out
+
+
 def rvq_rows(dev, stream, steps, hbm):
     """The RVQ codebook kernels (include/qp_rvq.h) on a codec-sized workload:
     16 EMA codebooks of 2048 x 512 and 16384 frames' codes.  The codec's
@@ -477,6 +540,7 @@ def main():
     if not args.no_sweep and world == 1:
         line["per_config"] = sweep(g, dev, stream, max(5, min(args.steps, 20)), hbm, tf_sust)
         line["next_rows"] = rvq_rows(dev, stream, max(5, min(args.steps, 20)), hbm)
+        line["next_rows"].update(exporter_rows(dev, stream, max(5, min(args.steps, 20)), hbm, tf_sust))
     if not args.no_cpu_baseline:
         fps, done, el = time_oracle(g, raw, w, min(B, 8), 10.0)
         line["cpu_baseline"] = {"value": fps, "unit": "frames/s", "cores": oracle_threads(), "kind": "oracle",

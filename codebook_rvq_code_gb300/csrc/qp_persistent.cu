@@ -1058,10 +1058,10 @@ __device__ void consumer_role(const PParams& p, Misc& ms, uint8_t* smem) {
     if (ms.fail) return;                      \
   }
   QP_SECTION(prep1_items(p));
-  QP_SECTION(epilogues<G_PROJ>(p, ms, keys, 0, seg));
   for (int k = 1; k <= p.n_steps; ++k) {
     if (k > 1) QP_SECTION(prepk_items(p, k));
-    if (k > 1 && p.proj_in) QP_SECTION(epilogues<G_PROJ>(p, ms, keys, gi_proj(p, k), seg));
+    // one call site: a section inlined twice costs instruction fetch
+    if (k == 1 || p.proj_in) QP_SECTION(epilogues<G_PROJ>(p, ms, keys, gi_proj(p, k), seg));
     for (int l = 0; l < p.L; ++l) {
       QP_SECTION(epilogues<G_QKV>(p, ms, keys, gi_of(p, k, l, 0), seg));
       QP_SECTION(attn_items(p, ms, k, l));

@@ -1143,10 +1143,10 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
     if (ms.fail) return;                      \
   }
   SM_SECTION(sm_prep1(p));
-  SM_SECTION(sm_gemm<S_PROJ>(p, ms, smem, 0, seg));
   for (int k = 1; k <= p.n_steps; ++k) {
     if (k > 1) SM_SECTION(sm_prepk(p, ms, k));
-    if (k > 1 && p.proj_in) SM_SECTION(sm_gemm<S_PROJ>(p, ms, smem, sgi_proj(p, k), seg));
+    // one call site: a GEMM section inlined twice costs instruction fetch
+    if (k == 1 || p.proj_in) SM_SECTION(sm_gemm<S_PROJ>(p, ms, smem, sgi_proj(p, k), seg));
     for (int l = 0; l < p.L; ++l) {
       if (p.fuse) {
         SM_SECTION(sm_gemm<S_QKV>(p, ms, smem, sgi_of(p, k, l, 0), seg));
