@@ -347,6 +347,70 @@ def exporter_rows(dev, stream, steps, hbm, tc):
     return out
 
 
+def work_step_call(g, B: int, n_groups: int, ctx: float):
+    """Algorithmic bytes of one state-slot step call: one step's layer
+    weights, one head per distinct step among the rows, each row's KV reads
+    (ctx positions on average) and appended position, input code, output
+    code and logits."""
+    d, qw, kvw, F, V = g.hidden, g.n_q_heads * g.head_dim, g.n_kv_heads * g.head_dim, g.ffn, g.vocab
+    layer_bytes = 2 * ((qw + 2 * kvw) * d + d * qw + 2 * F * d + d * F)
+    kv = B * g.layers * (ctx + 1) * 2 * kvw * 2
+    io = B * (4 + 4 + V * 4 + d * 2)
+    return g.layers * layer_bytes + n_groups * V * d * 2 + kv + io
+
+
+def sched_rows(dev, stream, steps, hbm):
+    """State-slot step calls (include/qp_sched.h): B rows at mixed steps
+    2..15 (one head per distinct step), each call one step of each row; the
+    begin call of B new frames beside it.  L2 flushed between calls."""
+    import numpy as np
+    import torch
+    import codebook_rvq_code_gb300 as qpk
+    import synthetic as S
+    g = S.Geometry()
+    raw = S.make_weights(g, seed=0)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    cp = qpk.CodePredictor(g, max_batch=64)
+    cp.load_raw_weights(raw, device=dev)
+    out = {}
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        tot = 0.0
+        for i in range(steps):
+            flush.fill_(float(i))
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        return tot / steps
+
+    for B in (1, 32, 64):
+        H, q0 = S.toy_inputs(g, B, seed=700 + B)
+        tH, tq = torch.from_numpy(H).to(dev), torch.from_numpy(q0).to(dev)
+        slots = list(range(B))
+        q1 = torch.empty(B, dtype=torch.int32, device=dev)
+        ms_begin = timed(lambda: cp.begin_frames(slots, tH, tq, out_q1=q1, stream=stream))
+        st = [8] if B == 1 else [2 + b % (g.n_steps - 1) for b in range(B)]
+        codes = torch.empty(B, dtype=torch.int32, device=dev)
+        ms_step = timed(lambda: cp.step_frames(slots, st, q1, out_codes=codes, stream=stream))
+        n_groups = len(set(st))
+        ctx = float(np.mean(st))
+        nbytes = work_step_call(g, B, n_groups, ctx)
+        out[f"step_call_B{B}"] = {
+            "workload": f"{B} rows at steps {sorted(set(st))} ({n_groups} step groups), 1.7B geometry, bf16, greedy",
+            "ms_per_call": ms_step, "rows_per_s": B / (ms_step / 1e3), "begin_ms_per_call": ms_begin,
+            "device_status": cp.device_status(),
+            "roofline": {"bound": "hbm", "frac": nbytes / (hbm * 1e9) / (ms_step / 1e3), "algorithmic_bytes": nbytes}}
+    cp.close()
+    return out
+
+
 def rvq_rows(dev, stream, steps, hbm):
     """The RVQ codebook kernels (include/qp_rvq.h) on a codec-sized workload:
     16 EMA codebooks of 2048 x 512 and 16384 frames' codes.  The codec's
@@ -541,6 +605,7 @@ def main():
         line["per_config"] = sweep(g, dev, stream, max(5, min(args.steps, 20)), hbm, tf_sust)
         line["next_rows"] = rvq_rows(dev, stream, max(5, min(args.steps, 20)), hbm)
         line["next_rows"].update(exporter_rows(dev, stream, max(5, min(args.steps, 20)), hbm, tf_sust))
+        line["next_rows"].update(sched_rows(dev, stream, max(5, min(args.steps, 20)), hbm))
     if not args.no_cpu_baseline:
         fps, done, el = time_oracle(g, raw, w, min(B, 8), 10.0)
         line["cpu_baseline"] = {"value": fps, "unit": "frames/s", "cores": oracle_threads(), "kind": "oracle",

@@ -10,6 +10,7 @@
 
 #include "qp_internal.h"
 #include "../../include/qp_debug.h"
+#include "../../include/qp_sched.h"
 
 namespace {
 
@@ -411,6 +412,50 @@ qp_status qp_predict_frames_static(qp_handle* h, int B, const float* H, const in
   qp::RunArgs a;
   a.B = B; a.H = H; a.q0 = q0; a.out_codes = out_codes; a.out_logits = out_logits;
   return qp::run_frames_static(h, a, static_cast<cudaStream_t>(s));
+}
+
+// Slots of one state-slot call: each in [0, max_batch), none repeated.
+static bool slots_ok(const qp_handle* h, int B, const int32_t* slots) {
+  for (int b = 0; b < B; ++b) {
+    if (slots[b] < 0 || slots[b] >= h->max_batch) return false;
+    for (int c = 0; c < b; ++c)
+      if (slots[c] == slots[b]) return false;
+  }
+  return true;
+}
+
+static qp_status run_slots(qp_handle* h, const qp::SlotArgs& a, qp_stream s) {
+  DeviceGuard dg(h->device);
+  if (!dg.ok) return QP_ERR_CUDA;
+  return qp::run_slots_small(h, a, static_cast<uint8_t*>(h->sarena), h->scr, h->max_batch, static_cast<cudaStream_t>(s));
+}
+
+qp_status qp_begin_frames(qp_handle* h, int B, const int32_t* slots, const float* H, const int32_t* q0,
+                          int32_t* out_q1, float* out_logits, qp_stream s) {
+  if (!h) return QP_ERR_ARG;
+  if (!h->loaded) return QP_ERR_STATE;
+  if (B < 1 || B > h->max_batch || B > qp::kSmallMaxFrames || !slots || !H || !q0 || !out_q1) return QP_ERR_ARG;
+  if (!aligned16(H) || (out_logits && !aligned16(out_logits)) || !slots_ok(h, B, slots)) return QP_ERR_ARG;
+  if (h->wfmt != qp::WF_BF16 || h->hfmt != qp::WF_BF16) return QP_ERR_ARG;
+  qp::SlotArgs a;
+  a.mode = 1; a.B = B; a.slots = slots; a.H = H; a.q0 = q0; a.out_codes = out_q1; a.out_logits = out_logits;
+  return run_slots(h, a, s);
+}
+
+qp_status qp_step_frames(qp_handle* h, int B, const int32_t* slots, const int32_t* steps, const int32_t* codes_in,
+                         int32_t* out_codes, float* out_logits, qp_stream s) {
+  if (!h) return QP_ERR_ARG;
+  if (!h->loaded) return QP_ERR_STATE;
+  if (B < 1 || B > h->max_batch || B > qp::kSmallMaxFrames || !slots || !steps || !codes_in || !out_codes)
+    return QP_ERR_ARG;
+  if ((out_logits && !aligned16(out_logits)) || !slots_ok(h, B, slots)) return QP_ERR_ARG;
+  for (int b = 0; b < B; ++b)
+    if (steps[b] < 2 || steps[b] > h->g.n_steps) return QP_ERR_ARG;
+  if (h->wfmt != qp::WF_BF16 || h->hfmt != qp::WF_BF16) return QP_ERR_ARG;
+  qp::SlotArgs a;
+  a.mode = 2; a.B = B; a.slots = slots; a.steps = steps; a.codes_in = codes_in; a.out_codes = out_codes;
+  a.out_logits = out_logits;
+  return run_slots(h, a, s);
 }
 
 qp_status qp_get_device_status(qp_handle* h, qp_stream sv) {

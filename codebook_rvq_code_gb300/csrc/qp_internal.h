@@ -56,6 +56,21 @@ struct RunArgs {
   const float* gumbel = nullptr;
 };
 
+// A state-slot call (include/qp_sched.h): mode 1 runs step 1 of new frames
+// into their slots, mode 2 one step of rows at their own steps.  slots and
+// steps are host arrays [B]; the rest are device pointers in caller order.
+struct SlotArgs {
+  int mode = 0;
+  int B = 0;
+  const int32_t* slots = nullptr;
+  const int32_t* steps = nullptr;      // mode 2
+  const float* H = nullptr;            // mode 1
+  const int32_t* q0 = nullptr;         // mode 1
+  const int32_t* codes_in = nullptr;   // mode 2
+  int32_t* out_codes = nullptr;
+  float* out_logits = nullptr;
+};
+
 // Rows of the MMA operand buffer for R activation rows (chunks of <= 128).
 inline size_t operand_rows(size_t R) {
   const size_t r16 = (R + 15) / 16 * 16;
@@ -138,6 +153,9 @@ bool small_supported(const qp_handle* h, const RunArgs& a);
 qp_status run_frames_small(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
                            cudaStream_t s);
 size_t small_smem_bytes();
+// state-slot calls on the small-batch engine's kernel built from qp_small_slots.cu
+qp_status run_slots_small(qp_handle* h, const SlotArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
+                          cudaStream_t s);
 // load-time weight preparation (qp_weights.cu)
 size_t packed_bytes(int fmt, int N, int K);
 // Pack `rows` rows of a caller matrix [rows, K] (16-bit -- f16 if src_f16,

@@ -28,6 +28,8 @@
 // grid-wide abort flag; each role walks the program in one order and waits
 // only on work earlier in that order, and all CTAs are co-resident
 // (cooperative launch).
+#include <algorithm>
+
 #include "qp_device.cuh"
 
 namespace qp {
@@ -63,6 +65,19 @@ constexpr int S_OA = 6;
 // when attention runs as a section of its own, each attention item scales
 // its frame's q, k and v itself, so the GEMM needs no row-scale pass.
 constexpr int S_QKVU = 7;
+
+// Call modes: a whole frame loop; step 1 only, into state slots; one step
+// of rows at mixed steps, from state slots (include/qp_sched.h).
+enum { SM_RUN = 0, SM_BEGIN = 1, SM_STEP = 2 };
+// This translation unit's kernel: the whole frame loop (SM_RUN), or, built
+// from qp_small_slots.cu, the state-slot calls (SM_BEGIN, SM_STEP).  Two
+// kernels keep the frame loop free of the state-slot paths' code and
+// registers; the state-slot kernel leaves out the fused attention and
+// sampling, which its calls do not use.
+#ifndef QP_SMALL_SLOTS
+#define QP_SMALL_SLOTS 0
+#endif
+constexpr bool kSmSlots = QP_SMALL_SLOTS != 0;
 
 struct SMisc {
   uint64_t wfull[kSmNW], wempty[kSmNW];
@@ -118,14 +133,31 @@ struct SParams {
   int fuse;                // attention inside the O projection's operand build
   int proj_in;             // code tables are Talker-wide: each step's input passes through small_to_mtp
   bool embed_f16;          // embedding tables are f16, else bf16
+  // state-slot calls (SM_BEGIN, SM_STEP); rows of an SM_STEP call are sorted
+  // by step, and row b is the caller's row row_perm[b]
+  int mode, n_run, k_first;        // steps run this call: k_first .. k_first + n_run - 1
+  int n_heads;                     // head GEMMs per step: 1, or one per step group (SM_STEP)
+  // row b's KV state slot, step and caller row; rows [group_start[h],
+  // group_start[h + 1]) are at step group_step[h] (SM_STEP)
+  int32_t row_slot[kSmallMaxFrames], row_step[kSmallMaxFrames], row_perm[kSmallMaxFrames];
+  int32_t group_start[kMaxSteps + 1], group_step[kMaxSteps];
+  const int32_t* code_in;          // SM_STEP: device [B], caller order
   int32_t* in_code;        // [step][frame]: the code whose embedding is step k's input (proj_in)
   int B; const float* H; const int32_t* q0; int32_t* out_codes; float* out_logits; const int32_t* forced;
   float temperature; int top_k; const float* gumbel;
 };
 
+__device__ __forceinline__ int sm_mode(const SParams& p) { return kSmSlots ? p.mode : int(SM_RUN); }
+__device__ __forceinline__ int sm_k_first(const SParams& p) { return kSmSlots ? p.k_first : 1; }
+__device__ __forceinline__ int sm_n_run(const SParams& p) { return kSmSlots ? p.n_run : p.n_steps; }
+__device__ __forceinline__ int sm_n_heads(const SParams& p) { return kSmSlots ? p.n_heads : 1; }
+__device__ __forceinline__ bool sm_fused(const SParams& p) { return !kSmSlots && p.fuse; }
+__device__ __forceinline__ bool sm_sampled(const SParams& p) { return !kSmSlots && p.temperature > 0.f; }
+
 // One GEMM of the program: n_mt tiles of 128 weight rows x n_ks slices of K.
 struct SG {
   int kind, k, l, R, N, n_mt, n_ks, ld;
+  int r0;   // first activation / output row (a step group's head)
   bool scaled;
   const uint16_t* w; float* out;
 };
@@ -133,18 +165,34 @@ struct SG {
 // then has, with Talker-wide code tables and k >= 2, the projection of its
 // input rows, then 4 GEMMs per layer (QKV, O, GU, down) and the head.
 __device__ __forceinline__ int sgi_base(const SParams& p, int k) {
+  // an SM_STEP call's program: [projection], 4 GEMMs per layer, one head per step group
+  if (sm_mode(p) == SM_STEP) return p.proj_in;
   return 1 + (k - 1) * (4 * p.L + 1) + p.proj_in * (k - 1);
 }
 __device__ __forceinline__ int sgi_of(const SParams& p, int k, int l, int t) { return sgi_base(p, k) + 4 * l + t; }
 __device__ __forceinline__ int sgi_head(const SParams& p, int k) { return sgi_base(p, k) + 4 * p.L; }
 __device__ __forceinline__ int sgi_proj(const SParams& p, int k) { return k == 1 ? 0 : sgi_base(p, k) - 1; }
+// the KV state of activation row b's frame: its slot in state-slot calls
+__device__ __forceinline__ int sm_slot(const SParams& p, int b) { return sm_mode(p) == SM_RUN ? b : p.row_slot[b]; }
 __device__ __forceinline__ int sm_cols(int R) { return (R + 15) & ~15; }
 
 __device__ SG sgemm(const SParams& p, int gi) {
   SG g;
   g.scaled = false;
+  g.r0 = 0;
   int r = -1;   // the GEMM's place in its step: -1 the projection, 4L the head
-  if (gi == 0) {
+  if (sm_mode(p) == SM_STEP) {
+    g.k = 2;
+    r = gi - p.proj_in;
+    if (r >= 4 * p.L) {   // the head of step group h
+      const int h = r - 4 * p.L;
+      g.kind = S_HEAD; g.k = p.group_step[h]; g.l = p.L - 1; g.r0 = p.group_start[h];
+      g.R = p.group_start[h + 1] - p.group_start[h]; g.n_mt = p.V / kTileM; g.n_ks = p.d / kKs;
+      g.w = p.w_head[g.k - 1]; g.out = p.logits; g.ld = p.V;
+      g.N = sm_cols(g.R);
+      return g;
+    }
+  } else if (gi == 0) {
     g.k = 1;
   } else {
     const int per1 = 4 * p.L + 1, perk = per1 + p.proj_in;
@@ -230,7 +278,8 @@ __device__ void sm_ready(const SParams& p, int gi, const unsigned*& ctr, unsigne
       if (g.k == 1) { all_of(0); return; }              // the input projection
       ctr = sm_prep(p, g.k); want = unsigned(p.B); return;   // the step's input rows
     case S_O: ctr = sm_att(p, g.k, g.l); want = unsigned(p.B * p.n_kv); return;
-    default: all_of(gi - 1); return;                     // GU: O; DOWN: GU; HEAD: the last DOWN
+    case S_HEAD: all_of(sm_mode(p) == SM_STEP ? sgi_of(p, 2, p.L - 1, 3) : gi - 1); return;   // the last DOWN
+    default: all_of(gi - 1); return;                     // GU: O; DOWN: GU
   }
 }
 
@@ -486,7 +535,8 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
         if (g.k > 1) {
           // step k >= 2 with Talker-wide code tables: row n is E[k-2][the frame's input code]
           const int32_t c = p.in_code[size_t(g.k - 1) * p.B + n];
-          const uint4 e = *reinterpret_cast<const uint4*>(p.embed[g.k - 2] + size_t(c) * p.th + k);
+          const int kt = sm_mode(p) == SM_STEP ? p.row_step[n] : g.k;   // the row's own step in SM_STEP
+          const uint4 e = *reinterpret_cast<const uint4*>(p.embed[kt - 2] + size_t(c) * p.th + k);
           const uint32_t w[4] = {e.x, e.y, e.z, e.w};
 #pragma unroll
           for (int i = 0; i < 4; ++i) { v[2 * i] = e16_to_f32(w[i], p.embed_f16); v[2 * i + 1] = e16_to_f32(w[i] >> 16, p.embed_f16); }
@@ -515,7 +565,7 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
         int row = n;
         if (kQkv<KIND>) wn = p.layer[g.l].attn_norm;
         else if (KIND == S_GU) wn = p.layer[g.l].ffn_norm;
-        else { wn = p.out_norm; row = g.k == 1 ? 2 * n + 1 : n; }   // head: each frame's last position
+        else { wn = p.out_norm; row = g.k == 1 ? 2 * n + 1 : g.r0 + n; }   // head: each frame's last position
         // both loads in flight together
         const float4 w0 = __ldg(reinterpret_cast<const float4*>(wn + k));
         const float4 w1 = __ldg(reinterpret_cast<const float4*>(wn + k + 4));
@@ -620,7 +670,7 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
           const float s = ms.inv[n];
           x.x *= s; x.y *= s; x.z *= s; x.w *= s;
         }
-        red_add_v4_f32(g.out + size_t(n) * g.ld + m0 + k4, x);
+        red_add_v4_f32(g.out + size_t(g.r0 + n) * g.ld + m0 + k4, x);
       }
     }
     __syncwarp();
@@ -839,8 +889,17 @@ __device__ float sm_row_inv(const SParams& p, SMisc& ms, int row) {
 // step's accumulation.
 // Sampling: the decision the sampling pass published.
 __device__ int sm_code(const SParams& p, SMisc& ms, int step, int b) {
+  // the head GEMM that produced row b's logits, and where the call's outputs go
+  int gih = sgi_head(p, step), out_row = b, out_step = step - sm_k_first(p);
+  if (sm_mode(p) == SM_STEP) {   // one step per row: the row's step group's head, the caller's row
+    int h = 0;
+    while (h + 1 < sm_n_heads(p) && b >= p.group_start[h + 1]) ++h;
+    gih += h;
+    out_row = p.row_perm[b];
+    out_step = 0;
+  }
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-  if (p.temperature > 0.f) {
+  if (sm_sampled(p)) {
     if (t == 0) {
       unsigned* dp = p.decided + size_t(step - 1) * p.B + b;
       ms.bcast = poll_geq(p, dp, 1u) ? int(ld_acquire_u32(dp)) - 1 : -1;
@@ -851,13 +910,13 @@ __device__ int sm_code(const SParams& p, SMisc& ms, int step, int b) {
     return code;
   }
   if (t == 0) {
-    const SG h = sgemm(p, sgi_head(p, step));
-    ms.bcast = poll_geq(p, sm_done(p, sgi_head(p, step)), unsigned(h.n_mt * h.n_ks)) ? 0 : -1;
+    const SG h = sgemm(p, gih);
+    ms.bcast = poll_geq(p, sm_done(p, gih), unsigned(h.n_mt * h.n_ks)) ? 0 : -1;
   }
   named_bar(SBAR_CONS, kSmConsumers);
   if (ms.bcast < 0) return -1;
   float* row = p.logits + size_t(b) * p.V;
-  float* dst = p.out_logits ? p.out_logits + (size_t(b) * p.n_steps + (step - 1)) * p.V : nullptr;
+  float* dst = p.out_logits ? p.out_logits + (size_t(out_row) * sm_n_run(p) + out_step) * p.V : nullptr;
   const float rs = dst && step > 1 ? sm_row_inv(p, ms, b) : 1.f;   // the head's input row
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   unsigned long long best = 0ull;
@@ -893,17 +952,61 @@ __device__ int sm_code(const SParams& p, SMisc& ms, int step, int b) {
   return unpack_argmax_index(v);
 }
 
+// SM_STEP inputs, one row per CTA: row b (the caller's row row_perm[b]) is
+// at step row_step[b], and its input code comes from the caller.  The
+// residual row starts at the row's code embedding (or, with Talker-wide
+// tables, at the projection's bias, the code recorded for the projection);
+// the row of both q|k|v accumulators and the logit row start at zero.
+__device__ bool sm_prep_step(const SParams& p, SMisc& ms) {
+  const int t = threadIdx.x, G = gridDim.x, qkvw = p.qw + 2 * p.kvw;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int b = (blockIdx.x + 3) % G; b < p.B; b += G) {
+    if (t == 0) {
+      int c = p.code_in[p.row_perm[b]];
+      if (c < 0 || c >= p.V) {
+        set_status(p.status, QP_ERR_BAD_TOKEN);
+        c = c < 0 ? 0 : p.V - 1;
+      }
+      ms.bcast = c;
+      if (p.proj_in) p.in_code[size_t(1) * p.B + b] = c;   // read by the step's projection (k = 2 slot)
+    }
+    named_bar(SBAR_CONS, kSmConsumers);
+    const int c = ms.bcast;
+    const uint16_t* e = p.embed[p.row_step[b] - 2] + size_t(c) * p.d;
+    for (int f = t * 4; f < p.d; f += 4 * kSmConsumers) {
+      float4 v;
+      if (p.proj_in) {
+        v = *reinterpret_cast<const float4*>(p.b_proj + f);
+      } else {
+        const uint2 ev = *reinterpret_cast<const uint2*>(e + f);
+        v = make_float4(e16_to_f32(ev.x, p.embed_f16), e16_to_f32(ev.x >> 16, p.embed_f16),
+                        e16_to_f32(ev.y, p.embed_f16), e16_to_f32(ev.y >> 16, p.embed_f16));
+      }
+      *reinterpret_cast<float4*>(p.x + size_t(b) * p.d + f) = v;
+    }
+    for (int f = t * 4; f < qkvw; f += 4 * kSmConsumers) {
+      *reinterpret_cast<float4*>(p.acc_qkv[0] + size_t(b) * qkvw + f) = z4;
+      *reinterpret_cast<float4*>(p.acc_qkv[1] + size_t(b) * qkvw + f) = z4;
+    }
+    for (int f = t * 4; f < p.V; f += 4 * kSmConsumers) *reinterpret_cast<float4*>(p.logits + size_t(b) * p.V + f) = z4;
+    named_bar(SBAR_CONS, kSmConsumers);   // the release below follows every thread's stores; ms.bcast is reused
+    if (t == 0) red_release_add(sm_prep(p, 2), 1u);
+  }
+  return true;
+}
+
 // Step k >= 2 inputs, one frame per CTA: report the previous step's code,
 // embed the next input (teacher-forced if asked) as residual row b.  With
 // Talker-wide code tables the row starts at the projection's bias instead
 // and the code is recorded for the projection's operand build.
 __device__ bool sm_prepk(const SParams& p, SMisc& ms, int k) {
+  if (kSmSlots) return sm_prep_step(p, ms);   // that kernel reaches step k >= 2 in SM_STEP calls only
   const int t = threadIdx.x, G = gridDim.x;
   for (int b = (blockIdx.x + k * 11) % G; b < p.B; b += G) {
     const int code = sm_code(p, ms, k - 1, b);
     if (code < 0) return false;
     if (t == 0) {
-      p.out_codes[size_t(b) * p.n_steps + (k - 2)] = code;
+      p.out_codes[size_t(b) * sm_n_run(p) + (k - 1 - sm_k_first(p))] = code;
       int nc = p.forced ? p.forced[size_t(b) * p.n_steps + (k - 2)] : code;
       if (nc < 0 || nc >= p.V) {
         set_status(p.status, QP_ERR_BAD_TOKEN);
@@ -933,12 +1036,14 @@ __device__ bool sm_prepk(const SParams& p, SMisc& ms, int k) {
   return true;
 }
 
+// The codes of the call's last step (in SM_STEP each row's own step).
 __device__ bool sm_final(const SParams& p, SMisc& ms) {
-  const int G = gridDim.x;
+  const int G = gridDim.x, k_last = sm_k_first(p) + sm_n_run(p) - 1;
   for (int b = (blockIdx.x + 5) % G; b < p.B; b += G) {
-    const int code = sm_code(p, ms, p.n_steps, b);
+    const int code = sm_code(p, ms, sm_mode(p) == SM_STEP ? p.row_step[b] : k_last, b);
     if (code < 0) return false;
-    if (threadIdx.x == 0) p.out_codes[size_t(b) * p.n_steps + (p.n_steps - 1)] = code;
+    const int out_row = sm_mode(p) == SM_STEP ? p.row_perm[b] : b;
+    if (threadIdx.x == 0) p.out_codes[size_t(out_row) * sm_n_run(p) + (sm_n_run(p) - 1)] = code;
   }
   return true;
 }
@@ -978,9 +1083,11 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
     if (!__all_sync(0xffffffffu, okl)) return false;
     __syncwarp();   // every lane's reads follow the acquires
     if (lane == 0) sm_ev(p, &ms.evc, SEV_ATT_READY, gi_q);
-    uint16_t* kvb = kvl + size_t(b) * ctx * 2 * p.kvw + j * kHeadDim + lane * 4;   // + (pos*2 + {0,1}) * kvw
+    // the frame's KV state (its slot in state-slot calls) and first new position (its own step in SM_STEP)
+    uint16_t* kvb = kvl + size_t(sm_slot(p, b)) * ctx * 2 * p.kvw + j * kHeadDim + lane * 4;   // + (pos*2 + {0,1}) * kvw
+    const int pos_b = sm_mode(p) == SM_STEP ? p.row_step[b] : pos0;
     for (int pp = 0; pp < P; ++pp) {
-      const int r = r0 + pp, pos = pos0 + pp;
+      const int r = r0 + pp, pos = pos_b + pp;
       float* row = p.acc_qkv[((k - 1) * p.L + l) & 1] + size_t(r) * qkvw;
       float* kr = row + p.qw + j * kHeadDim + lane * 4;
       float* vr = row + p.qw + p.kvw + j * kHeadDim + lane * 4;
@@ -1004,7 +1111,8 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
 #pragma unroll
       for (int t = 0; t < kMaxCtx; ++t) {
         kh[t] = t < pos ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 0) * p.kvw)) : make_uint2(0, 0);
-        vh[t] = t < pos ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 1) * p.kvw)) : make_uint2(0, 0);
+        if (!kSmSlots)
+          vh[t] = t < pos ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 1) * p.kvw)) : make_uint2(0, 0);
       }
       const float4 knew = norm_rope(kraw, L.k_norm, p.eps, p.rope_cs + pos * 64, lane);
       *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = pack4_f16(knew.x, knew.y, knew.z, knew.w);
@@ -1045,6 +1153,13 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
         for (int o = 8; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
         const float pr = den > 0.f ? e / den : 0.f;
         float4 o2[2] = {z4, z4};
+        // the state-slot kernel loads the values here, after the scores: its
+        // rows' positions differ, and holding both caches across the softmax
+        // spills registers there
+        if (kSmSlots)
+#pragma unroll
+          for (int t = 0; t < kMaxCtx; ++t)
+            vh[t] = t < pos ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 1) * p.kvw)) : make_uint2(0, 0);
 #pragma unroll
         for (int t = 0; t < kMaxCtx; ++t) {
           const float4 vv = t < pos ? unpack4_f16(vh[t]) : (t == pos ? vnew : z4);
@@ -1142,13 +1257,13 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
     ++sec;                                    \
     if (ms.fail) return;                      \
   }
-  SM_SECTION(sm_prep1(p));
-  for (int k = 1; k <= p.n_steps; ++k) {
+  if (sm_mode(p) != SM_STEP) SM_SECTION(sm_prep1(p));
+  for (int k = sm_k_first(p); k < sm_k_first(p) + sm_n_run(p); ++k) {
     if (k > 1) SM_SECTION(sm_prepk(p, ms, k));
     // one call site: a GEMM section inlined twice costs instruction fetch
     if (k == 1 || p.proj_in) SM_SECTION(sm_gemm<S_PROJ>(p, ms, smem, sgi_proj(p, k), seg));
     for (int l = 0; l < p.L; ++l) {
-      if (p.fuse) {
+      if (sm_fused(p)) {
         SM_SECTION(sm_gemm<S_QKV>(p, ms, smem, sgi_of(p, k, l, 0), seg));
         SM_SECTION(sm_gemm<S_OA>(p, ms, smem, sgi_of(p, k, l, 1), seg));
       } else {
@@ -1159,8 +1274,8 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
       SM_SECTION(sm_gemm<S_GU>(p, ms, smem, sgi_of(p, k, l, 2), seg));
       SM_SECTION(sm_gemm<S_DOWN>(p, ms, smem, sgi_of(p, k, l, 3), seg));
     }
-    SM_SECTION(sm_gemm<S_HEAD>(p, ms, smem, sgi_head(p, k), seg));
-    if (p.temperature > 0.f) SM_SECTION(sm_decide(p, ms, keys, k));
+    for (int h = 0; h < sm_n_heads(p); ++h) SM_SECTION(sm_gemm<S_HEAD>(p, ms, smem, sgi_head(p, k) + h, seg));
+    if (sm_sampled(p)) SM_SECTION(sm_decide(p, ms, keys, k));
   }
   SM_SECTION(sm_final(p, ms));
 #undef SM_SECTION
@@ -1209,10 +1324,15 @@ struct SmSync {
   int NGEMM, NHT;
 };
 
-SmSync sm_sync_layout(const qp_geometry& g, int B) {
+// The sync region of a call; n_heads > 0 lays out an SM_STEP call's
+// program ([projection], 4 GEMMs per layer, n_heads heads), n_heads < 0 an
+// SM_BEGIN call's (step 1 only).
+SmSync sm_sync_layout(const qp_geometry& g, int B, int n_heads = 0) {
   SmSync S{};
   const int proj_in = g.code_embed_dim != g.hidden;   // a projection GEMM per step k >= 2
   S.NGEMM = 1 + g.n_steps * (4 * g.layers + 1) + proj_in * (g.n_steps - 1);
+  if (n_heads < 0) S.NGEMM = 1 + 4 * g.layers + 1;
+  if (n_heads > 0) S.NGEMM = proj_in + 4 * g.layers + n_heads;
   S.NHT = g.n_q_heads + 2 * g.n_kv_heads;   // 128-row tiles of q|k|v (head_dim 128)
   const size_t steps = size_t(g.n_steps);
   size_t o = 0;
@@ -1273,12 +1393,41 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;
   p.temperature = a.temperature; p.top_k = a.top_k; p.gumbel = a.gumbel;
   p.fuse = a.B <= kSmFuseFrames;
+  p.mode = SM_RUN; p.k_first = 1; p.n_run = g.n_steps; p.n_heads = 1;
 }
 
 constexpr int kSmMaxDevices = 64;
 bool g_sm_attr[kSmMaxDevices] = {};
 
+qp_status sm_launch(const qp_handle* h, const SParams& p, uint8_t* sync, size_t sync_bytes, cudaStream_t s) {
+  const int dev = h->device;
+  bool local = false;
+  bool* attr = dev >= 0 && dev < kSmMaxDevices ? &g_sm_attr[dev] : &local;
+  const size_t smem = kSmOffMisc + sizeof(SMisc) + 1024;
+  if (!*attr) {
+    if (cudaFuncSetAttribute(k_frames_small, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) {
+      cudaGetLastError();
+      return QP_ERR_CUDA;
+    }
+    *attr = true;
+  }
+  if (cudaMemsetAsync(sync, 0, sync_bytes, s) != cudaSuccess) {
+    cudaGetLastError();
+    return QP_ERR_CUDA;
+  }
+  SParams pc = p;
+  void* args[] = {&pc};
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_frames_small), dim3(h->num_sms), dim3(kSmThreads), args,
+                                  smem, s) != cudaSuccess) {
+    cudaGetLastError();
+    return QP_ERR_CUDA;
+  }
+  return QP_OK;
+}
+
 }  // namespace
+
+#if !QP_SMALL_SLOTS
 
 size_t small_smem_bytes() { return kSmOffMisc + sizeof(SMisc) + 1024; }
 
@@ -1297,28 +1446,54 @@ qp_status run_frames_small(qp_handle* h, const RunArgs& a, uint8_t* scratch, con
   uint8_t* sync = scratch + L.sync;
   SParams p{};
   sm_fill(p, h, a, scratch, L, sync, S, bmax);
-  const int dev = h->device;
-  bool local = false;
-  bool* attr = dev >= 0 && dev < kSmMaxDevices ? &g_sm_attr[dev] : &local;
-  if (!*attr) {
-    if (cudaFuncSetAttribute(k_frames_small, cudaFuncAttributeMaxDynamicSharedMemorySize, int(small_smem_bytes())) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return QP_ERR_CUDA;
-    }
-    *attr = true;
-  }
-  if (cudaMemsetAsync(sync, 0, S.total, s) != cudaSuccess) {
-    cudaGetLastError();
-    return QP_ERR_CUDA;
-  }
-  void* args[] = {&p};
-  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_frames_small), dim3(h->num_sms), dim3(kSmThreads), args,
-                                  small_smem_bytes(), s) != cudaSuccess) {
-    cudaGetLastError();
-    return QP_ERR_CUDA;
-  }
-  return QP_OK;
+  return sm_launch(h, p, sync, S.total, s);
 }
+
+#else   // the state-slot kernel
+
+qp_status run_slots_small(qp_handle* h, const SlotArgs& sa, uint8_t* scratch, const Scratch& L, int bmax,
+                          cudaStream_t s) {
+  const qp_geometry& g = h->g;
+  const int B = sa.B;
+  if (B < 1 || B > kSmallMaxFrames || B > bmax || h->wfmt != WF_BF16 || h->hfmt != WF_BF16) return QP_ERR_ARG;
+  RunArgs a{};
+  a.B = B; a.H = sa.H; a.q0 = sa.q0; a.out_codes = sa.out_codes; a.out_logits = sa.out_logits;
+  SParams p{};
+  // rows in step order (a stable sort keeps the caller's order within a step)
+  int order[kSmallMaxFrames];
+  int n_heads = -1;
+  for (int b = 0; b < B; ++b) order[b] = b;
+  if (sa.mode == SM_STEP) {
+    std::stable_sort(order, order + B, [&](int x, int y) { return sa.steps[x] < sa.steps[y]; });
+    n_heads = 0;
+    for (int b = 0; b < B; ++b) {
+      const int st = sa.steps[order[b]];
+      if (b == 0 || st != sa.steps[order[b - 1]]) {
+        p.group_start[n_heads] = b;
+        p.group_step[n_heads] = st;
+        ++n_heads;
+      }
+    }
+    p.group_start[n_heads] = B;
+  }
+  for (int b = 0; b < B; ++b) {
+    p.row_perm[b] = order[b];
+    p.row_slot[b] = sa.slots[order[b]];
+    p.row_step[b] = sa.mode == SM_STEP ? sa.steps[order[b]] : 1;
+  }
+  const SmSync S = sm_sync_layout(g, B, n_heads);
+  if (L.total - L.sync < S.total) return QP_ERR_ARG;
+  uint8_t* sync = scratch + L.sync;
+  sm_fill(p, h, a, scratch, L, sync, S, bmax);
+  p.fuse = 0;
+  p.mode = sa.mode;
+  p.k_first = sa.mode == SM_STEP ? 2 : 1;
+  p.n_run = 1;
+  p.n_heads = sa.mode == SM_STEP ? n_heads : 1;
+  p.code_in = sa.codes_in;
+  return sm_launch(h, p, sync, S.total, s);
+}
+
+#endif
 
 }  // namespace qp
