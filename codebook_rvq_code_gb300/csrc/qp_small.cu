@@ -136,7 +136,7 @@ struct SParams {
   // state-slot calls (SM_BEGIN, SM_STEP); rows of an SM_STEP call are sorted
   // by step, and row b is the caller's row row_perm[b]
   int mode, n_run, k_first;        // steps run this call: k_first .. k_first + n_run - 1
-  int n_heads;                     // head GEMMs per step: 1, or one per step group (SM_STEP)
+  int n_groups, group_rows;        // SM_STEP: step groups, rows of the largest
   // row b's KV state slot, step and caller row; rows [group_start[h],
   // group_start[h + 1]) are at step group_step[h] (SM_STEP)
   int32_t row_slot[kSmallMaxFrames], row_step[kSmallMaxFrames], row_perm[kSmallMaxFrames];
@@ -150,7 +150,6 @@ struct SParams {
 __device__ __forceinline__ int sm_mode(const SParams& p) { return kSmSlots ? p.mode : int(SM_RUN); }
 __device__ __forceinline__ int sm_k_first(const SParams& p) { return kSmSlots ? p.k_first : 1; }
 __device__ __forceinline__ int sm_n_run(const SParams& p) { return kSmSlots ? p.n_run : p.n_steps; }
-__device__ __forceinline__ int sm_n_heads(const SParams& p) { return kSmSlots ? p.n_heads : 1; }
 __device__ __forceinline__ bool sm_fused(const SParams& p) { return !kSmSlots && p.fuse; }
 __device__ __forceinline__ bool sm_sampled(const SParams& p) { return !kSmSlots && p.temperature > 0.f; }
 
@@ -184,11 +183,9 @@ __device__ SG sgemm(const SParams& p, int gi) {
   if (sm_mode(p) == SM_STEP) {
     g.k = 2;
     r = gi - p.proj_in;
-    if (r >= 4 * p.L) {   // the head of step group h
-      const int h = r - 4 * p.L;
-      g.kind = S_HEAD; g.k = p.group_step[h]; g.l = p.L - 1; g.r0 = p.group_start[h];
-      g.R = p.group_start[h + 1] - p.group_start[h]; g.n_mt = p.V / kTileM; g.n_ks = p.d / kKs;
-      g.w = p.w_head[g.k - 1]; g.out = p.logits; g.ld = p.V;
+    if (r == 4 * p.L) {   // every step group's head: tile mt is group mt / (V / 128)'s
+      g.kind = S_HEAD; g.l = p.L - 1; g.R = p.group_rows; g.n_mt = p.n_groups * (p.V / kTileM);
+      g.n_ks = p.d / kKs; g.w = nullptr; g.out = p.logits; g.ld = p.V;
       g.N = sm_cols(g.R);
       return g;
     }
@@ -226,6 +223,30 @@ __device__ SG sgemm(const SParams& p, int gi) {
   }
   g.N = sm_cols(g.R);
   return g;
+}
+
+// The activation rows [r0, r0 + R) of tile mt, and the weight slice of unit
+// s.  An SM_STEP call's head GEMM holds one head per step group, each with
+// its own rows and matrix.
+__device__ __forceinline__ bool sm_grouped(const SParams& p, const SG& g) {
+  return kSmSlots && g.kind == S_HEAD && sm_mode(p) == SM_STEP;
+}
+__device__ __forceinline__ void sm_rows(const SParams& p, const SG& g, int mt, int& r0, int& R) {
+  if (sm_grouped(p, g)) {
+    const int h = mt / (p.V / kTileM);
+    r0 = p.group_start[h];
+    R = p.group_start[h + 1] - r0;
+  } else {
+    r0 = g.r0;
+    R = g.R;
+  }
+}
+__device__ __forceinline__ const uint8_t* sm_slice(const SParams& p, const SG& g, int s) {
+  if (sm_grouped(p, g)) {
+    const int per = (p.V / kTileM) * g.n_ks, h = s / per;
+    return reinterpret_cast<const uint8_t*>(p.w_head[p.group_step[h] - 1]) + size_t(s - h * per) * kSmWSlot;
+  }
+  return reinterpret_cast<const uint8_t*>(g.w) + size_t(s) * kSmWSlot;
 }
 
 // GEMMs whose partials are scaled by the input row's 1/RMS.  From step 2 on
@@ -278,8 +299,7 @@ __device__ void sm_ready(const SParams& p, int gi, const unsigned*& ctr, unsigne
       if (g.k == 1) { all_of(0); return; }              // the input projection
       ctr = sm_prep(p, g.k); want = unsigned(p.B); return;   // the step's input rows
     case S_O: ctr = sm_att(p, g.k, g.l); want = unsigned(p.B * p.n_kv); return;
-    case S_HEAD: all_of(sm_mode(p) == SM_STEP ? sgi_of(p, 2, p.L - 1, 3) : gi - 1); return;   // the last DOWN
-    default: all_of(gi - 1); return;                     // GU: O; DOWN: GU
+    default: all_of(gi - 1); return;                     // GU: O; DOWN: GU; HEAD: the last DOWN
   }
 }
 
@@ -340,7 +360,7 @@ __device__ void sm_producer(const SParams& p, SMisc& ms, uint8_t* smem) {
       sm_ev(p, &ms.evc, SEV_ISSUE, gi);
       mbar_expect_tx(&ms.wfull[slot], kSmWSlot);
       // tile mt, slice ks of the tile-packed matrix: one contiguous 32 KB run
-      bulk_g2s_stream(smem + kSmOffW + slot * kSmWSlot, reinterpret_cast<const uint8_t*>(g.w) + size_t(s) * kSmWSlot,
+      bulk_g2s_stream(smem + kSmOffW + slot * kSmWSlot, sm_slice(p, g, s),
                       kSmWSlot, &ms.wfull[slot], pol);
       ++it;
     }
@@ -565,7 +585,13 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
         int row = n;
         if (kQkv<KIND>) wn = p.layer[g.l].attn_norm;
         else if (KIND == S_GU) wn = p.layer[g.l].ffn_norm;
-        else { wn = p.out_norm; row = g.k == 1 ? 2 * n + 1 : g.r0 + n; }   // head: each frame's last position
+        else {   // head: each frame's last position
+          wn = p.out_norm;
+          int r0 = 0, R = g.R;
+          if (sm_grouped(p, g)) sm_rows(p, g, (u0 + ui) / g.n_ks, r0, R);
+          if (n >= R) continue;   // rows past the tile's group: their outputs are not read
+          row = g.k == 1 ? 2 * n + 1 : r0 + n;
+        }
         // both loads in flight together
         const float4 w0 = __ldg(reinterpret_cast<const float4*>(wn + k));
         const float4 w1 = __ldg(reinterpret_cast<const float4*>(wn + k + 4));
@@ -653,9 +679,12 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
   if (t == 0) sm_ev(p, &ms.evc, SEV_ACC, gi);
   tc_fence_after();
   const int quarter = warp & 3, half = warp >> 2, cols = g.N / 2;
-  const int m0 = mt * kTileM + quarter * 32;
+  int r0, R;
+  sm_rows(p, g, mt, r0, R);
+  // a grouped head's tile mt is tile mt % (V / 128) of its group's logits
+  const int m0 = (sm_grouped(p, g) ? mt % (p.V / kTileM) : mt) * kTileM + quarter * 32;
   float* tp = reinterpret_cast<float*>(smem + kSmOffKeys) + warp * 256;   // [8 rows][32 features]
-  for (int col = half * cols; col < (half + 1) * cols && col < g.R; col += 8) {   // warp-uniform bounds
+  for (int col = half * cols; col < (half + 1) * cols && col < R; col += 8) {   // warp-uniform bounds
     float v[8];
     tmem_ld8(ms.tmem_base + tb * 128 + (uint32_t(quarter * 32) << 16) + uint32_t(col), v);
 #pragma unroll
@@ -664,13 +693,13 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
 #pragma unroll
     for (int pass = 0; pass < 2; ++pass) {
       const int f = pass * 4 + (lane >> 3), k4 = (lane & 7) * 4, n = col + f;
-      if (n < g.R) {
+      if (n < R) {
         float4 x = *reinterpret_cast<const float4*>(tp + f * 32 + k4);
         if (sm_scaled<KIND>(g)) {
           const float s = ms.inv[n];
           x.x *= s; x.y *= s; x.z *= s; x.w *= s;
         }
-        red_add_v4_f32(g.out + size_t(g.r0 + n) * g.ld + m0 + k4, x);
+        red_add_v4_f32(g.out + size_t(r0 + n) * g.ld + m0 + k4, x);
       }
     }
     __syncwarp();
@@ -890,11 +919,9 @@ __device__ float sm_row_inv(const SParams& p, SMisc& ms, int row) {
 // Sampling: the decision the sampling pass published.
 __device__ int sm_code(const SParams& p, SMisc& ms, int step, int b) {
   // the head GEMM that produced row b's logits, and where the call's outputs go
-  int gih = sgi_head(p, step), out_row = b, out_step = step - sm_k_first(p);
-  if (sm_mode(p) == SM_STEP) {   // one step per row: the row's step group's head, the caller's row
-    int h = 0;
-    while (h + 1 < sm_n_heads(p) && b >= p.group_start[h + 1]) ++h;
-    gih += h;
+  const int gih = sgi_head(p, step);
+  int out_row = b, out_step = step - sm_k_first(p);
+  if (sm_mode(p) == SM_STEP) {   // one step per row, in the caller's row order
     out_row = p.row_perm[b];
     out_step = 0;
   }
@@ -1274,7 +1301,7 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
       SM_SECTION(sm_gemm<S_GU>(p, ms, smem, sgi_of(p, k, l, 2), seg));
       SM_SECTION(sm_gemm<S_DOWN>(p, ms, smem, sgi_of(p, k, l, 3), seg));
     }
-    for (int h = 0; h < sm_n_heads(p); ++h) SM_SECTION(sm_gemm<S_HEAD>(p, ms, smem, sgi_head(p, k) + h, seg));
+    SM_SECTION(sm_gemm<S_HEAD>(p, ms, smem, sgi_head(p, k), seg));
     if (sm_sampled(p)) SM_SECTION(sm_decide(p, ms, keys, k));
   }
   SM_SECTION(sm_final(p, ms));
@@ -1324,15 +1351,15 @@ struct SmSync {
   int NGEMM, NHT;
 };
 
-// The sync region of a call; n_heads > 0 lays out an SM_STEP call's
-// program ([projection], 4 GEMMs per layer, n_heads heads), n_heads < 0 an
-// SM_BEGIN call's (step 1 only).
-SmSync sm_sync_layout(const qp_geometry& g, int B, int n_heads = 0) {
+// The sync region of a call.  The program: SM_RUN the whole frame loop;
+// SM_BEGIN step 1 only; SM_STEP [the projection], 4 GEMMs per layer and the
+// grouped head.
+SmSync sm_sync_layout(const qp_geometry& g, int B, int mode = SM_RUN) {
   SmSync S{};
   const int proj_in = g.code_embed_dim != g.hidden;   // a projection GEMM per step k >= 2
   S.NGEMM = 1 + g.n_steps * (4 * g.layers + 1) + proj_in * (g.n_steps - 1);
-  if (n_heads < 0) S.NGEMM = 1 + 4 * g.layers + 1;
-  if (n_heads > 0) S.NGEMM = proj_in + 4 * g.layers + n_heads;
+  if (mode == SM_BEGIN) S.NGEMM = 1 + 4 * g.layers + 1;
+  if (mode == SM_STEP) S.NGEMM = proj_in + 4 * g.layers + 1;
   S.NHT = g.n_q_heads + 2 * g.n_kv_heads;   // 128-row tiles of q|k|v (head_dim 128)
   const size_t steps = size_t(g.n_steps);
   size_t o = 0;
@@ -1393,7 +1420,7 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;
   p.temperature = a.temperature; p.top_k = a.top_k; p.gumbel = a.gumbel;
   p.fuse = a.B <= kSmFuseFrames;
-  p.mode = SM_RUN; p.k_first = 1; p.n_run = g.n_steps; p.n_heads = 1;
+  p.mode = SM_RUN; p.k_first = 1; p.n_run = g.n_steps; p.n_groups = 1; p.group_rows = a.B;
 }
 
 constexpr int kSmMaxDevices = 64;
@@ -1461,27 +1488,29 @@ qp_status run_slots_small(qp_handle* h, const SlotArgs& sa, uint8_t* scratch, co
   SParams p{};
   // rows in step order (a stable sort keeps the caller's order within a step)
   int order[kSmallMaxFrames];
-  int n_heads = -1;
+  int n_groups = 1, group_rows = B;
   for (int b = 0; b < B; ++b) order[b] = b;
   if (sa.mode == SM_STEP) {
     std::stable_sort(order, order + B, [&](int x, int y) { return sa.steps[x] < sa.steps[y]; });
-    n_heads = 0;
+    n_groups = 0;
+    group_rows = 0;
     for (int b = 0; b < B; ++b) {
       const int st = sa.steps[order[b]];
       if (b == 0 || st != sa.steps[order[b - 1]]) {
-        p.group_start[n_heads] = b;
-        p.group_step[n_heads] = st;
-        ++n_heads;
+        p.group_start[n_groups] = b;
+        p.group_step[n_groups] = st;
+        ++n_groups;
       }
     }
-    p.group_start[n_heads] = B;
+    p.group_start[n_groups] = B;
+    for (int i = 0; i < n_groups; ++i) group_rows = std::max(group_rows, p.group_start[i + 1] - p.group_start[i]);
   }
   for (int b = 0; b < B; ++b) {
     p.row_perm[b] = order[b];
     p.row_slot[b] = sa.slots[order[b]];
     p.row_step[b] = sa.mode == SM_STEP ? sa.steps[order[b]] : 1;
   }
-  const SmSync S = sm_sync_layout(g, B, n_heads);
+  const SmSync S = sm_sync_layout(g, B, sa.mode);
   if (L.total - L.sync < S.total) return QP_ERR_ARG;
   uint8_t* sync = scratch + L.sync;
   sm_fill(p, h, a, scratch, L, sync, S, bmax);
@@ -1489,7 +1518,8 @@ qp_status run_slots_small(qp_handle* h, const SlotArgs& sa, uint8_t* scratch, co
   p.mode = sa.mode;
   p.k_first = sa.mode == SM_STEP ? 2 : 1;
   p.n_run = 1;
-  p.n_heads = sa.mode == SM_STEP ? n_heads : 1;
+  p.n_groups = n_groups;
+  p.group_rows = group_rows;
   p.code_in = sa.codes_in;
   return sm_launch(h, p, sync, S.total, s);
 }

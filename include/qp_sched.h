@@ -18,7 +18,9 @@
  * forced one), gets the codes and logits of qp_predict_frames.
  *
  * Served by the small-batch engine: bf16 weights, B <= 64 rows per call,
- * greedy decisions.  Slot and step arrays are HOST memory (a scheduler keeps
+ * greedy decisions.  A step call runs one step's layers over all its rows;
+ * its output head holds one head matrix per distinct step among the rows
+ * (the rows sorted into step groups), as one GEMM.  Slot and step arrays are HOST memory (a scheduler keeps
  * this bookkeeping on the host); the library sorts the rows by step and
  * stages the order to the device on `stream`.  Codes, logits and H/q0 are
  * device memory, in the caller's row order.  Rows of one call must name
