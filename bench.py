@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-sweep", action="store_true", help="skip the per-configuration summary")
+    ap.add_argument("--step-calls", action="store_true",
+                    help="time only the state-slot step calls and print their rows (a profiling entry)")
     return ap.parse_args()
 
 
@@ -504,6 +506,13 @@ def main():
         dist.init_process_group("nccl")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    if args.step_calls:
+        from codebook_rvq_code_gb300 import build as qb
+        qb.build()
+        rows = sched_rows(dev, torch.cuda.current_stream(dev), max(1, args.steps), peaks()[0])
+        if rank == 0:
+            print(json.dumps({"step_calls": rows}), flush=True)
+        return
 
     from codebook_rvq_code_gb300 import build as qb
     qb.build()

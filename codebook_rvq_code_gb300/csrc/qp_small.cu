@@ -1308,7 +1308,13 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
 #undef SM_SECTION
 }
 
-__global__ void __launch_bounds__(kSmThreads, 1) k_frames_small(const SParams p) {
+// The frame-loop kernel is k_frames_small, the state-slot kernel k_slots_small.
+#if QP_SMALL_SLOTS
+#define SM_KERNEL k_slots_small
+#else
+#define SM_KERNEL k_frames_small
+#endif
+__global__ void __launch_bounds__(kSmThreads, 1) SM_KERNEL(const SParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   SMisc& ms = *reinterpret_cast<SMisc*>(smem + kSmOffMisc);
@@ -1432,7 +1438,7 @@ qp_status sm_launch(const qp_handle* h, const SParams& p, uint8_t* sync, size_t 
   bool* attr = dev >= 0 && dev < kSmMaxDevices ? &g_sm_attr[dev] : &local;
   const size_t smem = kSmOffMisc + sizeof(SMisc) + 1024;
   if (!*attr) {
-    if (cudaFuncSetAttribute(k_frames_small, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) {
+    if (cudaFuncSetAttribute(SM_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) {
       cudaGetLastError();
       return QP_ERR_CUDA;
     }
@@ -1444,7 +1450,7 @@ qp_status sm_launch(const qp_handle* h, const SParams& p, uint8_t* sync, size_t 
   }
   SParams pc = p;
   void* args[] = {&pc};
-  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_frames_small), dim3(h->num_sms), dim3(kSmThreads), args,
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(SM_KERNEL), dim3(h->num_sms), dim3(kSmThreads), args,
                                   smem, s) != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;
