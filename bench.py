@@ -408,7 +408,8 @@ def sched_rows(dev, stream, steps, hbm):
             "workload": f"{B} rows at steps {sorted(set(st))} ({n_groups} step groups), 1.7B geometry, bf16, greedy",
             "ms_per_call": ms_step, "rows_per_s": B / (ms_step / 1e3), "begin_ms_per_call": ms_begin,
             "device_status": cp.device_status(),
-            "roofline": {"bound": "hbm", "frac": nbytes / (hbm * 1e9) / (ms_step / 1e3), "algorithmic_bytes": nbytes}}
+            "roofline": {"bound": "hbm", "frac": nbytes / (hbm * 1e9) / (ms_step / 1e3), "algorithmic_bytes": nbytes,
+                         "traffic": recorded_traffic(f"step_call_B{B}")}}
     cp.close()
     return out
 
