@@ -152,6 +152,9 @@ size_t persistent_smem_bytes();
 bool small_supported(const qp_handle* h, const RunArgs& a);
 qp_status run_frames_small(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
                            cudaStream_t s);
+// the same with Gumbel top-k sampling, on the kernel built from qp_small_sampled.cu
+qp_status run_frames_small_sampled(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
+                                   cudaStream_t s);
 size_t small_smem_bytes();
 // state-slot calls on the small-batch engine's kernel built from qp_small_slots.cu
 qp_status run_slots_small(qp_handle* h, const SlotArgs& a, uint8_t* scratch, const Scratch& L, int bmax,

@@ -18,9 +18,12 @@
 //   * the consumer warps of the CTA that runs a unit build its operand slice
 //     in shared memory from those f32 sources: x * w_norm, silu(g) * u, the
 //     f16 conversion -- the work the tile engine's finishing pass does once;
-//   * a GEMM whose input is RMS-normalised computes the rows' scale itself
-//     (from the complete residual rows) and applies it to its partials before
-//     they are added, so every accumulator holds final values.
+//   * the rows' RMS scale is applied where a complete residual row is at
+//     hand: the gate/up GEMM (and step 1's head) computes it from the rows
+//     and scales its partials before they are added; the QKV GEMM adds
+//     unscaled partials and each attention item scales its frame's q, k and
+//     v; from step 2 the head adds unscaled logits and the decision scales
+//     the row it copies out.
 //
 // Roles per CTA (one CTA per SM): warps 0-7 consume (operand builds,
 // accumulator drains, attention, step inputs, decisions), warp 8 streams
@@ -51,33 +54,31 @@ constexpr uint32_t kSmOffOp = kSmNW * kSmWSlot;
 constexpr uint32_t kSmOffKeys = kSmOffOp + kSmOpBytes;   // top-k keys, or the drain's transpose buffer
 constexpr uint32_t kSmOffMisc = kSmOffKeys + kMaxVocab * 4;
 constexpr uint32_t kSmTmemCols = 256;                // two accumulators of up to 128 columns
-// Largest batch whose attention runs inside the O projection's operand build
-// (each of the O projection's units then computes its q head for every
-// frame); larger batches run attention as a section of its own.
-constexpr int kSmFuseFrames = 8;
 
 enum { SBAR_CONS = 1 };
 enum { S_PROJ = 0, S_QKV, S_O, S_GU, S_DOWN, S_HEAD };
-// The O projection with attention folded into its operand build (a code
-// path of the S_O GEMM, not a GEMM of its own).
-constexpr int S_OA = 6;
 // The QKV projection without the row scale (a code path of the S_QKV GEMM):
-// when attention runs as a section of its own, each attention item scales
-// its frame's q, k and v itself, so the GEMM needs no row-scale pass.
+// each attention item scales its frame's q, k and v itself, so the GEMM
+// needs no row-scale pass.
 constexpr int S_QKVU = 7;
 
 // Call modes: a whole frame loop; step 1 only, into state slots; one step
 // of rows at mixed steps, from state slots (include/qp_sched.h).
 enum { SM_RUN = 0, SM_BEGIN = 1, SM_STEP = 2 };
-// This translation unit's kernel: the whole frame loop (SM_RUN), or, built
-// from qp_small_slots.cu, the state-slot calls (SM_BEGIN, SM_STEP).  Two
-// kernels keep the frame loop free of the state-slot paths' code and
-// registers; the state-slot kernel leaves out the fused attention and
-// sampling, which its calls do not use.
+// This translation unit's kernel: the greedy frame loop (SM_RUN); built from
+// qp_small_sampled.cu, the frame loop with Gumbel top-k sampling; built from
+// qp_small_slots.cu, the state-slot calls (SM_BEGIN, SM_STEP, greedy).  The
+// builds keep each kernel free of the others' code and registers: the
+// kernel carries every section inline, and code it does not run still costs
+// registers and instruction fetch.
 #ifndef QP_SMALL_SLOTS
 #define QP_SMALL_SLOTS 0
 #endif
+#ifndef QP_SMALL_SAMPLED
+#define QP_SMALL_SAMPLED 0
+#endif
 constexpr bool kSmSlots = QP_SMALL_SLOTS != 0;
+constexpr bool kSmSampled = QP_SMALL_SAMPLED != 0;
 
 struct SMisc {
   uint64_t wfull[kSmNW], wempty[kSmNW];
@@ -115,7 +116,7 @@ struct SParams {
   // scratch (rows: 2B at step 1, B later)
   float* x;                // residual stream [row][d]
   uint16_t* a_o;           // attention output, f16 [row][q_width]
-  float* acc_qkv[2];       // [row][q_width + 2 kv_width], scaled by the row's RMS; layers alternate
+  float* acc_qkv[2];       // [row][q_width + 2 kv_width], unscaled (attention applies the row's 1/RMS); layers alternate
   float* acc_gu;           // [row][2 ffn]: gate then up, scaled by the row's RMS
   float* logits;           // [frame][vocab]
   uint16_t* kv;            // f16 [layer][frame][pos][k|v][kv_width]
@@ -130,7 +131,6 @@ struct SParams {
   int NGEMM, NHT;
   unsigned long long* trace; int trace_n;
   // the call
-  int fuse;                // attention inside the O projection's operand build
   int proj_in;             // code tables are Talker-wide: each step's input passes through small_to_mtp
   bool embed_f16;          // embedding tables are f16, else bf16
   // state-slot calls (SM_BEGIN, SM_STEP); rows of an SM_STEP call are sorted
@@ -150,8 +150,7 @@ struct SParams {
 __device__ __forceinline__ int sm_mode(const SParams& p) { return kSmSlots ? p.mode : int(SM_RUN); }
 __device__ __forceinline__ int sm_k_first(const SParams& p) { return kSmSlots ? p.k_first : 1; }
 __device__ __forceinline__ int sm_n_run(const SParams& p) { return kSmSlots ? p.n_run : p.n_steps; }
-__device__ __forceinline__ bool sm_fused(const SParams& p) { return !kSmSlots && p.fuse; }
-__device__ __forceinline__ bool sm_sampled(const SParams& p) { return !kSmSlots && p.temperature > 0.f; }
+__device__ __forceinline__ bool sm_sampled(const SParams& p) { return kSmSampled && p.temperature > 0.f; }
 
 // One GEMM of the program: n_mt tiles of 128 weight rows x n_ks slices of K.
 struct SG {
@@ -442,97 +441,6 @@ __device__ __forceinline__ uint4 pack8h(const float (&v)[8]) {
 // [8 k] of f16 (all consumer threads; one thread per 8 consecutive columns
 // of a row, so global reads coalesce, and every unit's loads in one pass).
 // i0: the run index of unit u0 (its operand goes to slot (i0 + ui) % slots).
-// Attention of q head h for activation row n at layer l of step k (one warp;
-// lane l holds dims 4l..4l+3 of every 128-vector), stored as row n of the O
-// projection's operand slice for K slice h.  Per-head RMSNorm and RoPE of q
-// and of the frame's new key(s) (the step's positions come from the q|k|v
-// accumulator, earlier positions from the KV cache), causal softmax over
-// positions 0..pos, weighted sum of the values.  The per-head q/k norm
-// tensors and the 16 q / 8 kv heads of 128 are those of "rightkit-qts 0.2.3
-// - Qwen3-TTS 1.7B -> QTS GGUF", section "Loader contract"; where the norm
-// sits, the head grouping h / 2 and the 1/sqrt(128) scale are readings of
-// that geometry.  If `append`, the row's own key and value are stored in the
-// cache for the later steps.
-static_assert(kMaxCtx == 16, "sm_attn_row holds one score per position in a 16-way reduce-scatter");
-__device__ void sm_attn_row(const SParams& p, const float* acc, int k, int l, int h, int n, bool append,
-                            uint16_t* dst, int n8) {
-  const int lane = threadIdx.x & 31;
-  const int P = k == 1 ? 2 : 1, pos0 = k == 1 ? 0 : k;
-  const int b = n / P, pos = pos0 + (n - b * P);
-  const int qkvw = p.qw + 2 * p.kvw, j = h / (p.n_q / p.n_kv), ctx = p.n_steps + 1;
-  const SLayer& L = p.layer[l];
-  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  uint16_t* kvb = p.kv + (size_t(l) * p.Bmax + b) * ctx * 2 * p.kvw + j * kHeadDim + lane * 4;
-  const float* fr = acc + size_t(b) * P * qkvw;   // the frame's rows of this step
-  // independent loads first: q, the step's keys and values, then the cache
-  const float4 qraw = __ldcg(reinterpret_cast<const float4*>(acc + size_t(n) * qkvw + h * kHeadDim + lane * 4));
-  float4 kraw[2], vnew[2];
-#pragma unroll
-  for (int pp = 0; pp < 2; ++pp) {
-    kraw[pp] = pp < P ? __ldcg(reinterpret_cast<const float4*>(fr + pp * qkvw + p.qw + j * kHeadDim + lane * 4)) : z4;
-    vnew[pp] = pp < P ? __ldcg(reinterpret_cast<const float4*>(fr + pp * qkvw + p.qw + p.kvw + j * kHeadDim + lane * 4))
-                      : z4;
-  }
-  uint2 kh[kMaxCtx], vh[kMaxCtx];
-#pragma unroll
-  for (int t = 0; t < kMaxCtx; ++t) {
-    kh[t] = t < pos0 ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 0) * p.kvw)) : make_uint2(0, 0);
-    vh[t] = t < pos0 ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 1) * p.kvw)) : make_uint2(0, 0);
-  }
-  const float4 qn = norm_rope(qraw, L.q_norm, p.eps, p.rope_cs + pos * 64, lane);
-  float4 knew[2];
-#pragma unroll
-  for (int pp = 0; pp < 2; ++pp)
-    knew[pp] = pp < P ? norm_rope(kraw[pp], L.k_norm, p.eps, p.rope_cs + (pos0 + pp) * 64, lane) : z4;
-  if (append) {
-    const bool second = pos != pos0;
-    const float4 kk = second ? knew[1] : knew[0], vv = second ? vnew[1] : vnew[0];
-    *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = pack4_f16(kk.x, kk.y, kk.z, kk.w);
-    *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 1) * p.kvw) = pack4_f16(vv.x, vv.y, vv.z, vv.w);
-  }
-  float part[kMaxCtx];
-#pragma unroll
-  for (int t = 0; t < kMaxCtx; ++t) {
-    const float4 kk = t < pos0 ? unpack4_f16(kh[t]) : (t == pos0 ? knew[0] : (t == pos0 + 1 ? knew[1] : z4));
-    part[t] = qn.x * kk.x + qn.y * kk.y + qn.z * kk.z + qn.w * kk.w;
-  }
-  const int tl = lane >> 1;                           // the position whose score this lane holds
-  const float rsum = reduce_scatter16(part, lane);    // all 32 lanes take part
-  const bool valid = tl <= pos;
-  const float sc = valid ? rsum * rsqrtf(float(kHeadDim)) : -INFINITY;
-  float mx = sc;
-#pragma unroll
-  for (int o = 16; o >= 2; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  const float e = valid ? expf(sc - mx) : 0.f;
-  float den = e;
-#pragma unroll
-  for (int o = 16; o >= 2; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-  const float pr = e / den;                           // den >= 1: position 0 is always valid
-  float4 o4 = z4;
-#pragma unroll
-  for (int t = 0; t < kMaxCtx; ++t) {
-    const float4 vv = t < pos0 ? unpack4_f16(vh[t]) : (t == pos0 ? vnew[0] : (t == pos0 + 1 ? vnew[1] : z4));
-    const float w = __shfl_sync(0xffffffffu, pr, 2 * t);
-    o4.x += w * vv.x; o4.y += w * vv.y; o4.z += w * vv.z; o4.w += w * vv.w;
-  }
-  *reinterpret_cast<uint2*>(dst + (size_t((lane >> 1) * n8 + (n >> 3)) << 6) + ((n & 7) << 3) + (lane & 1) * 4) =
-      pack4_f16(o4.x, o4.y, o4.z, o4.w);
-}
-
-// The O projection's operand slices with attention folded in: one warp per
-// (unit, row); the unit's K slice is its q head.
-__device__ void sm_build_oa(const SParams& p, const SG& g, int u0, int nu, int i0, uint8_t* smem) {
-  const int n8 = g.N / 8, warp = threadIdx.x >> 5, grp = p.n_q / p.n_kv;
-  const uint32_t nop = sm_op_slots(g), obytes = sm_op_bytes(g);
-  const float* acc = p.acc_qkv[((g.k - 1) * p.L + g.l) & 1];
-  for (int it = warp; it < nu * g.R; it += kSmConsumerWarps) {
-    const int ui = it / g.R, n = it - ui * g.R, u = u0 + ui, h = u % g.n_ks;
-    uint16_t* dst = reinterpret_cast<uint16_t*>(smem + kSmOffOp + (uint32_t(i0 + ui) % nop) * obytes);
-    // the first tile's unit of each group's first q head appends the group's keys and values
-    sm_attn_row(p, acc, g.k, g.l, h, n, u < g.n_ks && h % grp == 0, dst, n8);
-  }
-}
-
 template <int KIND>
 __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, uint8_t* smem) {
   const int n8 = g.N / 8, per = g.R * 16;
@@ -720,30 +628,6 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
   return true;
 }
 
-// With attention inside the O projection, the q|k|v accumulator of layer n
-// is read by many units, so nothing zeroes it as it is read.  Instead the
-// layers alternate between two accumulators, and the O projection's units of
-// layer n clear, in equal shares by unit index: the gate|up accumulator that
-// layer n's GU projection adds into next (last read by layer n-1's down
-// projection), and the other q|k|v accumulator, which layer n+1's QKV
-// projection adds into (last read by layer n-1's O projection).  Both
-// earlier readers precede layer n's QKV projection, whose tiles these units
-// acquired; both later writers follow the O projection's completion count,
-// which these units release after the stores.
-__device__ void sm_zero_oa(const SParams& p, const SG& g, int beg, int end) {
-  const long long U = (long long)g.n_mt * g.n_ks;
-  const int n = (g.k - 1) * p.L + g.l;
-  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  const long long zg = (long long)g.R * (2 * p.F) / 4;
-  float4* gu = reinterpret_cast<float4*>(p.acc_gu);
-  for (long long i = zg * beg / U + threadIdx.x; i < zg * end / U; i += kSmConsumers) gu[i] = z4;
-  if (n + 1 < p.n_steps * p.L) {
-    const long long zq = (long long)g.R * (p.qw + 2 * p.kvw) / 4;
-    float4* q = reinterpret_cast<float4*>(p.acc_qkv[(n + 1) & 1]);
-    for (long long i = zq * beg / U + threadIdx.x; i < zq * end / U; i += kSmConsumers) q[i] = z4;
-  }
-}
-
 // This CTA's units of GEMM gi (all consumer threads): wait for the operand's
 // source, build the operand slices, drain the accumulators.
 //
@@ -761,20 +645,7 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
   sm_run(g, gi, beg, end);
   if (beg >= end) return true;
   const int t = threadIdx.x;
-  if (KIND == S_OA) {
-    // each unit's head needs its q tile and its group's k and v tiles
-    if (t < 32) {
-      const int grp = p.n_q / p.n_kv;
-      int ok = 1;
-      for (int i = t; i < 3 * (end - beg) && ok; i += 32) {
-        const int h = (beg + i / 3) % g.n_ks, j = h / grp, w = i % 3;
-        const int tile = w == 0 ? h : (w == 1 ? p.qw / kHeadDim + j : (p.qw + p.kvw) / kHeadDim + j);
-        ok = poll_geq(p, sm_qkv_tile(p, g.k, g.l, tile), unsigned(p.d / kKs));
-      }
-      ok = __all_sync(0xffffffffu, ok);
-      if (t == 0) ms.flag[2] = ok;
-    }
-  } else if (t == 0) {
+  if (t == 0) {
     const unsigned* ctr;
     unsigned want;
     sm_ready(p, gi, ctr, want);
@@ -802,8 +673,7 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
       }
       named_bar(SBAR_CONS, kSmConsumers);
       if (!ms.flag[3]) return false;
-      if constexpr (KIND == S_OA) sm_build_oa(p, g, u, nu, u - beg, smem);
-      else sm_build<KIND>(p, g, u, nu, u - beg, smem);
+      sm_build<KIND>(p, g, u, nu, u - beg, smem);
       fence_proxy_async_shared();   // the tensor cores read what these generic stores wrote
       named_bar(SBAR_CONS, kSmConsumers);
       if (t == 0)
@@ -825,7 +695,6 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
   };
   if (end - beg <= int(nop)) {
     if (!build(beg, end)) return false;
-    if (KIND == S_OA) sm_zero_oa(p, g, beg, end);
     scale();
     for (int s = beg; s < end;) {
       const int ks0 = s % g.n_ks, seg_end = min(end, s + (g.n_ks - ks0));
@@ -851,10 +720,7 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
     const int ks0 = s % g.n_ks, mt = s / g.n_ks;
     const int seg_end = min(end, s + (g.n_ks - ks0)), nsl = seg_end - s;
     if (!build(s, seg_end)) return false;
-    if (si == 0) {
-      if (KIND == S_OA) sm_zero_oa(p, g, beg, end);
-      scale();
-    }
+    if (si == 0) scale();
     if (si > 0 && !sm_drain<KIND>(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true)) return false;
     prev_mt = mt;
     prev_nsl = nsl;
@@ -1290,14 +1156,9 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
     // one call site: a GEMM section inlined twice costs instruction fetch
     if (k == 1 || p.proj_in) SM_SECTION(sm_gemm<S_PROJ>(p, ms, smem, sgi_proj(p, k), seg));
     for (int l = 0; l < p.L; ++l) {
-      if (sm_fused(p)) {
-        SM_SECTION(sm_gemm<S_QKV>(p, ms, smem, sgi_of(p, k, l, 0), seg));
-        SM_SECTION(sm_gemm<S_OA>(p, ms, smem, sgi_of(p, k, l, 1), seg));
-      } else {
-        SM_SECTION(sm_gemm<S_QKVU>(p, ms, smem, sgi_of(p, k, l, 0), seg));
-        SM_SECTION(sm_attn(p, ms, k, l));
-        SM_SECTION(sm_gemm<S_O>(p, ms, smem, sgi_of(p, k, l, 1), seg));
-      }
+      SM_SECTION(sm_gemm<S_QKVU>(p, ms, smem, sgi_of(p, k, l, 0), seg));
+      SM_SECTION(sm_attn(p, ms, k, l));
+      SM_SECTION(sm_gemm<S_O>(p, ms, smem, sgi_of(p, k, l, 1), seg));
       SM_SECTION(sm_gemm<S_GU>(p, ms, smem, sgi_of(p, k, l, 2), seg));
       SM_SECTION(sm_gemm<S_DOWN>(p, ms, smem, sgi_of(p, k, l, 3), seg));
     }
@@ -1308,9 +1169,12 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
 #undef SM_SECTION
 }
 
-// The frame-loop kernel is k_frames_small, the state-slot kernel k_slots_small.
+// The greedy frame-loop kernel is k_frames_small, the sampling one
+// k_frames_small_sampled, the state-slot kernel k_slots_small.
 #if QP_SMALL_SLOTS
 #define SM_KERNEL k_slots_small
+#elif QP_SMALL_SAMPLED
+#define SM_KERNEL k_frames_small_sampled
 #else
 #define SM_KERNEL k_frames_small
 #endif
@@ -1425,7 +1289,6 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   p.trace = h->trace; p.trace_n = h->trace_phases;
   p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;
   p.temperature = a.temperature; p.top_k = a.top_k; p.gumbel = a.gumbel;
-  p.fuse = a.B <= kSmFuseFrames;
   p.mode = SM_RUN; p.k_first = 1; p.n_run = g.n_steps; p.n_groups = 1; p.group_rows = a.B;
 }
 
@@ -1460,7 +1323,7 @@ qp_status sm_launch(const qp_handle* h, const SParams& p, uint8_t* sync, size_t 
 
 }  // namespace
 
-#if !QP_SMALL_SLOTS
+#if !QP_SMALL_SLOTS && !QP_SMALL_SAMPLED
 
 size_t small_smem_bytes() { return kSmOffMisc + sizeof(SMisc) + 1024; }
 
@@ -1474,6 +1337,19 @@ bool small_supported(const qp_handle* h, const RunArgs& a) {
 qp_status run_frames_small(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
                            cudaStream_t s) {
   if (!small_supported(h, a) || a.B > bmax) return QP_ERR_ARG;
+  if (a.temperature > 0.f) return run_frames_small_sampled(h, a, scratch, L, bmax, s);
+  const SmSync S = sm_sync_layout(h->g, a.B);
+  if (L.total - L.sync < S.total) return QP_ERR_ARG;
+  uint8_t* sync = scratch + L.sync;
+  SParams p{};
+  sm_fill(p, h, a, scratch, L, sync, S, bmax);
+  return sm_launch(h, p, sync, S.total, s);
+}
+
+#elif QP_SMALL_SAMPLED   // the sampling frame-loop kernel
+
+qp_status run_frames_small_sampled(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
+                                   cudaStream_t s) {
   const SmSync S = sm_sync_layout(h->g, a.B);
   if (L.total - L.sync < S.total) return QP_ERR_ARG;
   uint8_t* sync = scratch + L.sync;
@@ -1520,7 +1396,6 @@ qp_status run_slots_small(qp_handle* h, const SlotArgs& sa, uint8_t* scratch, co
   if (L.total - L.sync < S.total) return QP_ERR_ARG;
   uint8_t* sync = scratch + L.sync;
   sm_fill(p, h, a, scratch, L, sync, S, bmax);
-  p.fuse = 0;
   p.mode = sa.mode;
   p.k_first = sa.mode == SM_STEP ? 2 : 1;
   p.n_run = 1;
