@@ -53,6 +53,8 @@ template <typename T>
 size_t carve_size(size_t count) { return (count * sizeof(T) + 255) & ~size_t(255); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+// int32 / f32 device arrays are read and written element by element
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3) == 0; }
 
 // What a tensor name maps to, and the shape it must have.
 struct Slot {
@@ -348,10 +350,10 @@ static qp_status check_run(qp_handle* h, int B, const float* H, const int32_t* q
   if (!h) return QP_ERR_ARG;
   if (!h->loaded) return QP_ERR_STATE;
   if (B < 1 || B > h->max_batch || !H || !q0 || !out_codes) return QP_ERR_ARG;
-  if (device_ptrs && !aligned16(H)) return QP_ERR_ARG;
+  if (device_ptrs && (!aligned16(H) || !aligned4(q0) || !aligned4(out_codes))) return QP_ERR_ARG;
   if (samp) {
     if (!(samp->temperature > 0.f) || !std::isfinite(samp->temperature)) return QP_ERR_ARG;
-    if (samp->top_k < 1 || samp->top_k > h->g.vocab || !samp->gumbel) return QP_ERR_ARG;
+    if (samp->top_k < 1 || samp->top_k > h->g.vocab || !samp->gumbel || !aligned4(samp->gumbel)) return QP_ERR_ARG;
     if (h->g.vocab > qp::kMaxVocab) return QP_ERR_ARG;
   }
   return QP_OK;
@@ -362,7 +364,7 @@ qp_status qp_predict_frames_ex(qp_handle* h, int B, const float* H, const int32_
                                qp_stream s) {
   qp_status st = check_run(h, B, H, q0, out_codes, samp, true);
   if (st != QP_OK) return st;
-  if (out_logits && !aligned16(out_logits)) return QP_ERR_ARG;
+  if ((out_logits && !aligned16(out_logits)) || !aligned4(forced_codes)) return QP_ERR_ARG;
   DeviceGuard dg(h->device);
   if (!dg.ok) return QP_ERR_CUDA;
   qp::RunArgs a;
@@ -435,7 +437,9 @@ qp_status qp_begin_frames(qp_handle* h, int B, const int32_t* slots, const float
   if (!h) return QP_ERR_ARG;
   if (!h->loaded) return QP_ERR_STATE;
   if (B < 1 || B > h->max_batch || B > qp::kSmallMaxFrames || !slots || !H || !q0 || !out_q1) return QP_ERR_ARG;
-  if (!aligned16(H) || (out_logits && !aligned16(out_logits)) || !slots_ok(h, B, slots)) return QP_ERR_ARG;
+  if (!aligned16(H) || !aligned4(q0) || !aligned4(out_q1) || (out_logits && !aligned16(out_logits)) ||
+      !slots_ok(h, B, slots))
+    return QP_ERR_ARG;
   if (h->wfmt != qp::WF_BF16 || h->hfmt != qp::WF_BF16) return QP_ERR_ARG;
   qp::SlotArgs a;
   a.mode = 1; a.B = B; a.slots = slots; a.H = H; a.q0 = q0; a.out_codes = out_q1; a.out_logits = out_logits;
@@ -448,7 +452,8 @@ qp_status qp_step_frames(qp_handle* h, int B, const int32_t* slots, const int32_
   if (!h->loaded) return QP_ERR_STATE;
   if (B < 1 || B > h->max_batch || B > qp::kSmallMaxFrames || !slots || !steps || !codes_in || !out_codes)
     return QP_ERR_ARG;
-  if ((out_logits && !aligned16(out_logits)) || !slots_ok(h, B, slots)) return QP_ERR_ARG;
+  if (!aligned4(codes_in) || !aligned4(out_codes) || (out_logits && !aligned16(out_logits)) || !slots_ok(h, B, slots))
+    return QP_ERR_ARG;
   for (int b = 0; b < B; ++b)
     if (steps[b] < 2 || steps[b] > h->g.n_steps) return QP_ERR_ARG;
   if (h->wfmt != qp::WF_BF16 || h->hfmt != qp::WF_BF16) return QP_ERR_ARG;

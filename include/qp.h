@@ -146,10 +146,12 @@ qp_status qp_create(const qp_geometry* g, int max_batch, qp_handle** out);
 qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream s);
 
 /* Greedy prediction for B frames (1 <= B <= max_batch), enqueued on s.
- *   H          device, [B, talker_hidden] f32, row-major
+ *   H          device, [B, talker_hidden] f32, row-major, 16-byte aligned
  *   q0         device, [B] int32 in [0, q0_vocab)
  *   out_codes  device, [B, n_steps] int32: q1..q15 per frame
- *   out_logits device, [B, n_steps, vocab] f32, or NULL to skip */
+ *   out_logits device, [B, n_steps, vocab] f32, 16-byte aligned, or NULL to skip
+ * int32 and f32 arrays must be 4-byte aligned; a misaligned pointer is
+ * QP_ERR_ARG. */
 qp_status qp_predict_frames(qp_handle* h, int B, const float* H, const int32_t* q0,
                             int32_t* out_codes, float* out_logits, qp_stream s);
 

@@ -23,8 +23,9 @@
  * (the rows sorted into step groups), as one GEMM.  Slot and step arrays are HOST memory (a scheduler keeps
  * this bookkeeping on the host); the library sorts the rows by step and
  * stages the order to the device on `stream`.  Codes, logits and H/q0 are
- * device memory, in the caller's row order.  Rows of one call must name
- * distinct slots.
+ * device memory, in the caller's row order, aligned as for
+ * qp_predict_frames (H and logits 16 bytes, int32 arrays 4).  Rows of one
+ * call must name distinct slots.
  */
 #ifndef QP_SCHED_H
 #define QP_SCHED_H

@@ -290,3 +290,60 @@ def test_state_slots_need_16_bit_weights(qpk):
         assert e.value.code == 1
     finally:
         cp.close()
+
+
+def test_sixty_four_rows_at_mixed_steps(qpk):
+    """The largest call: 64 slots, every call holding up to 64 rows spread
+    over many steps (uneven step groups), teacher-forced to the oracle."""
+    import torch
+    g = SMALL
+    raw, P, cp = _handle(qpk, g, 74, 64)
+    try:
+        F = 64
+        H, q0 = S.toy_inputs(g, F, seed=570)
+        ref = O.predict_frames(P, H, q0, tol=TOL)
+        chk = Checker(ref)
+        tH, tq = torch.from_numpy(H).cuda(), torch.from_numpy(q0.astype(np.int32)).cuda()
+        lg = torch.empty((F, g.vocab), dtype=torch.float32, device="cuda")
+        slots = list(range(F))
+        chk.add(range(F), [1] * F, cp.begin_frames(slots, tH, tq, out_logits=lg).cpu().numpy(), lg.cpu().numpy())
+        nxt = np.full(F, 2)
+        tick = 0
+        while (nxt <= g.n_steps).any():
+            # frame f starts moving at tick f % 9, so the calls hold frames at many steps
+            rows = [f for f in range(F) if nxt[f] <= g.n_steps and tick >= f % 9]
+            tick += 1
+            if not rows:
+                continue
+            steps = [int(nxt[f]) for f in rows]
+            cin = torch.from_numpy(np.array([ref["codes"][f, s - 2] for f, s in zip(rows, steps)], np.int32)).cuda()
+            lg = torch.empty((len(rows), g.vocab), dtype=torch.float32, device="cuda")
+            out = cp.step_frames([slots[f] for f in rows], steps, cin, out_logits=lg)
+            chk.add(rows, steps, out.cpu().numpy(), lg.cpu().numpy())
+            nxt[rows] += 1
+        assert cp.device_status() == 0
+        assert chk.seen.all()
+        assert chk.err <= TOL, chk.err
+        assert chk.mismatch == 0
+    finally:
+        cp.close()
+
+
+def test_misaligned_pointers_are_refused(small, qpk):
+    import torch
+    raw, P, cp = small
+    g = SMALL
+    buf = torch.zeros(64, dtype=torch.int32, device="cuda")
+    odd = buf.view(torch.uint8)[1:].data_ptr()   # an int32 array cannot start here
+    H = torch.zeros((2, g.talker_hidden), device="cuda")
+    lib = cp._lib
+    import ctypes
+    sl = (ctypes.c_int32 * 2)(0, 1)
+    st = (ctypes.c_int32 * 2)(2, 3)
+    assert lib.qp_begin_frames(cp._h, 2, sl, H.data_ptr(), odd, buf.data_ptr(), None, None) == 1
+    assert lib.qp_begin_frames(cp._h, 2, sl, H.data_ptr(), buf.data_ptr(), odd, None, None) == 1
+    assert lib.qp_step_frames(cp._h, 2, sl, st, odd, buf.data_ptr(), None, None) == 1
+    assert lib.qp_step_frames(cp._h, 2, sl, st, buf.data_ptr(), buf.data_ptr() + 4 * 8, H.data_ptr() + 4, None) == 1
+    assert lib.qp_predict_frames(cp._h, 2, H.data_ptr(), odd, buf.data_ptr(), None, None) == 1
+    assert lib.qp_predict_frames(cp._h, 2, H.data_ptr(), buf.data_ptr(), odd, None, None) == 1
+    assert cp.device_status() == 0
