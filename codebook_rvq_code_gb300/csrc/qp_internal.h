@@ -149,6 +149,8 @@ namespace qp {
 qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s);
 qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s);
 size_t persistent_smem_bytes();
+// the Q8_0 build of the tile engine's kernel (qp_persistent_q8.cu)
+qp_status run_tile_q8(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax, cudaStream_t s);
 // small-batch engine (qp_small.cu): bf16 weights, at most kSmallMaxFrames
 bool small_supported(const qp_handle* h, const RunArgs& a);
 qp_status run_frames_small(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax,

@@ -49,7 +49,16 @@ constexpr int kProducerWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr int kDeqWarp0 = 10;
 constexpr int kDeqThreads = 4 * 32;
-constexpr int kThreads = (kConsumerWarps + 2 + 4) * 32;   // 448
+// This translation unit's kernel: k_frames for 16-bit weights (10 warps:
+// consumers, producer, MMA), or, built from qp_persistent_q8.cu, k_frames_q8
+// for Q8_0 matrices, whose 4 more warps dequantise.  Without them a thread
+// may hold 168 registers instead of 128, and the 16-bit kernel does not
+// spill.
+#ifndef QP_TILE_Q8
+#define QP_TILE_Q8 0
+#endif
+constexpr bool kTileQ8 = QP_TILE_Q8 != 0;
+constexpr int kThreads = (kConsumerWarps + 2 + (kTileQ8 ? 4 : 0)) * 32;   // 320 or 448
 
 constexpr uint32_t kSlotBytes = kTileM * kKs * 2;              // 32 KB f16 slice
 constexpr uint32_t kQ8Bytes = kTileM * kKs;                    // 16 KB int8 slice
@@ -124,6 +133,9 @@ struct PParams {
   int B; const float* H; const int32_t* q0; int32_t* out_codes; float* out_logits; const int32_t* forced;
   float temperature; int top_k; const float* gumbel;
 };
+
+// Q8_0 matrices: only the Q8_0 build of the kernel has the dequantising warps.
+__device__ __forceinline__ bool tq8(const PParams& p) { return kTileQ8 && p.q8; }
 
 // ------------------------------------------------------------ event log
 // With tracing on, each CTA also keeps an event log after the section stamps:
@@ -277,12 +289,12 @@ __device__ __forceinline__ unsigned* head_done(const PParams& p, int k, int ch) 
 // Every slice thus takes the same path in program order: each mbarrier's
 // waiters stay within one phase of it, which parity waits require.
 __device__ __forceinline__ bool slice_is_q8(const PParams& p, const GI& G) {
-  return p.q8 && (G.kind != G_HEAD || p.q8_head);
+  return tq8(p) && (G.kind != G_HEAD || p.q8_head);
 }
 
 __device__ void producer_role(const PParams& p, Misc& ms, uint8_t* smem) {
-  const int nslot = p.q8 ? kNSlotQ8 : kNSlotF16;
-  const uint32_t stride = p.q8 ? kQ8SlotBytes : kSlotBytes;
+  const int nslot = tq8(p) ? kNSlotQ8 : kNSlotF16;
+  const uint32_t stride = tq8(p) ? kQ8SlotBytes : kSlotBytes;
   const uint64_t pol = policy_evict_first();
   uint32_t it = 0;      // raw-slot copies issued
   for (int gi = 0; gi < p.NGEMM; ++gi) {
@@ -293,7 +305,7 @@ __device__ void producer_role(const PParams& p, Misc& ms, uint8_t* smem) {
     my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
     for (int s = beg; s < end; ++s) {
       const int ks = s % G.n_ks, mt = (s / G.n_ks) % G.n_mt;
-      if (p.q8 && !q8g) {
+      if (tq8(p) && !q8g) {
         const size_t tile = size_t(mt) * G.n_ks + ks;
         for (int h = 0; h < 2; ++h, ++it) {
           const uint32_t slot = it % nslot, u = it / nslot;
@@ -309,7 +321,7 @@ __device__ void producer_role(const PParams& p, Misc& ms, uint8_t* smem) {
       {
         const size_t tile = size_t(mt) * G.n_ks + ks;
         uint8_t* dst = smem + kOffRing + slot * stride;
-        if (p.q8) {
+        if (tq8(p)) {
           mbar_expect_tx(&ms.wfull[slot], kQ8SlotBytes);
           bulk_g2s_stream(dst, G.w + tile * kQ8Bytes, kQ8Bytes, &ms.wfull[slot], pol);
           bulk_g2s_stream(dst + kQ8Bytes, reinterpret_cast<const uint8_t*>(G.s) + tile * kQ8ScaleBytes, kQ8ScaleBytes,
@@ -467,7 +479,7 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
       const uint32_t a = a_comp % kNAct, au = a_comp / kNAct;
       const uint8_t* A;
       uint64_t* wfree;
-      if (p.q8) {
+      if (tq8(p)) {
         const uint32_t ds = wit % kNDeq;
         if (!mwait(p, &ms.dfull[ds], (wit / kNDeq) & 1)) { ok = false; break; }
         A = smem + kOffDeq + ds * kSlotBytes;
@@ -1076,7 +1088,12 @@ __device__ void consumer_role(const PParams& p, Misc& ms, uint8_t* smem) {
 #undef QP_SECTION
 }
 
-__global__ void __launch_bounds__(kThreads, 1) k_frames(const PParams p) {
+#if QP_TILE_Q8
+#define TILE_KERNEL k_frames_q8
+#else
+#define TILE_KERNEL k_frames
+#endif
+__global__ void __launch_bounds__(kThreads, 1) TILE_KERNEL(const PParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   Misc& ms = *reinterpret_cast<Misc*>(smem + kOffMisc);
@@ -1105,7 +1122,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_frames(const PParams p) {
   } else if (warp == kMmaWarp) {
     if ((t & 31) == 0) mma_role(p, ms, smem);
     __syncwarp();
-  } else if (p.q8) {
+  } else if (tq8(p)) {
     dequant_role(p, ms, smem);
   }
   tc_fence_before();
@@ -1207,7 +1224,7 @@ qp_status launch(qp_handle* h, PParams& p, uint8_t* scratch, const Scratch& L, u
                  cudaStream_t s, bool* attr_done) {
   const qp_geometry& g = h->g;
   if (!*attr_done) {
-    if (cudaFuncSetAttribute(k_frames, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(TILE_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(persistent_smem_bytes())) != cudaSuccess) {
       cudaGetLastError();
       return QP_ERR_CUDA;
@@ -1226,7 +1243,7 @@ qp_status launch(qp_handle* h, PParams& p, uint8_t* scratch, const Scratch& L, u
     return QP_ERR_CUDA;
   }
   void* args[] = {&p};
-  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(k_frames), dim3(h->num_sms), dim3(kThreads), args,
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(TILE_KERNEL), dim3(h->num_sms), dim3(kThreads), args,
                                   persistent_smem_bytes(), s) != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;
@@ -1237,6 +1254,21 @@ qp_status launch(qp_handle* h, PParams& p, uint8_t* scratch, const Scratch& L, u
 bool g_attr_done[64] = {};
 
 }  // namespace
+
+#if QP_TILE_Q8
+
+// The Q8_0 kernel's launch; run_frames_persistent and run_frames_static
+// (16-bit build) send calls with Q8_0 matrices here.
+qp_status run_tile_q8(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax, cudaStream_t s) {
+  const SyncLayout S = sync_layout(h->g, a.B);
+  PParams p{};
+  fill_params(p, h, a, scratch, L, scratch + L.sync, S, bmax);
+  bool* done = h->device >= 0 && h->device < 64 ? &g_attr_done[h->device] : nullptr;
+  bool local = false;
+  return launch(h, p, scratch, L, scratch + L.sync, S, s, done ? done : &local);
+}
+
+#else
 
 size_t persistent_smem_bytes() { return kOffMisc + sizeof(Misc) + 1024; }
 
@@ -1270,6 +1302,7 @@ size_t sync_bytes(const qp_geometry& g, int B) { return sync_layout(g, B).total;
 qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   if (a.temperature > 0.f && h->g.vocab > kMaxVocab) return QP_ERR_ARG;
   uint8_t* scratch = static_cast<uint8_t*>(h->sarena);
+  if (h->wfmt == WF_Q8_0) return run_tile_q8(h, a, scratch, h->scr, h->max_batch, s);
   const SyncLayout S = sync_layout(h->g, a.B);
   PParams p{};
   fill_params(p, h, a, scratch, h->scr, scratch + h->scr.sync, S, h->max_batch);
@@ -1328,11 +1361,14 @@ qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   if (h->engine == QP_ENGINE_SMALL && !sm) return QP_ERR_ARG;
   const bool pick = h->engine == QP_ENGINE_SMALL || (h->engine == QP_ENGINE_AUTO && a.B <= kSmallAutoFrames);
   if (sm && pick) return run_frames_small(h, ga, base, L, a.B, s);
+  if (h->wfmt == WF_Q8_0) return run_tile_q8(h, ga, base, L, a.B, s);
   PParams p{};
   fill_params(p, h, ga, base, L, base + L.sync, S, a.B);
   // the launch zeroes the synchronisation words and accumulators; every
   // other byte is written before it is read within the call
   return launch(h, p, base, L, base + L.sync, S, s, &g_static_attr[h->device]);
 }
+
+#endif
 
 }  // namespace qp
