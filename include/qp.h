@@ -31,7 +31,12 @@
  *     are latched in a device status word; qp_get_device_status reads and
  *     clears it.  Kernels never trap: a bad token is clamped for addressing
  *     and reported.
- *   - A handle may be used from one host thread at a time.
+ *   - A handle may be used from one host thread at a time, and its calls
+ *     share one scratch area (activations, KV cache, synchronisation
+ *     words): calls on one handle must not overlap on the GPU, so a caller
+ *     that uses several streams orders them (events) or uses one handle per
+ *     stream.  The KV state slots of include/qp_sched.h live in that same
+ *     area, so a prediction call on a handle ends the frames in its slots.
  */
 #ifndef QP_H
 #define QP_H
