@@ -266,6 +266,27 @@ __device__ __forceinline__ void my_run(int tiles, int n_ks, int gi, int& beg, in
   end = (p1 / S) * n_ks + ((p1 % S) * n_ks) / S;
 }
 
+// This CTA's place among the contributors of tile tt in my_run's split (the
+// owners of the tile's S parts).  Returns the rank of this CTA (-1 if it
+// holds no part of the tile) and sets n to the number of contributors.
+// With fewer parts than CTAs each CTA holds at most one part, and the S
+// owners need not be consecutive; otherwise every CTA holds a part and the
+// owners are consecutive in the rotated CTA index.
+__device__ __forceinline__ int tile_share(int tiles, int n_ks, int gi, int tt, int& n) {
+  const int G = gridDim.x, g = (blockIdx.x + gi * 37) % G;
+  const int S = max(1, min(n_ks, G / tiles));
+  const long long P = (long long)tiles * S, q0 = (long long)tt * S;
+  if (P < G) {
+    const long long p0 = P * g / G, p1 = P * (g + 1) / G;
+    n = S;
+    return p1 > p0 && p0 >= q0 && p0 < q0 + S ? int(p0 - q0) : -1;
+  }
+  // the owner of part q: the largest g with floor(P * g / G) <= q
+  const int g0 = int(((q0 + 1) * G - 1) / P), g1 = int(((q0 + S) * G - 1) / P);
+  n = g1 - g0 + 1;
+  return g >= g0 && g <= g1 ? g - g0 : -1;
+}
+
 // sync-region accessors
 __device__ __forceinline__ unsigned* tile_cnt(const PParams& p, int gi, int ch, int mt) {
   return p.tile_cnt + (size_t(gi) * p.NCH + ch) * p.MT + mt;
@@ -783,16 +804,16 @@ __device__ bool attn_items(const PParams& p, Misc& ms, int k, int l) {
   return true;
 }
 
-// Finishing work of a completed tile, by the CTA whose contribution
-// completed it (all consumer threads).  Each warp takes rows warp, warp + 8,
-// ...; the loads of several of its rows are issued together.
+// Finishing work of rows [lo, hi) of a completed tile (all consumer threads
+// of one of the tile's contributing CTAs; the contributors split the rows).
+// Each warp takes rows lo + warp, lo + warp + 8, ...; the loads of several
+// of its rows are issued together.
 template <int KIND>
-__device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, int ch, int mt, Ck c) {
+__device__ bool finish_rows(const PParams& p, Misc& ms, const GI& G, int gi, int ch, int mt, Ck c, int lo, int hi) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   if (KIND == G_QKV) return true;
   if (KIND == G_PROJ || KIND == G_O || KIND == G_DOWN) {
-    const int rows = rows_in(G.R, c, ch);
     const float* X = G.acc;
     const int feat = mt * kTileM + lane * 4;
     bool to_head = false;
@@ -811,18 +832,18 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
     const float4 wv = *reinterpret_cast<const float4*>(w + feat);
     const int P = G.k == 1 ? 2 : 1;
     const Ck ch_h = chunking(p.B);
-    for (int r0 = warp; r0 < rows; r0 += 8 * kConsumerWarps) {
+    for (int r0 = lo + warp; r0 < hi; r0 += 8 * kConsumerWarps) {
       float4 xv[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int row = r0 + u * kConsumerWarps, n = ch * c.Nc + row;
-        const bool use = row < rows && (!to_head || (n % P) == P - 1);
+        const bool use = row < hi && (!to_head || (n % P) == P - 1);
         xv[u] = use ? __ldcg(reinterpret_cast<const float4*>(X + size_t(n) * p.d + feat)) : z4;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int row = r0 + u * kConsumerWarps, n = ch * c.Nc + row;
-        if (row >= rows || (to_head && (n % P) != P - 1)) continue;
+        if (row >= hi || (to_head && (n % P) != P - 1)) continue;
         const float4 x = xv[u];
         const float sq = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
         const int nr = to_head ? n / P : n;
@@ -832,14 +853,14 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
       }
     }
     named_bar(BAR_CONS, kConsumers);
-    if (t == 0) {
+    if (t == 0 && hi > lo) {
       // release: the bar.sync above orders every consumer thread's writes first
       if (!to_head) {
-        red_release_add(ready_cnt(p, gi_n, ch, mt), unsigned(rows));
-        red_release_add(ss_cnt(p, gi_n, ch), unsigned(rows));
+        red_release_add(ready_cnt(p, gi_n, ch, mt), unsigned(hi - lo));
+        red_release_add(ss_cnt(p, gi_n, ch), unsigned(hi - lo));
       } else {
-        // frames whose last position lies in this chunk: [nlo/P, nhi/P)
-        const int f0 = (ch * c.Nc) / P, f1 = (ch * c.Nc + rows) / P;
+        // frames whose last position lies in these rows: [nlo/P, nhi/P)
+        const int f0 = (ch * c.Nc + lo) / P, f1 = (ch * c.Nc + hi) / P;
         for (int hc = f0 / ch_h.Nc; f1 > f0 && hc <= (f1 - 1) / ch_h.Nc; ++hc) {
           const int lo = max(f0, hc * ch_h.Nc), hi = min(f1, (hc + 1) * ch_h.Nc);
           red_release_add(ready_cnt(p, gi_n, hc, mt), unsigned(hi - lo));
@@ -850,26 +871,24 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
     return true;
   }
   if (KIND == G_GU) {
-    const int nkd = p.F / kTileM, kd = mt % nkd;
-    if (t == 0) ms.flag[2] = atom_add_acq_rel(pair_cnt(p, G.k, G.l, ch, kd), 1u) == 1u;
-    named_bar(BAR_CONS, kConsumers);
-    if (!ms.flag[2]) return true;
-    const int rows = rows_in(G.R, c, ch);
+    // mt is the pair's gate tile: gate|up tiles mt and F/128 + mt hold
+    // columns 128 mt .. +127 of gate and of up
+    const int kd = mt;
     uint16_t* act_d = G.k == 1 ? p.a1[4] : p.ak[3];
     const int feat = kd * kTileM + lane * 4;
-    for (int r0 = warp; r0 < rows; r0 += 4 * kConsumerWarps) {
+    for (int r0 = lo + warp; r0 < hi; r0 += 4 * kConsumerWarps) {
       float4 gv[4], uv[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int row = r0 + u * kConsumerWarps;
         const float* gp = G.acc + size_t(ch * c.Nc + row) * 2 * p.F + feat;
-        gv[u] = row < rows ? __ldcg(reinterpret_cast<const float4*>(gp)) : z4;
-        uv[u] = row < rows ? __ldcg(reinterpret_cast<const float4*>(gp + p.F)) : z4;
+        gv[u] = row < hi ? __ldcg(reinterpret_cast<const float4*>(gp)) : z4;
+        uv[u] = row < hi ? __ldcg(reinterpret_cast<const float4*>(gp + p.F)) : z4;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int row = r0 + u * kConsumerWarps, n = ch * c.Nc + row;
-        if (row >= rows) continue;
+        if (row >= hi) continue;
         float* gp = G.acc + size_t(n) * 2 * p.F + feat;
         const float4 g = gv[u], uu = uv[u];
         *reinterpret_cast<uint2*>(act_d + act_off(n, feat, p.F, c)) =
@@ -879,25 +898,24 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
       }
     }
     named_bar(BAR_CONS, kConsumers);
-    if (t == 0) red_release_add(ready_cnt(p, gi + 1, ch, kd), unsigned(rows));
+    if (t == 0 && hi > lo) red_release_add(ready_cnt(p, gi + 1, ch, kd), unsigned(hi - lo));
     return true;
   }
   // G_HEAD: final logits of 128 codebook entries for the chunk's frames
   {
-    const int rows = rows_in(p.B, c, ch);
     const int col = mt * kTileM + lane * 4;
     const bool greedy = p.temperature <= 0.f;
-    for (int r0 = warp; r0 < rows; r0 += 4 * kConsumerWarps) {
+    for (int r0 = lo + warp; r0 < hi; r0 += 4 * kConsumerWarps) {
       float4 lv[4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int row = r0 + u * kConsumerWarps;
-        lv[u] = row < rows ? __ldcg(reinterpret_cast<const float4*>(p.logits + size_t(ch * c.Nc + row) * p.V + col)) : z4;
+        lv[u] = row < hi ? __ldcg(reinterpret_cast<const float4*>(p.logits + size_t(ch * c.Nc + row) * p.V + col)) : z4;
       }
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int row = r0 + u * kConsumerWarps, b = ch * c.Nc + row;
-        if (row >= rows) continue;
+        if (row >= hi) continue;
         const float4 lg = lv[u];
         if (p.out_logits)
           *reinterpret_cast<float4*>(p.out_logits + (size_t(b) * p.n_steps + (G.k - 1)) * p.V + col) = lg;
@@ -915,7 +933,12 @@ __device__ bool last_arriver(const PParams& p, Misc& ms, const GI& G, int gi, in
       }
     }
     named_bar(BAR_CONS, kConsumers);
-    if (t == 0) red_release_add(head_done(p, G.k, ch), 1u);
+    if (t == 0 && hi > lo) {
+      // the tile counter counts the finished rows past its K slices: the
+      // share that completes the tile's rows counts the tile done
+      const unsigned add = unsigned(hi - lo), full = unsigned(G.n_ks) + unsigned(rows_in(G.R, c, ch));
+      if (atom_add_acq_rel(tile_cnt(p, gi, ch, mt), add) + add == full) red_release_add(head_done(p, G.k, ch), 1u);
+    }
     return true;
   }
 }
@@ -984,17 +1007,42 @@ __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, ui
     named_bar(BAR_CONS, kConsumers);
     if (t == 0) {
       ev_cons(p, &ms.evc, EV_REDS, gi);
-      const unsigned old = atom_add_acq_rel(tile_cnt(p, gi, ch, mt), unsigned(nsl));
-      ms.flag[0] = old + unsigned(nsl) == unsigned(G.n_ks);
+      // release: the bar.sync above orders every consumer thread's reductions first
+      red_release_add(tile_cnt(p, gi, ch, mt), unsigned(nsl));
       ev_cons(p, &ms.evc, EV_COUNTED, gi);
-    }
-    named_bar(BAR_CONS, kConsumers);
-    if (ms.flag[0]) {
-      if (!last_arriver<KIND>(p, ms, G, gi, ch, mt, c)) return false;
-      if (t == 0) ev_cons(p, &ms.evc, EV_LASTDONE, gi);
     }
     ++seg;
     s = seg_end;
+  }
+  if (KIND == G_QKV || beg >= end) return true;   // attention items read the QKV tiles as they complete
+  // The finishing passes of the tiles this CTA added into, once every
+  // contribution is in: the tile's contributors split its rows, so a pass
+  // takes a fraction of one CTA's time.  All of this CTA's drains precede
+  // these waits, and every contributor drains before it waits, so each wait
+  // ends.  A gate|up pair (gate tile kd, up tile F/128 + kd) is finished by
+  // the contributors of both.
+  const int tiles = c.n * G.n_mt;
+  for (int tt = beg / G.n_ks; tt <= (end - 1) / G.n_ks; ++tt) {
+    const int mt = tt % G.n_mt, ch = tt / G.n_mt, rows = rows_in(G.R, c, ch);
+    int n = 0, rank = tile_share(tiles, G.n_ks, gi, tt, n), mt_f = mt;
+    if (KIND == G_GU) {
+      const int nkd = p.F / kTileM, kd = mt % nkd, tg = ch * G.n_mt + kd, tu = tg + nkd;
+      int ng = 0, nu = 0;
+      const int rg = tile_share(tiles, G.n_ks, gi, tg, ng), ru = tile_share(tiles, G.n_ks, gi, tu, nu);
+      rank = mt < nkd ? rg : ng + ru;
+      n = ng + nu;
+      mt_f = kd;
+      if (t == 0)
+        ms.flag[1] = poll_geq(p, tile_cnt(p, gi, ch, kd), unsigned(G.n_ks)) &&
+                     poll_geq(p, tile_cnt(p, gi, ch, kd + nkd), unsigned(G.n_ks));
+    } else if (t == 0) {
+      ms.flag[1] = poll_geq(p, tile_cnt(p, gi, ch, mt), unsigned(G.n_ks));
+    }
+    named_bar(BAR_CONS, kConsumers);
+    if (!ms.flag[1]) return false;
+    const int lo = int((long long)rows * rank / n), hi = int((long long)rows * (rank + 1) / n);
+    if (!finish_rows<KIND>(p, ms, G, gi, ch, mt_f, c, lo, hi)) return false;
+    if (t == 0) ev_cons(p, &ms.evc, EV_LASTDONE, gi);
   }
   return true;
 }
