@@ -239,8 +239,8 @@ def whole_job(local_ms: float, frames_per_step: int, steps: int, world: int, dev
 
 def engine_of(B: int, gemm_format: str) -> str:
     """The schedule QP_ENGINE_AUTO picks (include/qp_debug.h): the small-batch
-    engine for bf16 calls of at most 48 frames, the tile engine otherwise."""
-    return "small" if gemm_format == "bf16" and B <= 48 else "tile"
+    engine for bf16 calls of at most 40 frames, the tile engine otherwise."""
+    return "small" if gemm_format == "bf16" and B <= 40 else "tile"
 
 
 def sweep(g, dev, stream, steps, hbm, tf):

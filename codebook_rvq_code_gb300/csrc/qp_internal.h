@@ -96,11 +96,11 @@ size_t sync_bytes(const qp_geometry& g, int B);
 // Largest batch the small-batch engine serves (2B <= 128 activation rows at
 // step 1: one tensor-core N chunk), and the largest it is chosen for
 // automatically: its operand slices are built from f32 sources by every CTA
-// that uses them, which beyond ~52 frames costs more per step on GB300 than
-// the tile engine's one finishing pass (measured: 221 vs 230 us per step at
-// 48 frames, 243 vs 239 at 56).
+// that uses them, which beyond ~40 frames costs more per step on GB300 than
+// the tile engine's shared finishing passes (measured: 205.5 vs 207.7 us per
+// step at 40 frames, 221.7 vs 209.1 at 48).
 constexpr int kSmallMaxFrames = 64;
-constexpr int kSmallAutoFrames = 48;
+constexpr int kSmallAutoFrames = 40;
 
 }  // namespace qp
 

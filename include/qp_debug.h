@@ -28,7 +28,7 @@ extern "C" {
  * weights with at most 64 frames per call: partials go straight into their
  * destination and each consumer builds its operand slice from it, which
  * removes one dependent global round trip per GEMM.  QP_ENGINE_AUTO (the
- * default) takes the small-batch engine for bf16 calls of at most 48 frames,
+ * default) takes the small-batch engine for bf16 calls of at most 40 frames,
  * where it is the faster of the two on GB300, and the tile engine otherwise. */
 typedef enum {
   QP_ENGINE_AUTO = 0,
