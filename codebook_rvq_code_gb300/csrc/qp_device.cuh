@@ -60,6 +60,11 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
   asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+// A relaxed add: after fence_acq_rel_gpu(), a run of these releases the
+// writes before the fence as each red.release would, with one fence.
+__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
 // Fetch-and-add with acquire-release semantics at GPU scope: publishes this
 // CTA's earlier writes (ordered before it by bar.sync) and, for the caller
 // that completes a count, makes every earlier contributor's writes visible.

@@ -575,8 +575,10 @@ __device__ bool prep1_items(const PParams& p) {
     for (int kk = lane * 4; kk < p.d; kk += 128)
       *reinterpret_cast<float4*>(p.x1 + size_t(r) * p.d + kk) = *reinterpret_cast<const float4*>(p.b_proj + kk);
     __syncwarp();
-    if (lane == 0)
-      for (int ks = 0; ks < p.th / kKs; ++ks) red_release_add(ready_cnt(p, 0, ch, ks), 1);
+    if (lane == 0) {
+      fence_acq_rel_gpu();   // one fence releases the row for every slice count below
+      for (int ks = 0; ks < p.th / kKs; ++ks) red_relaxed_add(ready_cnt(p, 0, ch, ks), 1);
+    }
   }
   return true;
 }
@@ -637,7 +639,8 @@ __device__ bool prepk_items(const PParams& p, int k) {
       __syncwarp();
       if (lane == 0) {
         const int ch = b / c.Nc;
-        for (int ks = 0; ks < p.th / kKs; ++ks) red_release_add(ready_cnt(p, gp, ch, ks), 1);
+        fence_acq_rel_gpu();   // one fence releases the row for every slice count below
+        for (int ks = 0; ks < p.th / kKs; ++ks) red_relaxed_add(ready_cnt(p, gp, ch, ks), 1);
       }
       continue;
     }
@@ -654,8 +657,9 @@ __device__ bool prepk_items(const PParams& p, int k) {
     __syncwarp();
     if (lane == 0) {
       const int ch = b / c.Nc;
-      for (int ks = 0; ks < p.d / kKs; ++ks) red_release_add(ready_cnt(p, gi, ch, ks), 1);
-      red_release_add(ss_cnt(p, gi, ch), unsigned(p.d / kTileM));
+      fence_acq_rel_gpu();   // one fence releases the row for every count below
+      for (int ks = 0; ks < p.d / kKs; ++ks) red_relaxed_add(ready_cnt(p, gi, ch, ks), 1);
+      red_relaxed_add(ss_cnt(p, gi, ch), unsigned(p.d / kTileM));
     }
   }
   return true;
@@ -855,16 +859,17 @@ __device__ bool finish_rows(const PParams& p, Misc& ms, const GI& G, int gi, int
     named_bar(BAR_CONS, kConsumers);
     if (t == 0 && hi > lo) {
       // release: the bar.sync above orders every consumer thread's writes first
+      fence_acq_rel_gpu();   // one fence releases the rows for every count below
       if (!to_head) {
-        red_release_add(ready_cnt(p, gi_n, ch, mt), unsigned(hi - lo));
-        red_release_add(ss_cnt(p, gi_n, ch), unsigned(hi - lo));
+        red_relaxed_add(ready_cnt(p, gi_n, ch, mt), unsigned(hi - lo));
+        red_relaxed_add(ss_cnt(p, gi_n, ch), unsigned(hi - lo));
       } else {
         // frames whose last position lies in these rows: [nlo/P, nhi/P)
         const int f0 = (ch * c.Nc + lo) / P, f1 = (ch * c.Nc + hi) / P;
         for (int hc = f0 / ch_h.Nc; f1 > f0 && hc <= (f1 - 1) / ch_h.Nc; ++hc) {
           const int lo = max(f0, hc * ch_h.Nc), hi = min(f1, (hc + 1) * ch_h.Nc);
-          red_release_add(ready_cnt(p, gi_n, hc, mt), unsigned(hi - lo));
-          red_release_add(ss_cnt(p, gi_n, hc), unsigned(hi - lo));
+          red_relaxed_add(ready_cnt(p, gi_n, hc, mt), unsigned(hi - lo));
+          red_relaxed_add(ss_cnt(p, gi_n, hc), unsigned(hi - lo));
         }
       }
     }

@@ -620,8 +620,9 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
     named_bar(SBAR_CONS, kSmConsumers);
     if (t == 0) {
       // release: the bar.sync above orders every consumer thread's reductions first
-      if (kQkv<KIND>) red_release_add(sm_qkv_tile(p, g.k, g.l, mt), unsigned(nsl));
-      red_release_add(sm_done(p, gi), unsigned(nsl));
+      fence_acq_rel_gpu();   // one fence releases the reductions for both counts
+      if (kQkv<KIND>) red_relaxed_add(sm_qkv_tile(p, g.k, g.l, mt), unsigned(nsl));
+      red_relaxed_add(sm_done(p, gi), unsigned(nsl));
       sm_ev(p, &ms.evc, SEV_PUBLISHED, gi);
     }
   }
@@ -703,14 +704,16 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
     }
     named_bar(SBAR_CONS, kSmConsumers);
     if (t == 0) {
-      // release: the bar.sync above orders every consumer thread's reductions first
+      // release: the bar.sync above orders every consumer thread's reductions
+      // first, and one fence releases them for every count below
+      fence_acq_rel_gpu();
       if (kQkv<KIND>)
         for (int s = beg; s < end;) {
           const int ks0 = s % g.n_ks, seg_end = min(end, s + (g.n_ks - ks0));
-          red_release_add(sm_qkv_tile(p, g.k, g.l, s / g.n_ks), unsigned(seg_end - s));
+          red_relaxed_add(sm_qkv_tile(p, g.k, g.l, s / g.n_ks), unsigned(seg_end - s));
           s = seg_end;
         }
-      red_release_add(sm_done(p, gi), unsigned(end - beg));
+      red_relaxed_add(sm_done(p, gi), unsigned(end - beg));
       sm_ev(p, &ms.evc, SEV_PUBLISHED, gi);
     }
     return true;
