@@ -1,7 +1,7 @@
 """Both schedules of the frame loop against the oracle, through the C ABI.
 
 The small-batch engine serves bf16 calls of at most 64 frames (the default
-for them); the tile engine serves every call.  Each is forced here on the
+for them up to 40); the tile engine serves every call.  Each is forced here on the
 batch sizes the other would take, and the two are compared with each other.
 """
 import numpy as np
@@ -145,3 +145,39 @@ def test_full_size_sampling_small(full_bf16):
     finally:
         cp.set_engine("auto")
     assert_parity(st)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "q8_0"])
+@pytest.mark.parametrize("B", [129, 300])
+def test_tile_engine_repeated_calls_ragged_chunks(qpk, fmt, B):
+    """Row chunks of 128 with a ragged last chunk, called repeatedly: every
+    call's sampled frames match the oracle (teacher-forced) and the device
+    status stays clear, so no wait between the CTAs that finish a tile
+    together ever runs out."""
+    import torch
+    g = SMALL
+    raw = S.make_weights(g, seed=13, gemm_format=fmt, norm_mode="perturbed")
+    P = O.Predictor.from_raw(g, raw)
+    cp = qpk.CodePredictor(g, max_batch=B)
+    try:
+        cp.load_raw_weights(raw)
+        cp.set_engine("tile")
+        H, q0 = S.toy_inputs(g, B, seed=B)
+        rows = sample_rows(B, 12)
+        ref = O.predict_frames(P, H[rows], q0[rows], tol=TOL)
+        forced = np.zeros((B, g.n_steps), np.int32)
+        forced[rows] = ref["codes"]
+        tH, tq = torch.from_numpy(H).cuda(), torch.from_numpy(q0.astype(np.int32)).cuda()
+        tf = torch.from_numpy(forced).cuda()
+        for _ in range(5):
+            lg = torch.full((B, g.n_steps, g.vocab), float("nan"), device="cuda")
+            codes = cp.predict(tH, tq, out_logits=lg, forced=tf)
+            torch.cuda.synchronize()
+            assert cp.device_status() == 0
+            got = lg.cpu().numpy()[rows]
+            assert np.isfinite(got).all()
+            assert float(np.abs(got - ref["logits"]).max()) <= TOL
+            c = codes.cpu().numpy()[rows]
+            assert (c[ref["decidable"]] == ref["codes"][ref["decidable"]]).all()
+    finally:
+        cp.close()
