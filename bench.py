@@ -56,7 +56,8 @@ def peaks():
 
 
 # ---------------------------------------------------------------------------
-# algorithmic work of one call ("Roofline")
+# algorithmic work of one call: weight bytes of the whole loop plus frame I/O,
+# and the FLOPs of every position's GEMMs, heads and attention
 # ---------------------------------------------------------------------------
 
 def work_of(g, B: int, gemm_format: str, sampling: bool):

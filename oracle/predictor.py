@@ -24,7 +24,7 @@ What it computes, and where the pages say so:
   tables and 15 lm_heads) and "Expected verification shapes" (HF [out, in]).
   "No ... RoPE permutation occurs" in the same section: rotate-half RoPE.
 
-Readings taken where the pages are silent (each is listed in the design doc):
+Readings taken where the pages are silent:
 positions 0 = small_to_mtp(H), 1 = small_to_mtp(E0[q0]), k+1 = E[k-1][q_k]
 for k = 1..14 (hidden-wide tables enter unprojected; Talker-wide tables,
 2048 x 2048 in the exporter page's shapes, pass through small_to_mtp); RMSNorm x*rsqrt(mean
