@@ -185,6 +185,13 @@ def time_oracle(g, raw, w, frames: int, budget_s: float):
     return done / el, done, el
 
 
+def config_of(g, w, world: int):
+    """The workload's config, the same on both arms."""
+    return {"workload": w.name, "B": w.B, "steps_per_frame": g.n_steps, "engine": engine_of(w.B, w.gemm_format),
+            "l2": f"flushed between timed iterations ({L2_FLUSH_BYTES >> 20} MB write)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
+
+
 def reference_arm(args, g, raw, w):
     import oracle as O
     P = O.Predictor.from_raw(g, raw)
@@ -206,7 +213,7 @@ def reference_arm(args, g, raw, w):
         "impl": "reference", "metric": METRIC, "value": fps, "unit": "frames/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "frames_per_step": frames},
+        "data": "synthetic", "config": config_of(g, w, args.gpus),
         "cpu_baseline": {"value": fps, "unit": "frames/s", "cores": cores, "kind": "oracle", "sample": sample},
         "e2e": {"value": fps, "unit": "frames/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -602,9 +609,7 @@ def main():
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16" if w.gemm_format == "bf16" else "q8_0",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": B, "steps_per_frame": g.n_steps, "engine": engine_of(B, w.gemm_format),
-                   "l2": f"flushed between timed iterations ({L2_FLUSH_BYTES >> 20} MB write)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": config_of(g, w, world),
         "us_per_step": 1e3 * ms_per_step / g.n_steps,
         "roofline": roof,
         "gpu_launches": launches,
