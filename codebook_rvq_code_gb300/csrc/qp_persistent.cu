@@ -125,7 +125,7 @@ struct PParams {
   uint16_t* kv;   // f16 [layer][frame][pos][k|v][kv_width]
   int Bmax;
   // per-call synchronisation (zeroed before the launch)
-  unsigned* tile_cnt; unsigned* ready; unsigned* ss_cnt; float* ss; unsigned* pair; unsigned* head_done;
+  unsigned* tile_cnt; unsigned* ready; unsigned* ss_cnt; float* ss; unsigned* head_done;
   unsigned long long* codepk; unsigned* decided; int* abort_flag; int* status;
   int NCH, MT, KS, NGEMM;
   unsigned long long* trace; int trace_n;
@@ -296,9 +296,6 @@ __device__ __forceinline__ unsigned* ready_cnt(const PParams& p, int gi, int ch,
 }
 __device__ __forceinline__ unsigned* ss_cnt(const PParams& p, int gi, int ch) { return p.ss_cnt + size_t(gi) * p.NCH + ch; }
 __device__ __forceinline__ float* ss_at(const PParams& p, int gi, int row) { return p.ss + size_t(gi) * 2 * p.B + row; }
-__device__ __forceinline__ unsigned* pair_cnt(const PParams& p, int k, int l, int ch, int kd) {
-  return p.pair + ((size_t(k - 1) * p.L + l) * p.NCH + ch) * (p.F / kTileM) + kd;
-}
 __device__ __forceinline__ unsigned* head_done(const PParams& p, int k, int ch) {
   return p.head_done + size_t(k - 1) * p.NCH + ch;
 }
@@ -1188,7 +1185,7 @@ __global__ void __launch_bounds__(kThreads, 1) TILE_KERNEL(const PParams p) {
 size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
 struct SyncLayout {
-  size_t tile_cnt, ready, ss_cnt, ss, pair, head_done, codepk, decided, abort_flag, total;
+  size_t tile_cnt, ready, ss_cnt, ss, head_done, codepk, decided, abort_flag, total;
   int NCH, MT, KS, NGEMM;
 };
 
@@ -1213,7 +1210,6 @@ SyncLayout sync_layout(const qp_geometry& g, int B) {
   S.ready = o;    o += al256(size_t(S.NGEMM) * S.NCH * S.KS * 4);
   S.ss_cnt = o;   o += al256(size_t(S.NGEMM) * S.NCH * 4);
   S.ss = o;       o += al256(size_t(S.NGEMM) * R1 * 4);
-  S.pair = o;     o += al256(size_t(g.n_steps) * g.layers * S.NCH * (g.ffn / kTileM) * 4);
   S.head_done = o; o += al256(size_t(g.n_steps) * S.NCH * 4);
   S.codepk = o;   o += al256(size_t(g.n_steps) * B * 8);
   S.decided = o;  o += al256(size_t(g.n_steps) * B * 4);
@@ -1260,7 +1256,6 @@ void fill_params(PParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scra
   p.ready = reinterpret_cast<unsigned*>(sync + S.ready);
   p.ss_cnt = reinterpret_cast<unsigned*>(sync + S.ss_cnt);
   p.ss = reinterpret_cast<float*>(sync + S.ss);
-  p.pair = reinterpret_cast<unsigned*>(sync + S.pair);
   p.head_done = reinterpret_cast<unsigned*>(sync + S.head_done);
   p.codepk = reinterpret_cast<unsigned long long*>(sync + S.codepk);
   p.decided = reinterpret_cast<unsigned*>(sync + S.decided);
