@@ -551,10 +551,20 @@ __device__ bool prep1_items(const PParams& p) {
   const Ck c = chunking(R);
   for (int r = blockIdx.x + warp * G; r < R; r += kConsumerWarps * G) {
     const int b = r >> 1, ch = r / c.Nc;
+    constexpr int kG = 8;   // loads in flight per lane before the stores
     if ((r & 1) == 0) {
-      for (int kk = lane * 4; kk < p.th; kk += 128) {
-        const float4 h = *reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + kk);
-        *reinterpret_cast<uint2*>(p.a1[0] + act_off(r, kk, p.th, c)) = pack4_f16(h.x, h.y, h.z, h.w);
+      for (int k0 = lane * 4; k0 < p.th; k0 += 128 * kG) {
+        float4 hv[kG];
+#pragma unroll
+        for (int i = 0; i < kG; ++i)
+          hv[i] = k0 + i * 128 < p.th ? __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k0 + i * 128))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < kG; ++i) {
+          if (k0 + i * 128 >= p.th) break;
+          *reinterpret_cast<uint2*>(p.a1[0] + act_off(r, k0 + i * 128, p.th, c)) =
+              pack4_f16(hv[i].x, hv[i].y, hv[i].z, hv[i].w);
+        }
       }
     } else {
       int q = p.q0[b];
@@ -562,11 +572,19 @@ __device__ bool prep1_items(const PParams& p) {
         if (lane == 0) set_status(p.status, QP_ERR_BAD_TOKEN);
         q = q < 0 ? 0 : p.q0_vocab - 1;
       }
-      for (int kk = lane * 4; kk < p.th; kk += 128) {
-        const uint2 e = *reinterpret_cast<const uint2*>(p.e0 + size_t(q) * p.th + kk);
-        *reinterpret_cast<uint2*>(p.a1[0] + act_off(r, kk, p.th, c)) =
-            pack4_f16(e16_to_f32(e.x, p.embed_f16), e16_to_f32(e.x >> 16, p.embed_f16), e16_to_f32(e.y, p.embed_f16),
-                      e16_to_f32(e.y >> 16, p.embed_f16));
+      for (int k0 = lane * 4; k0 < p.th; k0 += 128 * kG) {
+        uint2 ev[kG];
+#pragma unroll
+        for (int i = 0; i < kG; ++i)
+          ev[i] = k0 + i * 128 < p.th ? __ldg(reinterpret_cast<const uint2*>(p.e0 + size_t(q) * p.th + k0 + i * 128))
+                                      : make_uint2(0, 0);
+#pragma unroll
+        for (int i = 0; i < kG; ++i) {
+          if (k0 + i * 128 >= p.th) break;
+          *reinterpret_cast<uint2*>(p.a1[0] + act_off(r, k0 + i * 128, p.th, c)) =
+              pack4_f16(e16_to_f32(ev[i].x, p.embed_f16), e16_to_f32(ev[i].x >> 16, p.embed_f16),
+                        e16_to_f32(ev[i].y, p.embed_f16), e16_to_f32(ev[i].y >> 16, p.embed_f16));
+        }
       }
     }
     for (int kk = lane * 4; kk < p.d; kk += 128)
@@ -625,11 +643,19 @@ __device__ bool prepk_items(const PParams& p, int k) {
       // f16(E[k-2][nc]); the residual row starts at the projection's bias
       const int gp = gi_proj(p, k);
       const uint16_t* e = p.embed[k - 2] + size_t(nc) * p.th;
-      for (int kk = lane * 4; kk < p.th; kk += 128) {
-        const uint2 ev = *reinterpret_cast<const uint2*>(e + kk);
-        *reinterpret_cast<uint2*>(p.a1[0] + act_off(b, kk, p.th, c)) =
-            pack4_f16(e16_to_f32(ev.x, p.embed_f16), e16_to_f32(ev.x >> 16, p.embed_f16),
-                      e16_to_f32(ev.y, p.embed_f16), e16_to_f32(ev.y >> 16, p.embed_f16));
+      constexpr int kG = 8;   // loads in flight per lane before the stores
+      for (int k0 = lane * 4; k0 < p.th; k0 += 128 * kG) {
+        uint2 ev[kG];
+#pragma unroll
+        for (int i = 0; i < kG; ++i)
+          ev[i] = k0 + i * 128 < p.th ? __ldg(reinterpret_cast<const uint2*>(e + k0 + i * 128)) : make_uint2(0, 0);
+#pragma unroll
+        for (int i = 0; i < kG; ++i) {
+          if (k0 + i * 128 >= p.th) break;
+          *reinterpret_cast<uint2*>(p.a1[0] + act_off(b, k0 + i * 128, p.th, c)) =
+              pack4_f16(e16_to_f32(ev[i].x, p.embed_f16), e16_to_f32(ev[i].x >> 16, p.embed_f16),
+                        e16_to_f32(ev[i].y, p.embed_f16), e16_to_f32(ev[i].y >> 16, p.embed_f16));
+        }
       }
       for (int kk = lane * 4; kk < p.d; kk += 128)
         *reinterpret_cast<float4*>(p.xk + size_t(b) * p.d + kk) = *reinterpret_cast<const float4*>(p.b_proj + kk);
@@ -642,13 +668,29 @@ __device__ bool prepk_items(const PParams& p, int k) {
       continue;
     }
     const uint16_t* e = p.embed[k - 2] + size_t(nc) * p.d;
-    for (int kk = lane * 4; kk < p.d; kk += 128) {
-      const uint2 ev = *reinterpret_cast<const uint2*>(e + kk);
-      const float v0 = e16_to_f32(ev.x, p.embed_f16), v1 = e16_to_f32(ev.x >> 16, p.embed_f16);
-      const float v2 = e16_to_f32(ev.y, p.embed_f16), v3 = e16_to_f32(ev.y >> 16, p.embed_f16);
-      *reinterpret_cast<float4*>(p.xk + size_t(b) * p.d + kk) = make_float4(v0, v1, v2, v3);
-      const float4 w = *reinterpret_cast<const float4*>(wn + kk);
-      *reinterpret_cast<uint2*>(p.ak[0] + act_off(b, kk, p.d, c)) = pack4_f16(v0 * w.x, v1 * w.y, v2 * w.z, v3 * w.w);
+    // the row's loads all in flight before its stores (a store could alias a
+    // later load, so the compiler keeps a fused loop's loads in order)
+    constexpr int kG = 8;   // 1024 columns per pass
+    for (int k0 = lane * 4; k0 < p.d; k0 += 128 * kG) {
+      uint2 ev[kG];
+      float4 wv[kG];
+#pragma unroll
+      for (int i = 0; i < kG; ++i) {
+        const int kk = k0 + i * 128;
+        ev[i] = kk < p.d ? __ldg(reinterpret_cast<const uint2*>(e + kk)) : make_uint2(0, 0);
+        wv[i] = kk < p.d ? __ldg(reinterpret_cast<const float4*>(wn + kk)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int i = 0; i < kG; ++i) {
+        const int kk = k0 + i * 128;
+        if (kk >= p.d) break;
+        const float v0 = e16_to_f32(ev[i].x, p.embed_f16), v1 = e16_to_f32(ev[i].x >> 16, p.embed_f16);
+        const float v2 = e16_to_f32(ev[i].y, p.embed_f16), v3 = e16_to_f32(ev[i].y >> 16, p.embed_f16);
+        *reinterpret_cast<float4*>(p.xk + size_t(b) * p.d + kk) = make_float4(v0, v1, v2, v3);
+        const float4 w = wv[i];
+        *reinterpret_cast<uint2*>(p.ak[0] + act_off(b, kk, p.d, c)) =
+            pack4_f16(v0 * w.x, v1 * w.y, v2 * w.z, v3 * w.w);
+      }
     }
     if (lane == 0) *ss_at(p, gi, b) = p.embed_ss[k - 2][nc];
     __syncwarp();
