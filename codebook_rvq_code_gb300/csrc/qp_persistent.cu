@@ -1101,7 +1101,15 @@ __device__ bool decide_items(const PParams& p, Misc& ms, uint32_t* keys, int k) 
     named_bar(BAR_CONS, kConsumers);
     if (!ms.flag[3]) return false;
     float* l = p.logits + size_t(b) * V;
-    for (int i = t; i < V; i += kConsumers) keys[i] = f32_order_key(__ldcg(l + i) / T);
+    // the row's loads all in flight before the key stores (8 per thread at V = 2048)
+    for (int i0 = t; i0 < V; i0 += 8 * kConsumers) {
+      float lv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) lv[u] = i0 + u * kConsumers < V ? __ldcg(l + i0 + u * kConsumers) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u * kConsumers < V) keys[i0 + u * kConsumers] = f32_order_key(lv[u] / T);
+    }
     int remaining;
     const uint32_t kth = topk_kth_key<kConsumers>(keys, V, p.top_k, ms.hist, ms.sel, BAR_CONS, remaining);
     const int per = (V + kConsumers - 1) / kConsumers, lo = t * per, hi = min(V, lo + per);

@@ -1097,7 +1097,15 @@ __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
     if (!ms.flag[3]) return false;
     float* l = p.logits + size_t(b) * V;
     const float rs = k > 1 ? sm_row_inv(p, ms, b) : 1.f;
-    for (int i = t; i < V; i += kSmConsumers) keys[i] = f32_order_key(__ldcg(l + i) * rs / T);
+    // the row's loads all in flight before the key stores (8 per thread at V = 2048)
+    for (int i0 = t; i0 < V; i0 += 8 * kSmConsumers) {
+      float lv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) lv[u] = i0 + u * kSmConsumers < V ? __ldcg(l + i0 + u * kSmConsumers) : 0.f;
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if (i0 + u * kSmConsumers < V) keys[i0 + u * kSmConsumers] = f32_order_key(lv[u] * rs / T);
+    }
     int remaining;
     const uint32_t kth = topk_kth_key<kSmConsumers>(keys, V, p.top_k, ms.hist, ms.sel, SBAR_CONS, remaining);
     const int per = (V + kSmConsumers - 1) / kSmConsumers, lo = t * per, hi = min(V, lo + per);
