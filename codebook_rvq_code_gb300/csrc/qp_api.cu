@@ -165,8 +165,7 @@ qp_status qp_create(const qp_geometry* gp, int max_batch, qp_handle** out) {
   const int ctx = g.n_steps + 1;
   const size_t fbytes = carve_size<int>(64) + carve_size<float2>(size_t(ctx) * 64) +
                         carve_size<float>(size_t(max_batch) * g.talker_hidden) + carve_size<int32_t>(max_batch) +
-                        carve_size<int32_t>(size_t(max_batch) * g.n_steps) +
-                        carve_size<const uint16_t*>(qp::kMaxSteps);
+                        carve_size<int32_t>(size_t(max_batch) * g.n_steps);
   if (cudaMalloc(&h->farena, fbytes) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(h->sarena);
@@ -179,7 +178,6 @@ qp_status qp_create(const qp_geometry* gp, int max_batch, qp_handle** out) {
   h->H_stage = carve<float>(p, size_t(max_batch) * g.talker_hidden);
   h->q0_stage = carve<int32_t>(p, max_batch);
   h->codes_stage = carve<int32_t>(p, size_t(max_batch) * g.n_steps);
-  h->embed_dev = carve<const uint16_t*>(p, qp::kMaxSteps);
 
   // RoPE table: angle pos * theta^(-2i/head_dim) formed in double, rounded once.
   std::vector<float2> cs(size_t(ctx) * 64);
@@ -334,9 +332,6 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
     h->head[j] = alloc_mat(g.vocab, d, hfmt);
     put(h->head[j], 0, "code_pred.lm_head." + std::to_string(j) + ".weight");
   }
-  // the tables' device addresses, for qp_code_embeddings (from the handle's
-  // own array, which outlives the copy)
-  chk(cudaMemcpyAsync(h->embed_dev, h->embed, size_t(g.n_steps) * sizeof(void*), cudaMemcpyHostToDevice, s));
   if (err != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;
@@ -540,7 +535,7 @@ qp_status qp_code_embeddings(qp_handle* h, int B, const int32_t* codes, float* o
   DeviceGuard dg(h->device);
   if (!dg.ok) return QP_ERR_CUDA;
   const qp_geometry& g = h->g;
-  if (qp::code_embeddings(h->embed_dev, g.n_steps, g.vocab, g.code_embed_dim, codes, B, out, h->status, h->embed_f16,
+  if (qp::code_embeddings(h->embed, g.n_steps, g.vocab, g.code_embed_dim, codes, B, out, h->status, h->embed_f16,
                           static_cast<cudaStream_t>(sv)) != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;

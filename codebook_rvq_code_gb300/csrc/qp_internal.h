@@ -137,7 +137,6 @@ struct qp_handle {
   float* H_stage = nullptr;                     // host-buffer entry point staging
   int32_t* q0_stage = nullptr;
   int32_t* codes_stage = nullptr;
-  const uint16_t** embed_dev = nullptr;         // device copy of embed[] (qp_code_embeddings)
   unsigned long long* trace = nullptr;          // optional phase trace (qp_debug.h)
   int trace_phases = 0;
 
@@ -170,10 +169,10 @@ size_t packed_bytes(int fmt, int N, int K);
 cudaError_t pack_rows(const void* src, int fmt, bool src_f16, int rows, int K, const PackedMat& dst, int row0,
                       cudaStream_t s);
 // out[b][j] = tables[j][codes[b][j]] as f32 for b < B, j < n_tables
-// (tables_dev: a device array of n_tables device pointers to [V, d] tables,
-// f16 if f16, else bf16).
-cudaError_t code_embeddings(const uint16_t* const* tables_dev, int n_tables, int V, int d, const int32_t* codes,
-                            int B, float* out, int* status, bool f16, cudaStream_t s);
+// (tables: a host array of n_tables <= kMaxSteps device pointers to [V, d]
+// tables, f16 if f16, else bf16).
+cudaError_t code_embeddings(const uint16_t* const* tables, int n_tables, int V, int d, const int32_t* codes, int B,
+                            float* out, int* status, bool f16, cudaStream_t s);
 // out[r] = sum_i E[r, i]^2 (f32) for a [rows, cols] 16-bit table (f16 if f16, else bf16).
 cudaError_t row_sumsq_e16(const uint16_t* E, int rows, int cols, bool f16, float* out, cudaStream_t s);
 }  // namespace qp

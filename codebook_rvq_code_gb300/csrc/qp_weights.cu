@@ -80,23 +80,39 @@ __global__ void k_row_sumsq(const uint16_t* __restrict__ E, int cols, float* __r
 }
 
 // out[b][j][:] = E_j[codes[b][j]][:] (f16 or bf16 -> f32, exact), 4 values a thread.
-__global__ void k_code_embeddings(const uint16_t* const* __restrict__ tables, int n_tables, int V, int d,
-                                  const int32_t* __restrict__ codes, long long B, float* __restrict__ out,
-                                  int* status, bool f16) {
-  const int d4 = d / 4;
-  const long long total = B * n_tables * d4;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < total;
-       i += (long long)gridDim.x * blockDim.x) {
-    const long long row = i / d4;                 // b * n_tables + j
-    const int j = int(row % n_tables), c4 = int(i % d4);
+struct EmbTables {
+  const uint16_t* t[kMaxSteps];
+};
+
+// One warp per output row (frame b, table j): the row's code once, then all
+// of a lane's pieces of the table row loaded before any of its stores.
+__global__ void k_code_embeddings(EmbTables tabs, int n_tables, int V, int d, const int32_t* __restrict__ codes,
+                                  long long rows, float* __restrict__ out, int* status, bool f16) {
+  const int lane = threadIdx.x & 31;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long row = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5; row < rows; row += nw) {
+    const int j = int(row % n_tables);
     int code = codes[row];
     if (code < 0 || code >= V) {
-      if (c4 == 0) set_status(status, QP_ERR_BAD_TOKEN);
+      if (lane == 0) set_status(status, QP_ERR_BAD_TOKEN);
       code = code < 0 ? 0 : V - 1;
     }
-    const uint2 e = *reinterpret_cast<const uint2*>(tables[j] + size_t(code) * d + c4 * 4);
-    *reinterpret_cast<float4*>(out + row * d + c4 * 4) =
-        make_float4(e16_to_f32(e.x, f16), e16_to_f32(e.x >> 16, f16), e16_to_f32(e.y, f16), e16_to_f32(e.y >> 16, f16));
+    const uint16_t* src = tabs.t[j] + size_t(code) * d;
+    float* dst = out + row * d;
+    constexpr int kG = 8;   // 1024 columns per pass
+    for (int c0 = lane * 4; c0 < d; c0 += 128 * kG) {
+      uint2 e[kG];
+#pragma unroll
+      for (int i = 0; i < kG; ++i)
+        e[i] = c0 + i * 128 < d ? __ldg(reinterpret_cast<const uint2*>(src + c0 + i * 128)) : make_uint2(0, 0);
+#pragma unroll
+      for (int i = 0; i < kG; ++i) {
+        if (c0 + i * 128 >= d) break;
+        *reinterpret_cast<float4*>(dst + c0 + i * 128) =
+            make_float4(e16_to_f32(e[i].x, f16), e16_to_f32(e[i].x >> 16, f16), e16_to_f32(e[i].y, f16),
+                        e16_to_f32(e[i].y >> 16, f16));
+      }
+    }
   }
 }
 
@@ -121,10 +137,15 @@ cudaError_t pack_rows(const void* src, int fmt, bool src_f16, int rows, int K, c
   return cudaGetLastError();
 }
 
-cudaError_t code_embeddings(const uint16_t* const* tables_dev, int n_tables, int V, int d, const int32_t* codes,
-                            int B, float* out, int* status, bool f16, cudaStream_t s) {
-  const size_t total = size_t(B) * n_tables * (d / 4);
-  k_code_embeddings<<<grid_for(total), 256, 0, s>>>(tables_dev, n_tables, V, d, codes, B, out, status, f16);
+cudaError_t code_embeddings(const uint16_t* const* tables, int n_tables, int V, int d, const int32_t* codes, int B,
+                            float* out, int* status, bool f16, cudaStream_t s) {
+  if (n_tables < 1 || n_tables > kMaxSteps) return cudaErrorInvalidValue;
+  EmbTables tabs{};
+  for (int j = 0; j < n_tables; ++j) tabs.t[j] = tables[j];
+  const long long rows = (long long)B * n_tables;
+  const long long blocks = (rows + 7) / 8;   // 8 warps of 256 threads, a row each
+  k_code_embeddings<<<int(blocks < 8192 ? blocks : 8192), 256, 0, s>>>(tabs, n_tables, V, d, codes, rows, out, status,
+                                                                       f16);
   return cudaGetLastError();
 }
 
