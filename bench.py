@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import glob
 import json
 import os
@@ -80,9 +81,14 @@ def work_of(g, B: int, gemm_format: str, sampling: bool):
 
 
 def source_hash():
+    """Hash of the CUDA sources with comments and blank space removed, so that
+    a recorded traffic figure stays valid across comment-only edits."""
     h = hashlib.sha256()
     for f in sorted(glob.glob(os.path.join(ROOT, "codebook_rvq_code_gb300", "csrc", "*"))):
-        h.update(open(f, "rb").read())
+        text = open(f, encoding="utf-8").read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -26,12 +26,12 @@
 //   consumer warps drain accumulators into f32 buffers (red.add, so slices
 //                  of one tile may come from several CTAs), and run the
 //                  elementwise work.
-// There are no grid-wide barriers.  Each output tile carries a counter; the
-// CTA whose contribution completes a tile (the "last arriver") finishes it:
-// an x tile becomes the next GEMM's operand f16(x * w_norm) plus partial
-// sums of squares (the next GEMM scales its output by 1/rms), a gate/up tile
-// pair becomes the down operand silu(g)*u, a logits tile feeds the greedy
-// argmax.  Attention runs one warp per (frame, kv head) as soon as that
+// There are no grid-wide barriers.  Each output tile carries a counter; once
+// it is complete, the CTAs that added into the tile finish it, each its share
+// of the rows: an x tile becomes the next GEMM's operand f16(x * w_norm) plus
+// partial sums of squares (the next GEMM scales its output by 1/rms), a
+// gate/up tile pair becomes the down operand silu(g)*u, a logits tile feeds
+// the greedy argmax.  Attention runs one warp per (frame, kv head) as soon as that
 // head's q/k/v tiles are complete.  Consumers wait only on work earlier in
 // the one program order every CTA follows, so the earliest pending item can
 // always run: no deadlock.  Every wait is bounded; one that runs out latches
