@@ -33,10 +33,10 @@ h // (Hq/Hkv); scale 1/sqrt(head_dim); SwiGLU silu(gate)*up; greedy =
 lowest index among maxima; sampling = Gumbel-max over the top-k of
 logits/T, ordered (value desc, index asc), lowest index on ties.
 
-Everything is float32 (the precision the task fixes for this oracle).
-Weights are the exact f32 values of their bf16 storage; Q8_0 weights are
-d*q rounded once to f16, the value the tensor cores multiply by (the
-comparison is to run on the same rounded weights as the GPU).
+Everything is float32 (the precision fixed for this oracle).  Weights are
+the exact f32 values of their stored form: the bf16 bit patterns, and for
+Q8_0 the product d*q of each block's f16 scale and int8 value, which the
+GGUF exporter page gives as the weight's value and which is exact in f32.
 """
 from __future__ import annotations
 
@@ -94,12 +94,15 @@ def round_to_f16(w: np.ndarray) -> np.ndarray:
     return w.astype(np.float16).astype(np.float32)
 
 
-def weights_to_f32(raw, q8_0_operand: str = "f16") -> Dict[str, np.ndarray]:
+def weights_to_f32(raw, q8_0_operand: str = "exact") -> Dict[str, np.ndarray]:
     """Map ``{name: synthetic.RawTensor}`` to ``{name: f32 array}``.
 
-    Q8_0 matrices: the predictor computes with the dequantised weights as
-    rounded for its tensor-core operands, so ``q8_0_operand='f16'`` (the
-    default) gives f16(d*q); ``'exact'`` gives d*q itself."""
+    Q8_0 matrices take their stored value d*q ("rightkit-qts 0.2.3",
+    "Upstream differences & verification scope").  ``q8_0_operand='f16'``
+    is a diagnostic only: it rounds d*q once to f16, which shows how much
+    of a difference a single f16 rounding of the weights accounts for."""
+    if q8_0_operand not in ("exact", "f16"):
+        raise ValueError(f"q8_0_operand must be 'exact' or 'f16', not {q8_0_operand!r}")
     out = {}
     for name, t in raw.items():
         if t.dtype == "bf16":
@@ -204,7 +207,7 @@ class Predictor:
         self.e0 = W["talker.codec_embd.weight"]
 
     @classmethod
-    def from_raw(cls, g, raw, q8_0_operand: str = "f16"):
+    def from_raw(cls, g, raw, q8_0_operand: str = "exact"):
         return cls(g, weights_to_f32(raw, q8_0_operand))
 
     # -- one decoder layer applied to one new position of every row ---------

@@ -513,16 +513,21 @@ def test_mutant_without_cache_append_is_caught():
     assert not np.allclose(a["logits"], b["logits"], rtol=1e-5, atol=1e-5)
 
 
-def test_q8_0_operand_rounding_is_nearest_f16():
-    """The f16 operand of a dequantised weight is d*q rounded to nearest-even,
-    which numpy's float16 conversion (a library routine) also gives; values
-    already on the f16 grid pass unchanged."""
+def test_q8_0_weight_value_is_exact_d_times_q():
+    """By default a Q8_0 weight is d*q itself (the exporter page's value), not
+    a rounding of it: the oracle's weights equal the product of the block's
+    f16 scale and int8 value formed here in f64, and the f16 diagnostic
+    variant is d*q rounded to nearest-even, which numpy's float16
+    conversion (a library routine) also gives; values already on the f16
+    grid pass unchanged."""
     rng = np.random.default_rng(14)
     qq = rng.integers(-127, 128, size=(3, 64)).astype(np.int8)
     dd = rng.uniform(1e-4, 2e-3, size=(3, 2)).astype(np.float16)
     raw = {"m": S.RawTensor("m", S.Q8_0, (3, 64), S.pack_q8_0(qq, dd))}
-    exact = O.weights_to_f32(raw, "exact")["m"]
-    got = O.weights_to_f32(raw)["m"]
+    exact = O.weights_to_f32(raw)["m"]
+    want = (qq.astype(np.float64).reshape(3, 2, 32) * dd.astype(np.float64)[:, :, None]).reshape(3, 64)
+    np.testing.assert_array_equal(exact.astype(np.float64), want)
+    got = O.weights_to_f32(raw, "f16")["m"]
     np.testing.assert_array_equal(got, exact.astype(np.float16).astype(np.float32))
     assert np.abs(got - exact).max() <= np.abs(exact).max() * 2.0 ** -11
     on_grid = np.float16([0.5, -0.25, 1.5e-3]).astype(np.float32)
