@@ -64,19 +64,26 @@ constexpr uint32_t kSlotBytes = kTileM * kKs * 2;              // 32 KB f16 slic
 constexpr uint32_t kQ8Bytes = kTileM * kKs;                    // 16 KB int8 slice
 constexpr uint32_t kQ8ScaleBytes = (kKs / 32) * kTileM * 2;    // 1 KB of scales
 constexpr uint32_t kQ8SlotBytes = kQ8Bytes + kQ8ScaleBytes;
-constexpr int kNSlotF16 = 4, kNSlotQ8 = 3, kNDeq = 2, kNAct = 2;
+// A dequantised Q8_0 slice is two f16 images, hi = f16(d*q) and lo =
+// f16(d*q - hi), whose sum is d*q exactly (below); they take two
+// consecutive places of a ring of kNDeq 32 KB places, a 16-bit head slice
+// among Q8_0 matrices one.
+constexpr int kNSlotF16 = 4, kNSlotQ8 = 2, kNDeq = 3, kNAct = 2;
 constexpr uint32_t kActBytes = kKs * kMaxNc * 2;               // 32 KB operand slice
 constexpr uint32_t kTmemCols = 256;                            // two 128-column accumulators
 
-// shared memory map (offsets from a 1 KB aligned base)
+// shared memory map (offsets from a 1 KB aligned base).  The 16-bit kernel
+// has no dequantised places; the Q8_0 kernel's raw ring is smaller than the
+// 16-bit ring, and its activation slots sit after the dequantised places.
 constexpr uint32_t kOffRing = 0;                               // f16 slots, or Q8_0 raw slots
-constexpr uint32_t kOffDeq = 53248;                            // Q8_0: dequantised slots
-constexpr uint32_t kOffAct = 131072;                           // activation operand slots
+constexpr uint32_t kOffDeq = 35840;                            // Q8_0: dequantised places
+constexpr uint32_t kOffAct = kTileQ8 ? kOffDeq + kNDeq * kSlotBytes : kNSlotF16 * kSlotBytes;   // activation slots
 constexpr uint32_t kOffKeys = kOffAct + kNAct * kActBytes;     // top-k keys
 constexpr uint32_t kOffMisc = kOffKeys + kMaxVocab * 4;
 static_assert(kNSlotQ8 * kQ8SlotBytes <= kOffDeq, "raw Q8_0 slots overlap the dequantised ones");
 static_assert(kSlotBytes / 2 <= kQ8SlotBytes && kNSlotQ8 >= 2, "a 16-bit slice takes two raw slots");
-static_assert(kOffDeq + kNDeq * kSlotBytes <= kOffAct, "dequantised slots overlap the operand slots");
+static_assert(kNDeq >= 2, "a Q8_0 slice takes two dequantised places");
+static_assert(kOffDeq % 1024 == 0 && kOffAct % 1024 == 0, "operand images start on 1 KB boundaries");
 static_assert(kNSlotF16 * kSlotBytes <= kOffAct, "f16 slots overlap the operand slots");
 
 enum { BAR_CONS = 1, BAR_DEQ = 2 };
@@ -358,37 +365,49 @@ drain:
 }
 
 // --------------------------------------------------------- Q8_0 dequant
-// Four int8 values (one 32-bit word, little-endian) times an f16 scale, as
-// four f16: q is made exact in f16 as (1024 + (q + 128)) - 1152 -- the
-// mantissa of an f16 in [1024, 2048) holds the integer -- and the product
-// d * q is one correctly rounded f16 multiply, i.e. d * q rounded to the
-// nearest f16.
-__device__ __forceinline__ uint2 q8x4_to_f16x4(uint32_t w, __half2 d2) {
+// Four int8 values (one 32-bit word, little-endian) times an f16 scale d, as
+// two f16 quadruples hi and lo with hi + lo = d * q.  q is made exact in
+// f16 as (1024 + (q + 128)) - 1152 -- the mantissa of an f16 in [1024, 2048)
+// holds the integer; hi = d * q rounded once to the nearest f16 (one f16
+// multiply), lo = d * q - hi from one fused multiply-add, rounded once.
+// d * q - hi is a multiple of d's last place (q is an integer) and at most
+// half of hi's, so it needs at most 7 significant bits and lo holds it
+// exactly whenever d >= 2^-14 (the smallest normal f16): the pair is the
+// stored weight d * q, with no rounding.
+__device__ __forceinline__ void q8x4_to_f16x4_hilo(uint32_t w, __half2 d2, uint2& hi, uint2& lo) {
   const uint32_t u = w ^ 0x80808080u;                 // q + 128 in each byte
-  const uint32_t lo = __byte_perm(u, 0x64646464u, 0x5150);   // bytes 0,1 -> f16 0x64xx
-  const uint32_t hi = __byte_perm(u, 0x64646464u, 0x5352);   // bytes 2,3
+  const uint32_t b01 = __byte_perm(u, 0x64646464u, 0x5150);   // bytes 0,1 -> f16 0x64xx
+  const uint32_t b23 = __byte_perm(u, 0x64646464u, 0x5352);   // bytes 2,3
   const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
-  const __half2 a = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&lo), bias), d2);
-  const __half2 b = __hmul2(__hsub2(*reinterpret_cast<const __half2*>(&hi), bias), d2);
-  return make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+  const __half2 qa = __hsub2(*reinterpret_cast<const __half2*>(&b01), bias);
+  const __half2 qb = __hsub2(*reinterpret_cast<const __half2*>(&b23), bias);
+  const __half2 ha = __hmul2(qa, d2), hb = __hmul2(qb, d2);
+  const __half2 la = __hfma2(qa, d2, __hneg2(ha)), lb = __hfma2(qb, d2, __hneg2(hb));
+  hi = make_uint2(*reinterpret_cast<const uint32_t*>(&ha), *reinterpret_cast<const uint32_t*>(&hb));
+  lo = make_uint2(*reinterpret_cast<const uint32_t*>(&la), *reinterpret_cast<const uint32_t*>(&lb));
 }
 
+// Dequantised places: a ring of kNDeq 32 KB images that the dequantising
+// warps fill in program order and the MMA warp empties in the same order;
+// a Q8_0 slice takes two consecutive places (hi, lo), a 16-bit slice one.
 __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
   const int t = threadIdx.x - kDeqWarp0 * 32;
-  uint32_t it = 0, rit = 0;   // dequantised-slot sequence; raw slots
+  uint32_t it = 0, rit = 0;   // dequantised places used; raw slots used
   for (int gi = 0; gi < p.NGEMM; ++gi) {
     const GI G = gemm_inst(p, gi);
     const Ck c = chunking(G.R);
     const bool q8g = slice_is_q8(p, G);
     int beg, end;
     my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
-    for (int s = beg; s < end; ++s, ++it, rit += q8g ? 1 : 2) {
-      const uint32_t rs = rit % kNSlotQ8, ru = rit / kNSlotQ8, ds = it % kNDeq, du = it / kNDeq;
+    for (int s = beg; s < end; ++s, it += q8g ? 2 : 1, rit += q8g ? 1 : 2) {
+      const uint32_t rs = rit % kNSlotQ8, ru = rit / kNSlotQ8;
       const uint32_t rs2 = (rit + 1) % kNSlotQ8, ru2 = (rit + 1) / kNSlotQ8;
+      const uint32_t ds = it % kNDeq, du = it / kNDeq, ds2 = (it + 1) % kNDeq, du2 = (it + 1) / kNDeq;
       if (t == 0) {   // the leader waits for every dequant thread, then broadcasts
         bool w = mwait(p, &ms.wfull[rs], ru & 1);
         if (w && !q8g) w = mwait(p, &ms.wfull[rs2], ru2 & 1);
         if (w && du > 0) w = mwait(p, &ms.dempty[ds], (du - 1) & 1);
+        if (w && q8g && du2 > 0) w = mwait(p, &ms.dempty[ds2], (du2 - 1) & 1);
         ms.deq_ok = w;
       }
       named_bar(BAR_DEQ, kDeqThreads);
@@ -412,12 +431,13 @@ __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
       const uint8_t* src = smem + kOffRing + rs * kQ8SlotBytes;
       const int8_t* qv = reinterpret_cast<const int8_t*>(src);
       const __half* sc = reinterpret_cast<const __half*>(src + kQ8Bytes);
-      uint16_t* dq = reinterpret_cast<uint16_t*>(smem + kOffDeq + ds * kSlotBytes);
+      uint16_t* dh = reinterpret_cast<uint16_t*>(smem + kOffDeq + ds * kSlotBytes);
+      uint16_t* dl = reinterpret_cast<uint16_t*>(smem + kOffDeq + ds2 * kSlotBytes);
       for (int e = t * 16; e < kTileM * kKs; e += kDeqThreads * 16) {
         // e walks [k8][m8][8 rows][8 k]; 16 values are two rows of one core matrix
         const uint4 raw = *reinterpret_cast<const uint4*>(qv + e);
         const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t out[8];
+        uint32_t hi8[8], lo8[8];
 #pragma unroll
         for (int h2 = 0; h2 < 2; ++h2) {
           const int ee = e + h2 * 8;
@@ -425,19 +445,23 @@ __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
           const __half2 d2 = __half2half2(sc[(k8 >> 2) * kTileM + m]);
 #pragma unroll
           for (int i = 0; i < 2; ++i) {
-            const uint2 pr = q8x4_to_f16x4(w4[h2 * 2 + i], d2);
-            out[h2 * 4 + i * 2] = pr.x;
-            out[h2 * 4 + i * 2 + 1] = pr.y;
+            uint2 h, l;
+            q8x4_to_f16x4_hilo(w4[h2 * 2 + i], d2, h, l);
+            hi8[h2 * 4 + i * 2] = h.x; hi8[h2 * 4 + i * 2 + 1] = h.y;
+            lo8[h2 * 4 + i * 2] = l.x; lo8[h2 * 4 + i * 2 + 1] = l.y;
           }
         }
-        *reinterpret_cast<uint4*>(dq + e) = make_uint4(out[0], out[1], out[2], out[3]);
-        *reinterpret_cast<uint4*>(dq + e + 8) = make_uint4(out[4], out[5], out[6], out[7]);
+        *reinterpret_cast<uint4*>(dh + e) = make_uint4(hi8[0], hi8[1], hi8[2], hi8[3]);
+        *reinterpret_cast<uint4*>(dh + e + 8) = make_uint4(hi8[4], hi8[5], hi8[6], hi8[7]);
+        *reinterpret_cast<uint4*>(dl + e) = make_uint4(lo8[0], lo8[1], lo8[2], lo8[3]);
+        *reinterpret_cast<uint4*>(dl + e + 8) = make_uint4(lo8[4], lo8[5], lo8[6], lo8[7]);
       }
       fence_proxy_async_shared();
       named_bar(BAR_DEQ, kDeqThreads);
       if (t == 0) {
         mbar_arrive(&ms.wempty[rs]);
         mbar_arrive(&ms.dfull[ds]);
+        mbar_arrive(&ms.dfull[ds2]);
       }
     }
   }
@@ -458,6 +482,7 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
     my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
     const uint32_t idesc = idesc_f16(kTileM, c.Nc);
     const uint32_t abytes = uint32_t(kKs) * c.Nc * 2;
+    const bool q8g = slice_is_q8(p, G);
     // Readiness of the run's operand slices: one batch of relaxed loads and a
     // single acquire fence up front, instead of an acquire round trip per slice.
     const int ch_lo = beg < end ? beg / G.n_ks / G.n_mt : 0;
@@ -495,18 +520,26 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
       const bool first = s == beg || ks == 0;
       const bool last = s == end - 1 || ks == G.n_ks - 1;
       const uint32_t a = a_comp % kNAct, au = a_comp / kNAct;
-      const uint8_t* A;
-      uint64_t* wfree;
+      // the weight images of the slice: one f16 image, or (Q8_0) the pair
+      // hi, lo in two consecutive dequantised places, both multiplied into
+      // the same accumulator
+      const uint8_t* A[2];
+      uint64_t* wfree[2];
+      int nA = 1;
       if (tq8(p)) {
-        const uint32_t ds = wit % kNDeq;
-        if (!mwait(p, &ms.dfull[ds], (wit / kNDeq) & 1)) { ok = false; break; }
-        A = smem + kOffDeq + ds * kSlotBytes;
-        wfree = &ms.dempty[ds];
+        nA = q8g ? 2 : 1;
+        for (int i = 0; i < nA; ++i) {
+          const uint32_t ds = (wit + i) % kNDeq;
+          if (!mwait(p, &ms.dfull[ds], ((wit + i) / kNDeq) & 1)) { ok = false; break; }
+          A[i] = smem + kOffDeq + ds * kSlotBytes;
+          wfree[i] = &ms.dempty[ds];
+        }
+        if (!ok) break;
       } else {
         const uint32_t ws = wit % kNSlotF16;
         if (!mwait(p, &ms.wfull[ws], (wit / kNSlotF16) & 1)) { ok = false; break; }
-        A = smem + kOffRing + ws * kSlotBytes;
-        wfree = &ms.wempty[ws];
+        A[0] = smem + kOffRing + ws * kSlotBytes;
+        wfree[0] = &ms.wempty[ws];
       }
       ev_mma(p, evi, EV_WEIGHTS, gi);
       const uint32_t tb = seg & 1;
@@ -514,14 +547,17 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
       if (!mwait(p, &ms.afull[a], au & 1)) { ok = false; break; }
       ev_mma(p, evi, EV_LANDED, gi);
       tc_fence_after();
-      const uint32_t a0 = smem_u32(A), b0 = smem_u32(smem + kOffAct + a * kActBytes), d = ms.tmem_base + tb * 128;
+      const uint32_t b0 = smem_u32(smem + kOffAct + a * kActBytes), d = ms.tmem_base + tb * 128;
+      for (int i = 0; i < nA; ++i) {
+        const uint32_t a0 = smem_u32(A[i]);
 #pragma unroll
-      for (int j = 0; j < kKs / 16; ++j) {
-        const uint64_t ad = smem_desc(a0 + j * 2 * (kTileM / 8) * 128, (kTileM / 8) * 128, 128);
-        const uint64_t bd = smem_desc(b0 + j * 2 * (c.Nc / 8) * 128, (c.Nc / 8) * 128, 128);
-        mma_f16(d, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
+        for (int j = 0; j < kKs / 16; ++j) {
+          const uint64_t ad = smem_desc(a0 + j * 2 * (kTileM / 8) * 128, (kTileM / 8) * 128, 128);
+          const uint64_t bd = smem_desc(b0 + j * 2 * (c.Nc / 8) * 128, (c.Nc / 8) * 128, 128);
+          mma_f16(d, ad, bd, idesc, (first && i == 0 && j == 0) ? 0u : 1u);
+        }
       }
-      mma_commit(wfree);
+      for (int i = 0; i < nA; ++i) mma_commit(wfree[i]);
       mma_commit(&ms.aempty[a]);
       if (last) {
         mma_commit(&ms.accfull[tb]);
@@ -531,7 +567,7 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
         ev_mma(p, evi, EV_COMMIT, gi);
         ++seg;
       }
-      ++wit;
+      wit += nA;
       ++a_comp;
     }
   }
@@ -1234,6 +1270,10 @@ __global__ void __launch_bounds__(kThreads, 1) TILE_KERNEL(const PParams p) {
 // ----------------------------------------------------------------- host
 size_t al256(size_t b) { return (b + 255) & ~size_t(255); }
 
+// This build's dynamic shared memory (the two kernels' maps differ).
+constexpr size_t kernel_smem_bytes() { return kOffMisc + sizeof(Misc) + 1024; }
+static_assert(kernel_smem_bytes() <= 232448, "more shared memory than a CTA may have");
+
 struct SyncLayout {
   size_t tile_cnt, ready, ss_cnt, ss, head_done, codepk, decided, abort_flag, total;
   int NCH, MT, KS, NGEMM;
@@ -1323,7 +1363,7 @@ qp_status launch(qp_handle* h, PParams& p, uint8_t* scratch, const Scratch& L, u
   const qp_geometry& g = h->g;
   if (!*attr_done) {
     if (cudaFuncSetAttribute(TILE_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             int(persistent_smem_bytes())) != cudaSuccess) {
+                             int(kernel_smem_bytes())) != cudaSuccess) {
       cudaGetLastError();
       return QP_ERR_CUDA;
     }
@@ -1342,7 +1382,7 @@ qp_status launch(qp_handle* h, PParams& p, uint8_t* scratch, const Scratch& L, u
   }
   void* args[] = {&p};
   if (cudaLaunchCooperativeKernel(reinterpret_cast<void*>(TILE_KERNEL), dim3(h->num_sms), dim3(kThreads), args,
-                                  persistent_smem_bytes(), s) != cudaSuccess) {
+                                  kernel_smem_bytes(), s) != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;
   }
@@ -1368,7 +1408,7 @@ qp_status run_tile_q8(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Sc
 
 #else
 
-size_t persistent_smem_bytes() { return kOffMisc + sizeof(Misc) + 1024; }
+size_t persistent_smem_bytes() { return kernel_smem_bytes(); }
 
 Scratch scratch_layout(const qp_geometry& g, int bmax) {
   Scratch L{};
