@@ -79,6 +79,24 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
   return v;
 }
 
+// ------------------------------------------------------ f16 operand range
+// A GEMM operand row built from the residual stream (or from H) is
+// multiplied by 2^-e before its f16 conversion, and the GEMM's f32 result
+// by 2^e after it (both exact), so that rows of any magnitude stay inside
+// f16's range (65504).  e comes from the mean square ms of a reference row
+// known before the operand is built -- the row itself where it is complete,
+// else the same frame's most recent complete residual row: 2^-e brings that
+// row's RMS into [2^-5, 2^-4), or e = 0 (no scaling) when the RMS is below
+// 2^-5.  A row may grow far past its reference within one sublayer before
+// 2^-e * |x| * |w_norm| reaches 65504, and f16's relative precision does not
+// depend on the scale above its smallest normal value (2^-14).
+__device__ __forceinline__ int range_exp(float ms) {
+  const int E = int((__float_as_uint(ms) >> 23) & 255u) - 127;   // floor(log2(ms)) for ms >= 2^-126
+  const int e = (E >> 1) + 5;                                      // floor(log2(RMS)) + 5
+  return e < 0 ? 0 : (e > 100 ? 100 : e);
+}
+__device__ __forceinline__ float exp2i(int e) { return __uint_as_float(uint32_t(127 + e) << 23); }   // |e| <= 126
+
 __device__ __forceinline__ uint2 pack4_f16(float a, float b, float c, float d) {
   return make_uint2(uint32_t(f32_to_f16_bits(a)) | (uint32_t(f32_to_f16_bits(b)) << 16),
                     uint32_t(f32_to_f16_bits(c)) | (uint32_t(f32_to_f16_bits(d)) << 16));

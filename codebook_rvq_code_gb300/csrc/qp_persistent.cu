@@ -133,6 +133,7 @@ struct PParams {
   int Bmax;
   // per-call synchronisation (zeroed before the launch)
   unsigned* tile_cnt; unsigned* ready; unsigned* ss_cnt; float* ss; unsigned* head_done;
+  int* rexp;   // [gemm][row]: range exponent e of the operand row (f16(v * 2^-e); 0 = unscaled)
   unsigned long long* codepk; unsigned* decided; int* abort_flag; int* status;
   int NCH, MT, KS, NGEMM;
   unsigned long long* trace; int trace_n;
@@ -303,6 +304,7 @@ __device__ __forceinline__ unsigned* ready_cnt(const PParams& p, int gi, int ch,
 }
 __device__ __forceinline__ unsigned* ss_cnt(const PParams& p, int gi, int ch) { return p.ss_cnt + size_t(gi) * p.NCH + ch; }
 __device__ __forceinline__ float* ss_at(const PParams& p, int gi, int row) { return p.ss + size_t(gi) * 2 * p.B + row; }
+__device__ __forceinline__ int* rexp_at(const PParams& p, int gi, int row) { return p.rexp + size_t(gi) * 2 * p.B + row; }
 __device__ __forceinline__ unsigned* head_done(const PParams& p, int k, int ch) {
   return p.head_done + size_t(k - 1) * p.NCH + ch;
 }
@@ -589,17 +591,36 @@ __device__ bool prep1_items(const PParams& p) {
     const int b = r >> 1, ch = r / c.Nc;
     constexpr int kG = 8;   // loads in flight per lane before the stores
     if ((r & 1) == 0) {
+      // the row's range exponent from its mean square; the projection's
+      // output (and so layer 0's QKV operand of this row) takes the same
+      const float* hr = p.H + size_t(b) * p.th;
+      float ss = 0.f;
       for (int k0 = lane * 4; k0 < p.th; k0 += 128 * kG) {
         float4 hv[kG];
 #pragma unroll
         for (int i = 0; i < kG; ++i)
-          hv[i] = k0 + i * 128 < p.th ? __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k0 + i * 128))
+          hv[i] = k0 + i * 128 < p.th ? __ldg(reinterpret_cast<const float4*>(hr + k0 + i * 128))
+                                      : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < kG; ++i) ss += hv[i].x * hv[i].x + hv[i].y * hv[i].y + hv[i].z * hv[i].z + hv[i].w * hv[i].w;
+      }
+      const int e = range_exp(warp_sum(ss) / float(p.th));
+      const float sc = exp2i(-e);
+      if (lane == 0) {
+        *rexp_at(p, 0, r) = e;
+        *rexp_at(p, gi_of(p, 1, 0, 0), r) = e;
+      }
+      for (int k0 = lane * 4; k0 < p.th; k0 += 128 * kG) {
+        float4 hv[kG];
+#pragma unroll
+        for (int i = 0; i < kG; ++i)
+          hv[i] = k0 + i * 128 < p.th ? __ldg(reinterpret_cast<const float4*>(hr + k0 + i * 128))
                                       : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int i = 0; i < kG; ++i) {
           if (k0 + i * 128 >= p.th) break;
           *reinterpret_cast<uint2*>(p.a1[0] + act_off(r, k0 + i * 128, p.th, c)) =
-              pack4_f16(hv[i].x, hv[i].y, hv[i].z, hv[i].w);
+              pack4_f16(hv[i].x * sc, hv[i].y * sc, hv[i].z * sc, hv[i].w * sc);
         }
       }
     } else {
@@ -911,6 +932,15 @@ __device__ bool finish_rows(const PParams& p, Misc& ms, const GI& G, int gi, int
     const float4 wv = *reinterpret_cast<const float4*>(w + feat);
     const int P = G.k == 1 ? 2 : 1;
     const Ck ch_h = chunking(p.B);
+    // The range exponent of each row of the next operand: from the mean
+    // square of the row as it entered this GEMM's sublayer (the QKV input
+    // for O, the gate/up input for down), which is complete; for the
+    // projection, the one the step-1 input pass chose from H (0 for table
+    // rows).  Every tile of a row computes the same exponent; tile 0 records it.
+    auto row_exp = [&](int n) -> int {
+      if (KIND == G_PROJ) return G.k == 1 ? __ldcg(rexp_at(p, gi_n, n)) : 0;
+      return range_exp(__ldcg(ss_at(p, gi - 1, n)) / float(p.d));
+    };
     for (int r0 = lo + warp; r0 < hi; r0 += 8 * kConsumerWarps) {
       float4 xv[8];
 #pragma unroll
@@ -926,9 +956,14 @@ __device__ bool finish_rows(const PParams& p, Misc& ms, const GI& G, int gi, int
         const float4 x = xv[u];
         const float sq = warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w);
         const int nr = to_head ? n / P : n;
-        if (lane == 0) red_add_f32(ss_at(p, gi_n, nr), sq);
+        const int e = row_exp(n);
+        const float sc = exp2i(-e);
+        if (lane == 0) {
+          red_add_f32(ss_at(p, gi_n, nr), sq);
+          if (mt == 0 && KIND != G_PROJ) *rexp_at(p, gi_n, nr) = e;
+        }
         *reinterpret_cast<uint2*>(act_n + act_off(nr, feat, p.d, to_head ? ch_h : c)) =
-            pack4_f16(x.x * wv.x, x.y * wv.y, x.z * wv.z, x.w * wv.w);
+            pack4_f16(x.x * wv.x * sc, x.y * wv.y * sc, x.z * wv.z * sc, x.w * wv.w * sc);
       }
     }
     named_bar(BAR_CONS, kConsumers);
@@ -1041,13 +1076,16 @@ __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, ui
     // consumer-wide waits are taken by thread 0 and broadcast, so that every
     // consumer thread leaves (or stays) together.  The norm statistics of a
     // scaled GEMM are gathered first, while the MMAs may still run.
+    // Each row's factor: 1/RMS of the normalised input times 2^e, which
+    // undoes the operand's range scaling 2^-e.
     if (scaled) {
       if (t == 0) ms.flag[1] = poll_geq(p, ss_cnt(p, gi, ch), unsigned(rows * (p.d / kTileM)));
       named_bar(BAR_CONS, kConsumers);
       if (!ms.flag[1]) return false;
       for (int col = t; col < c.Nc; col += kConsumers) {
         const int n = ch * c.Nc + col;
-        ms.inv[col] = n < G.R ? rsqrtf(__ldcg(ss_at(p, gi, n)) / float(p.d) + p.eps) : 0.f;
+        ms.inv[col] = n < G.R ? rsqrtf(__ldcg(ss_at(p, gi, n)) / float(p.d) + p.eps) * exp2i(__ldcg(rexp_at(p, gi, n)))
+                              : 0.f;
       }
     }
     if (t == 0) ms.flag[1] = mwait(p, &ms.accfull[tb], (seg >> 1) & 1);
@@ -1072,8 +1110,11 @@ __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, ui
         const int f = pass * 4 + (lane >> 3), k4 = (lane & 7) * 4, n = ch * c.Nc + col + f;
         if (n < G.R) {
           float4 x = *reinterpret_cast<const float4*>(tp + f * 32 + k4);
-          if (scaled) {
-            const float s = ms.inv[col + f];
+          if (scaled || KIND == G_PROJ) {
+            // the projection's factor is read here, after the accumulator
+            // wait, which orders it after the step-1 input passes of every
+            // row of the chunk (they publish the rows' exponents)
+            const float s = scaled ? ms.inv[col + f] : (G.k == 1 ? exp2i(__ldcg(rexp_at(p, gi, n))) : 1.f);
             x.x *= s; x.y *= s; x.z *= s; x.w *= s;
           }
           red_add_v4_f32(G.acc + size_t(n) * G.ld + m0 + k4, x);
@@ -1275,7 +1316,7 @@ constexpr size_t kernel_smem_bytes() { return kOffMisc + sizeof(Misc) + 1024; }
 static_assert(kernel_smem_bytes() <= 232448, "more shared memory than a CTA may have");
 
 struct SyncLayout {
-  size_t tile_cnt, ready, ss_cnt, ss, head_done, codepk, decided, abort_flag, total;
+  size_t tile_cnt, ready, ss_cnt, ss, rexp, head_done, codepk, decided, abort_flag, total;
   int NCH, MT, KS, NGEMM;
 };
 
@@ -1300,6 +1341,7 @@ SyncLayout sync_layout(const qp_geometry& g, int B) {
   S.ready = o;    o += al256(size_t(S.NGEMM) * S.NCH * S.KS * 4);
   S.ss_cnt = o;   o += al256(size_t(S.NGEMM) * S.NCH * 4);
   S.ss = o;       o += al256(size_t(S.NGEMM) * R1 * 4);
+  S.rexp = o;     o += al256(size_t(S.NGEMM) * R1 * 4);
   S.head_done = o; o += al256(size_t(g.n_steps) * S.NCH * 4);
   S.codepk = o;   o += al256(size_t(g.n_steps) * B * 8);
   S.decided = o;  o += al256(size_t(g.n_steps) * B * 4);
@@ -1346,6 +1388,7 @@ void fill_params(PParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scra
   p.ready = reinterpret_cast<unsigned*>(sync + S.ready);
   p.ss_cnt = reinterpret_cast<unsigned*>(sync + S.ss_cnt);
   p.ss = reinterpret_cast<float*>(sync + S.ss);
+  p.rexp = reinterpret_cast<int*>(sync + S.rexp);
   p.head_done = reinterpret_cast<unsigned*>(sync + S.head_done);
   p.codepk = reinterpret_cast<unsigned long long*>(sync + S.codepk);
   p.decided = reinterpret_cast<unsigned*>(sync + S.decided);

@@ -127,6 +127,7 @@ struct SParams {
   unsigned* att;           // [step][layer]: attention items finished
   unsigned* prep;          // [step]: input rows finished
   unsigned* decided;       // [step][frame]: sampled code + 1
+  int* rexp;               // [gemm][row]: range exponent e of the operand row (f16(v * 2^-e); 0 = unscaled)
   int* abort_flag; int* status;
   int NGEMM, NHT;
   unsigned long long* trace; int trace_n;
@@ -260,6 +261,12 @@ template <int KIND>
 __device__ __forceinline__ bool sm_scaled(const SG& g) { return kScaled<KIND> || (KIND == S_HEAD && g.k == 1); }
 template <int KIND>
 constexpr bool kQkv = KIND == S_QKV || KIND == S_QKVU;
+// GEMMs whose operand rows come from the residual stream or from H: each
+// row is built as f16(v * 2^-e) and its partial products are multiplied by
+// 2^e as they are added (qp_device.cuh, range_exp).
+template <int KIND>
+constexpr bool kRange = KIND == S_PROJ || kQkv<KIND> || KIND == S_GU || KIND == S_HEAD;
+__device__ __forceinline__ int* sm_rexp(const SParams& p, int gi, int row) { return p.rexp + size_t(gi) * 2 * p.B + row; }
 
 // The operand ring of a GEMM: slots of N x 128 f16 (the GEMM's own width),
 // as many as fit the region.  A CTA's unit i of the GEMM uses slot i % n.
@@ -442,7 +449,7 @@ __device__ __forceinline__ uint4 pack8h(const float (&v)[8]) {
 // of a row, so global reads coalesce, and every unit's loads in one pass).
 // i0: the run index of unit u0 (its operand goes to slot (i0 + ui) % slots).
 template <int KIND>
-__device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, uint8_t* smem) {
+__device__ void sm_build(const SParams& p, const SG& g, int gi, int u0, int nu, int i0, uint8_t* smem) {
   const int n8 = g.N / 8, per = g.R * 16;
   const uint32_t nop = sm_op_slots(g), obytes = sm_op_bytes(g);
   for (int it = threadIdx.x; it < nu * per; it += kSmConsumers) {
@@ -450,6 +457,7 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
     const int n = rem >> 4, k8 = rem & 15, k = ((u0 + ui) % g.n_ks) * kKs + k8 * 8;
     uint16_t* dst = reinterpret_cast<uint16_t*>(smem + kSmOffOp + (uint32_t(i0 + ui) % nop) * obytes);
     uint4 h;
+    int rx = 0;   // the row's range exponent (H rows and residual rows), loaded alongside its values
     if (KIND == S_O) {
       h = __ldcg(reinterpret_cast<const uint4*>(p.a_o + size_t(n) * p.qw + k));
     } else {
@@ -469,6 +477,7 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
 #pragma unroll
           for (int i = 0; i < 4; ++i) { v[2 * i] = e16_to_f32(w[i], p.embed_f16); v[2 * i + 1] = e16_to_f32(w[i] >> 16, p.embed_f16); }
         } else if ((n & 1) == 0) {
+          rx = __ldcg(sm_rexp(p, gi, n));
           const float4 a = __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k));
           const float4 c = __ldg(reinterpret_cast<const float4*>(p.H + size_t(b) * p.th + k + 4));
           v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = c.x; v[5] = c.y; v[6] = c.z; v[7] = c.w;
@@ -490,7 +499,7 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
         // x * w_norm of an RMS-normalised input; the row scale is applied to
         // the GEMM's partial products instead
         const float* wn;
-        int row = n;
+        int row = n, gr = n;   // the residual row; the GEMM's row
         if (kQkv<KIND>) wn = p.layer[g.l].attn_norm;
         else if (KIND == S_GU) wn = p.layer[g.l].ffn_norm;
         else {   // head: each frame's last position
@@ -499,14 +508,21 @@ __device__ void sm_build(const SParams& p, const SG& g, int u0, int nu, int i0, 
           if (sm_grouped(p, g)) sm_rows(p, g, (u0 + ui) / g.n_ks, r0, R);
           if (n >= R) continue;   // rows past the tile's group: their outputs are not read
           row = g.k == 1 ? 2 * n + 1 : r0 + n;
+          gr = r0 + n;
         }
-        // both loads in flight together
+        // the loads in flight together
+        rx = __ldcg(sm_rexp(p, gi, gr));
         const float4 w0 = __ldg(reinterpret_cast<const float4*>(wn + k));
         const float4 w1 = __ldg(reinterpret_cast<const float4*>(wn + k + 4));
         ld8f(p.x + size_t(row) * p.d + k, v);
         const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] *= w[i];
+      }
+      if (kRange<KIND>) {
+        const float sc = exp2i(-rx);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] *= sc;
       }
       h = pack8h(v);
     }
@@ -554,8 +570,12 @@ __device__ __forceinline__ void sm_ssq(const SParams& p, const SG& g, SMisc& ms,
 // inv[n] = 1 / RMS of the GEMM's input row n, from the complete residual row
 // (all consumer threads; the warps' partial sums meet in shared memory).  The
 // caller's next barrier publishes ms.inv.
+// The factor also undoes the operand's range scaling (times 2^e).  The
+// gate/up GEMM's first CTA (record) writes the range exponent of each row
+// for the GEMM after down, the next layer's QKV or the step's head, whose
+// input row has grown from this one by the down projection only.
 template <int KIND>
-__device__ void sm_inv(const SParams& p, const SG& g, SMisc& ms) {
+__device__ void sm_inv(const SParams& p, const SG& g, int gi, SMisc& ms, bool record) {
   const int t = threadIdx.x;
   if (g.R <= 8) {
     sm_ssq<KIND, 8>(p, g, ms, 0);
@@ -567,7 +587,12 @@ __device__ void sm_inv(const SParams& p, const SG& g, SMisc& ms) {
     float ss = 0.f;
 #pragma unroll
     for (int w = 0; w < kSmConsumerWarps; ++w) ss += ms.ssp[w][t];
-    ms.inv[t] = rsqrtf(ss / float(p.d) + p.eps);
+    ms.inv[t] = rsqrtf(ss / float(p.d) + p.eps) * exp2i(__ldcg(sm_rexp(p, gi, t)));
+    if (KIND == S_GU && record) {
+      const int e = range_exp(ss / float(p.d));
+      if (g.l + 1 < p.L || g.k > 1 || sm_mode(p) == SM_STEP) *sm_rexp(p, gi + 2, t) = e;
+      else if (t & 1) *sm_rexp(p, gi + 2, t >> 1) = e;   // step 1's head reads rows 2b+1 as row b
+    }
   }
 }
 
@@ -603,8 +628,8 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
       const int f = pass * 4 + (lane >> 3), k4 = (lane & 7) * 4, n = col + f;
       if (n < R) {
         float4 x = *reinterpret_cast<const float4*>(tp + f * 32 + k4);
-        if (sm_scaled<KIND>(g)) {
-          const float s = ms.inv[n];
+        if (kRange<KIND> || sm_scaled<KIND>(g)) {
+          const float s = ms.inv[r0 + n];
           x.x *= s; x.y *= s; x.z *= s; x.w *= s;
         }
         red_add_v4_f32(g.out + size_t(r0 + n) * g.ld + m0 + k4, x);
@@ -674,7 +699,7 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
       }
       named_bar(SBAR_CONS, kSmConsumers);
       if (!ms.flag[3]) return false;
-      sm_build<KIND>(p, g, u, nu, u - beg, smem);
+      sm_build<KIND>(p, g, gi, u, nu, u - beg, smem);
       fence_proxy_async_shared();   // the tensor cores read what these generic stores wrote
       named_bar(SBAR_CONS, kSmConsumers);
       if (t == 0)
@@ -690,7 +715,14 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
   };
   auto scale = [&]() {
     if (sm_scaled<KIND>(g)) {
-      sm_inv<KIND>(p, g, ms);
+      sm_inv<KIND>(p, g, gi, ms, beg == 0);
+      named_bar(SBAR_CONS, kSmConsumers);
+    } else if (kRange<KIND>) {
+      // unscaled, but the operand rows carry range exponents (a grouped
+      // head's rows are every step group's, all of the call's rows)
+      const int nr = sm_grouped(p, g) ? p.B : g.R;
+      for (int n = t; n < nr; n += kSmConsumers)
+        ms.inv[n] = KIND != S_PROJ || g.k == 1 ? exp2i(__ldcg(sm_rexp(p, gi, n))) : 1.f;
       named_bar(SBAR_CONS, kSmConsumers);
     }
   };
@@ -736,7 +768,9 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
 // Step-1 setup, one warp per row r < 2B: the residual row starts at the
 // projection bias (the projection's partials are added to it); the row of
 // both q|k|v accumulators and the frame's logit row start at zero;
-// out-of-range first codes are reported.
+// out-of-range first codes are reported.  An H row's range exponent, from
+// its mean square, serves the projection's operand row and, as the
+// reference of the projection's output, layer 0's QKV operand row.
 __device__ bool sm_prep1(const SParams& p) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, G = gridDim.x;
   const int qkvw = p.qw + 2 * p.kvw;
@@ -753,6 +787,19 @@ __device__ bool sm_prep1(const SParams& p) {
     if ((r & 1) && lane == 0) {
       const int q = p.q0[r >> 1];
       if (q < 0 || q >= p.q0_vocab) set_status(p.status, QP_ERR_BAD_TOKEN);
+    }
+    if ((r & 1) == 0) {
+      const float* hr = p.H + size_t(r >> 1) * p.th;
+      float ss = 0.f;
+      for (int f = lane * 4; f < p.th; f += 128) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(hr + f));
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+      }
+      const int e = range_exp(warp_sum(ss) / float(p.th));
+      if (lane == 0) {
+        *sm_rexp(p, 0, r) = e;
+        *sm_rexp(p, sgi_of(p, 1, 0, 0), r) = e;
+      }
     }
     __syncwarp();
     if (lane == 0) red_release_add(sm_prep(p, 1), 1u);
@@ -1000,7 +1047,11 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh)
         qraw[hh] = hh < grp ? __ldcg(reinterpret_cast<const float4*>(row + (j * grp + hh) * kHeadDim + lane * 4)) : z4;
-      const float rs = rsqrtf(warp_sum(ss) / float(p.d) + p.eps);
+      const float ms_x = warp_sum(ss) / float(p.d);
+      const float rs = rsqrtf(ms_x + p.eps);
+      // this row's range exponent for the gate/up operand, whose input row
+      // grows from this one by the O projection only
+      if (j == 0 && lane == 0) *sm_rexp(p, sgi_of(p, k, l, 2), r) = range_exp(ms_x);
       kraw.x *= rs; kraw.y *= rs; kraw.z *= rs; kraw.w *= rs;
       vnew.x *= rs; vnew.y *= rs; vnew.z *= rs; vnew.w *= rs;
       uint2 kh[kMaxCtx], vh[kMaxCtx];
@@ -1228,7 +1279,7 @@ __global__ void __launch_bounds__(kSmThreads, 1) SM_KERNEL(const SParams p) {
 size_t sm_al256(size_t b) { return (b + 255) & ~size_t(255); }
 
 struct SmSync {
-  size_t done, qkv_tile, att, prep, decided, in_code, abort_flag, total;
+  size_t done, qkv_tile, att, prep, decided, in_code, rexp, abort_flag, total;
   int NGEMM, NHT;
 };
 
@@ -1250,6 +1301,7 @@ SmSync sm_sync_layout(const qp_geometry& g, int B, int mode = SM_RUN) {
   S.prep = o;       o += sm_al256(steps * 4);
   S.decided = o;    o += sm_al256(steps * B * 4);
   S.in_code = o;    o += sm_al256(steps * B * 4);
+  S.rexp = o;       o += sm_al256(size_t(S.NGEMM) * 2 * B * 4);
   S.abort_flag = o; o += 256;
   S.total = o;
   return S;
@@ -1293,6 +1345,7 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   p.prep = reinterpret_cast<unsigned*>(sync + S.prep);
   p.decided = reinterpret_cast<unsigned*>(sync + S.decided);
   p.in_code = reinterpret_cast<int32_t*>(sync + S.in_code);
+  p.rexp = reinterpret_cast<int*>(sync + S.rexp);
   p.proj_in = g.code_embed_dim != g.hidden;
   p.abort_flag = reinterpret_cast<int*>(sync + S.abort_flag);
   p.status = h->status;

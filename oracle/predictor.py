@@ -149,7 +149,10 @@ def rope(x: np.ndarray, pos: int, theta: float) -> np.ndarray:
 
 
 def silu(z: np.ndarray) -> np.ndarray:
-    return (z / (F32(1.0) + np.exp(-z))).astype(F32)
+    """z / (1 + e^-z); for very negative z, e^-z overflows to inf and the
+    quotient is the correct limit 0."""
+    with np.errstate(over="ignore"):
+        return (z / (F32(1.0) + np.exp(-z))).astype(F32)
 
 
 def attend(q: np.ndarray, K: np.ndarray, V: np.ndarray, n_kv_heads: int) -> np.ndarray:

@@ -151,7 +151,9 @@ def make_weights(g: Geometry = Geometry(), seed: int = 0, gemm_format: str = BF1
     * embeddings: N(0, std) -> bf16, or f16 with embed_format == 'f16' (the
       exporter's layout: f16 embeddings and heads over Q8_0 matrices);
     * bias: N(0, std) f32;  norm vectors: 1.0 ('ones') or 1 + N(0, 0.1)
-      ('perturbed', so that a dropped norm-weight multiply is visible).
+      ('perturbed', so that a dropped norm-weight multiply is visible), or
+      ('wide') the layers' attn_norm and ffn_norm log-uniform on [1, 30] and
+      the other norms 1 + N(0, 0.1): large residual-stream operands.
     Everything is drawn from one ``numpy.random.default_rng(seed)`` in the
     order of :func:`tensor_specs`.
     """
@@ -176,8 +178,12 @@ def make_weights(g: Geometry = Geometry(), seed: int = 0, gemm_format: str = BF1
         else:  # norm
             if norm_mode == "ones":
                 w = np.ones(shape, dtype=np.float32)
-            else:
+            elif norm_mode == "wide" and name.endswith(("attn_norm.weight", "ffn_norm.weight")):
+                w = np.exp(rng.uniform(0.0, np.log(30.0), size=shape)).astype(np.float32)
+            elif norm_mode in ("perturbed", "wide"):
                 w = (1.0 + 0.1 * rng.standard_normal(shape, dtype=np.float32)).astype(np.float32)
+            else:
+                raise ValueError(f"unknown norm_mode {norm_mode!r}")
             out[name] = RawTensor(name, F32, shape, w)
     return out
 
