@@ -26,7 +26,7 @@ EXPORTED = [
     "qp_abi_version", "qp_status_string", "qp_default_geometry", "qp_create", "qp_load_weights",
     "qp_predict_frames", "qp_predict_frames_ex", "qp_predict_frames_host", "qp_get_device_status",
     "qp_launches_per_call", "qp_destroy", "qp_predict_frames_static", "qp_code_embeddings",
-    "qp_set_engine", "qp_trace_enable", "qp_trace_read",   # include/qp_debug.h
+    "qp_set_engine", "qp_trace_enable", "qp_trace_read", "qp_debug_waits",   # include/qp_debug.h
     "qp_rvq_normalize", "qp_rvq_decode",                   # include/qp_rvq.h
     "qp_gguf_open", "qp_gguf_close", "qp_gguf_tensor_count", "qp_gguf_tensor_info",   # include/qp_gguf.h
     "qp_gguf_geometry", "qp_gguf_load_weights",
@@ -87,6 +87,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qp_destroy.argtypes = [vp]
     lib.qp_set_engine.restype = i32
     lib.qp_set_engine.argtypes = [vp, i32]
+    lib.qp_debug_waits.restype = i32
+    lib.qp_debug_waits.argtypes = [vp, i32, i32]
     lib.qp_trace_enable.restype = i32
     lib.qp_trace_enable.argtypes = [vp, i32]
     lib.qp_trace_read.restype = i32
@@ -366,6 +368,11 @@ class CodePredictor:
         """Schedule for later calls (include/qp_debug.h): "auto", "tile" or
         "small"."""
         _check("qp_set_engine", self._lib.qp_set_engine(self._h, self.ENGINES[engine]))
+
+    def debug_waits(self, wait_limit_us: int = 0, withhold_gemm: int = -1):
+        """Wait limit and withheld count of include/qp_debug.h (testing the
+        device-side failure path)."""
+        _check("qp_debug_waits", self._lib.qp_debug_waits(self._h, int(wait_limit_us), int(withhold_gemm)))
 
     def trace(self, enable: bool = True):
         """Turn the phase trace of include/qp_debug.h on or off."""

@@ -149,7 +149,8 @@ qp_status qp_create(const qp_geometry* gp, int max_batch, qp_handle** out) {
   h->g = g;
   h->max_batch = max_batch;
   h->device = dev;
-  if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+  if (cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->clock_khz, cudaDevAttrClockRate, dev) != cudaSuccess) {
     delete h;
     return QP_ERR_CUDA;
   }
@@ -475,6 +476,13 @@ qp_status qp_get_device_status(qp_handle* h, qp_stream sv) {
 int qp_launches_per_call(qp_handle* h, int B, int /*sampling*/) {
   if (!h || B < 1 || B > h->max_batch) return -1;
   return 1;   // one persistent kernel per call
+}
+
+qp_status qp_debug_waits(qp_handle* h, int wait_limit_us, int withhold_gemm) {
+  if (!h || wait_limit_us < 0 || withhold_gemm < -1) return QP_ERR_ARG;
+  h->wait_ticks = (long long)wait_limit_us * (h->clock_khz > 0 ? h->clock_khz : 2000000) / 1000;
+  h->withhold_gemm = withhold_gemm;
+  return QP_OK;
 }
 
 qp_status qp_set_engine(qp_handle* h, int engine) {

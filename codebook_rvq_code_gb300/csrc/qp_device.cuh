@@ -1,7 +1,8 @@
 // Device helpers shared by the frame-loop kernels: bounded waits that honour
 // a grid-wide abort flag, counter atomics with explicit memory order, f16
 // packing, and the per-warp RMSNorm + RoPE and score reduction of attention.
-// A params type passed to the waits has int* members abort_flag and status.
+// A params type passed to the waits has int* members abort_flag and status
+// and a long long spin_limit (clock64 ticks).
 #pragma once
 
 #include "qp_common.cuh"
@@ -32,7 +33,7 @@ __device__ bool poll_geq(const Par& p, const unsigned* ctr, unsigned want) {
     if (it > 2) __nanosleep(32);
     if ((it & 63) == 0) {
       if (aborted(p)) return false;
-      if (clock64() - t0 > kSpinLimit) { abort_all(p); return false; }
+      if (clock64() - t0 > p.spin_limit) { abort_all(p); return false; }
     }
   }
 }
@@ -46,7 +47,7 @@ __device__ bool mwait(const Par& p, uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 255) == 0) {
       if (aborted(p)) return false;
-      if (clock64() - t0 > kSpinLimit) { abort_all(p); return false; }
+      if (clock64() - t0 > p.spin_limit) { abort_all(p); return false; }
     }
   }
 }

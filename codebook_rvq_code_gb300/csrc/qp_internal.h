@@ -141,6 +141,9 @@ struct qp_handle {
   int trace_phases = 0;
 
   int engine = 0;                               // qp_engine (qp_debug.h)
+  long long wait_ticks = 0;                     // spin limit of the kernels' waits (0: the default)
+  int withhold_gemm = -1;                       // testing: one CTA skips its count of this GEMM
+  int clock_khz = 0;                            // the device's SM clock (kHz), for wait_ticks
 };
 
 namespace qp {

@@ -135,6 +135,8 @@ struct PParams {
   unsigned* tile_cnt; unsigned* ready; unsigned* ss_cnt; float* ss; unsigned* head_done;
   int* rexp;   // [gemm][row]: range exponent e of the operand row (f16(v * 2^-e); 0 = unscaled)
   unsigned long long* codepk; unsigned* decided; int* abort_flag; int* status;
+  long long spin_limit;   // clock64 ticks a wait may take before the call aborts
+  int withhold;           // testing (qp_debug.h): GEMM whose first tile count CTA run 0 skips; -1 none
   int NCH, MT, KS, NGEMM;
   unsigned long long* trace; int trace_n;
   // the call
@@ -1129,7 +1131,8 @@ __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, ui
     if (t == 0) {
       ev_cons(p, &ms.evc, EV_REDS, gi);
       // release: the bar.sync above orders every consumer thread's reductions first
-      red_release_add(tile_cnt(p, gi, ch, mt), unsigned(nsl));
+      // (a test of the failure path makes one count go missing)
+      if (!(gi == p.withhold && beg == 0 && s == beg)) red_release_add(tile_cnt(p, gi, ch, mt), unsigned(nsl));
       ev_cons(p, &ms.evc, EV_COUNTED, gi);
     }
     ++seg;
@@ -1394,6 +1397,8 @@ void fill_params(PParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scra
   p.decided = reinterpret_cast<unsigned*>(sync + S.decided);
   p.abort_flag = reinterpret_cast<int*>(sync + S.abort_flag);
   p.status = h->status;
+  p.spin_limit = h->wait_ticks > 0 ? h->wait_ticks : kSpinLimit;
+  p.withhold = h->withhold_gemm;
   p.NCH = S.NCH; p.MT = S.MT; p.KS = S.KS; p.NGEMM = S.NGEMM;
   p.trace = h->trace; p.trace_n = h->trace_phases;
   p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;

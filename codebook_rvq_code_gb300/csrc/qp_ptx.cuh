@@ -6,9 +6,11 @@
 
 namespace qp {
 
-// Spin limit for every wait inside the persistent kernel (clock64 ticks,
-// about one second at GB300 clocks).  A wait that runs out latches
-// QP_ERR_TIMEOUT and the kernel unwinds instead of hanging.
+// Default spin limit of every wait inside the persistent kernels (clock64
+// ticks, about one second at GB300 clocks); a call may set a shorter one
+// (include/qp_debug.h).  A wait that runs out latches QP_ERR_TIMEOUT and the
+// kernel unwinds instead of hanging.  The waits of the final drains (copies
+// and MMAs already in flight) always use this one.
 constexpr long long kSpinLimit = 2000000000LL;
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

@@ -129,6 +129,8 @@ struct SParams {
   unsigned* decided;       // [step][frame]: sampled code + 1
   int* rexp;               // [gemm][row]: range exponent e of the operand row (f16(v * 2^-e); 0 = unscaled)
   int* abort_flag; int* status;
+  long long spin_limit;    // clock64 ticks a wait may take before the call aborts
+  int withhold;            // testing (qp_debug.h): GEMM whose count CTA run 0 skips; -1 none
   int NGEMM, NHT;
   unsigned long long* trace; int trace_n;
   // the call
@@ -603,7 +605,7 @@ __device__ void sm_inv(const SParams& p, const SG& g, int gi, SMisc& ms, bool re
 // consecutive features per thread with one vector reduction.
 template <int KIND>
 __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g, int gi, int mt, int nsl,
-                         uint32_t& seg, bool publish) {
+                         uint32_t& seg, bool publish, bool publish_first = false) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const uint32_t tb = seg & 1;
   if (t == 0) ms.flag[1] = mwait(p, &ms.accfull[tb], (seg >> 1) & 1);
@@ -646,8 +648,10 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
     if (t == 0) {
       // release: the bar.sync above orders every consumer thread's reductions first
       fence_acq_rel_gpu();   // one fence releases the reductions for both counts
-      if (kQkv<KIND>) red_relaxed_add(sm_qkv_tile(p, g.k, g.l, mt), unsigned(nsl));
-      red_relaxed_add(sm_done(p, gi), unsigned(nsl));
+      if (gi != p.withhold || !publish_first) {   // a test of the failure path makes one count go missing
+        if (kQkv<KIND>) red_relaxed_add(sm_qkv_tile(p, g.k, g.l, mt), unsigned(nsl));
+        red_relaxed_add(sm_done(p, gi), unsigned(nsl));
+      }
       sm_ev(p, &ms.evc, SEV_PUBLISHED, gi);
     }
   }
@@ -739,6 +743,7 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
       // release: the bar.sync above orders every consumer thread's reductions
       // first, and one fence releases them for every count below
       fence_acq_rel_gpu();
+      if (gi == p.withhold && beg == 0) return true;   // a test of the failure path makes the counts go missing
       if (kQkv<KIND>)
         for (int s = beg; s < end;) {
           const int ks0 = s % g.n_ks, seg_end = min(end, s + (g.n_ks - ks0));
@@ -756,13 +761,13 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
     const int seg_end = min(end, s + (g.n_ks - ks0)), nsl = seg_end - s;
     if (!build(s, seg_end)) return false;
     if (si == 0) scale();
-    if (si > 0 && !sm_drain<KIND>(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true)) return false;
+    if (si > 0 && !sm_drain<KIND>(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true, si == 1 && beg == 0)) return false;
     prev_mt = mt;
     prev_nsl = nsl;
     ++si;
     s = seg_end;
   }
-  return sm_drain<KIND>(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true);
+  return sm_drain<KIND>(p, ms, smem, g, gi, prev_mt, prev_nsl, seg, true, si == 1 && beg == 0);
 }
 
 // Step-1 setup, one warp per row r < 2B: the residual row starts at the
@@ -1349,6 +1354,8 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   p.proj_in = g.code_embed_dim != g.hidden;
   p.abort_flag = reinterpret_cast<int*>(sync + S.abort_flag);
   p.status = h->status;
+  p.spin_limit = h->wait_ticks > 0 ? h->wait_ticks : kSpinLimit;
+  p.withhold = h->withhold_gemm;
   p.NGEMM = S.NGEMM; p.NHT = S.NHT;
   p.trace = h->trace; p.trace_n = h->trace_phases;
   p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;

@@ -27,9 +27,9 @@
  *   - qp_stream is a cudaStream_t passed as void*; NULL means the legacy
  *     default stream.
  *   - A call that returns anything but QP_OK enqueued nothing.
- *   - Errors the GPU detects (an out-of-range token, a stalled grid barrier)
- *     are latched in a device status word; qp_get_device_status reads and
- *     clears it.  Kernels never trap: a bad token is clamped for addressing
+ *   - Errors the GPU detects (an out-of-range token, a wait on another
+ *     CTA's work that ran out of time) are latched in a device status word;
+ *     qp_get_device_status reads and clears it.  Kernels never trap: a bad token is clamped for addressing
  *     and reported.
  *   - A handle may be used from one host thread at a time, and its calls
  *     share one scratch area (activations, KV cache, synchronisation
@@ -57,7 +57,7 @@ typedef enum qp_status {
   QP_ERR_WEIGHT_SHAPE = 4,   /* shape differs from the geometry              */
   QP_ERR_WEIGHT_DTYPE = 5,   /* storage type not accepted for that tensor    */
   QP_ERR_CUDA = 6,           /* a CUDA runtime call failed                   */
-  QP_ERR_TIMEOUT = 7,        /* device: a grid barrier gave up waiting       */
+  QP_ERR_TIMEOUT = 7,        /* device: a wait on another CTA's work ran out */
   QP_ERR_BAD_TOKEN = 8,      /* device: q0 or a forced code out of range     */
   QP_ERR_OOM = 9,            /* device allocation failed in create/load      */
   QP_ERR_UNKNOWN_WEIGHT = 10,/* a supplied name is not a predictor tensor    */

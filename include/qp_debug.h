@@ -41,6 +41,23 @@ typedef enum {
  * returns QP_ERR_ARG.  QP_ERR_ARG for a null handle or an unknown engine. */
 qp_status qp_set_engine(qp_handle* h, int engine);
 
+/* Testing aid for the device-side failure path.  Every wait inside the
+ * frame-loop kernels (on another CTA's counter, on a shared-memory barrier)
+ * is bounded; one that runs out latches QP_ERR_TIMEOUT in the status word
+ * and raises an abort flag that every other wait honours, so all CTAs
+ * unwind -- copies and MMAs in flight retire, TMEM is freed -- and the
+ * kernel returns.  Nothing traps.
+ *   wait_limit_us > 0: the limit of each wait in later calls on h, in
+ *     microseconds of SM clock; 0 restores the default (about one second).
+ *   withhold_gemm >= 0: in later frame-loop calls on h, the CTA whose share
+ *     of that GEMM of the program starts at its first unit leaves its first
+ *     completion count out, so the GEMM's consumers wait until the limit
+ *     runs out.  The program's GEMMs are numbered in order: 0 is step 1's
+ *     projection, then each step's GEMMs (4 per layer: QKV, O, gate/up,
+ *     down; then the head).  -1 (the default) turns it off.
+ * QP_ERR_ARG for a null handle, wait_limit_us < 0 or withhold_gemm < -1. */
+qp_status qp_debug_waits(qp_handle* h, int wait_limit_us, int withhold_gemm);
+
 /* Tracing is compiled in only when libqp is built with QP_TRACE=1 in the
  * environment (codebook_rvq_code_gb300/build.py): the hooks sit on the
  * loop's critical path.  Without them, enable != 0 returns QP_ERR_STATE.
