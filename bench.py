@@ -80,15 +80,42 @@ def work_of(g, B: int, gemm_format: str, sampling: bool):
     return weight_bytes + io, float(flops)
 
 
+def _strip_comments(text: str) -> str:
+    """C/C++ source without its comments (string and character literals are
+    kept as they are, so a '//' inside a literal is not taken for one)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        c = text[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and text[j] != c:
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        elif text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+            out.append(" ")
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def source_hash():
-    """Hash of the CUDA sources with comments and blank space removed, so that
-    a recorded traffic figure stays valid across comment-only edits."""
+    """Hash of what the kernels are built from: the CUDA sources and headers
+    with comments and blank space removed (so a recorded traffic figure stays
+    valid across comment-only edits) and the compiler's command-line flags."""
+    from codebook_rvq_code_gb300 import build as qb
     h = hashlib.sha256()
-    for f in sorted(glob.glob(os.path.join(ROOT, "codebook_rvq_code_gb300", "csrc", "*"))):
-        text = open(f, encoding="utf-8").read()
-        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
-        text = re.sub(r"//[^\n]*", " ", text)
-        h.update(" ".join(text.split()).encode())
+    for f in sorted(glob.glob(os.path.join(ROOT, "codebook_rvq_code_gb300", "csrc", "*"))
+                    + glob.glob(os.path.join(ROOT, "include", "*.h"))):
+        h.update(" ".join(_strip_comments(open(f, encoding="utf-8").read()).split()).encode())
+    h.update(" ".join(qb.ARCH + qb.NVCC_FLAGS).encode())
     return h.hexdigest()[:16]
 
 
@@ -164,6 +191,7 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 def oracle_threads():
+    """Threads the oracle's matrix products run on (numpy's BLAS pool)."""
     try:
         from threadpoolctl import threadpool_info
         n = [i.get("num_threads") for i in threadpool_info() if i.get("user_api") == "blas"]
@@ -172,6 +200,56 @@ def oracle_threads():
     except Exception:
         pass
     return os.cpu_count() or 1
+
+
+def cpu_model() -> str:
+    """The host CPU's model name, as the kernel reports it."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def host_cpu():
+    return {"cpu_model": cpu_model(), "host_cores": os.cpu_count() or 1}
+
+
+_SINGLE_THREAD = """
+import json, sys, time
+sys.path.insert(0, {root!r})
+import bench, synthetic as S
+g = S.Geometry()
+w = S.make_workload({cfg}, g)
+rate, done, el = bench.time_oracle(g, S.workload_weights(w, g), w, {frames}, {budget})
+print(json.dumps([rate, done, el]))
+"""
+
+
+def oracle_rate(g, raw, w, frames: int, budget_s: float, cfg=None, single_thread=False):
+    """frames/s of the oracle over the first `frames` frames of the workload
+    (one batch per pass, passes until about budget_s).  single_thread: in a
+    fresh process whose BLAS pool is held to one thread by the environment
+    (the pool size is fixed when numpy loads).  Returns (rate, frames done,
+    seconds, threads used)."""
+    if not single_thread:
+        rate, done, el = time_oracle(g, raw, w, frames, budget_s)
+        return rate, done, el, oracle_threads()
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
+    code = _SINGLE_THREAD.format(root=ROOT, cfg=cfg, frames=frames, budget=budget_s)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+    rate, done, el = json.loads(r.stdout.strip().splitlines()[-1])
+    return rate, done, el, 1
 
 
 def time_oracle(g, raw, w, frames: int, budget_s: float):
@@ -214,7 +292,8 @@ def reference_arm(args, g, raw, w):
     sec = sum(times)
     fps = frames * args.steps / sec
     cores = oracle_threads()
-    sample = f"first {frames} of the {w.B} frames of {w.name}, full 15-step loop, per step"
+    sample = (f"first {frames} of the {w.B} frames of {w.name}, full 15-step loop, per step; "
+              f"{cores} BLAS threads on {cpu_model()} ({os.cpu_count()} host cores)")
     return {
         "impl": "reference", "metric": METRIC, "value": fps, "unit": "frames/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sec / args.steps,
@@ -298,6 +377,34 @@ def sweep(g, dev, stream, steps, hbm, tf):
                        "us_per_step": 1e3 * ms / g.n_steps, "roofline_bound": roof["bound"],
                        "roofline_frac": roof["frac"], "device_status": st}
     return out
+
+
+def cpu_sweep(g, per_config):
+    """The oracle beside each configuration's GPU row: frames/s on a bounded
+    sample of that configuration (its first frames, at most 32 per pass, on
+    the BLAS pool's threads), and for configuration 1 also single-threaded
+    at B = 1, with the µs per step that gives."""
+    import synthetic as S
+    raw_cache = {}
+    for cfg in (1, 2, 3, 4, 5):
+        w = S.make_workload(cfg, g)
+        row = per_config.get(w.name)
+        if row is None:
+            continue
+        if w.gemm_format not in raw_cache:
+            raw_cache[w.gemm_format] = S.workload_weights(w, g)
+        raw = raw_cache[w.gemm_format]
+        frames = min(w.B, 32)
+        fps, done, el, used = oracle_rate(g, raw, w, frames, 4.0)
+        cb = {"value": fps, "unit": "frames/s", "cores": used, "kind": "oracle",
+              "sample": f"{done} frames ({frames} per pass) of {w.name} in {el:.1f} s"}
+        if cfg == 1:
+            fps1, done1, el1, used1 = oracle_rate(g, raw, w, 1, 4.0, cfg=1, single_thread=True)
+            cb["single_thread_B1"] = {"value": fps1, "unit": "frames/s", "cores": used1,
+                                      "us_per_step": 1e6 / fps1 / g.n_steps,
+                                      "sample": f"{done1} frames (1 per pass) in {el1:.1f} s"}
+        row["cpu_baseline"] = dict(cb, **host_cpu())
+        row["gpu_over_cpu"] = row["frames_per_s"] / fps
 
 
 def work_exporter(g, B: int):
@@ -596,14 +703,17 @@ def main():
             dist.destroy_process_group()
         return
 
+    # One call is one kernel launch of at most a few ms, timed on its own:
+    # the burst tensor-core peak is its ceiling (the sustained one is for
+    # kernels timed inside a seconds-long loop).
     hbm, tf_burst, tf_sust, peak_src = peaks()
     nbytes, flops = work_of(g, B, w.gemm_format, samp is not None)
     sec = ms_per_step / 1e3
-    t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tf_sust * 1e12)
+    t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tf_burst * 1e12)
     if t_hbm >= t_tc:
         roof = {"bound": "hbm", "achieved": nbytes / sec / 1e9, "peak": hbm, "unit": "GB/s"}
     else:
-        roof = {"bound": "tensor", "achieved": flops / sec / 1e12, "peak": tf_sust, "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": flops / sec / 1e12, "peak": tf_burst, "unit": "TFLOP/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["peak_source"] = f"{peak_src} (MEASURED_PEAKS.json)" if peak_src == "measured" else "fallback"
     roof["algorithmic_bytes_per_launch"] = nbytes
@@ -613,7 +723,10 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "frames/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16" if w.gemm_format == "bf16" else "q8_0",
+        "vs_baseline": None, "dtype": "f16",
+        "arithmetic": ("tensor-core operands f16 (bf16 weights converted exactly; Q8_0 weights as an exact f16 "
+                       "pair hi + lo), f32 accumulation; norms, softmax and decisions f32"),
+        "weights": w.gemm_format,
         "data": "synthetic",
         "config": config_of(g, w, world),
         "us_per_step": 1e3 * ms_per_step / g.n_steps,
@@ -624,14 +737,21 @@ def main():
     if e2e:
         line["e2e"] = e2e
     if not args.no_sweep and world == 1:
-        line["per_config"] = sweep(g, dev, stream, max(5, min(args.steps, 20)), hbm, tf_sust)
+        line["per_config"] = sweep(g, dev, stream, max(5, min(args.steps, 20)), hbm, tf_burst)
+        b1 = [v for v in line["per_config"].values() if v["B"] == 1]
+        if b1:
+            line["us_per_step_at_B1"] = b1[0]["us_per_step"]
         line["next_rows"] = rvq_rows(dev, stream, max(5, min(args.steps, 20)), hbm)
-        line["next_rows"].update(exporter_rows(dev, stream, max(5, min(args.steps, 20)), hbm, tf_sust))
+        line["next_rows"].update(exporter_rows(dev, stream, max(5, min(args.steps, 20)), hbm, tf_burst))
         line["next_rows"].update(sched_rows(dev, stream, max(5, min(args.steps, 20)), hbm))
     if not args.no_cpu_baseline:
-        fps, done, el = time_oracle(g, raw, w, min(B, 8), 10.0)
-        line["cpu_baseline"] = {"value": fps, "unit": "frames/s", "cores": oracle_threads(), "kind": "oracle",
-                                "sample": f"{done} frames ({min(B, 8)} per pass) of {w.name} in {el:.1f} s"}
+        frames = min(B, 32)
+        fps, done, el, used = oracle_rate(g, raw, w, frames, 10.0)
+        line["cpu_baseline"] = dict({"value": fps, "unit": "frames/s", "cores": used, "kind": "oracle",
+                                     "sample": f"{done} frames ({frames} per pass) of {w.name} in {el:.1f} s"},
+                                    **host_cpu())
+        if not args.no_sweep and world == 1:
+            cpu_sweep(g, line["per_config"])
     cp.close()
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -42,15 +42,20 @@ int scalar_size(uint32_t t) {
   }
 }
 
-// Bytes of a tensor's data, or 0 for a type not read here.
+// Bytes of a tensor's data, or 0 for a type not read here or a size that
+// does not fit in 64 bits (dimensions come from the file).
 uint64_t tensor_bytes(const Tensor& t) {
   if (t.dims.empty()) return 0;
+  constexpr uint64_t kMax = ~uint64_t(0);
   uint64_t n = 1;
-  for (uint64_t d : t.dims) n *= d;
+  for (uint64_t d : t.dims) {
+    if (d != 0 && n > kMax / d) return 0;
+    n *= d;
+  }
   switch (t.type) {
-    case kGgmlF32: return n * 4;
-    case kGgmlF16: case kGgmlBF16: return n * 2;
-    case kGgmlQ8_0: return t.dims[0] % 32 ? 0 : n / 32 * 34;
+    case kGgmlF32: return n > kMax / 4 ? 0 : n * 4;
+    case kGgmlF16: case kGgmlBF16: return n > kMax / 2 ? 0 : n * 2;
+    case kGgmlQ8_0: return t.dims[0] % 32 || n / 32 > kMax / 34 ? 0 : n / 32 * 34;
     default: return 0;
   }
 }
@@ -200,9 +205,12 @@ qp_status qp_gguf_open(const char* path, qp_gguf** out) {
     ok = ok && fseeko(fp, 0, SEEK_END) == 0;
     const off_t end = ok ? ftello(fp) : off_t(-1);
     ok = ok && end >= 0;
+    // (written so that no sum can wrap around)
+    const uint64_t room = ok && uint64_t(end) >= f->data_start ? uint64_t(end) - f->data_start : 0;
+    ok = ok && uint64_t(end) >= f->data_start;
     for (const Tensor& t : f->tensors) {
       const uint64_t b = tensor_bytes(t);
-      if (ok && b && (t.offset % alignment || f->data_start + t.offset + b > uint64_t(end))) ok = false;
+      if (ok && b && (t.offset % alignment || t.offset > room || b > room - t.offset)) ok = false;
     }
   }
   std::fclose(fp);

@@ -36,6 +36,8 @@
 // the one program order every CTA follows, so the earliest pending item can
 // always run: no deadlock.  Every wait is bounded; one that runs out latches
 // QP_ERR_TIMEOUT and sets an abort flag that every other wait honours.
+#include <atomic>
+
 #include "qp_device.cuh"
 #include "../../include/qp_debug.h"
 
@@ -1407,15 +1409,15 @@ void fill_params(PParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scra
 
 // Zero what must start at zero, then launch.
 qp_status launch(qp_handle* h, PParams& p, uint8_t* scratch, const Scratch& L, uint8_t* sync, const SyncLayout& S,
-                 cudaStream_t s, bool* attr_done) {
+                 cudaStream_t s, std::atomic<bool>* attr_done) {
   const qp_geometry& g = h->g;
-  if (!*attr_done) {
+  if (!attr_done->load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(TILE_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              int(kernel_smem_bytes())) != cudaSuccess) {
       cudaGetLastError();
       return QP_ERR_CUDA;
     }
-    *attr_done = true;
+    attr_done->store(true, std::memory_order_release);
   }
   const size_t B = size_t(p.B), qkvw = size_t(g.n_q_heads + 2 * g.n_kv_heads) * 128, F2 = size_t(2) * g.ffn;
   cudaError_t e = cudaMemsetAsync(sync, 0, S.total, s);
@@ -1437,7 +1439,10 @@ qp_status launch(qp_handle* h, PParams& p, uint8_t* scratch, const Scratch& L, u
   return QP_OK;
 }
 
-bool g_attr_done[64] = {};
+// Per device: the kernel's shared-memory limit has been set.  First calls
+// from several host threads may race to set it (an idempotent call); the
+// flag itself is atomic.
+std::atomic<bool> g_attr_done[64];
 
 }  // namespace
 
@@ -1449,8 +1454,8 @@ qp_status run_tile_q8(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Sc
   const SyncLayout S = sync_layout(h->g, a.B);
   PParams p{};
   fill_params(p, h, a, scratch, L, scratch + L.sync, S, bmax);
-  bool* done = h->device >= 0 && h->device < 64 ? &g_attr_done[h->device] : nullptr;
-  bool local = false;
+  std::atomic<bool>* done = h->device >= 0 && h->device < 64 ? &g_attr_done[h->device] : nullptr;
+  std::atomic<bool> local(false);
   return launch(h, p, scratch, L, scratch + L.sync, S, s, done ? done : &local);
 }
 
@@ -1492,8 +1497,8 @@ qp_status run_frames_persistent(qp_handle* h, const RunArgs& a, cudaStream_t s) 
   const SyncLayout S = sync_layout(h->g, a.B);
   PParams p{};
   fill_params(p, h, a, scratch, h->scr, scratch + h->scr.sync, S, h->max_batch);
-  bool* done = h->device >= 0 && h->device < 64 ? &g_attr_done[h->device] : nullptr;
-  bool local = false;
+  std::atomic<bool>* done = h->device >= 0 && h->device < 64 ? &g_attr_done[h->device] : nullptr;
+  std::atomic<bool> local(false);
   return launch(h, p, scratch, h->scr, scratch + h->scr.sync, S, s, done ? done : &local);
 }
 
@@ -1519,8 +1524,10 @@ static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBy
 
 namespace {
 constexpr int kMaxDevices = 64;
-void* g_static_ptr[kMaxDevices] = {};
-bool g_static_attr[kMaxDevices] = {};
+// Per device, looked up on the first call (atomic: first calls from several
+// host threads may race; each stores the same address).
+std::atomic<void*> g_static_ptr[kMaxDevices];
+std::atomic<bool> g_static_attr[kMaxDevices];
 }  // namespace
 
 qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s) {
@@ -1530,15 +1537,15 @@ qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   if (L.total > kStaticScratchBytes) return QP_ERR_ARG;
   if (h->device < 0 || h->device >= kMaxDevices) return QP_ERR_ARG;
   // once per device, with that device current: the array's device address
-  if (!g_static_ptr[h->device]) {
+  if (!g_static_ptr[h->device].load(std::memory_order_acquire)) {
     void* ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) {
       cudaGetLastError();
       return QP_ERR_CUDA;
     }
-    g_static_ptr[h->device] = ptr;
+    g_static_ptr[h->device].store(ptr, std::memory_order_release);
   }
-  uint8_t* base = static_cast<uint8_t*>(g_static_ptr[h->device]);
+  uint8_t* base = static_cast<uint8_t*>(g_static_ptr[h->device].load(std::memory_order_acquire));
   const SyncLayout S = sync_layout(g, a.B);
   RunArgs ga = a;
   ga.forced = nullptr;

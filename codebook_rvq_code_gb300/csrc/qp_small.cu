@@ -32,6 +32,7 @@
 // only on work earlier in that order, and all CTAs are co-resident
 // (cooperative launch).
 #include <algorithm>
+#include <atomic>
 
 #include "qp_device.cuh"
 
@@ -1364,19 +1365,21 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
 }
 
 constexpr int kSmMaxDevices = 64;
-bool g_sm_attr[kSmMaxDevices] = {};
+// Per device: the kernel's shared-memory limit has been set (atomic: first
+// calls from several host threads may race to set it, an idempotent call).
+std::atomic<bool> g_sm_attr[kSmMaxDevices];
 
 qp_status sm_launch(const qp_handle* h, const SParams& p, uint8_t* sync, size_t sync_bytes, cudaStream_t s) {
   const int dev = h->device;
-  bool local = false;
-  bool* attr = dev >= 0 && dev < kSmMaxDevices ? &g_sm_attr[dev] : &local;
+  std::atomic<bool> local(false);
+  std::atomic<bool>* attr = dev >= 0 && dev < kSmMaxDevices ? &g_sm_attr[dev] : &local;
   const size_t smem = kSmOffMisc + sizeof(SMisc) + 1024;
-  if (!*attr) {
+  if (!attr->load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(SM_KERNEL, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess) {
       cudaGetLastError();
       return QP_ERR_CUDA;
     }
-    *attr = true;
+    attr->store(true, std::memory_order_release);
   }
   if (cudaMemsetAsync(sync, 0, sync_bytes, s) != cudaSuccess) {
     cudaGetLastError();

@@ -4,8 +4,10 @@ It serves callers that cannot let the library call cudaMalloc for them (their
 own allocator holds the GPU's memory, or their audio path forbids allocation
 once running): the kernel's scratch sits in a static device array instead.
 This checks, through the C ABI, that two calls in a row give what
-qp_predict_frames gives on the same handle and inputs, within the tolerance
-the parity tests use, and that sizes beyond the array are refused.  The file
+qp_predict_frames gives on the same handle and inputs, and what the oracle
+gives, within the tolerance the parity tests use, on every engine and
+weight format the entry point serves, and that sizes beyond the array are
+refused.  The file
 is collected last so that a failure here never hides another test.
 """
 import ctypes
@@ -31,12 +33,33 @@ def qpk():
     return m
 
 
-@pytest.mark.parametrize("geometry,B", [(S.Geometry(), 1), (S.Geometry(), 8), (SMALL, 5)])
-def test_static_entry_matches_the_allocating_entry(qpk, geometry, B):
+def _free_prefix(ref):
+    """The oracle's codes and logits that a free-running call must give:
+    each frame up to its first near-tie (top-2 gap within the tolerance),
+    after which either choice is correct and the frame may follow it."""
+    dec = ref["decidable"]
+    n = dec.shape[1]
+    first = np.where(dec.all(axis=1), n, np.argmin(dec, axis=1))
+    steps = np.arange(n)[None, :]
+    return steps < first[:, None], steps <= first[:, None]
+
+
+# Every branch of the entry point: the small-batch engine (bf16, the
+# default up to 40 frames), the tile engine's 16-bit kernel (forced) and its
+# Q8_0 kernel (every Q8_0 handle), at 1, 5 and 8 frames.
+CASES = [("full", 1, "bf16", "auto"), ("full", 8, "bf16", "auto"), ("small", 5, "bf16", "auto"),
+         ("full", 1, "bf16", "tile"), ("full", 8, "bf16", "tile"), ("small", 5, "bf16", "tile"),
+         ("full", 1, "q8_0", "auto"), ("full", 5, "q8_0", "auto"), ("small", 8, "q8_0", "auto")]
+
+
+@pytest.mark.parametrize("geo,B,fmt,engine", CASES)
+def test_static_entry_matches_the_allocating_entry_and_the_oracle(qpk, geo, B, fmt, engine):
     import torch
-    raw = S.make_weights(geometry, seed=11, norm_mode="perturbed")
+    geometry = S.Geometry() if geo == "full" else SMALL
+    raw = S.make_weights(geometry, seed=11, norm_mode="perturbed", gemm_format=fmt)
     cp = qpk.CodePredictor(geometry, max_batch=B)
     cp.load_raw_weights(raw)
+    cp.set_engine(engine)
     H, q0 = S.toy_inputs(geometry, B, seed=3)
     tH = torch.from_numpy(H).cuda()
     tq = torch.from_numpy(q0.astype(np.int32)).cuda()
@@ -49,6 +72,8 @@ def test_static_entry_matches_the_allocating_entry(qpk, geometry, B):
     torch.cuda.synchronize()
     ref_l = ref_logits.cpu().numpy()
     ref_c = ref_codes.cpu().numpy()
+    orc = O.predict_frames(O.Predictor.from_raw(geometry, raw), H, q0, tol=TOL)
+    o_codes, o_logits = _free_prefix(orc)
     for _ in range(2):   # the array keeps the previous call's contents
         codes = torch.full((B, n), -1, dtype=torch.int32, device="cuda")
         logits = torch.full((B, n, V), float("nan"), dtype=torch.float32, device="cuda")
@@ -57,10 +82,15 @@ def test_static_entry_matches_the_allocating_entry(qpk, geometry, B):
         torch.cuda.synchronize()
         assert cp.device_status() == 0
         got_l = logits.cpu().numpy()
+        got_c = codes.cpu().numpy()
         assert np.all(np.isfinite(got_l))
+        # against the allocating entry on the same handle
         code_mask, logit_mask = decided_prefix(ref_l, got_l)   # near-ties may go either way
         assert np.abs(got_l - ref_l)[logit_mask].max() <= TOL
-        np.testing.assert_array_equal(codes.cpu().numpy()[code_mask], ref_c[code_mask])
+        np.testing.assert_array_equal(got_c[code_mask], ref_c[code_mask])
+        # against the oracle, free-running
+        assert np.abs(got_l - orc["logits"])[o_logits].max() <= TOL
+        np.testing.assert_array_equal(got_c[o_codes], orc["codes"][o_codes])
     cp.close()
 
 
