@@ -265,8 +265,11 @@ __device__ __forceinline__ bool sm_scaled(const SG& g) { return kScaled<KIND> ||
 template <int KIND>
 constexpr bool kQkv = KIND == S_QKV || KIND == S_QKVU;
 // GEMMs whose operand rows come from the residual stream or from H: each
-// row is built as f16(v * 2^-e) and its partial products are multiplied by
-// 2^e as they are added (qp_device.cuh, range_exp).
+// row is built as f16(v * 2^-e) (qp_device.cuh, range_exp), and 2^e is
+// applied with the row scale where that is applied: to the partial products
+// of the gate/up GEMM, step 1's head and step 1's projection as they are
+// added; by the attention items (QKV) and by the decision (the head from
+// step 2), which read the accumulated values.
 template <int KIND>
 constexpr bool kRange = KIND == S_PROJ || kQkv<KIND> || KIND == S_GU || KIND == S_HEAD;
 __device__ __forceinline__ int* sm_rexp(const SParams& p, int gi, int row) { return p.rexp + size_t(gi) * 2 * p.B + row; }
@@ -631,7 +634,7 @@ __device__ bool sm_drain(const SParams& p, SMisc& ms, uint8_t* smem, const SG& g
       const int f = pass * 4 + (lane >> 3), k4 = (lane & 7) * 4, n = col + f;
       if (n < R) {
         float4 x = *reinterpret_cast<const float4*>(tp + f * 32 + k4);
-        if (kRange<KIND> || sm_scaled<KIND>(g)) {
+        if (sm_scaled<KIND>(g) || (KIND == S_PROJ && g.k == 1)) {
           const float s = ms.inv[r0 + n];
           x.x *= s; x.y *= s; x.z *= s; x.w *= s;
         }
@@ -722,12 +725,9 @@ __device__ bool sm_gemm(const SParams& p, SMisc& ms, uint8_t* smem, int gi, uint
     if (sm_scaled<KIND>(g)) {
       sm_inv<KIND>(p, g, gi, ms, beg == 0);
       named_bar(SBAR_CONS, kSmConsumers);
-    } else if (kRange<KIND>) {
-      // unscaled, but the operand rows carry range exponents (a grouped
-      // head's rows are every step group's, all of the call's rows)
-      const int nr = sm_grouped(p, g) ? p.B : g.R;
-      for (int n = t; n < nr; n += kSmConsumers)
-        ms.inv[n] = KIND != S_PROJ || g.k == 1 ? exp2i(__ldcg(sm_rexp(p, gi, n))) : 1.f;
+    } else if (KIND == S_PROJ && g.k == 1) {
+      // unscaled, but the H rows carry range exponents
+      for (int n = t; n < g.R; n += kSmConsumers) ms.inv[n] = exp2i(__ldcg(sm_rexp(p, gi, n)));
       named_bar(SBAR_CONS, kSmConsumers);
     }
   };
@@ -866,7 +866,8 @@ __device__ int sm_code(const SParams& p, SMisc& ms, int step, int b) {
   if (ms.bcast < 0) return -1;
   float* row = p.logits + size_t(b) * p.V;
   float* dst = p.out_logits ? p.out_logits + (size_t(out_row) * sm_n_run(p) + out_step) * p.V : nullptr;
-  const float rs = dst && step > 1 ? sm_row_inv(p, ms, b) : 1.f;   // the head's input row
+  // the head's input row scale, and the range factor of its operand row
+  const float rs = dst && step > 1 ? sm_row_inv(p, ms, b) * exp2i(__ldcg(sm_rexp(p, gih, b))) : 1.f;
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   unsigned long long best = 0ull;
   for (int f0 = t * 4; f0 < p.V; f0 += 2 * 4 * kSmConsumers) {
@@ -1041,6 +1042,8 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
       float* kr = row + p.qw + j * kHeadDim + lane * 4;
       float* vr = row + p.qw + p.kvw + j * kHeadDim + lane * 4;
       // independent loads first: the input row, new k, v, the first two q heads, then the cache
+      // the QKV operand row's range exponent (its partials were added unscaled)
+      const int rx = __ldcg(sm_rexp(p, gi_q, r));
       float ss = 0.f;
 #pragma unroll 8
       for (int c = lane * 4; c < p.d; c += 128) {
@@ -1054,7 +1057,7 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
       for (int hh = 0; hh < 2; ++hh)
         qraw[hh] = hh < grp ? __ldcg(reinterpret_cast<const float4*>(row + (j * grp + hh) * kHeadDim + lane * 4)) : z4;
       const float ms_x = warp_sum(ss) / float(p.d);
-      const float rs = rsqrtf(ms_x + p.eps);
+      const float rs = rsqrtf(ms_x + p.eps) * exp2i(rx);
       // this row's range exponent for the gate/up operand, whose input row
       // grows from this one by the O projection only
       if (j == 0 && lane == 0) *sm_rexp(p, sgi_of(p, k, l, 2), r) = range_exp(ms_x);
@@ -1153,7 +1156,7 @@ __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
     named_bar(SBAR_CONS, kSmConsumers);
     if (!ms.flag[3]) return false;
     float* l = p.logits + size_t(b) * V;
-    const float rs = k > 1 ? sm_row_inv(p, ms, b) : 1.f;
+    const float rs = k > 1 ? sm_row_inv(p, ms, b) * exp2i(__ldcg(sm_rexp(p, sgi_head(p, k), b))) : 1.f;
     // the row's loads all in flight before the key stores (8 per thread at V = 2048)
     for (int i0 = t; i0 < V; i0 += 8 * kSmConsumers) {
       float lv[8];
