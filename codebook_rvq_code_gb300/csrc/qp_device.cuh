@@ -140,64 +140,22 @@ __device__ __forceinline__ float reduce_scatter32(float (&v)[32], int lane) {
 }
 
 // ------------------------------------------------------ top-k selection
-// The top_k-th largest of the order keys keys[0..V) in shared memory, by a
-// most-significant-digit radix select over four 8-bit digits (all NT
-// consumer threads of the CTA, which meet at named barrier `bar`; hist has
-// 256 entries, sel 2).  Returns that key; `remaining` says how many keys
-// equal to it belong to the top_k (the first ones in index order).  Each
-// digit is chosen by one warp: lane l holds the 8 bins 255-8l .. 248-8l, a
-// shuffle prefix sum gives every lane the count above its bins, and the lane
-// whose range reaches `remaining` picks the digit.
-template <int NT>
-__device__ uint32_t topk_kth_key(const uint32_t* keys, int V, int top_k, int* hist, int* sel, int bar,
-                                 int& remaining) {
-  const int t = threadIdx.x, lane = t & 31;
-  uint32_t prefix = 0, mask = 0;
-  remaining = top_k;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = t; i < 256; i += NT) hist[i] = 0;
-    named_bar(bar, NT);
-    for (int i = t; i < V; i += NT) {
-      const uint32_t kk = keys[i];
-      if ((kk & mask) == prefix) atomicAdd(&hist[(kk >> shift) & 255], 1);
-    }
-    named_bar(bar, NT);
-    if (t < 32) {
-      int c[8], s = 0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) { c[i] = hist[255 - 8 * lane - i]; s += c[i]; }
-      int incl = s;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int v = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      const int excl = incl - s;
-      if (excl < remaining && remaining <= incl) {   // exactly one lane
-        int cum = excl;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (cum + c[i] >= remaining) { sel[0] = 255 - 8 * lane - i; sel[1] = remaining - cum; break; }
-          cum += c[i];
-        }
-      }
-      if (lane == 31 && incl < remaining) { sel[0] = 0; sel[1] = remaining - incl; }   // not reached for top_k <= V
-    }
-    named_bar(bar, NT);
-    prefix |= uint32_t(sel[0]) << shift;
-    mask |= 255u << shift;
-    remaining = sel[1];
-    named_bar(bar, NT);   // sel and hist are rewritten by the next digit
-  }
-  return prefix;
-}
+// Shared memory one group of threads needs for one frame's decision.
+struct TopkScratch {
+  unsigned cnt[2][4];          // per round parity, warp: counts of the digits 1, 2, 3 (10 bits each), or of ties
+  int wtot[4];                 // per-warp totals of the tie scan
+  int last_tie;                // index of the last kept key equal to the threshold
+  unsigned long long red[4];   // per-warp (value, index) maxima
+  float rsum[4];               // per-warp partial sums (row scale)
+};
 
-// Exclusive prefix sum of v over the NT threads in thread order (CTA-wide;
-// wtot holds NT / 32 ints).  Ends with the barrier that publishes the warp
-// totals; the caller's next barrier must come before wtot is rewritten.
-template <int NT>
-__device__ int block_exclusive_scan(int v, int* wtot, int bar) {
-  const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+// Exclusive prefix sum of v over the NG threads of a group in thread order
+// (tg = thread index in the group; wtot holds NG / 32 ints; `bar` is the
+// group's named barrier).  Ends with the barrier that publishes the warp
+// totals; the group's next barrier must come before wtot is rewritten.
+template <int NG>
+__device__ int group_exclusive_scan(int v, int* wtot, int bar, int tg) {
+  const int lane = tg & 31, warp = tg >> 5;
   int incl = v;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -205,10 +163,127 @@ __device__ int block_exclusive_scan(int v, int* wtot, int bar) {
     if (lane >= o) incl += u;
   }
   if (lane == 31) wtot[warp] = incl;
-  named_bar(bar, NT);
+  named_bar(bar, NG);
   int off = 0;
   for (int w = 0; w < warp; ++w) off += wtot[w];
   return off + incl - v;
+}
+
+// The Gumbel top-k decision of one frame by a group of NG = 128 threads (tg
+// = the thread's index in the group, `bar` the group's named barrier): z =
+// logit * rs / T; the candidate set is the top_k largest z, ties at the
+// threshold kept lowest index first; the code is the argmax over the set of
+// z + g, lowest index on ties.  Every thread of the group returns it.  V is
+// a multiple of NG and at most 32 * NG; keys (shared memory, V words) is
+// read only when ties at the threshold must be ranked.
+//
+// The top_k-th largest order key comes from a bitwise radix select with no
+// atomics and no divergent branches: each thread holds its keys (indices tg
+// + NG u) in registers, and each of 16 rounds fixes two more bits of the
+// threshold from the counts of the keys sharing the bits fixed so far whose
+// next two bits are 1, 2 or 3 -- packed 10 bits apart into one word, summed
+// over the warp by one reduction, then one group barrier (the count buffers
+// alternate by round, so a round needs no second barrier).
+template <int NG>
+__device__ int gumbel_topk_group(const float* l, float rs, float T, const float* gb, int V, int top_k,
+                                 uint32_t* keys, TopkScratch& sc, int bar, int tg) {
+  static_assert(NG == 128, "four warps per group");
+  constexpr int KPT = 32;   // keys per thread at most (V <= 4096)
+  const int lane = tg & 31, w = tg >> 5, kpt = V / NG;
+  uint32_t key[KPT];
+#pragma unroll
+  for (int u0 = 0; u0 < KPT; u0 += 8) {   // eight loads in flight at a time
+    float lv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) lv[u] = u0 + u < kpt ? __ldcg(l + tg + (u0 + u) * NG) : 0.f;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) key[u0 + u] = u0 + u < kpt ? f32_order_key(lv[u] * rs / T) : 0u;
+  }
+  uint32_t prefix = 0;
+  int rem = top_k, par = 0;
+  for (int shift = 30; shift >= 0; shift -= 2, par ^= 1) {
+    const uint32_t hmask = shift == 30 ? 0u : (0xFFFFFFFFu << (shift + 2));
+    unsigned packed = 0;   // digit d >= 1 counts at bits 10 (d - 1): a warp's count is at most 1024 - 1
+#pragma unroll
+    for (int u = 0; u < KPT; ++u) {
+      if (u >= kpt) break;   // warp-uniform
+      const uint32_t kk = key[u], d = (kk >> shift) & 3u;
+      const unsigned one = (kk & hmask) == prefix && d != 0u ? 1u : 0u;
+      packed += one << (10u * (d - 1u) & 31u);
+    }
+    packed = __reduce_add_sync(0xffffffffu, packed);
+    if (lane == 0) sc.cnt[par][w] = packed;
+    named_bar(bar, NG);
+    int s1 = 0, s2 = 0, s3 = 0;
+#pragma unroll
+    for (int i = 0; i < NG / 32; ++i) {
+      const unsigned c = sc.cnt[par][i];
+      s1 += int(c & 1023u); s2 += int((c >> 10) & 1023u); s3 += int(c >> 20);
+    }
+    uint32_t d;
+    if (s3 >= rem) d = 3u;
+    else if (s3 + s2 >= rem) { d = 2u; rem -= s3; }
+    else if (s3 + s2 + s1 >= rem) { d = 1u; rem -= s3 + s2; }
+    else { d = 0u; rem -= s3 + s2 + s1; }
+    prefix |= d << shift;
+  }
+  const uint32_t kth = prefix;   // the top_k-th largest key; rem of the keys equal to it are kept
+  unsigned eq = 0;
+#pragma unroll
+  for (int u = 0; u < KPT; ++u) {
+    if (u >= kpt) break;
+    eq += key[u] == kth ? 1u : 0u;
+  }
+  eq = __reduce_add_sync(0xffffffffu, eq);
+  if (lane == 0) sc.cnt[par][w] = eq;
+  named_bar(bar, NG);
+  int equal = 0;
+#pragma unroll
+  for (int i = 0; i < NG / 32; ++i) equal += int(sc.cnt[par][i]);
+  int last_tie = V;
+  if (rem < equal) {   // not every key equal to the threshold is kept: the rem lowest indices are
+#pragma unroll
+    for (int u = 0; u < KPT; ++u)
+      if (u < kpt) keys[tg + u * NG] = key[u];
+    named_bar(bar, NG);
+    const int lo = tg * kpt;
+    int cnt = 0;
+    for (int i = lo; i < lo + kpt; ++i) cnt += keys[i] == kth;
+    int rank = group_exclusive_scan<NG>(cnt, sc.wtot, bar, tg);
+    if (rank < rem && rem <= rank + cnt)
+      for (int i = lo; i < lo + kpt; ++i)
+        if (keys[i] == kth && ++rank == rem) { sc.last_tie = i; break; }
+    named_bar(bar, NG);
+    last_tie = sc.last_tie;
+  }
+  // the kept keys' logits and noise: predicated loads, all in flight together
+  unsigned long long best = 0ull;
+#pragma unroll
+  for (int u0 = 0; u0 < KPT; u0 += 16) {
+    if (u0 >= kpt) break;
+    float lz[16], gz[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = tg + (u0 + u) * NG;
+      const bool in = u0 + u < kpt && (key[u0 + u] > kth || (key[u0 + u] == kth && i <= last_tie));
+      lz[u] = in ? __ldcg(l + i) : 0.f;
+      gz[u] = in ? __ldg(gb + i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int i = tg + (u0 + u) * NG;
+      const bool in = u0 + u < kpt && (key[u0 + u] > kth || (key[u0 + u] == kth && i <= last_tie));
+      const unsigned long long pk = in ? pack_argmax(lz[u] * rs / T + gz[u], i) : 0ull;
+      best = pk > best ? pk : best;
+    }
+  }
+  best = warp_max_u64(best);
+  if (lane == 0) sc.red[w] = best;
+  named_bar(bar, NG);
+  unsigned long long v = sc.red[0];
+#pragma unroll
+  for (int i = 1; i < NG / 32; ++i) v = sc.red[i] > v ? sc.red[i] : v;
+  return unpack_argmax_index(v);
 }
 
 // Sixteen warp-wide sums: lane l ends with the total over all 32 lanes of

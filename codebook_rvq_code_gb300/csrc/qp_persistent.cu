@@ -88,7 +88,7 @@ static_assert(kNDeq >= 2, "a Q8_0 slice takes two dequantised places");
 static_assert(kOffDeq % 1024 == 0 && kOffAct % 1024 == 0, "operand images start on 1 KB boundaries");
 static_assert(kNSlotF16 * kSlotBytes <= kOffAct, "f16 slots overlap the operand slots");
 
-enum { BAR_CONS = 1, BAR_DEQ = 2 };
+enum { BAR_CONS = 1, BAR_DEQ = 2, BAR_HALF0 = 3 };   // BAR_HALF0 + h: consumer half h (4 warps)
 enum { G_PROJ = 0, G_QKV, G_O, G_GU, G_DOWN, G_HEAD };
 
 struct Misc {
@@ -106,6 +106,8 @@ struct Misc {
   unsigned long long redu[8];
   int sel[2];
   int hist[256];
+  TopkScratch topk[2];   // sampling: one frame per consumer half
+  int hflag[2];
   float inv[kMaxNc];
 };
 
@@ -157,7 +159,8 @@ enum {
   EV_READY = 1, EV_LANDED, EV_COMMIT,            // MMA warp, per slice / segment
   EV_ACC = 4, EV_REDS, EV_COUNTED, EV_LASTDONE,   // consumer epilogue, per segment
   EV_ATT_READY = 8, EV_ATT_DONE,                  // attention warp, per item
-  EV_WEIGHTS = 10                                 // MMA warp: the slice's weights are in shared memory
+  EV_WEIGHTS = 10,                                // MMA warp: the slice's weights are in shared memory
+  EV_DEC_READY = 11, EV_DEC_DONE = 12             // sampling: a frame's logits complete; its code published
 };
 __device__ __forceinline__ unsigned long long* ev_base(const PParams& p) {
   return p.trace ? p.trace + size_t(p.trace_n) * gridDim.x * 2 + size_t(blockIdx.x) * 16384 : nullptr;
@@ -1173,54 +1176,32 @@ __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, ui
   return true;
 }
 
-// Gumbel top-k decisions of step k, one frame per CTA pass (all consumers).
+// Gumbel top-k decisions of step k: each half of the consumer warps (4
+// warps) decides one frame, so a CTA takes two frames at a time (one, by
+// half 0, when the vocabulary is too large for two key arrays).
 __device__ bool decide_items(const PParams& p, Misc& ms, uint32_t* keys, int k) {
-  const int V = p.V, t = threadIdx.x, lane = t & 31, w = t >> 5, G = gridDim.x;
+  constexpr int NG = kConsumers / 2;
+  const int V = p.V, t = threadIdx.x, G = gridDim.x, half = t / NG, tg = t - half * NG;
+  const bool two = 2 * V <= kMaxVocab;
   const Ck c = chunking(p.B);
-  const float T = p.temperature;
-  for (int b = (blockIdx.x + k * 7) % G; b < p.B; b += G) {
-    if (t == 0) ms.flag[3] = poll_geq(p, head_done(p, k, b / c.Nc), unsigned(V / kTileM));
-    named_bar(BAR_CONS, kConsumers);
-    if (!ms.flag[3]) return false;
+  const int bar = BAR_HALF0 + half;
+  for (int b0 = (blockIdx.x + k * 7) % G; b0 < p.B; b0 += two ? 2 * G : G) {
+    const int b = b0 + (two ? half * G : 0);
+    if (b >= p.B || (!two && half == 1)) continue;   // warp-uniform: the half sits this frame out
+    if (tg == 0) ms.hflag[half] = poll_geq(p, head_done(p, k, b / c.Nc), unsigned(V / kTileM));
+    named_bar(bar, NG);
+    if (!ms.hflag[half]) return false;
+    if (tg == 0) ev_cons(p, &ms.evc, EV_DEC_READY, gi_head(p, k));
     float* l = p.logits + size_t(b) * V;
-    // the row's loads all in flight before the key stores (8 per thread at V = 2048)
-    for (int i0 = t; i0 < V; i0 += 8 * kConsumers) {
-      float lv[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) lv[u] = i0 + u * kConsumers < V ? __ldcg(l + i0 + u * kConsumers) : 0.f;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (i0 + u * kConsumers < V) keys[i0 + u * kConsumers] = f32_order_key(lv[u] / T);
-    }
-    int remaining;
-    const uint32_t kth = topk_kth_key<kConsumers>(keys, V, p.top_k, ms.hist, ms.sel, BAR_CONS, remaining);
-    const int per = (V + kConsumers - 1) / kConsumers, lo = t * per, hi = min(V, lo + per);
-    int cnt = 0;
-    for (int i = lo; i < hi; ++i) cnt += keys[i] == kth;
-    // keys equal to the threshold are kept lowest index first: this thread's
-    // first one has rank (number of equal keys in earlier threads' chunks)
-    int eq_rank = block_exclusive_scan<kConsumers>(cnt, ms.hist, BAR_CONS);
     const float* gb = p.gumbel + (size_t(b) * p.n_steps + (k - 1)) * V;
-    unsigned long long best = 0ull;
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t kk = keys[i];
-      bool in = kk > kth;
-      if (kk == kth) { in = eq_rank < remaining; ++eq_rank; }
-      if (in) {
-        const unsigned long long pk = pack_argmax(__ldcg(l + i) / T + gb[i], i);
-        best = pk > best ? pk : best;
-      }
-    }
-    best = warp_max_u64(best);
-    if (lane == 0) ms.redu[w] = best;
-    named_bar(BAR_CONS, kConsumers);
-    for (int i = t; i < V; i += kConsumers) l[i] = 0.f;   // the buffer is reused next step
-    named_bar(BAR_CONS, kConsumers);
-    if (t == 0) {
-      unsigned long long v = ms.redu[0];
-      for (int i = 1; i < kConsumerWarps; ++i) v = ms.redu[i] > v ? ms.redu[i] : v;
+    const int code = gumbel_topk_group<NG>(l, 1.f, p.temperature, gb, V, p.top_k, keys + (two ? half * V : 0),
+                                           ms.topk[half], bar, tg);
+    for (int i = tg; i < V; i += NG) l[i] = 0.f;   // the buffer is reused next step
+    named_bar(bar, NG);
+    if (tg == 0) {
       __threadfence();
-      atomicExch(p.decided + size_t(k - 1) * p.B + b, unsigned(unpack_argmax_index(v) + 1));
+      atomicExch(p.decided + size_t(k - 1) * p.B + b, unsigned(code + 1));
+      ev_cons(p, &ms.evc, EV_DEC_DONE, gi_head(p, k));
     }
   }
   return true;

@@ -56,7 +56,7 @@ constexpr uint32_t kSmOffKeys = kSmOffOp + kSmOpBytes;   // top-k keys, or the d
 constexpr uint32_t kSmOffMisc = kSmOffKeys + kMaxVocab * 4;
 constexpr uint32_t kSmTmemCols = 256;                // two accumulators of up to 128 columns
 
-enum { SBAR_CONS = 1 };
+enum { SBAR_CONS = 1, SBAR_HALF0 = 2 };   // SBAR_HALF0 + h: consumer half h (4 warps)
 enum { S_PROJ = 0, S_QKV, S_O, S_GU, S_DOWN, S_HEAD };
 // The QKV projection without the row scale (a code path of the S_QKV GEMM):
 // each attention item scales its frame's q, k and v itself, so the GEMM
@@ -93,6 +93,8 @@ struct SMisc {
   unsigned long long redu[kSmConsumerWarps];
   int sel[2];
   int hist[256];
+  TopkScratch topk[2];   // sampling: one frame per consumer half
+  int hflag[2];
   float inv[kMaxNc];
   float ssp[kSmConsumerWarps][kMaxNc];   // per-warp partial sums of squares
   int bcast;
@@ -1142,65 +1144,55 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
   return true;
 }
 
-// Gumbel top-k decisions of step k, one frame per CTA pass (all consumers):
-// the row's logits are the accumulated ones, times the head input row's
-// scale from step 2 on; radix select of the k-th largest logit / T, then the argmax of
-// logit / T + g over the kept set (ties at the threshold kept lowest index
-// first).  The logit row is copied out if asked and zeroed for the next step.
+// Gumbel top-k decisions of step k: each half of the consumer warps (4
+// warps) decides one frame, so a CTA takes two frames at a time (one, by
+// half 0, when the vocabulary is too large for two key arrays).  The row's
+// logits are the accumulated ones, times the head input row's scale (and
+// its operand's range factor) from step 2 on.  The logit row is copied out
+// if asked and zeroed for the next step.
 __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
-  const int V = p.V, t = threadIdx.x, lane = t & 31, w = t >> 5, G = gridDim.x;
-  const float T = p.temperature;
-  const SG h = sgemm(p, sgi_head(p, k));
-  for (int b = (blockIdx.x + k * 7) % G; b < p.B; b += G) {
-    if (t == 0) ms.flag[3] = poll_geq(p, sm_done(p, sgi_head(p, k)), unsigned(h.n_mt * h.n_ks));
-    named_bar(SBAR_CONS, kSmConsumers);
-    if (!ms.flag[3]) return false;
+  constexpr int NG = kSmConsumers / 2;
+  const int V = p.V, t = threadIdx.x, G = gridDim.x, half = t / NG, tg = t - half * NG;
+  const int lane = tg & 31, w = tg >> 5;
+  const bool two = 2 * V <= kMaxVocab;
+  const int bar = SBAR_HALF0 + half, gih = sgi_head(p, k);
+  const SG h = sgemm(p, gih);
+  TopkScratch& sc = ms.topk[half];
+  for (int b0 = (blockIdx.x + k * 7) % G; b0 < p.B; b0 += two ? 2 * G : G) {
+    const int b = b0 + (two ? half * G : 0);
+    if (b >= p.B || (!two && half == 1)) continue;   // warp-uniform: the half sits this frame out
+    if (tg == 0) ms.hflag[half] = poll_geq(p, sm_done(p, gih), unsigned(h.n_mt * h.n_ks));
+    named_bar(bar, NG);
+    if (!ms.hflag[half]) return false;
     float* l = p.logits + size_t(b) * V;
-    const float rs = k > 1 ? sm_row_inv(p, ms, b) * exp2i(__ldcg(sm_rexp(p, sgi_head(p, k), b))) : 1.f;
-    // the row's loads all in flight before the key stores (8 per thread at V = 2048)
-    for (int i0 = t; i0 < V; i0 += 8 * kSmConsumers) {
-      float lv[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) lv[u] = i0 + u * kSmConsumers < V ? __ldcg(l + i0 + u * kSmConsumers) : 0.f;
-#pragma unroll
-      for (int u = 0; u < 8; ++u)
-        if (i0 + u * kSmConsumers < V) keys[i0 + u * kSmConsumers] = f32_order_key(lv[u] * rs / T);
-    }
-    int remaining;
-    const uint32_t kth = topk_kth_key<kSmConsumers>(keys, V, p.top_k, ms.hist, ms.sel, SBAR_CONS, remaining);
-    const int per = (V + kSmConsumers - 1) / kSmConsumers, lo = t * per, hi = min(V, lo + per);
-    int cnt = 0;
-    for (int i = lo; i < hi; ++i) cnt += keys[i] == kth;
-    // keys equal to the threshold are kept lowest index first: this thread's
-    // first one has rank (number of equal keys in earlier threads' chunks)
-    int eq_rank = block_exclusive_scan<kSmConsumers>(cnt, ms.hist, SBAR_CONS);
-    const float* gb = p.gumbel + (size_t(b) * p.n_steps + (k - 1)) * V;
-    unsigned long long best = 0ull;
-    for (int i = lo; i < hi; ++i) {
-      const uint32_t kk = keys[i];
-      bool in = kk > kth;
-      if (kk == kth) { in = eq_rank < remaining; ++eq_rank; }
-      if (in) {
-        const unsigned long long pk = pack_argmax(__ldcg(l + i) * rs / T + gb[i], i);
-        best = pk > best ? pk : best;
+    float rs = 1.f;
+    if (k > 1) {   // 1/RMS of the head's input row, by this half
+      float ss = 0.f;
+      for (int c = tg * 4; c < p.d; c += 4 * NG) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.x + size_t(b) * p.d + c));
+        ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
       }
+      ss = warp_sum(ss);
+      if (lane == 0) sc.rsum[w] = ss;
+      named_bar(bar, NG);
+      float tot = 0.f;
+#pragma unroll
+      for (int i = 0; i < NG / 32; ++i) tot += sc.rsum[i];
+      rs = rsqrtf(tot / float(p.d) + p.eps) * exp2i(__ldcg(sm_rexp(p, gih, b)));
     }
-    best = warp_max_u64(best);
-    if (lane == 0) ms.redu[w] = best;
-    named_bar(SBAR_CONS, kSmConsumers);
+    const float* gb = p.gumbel + (size_t(b) * p.n_steps + (k - 1)) * V;
+    const int code = gumbel_topk_group<NG>(l, rs, p.temperature, gb, V, p.top_k, keys + (two ? half * V : 0), sc,
+                                           bar, tg);
     float* dst = p.out_logits ? p.out_logits + (size_t(b) * p.n_steps + (k - 1)) * V : nullptr;
-    for (int i = t; i < V; i += kSmConsumers) {
+    for (int i = tg; i < V; i += NG) {
       if (dst) dst[i] = __ldcg(l + i) * rs;
       l[i] = 0.f;
     }
-    named_bar(SBAR_CONS, kSmConsumers);
-    if (t == 0) {
-      unsigned long long v = ms.redu[0];
-      for (int i = 1; i < kSmConsumerWarps; ++i) v = ms.redu[i] > v ? ms.redu[i] : v;
+    named_bar(bar, NG);
+    if (tg == 0) {
       __threadfence();
-      atomicExch(p.decided + size_t(k - 1) * p.B + b, unsigned(unpack_argmax_index(v) + 1));
+      atomicExch(p.decided + size_t(k - 1) * p.B + b, unsigned(code + 1));
     }
-    named_bar(SBAR_CONS, kSmConsumers);   // keys and ms.redu are reused by the next frame
   }
   return true;
 }
