@@ -416,7 +416,6 @@ __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
         bool w = mwait(p, &ms.wfull[rs], ru & 1);
         if (w && !q8g) w = mwait(p, &ms.wfull[rs2], ru2 & 1);
         if (w && du > 0) w = mwait(p, &ms.dempty[ds], (du - 1) & 1);
-        if (w && q8g && du2 > 0) w = mwait(p, &ms.dempty[ds2], (du2 - 1) & 1);
         ms.deq_ok = w;
       }
       named_bar(BAR_DEQ, kDeqThreads);
@@ -440,37 +439,42 @@ __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
       const uint8_t* src = smem + kOffRing + rs * kQ8SlotBytes;
       const int8_t* qv = reinterpret_cast<const int8_t*>(src);
       const __half* sc = reinterpret_cast<const __half*>(src + kQ8Bytes);
-      uint16_t* dh = reinterpret_cast<uint16_t*>(smem + kOffDeq + ds * kSlotBytes);
-      uint16_t* dl = reinterpret_cast<uint16_t*>(smem + kOffDeq + ds2 * kSlotBytes);
-      for (int e = t * 16; e < kTileM * kKs; e += kDeqThreads * 16) {
-        // e walks [k8][m8][8 rows][8 k]; 16 values are two rows of one core matrix
-        const uint4 raw = *reinterpret_cast<const uint4*>(qv + e);
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t hi8[8], lo8[8];
-#pragma unroll
-        for (int h2 = 0; h2 < 2; ++h2) {
-          const int ee = e + h2 * 8;
-          const int k8 = ee >> 10, m = ((ee >> 6) & 15) * 8 + ((ee >> 3) & 7);
-          const __half2 d2 = __half2half2(sc[(k8 >> 2) * kTileM + m]);
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            uint2 h, l;
-            q8x4_to_f16x4_hilo(w4[h2 * 2 + i], d2, h, l);
-            hi8[h2 * 4 + i * 2] = h.x; hi8[h2 * 4 + i * 2 + 1] = h.y;
-            lo8[h2 * 4 + i * 2] = l.x; lo8[h2 * 4 + i * 2 + 1] = l.y;
-          }
+      // two passes, hi then lo, each published on its own: the MMA warp
+      // multiplies the hi image while the lo image is written
+      for (int pass = 0; pass < 2; ++pass) {
+        if (pass == 1) {
+          if (t == 0) ms.deq_ok = du2 == 0 || mwait(p, &ms.dempty[ds2], (du2 - 1) & 1);
+          named_bar(BAR_DEQ, kDeqThreads);
+          if (!ms.deq_ok) return;
         }
-        *reinterpret_cast<uint4*>(dh + e) = make_uint4(hi8[0], hi8[1], hi8[2], hi8[3]);
-        *reinterpret_cast<uint4*>(dh + e + 8) = make_uint4(hi8[4], hi8[5], hi8[6], hi8[7]);
-        *reinterpret_cast<uint4*>(dl + e) = make_uint4(lo8[0], lo8[1], lo8[2], lo8[3]);
-        *reinterpret_cast<uint4*>(dl + e + 8) = make_uint4(lo8[4], lo8[5], lo8[6], lo8[7]);
-      }
-      fence_proxy_async_shared();
-      named_bar(BAR_DEQ, kDeqThreads);
-      if (t == 0) {
-        mbar_arrive(&ms.wempty[rs]);
-        mbar_arrive(&ms.dfull[ds]);
-        mbar_arrive(&ms.dfull[ds2]);
+        uint16_t* dq = reinterpret_cast<uint16_t*>(smem + kOffDeq + (pass ? ds2 : ds) * kSlotBytes);
+        for (int e = t * 16; e < kTileM * kKs; e += kDeqThreads * 16) {
+          // e walks [k8][m8][8 rows][8 k]; 16 values are two rows of one core matrix
+          const uint4 raw = *reinterpret_cast<const uint4*>(qv + e);
+          const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+          uint32_t o8[8];
+#pragma unroll
+          for (int h2 = 0; h2 < 2; ++h2) {
+            const int ee = e + h2 * 8;
+            const int k8 = ee >> 10, m = ((ee >> 6) & 15) * 8 + ((ee >> 3) & 7);
+            const __half2 d2 = __half2half2(sc[(k8 >> 2) * kTileM + m]);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+              uint2 h, l;
+              q8x4_to_f16x4_hilo(w4[h2 * 2 + i], d2, h, l);
+              const uint2 v = pass ? l : h;
+              o8[h2 * 4 + i * 2] = v.x; o8[h2 * 4 + i * 2 + 1] = v.y;
+            }
+          }
+          *reinterpret_cast<uint4*>(dq + e) = make_uint4(o8[0], o8[1], o8[2], o8[3]);
+          *reinterpret_cast<uint4*>(dq + e + 8) = make_uint4(o8[4], o8[5], o8[6], o8[7]);
+        }
+        fence_proxy_async_shared();
+        named_bar(BAR_DEQ, kDeqThreads);
+        if (t == 0) {
+          if (pass == 1) mbar_arrive(&ms.wempty[rs]);
+          mbar_arrive(&ms.dfull[pass ? ds2 : ds]);
+        }
       }
     }
   }
@@ -536,14 +540,15 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
       uint64_t* wfree[2];
       int nA = 1;
       if (tq8(p)) {
+        // the first image now; a Q8_0 slice's lo image is waited for after
+        // the hi image's MMAs are issued
         nA = q8g ? 2 : 1;
         for (int i = 0; i < nA; ++i) {
           const uint32_t ds = (wit + i) % kNDeq;
-          if (!mwait(p, &ms.dfull[ds], ((wit + i) / kNDeq) & 1)) { ok = false; break; }
           A[i] = smem + kOffDeq + ds * kSlotBytes;
           wfree[i] = &ms.dempty[ds];
         }
-        if (!ok) break;
+        if (!mwait(p, &ms.dfull[wit % kNDeq], (wit / kNDeq) & 1)) { ok = false; break; }
       } else {
         const uint32_t ws = wit % kNSlotF16;
         if (!mwait(p, &ms.wfull[ws], (wit / kNSlotF16) & 1)) { ok = false; break; }
@@ -558,6 +563,10 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
       tc_fence_after();
       const uint32_t b0 = smem_u32(smem + kOffAct + a * kActBytes), d = ms.tmem_base + tb * 128;
       for (int i = 0; i < nA; ++i) {
+        if (i > 0) {
+          if (!mwait(p, &ms.dfull[(wit + i) % kNDeq], ((wit + i) / kNDeq) & 1)) { ok = false; break; }
+          tc_fence_after();
+        }
         const uint32_t a0 = smem_u32(A[i]);
 #pragma unroll
         for (int j = 0; j < kKs / 16; ++j) {
@@ -565,8 +574,9 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
           const uint64_t bd = smem_desc(b0 + j * 2 * (c.Nc / 8) * 128, (c.Nc / 8) * 128, 128);
           mma_f16(d, ad, bd, idesc, (first && i == 0 && j == 0) ? 0u : 1u);
         }
+        mma_commit(wfree[i]);   // the image's place is free once these MMAs complete
       }
-      for (int i = 0; i < nA; ++i) mma_commit(wfree[i]);
+      if (!ok) break;
       mma_commit(&ms.aempty[a]);
       if (last) {
         mma_commit(&ms.accfull[tb]);
