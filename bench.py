@@ -407,6 +407,49 @@ def cpu_sweep(g, per_config):
         row["gpu_over_cpu"] = row["frames_per_s"] / fps
 
 
+def deterministic_rows(g, dev, stream, steps, per_config):
+    """What the deterministic mode (include/qp.h, qp_set_deterministic)
+    costs: configurations 1, 2 and 4 timed again with it on, beside their
+    ordinary rows."""
+    import torch
+    import synthetic as S
+    import codebook_rvq_code_gb300 as qpk
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    raw = None
+    out = {}
+    for cfg in (1, 2, 4):
+        w = S.make_workload(cfg, g)
+        raw = raw or S.workload_weights(w, g)
+        cp = qpk.CodePredictor(g, max_batch=w.B)
+        cp.load_raw_weights(raw, device=dev)
+        cp.set_deterministic(True)
+        H = torch.from_numpy(w.H).to(dev)
+        q0 = torch.from_numpy(w.q0).to(dev)
+        samp = None if w.gumbel is None else (w.temperature, w.top_k, torch.from_numpy(w.gumbel).to(dev))
+        codes = torch.empty((w.B, g.n_steps), dtype=torch.int32, device=dev)
+        for _ in range(3):
+            cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream)
+        torch.cuda.synchronize()
+        tot = 0.0
+        for i in range(steps):
+            flush.fill_(float(i))
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream)
+            b.record(stream)
+            torch.cuda.synchronize()
+            tot += a.elapsed_time(b)
+        ms = tot / steps
+        base = per_config.get(w.name, {}).get("ms_per_call")
+        out[f"deterministic_{w.name}"] = {"ms_per_call": ms, "us_per_step": 1e3 * ms / g.n_steps,
+                                          "frames_per_s": w.B / (ms / 1e3), "ordinary_ms_per_call": base,
+                                          "cost": (ms / base - 1.0) if base else None,
+                                          "device_status": cp.device_status()}
+        cp.close()
+    return out
+
+
 def work_exporter(g, B: int):
     """(bytes, flops) of one call in the exporter's model layout: Talker-wide
     code tables projected at every step, Q8_0 projection and layer matrices
@@ -744,6 +787,7 @@ def main():
         line["next_rows"] = rvq_rows(dev, stream, max(5, min(args.steps, 20)), hbm)
         line["next_rows"].update(exporter_rows(dev, stream, max(5, min(args.steps, 20)), hbm, tf_burst))
         line["next_rows"].update(sched_rows(dev, stream, max(5, min(args.steps, 20)), hbm))
+        line["next_rows"].update(deterministic_rows(g, dev, stream, max(5, min(args.steps, 20)), line["per_config"]))
     if not args.no_cpu_baseline:
         frames = min(B, 32)
         fps, done, el, used = oracle_rate(g, raw, w, frames, 10.0)

@@ -26,6 +26,7 @@ EXPORTED = [
     "qp_abi_version", "qp_status_string", "qp_default_geometry", "qp_create", "qp_load_weights",
     "qp_predict_frames", "qp_predict_frames_ex", "qp_predict_frames_host", "qp_get_device_status",
     "qp_launches_per_call", "qp_destroy", "qp_predict_frames_static", "qp_code_embeddings",
+    "qp_set_deterministic",
     "qp_set_engine", "qp_trace_enable", "qp_trace_read", "qp_debug_waits",   # include/qp_debug.h
     "qp_rvq_normalize", "qp_rvq_decode",                   # include/qp_rvq.h
     "qp_gguf_open", "qp_gguf_close", "qp_gguf_tensor_count", "qp_gguf_tensor_info",   # include/qp_gguf.h
@@ -87,6 +88,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qp_destroy.argtypes = [vp]
     lib.qp_set_engine.restype = i32
     lib.qp_set_engine.argtypes = [vp, i32]
+    lib.qp_set_deterministic.restype = i32
+    lib.qp_set_deterministic.argtypes = [vp, i32]
     lib.qp_debug_waits.restype = i32
     lib.qp_debug_waits.argtypes = [vp, i32, i32]
     lib.qp_trace_enable.restype = i32
@@ -368,6 +371,10 @@ class CodePredictor:
         """Schedule for later calls (include/qp_debug.h): "auto", "tile" or
         "small"."""
         _check("qp_set_engine", self._lib.qp_set_engine(self._h, self.ENGINES[engine]))
+
+    def set_deterministic(self, on: bool = True):
+        """Bit-identical results run to run (include/qp.h, qp_set_deterministic)."""
+        _check("qp_set_deterministic", self._lib.qp_set_deterministic(self._h, int(bool(on))))
 
     def debug_waits(self, wait_limit_us: int = 0, withhold_gemm: int = -1):
         """Wait limit and withheld count of include/qp_debug.h (testing the

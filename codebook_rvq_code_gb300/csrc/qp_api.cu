@@ -98,6 +98,10 @@ size_t matrix_bytes(int fmt, int64_t N, int64_t K) {
 
 // The engine that serves a call (qp_debug.h, qp_engine).
 qp_status run(qp_handle* h, const qp::RunArgs& a, cudaStream_t s) {
+  if (h->deterministic) {   // the tile engine's deterministic schedule
+    if (h->engine == QP_ENGINE_SMALL) return QP_ERR_ARG;
+    return qp::run_frames_persistent(h, a, s);
+  }
   const bool sm = qp::small_supported(h, a);
   if (h->engine == QP_ENGINE_SMALL && !sm) return QP_ERR_ARG;
   const bool pick = h->engine == QP_ENGINE_SMALL || (h->engine == QP_ENGINE_AUTO && a.B <= qp::kSmallAutoFrames);
@@ -476,6 +480,12 @@ qp_status qp_get_device_status(qp_handle* h, qp_stream sv) {
 int qp_launches_per_call(qp_handle* h, int B, int /*sampling*/) {
   if (!h || B < 1 || B > h->max_batch) return -1;
   return 1;   // one persistent kernel per call
+}
+
+qp_status qp_set_deterministic(qp_handle* h, int on) {
+  if (!h) return QP_ERR_ARG;
+  h->deterministic = on != 0;
+  return QP_OK;
 }
 
 qp_status qp_debug_waits(qp_handle* h, int wait_limit_us, int withhold_gemm) {

@@ -143,6 +143,7 @@ struct qp_handle {
   int engine = 0;                               // qp_engine (qp_debug.h)
   long long wait_ticks = 0;                     // spin limit of the kernels' waits (0: the default)
   int withhold_gemm = -1;                       // testing: one CTA skips its count of this GEMM
+  bool deterministic = false;                   // qp_set_deterministic (tile engine, fixed-order sums)
   int clock_khz = 0;                            // the device's SM clock (kHz), for wait_ticks
 };
 

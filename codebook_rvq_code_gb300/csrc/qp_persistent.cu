@@ -140,6 +140,8 @@ struct PParams {
   int* rexp;   // [gemm][row]: range exponent e of the operand row (f16(v * 2^-e); 0 = unscaled)
   unsigned long long* codepk; unsigned* decided; int* abort_flag; int* status;
   long long spin_limit;   // clock64 ticks a wait may take before the call aborts
+  int det;                // deterministic mode: no split K; squared norms summed in tile order
+  float* ss_part;         // deterministic mode: [gemm][x tile][row] partial sums of squares
   int withhold;           // testing (qp_debug.h): GEMM whose first tile count CTA run 0 skips; -1 none
   int NCH, MT, KS, NGEMM;
   unsigned long long* trace; int trace_n;
@@ -272,9 +274,12 @@ __device__ GI gemm_inst(const PParams& p, int gi) {
 // tile's partial sums pass through the f32 accumulator as few times as the
 // grid allows.  This CTA takes a contiguous run of pieces -- a contiguous
 // run [beg, end) of slices -- rotated with the GEMM index.
-__device__ __forceinline__ void my_run(int tiles, int n_ks, int gi, int& beg, int& end) {
+__device__ __forceinline__ int split_of(int tiles, int n_ks, int det) {
+  return det ? 1 : max(1, min(n_ks, int(gridDim.x) / tiles));
+}
+__device__ __forceinline__ void my_run(int tiles, int n_ks, int gi, int& beg, int& end, int det) {
   const int G = gridDim.x, g = (blockIdx.x + gi * 37) % G;
-  const int S = max(1, min(n_ks, G / tiles));
+  const int S = split_of(tiles, n_ks, det);
   const long long P = (long long)tiles * S;
   const int p0 = int(P * g / G), p1 = int(P * (g + 1) / G);
   beg = (p0 / S) * n_ks + ((p0 % S) * n_ks) / S;
@@ -287,9 +292,9 @@ __device__ __forceinline__ void my_run(int tiles, int n_ks, int gi, int& beg, in
 // With fewer parts than CTAs each CTA holds at most one part, and the S
 // owners need not be consecutive; otherwise every CTA holds a part and the
 // owners are consecutive in the rotated CTA index.
-__device__ __forceinline__ int tile_share(int tiles, int n_ks, int gi, int tt, int& n) {
+__device__ __forceinline__ int tile_share(int tiles, int n_ks, int gi, int tt, int& n, int det) {
   const int G = gridDim.x, g = (blockIdx.x + gi * 37) % G;
-  const int S = max(1, min(n_ks, G / tiles));
+  const int S = split_of(tiles, n_ks, det);
   const long long P = (long long)tiles * S, q0 = (long long)tt * S;
   if (P < G) {
     const long long p0 = P * g / G, p1 = P * (g + 1) / G;
@@ -312,6 +317,18 @@ __device__ __forceinline__ unsigned* ready_cnt(const PParams& p, int gi, int ch,
 __device__ __forceinline__ unsigned* ss_cnt(const PParams& p, int gi, int ch) { return p.ss_cnt + size_t(gi) * p.NCH + ch; }
 __device__ __forceinline__ float* ss_at(const PParams& p, int gi, int row) { return p.ss + size_t(gi) * 2 * p.B + row; }
 __device__ __forceinline__ int* rexp_at(const PParams& p, int gi, int row) { return p.rexp + size_t(gi) * 2 * p.B + row; }
+// Deterministic mode: the partial sum of squares of x tile mt of a row.
+__device__ __forceinline__ float* ss_part_at(const PParams& p, int gi, int mt, int row) {
+  return p.ss_part + (size_t(gi) * (p.d / kTileM) + mt) * 2 * p.B + row;
+}
+// A row's sum of squares (complete): the accumulated word, or in
+// deterministic mode the tiles' partial sums added in tile order.
+__device__ __forceinline__ float ss_total(const PParams& p, int gi, int row) {
+  if (!p.det) return __ldcg(ss_at(p, gi, row));
+  float s = 0.f;
+  for (int mt = 0; mt < p.d / kTileM; ++mt) s += __ldcg(ss_part_at(p, gi, mt, row));
+  return s;
+}
 __device__ __forceinline__ unsigned* head_done(const PParams& p, int k, int ch) {
   return p.head_done + size_t(k - 1) * p.NCH + ch;
 }
@@ -336,7 +353,7 @@ __device__ void producer_role(const PParams& p, Misc& ms, uint8_t* smem) {
     const Ck c = chunking(G.R);
     const bool q8g = slice_is_q8(p, G);
     int beg, end;
-    my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
+    my_run(c.n * G.n_mt, G.n_ks, gi, beg, end, p.det);
     for (int s = beg; s < end; ++s) {
       const int ks = s % G.n_ks, mt = (s / G.n_ks) % G.n_mt;
       if (tq8(p) && !q8g) {
@@ -407,7 +424,7 @@ __device__ void dequant_role(const PParams& p, Misc& ms, uint8_t* smem) {
     const Ck c = chunking(G.R);
     const bool q8g = slice_is_q8(p, G);
     int beg, end;
-    my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
+    my_run(c.n * G.n_mt, G.n_ks, gi, beg, end, p.det);
     for (int s = beg; s < end; ++s, it += q8g ? 2 : 1, rit += q8g ? 1 : 2) {
       const uint32_t rs = rit % kNSlotQ8, ru = rit / kNSlotQ8;
       const uint32_t rs2 = (rit + 1) % kNSlotQ8, ru2 = (rit + 1) / kNSlotQ8;
@@ -492,7 +509,7 @@ __device__ void mma_role(const PParams& p, Misc& ms, uint8_t* smem) {
     const GI G = gemm_inst(p, gi);
     const Ck c = chunking(G.R);
     int beg, end;
-    my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
+    my_run(c.n * G.n_mt, G.n_ks, gi, beg, end, p.det);
     const uint32_t idesc = idesc_f16(kTileM, c.Nc);
     const uint32_t abytes = uint32_t(kKs) * c.Nc * 2;
     const bool q8g = slice_is_q8(p, G);
@@ -766,7 +783,13 @@ __device__ bool prepk_items(const PParams& p, int k) {
             pack4_f16(v0 * w.x, v1 * w.y, v2 * w.z, v3 * w.w);
       }
     }
-    if (lane == 0) *ss_at(p, gi, b) = p.embed_ss[k - 2][nc];
+    if (lane == 0) {
+      if (!p.det) {
+        *ss_at(p, gi, b) = p.embed_ss[k - 2][nc];
+      } else {
+        for (int mt = 0; mt < p.d / kTileM; ++mt) *ss_part_at(p, gi, mt, b) = mt == 0 ? p.embed_ss[k - 2][nc] : 0.f;
+      }
+    }
     __syncwarp();
     if (lane == 0) {
       const int ch = b / c.Nc;
@@ -956,7 +979,7 @@ __device__ bool finish_rows(const PParams& p, Misc& ms, const GI& G, int gi, int
     // rows).  Every tile of a row computes the same exponent; tile 0 records it.
     auto row_exp = [&](int n) -> int {
       if (KIND == G_PROJ) return G.k == 1 ? __ldcg(rexp_at(p, gi_n, n)) : 0;
-      return range_exp(__ldcg(ss_at(p, gi - 1, n)) / float(p.d));
+      return range_exp(ss_total(p, gi - 1, n) / float(p.d));
     };
     for (int r0 = lo + warp; r0 < hi; r0 += 8 * kConsumerWarps) {
       float4 xv[8];
@@ -976,7 +999,8 @@ __device__ bool finish_rows(const PParams& p, Misc& ms, const GI& G, int gi, int
         const int e = row_exp(n);
         const float sc = exp2i(-e);
         if (lane == 0) {
-          red_add_f32(ss_at(p, gi_n, nr), sq);
+          if (p.det) *ss_part_at(p, gi_n, mt, nr) = sq;
+          else red_add_f32(ss_at(p, gi_n, nr), sq);
           if (mt == 0 && KIND != G_PROJ) *rexp_at(p, gi_n, nr) = e;
         }
         *reinterpret_cast<uint2*>(act_n + act_off(nr, feat, p.d, to_head ? ch_h : c)) =
@@ -1081,7 +1105,7 @@ __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, ui
   const GI G = gemm_inst(p, gi);
   const Ck c = chunking(G.R);
   int beg, end;
-  my_run(c.n * G.n_mt, G.n_ks, gi, beg, end);
+  my_run(c.n * G.n_mt, G.n_ks, gi, beg, end, p.det);
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const bool scaled = KIND == G_QKV || KIND == G_GU || KIND == G_HEAD;
   int s = beg;
@@ -1101,7 +1125,7 @@ __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, ui
       if (!ms.flag[1]) return false;
       for (int col = t; col < c.Nc; col += kConsumers) {
         const int n = ch * c.Nc + col;
-        ms.inv[col] = n < G.R ? rsqrtf(__ldcg(ss_at(p, gi, n)) / float(p.d) + p.eps) * exp2i(__ldcg(rexp_at(p, gi, n)))
+        ms.inv[col] = n < G.R ? rsqrtf(ss_total(p, gi, n) / float(p.d) + p.eps) * exp2i(__ldcg(rexp_at(p, gi, n)))
                               : 0.f;
       }
     }
@@ -1163,11 +1187,11 @@ __device__ bool epilogues(const PParams& p, Misc& ms, uint32_t* keys, int gi, ui
   const int tiles = c.n * G.n_mt;
   for (int tt = beg / G.n_ks; tt <= (end - 1) / G.n_ks; ++tt) {
     const int mt = tt % G.n_mt, ch = tt / G.n_mt, rows = rows_in(G.R, c, ch);
-    int n = 0, rank = tile_share(tiles, G.n_ks, gi, tt, n), mt_f = mt;
+    int n = 0, rank = tile_share(tiles, G.n_ks, gi, tt, n, p.det), mt_f = mt;
     if (KIND == G_GU) {
       const int nkd = p.F / kTileM, kd = mt % nkd, tg = ch * G.n_mt + kd, tu = tg + nkd;
       int ng = 0, nu = 0;
-      const int rg = tile_share(tiles, G.n_ks, gi, tg, ng), ru = tile_share(tiles, G.n_ks, gi, tu, nu);
+      const int rg = tile_share(tiles, G.n_ks, gi, tg, ng, p.det), ru = tile_share(tiles, G.n_ks, gi, tu, nu, p.det);
       rank = mt < nkd ? rg : ng + ru;
       n = ng + nu;
       mt_f = kd;
@@ -1312,7 +1336,10 @@ constexpr size_t kernel_smem_bytes() { return kOffMisc + sizeof(Misc) + 1024; }
 static_assert(kernel_smem_bytes() <= 232448, "more shared memory than a CTA may have");
 
 struct SyncLayout {
-  size_t tile_cnt, ready, ss_cnt, ss, rexp, head_done, codepk, decided, abort_flag, total;
+  size_t tile_cnt, ready, ss_cnt, ss, rexp, head_done, codepk, decided, abort_flag;
+  size_t zeroed;   // bytes from the start zeroed before each launch
+  size_t ss_part;  // deterministic mode's partial sums (written before they are read; not zeroed)
+  size_t total;
   int NCH, MT, KS, NGEMM;
 };
 
@@ -1342,6 +1369,8 @@ SyncLayout sync_layout(const qp_geometry& g, int B) {
   S.codepk = o;   o += al256(size_t(g.n_steps) * B * 8);
   S.decided = o;  o += al256(size_t(g.n_steps) * B * 4);
   S.abort_flag = o; o += 256;
+  S.zeroed = o;
+  S.ss_part = o;  o += al256(size_t(S.NGEMM) * (g.hidden / kTileM) * R1 * 4);
   S.total = o;
   return S;
 }
@@ -1392,6 +1421,8 @@ void fill_params(PParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scra
   p.status = h->status;
   p.spin_limit = h->wait_ticks > 0 ? h->wait_ticks : kSpinLimit;
   p.withhold = h->withhold_gemm;
+  p.det = h->deterministic ? 1 : 0;
+  p.ss_part = reinterpret_cast<float*>(sync + S.ss_part);
   p.NCH = S.NCH; p.MT = S.MT; p.KS = S.KS; p.NGEMM = S.NGEMM;
   p.trace = h->trace; p.trace_n = h->trace_phases;
   p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;
@@ -1411,7 +1442,7 @@ qp_status launch(qp_handle* h, PParams& p, uint8_t* scratch, const Scratch& L, u
     attr_done->store(true, std::memory_order_release);
   }
   const size_t B = size_t(p.B), qkvw = size_t(g.n_q_heads + 2 * g.n_kv_heads) * 128, F2 = size_t(2) * g.ffn;
-  cudaError_t e = cudaMemsetAsync(sync, 0, S.total, s);
+  cudaError_t e = cudaMemsetAsync(sync, 0, S.zeroed, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(scratch + L.acc1_qkv, 0, 2 * B * qkvw * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(scratch + L.acck_qkv, 0, B * qkvw * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(scratch + L.acc1_gu, 0, 2 * B * F2 * 4, s);
@@ -1544,7 +1575,8 @@ qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   const bool sm = small_supported(h, ga);
   if (h->engine == QP_ENGINE_SMALL && !sm) return QP_ERR_ARG;
   const bool pick = h->engine == QP_ENGINE_SMALL || (h->engine == QP_ENGINE_AUTO && a.B <= kSmallAutoFrames);
-  if (sm && pick) return run_frames_small(h, ga, base, L, a.B, s);
+  if (h->deterministic && h->engine == QP_ENGINE_SMALL) return QP_ERR_ARG;   // the tile engine serves that mode
+  if (sm && pick && !h->deterministic) return run_frames_small(h, ga, base, L, a.B, s);
   if (h->wfmt == WF_Q8_0) return run_tile_q8(h, ga, base, L, a.B, s);
   PParams p{};
   fill_params(p, h, ga, base, L, base + L.sync, S, a.B);

@@ -204,6 +204,24 @@ qp_status qp_predict_frames_host(qp_handle* h, int B, const float* H_host,
 qp_status qp_predict_frames_static(qp_handle* h, int B, const float* H, const int32_t* q0,
                                    int32_t* out_codes, float* out_logits, qp_stream s);
 
+/* Deterministic mode, for callers that need run-to-run reproducibility
+ * (the pages have no counterpart; a serving option, not part of the
+ * method).  on != 0: later qp_predict_frames* calls on h give bit-identical
+ * codes and logits for bit-identical inputs (same weights, handle geometry
+ * and batch size).  Ordinarily the partial products of a weight matrix split
+ * over several SMs meet in f32 atomic additions, whose order -- and so
+ * whose last bits -- vary from run to run; a greedy or sampled code whose
+ * margin is within that noise can then flip.  In this mode every output
+ * tile's whole reduction runs on one SM (tensor-core accumulators, in a
+ * fixed order), each output element receives exactly one addition, and the
+ * rows' squared norms are summed from per-tile partial sums in tile order.
+ * The calls run on the tile engine and cost more time at small batches,
+ * where fewer SMs share each GEMM.  The state-slot calls of qp_sched.h are
+ * not covered.  on == 0 restores the default.  QP_ERR_ARG for a null
+ * handle; a later call with QP_ENGINE_SMALL forced (qp_debug.h) is
+ * QP_ERR_ARG. */
+qp_status qp_set_deterministic(qp_handle* h, int on);
+
 /* Synchronise s, read and clear the device status word: QP_OK, or the
  * first device-detected error since the last read. */
 qp_status qp_get_device_status(qp_handle* h, qp_stream s);
