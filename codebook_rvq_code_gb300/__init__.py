@@ -31,7 +31,7 @@ EXPORTED = [
     "qp_rvq_normalize", "qp_rvq_decode",                   # include/qp_rvq.h
     "qp_gguf_open", "qp_gguf_close", "qp_gguf_tensor_count", "qp_gguf_tensor_info",   # include/qp_gguf.h
     "qp_gguf_geometry", "qp_gguf_load_weights",
-    "qp_begin_frames", "qp_step_frames",                   # include/qp_sched.h
+    "qp_begin_frames", "qp_step_frames", "qp_begin_frames_ex", "qp_step_frames_ex",   # include/qp_sched.h
 ]
 
 
@@ -117,6 +117,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.qp_begin_frames.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
     lib.qp_step_frames.restype = i32
     lib.qp_step_frames.argtypes = [vp, i32, vp, vp, vp, vp, vp, vp]
+    lib.qp_begin_frames_ex.restype = i32
+    lib.qp_begin_frames_ex.argtypes = [vp, i32, vp, vp, vp, vp, vp, ctypes.POINTER(QpSampling), vp]
+    lib.qp_step_frames_ex.restype = i32
+    lib.qp_step_frames_ex.argtypes = [vp, i32, vp, vp, vp, vp, vp, ctypes.POINTER(QpSampling), vp]
     return lib
 
 
@@ -322,24 +326,35 @@ class CodePredictor:
         import numpy as np
         return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
 
-    def begin_frames(self, slots, H, q0, out_q1=None, out_logits=None, stream=None):
+    @staticmethod
+    def _sampling(sampling):
+        if sampling is None:
+            return None
+        T, k, gum = sampling
+        return QpSampling(float(T), int(k), _ptr(gum))
+
+    def begin_frames(self, slots, H, q0, out_q1=None, out_logits=None, sampling=None, stream=None):
         """Step 1 of new frames into state slots: slots host ints [B], H
         [B, talker_hidden] f32 cuda, q0 [B] int32 cuda.  Returns q1 [B] int32
-        cuda; out_logits, if given, is [B, vocab] f32 cuda."""
+        cuda; out_logits, if given, is [B, vocab] f32 cuda.  sampling: None
+        (greedy) or (temperature, top_k, gumbel [B, vocab] f32 cuda)."""
         import torch
         sl = self._host_i32(slots)
         B = int(sl.shape[0])
         if out_q1 is None:
             out_q1 = torch.empty((B,), dtype=torch.int32, device=H.device)
-        _check("qp_begin_frames", self._lib.qp_begin_frames(
-            self._h, B, sl.ctypes.data, _ptr(H), _ptr(q0), _ptr(out_q1), _ptr(out_logits), _stream_ptr(stream)))
+        samp = self._sampling(sampling)
+        _check("qp_begin_frames_ex", self._lib.qp_begin_frames_ex(
+            self._h, B, sl.ctypes.data, _ptr(H), _ptr(q0), _ptr(out_q1), _ptr(out_logits),
+            ctypes.byref(samp) if samp is not None else None, _stream_ptr(stream)))
         return out_q1
 
-    def step_frames(self, slots, steps, codes_in, out_codes=None, out_logits=None, stream=None):
+    def step_frames(self, slots, steps, codes_in, out_codes=None, out_logits=None, sampling=None, stream=None):
         """One step for each row: slots and steps host ints [B] (steps in
         2..n_steps), codes_in [B] int32 cuda (q_{step-1} of each row).
         Returns the step's codes [B] int32 cuda; out_logits, if given, is
-        [B, vocab] f32 cuda."""
+        [B, vocab] f32 cuda.  sampling as for begin_frames (each row's noise
+        for its own step)."""
         import torch
         sl, st = self._host_i32(slots), self._host_i32(steps)
         B = int(sl.shape[0])
@@ -347,9 +362,10 @@ class CodePredictor:
             raise ValueError("slots and steps differ in length")
         if out_codes is None:
             out_codes = torch.empty((B,), dtype=torch.int32, device=codes_in.device)
-        _check("qp_step_frames", self._lib.qp_step_frames(
+        samp = self._sampling(sampling)
+        _check("qp_step_frames_ex", self._lib.qp_step_frames_ex(
             self._h, B, sl.ctypes.data, st.ctypes.data, _ptr(codes_in), _ptr(out_codes), _ptr(out_logits),
-            _stream_ptr(stream)))
+            ctypes.byref(samp) if samp is not None else None, _stream_ptr(stream)))
         return out_codes
 
     def code_embeddings(self, codes, out=None, stream=None):

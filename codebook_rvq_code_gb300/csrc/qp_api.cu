@@ -432,8 +432,29 @@ static qp_status run_slots(qp_handle* h, const qp::SlotArgs& a, qp_stream s) {
   return qp::run_slots_small(h, a, static_cast<uint8_t*>(h->sarena), h->scr, h->max_batch, static_cast<cudaStream_t>(s));
 }
 
+// Sampling parameters of a state-slot call: as for qp_predict_frames_ex,
+// with the vocabulary within the sampling pass's key array.
+static bool slot_sampling_ok(const qp_handle* h, const qp_sampling* samp, qp::SlotArgs& a) {
+  if (!samp) return true;
+  if (!(samp->temperature > 0.f) || !std::isfinite(samp->temperature)) return false;
+  if (samp->top_k < 1 || samp->top_k > h->g.vocab || !samp->gumbel || !aligned4(samp->gumbel)) return false;
+  if (h->g.vocab > qp::kMaxVocab) return false;
+  a.temperature = samp->temperature; a.top_k = samp->top_k; a.gumbel = samp->gumbel;
+  return true;
+}
+
 qp_status qp_begin_frames(qp_handle* h, int B, const int32_t* slots, const float* H, const int32_t* q0,
                           int32_t* out_q1, float* out_logits, qp_stream s) {
+  return qp_begin_frames_ex(h, B, slots, H, q0, out_q1, out_logits, nullptr, s);
+}
+
+qp_status qp_step_frames(qp_handle* h, int B, const int32_t* slots, const int32_t* steps, const int32_t* codes_in,
+                         int32_t* out_codes, float* out_logits, qp_stream s) {
+  return qp_step_frames_ex(h, B, slots, steps, codes_in, out_codes, out_logits, nullptr, s);
+}
+
+qp_status qp_begin_frames_ex(qp_handle* h, int B, const int32_t* slots, const float* H, const int32_t* q0,
+                             int32_t* out_q1, float* out_logits, const qp_sampling* samp, qp_stream s) {
   if (!h) return QP_ERR_ARG;
   if (!h->loaded) return QP_ERR_STATE;
   if (B < 1 || B > h->max_batch || B > qp::kSmallMaxFrames || !slots || !H || !q0 || !out_q1) return QP_ERR_ARG;
@@ -443,11 +464,12 @@ qp_status qp_begin_frames(qp_handle* h, int B, const int32_t* slots, const float
   if (h->wfmt != qp::WF_BF16 || h->hfmt != qp::WF_BF16) return QP_ERR_ARG;
   qp::SlotArgs a;
   a.mode = 1; a.B = B; a.slots = slots; a.H = H; a.q0 = q0; a.out_codes = out_q1; a.out_logits = out_logits;
+  if (!slot_sampling_ok(h, samp, a)) return QP_ERR_ARG;
   return run_slots(h, a, s);
 }
 
-qp_status qp_step_frames(qp_handle* h, int B, const int32_t* slots, const int32_t* steps, const int32_t* codes_in,
-                         int32_t* out_codes, float* out_logits, qp_stream s) {
+qp_status qp_step_frames_ex(qp_handle* h, int B, const int32_t* slots, const int32_t* steps, const int32_t* codes_in,
+                            int32_t* out_codes, float* out_logits, const qp_sampling* samp, qp_stream s) {
   if (!h) return QP_ERR_ARG;
   if (!h->loaded) return QP_ERR_STATE;
   if (B < 1 || B > h->max_batch || B > qp::kSmallMaxFrames || !slots || !steps || !codes_in || !out_codes)
@@ -460,6 +482,7 @@ qp_status qp_step_frames(qp_handle* h, int B, const int32_t* slots, const int32_
   qp::SlotArgs a;
   a.mode = 2; a.B = B; a.slots = slots; a.steps = steps; a.codes_in = codes_in; a.out_codes = out_codes;
   a.out_logits = out_logits;
+  if (!slot_sampling_ok(h, samp, a)) return QP_ERR_ARG;
   return run_slots(h, a, s);
 }
 

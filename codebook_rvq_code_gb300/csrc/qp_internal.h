@@ -69,6 +69,9 @@ struct SlotArgs {
   const int32_t* codes_in = nullptr;   // mode 2
   int32_t* out_codes = nullptr;
   float* out_logits = nullptr;
+  float temperature = 0.f;             // 0 => greedy; else Gumbel top-k with the caller's noise
+  int top_k = 0;
+  const float* gumbel = nullptr;       // device [B][vocab]: each row's noise for its one step, caller order
 };
 
 // Rows of the MMA operand buffer for R activation rows (chunks of <= 128).
@@ -165,6 +168,9 @@ size_t small_smem_bytes();
 // state-slot calls on the small-batch engine's kernel built from qp_small_slots.cu
 qp_status run_slots_small(qp_handle* h, const SlotArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
                           cudaStream_t s);
+// the same with Gumbel top-k sampling, on the kernel built from qp_small_slots_sampled.cu
+qp_status run_slots_small_sampled(qp_handle* h, const SlotArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
+                                  cudaStream_t s);
 // load-time weight preparation (qp_weights.cu)
 size_t packed_bytes(int fmt, int N, int K);
 // Pack `rows` rows of a caller matrix [rows, K] (16-bit -- f16 if src_f16,

@@ -1161,6 +1161,12 @@ __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
   for (int b0 = (blockIdx.x + k * 7) % G; b0 < p.B; b0 += two ? 2 * G : G) {
     const int b = b0 + (two ? half * G : 0);
     if (b >= p.B || (!two && half == 1)) continue;   // warp-uniform: the half sits this frame out
+    // In state-slot calls a row decides one step (its own, in SM_STEP), its
+    // noise and logits are the caller's row row_perm[b], and the decision is
+    // filed under the row's step.
+    const bool slots = sm_mode(p) != SM_RUN;
+    const int kd = sm_mode(p) == SM_STEP ? p.row_step[b] : k;
+    const size_t orow = slots ? size_t(p.row_perm[b]) : size_t(b) * p.n_steps + (k - 1);
     if (tg == 0) ms.hflag[half] = poll_geq(p, sm_done(p, gih), unsigned(h.n_mt * h.n_ks));
     named_bar(bar, NG);
     if (!ms.hflag[half]) return false;
@@ -1180,10 +1186,10 @@ __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
       for (int i = 0; i < NG / 32; ++i) tot += sc.rsum[i];
       rs = rsqrtf(tot / float(p.d) + p.eps) * exp2i(__ldcg(sm_rexp(p, gih, b)));
     }
-    const float* gb = p.gumbel + (size_t(b) * p.n_steps + (k - 1)) * V;
+    const float* gb = p.gumbel + orow * V;
     const int code = gumbel_topk_group<NG>(l, rs, p.temperature, gb, V, p.top_k, keys + (two ? half * V : 0), sc,
                                            bar, tg);
-    float* dst = p.out_logits ? p.out_logits + (size_t(b) * p.n_steps + (k - 1)) * V : nullptr;
+    float* dst = p.out_logits ? p.out_logits + orow * V : nullptr;
     for (int i = tg; i < V; i += NG) {
       if (dst) dst[i] = __ldcg(l + i) * rs;
       l[i] = 0.f;
@@ -1191,7 +1197,7 @@ __device__ bool sm_decide(const SParams& p, SMisc& ms, uint32_t* keys, int k) {
     named_bar(bar, NG);
     if (tg == 0) {
       __threadfence();
-      atomicExch(p.decided + size_t(k - 1) * p.B + b, unsigned(code + 1));
+      atomicExch(p.decided + size_t(kd - 1) * p.B + b, unsigned(code + 1));
     }
   }
   return true;
@@ -1234,7 +1240,9 @@ __device__ void sm_consumer(const SParams& p, SMisc& ms, uint8_t* smem) {
 
 // The greedy frame-loop kernel is k_frames_small, the sampling one
 // k_frames_small_sampled, the state-slot kernel k_slots_small.
-#if QP_SMALL_SLOTS
+#if QP_SMALL_SLOTS && QP_SMALL_SAMPLED
+#define SM_KERNEL k_slots_small_sampled
+#elif QP_SMALL_SLOTS
 #define SM_KERNEL k_slots_small
 #elif QP_SMALL_SAMPLED
 #define SM_KERNEL k_frames_small_sampled
@@ -1415,7 +1423,7 @@ qp_status run_frames_small(qp_handle* h, const RunArgs& a, uint8_t* scratch, con
   return sm_launch(h, p, sync, S.total, s);
 }
 
-#elif QP_SMALL_SAMPLED   // the sampling frame-loop kernel
+#elif QP_SMALL_SAMPLED && !QP_SMALL_SLOTS   // the sampling frame-loop kernel
 
 qp_status run_frames_small_sampled(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
                                    cudaStream_t s) {
@@ -1427,15 +1435,22 @@ qp_status run_frames_small_sampled(qp_handle* h, const RunArgs& a, uint8_t* scra
   return sm_launch(h, p, sync, S.total, s);
 }
 
-#else   // the state-slot kernel
+#else   // the state-slot kernels, greedy (k_slots_small) and sampling (k_slots_small_sampled)
 
+#if QP_SMALL_SAMPLED
+qp_status run_slots_small_sampled(qp_handle* h, const SlotArgs& sa, uint8_t* scratch, const Scratch& L, int bmax,
+                                  cudaStream_t s) {
+#else
 qp_status run_slots_small(qp_handle* h, const SlotArgs& sa, uint8_t* scratch, const Scratch& L, int bmax,
                           cudaStream_t s) {
+  if (sa.temperature > 0.f) return run_slots_small_sampled(h, sa, scratch, L, bmax, s);
+#endif
   const qp_geometry& g = h->g;
   const int B = sa.B;
   if (B < 1 || B > kSmallMaxFrames || B > bmax || h->wfmt != WF_BF16 || h->hfmt != WF_BF16) return QP_ERR_ARG;
   RunArgs a{};
   a.B = B; a.H = sa.H; a.q0 = sa.q0; a.out_codes = sa.out_codes; a.out_logits = sa.out_logits;
+  a.temperature = sa.temperature; a.top_k = sa.top_k; a.gumbel = sa.gumbel;
   SParams p{};
   // rows in step order (a stable sort keeps the caller's order within a step)
   int order[kSmallMaxFrames];

@@ -18,7 +18,7 @@
  * forced one), gets the codes and logits of qp_predict_frames.
  *
  * Served by the small-batch engine: bf16 weights, B <= 64 rows per call,
- * greedy decisions.  A step call runs one step's layers over all its rows;
+ * greedy decisions or Gumbel top-k sampling (the _ex calls).  A step call runs one step's layers over all its rows;
  * its output head holds one head matrix per distinct step among the rows
  * (the rows sorted into step groups), as one GEMM.  Slot and step arrays are HOST memory (a scheduler keeps
  * this bookkeeping on the host); the library sorts the rows by step and
@@ -58,6 +58,20 @@ qp_status qp_begin_frames(qp_handle* h, int B, const int32_t* slots, const float
  * [0, vocab) latches QP_ERR_BAD_TOKEN and is clamped. */
 qp_status qp_step_frames(qp_handle* h, int B, const int32_t* slots, const int32_t* steps, const int32_t* codes_in,
                          int32_t* out_codes, float* out_logits, qp_stream stream);
+
+/* As qp_begin_frames and qp_step_frames, but each row's code is drawn by
+ * Gumbel top-k sampling (qp_sampling of qp.h: z = logits / temperature, the
+ * top_k largest z, argmax of z + g) when samp is not NULL, greedy when it
+ * is.  samp->gumbel is device [B][vocab] f32: row b's noise for the one step
+ * this call decides for it, in the caller's row order.  A frame run through
+ * these calls with the noise qp_predict_frames_ex would read for each of its
+ * steps gets the same codes.  QP_ERR_ARG additionally for a temperature that
+ * is not positive and finite, top_k outside [1, vocab], a null or
+ * misaligned noise array, or a vocabulary above 4096. */
+qp_status qp_begin_frames_ex(qp_handle* h, int B, const int32_t* slots, const float* H, const int32_t* q0,
+                             int32_t* out_q1, float* out_logits, const qp_sampling* samp, qp_stream stream);
+qp_status qp_step_frames_ex(qp_handle* h, int B, const int32_t* slots, const int32_t* steps, const int32_t* codes_in,
+                            int32_t* out_codes, float* out_logits, const qp_sampling* samp, qp_stream stream);
 
 #ifdef __cplusplus
 }

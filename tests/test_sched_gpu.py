@@ -78,11 +78,12 @@ class Checker:
                 self.mismatch += 1
 
 
-def run_schedule(cp, g, H, q0, ref, seed, max_rows=64, checked=None):
+def run_schedule(cp, g, H, q0, ref, seed, max_rows=64, checked=None, sampling=None):
     """Frames enter free slots at random ticks; each tick advances a random
     subset of the running frames by one step, in a random row order.  Every
     step's input is ref["codes"]; `checked` limits the comparison to those
-    frames."""
+    frames.  sampling: None (greedy) or (T, top_k, gumbel [F, n_steps,
+    vocab]); each call passes each row's noise for its own step."""
     import torch
     rng = np.random.default_rng(seed)
     F = H.shape[0]
@@ -101,7 +102,11 @@ def run_schedule(cp, g, H, q0, ref, seed, max_rows=64, checked=None):
             tH = torch.from_numpy(np.ascontiguousarray(H[frames])).cuda()
             tq = torch.from_numpy(q0[frames].astype(np.int32)).cuda()
             lg = torch.empty((nb, g.vocab), dtype=torch.float32, device="cuda")
-            q1 = cp.begin_frames(slots, tH, tq, out_logits=lg)
+            smp = None
+            if sampling is not None:
+                T, k, gum = sampling
+                smp = (T, k, torch.from_numpy(np.ascontiguousarray(gum[frames, 0])).cuda())
+            q1 = cp.begin_frames(slots, tH, tq, out_logits=lg, sampling=smp)
             chk.add(frames, [1] * nb, q1.cpu().numpy(), lg.cpu().numpy())
             for f, sl in zip(frames, slots):
                 running[f] = [sl, 2]
@@ -115,7 +120,11 @@ def run_schedule(cp, g, H, q0, ref, seed, max_rows=64, checked=None):
         steps = [running[f][1] for f in frames]
         cin = torch.from_numpy(np.array([ref["codes"][f, s - 2] for f, s in zip(frames, steps)], np.int32)).cuda()
         lg = torch.empty((n, g.vocab), dtype=torch.float32, device="cuda")
-        out = cp.step_frames(slots, steps, cin, out_logits=lg)
+        smp = None
+        if sampling is not None:
+            T, k, gum = sampling
+            smp = (T, k, torch.from_numpy(np.ascontiguousarray(gum[frames, np.array(steps) - 1])).cuda())
+        out = cp.step_frames(slots, steps, cin, out_logits=lg, sampling=smp)
         chk.add(frames, steps, out.cpu().numpy(), lg.cpu().numpy())
         calls += 1
         for f in frames:
@@ -139,6 +148,58 @@ def test_ragged_schedule_matches_the_oracle(small, seed):
     assert chk.mismatch == 0
     assert ref["decidable"].sum() > 0
     assert calls > F   # the frames were interleaved
+
+
+@pytest.mark.parametrize("T,k", [(0.9, 50), (0.6, 7), (1.3, 1)])
+def test_ragged_schedule_sampling_matches_the_oracle(small, T, k):
+    """Gumbel top-k sampling in state-slot calls (qp_begin_frames_ex /
+    qp_step_frames_ex): each row decides its own step with that step's noise;
+    teacher-forced to the oracle's sampled codes, every clear decision (the
+    sampling rule: the winner stays the winner under any change of the logits
+    within the tolerance) matches."""
+    raw, P, cp = small
+    F = 24
+    H, q0 = S.toy_inputs(SMALL, F, seed=560 + k)
+    gum = S.gumbel_noise((F, SMALL.n_steps, SMALL.vocab), seed=11 + k)
+    ref = O.predict_frames(P, H, q0, T, k, gum, tol=TOL)
+    chk, calls = run_schedule(cp, SMALL, H, q0, ref, 40 + k, sampling=(T, k, gum))
+    assert chk.err <= TOL, chk.err
+    assert chk.mismatch == 0
+    assert ref["decidable"].sum() > 0
+    assert calls > F
+
+
+def test_sampling_slot_calls_free_running_match_predict(small):
+    """Begin, then steps 2..n_steps fed the library's own sampled codes, with
+    the noise qp_predict_frames_ex reads for each step, equals one sampled
+    qp_predict_frames_ex call up to each frame's first unclear decision."""
+    import torch
+    raw, P, cp = small
+    g = SMALL
+    B, T, k = 9, 0.9, 20
+    H, q0 = S.toy_inputs(g, B, seed=580)
+    gum = S.gumbel_noise((B, g.n_steps, g.vocab), seed=12)
+    codes_p, logits_p = run_gpu(cp, H, q0, sampling=(T, k, gum))
+    slots = list(range(B))
+    codes = np.zeros((B, g.n_steps), np.int32)
+    logits = np.zeros((B, g.n_steps, g.vocab), np.float32)
+    lg = torch.empty((B, g.vocab), dtype=torch.float32, device="cuda")
+    c = cp.begin_frames(slots, torch.from_numpy(H).cuda(), torch.from_numpy(q0.astype(np.int32)).cuda(),
+                        out_logits=lg, sampling=(T, k, torch.from_numpy(np.ascontiguousarray(gum[:, 0])).cuda()))
+    codes[:, 0], logits[:, 0] = c.cpu().numpy(), lg.cpu().numpy()
+    for s in range(2, g.n_steps + 1):
+        c = cp.step_frames(slots, [s] * B, c, out_logits=lg,
+                           sampling=(T, k, torch.from_numpy(np.ascontiguousarray(gum[:, s - 1])).cuda()))
+        codes[:, s - 1], logits[:, s - 1] = c.cpu().numpy(), lg.cpu().numpy()
+    torch.cuda.synchronize()
+    assert cp.device_status() == 0
+    ref = O.predict_frames(P, H, q0, T, k, gum, tol=TOL)
+    dec = ref["decidable"]
+    first = np.where(dec.all(axis=1), g.n_steps, np.argmin(dec, axis=1))
+    for b in range(B):   # both runs follow the oracle up to its first unclear decision
+        j = first[b]
+        np.testing.assert_array_equal(codes[b, :j], codes_p[b, :j])
+        assert np.abs(logits[b, :j + 1] - logits_p[b, :j + 1]).max() <= TOL
 
 
 def test_ragged_schedule_talker_wide_tables(wide):
@@ -258,6 +319,14 @@ def test_state_slot_argument_errors(small, qpk):
         with pytest.raises(qpk.QpError) as e:
             cp.step_frames(slots, steps, c)
         assert e.value.code == 1, (slots, steps)
+    gum = torch.zeros((4, g.vocab), device="cuda")
+    for samp in [(0.0, 5, gum), (float("inf"), 5, gum), (0.9, 0, gum), (0.9, g.vocab + 1, gum), (0.9, 5, None)]:
+        with pytest.raises(qpk.QpError) as e:
+            cp.begin_frames([0, 1, 2, 3], H, q0, sampling=samp)
+        assert e.value.code == 1, samp[:2]
+        with pytest.raises(qpk.QpError) as e:
+            cp.step_frames([0, 1, 2, 3], [2, 2, 2, 2], c, sampling=samp)
+        assert e.value.code == 1, samp[:2]
     assert cp.device_status() == 0   # nothing was enqueued
 
 
