@@ -115,7 +115,7 @@ def source_hash():
     for f in sorted(glob.glob(os.path.join(ROOT, "codebook_rvq_code_gb300", "csrc", "*"))
                     + glob.glob(os.path.join(ROOT, "include", "*.h"))):
         h.update(" ".join(_strip_comments(open(f, encoding="utf-8").read()).split()).encode())
-    h.update(" ".join(qb.ARCH + qb.NVCC_FLAGS).encode())
+    h.update(" ".join(f.replace(ROOT, "<repo>") for f in qb.ARCH + qb.NVCC_FLAGS).encode())   # not where the repo sits
     return h.hexdigest()[:16]
 
 
