@@ -332,8 +332,9 @@ def whole_job(local_ms: float, frames_per_step: int, steps: int, world: int, dev
 
 def engine_of(B: int, gemm_format: str) -> str:
     """The schedule QP_ENGINE_AUTO picks (include/qp_debug.h): the small-batch
-    engine for bf16 calls of at most 40 frames, the tile engine otherwise."""
-    return "small" if gemm_format == "bf16" and B <= 40 else "tile"
+    engine for calls of at most 40 frames (either weight format), the tile
+    engine otherwise."""
+    return "small" if B <= 40 else "tile"
 
 
 def sweep(g, dev, stream, steps, hbm, tf):
@@ -469,7 +470,9 @@ def work_exporter(g, B: int):
 def exporter_rows(dev, stream, steps, hbm, tc):
     """The exporter's model layout (2048-wide code tables through small_to_mtp,
     Q8_0 matrices, f16 heads and tables), random weights, greedy, at one frame
-    and at 256 frames (tile engine: Q8_0 layers)."""
+    (the small-batch engine, which streams each Q8_0 matrix as its f16 hi and
+    lo images: 4 B per weight against the blocks' 1.0625) and at 256 frames
+    (the tile engine, which streams the blocks and dequantises on chip)."""
     import dataclasses
     import torch
     import codebook_rvq_code_gb300 as qpk
@@ -506,6 +509,7 @@ def exporter_rows(dev, stream, steps, hbm, tc):
             "workload": f"{B} frames, 1.7B geometry, 2048-wide code tables projected each step, "
                         "Q8_0 matrices, f16 heads and tables, greedy",
             "ms_per_call": ms, "us_per_step": 1e3 * ms / g.n_steps, "frames_per_s": B / (ms / 1e3),
+            "engine": engine_of(B, "q8_0"),
             "device_status": cp.device_status(),
             "roofline": {"bound": bound, "frac": (t_hbm if bound == "hbm" else t_tc) / (ms / 1e3),
                          "algorithmic_bytes": nbytes, "algorithmic_flops": flops}}

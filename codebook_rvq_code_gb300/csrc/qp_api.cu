@@ -91,9 +91,12 @@ std::unordered_map<std::string, Slot> build_slots(const qp_geometry& g) {
   return m;
 }
 
+// A packed matrix: 16-bit, or Q8_0 (int8 values and f16 scales) plus its
+// f16 hi and lo images for the small-batch engine.
 size_t matrix_bytes(int fmt, int64_t N, int64_t K) {
   return fmt == qp::WF_BF16 ? carve_size<uint8_t>(size_t(N) * K * 2)
-                            : carve_size<uint8_t>(size_t(N) * K) + carve_size<__half>(size_t(N) * (K / 32));
+                            : carve_size<uint8_t>(size_t(N) * K) + carve_size<__half>(size_t(N) * (K / 32)) +
+                                  2 * carve_size<uint8_t>(size_t(N) * K * 2);
 }
 
 // The engine that serves a call (qp_debug.h, qp_engine).
@@ -283,6 +286,8 @@ qp_status qp_load_weights(qp_handle* h, const qp_weight* w, int n, qp_stream sv)
     } else {
       m.w = carve<uint8_t>(p, size_t(N) * K);
       m.scale = carve<__half>(p, size_t(N) * (K / 32));
+      m.w16[0] = carve<uint8_t>(p, size_t(N) * K * 2);
+      m.w16[1] = carve<uint8_t>(p, size_t(N) * K * 2);
     }
     return m;
   };
@@ -461,7 +466,6 @@ qp_status qp_begin_frames_ex(qp_handle* h, int B, const int32_t* slots, const fl
   if (!aligned16(H) || !aligned4(q0) || !aligned4(out_q1) || (out_logits && !aligned16(out_logits)) ||
       !slots_ok(h, B, slots))
     return QP_ERR_ARG;
-  if (h->wfmt != qp::WF_BF16 || h->hfmt != qp::WF_BF16) return QP_ERR_ARG;
   qp::SlotArgs a;
   a.mode = 1; a.B = B; a.slots = slots; a.H = H; a.q0 = q0; a.out_codes = out_q1; a.out_logits = out_logits;
   if (!slot_sampling_ok(h, samp, a)) return QP_ERR_ARG;
@@ -478,7 +482,6 @@ qp_status qp_step_frames_ex(qp_handle* h, int B, const int32_t* slots, const int
     return QP_ERR_ARG;
   for (int b = 0; b < B; ++b)
     if (steps[b] < 2 || steps[b] > h->g.n_steps) return QP_ERR_ARG;
-  if (h->wfmt != qp::WF_BF16 || h->hfmt != qp::WF_BF16) return QP_ERR_ARG;
   qp::SlotArgs a;
   a.mode = 2; a.B = B; a.slots = slots; a.steps = steps; a.codes_in = codes_in; a.out_codes = out_codes;
   a.out_logits = out_logits;

@@ -30,6 +30,10 @@ struct PackedMat {
   __half* scale = nullptr;
   int N = 0, K = 0;
   int fmt = 0;    // WF_BF16 (16-bit source, packed as f16) or WF_Q8_0
+  // Q8_0 only: the weights d*q as two f16 images in the 16-bit packed layout,
+  // hi = f16(d*q) and lo = f16(d*q - hi) (hi + lo = d*q exactly), for the
+  // small-batch engine, which streams 16-bit slices and multiplies both.
+  uint8_t* w16[2] = {nullptr, nullptr};
 };
 
 struct LayerW {
@@ -157,7 +161,8 @@ qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s);
 size_t persistent_smem_bytes();
 // the Q8_0 build of the tile engine's kernel (qp_persistent_q8.cu)
 qp_status run_tile_q8(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax, cudaStream_t s);
-// small-batch engine (qp_small.cu): bf16 weights, at most kSmallMaxFrames
+// small-batch engine (qp_small.cu): 16-bit slices (Q8_0 matrices through
+// their hi and lo images), at most kSmallMaxFrames
 bool small_supported(const qp_handle* h, const RunArgs& a);
 qp_status run_frames_small(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax,
                            cudaStream_t s);
@@ -175,7 +180,7 @@ qp_status run_slots_small_sampled(qp_handle* h, const SlotArgs& a, uint8_t* scra
 size_t packed_bytes(int fmt, int N, int K);
 // Pack `rows` rows of a caller matrix [rows, K] (16-bit -- f16 if src_f16,
 // else bf16 -- or a Q8_0 block stream) into rows [row0, row0 + rows) of the
-// packed matrix dst.
+// packed matrix dst (and, for Q8_0, of its f16 hi and lo images).
 cudaError_t pack_rows(const void* src, int fmt, bool src_f16, int rows, int K, const PackedMat& dst, int row0,
                       cudaStream_t s);
 // out[b][j] = tables[j][codes[b][j]] as f32 for b < B, j < n_tables

@@ -103,18 +103,20 @@ struct SMisc {
 };
 
 struct SLayer {
-  const uint16_t* w[4];    // qkv, o, gu, down: tile-packed f16 (qp_weights.cu)
+  const uint16_t* w[4];    // qkv, o, gu, down: tile-packed f16 (qp_weights.cu); for Q8_0 matrices the hi image
+  const uint16_t* wl[4];   // Q8_0 matrices: the lo image (hi + lo = d * q), else null
   const float* attn_norm; const float* q_norm; const float* k_norm; const float* ffn_norm;
 };
 
 struct SParams {
   int d, qw, kvw, F, V, th, L, n_q, n_kv, n_steps, q0_vocab;
   float eps;
-  const uint16_t* w_proj; const float* b_proj; const uint16_t* e0;
+  const uint16_t* w_proj; const uint16_t* w_proj_lo; const float* b_proj; const uint16_t* e0;
   SLayer layer[kMaxLayers];
   const float* out_norm;
   const uint16_t* embed[kMaxSteps];
   const uint16_t* w_head[kMaxSteps];
+  const uint16_t* w_head_lo[kMaxSteps];   // Q8_0 heads: the lo images, else null
   const float2* rope_cs;
   // scratch (rows: 2B at step 1, B later)
   float* x;                // residual stream [row][d]
@@ -164,6 +166,7 @@ struct SG {
   int r0;   // first activation / output row (a step group's head)
   bool scaled;
   const uint16_t* w; float* out;
+  const uint16_t* wl;   // the lo image of a Q8_0 matrix (a unit then multiplies two slices), else null
 };
 // The program: GEMM 0 is step 1's projection (rows H_b, E0[q0_b]); step k
 // then has, with Talker-wide code tables and k >= 2, the projection of its
@@ -190,7 +193,7 @@ __device__ SG sgemm(const SParams& p, int gi) {
     r = gi - p.proj_in;
     if (r == 4 * p.L) {   // every step group's head: tile mt is group mt / (V / 128)'s
       g.kind = S_HEAD; g.l = p.L - 1; g.R = p.group_rows; g.n_mt = p.n_groups * (p.V / kTileM);
-      g.n_ks = p.d / kKs; g.w = nullptr; g.out = p.logits; g.ld = p.V;
+      g.n_ks = p.d / kKs; g.w = nullptr; g.wl = p.w_head_lo[0]; g.out = p.logits; g.ld = p.V;
       g.N = sm_cols(g.R);
       return g;
     }
@@ -208,14 +211,15 @@ __device__ SG sgemm(const SParams& p, int gi) {
   g.R = g.k == 1 ? 2 * p.B : p.B;
   if (r < 0) {
     g.kind = S_PROJ; g.l = 0; g.n_mt = p.d / kTileM; g.n_ks = p.th / kKs;
-    g.w = p.w_proj; g.out = p.x; g.ld = p.d;
+    g.w = p.w_proj; g.wl = p.w_proj_lo; g.out = p.x; g.ld = p.d;
   } else {
     if (r == 4 * p.L) {
       g.kind = S_HEAD; g.l = p.L - 1; g.R = p.B; g.n_mt = p.V / kTileM; g.n_ks = p.d / kKs;
-      g.w = p.w_head[g.k - 1]; g.out = p.logits; g.ld = p.V; g.scaled = true;
+      g.w = p.w_head[g.k - 1]; g.wl = p.w_head_lo[g.k - 1]; g.out = p.logits; g.ld = p.V; g.scaled = true;
     } else {
       g.l = r / 4;
       const SLayer& L = p.layer[g.l];
+      g.wl = L.wl[r % 4];
       switch (r % 4) {
         case 0: g.kind = S_QKV; g.n_mt = (p.qw + 2 * p.kvw) / kTileM; g.n_ks = p.d / kKs; g.w = L.w[0];
                 g.out = p.acc_qkv[((g.k - 1) * p.L + g.l) & 1]; g.ld = p.qw + 2 * p.kvw; g.scaled = true; break;
@@ -246,12 +250,15 @@ __device__ __forceinline__ void sm_rows(const SParams& p, const SG& g, int mt, i
     R = g.R;
   }
 }
-__device__ __forceinline__ const uint8_t* sm_slice(const SParams& p, const SG& g, int s) {
+// Image 0 is the 16-bit matrix (or a Q8_0 matrix's hi image), image 1 a
+// Q8_0 matrix's lo image.
+__device__ __forceinline__ const uint8_t* sm_slice(const SParams& p, const SG& g, int s, int img = 0) {
   if (sm_grouped(p, g)) {
     const int per = (p.V / kTileM) * g.n_ks, h = s / per;
-    return reinterpret_cast<const uint8_t*>(p.w_head[p.group_step[h] - 1]) + size_t(s - h * per) * kSmWSlot;
+    const uint16_t* m = img ? p.w_head_lo[p.group_step[h] - 1] : p.w_head[p.group_step[h] - 1];
+    return reinterpret_cast<const uint8_t*>(m) + size_t(s - h * per) * kSmWSlot;
   }
-  return reinterpret_cast<const uint8_t*>(g.w) + size_t(s) * kSmWSlot;
+  return reinterpret_cast<const uint8_t*>(img ? g.wl : g.w) + size_t(s) * kSmWSlot;
 }
 
 // GEMMs whose partials are scaled by the input row's 1/RMS.  From step 2 on
@@ -368,15 +375,17 @@ __device__ void sm_producer(const SParams& p, SMisc& ms, uint8_t* smem) {
     const SG g = sgemm(p, gi);
     int beg, end;
     sm_run(g, gi, beg, end);
+    const int nimg = g.wl ? 2 : 1;   // a Q8_0 matrix's unit takes its hi and lo slices
     for (int s = beg; s < end; ++s) {
-      const uint32_t slot = it % kSmNW, u = it / kSmNW;
-      if (u > 0 && !mwait(p, &ms.wempty[slot], (u - 1) & 1)) goto drain;
-      sm_ev(p, &ms.evc, SEV_ISSUE, gi);
-      mbar_expect_tx(&ms.wfull[slot], kSmWSlot);
-      // tile mt, slice ks of the tile-packed matrix: one contiguous 32 KB run
-      bulk_g2s_stream(smem + kSmOffW + slot * kSmWSlot, sm_slice(p, g, s),
-                      kSmWSlot, &ms.wfull[slot], pol);
-      ++it;
+      for (int img = 0; img < nimg; ++img) {
+        const uint32_t slot = it % kSmNW, u = it / kSmNW;
+        if (u > 0 && !mwait(p, &ms.wempty[slot], (u - 1) & 1)) goto drain;
+        sm_ev(p, &ms.evc, SEV_ISSUE, gi);
+        mbar_expect_tx(&ms.wfull[slot], kSmWSlot);
+        // tile mt, slice ks of the tile-packed matrix: one contiguous 32 KB run
+        bulk_g2s_stream(smem + kSmOffW + slot * kSmWSlot, sm_slice(p, g, s, img), kSmWSlot, &ms.wfull[slot], pol);
+        ++it;
+      }
     }
   }
 drain:
@@ -398,6 +407,7 @@ __device__ void sm_mma(const SParams& p, SMisc& ms, uint8_t* smem) {
     const uint32_t idesc = idesc_f16(kTileM, g.N);
     const uint32_t blb = uint32_t(g.N / 8) * 128;   // operand K-direction core-matrix stride
     const uint32_t nop = sm_op_slots(g), obytes = sm_op_bytes(g);
+    const uint32_t nimg = g.wl ? 2u : 1u;   // Q8_0: the hi and lo slices, multiplied into one accumulator
     for (int s = beg; s < end; ++s) {
       const int ks = s % g.n_ks;
       const bool first = s == beg || ks == 0;
@@ -409,28 +419,29 @@ __device__ void sm_mma(const SParams& p, SMisc& ms, uint8_t* smem) {
         if (!mwait(p, &ms.wfull[ws], (wit / kSmNW) & 1)) goto out;
         sm_ev_mma(p, evi, SEV_WEIGHTS, gi);
       }
+      if (nimg > 1 && !mwait(p, &ms.wfull[(wit + 1) % kSmNW], ((wit + 1) / kSmNW) & 1)) goto out;
       if (!mwait(p, &ms.ofull[os], ouse[os] & 1)) goto out;
       if (first && seg >= 2 && !mwait(p, &ms.accempty[tb], ((seg >> 1) - 1) & 1)) goto out;
       tc_fence_after();
-      {
-        const uint32_t a0 = smem_u32(smem + kSmOffW + ws * kSmWSlot);
+      for (uint32_t img = 0; img < nimg; ++img) {
+        const uint32_t a0 = smem_u32(smem + kSmOffW + ((wit + img) % kSmNW) * kSmWSlot);
         const uint32_t b0 = smem_u32(smem + kSmOffOp + os * obytes);
         const uint32_t d = ms.tmem_base + tb * 128;
 #pragma unroll
         for (int j = 0; j < kKs / 16; ++j) {
           const uint64_t ad = smem_desc(a0 + uint32_t(j) * 2 * (kTileM / 8) * 128, (kTileM / 8) * 128, 128);
           const uint64_t bd = smem_desc(b0 + uint32_t(j) * 2 * blb, blb, 128);
-          mma_f16(d, ad, bd, idesc, (first && j == 0) ? 0u : 1u);
+          mma_f16(d, ad, bd, idesc, (first && img == 0 && j == 0) ? 0u : 1u);
         }
+        mma_commit(&ms.wempty[(wit + img) % kSmNW]);
       }
-      mma_commit(&ms.wempty[ws]);
       mma_commit(&ms.oempty[os]);
       if (last) {
         mma_commit(&ms.accfull[tb]);
         sm_ev_mma(p, evi, SEV_COMMIT, gi);
         ++seg;
       }
-      ++wit;
+      wit += nimg;
       ++ouse[os];
     }
   }
@@ -1322,21 +1333,27 @@ void sm_fill(SParams& p, const qp_handle* h, const RunArgs& a, uint8_t* scratch,
   p.d = g.hidden; p.qw = g.n_q_heads * kHeadDim; p.kvw = g.n_kv_heads * kHeadDim; p.F = g.ffn; p.V = g.vocab;
   p.th = g.talker_hidden; p.L = g.layers; p.n_q = g.n_q_heads; p.n_kv = g.n_kv_heads; p.n_steps = g.n_steps;
   p.q0_vocab = g.q0_vocab; p.eps = g.rms_eps;
-  p.w_proj = reinterpret_cast<const uint16_t*>(h->proj.w); p.b_proj = h->b_proj; p.e0 = h->e0;
+  // 16-bit matrices as packed; Q8_0 matrices through their f16 hi and lo images
+  auto hi = [](const PackedMat& m) {
+    return reinterpret_cast<const uint16_t*>(m.fmt == WF_Q8_0 ? m.w16[0] : m.w);
+  };
+  auto lo = [](const PackedMat& m) {
+    return m.fmt == WF_Q8_0 ? reinterpret_cast<const uint16_t*>(m.w16[1]) : nullptr;
+  };
+  p.w_proj = hi(h->proj); p.w_proj_lo = lo(h->proj); p.b_proj = h->b_proj; p.e0 = h->e0;
   p.embed_f16 = h->embed_f16;
   for (int l = 0; l < g.layers; ++l) {
     const LayerW& Lw = h->layer[l];
-    p.layer[l].w[0] = reinterpret_cast<const uint16_t*>(Lw.qkv.w);
-    p.layer[l].w[1] = reinterpret_cast<const uint16_t*>(Lw.o.w);
-    p.layer[l].w[2] = reinterpret_cast<const uint16_t*>(Lw.gu.w);
-    p.layer[l].w[3] = reinterpret_cast<const uint16_t*>(Lw.down.w);
+    const PackedMat* mats[4] = {&Lw.qkv, &Lw.o, &Lw.gu, &Lw.down};
+    for (int i = 0; i < 4; ++i) { p.layer[l].w[i] = hi(*mats[i]); p.layer[l].wl[i] = lo(*mats[i]); }
     p.layer[l].attn_norm = Lw.attn_norm; p.layer[l].q_norm = Lw.q_norm;
     p.layer[l].k_norm = Lw.k_norm; p.layer[l].ffn_norm = Lw.ffn_norm;
   }
   p.out_norm = h->out_norm;
   for (int j = 0; j < g.n_steps; ++j) {
     p.embed[j] = h->embed[j];
-    p.w_head[j] = reinterpret_cast<const uint16_t*>(h->head[j].w);
+    p.w_head[j] = hi(h->head[j]);
+    p.w_head_lo[j] = lo(h->head[j]);
   }
   p.rope_cs = h->rope_cs;
   // the tile engine's buffers, each at least as large as this schedule needs
@@ -1405,7 +1422,8 @@ qp_status sm_launch(const qp_handle* h, const SParams& p, uint8_t* sync, size_t 
 size_t small_smem_bytes() { return kSmOffMisc + sizeof(SMisc) + 1024; }
 
 bool small_supported(const qp_handle* h, const RunArgs& a) {
-  if (h->wfmt != WF_BF16 || h->hfmt != WF_BF16) return false;
+  // Q8_0 matrices are served through their f16 hi and lo images (loaded beside them)
+  if (h->wfmt == WF_Q8_0 && !h->layer[0].qkv.w16[0]) return false;
   if (a.B < 1 || a.B > kSmallMaxFrames) return false;
   if (a.temperature > 0.f && h->g.vocab > kMaxVocab) return false;
   return true;
@@ -1447,7 +1465,7 @@ qp_status run_slots_small(qp_handle* h, const SlotArgs& sa, uint8_t* scratch, co
 #endif
   const qp_geometry& g = h->g;
   const int B = sa.B;
-  if (B < 1 || B > kSmallMaxFrames || B > bmax || h->wfmt != WF_BF16 || h->hfmt != WF_BF16) return QP_ERR_ARG;
+  if (B < 1 || B > kSmallMaxFrames || B > bmax) return QP_ERR_ARG;
   RunArgs a{};
   a.B = B; a.H = sa.H; a.q0 = sa.q0; a.out_codes = sa.out_codes; a.out_logits = sa.out_logits;
   a.temperature = sa.temperature; a.top_k = sa.top_k; a.gumbel = sa.gumbel;

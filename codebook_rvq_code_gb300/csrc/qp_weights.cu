@@ -67,6 +67,38 @@ __global__ void k_pack_q8(const uint8_t* __restrict__ src, int rows, int K, int8
   }
 }
 
+// Q8_0 block stream rows -> the f16 images hi = f16(d * q) and lo =
+// f16(d * q - hi) in the 16-bit packed layout.  d * q is exact in f32 (an
+// 11-bit times an 8-bit significand) and so is d * q - hi; lo holds it
+// exactly whenever d >= 2^-14 (it is a multiple of d's last place and below
+// half of hi's), so hi + lo is the stored weight.  One thread per 8 values.
+__global__ void k_pack_q8_hilo(const uint8_t* __restrict__ src, int rows, int K, uint16_t* __restrict__ hi,
+                               uint16_t* __restrict__ lo, int row0) {
+  const size_t total = size_t(rows) * (K / 8);
+  for (size_t i = blockIdx.x * size_t(blockDim.x) + threadIdx.x; i < total; i += size_t(gridDim.x) * blockDim.x) {
+    const int r = int(i / (K / 8)), k8 = int(i % (K / 8)), k = k8 * 8;
+    const uint8_t* b = src + (size_t(r) * (K / 32) + k / 32) * 34;
+    const float d = __half2float(__ushort_as_half(static_cast<unsigned short>(b[0] | (b[1] << 8))));
+    uint32_t oh[4], ol[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      uint32_t wh = 0, wl = 0;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float v = d * float(static_cast<int8_t>(b[2 + (k % 32) + 2 * j + e]));
+        const __half h = __float2half_rn(v);
+        const __half l = __float2half_rn(v - __half2float(h));
+        wh |= uint32_t(__half_as_ushort(h)) << (16 * e);
+        wl |= uint32_t(__half_as_ushort(l)) << (16 * e);
+      }
+      oh[j] = wh; ol[j] = wl;
+    }
+    const size_t o = packed_off(row0 + r, k, K);
+    *reinterpret_cast<uint4*>(hi + o) = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+    *reinterpret_cast<uint4*>(lo + o) = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+  }
+}
+
 __global__ void k_row_sumsq(const uint16_t* __restrict__ E, int cols, float* __restrict__ out, bool f16) {
   __shared__ float red[32];
   const uint16_t* row = E + size_t(blockIdx.x) * cols;
@@ -133,6 +165,10 @@ cudaError_t pack_rows(const void* src, int fmt, bool src_f16, int rows, int K, c
   } else {
     k_pack_q8<<<grid_for(size_t(rows) * (K / 32)), 256, 0, s>>>(static_cast<const uint8_t*>(src), rows, K,
                                                                  reinterpret_cast<int8_t*>(dst.w), dst.scale, row0);
+    if (dst.w16[0])
+      k_pack_q8_hilo<<<grid_for(size_t(rows) * (K / 8)), 256, 0, s>>>(
+          static_cast<const uint8_t*>(src), rows, K, reinterpret_cast<uint16_t*>(dst.w16[0]),
+          reinterpret_cast<uint16_t*>(dst.w16[1]), row0);
   }
   return cudaGetLastError();
 }

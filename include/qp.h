@@ -102,8 +102,11 @@ typedef struct qp_geometry {
  *         layout) but not Q8_0 over 16-bit ones.  Embedding tables (the
  *         code tables and the q0 table) accept QP_BF16 or QP_F16, one
  *         encoding for all of them; vectors (norms, bias) QP_F32.  A
- *         combination outside these is QP_ERR_WEIGHT_DTYPE.  Q8_0 layers
- *         are served by the tile engine only.
+ *         combination outside these is QP_ERR_WEIGHT_DTYPE.  A Q8_0
+ *         matrix is kept twice on the device: as its blocks (the tile
+ *         engine dequantises them on chip) and as two f16 images, hi =
+ *         f16(d*q) and lo = f16(d*q - hi), for the small-batch engine (4
+ *         more bytes per weight); hi + lo = d*q exactly for d >= 2^-14.
  * dev_ptr: device memory, row-major HF layout [shape[0], shape[1]]; a Q8_0
  *         tensor is its raw block stream, shape[0] rows of shape[1]/32
  *         blocks.  Vectors use shape = {n, 0}. */

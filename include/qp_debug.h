@@ -24,11 +24,12 @@ extern "C" {
  * every weight matrix into (128-row tile, 128-column K slice) units spread
  * over all SMs.  The tile engine serves any batch and both weight formats: a
  * completed tile is finished (residual, norm, SwiGLU, f16 operand) once by
- * the CTA whose partial completed it.  The small-batch engine serves bf16
- * weights with at most 64 frames per call: partials go straight into their
+ * the CTA whose partial completed it.  The small-batch engine serves both
+ * formats too (Q8_0 matrices as their f16 hi + lo images, two slices per
+ * unit) with at most 64 frames per call: partials go straight into their
  * destination and each consumer builds its operand slice from it, which
  * removes one dependent global round trip per GEMM.  QP_ENGINE_AUTO (the
- * default) takes the small-batch engine for bf16 calls of at most 40 frames,
+ * default) takes the small-batch engine for calls of at most 40 frames,
  * where it is the faster of the two on GB300, and the tile engine otherwise. */
 typedef enum {
   QP_ENGINE_AUTO = 0,
@@ -37,7 +38,8 @@ typedef enum {
 } qp_engine;
 
 /* Select the engine for later calls on h.  With QP_ENGINE_SMALL a call the
- * small-batch engine cannot serve (Q8_0 weights, more than 64 frames)
+ * small-batch engine cannot serve (more than 64 frames, sampling over a
+ * vocabulary above 4096, the deterministic schedule)
  * returns QP_ERR_ARG.  QP_ERR_ARG for a null handle or an unknown engine. */
 qp_status qp_set_engine(qp_handle* h, int engine);
 

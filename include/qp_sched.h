@@ -17,7 +17,8 @@
  * then steps 2..n_steps, feeding each step the code q_{k-1} it chose (or a
  * forced one), gets the codes and logits of qp_predict_frames.
  *
- * Served by the small-batch engine: bf16 weights, B <= 64 rows per call,
+ * Served by the small-batch engine: any weight format qp_load_weights
+ * accepts (Q8_0 matrices through their f16 hi + lo images), B <= 64 rows per call,
  * greedy decisions or Gumbel top-k sampling (the _ex calls).  A step call runs one step's layers over all its rows;
  * its output head holds one head matrix per distinct step among the rows
  * (the rows sorted into step groups), as one GEMM.  Slot and step arrays are HOST memory (a scheduler keeps
@@ -42,7 +43,7 @@ extern "C" {
  * state, out_q1[b] = the frame's first residual code (device [B] int32),
  * out_logits [B][vocab] f32 (device, or NULL).  QP_ERR_ARG for a bad B, a
  * slot outside [0, max_batch), repeated slots, null pointers, or a handle
- * this path cannot serve (not bf16, B > 64); QP_ERR_STATE without
+ * this path cannot serve (B > 64); QP_ERR_STATE without
  * weights.  Device errors latch in the status word as for
  * qp_predict_frames. */
 qp_status qp_begin_frames(qp_handle* h, int B, const int32_t* slots, const float* H, const int32_t* q0,

@@ -93,22 +93,26 @@ def test_small_refuses_what_it_cannot_serve(small, qpk):
     assert cp._lib.qp_set_engine(cp._h, 7) == 1   # unknown engine: QP_ERR_ARG
 
 
-def test_small_refuses_q8_0(qpk):
-    import torch
-    raw = S.make_weights(SMALL, seed=12, gemm_format="q8_0")
-    cp = qpk.CodePredictor(SMALL, max_batch=4)
-    cp.load_raw_weights(raw)
-    H = torch.zeros((4, SMALL.talker_hidden), device="cuda")
-    q0 = torch.zeros(4, dtype=torch.int32, device="cuda")
-    cp.set_engine("small")
-    with pytest.raises(qpk.QpError) as e:
-        cp.predict(H, q0)
-    assert e.value.code == 1
-    cp.set_engine("auto")                     # the tile engine serves it
-    cp.predict(H, q0)
-    torch.cuda.synchronize()
-    assert cp.device_status() == 0
-    cp.close()
+@pytest.mark.parametrize("B", [1, 5, 33])
+def test_small_engine_serves_q8_0(qpk, B):
+    """Q8_0 matrices on the small-batch engine, through the exact f16 pair
+    hi + lo packed at load time: every frame against the oracle's exact d*q
+    weights, and the two engines on the same handle agree."""
+    raw = S.make_weights(SMALL, seed=12, gemm_format="q8_0", norm_mode="perturbed")
+    P = O.Predictor.from_raw(SMALL, raw)
+    cp = qpk.CodePredictor(SMALL, max_batch=B)
+    try:
+        cp.load_raw_weights(raw)
+        H, q0 = S.toy_inputs(SMALL, B, seed=60 + B)
+        cp.set_engine("small")
+        assert_parity(check_parity(cp, P, H, q0, np.arange(B)))
+        _, l_small = run_gpu(cp, H, q0)
+        cp.set_engine("tile")
+        _, l_tile = run_gpu(cp, H, q0)
+        _, lmask = decided_prefix(l_small, l_tile)
+        assert np.abs(l_small - l_tile)[lmask].max() <= TOL
+    finally:
+        cp.close()
 
 
 @pytest.fixture(scope="module")

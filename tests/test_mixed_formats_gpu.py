@@ -72,16 +72,21 @@ def test_exporter_layout_wide_tables(qpk):
     _run(qpk, WIDE_SMALL, raw, 12, ["tile"])
 
 
-def test_small_engine_refuses_q8_0(qpk):
-    raw = S.make_weights(SMALL, seed=35, gemm_format="q8_0", head_format="f16")
-    cp = qpk.CodePredictor(SMALL, max_batch=4)
+@pytest.mark.parametrize("geometry,B", [("small", 6), ("wide", 3), ("full_wide", 1)])
+def test_small_engine_exporter_layout(qpk, geometry, B):
+    """The exporter's layout (Q8_0 matrices, f16 heads and tables; Talker-wide
+    tables) on the small-batch engine: Q8_0 slices as their f16 hi + lo pair,
+    16-bit head slices as they are."""
+    g = {"small": SMALL, "wide": WIDE_SMALL,
+         "full_wide": dataclasses.replace(S.Geometry(), code_embed_dim=S.Geometry().talker_hidden)}[geometry]
+    raw = S.make_weights(g, seed=35, gemm_format="q8_0", head_format="f16", embed_format="f16",
+                         norm_mode="perturbed")
+    cp = qpk.CodePredictor(g, max_batch=B)
     try:
         cp.load_raw_weights(raw)
         cp.set_engine("small")
-        import torch
-        H, q0 = S.toy_inputs(SMALL, 2, seed=1)
-        with pytest.raises(qpk.QpError):
-            cp.predict(torch.from_numpy(H).cuda(), torch.from_numpy(q0).cuda())
+        H, q0 = S.toy_inputs(g, B, seed=2)
+        assert_parity(check_parity(cp, O.Predictor.from_raw(g, raw), H, q0, np.arange(B)))
     finally:
         cp.close()
 

@@ -347,16 +347,25 @@ def test_state_slot_bad_codes_latch(small):
     assert cp.device_status() == 0
 
 
-def test_state_slots_need_16_bit_weights(qpk):
-    import torch
-    raw = S.make_weights(SMALL, seed=73, gemm_format="q8_0")
-    cp = qpk.CodePredictor(SMALL, max_batch=4)
+@pytest.mark.parametrize("sampled", [False, True])
+def test_state_slots_with_q8_0_weights(qpk, sampled):
+    """Q8_0 matrices in state-slot calls (the small-batch engine's hi + lo
+    images): a ragged schedule teacher-forced to the oracle's exact d*q
+    weights, greedy and sampled."""
+    raw = S.make_weights(SMALL, seed=73, gemm_format="q8_0", norm_mode="perturbed")
+    P = O.Predictor.from_raw(SMALL, raw)
+    cp = qpk.CodePredictor(SMALL, max_batch=16)
     try:
         cp.load_raw_weights(raw)
-        H = torch.zeros((2, SMALL.talker_hidden), device="cuda")
-        with pytest.raises(qpk.QpError) as e:
-            cp.begin_frames([0, 1], H, torch.zeros(2, dtype=torch.int32, device="cuda"))
-        assert e.value.code == 1
+        F = 18
+        H, q0 = S.toy_inputs(SMALL, F, seed=590)
+        samp = None
+        if sampled:
+            samp = (0.9, 40, S.gumbel_noise((F, SMALL.n_steps, SMALL.vocab), seed=13))
+        ref = O.predict_frames(P, H, q0, *(samp or (0.0, 0, None)), tol=TOL)
+        chk, _ = run_schedule(cp, SMALL, H, q0, ref, 77, sampling=samp)
+        assert chk.err <= TOL, chk.err
+        assert chk.mismatch == 0
     finally:
         cp.close()
 
