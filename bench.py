@@ -271,7 +271,7 @@ def time_oracle(g, raw, w, frames: int, budget_s: float):
 
 def config_of(g, w, world: int):
     """The workload's config, the same on both arms."""
-    return {"workload": w.name, "B": w.B, "steps_per_frame": g.n_steps, "engine": engine_of(w.B, w.gemm_format),
+    return {"workload": w.name, "B": w.B, "steps_per_frame": g.n_steps, "engine": engine_of(w.B, w.gemm_format, w.temperature > 0),
             "l2": f"flushed between timed iterations ({L2_FLUSH_BYTES >> 20} MB write)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
@@ -330,10 +330,13 @@ def whole_job(local_ms: float, frames_per_step: int, steps: int, world: int, dev
     return total_ms, world * frames_per_step * steps / (total_ms / 1e3)
 
 
-def engine_of(B: int, gemm_format: str) -> str:
-    """The schedule QP_ENGINE_AUTO picks (include/qp_debug.h): the small-batch
-    engine for calls of at most 40 frames (either weight format), the tile
-    engine otherwise."""
+def engine_of(B: int, gemm_format: str, sampled: bool = False) -> str:
+    """The schedule QP_ENGINE_AUTO picks (include/qp_debug.h) at the 1.7B
+    geometry: the cluster engine for greedy calls of at most 32 frames with
+    16-bit weights, else the small-batch engine for calls of at most 40
+    frames (either weight format), else the tile engine."""
+    if gemm_format == "bf16" and not sampled and B <= 32:
+        return "cluster"
     return "small" if B <= 40 else "tile"
 
 
@@ -373,7 +376,7 @@ def sweep(g, dev, stream, steps, hbm, tf):
         st = cp.device_status()
         cp.close()
         roof = roofline_of(g, w.B, w.gemm_format, samp is not None, ms, hbm, tf)
-        out[w.name] = {"B": w.B, "engine": engine_of(w.B, w.gemm_format), "ms_per_call": ms,
+        out[w.name] = {"B": w.B, "engine": engine_of(w.B, w.gemm_format, w.temperature > 0), "ms_per_call": ms,
                        "frames_per_s": w.B / (ms / 1e3),
                        "us_per_step": 1e3 * ms / g.n_steps, "roofline_bound": roof["bound"],
                        "roofline_frac": roof["frac"], "device_status": st}

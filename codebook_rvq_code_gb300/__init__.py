@@ -381,11 +381,11 @@ class CodePredictor:
                                                                   _stream_ptr(stream)))
         return out
 
-    ENGINES = {"auto": 0, "tile": 1, "small": 2}
+    ENGINES = {"auto": 0, "tile": 1, "small": 2, "cluster": 3}
 
     def set_engine(self, engine: str):
-        """Schedule for later calls (include/qp_debug.h): "auto", "tile" or
-        "small"."""
+        """Schedule for later calls (include/qp_debug.h): "auto", "tile",
+        "small" or "cluster"."""
         _check("qp_set_engine", self._lib.qp_set_engine(self._h, self.ENGINES[engine]))
 
     def set_deterministic(self, on: bool = True):

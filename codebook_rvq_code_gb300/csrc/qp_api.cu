@@ -1,5 +1,6 @@
 // C ABI of libqp: handle life cycle, weight validation and packing, and the
 // argument checks in front of the frame loop.  See include/qp.h.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -102,8 +103,13 @@ size_t matrix_bytes(int fmt, int64_t N, int64_t K) {
 // The engine that serves a call (qp_debug.h, qp_engine).
 qp_status run(qp_handle* h, const qp::RunArgs& a, cudaStream_t s) {
   if (h->deterministic) {   // the tile engine's deterministic schedule
-    if (h->engine == QP_ENGINE_SMALL) return QP_ERR_ARG;
+    if (h->engine == QP_ENGINE_SMALL || h->engine == QP_ENGINE_CLUSTER) return QP_ERR_ARG;
     return qp::run_frames_persistent(h, a, s);
+  }
+  if (h->engine == QP_ENGINE_CLUSTER || h->engine == QP_ENGINE_AUTO) {
+    const bool cl = qp::cluster_supported(h, a);
+    if (h->engine == QP_ENGINE_CLUSTER) return cl ? qp::run_frames_cluster(h, a, s) : QP_ERR_ARG;
+    if (cl) return qp::run_frames_cluster(h, a, s);
   }
   const bool sm = qp::small_supported(h, a);
   if (h->engine == QP_ENGINE_SMALL && !sm) return QP_ERR_ARG;
@@ -169,6 +175,16 @@ qp_status qp_create(const qp_geometry* gp, int max_batch, qp_handle** out) {
     return QP_ERR_OOM;
   }
   h->sarena_bytes = h->scr.total;
+  // the cluster engine's scratch, where it serves this geometry
+  if (qp::cluster_geometry_ok(g)) {
+    h->cmax_batch = std::min(max_batch, qp::kClusterMaxFrames);
+    if (cudaMalloc(&h->carena, qp::cluster_scratch_bytes(g, h->cmax_batch)) != cudaSuccess) {
+      cudaGetLastError();
+      cudaFree(h->sarena);
+      delete h;
+      return QP_ERR_OOM;
+    }
+  }
   // small fixed buffers: status word, RoPE table, host-entry staging
   const int ctx = g.n_steps + 1;
   const size_t fbytes = carve_size<int>(64) + carve_size<float2>(size_t(ctx) * 64) +
@@ -177,6 +193,7 @@ qp_status qp_create(const qp_geometry* gp, int max_batch, qp_handle** out) {
   if (cudaMalloc(&h->farena, fbytes) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(h->sarena);
+    if (h->carena) cudaFree(h->carena);
     delete h;
     return QP_ERR_OOM;
   }
@@ -199,6 +216,7 @@ qp_status qp_create(const qp_geometry* gp, int max_batch, qp_handle** out) {
       cudaMemset(h->status, 0, 64 * sizeof(int)) != cudaSuccess) {
     cudaGetLastError();
     cudaFree(h->sarena);
+    if (h->carena) cudaFree(h->carena);
     cudaFree(h->farena);
     delete h;
     return QP_ERR_CUDA;
@@ -522,7 +540,7 @@ qp_status qp_debug_waits(qp_handle* h, int wait_limit_us, int withhold_gemm) {
 }
 
 qp_status qp_set_engine(qp_handle* h, int engine) {
-  if (!h || engine < QP_ENGINE_AUTO || engine > QP_ENGINE_SMALL) return QP_ERR_ARG;
+  if (!h || engine < QP_ENGINE_AUTO || engine > QP_ENGINE_CLUSTER) return QP_ERR_ARG;
   h->engine = engine;
   return QP_OK;
 }
@@ -595,6 +613,7 @@ void qp_destroy(qp_handle* h) {
     if (h->trace) cudaFree(h->trace);
     if (h->warena) cudaFree(h->warena);
     if (h->sarena) cudaFree(h->sarena);
+    if (h->carena) cudaFree(h->carena);
     if (h->farena) cudaFree(h->farena);
   }
   delete h;

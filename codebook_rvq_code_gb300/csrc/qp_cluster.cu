@@ -1,0 +1,1115 @@
+// The Code Predictor frame loop for small batches on thread-block clusters:
+// one persistent kernel of 8-CTA clusters, scheduled so that most of a
+// layer's dependencies resolve inside a cluster.
+//
+// It computes what the other two schedules compute (the whole greedy frame
+// loop as one fixed GPU program over a preallocated KV cache for the short
+// bounded context: "テキスト音声合成モデルを50ミリ秒未満で応答させる方法",
+// section "Qwen3-TTSの最適化方法", item 3).  What differs is where partial
+// products meet.  A layer is two cluster jobs:
+//
+//   * attention, one cluster per kv head j: its 8 CTAs multiply the group's
+//     512 q|k|v weight rows (q heads 2j and 2j+1, k head j, v head j: four
+//     128-row tiles) by the normalised input, CTA r taking tile r/2 over
+//     half r%2 of K.  The partial products stay in each CTA's shared memory;
+//     each CTA then adds a frame's two halves straight out of its peers'
+//     shared memory (distributed shared memory), runs that frame's
+//     attention and writes the frame's output row into every peer's operand
+//     of the O projection.  CTA r multiplies O's 128-row tile r over the
+//     group's 256 columns and adds the result into the residual stream;
+//   * MLP, one cluster per 256 columns of the FFN: the gate and up tiles of
+//     those columns split the same way, SwiGLU from the peers' partials into
+//     every peer's down-projection operand, CTA r adds down's tile r over
+//     the 256 columns into the residual stream;
+//   * the head, one cluster per 512 logits (four tiles, two K halves): each
+//     CTA completes 64 logits per frame from its own and its partner's
+//     halves, writes them out if asked and folds their argmax into the
+//     frame's decision word with one 64-bit atomic max.
+//
+// A residual row's 1/RMS is known before its operand is built: each CTA
+// sums the squares of its K half and reads its partner's sum, so operands
+// are f16 of the normalised row (no range scaling needed there).  The only
+// grid-wide dependencies are the residual stream after O and after down
+// (counters in global memory, as in the other schedules) and the step's
+// decisions; cluster-local ones use an mbarrier in each CTA that every CTA
+// of the cluster arrives on.  Step 1's projection is spread over all CTAs
+// (partials added into the residual stream, each unit scaling its H slice
+// into f16's range by a power of two).
+//
+// Roles per CTA: warps 0-7 consume (operand builds, drains, attention,
+// SwiGLU, decisions), warp 8 streams weights, warp 9 issues the MMAs.  Every
+// wait is bounded and honours the grid-wide abort flag; no CTA leaves before
+// its whole cluster is done with its shared memory.
+#include <algorithm>
+#include <atomic>
+
+#include "qp_device.cuh"
+
+namespace qp {
+
+namespace {
+
+constexpr int kCl = 8;                        // CTAs per cluster
+constexpr int kClConsWarps = 8;
+constexpr int kClCons = kClConsWarps * 32;
+constexpr int kClProdWarp = 8;
+constexpr int kClMmaWarp = 9;
+constexpr int kClThreads = 10 * 32;
+constexpr int kClMaxRows = 64;                // activation rows of one GEMM (2B at step 1)
+constexpr int kClHold = 8;                    // input chunks a consumer thread keeps in registers
+
+constexpr uint32_t kClWSlot = kTileM * kKs * 2;       // one 128 x 128 f16 weight slice
+constexpr int kClNW = 5;                              // weight ring slots
+constexpr uint32_t kClOffW = 0;
+constexpr uint32_t kClOffOp = kClNW * kClWSlot;       // operand region (K half; then the partials)
+constexpr uint32_t kClOpBytes = 65536;
+constexpr uint32_t kClOffOp2 = kClOffOp + 32768;      // O / down operand (second half of the region)
+constexpr uint32_t kClOffMisc = kClOffOp + kClOpBytes;
+constexpr uint32_t kClTmemCols = 64;                  // one accumulator of up to 64 columns
+
+enum { CBAR_CONS = 1 };
+enum { T_PROJ = 0, T_QKV, T_O, T_GU, T_DOWN, T_HEAD };
+
+struct CMisc {
+  uint64_t wfull[kClNW], wempty[kClNW];
+  uint64_t opfull, accfull, mmadone;
+  uint64_t cbar[2];              // cluster syncs: one arrival from each CTA of the cluster
+  uint32_t tmem_base;
+  int flag[2];                   // a wait's outcome for all consumers (alternating: a fast thread's next
+                                 // wait may write before a slow one has read the last)
+  float ssw[kClConsWarps][kClMaxRows / 4];   // per-warp partial sums of squares of one pass's rows
+  float ssx[kClMaxRows];         // this CTA's K-half sums of squares per row (its partner reads them)
+  float inv[kClMaxRows];         // per row: the factor a drain applies (2^e / RMS, or 2^e for the projection)
+  float rsc[kClMaxRows];         // per row: 2^-e, the operand's range scale
+  int code[kClMaxRows];          // step k >= 2: the code each frame's input embeds
+};
+
+// dynamic shared memory (with 1 KB for aligning its base) within the 227 KB a CTA may use
+static_assert(kClOffMisc + sizeof(CMisc) + 1024 <= 227 * 1024, "shared memory layout too large");
+
+struct CLayer {
+  const uint16_t* w[4];    // qkv, o, gu, down: tile-packed f16 (qp_weights.cu)
+  const float* attn_norm; const float* q_norm; const float* k_norm; const float* ffn_norm;
+};
+
+struct CParams {
+  int d, qw, kvw, F, V, th, L, n_kv, n_steps, q0_vocab;
+  float eps;
+  bool embed_f16;
+  const uint16_t* w_proj; const float* b_proj; const uint16_t* e0;
+  CLayer layer[kMaxLayers];
+  const float* out_norm;
+  const uint16_t* embed[kMaxSteps];
+  const uint16_t* w_head[kMaxSteps];
+  const float2* rope_cs;
+  // scratch
+  float* x;                // residual streams [step][2B][d], zeroed per call
+  uint16_t* kv;            // f16 [layer][frame][pos][k|v][kv_width]
+  unsigned* proj_done;     // [1]: projection units finished
+  unsigned* att_done;      // [step][layer]: attention CTAs finished (O added)
+  unsigned* mlp_done;      // [step][layer]: MLP CTAs finished (down added)
+  unsigned* head_done;     // [step]: head CTAs finished (decisions folded in)
+  unsigned long long* best;   // [step][frame]: packed (logit, index) maximum
+  int* abort_flag; int* status;
+  long long spin_limit;
+  int withhold;            // testing (qp_debug.h): >= 0 makes CTA 0 skip its first attention count
+  unsigned long long* trace; int trace_n;   // event log (qp_debug.h), or null
+  // jobs
+  int n_cl;                // clusters in the grid
+  int n_att, n_mlp, n_head, n_proj;   // jobs of each kind (projection: units over all CTAs)
+  // call
+  int B;
+  const float* H; const int32_t* q0; int32_t* out_codes; float* out_logits; const int32_t* forced;
+};
+
+// ------------------------------------------------------------ cluster PTX
+__device__ __forceinline__ uint32_t cl_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// The address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cl_map(uint32_t a, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cl_arrive_remote(uint32_t cl_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
+}
+__device__ __forceinline__ bool cl_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ float4 cl_ld4(uint32_t a) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ float cl_ld1(uint32_t a) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
+  return v;
+}
+__device__ __forceinline__ void cl_st2(uint32_t a, uint2 v) {
+  asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(v.x), "r"(v.y) : "memory");
+}
+// Hardware barrier of every thread of the cluster.
+__device__ __forceinline__ void cl_barrier_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Generic-proxy writes to shared memory of any CTA of the cluster made
+// visible to the tensor cores' reads.
+__device__ __forceinline__ void fence_proxy_async_cluster() {
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+}
+
+// ------------------------------------------------------------ tracing
+// Per-CTA event log after the section stamps: consumer events in [0, 8192),
+// MMA-warp events in [8192, 16384); one word = (globaltimer ns mod 2^48) <<
+// 16 | code << 12 | task index.  Compiled in only with QP_TRACE.
+enum {
+  CEV_START = 1, CEV_READY = 2, CEV_SSYNC = 3, CEV_OPREADY = 4, CEV_ACC = 5, CEV_S1 = 6, CEV_WORK = 7,
+  CEV_S3 = 8, CEV_PUB = 9, CEV_WWAIT = 10, CEV_WREADY = 11, CEV_COMMIT = 12, CEV_MOP = 13, CEV_SUB = 14
+};
+#ifdef QP_TRACE
+__device__ __forceinline__ void cl_ev(const CParams& p, unsigned& idx, int base, int code, int task) {
+  if (p.trace && idx < 8192) {
+    unsigned long long* b = p.trace + size_t(p.trace_n) * gridDim.x * 2 + size_t(blockIdx.x) * 16384 + base;
+    b[idx++] = ((globaltimer_ns() & 0xFFFFFFFFFFFFull) << 16) | (unsigned long long)(code & 15) << 12 |
+               unsigned(task & 4095);
+  }
+}
+#else
+__device__ __forceinline__ void cl_ev(const CParams&, unsigned&, int, int, int) {}
+#endif
+
+// --------------------------------------------------------------- program
+// A CTA's tasks, in the order every role walks them.  Per step k: step 1's
+// projection units, then per layer this cluster's attention jobs (a QKV and
+// an O task each) and MLP jobs (gate/up and down), then its head jobs.
+struct Task {
+  int kind, k, l, job;
+};
+// Jobs of each kind are dealt to clusters round-robin; MLP jobs from the
+// last cluster down, so that clusters with an attention job take fewer.
+__device__ __forceinline__ int n_mine(int n_jobs, int n_cl, int c) { return c < n_jobs % n_cl ? n_jobs / n_cl + 1 : n_jobs / n_cl; }
+__device__ __forceinline__ int cl_proj_units(const CParams& p) {
+  const int g = blockIdx.x, G = gridDim.x;
+  return g < p.n_proj ? (p.n_proj - 1 - g) / G + 1 : 0;
+}
+struct Prog {
+  int c, na, nm, nh, np, per_layer, per_step;
+};
+__device__ __forceinline__ Prog cl_prog(const CParams& p) {
+  Prog g;
+  g.c = int(blockIdx.x) / kCl;
+  g.na = n_mine(p.n_att, p.n_cl, g.c);
+  g.nm = n_mine(p.n_mlp, p.n_cl, p.n_cl - 1 - g.c);
+  g.nh = n_mine(p.n_head, p.n_cl, g.c);
+  g.np = cl_proj_units(p);
+  g.per_layer = 2 * (g.na + g.nm);
+  g.per_step = p.L * g.per_layer + g.nh;
+  return g;
+}
+__device__ __forceinline__ int cl_n_tasks(const CParams& p, const Prog& g) { return g.np + p.n_steps * g.per_step; }
+__device__ Task cl_task(const CParams& p, const Prog& g, int i) {
+  Task t{};
+  if (i < g.np) {
+    t.kind = T_PROJ; t.k = 1; t.l = 0; t.job = int(blockIdx.x) + i * int(gridDim.x);
+    return t;
+  }
+  i -= g.np;
+  t.k = 1 + i / g.per_step;
+  i %= g.per_step;
+  if (i >= p.L * g.per_layer) {
+    t.kind = T_HEAD; t.l = p.L; t.job = g.c + (i - p.L * g.per_layer) * p.n_cl;
+    return t;
+  }
+  t.l = i / g.per_layer;
+  i %= g.per_layer;
+  if (i < 2 * g.na) {
+    t.kind = (i & 1) ? T_O : T_QKV;
+    t.job = g.c + (i >> 1) * p.n_cl;
+  } else {
+    i -= 2 * g.na;
+    t.kind = (i & 1) ? T_DOWN : T_GU;
+    t.job = (p.n_cl - 1 - g.c) + (i >> 1) * p.n_cl;
+  }
+  return t;
+}
+
+// Activation rows of a task's GEMM.
+__device__ __forceinline__ int cl_rows(const CParams& p, const Task& t) {
+  if (t.kind == T_HEAD) return p.B;
+  return t.k == 1 ? 2 * p.B : p.B;
+}
+__device__ __forceinline__ int cl_npad(int R) { return (R + 15) & ~15; }
+// The MMA of a task: its weight slices (0 = none: an O or down task whose
+// tile this CTA does not have).
+__device__ __forceinline__ int cl_nsl(const CParams& p, const Task& t) {
+  const int r = int(cl_rank());
+  switch (t.kind) {
+    case T_PROJ: return 1;
+    case T_O: case T_DOWN: return r < p.d / kTileM ? 2 : 0;
+    default: return p.d / 256;
+  }
+}
+// Weight slice s of the task's unit: tile `mt` of the matrix, K slice `ks`.
+__device__ __forceinline__ const uint8_t* cl_slice(const CParams& p, const Task& t, int s) {
+  const int r = int(cl_rank()), tq = r >> 1, h = r & 1, nkh = p.d / 256;
+  const uint16_t* w;
+  int mt, ks, K;
+  switch (t.kind) {
+    case T_PROJ: {
+      const int nks = p.th / kKs;
+      w = p.w_proj; K = p.th; mt = t.job / nks; ks = t.job % nks;
+      break;
+    }
+    case T_QKV: {
+      const int j = t.job;
+      const int tiles[4] = {2 * j, 2 * j + 1, p.qw / kTileM + j, (p.qw + p.kvw) / kTileM + j};
+      w = p.layer[t.l].w[0]; K = p.d; mt = tiles[tq]; ks = h * nkh + s;
+      break;
+    }
+    case T_O:
+      w = p.layer[t.l].w[1]; K = p.qw; mt = r; ks = 2 * t.job + s;
+      break;
+    case T_GU: {
+      const int m = t.job, fq = p.F / kTileM;
+      const int tiles[4] = {2 * m, 2 * m + 1, fq + 2 * m, fq + 2 * m + 1};
+      w = p.layer[t.l].w[2]; K = p.d; mt = tiles[tq]; ks = h * nkh + s;
+      break;
+    }
+    case T_DOWN:
+      w = p.layer[t.l].w[3]; K = p.F; mt = r; ks = 2 * t.job + s;
+      break;
+    default:   // T_HEAD
+      w = p.w_head[t.k - 1]; K = p.d; mt = 4 * t.job + tq; ks = h * nkh + s;
+      break;
+  }
+  return reinterpret_cast<const uint8_t*>(w) + (size_t(mt) * K * kTileM + size_t(ks) * kTileM * kKs) * 2;
+}
+// Operand slice s of the task in shared memory.
+__device__ __forceinline__ uint32_t cl_op_off(const Task& t, int s, uint32_t opsz) {
+  return ((t.kind == T_O || t.kind == T_DOWN) ? kClOffOp2 : kClOffOp) + uint32_t(s) * opsz;
+}
+
+// ---------------------------------------------------------------- producer
+__device__ void cl_producer(const CParams& p, CMisc& ms, uint8_t* smem) {
+  const uint64_t pol = policy_evict_first();
+  const Prog g = cl_prog(p);
+  const int n = cl_n_tasks(p, g);
+  uint32_t it = 0;
+  for (int i = 0; i < n; ++i) {
+    const Task t = cl_task(p, g, i);
+    const int nsl = cl_nsl(p, t);
+    for (int s = 0; s < nsl; ++s) {
+      const uint32_t slot = it % kClNW, u = it / kClNW;
+      if (u > 0 && !mwait(p, &ms.wempty[slot], (u - 1) & 1)) goto drain;
+      mbar_expect_tx(&ms.wfull[slot], kClWSlot);
+      bulk_g2s_stream(smem + kClOffW + slot * kClWSlot, cl_slice(p, t, s), kClWSlot, &ms.wfull[slot], pol);
+      ++it;
+    }
+  }
+drain:
+  for (uint32_t k = it > uint32_t(kClNW) ? it - kClNW : 0; k < it; ++k) mbar_wait(&ms.wfull[k % kClNW], (k / kClNW) & 1);
+}
+
+// --------------------------------------------------------------- MMA warp
+__device__ void cl_mma(const CParams& p, CMisc& ms, uint8_t* smem) {
+  const Prog g = cl_prog(p);
+  const int n = cl_n_tasks(p, g);
+  uint32_t wit = 0, opseq = 0;
+  unsigned evi = 0;
+  for (int i = 0; i < n; ++i) {
+    const Task t = cl_task(p, g, i);
+    const int nsl = cl_nsl(p, t);
+    if (nsl == 0) continue;
+    const int np = cl_npad(cl_rows(p, t));
+    const uint32_t idesc = idesc_f16(kTileM, np);
+    const uint32_t blb = uint32_t(np / 8) * 128, opsz = uint32_t(np) * kKs * 2;
+    // the task's weight slices first (usually there long before the operand):
+    // a wait between MMAs stalls the issuing thread while the tensor pipe drains
+    for (int s = 0; s < nsl; ++s) {
+      const uint32_t w = wit + uint32_t(s);
+      if (mbar_try_wait(&ms.wfull[w % kClNW], (w / kClNW) & 1)) {
+        cl_ev(p, evi, 8192, CEV_WREADY, i);
+      } else {
+        if (!mwait(p, &ms.wfull[w % kClNW], (w / kClNW) & 1)) goto out;
+        cl_ev(p, evi, 8192, CEV_WWAIT, i);
+      }
+    }
+    if (!mwait(p, &ms.opfull, opseq & 1)) goto out;
+    cl_ev(p, evi, 8192, CEV_MOP, i);
+    tc_fence_after();
+    for (int s = 0; s < nsl; ++s) {
+      const uint32_t ws = wit % kClNW;
+      const uint32_t a0 = smem_u32(smem + kClOffW + ws * kClWSlot);
+      const uint32_t b0 = smem_u32(smem + cl_op_off(t, s, opsz));
+#pragma unroll
+      for (int j = 0; j < kKs / 16; ++j) {
+        const uint64_t ad = smem_desc(a0 + uint32_t(j) * 2 * (kTileM / 8) * 128, (kTileM / 8) * 128, 128);
+        const uint64_t bd = smem_desc(b0 + uint32_t(j) * 2 * blb, blb, 128);
+        mma_f16(ms.tmem_base, ad, bd, idesc, (s == 0 && j == 0) ? 0u : 1u);
+      }
+      mma_commit(&ms.wempty[ws]);
+      ++wit;
+    }
+    mma_commit(&ms.accfull);
+    cl_ev(p, evi, 8192, CEV_COMMIT, i);
+    ++opseq;
+  }
+out:
+  mma_commit(&ms.mmadone);
+  mbar_wait(&ms.mmadone, 0);
+}
+
+// ------------------------------------------------------ consumer helpers
+struct CState {
+  uint32_t opseq;   // tasks whose MMA ran
+  uint32_t cseq;    // cluster syncs passed
+  uint32_t fseq;    // waits whose outcome went through ms.flag
+  int r;            // rank in the cluster
+  int task;         // the task in progress (event log)
+  unsigned evi;     // events logged (thread 0)
+};
+__device__ __forceinline__ void cev(const CParams& p, CState& st, int code) {
+  if (threadIdx.x == 0) cl_ev(p, st.evi, 0, code, st.task);
+}
+
+// Bounded wait for the cluster sync in flight (acquire at cluster scope).
+template <class Par>
+__device__ bool cl_mwait(const Par& p, uint64_t* bar, uint32_t parity) {
+  if (cl_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (unsigned it = 1;; ++it) {
+    if (cl_try_wait(bar, parity)) return true;
+    if ((it & 255) == 0) {
+      if (aborted(p)) return false;
+      if (clock64() - t0 > p.spin_limit) { abort_all(p); return false; }
+    }
+  }
+}
+// Every consumer thread of every CTA of the cluster reaches this point
+// before any goes on; the writes before it (shared memory of any CTA of the
+// cluster, and global memory) are visible after it.  Thread i < 8 arrives on
+// CTA i's barrier after this CTA's consumers meet; thread 0 waits on this
+// CTA's and the consumers meet again.
+__device__ bool cl_sync(const CParams& p, CMisc& ms, CState& st) {
+  named_bar(CBAR_CONS, kClCons);
+  const int t = threadIdx.x;
+  uint64_t* bar = &ms.cbar[st.cseq & 1];
+  if (t < kCl) cl_arrive_remote(cl_map(smem_u32(bar), uint32_t(t)));
+  int* f = &ms.flag[st.fseq++ & 1];
+  if (t == 0) *f = cl_mwait(p, bar, (st.cseq >> 1) & 1);
+  named_bar(CBAR_CONS, kClCons);
+  ++st.cseq;
+  return *f != 0;
+}
+
+// One thread waits on a global counter; the consumers meet and read after.
+__device__ bool cl_wait_ctr(const CParams& p, CMisc& ms, CState& st, const unsigned* ctr, unsigned want) {
+  int* f = &ms.flag[st.fseq++ & 1];
+  if (threadIdx.x == 0) *f = poll_geq(p, ctr, want);
+  cev(p, st, CEV_READY);
+  named_bar(CBAR_CONS, kClCons);
+  return *f != 0;
+}
+__device__ bool cl_wait_acc(const CParams& p, CMisc& ms, CState& st) {
+  int* f = &ms.flag[st.fseq++ & 1];
+  if (threadIdx.x == 0) *f = mwait(p, &ms.accfull, st.opseq & 1);
+  cev(p, st, CEV_ACC);
+  named_bar(CBAR_CONS, kClCons);
+  ++st.opseq;
+  tc_fence_after();
+  return *f != 0;
+}
+// The operand is complete in shared memory: hand it to the MMA warp.
+__device__ __forceinline__ void cl_op_ready(const CParams& p, CMisc& ms, CState& st) {
+  fence_proxy_async_shared();
+  named_bar(CBAR_CONS, kClCons);
+  if (threadIdx.x == 0) mbar_arrive(&ms.opfull);
+  cev(p, st, CEV_OPREADY);
+}
+// Publish this CTA's count on `ctr` after every consumer's global writes.
+__device__ __forceinline__ void cl_publish(const CParams& p, CState& st, unsigned* ctr) {
+  named_bar(CBAR_CONS, kClCons);
+  if (threadIdx.x == 0) {
+    fence_acq_rel_gpu();
+    red_relaxed_add(ctr, 1u);
+  }
+  cev(p, st, CEV_PUB);
+}
+
+__device__ __forceinline__ void ld8f(const float* src, float (&v)[8]) {
+  const float4 a = __ldcg(reinterpret_cast<const float4*>(src)), b = __ldcg(reinterpret_cast<const float4*>(src + 4));
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+__device__ __forceinline__ void ld8e(const uint16_t* src, bool f16, float (&v)[8]) {
+  const uint4 e = __ldg(reinterpret_cast<const uint4*>(src));
+  const uint32_t w[4] = {e.x, e.y, e.z, e.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) { v[2 * i] = e16_to_f32(w[i], f16); v[2 * i + 1] = e16_to_f32(w[i] >> 16, f16); }
+}
+__device__ __forceinline__ uint4 pack8h(const float (&v)[8]) {
+  const uint2 a = pack4_f16(v[0], v[1], v[2], v[3]), b = pack4_f16(v[4], v[5], v[6], v[7]);
+  return make_uint4(a.x, a.y, b.x, b.y);
+}
+// u16 index of operand element (row n, column k in its 128-column slice),
+// the K-major core-matrix image [16 k groups][npad/8][8 rows][8 k].
+__device__ __forceinline__ uint32_t op_idx(int n, int k, int n8) {
+  return uint32_t(((k >> 3) * n8 + (n >> 3)) * 64 + (n & 7) * 8 + (k & 7));
+}
+
+// The 8 input values at column `col` of row n of a normalised GEMM's input:
+// the residual row, or at step k >= 2 layer 0 the frame's code embedding.
+struct InSrc {
+  const float* x;          // residual rows (row stride d), or null
+  const uint16_t* emb;     // the step's code table (embedding rows), or null
+  int row_mul, row_add;    // residual row = n * row_mul + row_add
+};
+__device__ __forceinline__ void in_load8(const CParams& p, const CMisc& ms, const InSrc& in, int n, int col,
+                                         float (&v)[8]) {
+  if (in.emb) ld8e(in.emb + size_t(ms.code[n]) * p.d + col, p.embed_f16, v);
+  else ld8f(in.x + size_t(n * in.row_mul + in.row_add) * p.d + col, v);
+}
+
+// Build the operand of a normalised GEMM over this CTA's K half: rows
+// n < R of input * w_norm * 2^-e, as f16, into slices 0..nkh-1 of the
+// operand region, e from this half's mean square (qp_device.cuh,
+// range_exp), and hand it to the MMA warp.  While the MMAs run, the row's
+// 1/RMS follows from this half's sum of squares and the partner's (a
+// cluster sync); the drain applies 2^e / RMS to the partial products.
+// Thread t takes column chunk t % CH (8 columns) of rows t / CH + RP * i.
+__device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const InSrc& in,
+                              const float* wn, int R) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int half = p.d / 2, CH = half / 8, RP = kClCons / CH, c = t % CH, h = st.r & 1;
+  const int col = h * half + c * 8;   // global column
+  const int passes = (R + RP - 1) / RP;
+  const int np = cl_npad(R), n8 = np / 8;
+  const uint32_t opsz = uint32_t(np) * kKs * 2;
+  float hold[kClHold][8];
+  // pass 1: sums of squares, the first kClHold chunks kept in registers
+  // (their loads all in flight together); a warp's 32 lanes all belong to
+  // one row (CH >= 32)
+#pragma unroll
+  for (int i = 0; i < kClHold; ++i) {
+    const int n = t / CH + RP * i;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) hold[i][e] = 0.f;
+    if (i < passes && n < R) in_load8(p, ms, in, n, col, hold[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < kClHold; ++i) {
+    if (i < passes) {   // warp-uniform
+      float ss = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) ss += hold[i][e] * hold[i][e];
+      ss = warp_sum(ss);
+      if (lane == 0) ms.ssw[warp][i] = ss;
+    }
+  }
+  for (int i = kClHold; i < passes; ++i) {
+    const int n = t / CH + RP * i;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (n < R) in_load8(p, ms, in, n, col, v);
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss += v[e] * v[e];
+    ss = warp_sum(ss);
+    if (lane == 0) ms.ssw[warp][i] = ss;
+  }
+  named_bar(CBAR_CONS, kClCons);
+  if (t < R) {
+    const int slot = t % RP, i = t / RP, w0 = slot * CH / 32;
+    float s = 0.f;
+    for (int w = 0; w < CH / 32; ++w) s += ms.ssw[w0 + w][i];
+    ms.ssx[t] = s;
+    ms.rsc[t] = exp2i(-range_exp(s / float(half)));
+  }
+  named_bar(CBAR_CONS, kClCons);
+  // pass 2: f16(x * w * 2^-e) into the operand slices
+  const float4 w0 = __ldg(reinterpret_cast<const float4*>(wn + col));
+  const float4 w1 = __ldg(reinterpret_cast<const float4*>(wn + col + 4));
+  const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+  const int kl = c * 8, s = kl / kKs, kk = kl % kKs;
+  uint16_t* op = reinterpret_cast<uint16_t*>(smem + kClOffOp + uint32_t(s) * opsz);
+#pragma unroll
+  for (int i = 0; i < kClHold; ++i) {
+    const int n = t / CH + RP * i;
+    if (i < passes && n < R) {
+      const float sc = ms.rsc[n];
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) v[e] = hold[i][e] * sc * w[e];
+      *reinterpret_cast<uint4*>(op + op_idx(n, kk, n8)) = pack8h(v);
+    }
+  }
+  for (int i = kClHold; i < passes; ++i) {
+    const int n = t / CH + RP * i;
+    if (n >= R) break;
+    float v[8];
+    in_load8(p, ms, in, n, col, v);
+    const float sc = ms.rsc[n];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] *= sc * w[e];
+    *reinterpret_cast<uint4*>(op + op_idx(n, kk, n8)) = pack8h(v);
+  }
+  cl_op_ready(p, ms, st);
+  // the rows' 1/RMS from both halves, while the MMAs run; the drain's
+  // barrier publishes ms.inv
+  if (!cl_sync(p, ms, st)) return false;
+  cev(p, st, CEV_SSYNC);
+  if (t < R) {
+    const float other = cl_ld1(cl_map(smem_u32(&ms.ssx[t]), uint32_t(st.r ^ 1)));
+    ms.inv[t] = rsqrtf((ms.ssx[t] + other) / float(p.d) + p.eps) / ms.rsc[t];
+  }
+  return true;
+}
+
+// Drain the accumulator (128 weight rows x R activation rows) into this
+// CTA's partial buffer part[n][m] (f32, at the start of the operand region,
+// whose operand the MMAs have finished reading), each activation row n
+// scaled by ms.inv[n].
+__device__ bool cl_drain_part(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, int R) {
+  if (!cl_wait_acc(p, ms, st)) return false;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ch = warp >> 2;
+  float* part = reinterpret_cast<float*>(smem + kClOffOp);
+  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {   // warp-uniform
+    float v[8];
+    tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (col + i < R) part[(col + i) * kTileM + q * 32 + lane] = v[i] * ms.inv[col + i];
+  }
+  tc_fence_before();
+  return true;
+}
+
+// Drain the accumulator of an O or down tile (rows m0 .. m0+127 of the
+// residual stream) into the residual rows n < R: one reduction per value,
+// a warp's 32 lanes on 32 consecutive features.  emb: also add the frame's
+// code embedding (step k >= 2, layer 0, first kv group).
+__device__ bool cl_drain_resid(const CParams& p, CMisc& ms, CState& st, float* xrows, int R, int m0,
+                               const uint16_t* emb) {
+  if (!cl_wait_acc(p, ms, st)) return false;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ch = warp >> 2;
+  const int m = m0 + q * 32 + lane;
+  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {
+    float v[8];
+    tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int n = col + i;
+      if (n < R) {
+        float a = v[i];
+        if (emb) {
+          const uint16_t e = emb[size_t(ms.code[n]) * p.d + m];
+          a += p.embed_f16 ? f16_bits_to_f32(e) : bf16_bits_to_f32(e);
+        }
+        red_add_f32(xrows + size_t(n) * p.d + m, a);
+      }
+    }
+  }
+  tc_fence_before();
+  return true;
+}
+
+// ------------------------------------------------------------ the tasks
+// Step 1's projection unit u (tile u / (th/128), K slice u % (th/128)):
+// rows 2b = H_b and 2b+1 = E0[q0_b], the first two positions of frame b (H
+// and q0 feed the residual loop: "拆解 Qwen3-TTS：OpenVINO 移植过程中的图分离
+// 与调度实践", section 1; their order is a reading).  Each row's slice is
+// scaled by 2^-e into f16's range (e from the slice's mean square) and the
+// partial product by 2^e; the K slice 0 unit adds the bias.
+__device__ bool cl_proj(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
+  const int t = threadIdx.x, R = 2 * p.B, np = cl_npad(R), n8 = np / 8;
+  const int nks = p.th / kKs, mt = tk.job / nks, ks = tk.job % nks;
+  uint16_t* op = reinterpret_cast<uint16_t*>(smem + kClOffOp);
+  const int c = t & 15, kl = c * 8;
+  for (int n = t >> 4; n < np; n += kClCons / 16) {   // warp-uniform: np is a multiple of 16
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (n < R) {
+      const int b = n >> 1;
+      if ((n & 1) == 0) {
+        const float* hr = p.H + size_t(b) * p.th + ks * kKs + kl;
+        const float4 a = __ldg(reinterpret_cast<const float4*>(hr));
+        const float4 e = __ldg(reinterpret_cast<const float4*>(hr + 4));
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = e.x; v[5] = e.y; v[6] = e.z; v[7] = e.w;
+      } else {
+        int q = p.q0[b];
+        if (q < 0 || q >= p.q0_vocab) {
+          if (c == 0 && mt == 0 && ks == 0) set_status(p.status, QP_ERR_BAD_TOKEN);
+          q = q < 0 ? 0 : p.q0_vocab - 1;
+        }
+        ld8e(p.e0 + size_t(q) * p.th + ks * kKs + kl, p.embed_f16, v);
+      }
+    }
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss += v[e] * v[e];
+#pragma unroll
+    for (int o = 8; o >= 1; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const int ex = range_exp(ss / float(kKs));
+    const float sc = exp2i(-ex);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) v[e] *= sc;
+    if (n < R) {
+      *reinterpret_cast<uint4*>(op + op_idx(n, kl, n8)) = pack8h(v);
+      if (c == 0) ms.inv[n] = exp2i(ex);
+    }
+  }
+  cl_op_ready(p, ms, st);
+  if (!cl_wait_acc(p, ms, st)) return false;
+  const int warp = t >> 5, lane = t & 31, q = warp & 3, ch = warp >> 2, m = mt * kTileM + q * 32 + lane;
+  const float bias = ks == 0 ? p.b_proj[m] : 0.f;
+  float* x1 = p.x;
+  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {
+    float v[8];
+    tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (col + i < R) red_add_f32(x1 + size_t(col + i) * p.d + m, v[i] * ms.inv[col + i] + bias);
+  }
+  tc_fence_before();
+  cl_publish(p, st, p.proj_done);
+  return true;
+}
+
+__device__ __forceinline__ float* cl_x(const CParams& p, int k) { return p.x + size_t(k - 1) * 2 * p.B * p.d; }
+
+// The wait before a step's layer-l attention job and where its input rows
+// come from.  Step k >= 2, layer 0: the previous step's decisions (each
+// frame's code, or the forced one) select the code embedding rows.
+__device__ bool cl_att_input(const CParams& p, CMisc& ms, CState& st, const Task& tk, InSrc& in) {
+  const int k = tk.k, l = tk.l;
+  in.x = cl_x(p, k); in.emb = nullptr; in.row_mul = 1; in.row_add = 0;
+  if (l > 0) return cl_wait_ctr(p, ms, st, p.mlp_done + (k - 1) * p.L + (l - 1), unsigned(p.n_mlp * kCl));
+  if (k == 1) return cl_wait_ctr(p, ms, st, p.proj_done, unsigned(p.n_proj));
+  if (!cl_wait_ctr(p, ms, st, p.head_done + (k - 2), unsigned(p.n_head * kCl))) return false;
+  const int t = threadIdx.x;
+  if (t < p.B) {
+    int code = unpack_argmax_index(__ldcg(p.best + size_t(k - 2) * p.B + t));
+    if (p.forced) code = p.forced[size_t(t) * p.n_steps + (k - 2)];
+    if (code < 0 || code >= p.V) {
+      set_status(p.status, QP_ERR_BAD_TOKEN);
+      code = code < 0 ? 0 : p.V - 1;
+    }
+    ms.code[t] = code;
+  }
+  named_bar(CBAR_CONS, kClCons);
+  in.x = nullptr;
+  in.emb = p.embed[k - 2];
+  return true;
+}
+
+// Attention job j of layer l at step k, through the O operand: the QKV
+// GEMM over this CTA's tile and K half, then for the frames b = r (mod 8),
+// one warp per (frame, q head), the frame's q|k|v from the peers' partials,
+// per-head RMSNorm and RoPE of the new position(s), KV append (by the head-0
+// warp), causal softmax over positions 0..pos and the head's output written
+// into every peer's O operand.  Lane l holds dims 4l..4l+3 of every
+// 128-vector; the scores of 16 positions are 16 partial dot products per
+// lane, summed by one reduce-scatter.
+__device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
+  const int k = tk.k, l = tk.l, j = tk.job, R = cl_rows(p, tk), np = cl_npad(R), n8 = np / 8;
+  InSrc in;
+  if (!cl_att_input(p, ms, st, tk, in)) return false;
+  if (!cl_build_norm(p, ms, st, smem, in, p.layer[l].attn_norm, R)) return false;
+  if (!cl_drain_part(p, ms, st, smem, R)) return false;
+  if (!cl_sync(p, ms, st)) return false;
+  cev(p, st, CEV_S1);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, hh = warp & 1;
+  const int P = k == 1 ? 2 : 1, ctx = p.n_steps + 1, pos0 = k == 1 ? 0 : k;
+  const float scale = rsqrtf(float(kHeadDim));
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  const CLayer& L = p.layer[l];
+  const uint32_t part0 = smem_u32(smem + kClOffOp) + uint32_t(lane) * 16;
+  const uint32_t opsz = uint32_t(np) * kKs * 2;
+  const uint32_t o0 = smem_u32(smem + kClOffOp2) + uint32_t(hh) * opsz;
+  uint16_t* kvl = p.kv + size_t(l) * p.B * ctx * 2 * p.kvw;
+  // warp w: q head hh = w % 2 of frames b = r + 8 (w / 2) (mod 32)
+  for (int b = st.r + kCl * (warp >> 1); b < p.B; b += kCl * (kClConsWarps / 2)) {
+    uint16_t* kvb = kvl + size_t(b) * ctx * 2 * p.kvw + j * kHeadDim + lane * 4;   // + (pos*2 + {0,1}) * kvw
+    // the positions of earlier steps, from the cache (written by this CTA's head-0 warps)
+    uint2 kh[kMaxCtx], vh[kMaxCtx];
+#pragma unroll
+    for (int tt = 0; tt < kMaxCtx; ++tt) {
+      kh[tt] = tt < pos0 ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(tt) * 2 + 0) * p.kvw)) : make_uint2(0, 0);
+      vh[tt] = tt < pos0 ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(tt) * 2 + 1) * p.kvw)) : make_uint2(0, 0);
+    }
+    float4 kprev = z4, vprev = z4;   // step 1: position 0's k and v, for position 1
+    for (int pp = 0; pp < P; ++pp) {
+      const int n = b * P + pp, pos = pos0 + pp;
+      // the frame's q (head hh), k and v: the two K halves of tiles hh, 2 and 3
+      float4 v4[3];
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        const int tq = i == 0 ? hh : i + 1;
+        const uint32_t a = part0 + uint32_t(n) * kTileM * 4;
+        const float4 h0 = cl_ld4(cl_map(a, uint32_t(2 * tq)));
+        const float4 h1 = cl_ld4(cl_map(a, uint32_t(2 * tq + 1)));
+        v4[i] = make_float4(h0.x + h1.x, h0.y + h1.y, h0.z + h1.z, h0.w + h1.w);
+      }
+      if (lane == 0 && threadIdx.x == 0) cl_ev(p, st.evi, 0, CEV_SUB, st.task);
+      const float4 knew = norm_rope(v4[1], L.k_norm, p.eps, p.rope_cs + pos * 64, lane);
+      const float4 vnew = v4[2];
+      if (hh == 0) {
+        *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = pack4_f16(knew.x, knew.y, knew.z, knew.w);
+        *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 1) * p.kvw) = pack4_f16(vnew.x, vnew.y, vnew.z, vnew.w);
+      }
+      const float4 qn = norm_rope(v4[0], L.q_norm, p.eps, p.rope_cs + pos * 64, lane);
+      float part[16];
+#pragma unroll
+      for (int tt = 0; tt < kMaxCtx; ++tt) {
+        const float4 kk = tt < pos0 ? unpack4_f16(kh[tt]) : (tt == pos ? knew : (tt < pos ? kprev : z4));
+        part[tt] = qn.x * kk.x + qn.y * kk.y + qn.z * kk.z + qn.w * kk.w;
+      }
+      if (lane == 0 && threadIdx.x == 0) cl_ev(p, st.evi, 0, CEV_SUB, st.task);
+      const float rsum = reduce_scatter16(part, lane);   // lanes 2t and 2t + 1: position t
+      const bool valid = ((lane >> 1) & 15) <= pos;
+      const float sc = valid ? rsum * scale : -INFINITY;
+      float mx = sc;
+#pragma unroll
+      for (int o = 16; o >= 2; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      const float e = valid ? expf(sc - mx) : 0.f;
+      float den = e;
+#pragma unroll
+      for (int o = 16; o >= 2; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+      const float pr = den > 0.f ? e / den : 0.f;
+      float4 o1 = z4;
+#pragma unroll
+      for (int tt = 0; tt < kMaxCtx; ++tt) {
+        const float4 vv = tt < pos0 ? unpack4_f16(vh[tt]) : (tt == pos ? vnew : (tt < pos ? vprev : z4));
+        const float w = __shfl_sync(0xffffffffu, pr, 2 * tt);
+        o1.x += w * vv.x; o1.y += w * vv.y; o1.z += w * vv.z; o1.w += w * vv.w;
+      }
+      if (lane == 0 && threadIdx.x == 0) cl_ev(p, st.evi, 0, CEV_SUB, st.task);
+      // row n of the O operand (K = the group's 256 columns: head hh in slice hh) in every CTA
+      const uint2 hv = pack4_f16(o1.x, o1.y, o1.z, o1.w);
+      const uint32_t a = o0 + op_idx(n, lane * 4, n8) * 2;
+#pragma unroll
+      for (int dst = 0; dst < kCl; ++dst) cl_st2(cl_map(a, uint32_t(dst)), hv);
+      kprev = knew;
+      vprev = vnew;
+    }
+    fence_proxy_async_cluster();   // the rows written for the peers' tensor cores
+  }
+  cev(p, st, CEV_WORK);
+  const bool ok = cl_sync(p, ms, st);   // every O operand row is in place
+  cev(p, st, CEV_S3);
+  return ok;
+}
+
+// O projection of attention job j (after cl_qkv): tile r of W_o over the
+// group's 256 columns, added into the residual stream.
+__device__ bool cl_out(const CParams& p, CMisc& ms, CState& st, const Task& tk) {
+  const int R = cl_rows(p, tk);
+  const bool mine = cl_nsl(p, tk) > 0;
+  if (mine) {
+    if (threadIdx.x == 0) mbar_arrive(&ms.opfull);   // the rows' writers fenced before the sync
+    const uint16_t* emb = (tk.kind == T_O && tk.k > 1 && tk.l == 0 && tk.job == 0) ? p.embed[tk.k - 2] : nullptr;
+    if (!cl_drain_resid(p, ms, st, cl_x(p, tk.k), R, st.r * kTileM, emb)) return false;
+  }
+  unsigned* ctr = tk.kind == T_O ? p.att_done + (tk.k - 1) * p.L + tk.l : p.mlp_done + (tk.k - 1) * p.L + tk.l;
+  if (tk.kind == T_O && p.withhold >= 0 && blockIdx.x == 0 && tk.k == 1 && tk.l == 0) {
+    named_bar(CBAR_CONS, kClCons);   // a test of the failure path: this count goes missing
+    return true;
+  }
+  cl_publish(p, st, ctr);
+  return true;
+}
+
+// MLP job m of layer l at step k, through the down operand: gate/up over
+// this CTA's tile and K half, then SwiGLU of columns 32r .. 32r+31 of the
+// job's 256 from the peers' partials, written into every peer's down operand.
+__device__ bool cl_gu(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
+  const int k = tk.k, l = tk.l, R = cl_rows(p, tk), np = cl_npad(R), n8 = np / 8;
+  if (!cl_wait_ctr(p, ms, st, p.att_done + (k - 1) * p.L + l, unsigned(p.n_att * kCl))) return false;
+  InSrc in{cl_x(p, k), nullptr, 1, 0};
+  if (!cl_build_norm(p, ms, st, smem, in, p.layer[l].ffn_norm, R)) return false;
+  if (!cl_drain_part(p, ms, st, smem, R)) return false;
+  if (!cl_sync(p, ms, st)) return false;
+  cev(p, st, CEV_S1);
+  const int t = threadIdx.x, c4 = t & 7, r = st.r;
+  const int tg = r >> 2, tu = 2 + (r >> 2), m = 32 * (r & 3) + 4 * c4;   // tiles of gate and up, row in tile
+  const uint32_t opsz = uint32_t(np) * kKs * 2;
+  const uint32_t part0 = smem_u32(smem + kClOffOp) + uint32_t(m) * 4;
+  const uint32_t o0 = smem_u32(smem + kClOffOp2) + uint32_t(tg) * opsz;   // slice c / 128 = r / 4
+  for (int n = t >> 3; n < R; n += kClCons / 8) {
+    const uint32_t a = part0 + uint32_t(n) * kTileM * 4;
+    const float4 g0 = cl_ld4(cl_map(a, uint32_t(2 * tg))), g1 = cl_ld4(cl_map(a, uint32_t(2 * tg + 1)));
+    const float4 u0 = cl_ld4(cl_map(a, uint32_t(2 * tu))), u1 = cl_ld4(cl_map(a, uint32_t(2 * tu + 1)));
+    const uint2 hv = pack4_f16(silu_f(g0.x + g1.x) * (u0.x + u1.x), silu_f(g0.y + g1.y) * (u0.y + u1.y),
+                               silu_f(g0.z + g1.z) * (u0.z + u1.z), silu_f(g0.w + g1.w) * (u0.w + u1.w));
+    const uint32_t d = o0 + op_idx(n, m, n8) * 2;
+#pragma unroll
+    for (int dst = 0; dst < kCl; ++dst) cl_st2(cl_map(d, uint32_t(dst)), hv);
+  }
+  if ((t >> 3) < R) fence_proxy_async_cluster();   // the rows written for the peers' tensor cores
+  cev(p, st, CEV_WORK);
+  const bool ok = cl_sync(p, ms, st);   // every down operand row is in place
+  cev(p, st, CEV_S3);
+  return ok;
+}
+
+// Head job hj at step k: logits 512 hj .. 512 hj + 511 of the step's head
+// for every frame's last position; CTA r completes rows 64 (r%2) .. +63 of
+// tile r/2, writes them out if asked and folds their argmax (lowest index
+// on ties) into the frame's decision word.
+__device__ bool cl_head(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
+  const int k = tk.k, R = p.B;
+  if (!cl_wait_ctr(p, ms, st, p.mlp_done + (k - 1) * p.L + (p.L - 1), unsigned(p.n_mlp * kCl))) return false;
+  InSrc in{cl_x(p, k), nullptr, k == 1 ? 2 : 1, k == 1 ? 1 : 0};
+  if (!cl_build_norm(p, ms, st, smem, in, p.out_norm, R)) return false;
+  if (!cl_drain_part(p, ms, st, smem, R)) return false;
+  if (!cl_sync(p, ms, st)) return false;
+  cev(p, st, CEV_S1);
+  const int t = threadIdx.x, mg = t & 7, n = t >> 3, r = st.r;
+  const int m = 64 * (r & 1) + 8 * mg;
+  unsigned long long key = 0ull;
+  if (n < R) {
+    const float* part = reinterpret_cast<const float*>(smem + kClOffOp) + n * kTileM + m;
+    const uint32_t pa = cl_map(smem_u32(part), uint32_t(r ^ 1));
+    const float4 a0 = *reinterpret_cast<const float4*>(part), a1 = *reinterpret_cast<const float4*>(part + 4);
+    const float4 b0 = cl_ld4(pa), b1 = cl_ld4(pa + 16);
+    const float lg[8] = {a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w,
+                         a1.x + b1.x, a1.y + b1.y, a1.z + b1.z, a1.w + b1.w};
+    const int v0 = 512 * tk.job + kTileM * (r >> 1) + m;
+    if (p.out_logits) {
+      float* o = p.out_logits + (size_t(n) * p.n_steps + (k - 1)) * p.V + v0;
+      *reinterpret_cast<float4*>(o) = make_float4(lg[0], lg[1], lg[2], lg[3]);
+      *reinterpret_cast<float4*>(o + 4) = make_float4(lg[4], lg[5], lg[6], lg[7]);
+    }
+    key = pack_argmax(lg[0], v0);
+#pragma unroll
+    for (int i = 1; i < 8; ++i) {
+      const unsigned long long kk = pack_argmax(lg[i], v0 + i);
+      key = kk > key ? kk : key;
+    }
+  }
+#pragma unroll
+  for (int o = 4; o >= 1; o >>= 1) {   // the frame's 8 threads (all lanes take part)
+    const unsigned long long w = __shfl_xor_sync(0xffffffffu, key, o);
+    key = w > key ? w : key;
+  }
+  if (n < R && mg == 0) atomicMax(p.best + size_t(k - 1) * p.B + n, key);
+  cl_publish(p, st, p.head_done + (k - 1));
+  return true;
+}
+
+__device__ void cl_consumer(const CParams& p, CMisc& ms, uint8_t* smem) {
+  CState st{0u, 0u, 0u, int(cl_rank()), 0, 0u};
+  const Prog g = cl_prog(p);
+  const int nt = cl_n_tasks(p, g);
+  for (int i = 0; i < nt; ++i) {
+    const Task tk = cl_task(p, g, i);
+    st.task = i;
+    cev(p, st, CEV_START);
+    bool ok = true;
+    switch (tk.kind) {
+      case T_PROJ: ok = cl_proj(p, ms, st, smem, tk); break;
+      case T_QKV: ok = cl_qkv(p, ms, st, smem, tk); break;
+      case T_GU: ok = cl_gu(p, ms, st, smem, tk); break;
+      case T_HEAD: ok = cl_head(p, ms, st, smem, tk); break;
+      default: ok = cl_out(p, ms, st, tk); break;   // T_O, T_DOWN
+    }
+    if (!ok) return;
+  }
+  // the codes of every step, once the last step's decisions are in
+  if (blockIdx.x == 0) {
+    if (!cl_wait_ctr(p, ms, st, p.head_done + (p.n_steps - 1), unsigned(p.n_head * kCl))) return;
+    for (int i = threadIdx.x; i < p.B * p.n_steps; i += kClCons) {
+      const int b = i / p.n_steps, k = i % p.n_steps;
+      p.out_codes[i] = unpack_argmax_index(__ldcg(p.best + size_t(k) * p.B + b));
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kClThreads, 1) k_frames_cluster(const CParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  CMisc& ms = *reinterpret_cast<CMisc*>(smem + kClOffMisc);
+  const int t = threadIdx.x, warp = t >> 5;
+  if (t == 0) {
+    for (int i = 0; i < kClNW; ++i) { mbar_init(&ms.wfull[i], 1); mbar_init(&ms.wempty[i], 1); }
+    mbar_init(&ms.opfull, 1);
+    mbar_init(&ms.accfull, 1);
+    mbar_init(&ms.mmadone, 1);
+    mbar_init(&ms.cbar[0], kCl);
+    mbar_init(&ms.cbar[1], kCl);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 0) tmem_alloc(&ms.tmem_base, kClTmemCols);
+  tc_fence_before();
+  cl_barrier_all();   // every CTA's barriers are initialised before any peer arrives on them
+  tc_fence_after();
+
+  if (warp < kClConsWarps) {
+    cl_consumer(p, ms, smem);
+  } else if (warp == kClProdWarp) {
+    if ((t & 31) == 0) cl_producer(p, ms, smem);
+    __syncwarp();
+  } else if (warp == kClMmaWarp) {
+    if ((t & 31) == 0) cl_mma(p, ms, smem);
+    __syncwarp();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(ms.tmem_base, kClTmemCols);
+  cl_barrier_all();   // no CTA leaves while a peer may still use its shared memory
+}
+
+// ------------------------------------------------------------------ host
+size_t cl_al256(size_t b) { return (b + 255) & ~size_t(255); }
+
+struct ClLayout {
+  size_t x, proj_done, att_done, mlp_done, head_done, best, abort_flag, zeroed, kv, total;
+};
+ClLayout cl_layout(const qp_geometry& g, int B) {
+  ClLayout Lo{};
+  const size_t steps = size_t(g.n_steps), L = size_t(g.layers);
+  size_t o = 0;
+  Lo.x = o;          o += cl_al256(steps * 2 * B * g.hidden * 4);
+  Lo.proj_done = o;  o += 256;
+  Lo.att_done = o;   o += cl_al256(steps * L * 4);
+  Lo.mlp_done = o;   o += cl_al256(steps * L * 4);
+  Lo.head_done = o;  o += cl_al256(steps * 4);
+  Lo.best = o;       o += cl_al256(steps * B * 8);
+  Lo.abort_flag = o; o += 256;
+  Lo.zeroed = o;
+  Lo.kv = o;         o += cl_al256(L * B * (steps + 1) * 2 * size_t(g.n_kv_heads) * kHeadDim * 2);
+  Lo.total = o;
+  return Lo;
+}
+
+constexpr int kClMaxDevices = 64;
+// Per device: the kernel's shared-memory limit is set (1) and the clusters
+// that fit at once (> 0), or no cluster launch is possible (-1).
+std::atomic<int> g_cl_clusters[kClMaxDevices];
+
+size_t cl_smem_bytes() { return kClOffMisc + sizeof(CMisc) + 1024; }
+
+int cl_clusters(int dev) {
+  std::atomic<int> local(0);
+  std::atomic<int>* slot = dev >= 0 && dev < kClMaxDevices ? &g_cl_clusters[dev] : &local;
+  int n = slot->load(std::memory_order_acquire);
+  if (n != 0) return n;
+  const int smem = int(cl_smem_bytes());
+  if (cudaFuncSetAttribute(k_frames_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+    cudaGetLastError();
+    n = -1;
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = kCl; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(kCl); cfg.blockDim = dim3(kClThreads); cfg.dynamicSmemBytes = size_t(smem);
+    cfg.attrs = at; cfg.numAttrs = 1;
+    int m = 0;
+    if (cudaOccupancyMaxActiveClusters(&m, k_frames_cluster, &cfg) != cudaSuccess || m < 1) {
+      cudaGetLastError();
+      n = -1;
+    } else {
+      n = m;
+    }
+  }
+  slot->store(n, std::memory_order_release);
+  return n;
+}
+
+}  // namespace
+
+size_t cluster_scratch_bytes(const qp_geometry& g, int bmax) { return cl_layout(g, bmax).total; }
+
+bool cluster_geometry_ok(const qp_geometry& g) {
+  return g.head_dim == kHeadDim && g.n_q_heads == 2 * g.n_kv_heads && g.hidden % 256 == 0 && g.hidden >= 512 &&
+         g.hidden <= 1024 &&
+         g.ffn % 256 == 0 && g.vocab % 512 == 0 && g.code_embed_dim == g.hidden && g.talker_hidden % kKs == 0 &&
+         g.n_steps + 1 <= kMaxCtx && g.layers <= kMaxLayers;
+}
+
+bool cluster_supported(const qp_handle* h, const RunArgs& a) {
+  if (!h->carena || !cluster_geometry_ok(h->g)) return false;
+  if (h->wfmt != WF_BF16 || h->hfmt != WF_BF16) return false;
+  if (a.B < 1 || a.B > h->cmax_batch || a.B > kClusterMaxFrames) return false;
+  if (a.temperature > 0.f) return false;
+  return cl_clusters(h->device) > 0;
+}
+
+qp_status run_frames_cluster(qp_handle* h, const RunArgs& a, cudaStream_t s) {
+  if (!cluster_supported(h, a)) return QP_ERR_ARG;
+  const qp_geometry& g = h->g;
+  const int n_cl = std::min(cl_clusters(h->device), h->num_sms / kCl);
+  if (n_cl < 1) return QP_ERR_ARG;
+  const ClLayout Lo = cl_layout(g, a.B);
+  uint8_t* base = static_cast<uint8_t*>(h->carena);
+  CParams p{};
+  p.d = g.hidden; p.qw = g.n_q_heads * kHeadDim; p.kvw = g.n_kv_heads * kHeadDim; p.F = g.ffn; p.V = g.vocab;
+  p.th = g.talker_hidden; p.L = g.layers; p.n_kv = g.n_kv_heads; p.n_steps = g.n_steps; p.q0_vocab = g.q0_vocab;
+  p.eps = g.rms_eps;
+  p.embed_f16 = h->embed_f16;
+  p.w_proj = reinterpret_cast<const uint16_t*>(h->proj.w); p.b_proj = h->b_proj; p.e0 = h->e0;
+  for (int l = 0; l < g.layers; ++l) {
+    const LayerW& Lw = h->layer[l];
+    p.layer[l].w[0] = reinterpret_cast<const uint16_t*>(Lw.qkv.w);
+    p.layer[l].w[1] = reinterpret_cast<const uint16_t*>(Lw.o.w);
+    p.layer[l].w[2] = reinterpret_cast<const uint16_t*>(Lw.gu.w);
+    p.layer[l].w[3] = reinterpret_cast<const uint16_t*>(Lw.down.w);
+    p.layer[l].attn_norm = Lw.attn_norm; p.layer[l].q_norm = Lw.q_norm;
+    p.layer[l].k_norm = Lw.k_norm; p.layer[l].ffn_norm = Lw.ffn_norm;
+  }
+  p.out_norm = h->out_norm;
+  for (int j = 0; j < g.n_steps; ++j) {
+    p.embed[j] = h->embed[j];
+    p.w_head[j] = reinterpret_cast<const uint16_t*>(h->head[j].w);
+  }
+  p.rope_cs = h->rope_cs;
+  p.x = reinterpret_cast<float*>(base + Lo.x);
+  p.kv = reinterpret_cast<uint16_t*>(base + Lo.kv);
+  p.proj_done = reinterpret_cast<unsigned*>(base + Lo.proj_done);
+  p.att_done = reinterpret_cast<unsigned*>(base + Lo.att_done);
+  p.mlp_done = reinterpret_cast<unsigned*>(base + Lo.mlp_done);
+  p.head_done = reinterpret_cast<unsigned*>(base + Lo.head_done);
+  p.best = reinterpret_cast<unsigned long long*>(base + Lo.best);
+  p.abort_flag = reinterpret_cast<int*>(base + Lo.abort_flag);
+  p.status = h->status;
+  p.spin_limit = h->wait_ticks > 0 ? h->wait_ticks : kSpinLimit;
+  p.withhold = h->withhold_gemm;
+  p.trace = h->trace; p.trace_n = h->trace_phases;
+  p.n_cl = n_cl;
+  p.n_att = g.n_kv_heads; p.n_mlp = g.ffn / 256; p.n_head = g.vocab / 512;
+  p.n_proj = (g.hidden / kTileM) * (g.talker_hidden / kKs);
+  p.B = a.B; p.H = a.H; p.q0 = a.q0; p.out_codes = a.out_codes; p.out_logits = a.out_logits; p.forced = a.forced;
+
+  if (cudaMemsetAsync(base, 0, Lo.zeroed, s) != cudaSuccess) {
+    cudaGetLastError();
+    return QP_ERR_CUDA;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kCl; at[0].val.clusterDim.y = 1; at[0].val.clusterDim.z = 1;
+  at[1].id = cudaLaunchAttributeCooperative;
+  at[1].val.cooperative = 1;
+  cfg.gridDim = dim3(n_cl * kCl); cfg.blockDim = dim3(kClThreads); cfg.dynamicSmemBytes = cl_smem_bytes();
+  cfg.stream = s; cfg.attrs = at; cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, k_frames_cluster, p) != cudaSuccess) {
+    cudaGetLastError();
+    return QP_ERR_CUDA;
+  }
+  return QP_OK;
+}
+
+}  // namespace qp

@@ -108,6 +108,12 @@ size_t sync_bytes(const qp_geometry& g, int B);
 // step at 40 frames, 221.7 vs 209.1 at 48).
 constexpr int kSmallMaxFrames = 64;
 constexpr int kSmallAutoFrames = 40;
+// Largest batch the cluster engine serves (2B <= 64 activation rows at step
+// 1: its operand and partial buffers share 64 KB of shared memory).  Where it
+// serves a call, QP_ENGINE_AUTO takes it: measured on GB300 at the 1.7B
+// geometry, 121.4 vs 135.6 us per step at 1 frame (small-batch engine),
+// 129.7 vs 144.4 at 8, 177.7 vs 192.8 at 32.
+constexpr int kClusterMaxFrames = 32;
 
 }  // namespace qp
 
@@ -137,6 +143,10 @@ struct qp_handle {
   void* sarena = nullptr;
   size_t sarena_bytes = 0;
   qp::Scratch scr;
+  // the cluster engine's scratch (qp_cluster.cu), for batches of up to cmax_batch frames; null where
+  // the geometry is not one it serves
+  void* carena = nullptr;
+  int cmax_batch = 0;
   // small fixed buffers
   void* farena = nullptr;
   int* status = nullptr;                        // device status word
@@ -161,6 +171,11 @@ qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s);
 size_t persistent_smem_bytes();
 // the Q8_0 build of the tile engine's kernel (qp_persistent_q8.cu)
 qp_status run_tile_q8(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax, cudaStream_t s);
+// cluster engine (qp_cluster.cu): greedy frame loop, 16-bit weights, at most kClusterMaxFrames
+size_t cluster_scratch_bytes(const qp_geometry& g, int bmax);
+bool cluster_geometry_ok(const qp_geometry& g);
+bool cluster_supported(const qp_handle* h, const RunArgs& a);
+qp_status run_frames_cluster(qp_handle* h, const RunArgs& a, cudaStream_t s);
 // small-batch engine (qp_small.cu): 16-bit slices (Q8_0 matrices through
 // their hi and lo images), at most kSmallMaxFrames
 bool small_supported(const qp_handle* h, const RunArgs& a);

@@ -20,7 +20,7 @@
 extern "C" {
 #endif
 
-/* The frame loop has two schedules of the same computation, both splitting
+/* The frame loop has three schedules of the same computation.  Two split
  * every weight matrix into (128-row tile, 128-column K slice) units spread
  * over all SMs.  The tile engine serves any batch and both weight formats: a
  * completed tile is finished (residual, norm, SwiGLU, f16 operand) once by
@@ -28,19 +28,31 @@ extern "C" {
  * formats too (Q8_0 matrices as their f16 hi + lo images, two slices per
  * unit) with at most 64 frames per call: partials go straight into their
  * destination and each consumer builds its operand slice from it, which
- * removes one dependent global round trip per GEMM.  QP_ENGINE_AUTO (the
- * default) takes the small-batch engine for calls of at most 40 frames,
- * where it is the faster of the two on GB300, and the tile engine otherwise. */
+ * removes one dependent global round trip per GEMM.  The cluster engine
+ * serves greedy calls of at most 32 frames with 16-bit weights, for
+ * geometries with head_dim 128, two q heads per kv head, a hidden size of
+ * 512 to 1024 (a multiple of 256), an FFN size a multiple of 256, a
+ * vocabulary a multiple of 512 and code tables as wide as the hidden size
+ * (the 1.7B predictor's): one 8-CTA thread-block cluster per kv head runs
+ * QKV, attention and O, one per 256 FFN columns gate/up, SwiGLU and down,
+ * partial products meeting in the cluster's shared memory, so a layer has two
+ * grid-wide dependencies instead of five.  QP_ENGINE_AUTO (the default) takes
+ * the cluster engine where it serves the call, else the small-batch engine
+ * for calls of at most 40 frames, else the tile engine: the order of their
+ * speed on GB300. */
 typedef enum {
   QP_ENGINE_AUTO = 0,
   QP_ENGINE_TILE = 1,
-  QP_ENGINE_SMALL = 2
+  QP_ENGINE_SMALL = 2,
+  QP_ENGINE_CLUSTER = 3
 } qp_engine;
 
-/* Select the engine for later calls on h.  With QP_ENGINE_SMALL a call the
- * small-batch engine cannot serve (more than 64 frames, sampling over a
- * vocabulary above 4096, the deterministic schedule)
- * returns QP_ERR_ARG.  QP_ERR_ARG for a null handle or an unknown engine. */
+/* Select the engine for later calls on h.  A call the selected engine cannot
+ * serve returns QP_ERR_ARG: with QP_ENGINE_SMALL more than 64 frames,
+ * sampling over a vocabulary above 4096, or the deterministic schedule; with
+ * QP_ENGINE_CLUSTER anything outside the calls and geometries above (or the
+ * deterministic schedule).  QP_ERR_ARG for a null handle or an unknown
+ * engine. */
 qp_status qp_set_engine(qp_handle* h, int engine);
 
 /* Testing aid for the device-side failure path.  Every wait inside the
