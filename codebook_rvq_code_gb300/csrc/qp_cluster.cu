@@ -66,6 +66,7 @@ constexpr uint32_t kClOpBytes = 65536;
 constexpr uint32_t kClOffOp2 = kClOffOp + 32768;      // O / down operand (second half of the region)
 constexpr uint32_t kClOffMisc = kClOffOp + kClOpBytes;
 constexpr uint32_t kClTmemCols = 64;                  // one accumulator of up to 64 columns
+static_assert(kClusterMaxFrames <= kCl * kClConsWarps / 2, "attention: one (frame, q head) per warp");
 
 enum { CBAR_CONS = 1 };
 enum { T_PROJ = 0, T_QKV, T_O, T_GU, T_DOWN, T_HEAD };
@@ -178,7 +179,8 @@ __device__ __forceinline__ void fence_proxy_async_cluster() {
 // 16 | code << 12 | task index.  Compiled in only with QP_TRACE.
 enum {
   CEV_START = 1, CEV_READY = 2, CEV_SSYNC = 3, CEV_OPREADY = 4, CEV_ACC = 5, CEV_S1 = 6, CEV_WORK = 7,
-  CEV_S3 = 8, CEV_PUB = 9, CEV_WWAIT = 10, CEV_WREADY = 11, CEV_COMMIT = 12, CEV_MOP = 13, CEV_SUB = 14
+  CEV_S3 = 8, CEV_PUB = 9, CEV_WWAIT = 10, CEV_WREADY = 11, CEV_COMMIT = 12, CEV_MOP = 13, CEV_SUB = 14,
+  CEV_BSUB = 15
 };
 #ifdef QP_TRACE
 __device__ __forceinline__ void cl_ev(const CParams& p, unsigned& idx, int base, int code, int task) {
@@ -366,6 +368,7 @@ __device__ void cl_mma(const CParams& p, CMisc& ms, uint8_t* smem) {
     }
     mma_commit(&ms.accfull);
     cl_ev(p, evi, 8192, CEV_COMMIT, i);
+
     ++opseq;
   }
 out:
@@ -450,8 +453,35 @@ __device__ __forceinline__ void cl_publish(const CParams& p, CState& st, unsigne
   cev(p, st, CEV_PUB);
 }
 
+// RMSNorm of a 128-vector held as 4 values per lane with the norm's weights
+// w (this lane's four), then rotate-half RoPE with this lane's factors c
+// (pairs (i, i+64) sit in lanes l and l^16).
+__device__ __forceinline__ float4 norm_rope_w(float4 x, float4 w, const float2 (&c)[4], float eps, int lane) {
+  const float r = rsqrtf(warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w) / 128.f + eps);
+  const float v[4] = {x.x * r * w.x, x.y * r * w.y, x.z * r * w.z, x.w * r * w.w};
+  float o[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const float partner = __shfl_xor_sync(0xffffffffu, v[e], 16);
+    o[e] = lane < 16 ? v[e] * c[e].x - partner * c[e].y : v[e] * c[e].x + partner * c[e].y;
+  }
+  return make_float4(o[0], o[1], o[2], o[3]);
+}
+
+// L2 loads issued where they stand (volatile: the compiler keeps them ahead
+// of the barriers that follow, so their latency overlaps the wait).
+__device__ __forceinline__ float4 ldv_f4(const void* src) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(src));
+  return v;
+}
+__device__ __forceinline__ uint2 ldv_u2(const void* src) {
+  uint2 v;
+  asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(src));
+  return v;
+}
 __device__ __forceinline__ void ld8f(const float* src, float (&v)[8]) {
-  const float4 a = __ldcg(reinterpret_cast<const float4*>(src)), b = __ldcg(reinterpret_cast<const float4*>(src + 4));
+  const float4 a = ldv_f4(src), b = ldv_f4(src + 4);
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
 }
 __device__ __forceinline__ void ld8e(const uint16_t* src, bool f16, float (&v)[8]) {
@@ -519,6 +549,7 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
       if (lane == 0) ms.ssw[warp][i] = ss;
     }
   }
+  cev(p, st, CEV_BSUB);
   for (int i = kClHold; i < passes; ++i) {
     const int n = t / CH + RP * i;
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -538,6 +569,7 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
     ms.rsc[t] = exp2i(-range_exp(s / float(half)));
   }
   named_bar(CBAR_CONS, kClCons);
+  cev(p, st, CEV_BSUB);
   // pass 2: f16(x * w * 2^-e) into the operand slices
   const float4 w0 = __ldg(reinterpret_cast<const float4*>(wn + col));
   const float4 w1 = __ldg(reinterpret_cast<const float4*>(wn + col + 4));
@@ -597,29 +629,38 @@ __device__ bool cl_drain_part(const CParams& p, CMisc& ms, CState& st, uint8_t* 
 }
 
 // Drain the accumulator of an O or down tile (rows m0 .. m0+127 of the
-// residual stream) into the residual rows n < R: one reduction per value,
-// a warp's 32 lanes on 32 consecutive features.  emb: also add the frame's
-// code embedding (step k >= 2, layer 0, first kv group).
-__device__ bool cl_drain_resid(const CParams& p, CMisc& ms, CState& st, float* xrows, int R, int m0,
+// residual stream) into the residual rows n < R.  Each warp drains 32
+// features x 8 rows at a time, transposes them through 1 KB of shared
+// memory (the start of the operand region: the partials there were read
+// before the last cluster sync) and adds 4 consecutive features per thread
+// with one vector reduction.  emb: also add the frame's code embedding
+// (step k >= 2, layer 0, first kv group).
+__device__ bool cl_drain_resid(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, float* xrows, int R, int m0,
                                const uint16_t* emb) {
   if (!cl_wait_acc(p, ms, st)) return false;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ch = warp >> 2;
-  const int m = m0 + q * 32 + lane;
-  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {
+  float* tp = reinterpret_cast<float*>(smem + kClOffOp) + warp * 256;   // [8 rows][32 features]
+  const int mq = m0 + q * 32;
+  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {   // warp-uniform
     float v[8];
     tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int n = col + i;
+    for (int i = 0; i < 8; ++i) tp[i * 32 + lane] = v[i];
+    __syncwarp();
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int f = pass * 4 + (lane >> 3), k4 = (lane & 7) * 4, n = col + f;
       if (n < R) {
-        float a = v[i];
+        float4 a = *reinterpret_cast<const float4*>(tp + f * 32 + k4);
         if (emb) {
-          const uint16_t e = emb[size_t(ms.code[n]) * p.d + m];
-          a += p.embed_f16 ? f16_bits_to_f32(e) : bf16_bits_to_f32(e);
+          const uint2 e = *reinterpret_cast<const uint2*>(emb + size_t(ms.code[n]) * p.d + mq + k4);
+          a.x += e16_to_f32(e.x, p.embed_f16); a.y += e16_to_f32(e.x >> 16, p.embed_f16);
+          a.z += e16_to_f32(e.y, p.embed_f16); a.w += e16_to_f32(e.y >> 16, p.embed_f16);
         }
-        red_add_f32(xrows + size_t(n) * p.d + m, a);
+        red_add_v4_f32(xrows + size_t(n) * p.d + mq + k4, a);
       }
     }
+    __syncwarp();
   }
   tc_fence_before();
   return true;
@@ -726,28 +767,36 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
   InSrc in;
   if (!cl_att_input(p, ms, st, tk, in)) return false;
   if (!cl_build_norm(p, ms, st, smem, in, p.layer[l].attn_norm, R)) return false;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, hh = warp & 1;
+  const int P = k == 1 ? 2 : 1, ctx = p.n_steps + 1, pos0 = k == 1 ? 0 : k;
+  // warp w: q head hh = w % 2 of frame b = r + 8 (w / 2) (at most 32 frames: one per warp)
+  const int b = st.r + kCl * (warp >> 1);
+  uint16_t* kvb = p.kv + (size_t(l) * p.B + b) * ctx * 2 * p.kvw + j * kHeadDim + lane * 4;   // + (pos*2 + {0,1}) * kvw
+  // the positions of earlier steps, from the cache (written by this CTA's head-0 warps), loaded
+  // while the MMAs run
+  uint2 kh[kMaxCtx], vh[kMaxCtx];
+#pragma unroll
+  for (int tt = 0; tt < kMaxCtx; ++tt) {
+    const bool c = b < p.B && tt < pos0;
+    kh[tt] = c ? ldv_u2(kvb + (size_t(tt) * 2 + 0) * p.kvw) : make_uint2(0, 0);
+    vh[tt] = c ? ldv_u2(kvb + (size_t(tt) * 2 + 1) * p.kvw) : make_uint2(0, 0);
+  }
+  // the head norms' weights and the new positions' RoPE factors, also ahead of the sync
+  const CLayer& L = p.layer[l];
+  const float4 qnw = __ldg(reinterpret_cast<const float4*>(L.q_norm + lane * 4));
+  const float4 knw = __ldg(reinterpret_cast<const float4*>(L.k_norm + lane * 4));
+  float2 cs[4];   // position pos0's (step 1 reloads them for position 1)
+#pragma unroll
+  for (int e = 0; e < 4; ++e) cs[e] = __ldg(p.rope_cs + pos0 * 64 + ((lane * 4 + e) & 63));
   if (!cl_drain_part(p, ms, st, smem, R)) return false;
   if (!cl_sync(p, ms, st)) return false;
   cev(p, st, CEV_S1);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, hh = warp & 1;
-  const int P = k == 1 ? 2 : 1, ctx = p.n_steps + 1, pos0 = k == 1 ? 0 : k;
   const float scale = rsqrtf(float(kHeadDim));
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  const CLayer& L = p.layer[l];
   const uint32_t part0 = smem_u32(smem + kClOffOp) + uint32_t(lane) * 16;
   const uint32_t opsz = uint32_t(np) * kKs * 2;
   const uint32_t o0 = smem_u32(smem + kClOffOp2) + uint32_t(hh) * opsz;
-  uint16_t* kvl = p.kv + size_t(l) * p.B * ctx * 2 * p.kvw;
-  // warp w: q head hh = w % 2 of frames b = r + 8 (w / 2) (mod 32)
-  for (int b = st.r + kCl * (warp >> 1); b < p.B; b += kCl * (kClConsWarps / 2)) {
-    uint16_t* kvb = kvl + size_t(b) * ctx * 2 * p.kvw + j * kHeadDim + lane * 4;   // + (pos*2 + {0,1}) * kvw
-    // the positions of earlier steps, from the cache (written by this CTA's head-0 warps)
-    uint2 kh[kMaxCtx], vh[kMaxCtx];
-#pragma unroll
-    for (int tt = 0; tt < kMaxCtx; ++tt) {
-      kh[tt] = tt < pos0 ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(tt) * 2 + 0) * p.kvw)) : make_uint2(0, 0);
-      vh[tt] = tt < pos0 ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(tt) * 2 + 1) * p.kvw)) : make_uint2(0, 0);
-    }
+  if (b < p.B) {
     float4 kprev = z4, vprev = z4;   // step 1: position 0's k and v, for position 1
     for (int pp = 0; pp < P; ++pp) {
       const int n = b * P + pp, pos = pos0 + pp;
@@ -762,13 +811,16 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
         v4[i] = make_float4(h0.x + h1.x, h0.y + h1.y, h0.z + h1.z, h0.w + h1.w);
       }
       if (lane == 0 && threadIdx.x == 0) cl_ev(p, st.evi, 0, CEV_SUB, st.task);
-      const float4 knew = norm_rope(v4[1], L.k_norm, p.eps, p.rope_cs + pos * 64, lane);
+      if (pp > 0)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) cs[e] = __ldg(p.rope_cs + pos * 64 + ((lane * 4 + e) & 63));
+      const float4 knew = norm_rope_w(v4[1], knw, cs, p.eps, lane);
       const float4 vnew = v4[2];
       if (hh == 0) {
         *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = pack4_f16(knew.x, knew.y, knew.z, knew.w);
         *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 1) * p.kvw) = pack4_f16(vnew.x, vnew.y, vnew.z, vnew.w);
       }
-      const float4 qn = norm_rope(v4[0], L.q_norm, p.eps, p.rope_cs + pos * 64, lane);
+      const float4 qn = norm_rope_w(v4[0], qnw, cs, p.eps, lane);
       float part[16];
 #pragma unroll
       for (int tt = 0; tt < kMaxCtx; ++tt) {
@@ -813,13 +865,13 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
 
 // O projection of attention job j (after cl_qkv): tile r of W_o over the
 // group's 256 columns, added into the residual stream.
-__device__ bool cl_out(const CParams& p, CMisc& ms, CState& st, const Task& tk) {
+__device__ bool cl_out(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
   const int R = cl_rows(p, tk);
   const bool mine = cl_nsl(p, tk) > 0;
   if (mine) {
     if (threadIdx.x == 0) mbar_arrive(&ms.opfull);   // the rows' writers fenced before the sync
     const uint16_t* emb = (tk.kind == T_O && tk.k > 1 && tk.l == 0 && tk.job == 0) ? p.embed[tk.k - 2] : nullptr;
-    if (!cl_drain_resid(p, ms, st, cl_x(p, tk.k), R, st.r * kTileM, emb)) return false;
+    if (!cl_drain_resid(p, ms, st, smem, cl_x(p, tk.k), R, st.r * kTileM, emb)) return false;
   }
   unsigned* ctr = tk.kind == T_O ? p.att_done + (tk.k - 1) * p.L + tk.l : p.mlp_done + (tk.k - 1) * p.L + tk.l;
   if (tk.kind == T_O && p.withhold >= 0 && blockIdx.x == 0 && tk.k == 1 && tk.l == 0) {
@@ -922,7 +974,7 @@ __device__ void cl_consumer(const CParams& p, CMisc& ms, uint8_t* smem) {
       case T_QKV: ok = cl_qkv(p, ms, st, smem, tk); break;
       case T_GU: ok = cl_gu(p, ms, st, smem, tk); break;
       case T_HEAD: ok = cl_head(p, ms, st, smem, tk); break;
-      default: ok = cl_out(p, ms, st, tk); break;   // T_O, T_DOWN
+      default: ok = cl_out(p, ms, st, smem, tk); break;   // T_O, T_DOWN
     }
     if (!ok) return;
   }
