@@ -57,6 +57,7 @@ constexpr int kClMmaWarp = 9;
 constexpr int kClThreads = 10 * 32;
 constexpr int kClMaxRows = 64;                // activation rows of one GEMM (2B at step 1)
 constexpr int kClHold = 8;                    // input chunks a consumer thread keeps in registers
+constexpr int kClSplitRows = 24;              // from this many rows the four CTAs of a K half share the loads
 
 constexpr uint32_t kClWSlot = kTileM * kKs * 2;       // one 128 x 128 f16 weight slice
 constexpr int kClNW = 5;                              // weight ring slots
@@ -159,6 +160,10 @@ __device__ __forceinline__ float cl_ld1(uint32_t a) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
   return v;
+}
+__device__ __forceinline__ void cl_st4(uint32_t a, uint4 v) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
 }
 __device__ __forceinline__ void cl_st2(uint32_t a, uint2 v) {
   asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(v.x), "r"(v.y) : "memory");
@@ -515,17 +520,28 @@ __device__ __forceinline__ void in_load8(const CParams& p, const CMisc& ms, cons
 
 // Build the operand of a normalised GEMM over this CTA's K half: rows
 // n < R of input * w_norm * 2^-e, as f16, into slices 0..nkh-1 of the
-// operand region, e from this half's mean square (qp_device.cuh,
-// range_exp), and hand it to the MMA warp.  While the MMAs run, the row's
-// 1/RMS follows from this half's sum of squares and the partner's (a
-// cluster sync); the drain applies 2^e / RMS to the partial products.
-// Thread t takes column chunk t % CH (8 columns) of rows t / CH + RP * i.
+// operand region, e from the row's mean square over this K half
+// (qp_device.cuh, range_exp), and hand it to the MMA warp; the drain applies
+// 2^e / RMS to the partial products, the row's 1/RMS following from this
+// half's sum of squares and the partner's.
+//   * Up to kClSplitRows rows each CTA loads every row of its half, starts
+//     the MMAs, and exchanges the sums of squares (a cluster sync) while they
+//     run.
+//   * From kClSplitRows rows the four CTAs of a half (ranks h, h+2, h+4,
+//     h+6) share the loads: CTA h+2g loads, scales and converts rows n = g
+//     (mod 4) and writes them into all four operands; one cluster sync then
+//     publishes the rows and the sums of squares before the MMAs start.
+// Thread t takes column chunk t % CH (8 columns) of local rows t / CH + RP i.
+template <bool SPLIT>
 __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const InSrc& in,
                               const float* wn, int R) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
   const int half = p.d / 2, CH = half / 8, RP = kClCons / CH, c = t % CH, h = st.r & 1;
+  const bool split = SPLIT && R >= kClSplitRows;
+  const int G = split ? 4 : 1, g = split ? st.r >> 1 : 0;
+  const int RL = R > g ? (R - g + G - 1) / G : 0;   // this CTA's rows: n = g + G * (local row)
   const int col = h * half + c * 8;   // global column
-  const int passes = (R + RP - 1) / RP;
+  const int passes = (RL + RP - 1) / RP;
   const int np = cl_npad(R), n8 = np / 8;
   const uint32_t opsz = uint32_t(np) * kKs * 2;
   float hold[kClHold][8];
@@ -534,10 +550,10 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
   // one row (CH >= 32)
 #pragma unroll
   for (int i = 0; i < kClHold; ++i) {
-    const int n = t / CH + RP * i;
+    const int li = t / CH + RP * i;
 #pragma unroll
     for (int e = 0; e < 8; ++e) hold[i][e] = 0.f;
-    if (i < passes && n < R) in_load8(p, ms, in, n, col, hold[i]);
+    if (i < passes && li < RL) in_load8(p, ms, in, g + G * li, col, hold[i]);
   }
 #pragma unroll
   for (int i = 0; i < kClHold; ++i) {
@@ -551,9 +567,9 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
   }
   cev(p, st, CEV_BSUB);
   for (int i = kClHold; i < passes; ++i) {
-    const int n = t / CH + RP * i;
+    const int li = t / CH + RP * i;
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    if (n < R) in_load8(p, ms, in, n, col, v);
+    if (li < RL) in_load8(p, ms, in, g + G * li, col, v);
     float ss = 0.f;
 #pragma unroll
     for (int e = 0; e < 8; ++e) ss += v[e] * v[e];
@@ -561,50 +577,76 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
     if (lane == 0) ms.ssw[warp][i] = ss;
   }
   named_bar(CBAR_CONS, kClCons);
-  if (t < R) {
-    const int slot = t % RP, i = t / RP, w0 = slot * CH / 32;
+  if (t < RL) {
+    const int slot = t % RP, i = t / RP, w0 = slot * CH / 32, n = g + G * t;
     float s = 0.f;
     for (int w = 0; w < CH / 32; ++w) s += ms.ssw[w0 + w][i];
-    ms.ssx[t] = s;
-    ms.rsc[t] = exp2i(-range_exp(s / float(half)));
+    ms.ssx[n] = s;
+    ms.rsc[n] = exp2i(-range_exp(s / float(half)));
   }
   named_bar(CBAR_CONS, kClCons);
   cev(p, st, CEV_BSUB);
-  // pass 2: f16(x * w * 2^-e) into the operand slices
+  // pass 2: f16(x * w * 2^-e) into the operand slices (of all four CTAs of the half, split)
   const float4 w0 = __ldg(reinterpret_cast<const float4*>(wn + col));
   const float4 w1 = __ldg(reinterpret_cast<const float4*>(wn + col + 4));
   const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
   const int kl = c * 8, s = kl / kKs, kk = kl % kKs;
   uint16_t* op = reinterpret_cast<uint16_t*>(smem + kClOffOp + uint32_t(s) * opsz);
+  auto put = [&](int n, const float (&v)[8]) {
+    const uint4 hv = pack8h(v);
+    if (!split) {
+      *reinterpret_cast<uint4*>(op + op_idx(n, kk, n8)) = hv;
+    } else {
+      const uint32_t a = smem_u32(op + op_idx(n, kk, n8));
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) cl_st4(cl_map(a, uint32_t(h + 2 * gg)), hv);
+    }
+  };
 #pragma unroll
   for (int i = 0; i < kClHold; ++i) {
-    const int n = t / CH + RP * i;
-    if (i < passes && n < R) {
+    const int li = t / CH + RP * i;
+    if (i < passes && li < RL) {
+      const int n = g + G * li;
       const float sc = ms.rsc[n];
       float v[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) v[e] = hold[i][e] * sc * w[e];
-      *reinterpret_cast<uint4*>(op + op_idx(n, kk, n8)) = pack8h(v);
+      put(n, v);
     }
   }
   for (int i = kClHold; i < passes; ++i) {
-    const int n = t / CH + RP * i;
-    if (n >= R) break;
+    const int li = t / CH + RP * i;
+    if (li >= RL) break;
+    const int n = g + G * li;
     float v[8];
     in_load8(p, ms, in, n, col, v);
     const float sc = ms.rsc[n];
 #pragma unroll
     for (int e = 0; e < 8; ++e) v[e] *= sc * w[e];
-    *reinterpret_cast<uint4*>(op + op_idx(n, kk, n8)) = pack8h(v);
+    put(n, v);
   }
-  cl_op_ready(p, ms, st);
-  // the rows' 1/RMS from both halves, while the MMAs run; the drain's
-  // barrier publishes ms.inv
+  if (!split) {
+    cl_op_ready(p, ms, st);
+    // the rows' 1/RMS from both halves, while the MMAs run; the drain's
+    // barrier publishes ms.inv
+    if (!cl_sync(p, ms, st)) return false;
+    cev(p, st, CEV_SSYNC);
+    if (t < R) {
+      const float other = cl_ld1(cl_map(smem_u32(&ms.ssx[t]), uint32_t(st.r ^ 1)));
+      ms.inv[t] = rsqrtf((ms.ssx[t] + other) / float(p.d) + p.eps) / ms.rsc[t];
+    }
+    return true;
+  }
+  fence_proxy_async_cluster();   // the rows written for the four CTAs' tensor cores
   if (!cl_sync(p, ms, st)) return false;
+  cl_op_ready(p, ms, st);
   cev(p, st, CEV_SSYNC);
-  if (t < R) {
-    const float other = cl_ld1(cl_map(smem_u32(&ms.ssx[t]), uint32_t(st.r ^ 1)));
-    ms.inv[t] = rsqrtf((ms.ssx[t] + other) / float(p.d) + p.eps) / ms.rsc[t];
+  if (t < R) {   // row t's sums of squares and scale sit with the CTAs that built it
+    const uint32_t own = uint32_t(h + 2 * (t & 3)), other = uint32_t((h ^ 1) + 2 * (t & 3));
+    const float so = cl_ld1(cl_map(smem_u32(&ms.ssx[t]), own));
+    const float sp = cl_ld1(cl_map(smem_u32(&ms.ssx[t]), other));
+    const float rs = cl_ld1(cl_map(smem_u32(&ms.rsc[t]), own));
+    ms.inv[t] = rsqrtf((so + sp) / float(p.d) + p.eps) / rs;
   }
   return true;
 }
@@ -762,11 +804,12 @@ __device__ bool cl_att_input(const CParams& p, CMisc& ms, CState& st, const Task
 // into every peer's O operand.  Lane l holds dims 4l..4l+3 of every
 // 128-vector; the scores of 16 positions are 16 partial dot products per
 // lane, summed by one reduce-scatter.
+template <bool SPLIT>
 __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
   const int k = tk.k, l = tk.l, j = tk.job, R = cl_rows(p, tk), np = cl_npad(R), n8 = np / 8;
   InSrc in;
   if (!cl_att_input(p, ms, st, tk, in)) return false;
-  if (!cl_build_norm(p, ms, st, smem, in, p.layer[l].attn_norm, R)) return false;
+  if (!cl_build_norm<SPLIT>(p, ms, st, smem, in, p.layer[l].attn_norm, R)) return false;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, hh = warp & 1;
   const int P = k == 1 ? 2 : 1, ctx = p.n_steps + 1, pos0 = k == 1 ? 0 : k;
   // warp w: q head hh = w % 2 of frame b = r + 8 (w / 2) (at most 32 frames: one per warp)
@@ -885,11 +928,12 @@ __device__ bool cl_out(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
 // MLP job m of layer l at step k, through the down operand: gate/up over
 // this CTA's tile and K half, then SwiGLU of columns 32r .. 32r+31 of the
 // job's 256 from the peers' partials, written into every peer's down operand.
+template <bool SPLIT>
 __device__ bool cl_gu(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
   const int k = tk.k, l = tk.l, R = cl_rows(p, tk), np = cl_npad(R), n8 = np / 8;
   if (!cl_wait_ctr(p, ms, st, p.att_done + (k - 1) * p.L + l, unsigned(p.n_att * kCl))) return false;
   InSrc in{cl_x(p, k), nullptr, 1, 0};
-  if (!cl_build_norm(p, ms, st, smem, in, p.layer[l].ffn_norm, R)) return false;
+  if (!cl_build_norm<SPLIT>(p, ms, st, smem, in, p.layer[l].ffn_norm, R)) return false;
   if (!cl_drain_part(p, ms, st, smem, R)) return false;
   if (!cl_sync(p, ms, st)) return false;
   cev(p, st, CEV_S1);
@@ -919,11 +963,12 @@ __device__ bool cl_gu(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, co
 // for every frame's last position; CTA r completes rows 64 (r%2) .. +63 of
 // tile r/2, writes them out if asked and folds their argmax (lowest index
 // on ties) into the frame's decision word.
+template <bool SPLIT>
 __device__ bool cl_head(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
   const int k = tk.k, R = p.B;
   if (!cl_wait_ctr(p, ms, st, p.mlp_done + (k - 1) * p.L + (p.L - 1), unsigned(p.n_mlp * kCl))) return false;
   InSrc in{cl_x(p, k), nullptr, k == 1 ? 2 : 1, k == 1 ? 1 : 0};
-  if (!cl_build_norm(p, ms, st, smem, in, p.out_norm, R)) return false;
+  if (!cl_build_norm<SPLIT>(p, ms, st, smem, in, p.out_norm, R)) return false;
   if (!cl_drain_part(p, ms, st, smem, R)) return false;
   if (!cl_sync(p, ms, st)) return false;
   cev(p, st, CEV_S1);
@@ -960,6 +1005,7 @@ __device__ bool cl_head(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, 
   return true;
 }
 
+template <bool SPLIT>
 __device__ void cl_consumer(const CParams& p, CMisc& ms, uint8_t* smem) {
   CState st{0u, 0u, 0u, int(cl_rank()), 0, 0u};
   const Prog g = cl_prog(p);
@@ -971,9 +1017,9 @@ __device__ void cl_consumer(const CParams& p, CMisc& ms, uint8_t* smem) {
     bool ok = true;
     switch (tk.kind) {
       case T_PROJ: ok = cl_proj(p, ms, st, smem, tk); break;
-      case T_QKV: ok = cl_qkv(p, ms, st, smem, tk); break;
-      case T_GU: ok = cl_gu(p, ms, st, smem, tk); break;
-      case T_HEAD: ok = cl_head(p, ms, st, smem, tk); break;
+      case T_QKV: ok = cl_qkv<SPLIT>(p, ms, st, smem, tk); break;
+      case T_GU: ok = cl_gu<SPLIT>(p, ms, st, smem, tk); break;
+      case T_HEAD: ok = cl_head<SPLIT>(p, ms, st, smem, tk); break;
       default: ok = cl_out(p, ms, st, smem, tk); break;   // T_O, T_DOWN
     }
     if (!ok) return;
@@ -988,6 +1034,11 @@ __device__ void cl_consumer(const CParams& p, CMisc& ms, uint8_t* smem) {
   }
 }
 
+// SPLIT: the build that shares the loads of a K half among four CTAs is
+// compiled in (batches of kClSplitRows frames and more); without it the
+// kernel's code stays smaller, which shows at small batches (119.8 vs 125.0
+// us per step at one frame, measured).
+template <bool SPLIT>
 __global__ void __launch_bounds__(kClThreads, 1) k_frames_cluster(const CParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1008,7 +1059,7 @@ __global__ void __launch_bounds__(kClThreads, 1) k_frames_cluster(const CParams 
   tc_fence_after();
 
   if (warp < kClConsWarps) {
-    cl_consumer(p, ms, smem);
+    cl_consumer<SPLIT>(p, ms, smem);
   } else if (warp == kClProdWarp) {
     if ((t & 31) == 0) cl_producer(p, ms, smem);
     __syncwarp();
@@ -1059,7 +1110,8 @@ int cl_clusters(int dev) {
   int n = slot->load(std::memory_order_acquire);
   if (n != 0) return n;
   const int smem = int(cl_smem_bytes());
-  if (cudaFuncSetAttribute(k_frames_cluster, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+  if (cudaFuncSetAttribute(k_frames_cluster<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_frames_cluster<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
     cudaGetLastError();
     n = -1;
   } else {
@@ -1070,11 +1122,13 @@ int cl_clusters(int dev) {
     cfg.gridDim = dim3(kCl); cfg.blockDim = dim3(kClThreads); cfg.dynamicSmemBytes = size_t(smem);
     cfg.attrs = at; cfg.numAttrs = 1;
     int m = 0;
-    if (cudaOccupancyMaxActiveClusters(&m, k_frames_cluster, &cfg) != cudaSuccess || m < 1) {
+    int m2 = 0;
+    if (cudaOccupancyMaxActiveClusters(&m, k_frames_cluster<false>, &cfg) != cudaSuccess || m < 1 ||
+        cudaOccupancyMaxActiveClusters(&m2, k_frames_cluster<true>, &cfg) != cudaSuccess || m2 < 1) {
       cudaGetLastError();
       n = -1;
     } else {
-      n = m;
+      n = std::min(m, m2);
     }
   }
   slot->store(n, std::memory_order_release);
@@ -1157,7 +1211,10 @@ qp_status run_frames_cluster(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   at[1].val.cooperative = 1;
   cfg.gridDim = dim3(n_cl * kCl); cfg.blockDim = dim3(kClThreads); cfg.dynamicSmemBytes = cl_smem_bytes();
   cfg.stream = s; cfg.attrs = at; cfg.numAttrs = 2;
-  if (cudaLaunchKernelEx(&cfg, k_frames_cluster, p) != cudaSuccess) {
+  // the build that shares loads pays off once every step's rows reach kClSplitRows
+  const cudaError_t e = a.B >= kClSplitRows ? cudaLaunchKernelEx(&cfg, k_frames_cluster<true>, p)
+                                                : cudaLaunchKernelEx(&cfg, k_frames_cluster<false>, p);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;
   }

@@ -111,8 +111,8 @@ constexpr int kSmallAutoFrames = 40;
 // Largest batch the cluster engine serves (2B <= 64 activation rows at step
 // 1: its operand and partial buffers share 64 KB of shared memory).  Where it
 // serves a call, QP_ENGINE_AUTO takes it: measured on GB300 at the 1.7B
-// geometry, 118.8 vs 135.6 us per step at 1 frame (small-batch engine),
-// 127.0 vs 143.9 at 8, 165.3 vs 192.7 at 32.
+// geometry, 119.8 vs 135.8 us per step at 1 frame (small-batch engine),
+// 128.2 vs 144.2 at 8, 157.5 vs 193.3 at 32.
 constexpr int kClusterMaxFrames = 32;
 
 }  // namespace qp
