@@ -458,19 +458,31 @@ __device__ __forceinline__ void cl_publish(const CParams& p, CState& st, unsigne
   cev(p, st, CEV_PUB);
 }
 
-// RMSNorm of a 128-vector held as 4 values per lane with the norm's weights
-// w (this lane's four), then rotate-half RoPE with this lane's factors c
-// (pairs (i, i+64) sit in lanes l and l^16).
-__device__ __forceinline__ float4 norm_rope_w(float4 x, float4 w, const float2 (&c)[4], float eps, int lane) {
-  const float r = rsqrtf(warp_sum(x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w) / 128.f + eps);
-  const float v[4] = {x.x * r * w.x, x.y * r * w.y, x.z * r * w.z, x.w * r * w.w};
-  float o[4];
+// RMSNorm of two 128-vectors held as 4 values per lane (a frame's k and its
+// q head) with their norms' weights (this lane's four), then rotate-half
+// RoPE with this lane's factors c (pairs (i, i+64) sit in lanes l and l^16);
+// the two warp reductions interleave, so their shuffle latencies overlap.
+__device__ __forceinline__ void norm_rope_w2(float4 xa, float4 wa, float4 xb, float4 wb, const float2 (&c)[4],
+                                             float eps, int lane, float4& oa, float4& ob) {
+  float sa = xa.x * xa.x + xa.y * xa.y + xa.z * xa.z + xa.w * xa.w;
+  float sb = xb.x * xb.x + xb.y * xb.y + xb.z * xb.z + xb.w * xb.w;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    sa += __shfl_xor_sync(0xffffffffu, sa, o);
+    sb += __shfl_xor_sync(0xffffffffu, sb, o);
+  }
+  const float ra = rsqrtf(sa / 128.f + eps), rb = rsqrtf(sb / 128.f + eps);
+  const float va[4] = {xa.x * ra * wa.x, xa.y * ra * wa.y, xa.z * ra * wa.z, xa.w * ra * wa.w};
+  const float vb[4] = {xb.x * rb * wb.x, xb.y * rb * wb.y, xb.z * rb * wb.z, xb.w * rb * wb.w};
+  float a[4], b[4];
 #pragma unroll
   for (int e = 0; e < 4; ++e) {
-    const float partner = __shfl_xor_sync(0xffffffffu, v[e], 16);
-    o[e] = lane < 16 ? v[e] * c[e].x - partner * c[e].y : v[e] * c[e].x + partner * c[e].y;
+    const float pa = __shfl_xor_sync(0xffffffffu, va[e], 16), pb = __shfl_xor_sync(0xffffffffu, vb[e], 16);
+    a[e] = lane < 16 ? va[e] * c[e].x - pa * c[e].y : va[e] * c[e].x + pa * c[e].y;
+    b[e] = lane < 16 ? vb[e] * c[e].x - pb * c[e].y : vb[e] * c[e].x + pb * c[e].y;
   }
-  return make_float4(o[0], o[1], o[2], o[3]);
+  oa = make_float4(a[0], a[1], a[2], a[3]);
+  ob = make_float4(b[0], b[1], b[2], b[3]);
 }
 
 // L2 loads issued where they stand (volatile: the compiler keeps them ahead
@@ -857,13 +869,13 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
       if (pp > 0)
 #pragma unroll
         for (int e = 0; e < 4; ++e) cs[e] = __ldg(p.rope_cs + pos * 64 + ((lane * 4 + e) & 63));
-      const float4 knew = norm_rope_w(v4[1], knw, cs, p.eps, lane);
+      float4 knew, qn;
+      norm_rope_w2(v4[1], knw, v4[0], qnw, cs, p.eps, lane, knew, qn);
       const float4 vnew = v4[2];
       if (hh == 0) {
         *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = pack4_f16(knew.x, knew.y, knew.z, knew.w);
         *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 1) * p.kvw) = pack4_f16(vnew.x, vnew.y, vnew.z, vnew.w);
       }
-      const float4 qn = norm_rope_w(v4[0], qnw, cs, p.eps, lane);
       float part[16];
 #pragma unroll
       for (int tt = 0; tt < kMaxCtx; ++tt) {
