@@ -42,6 +42,7 @@
 // its whole cluster is done with its shared memory.
 #include <algorithm>
 #include <atomic>
+#include <cstdlib>
 
 #include "qp_device.cuh"
 
@@ -1222,7 +1223,14 @@ qp_status run_frames_cluster(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   at[1].id = cudaLaunchAttributeCooperative;
   at[1].val.cooperative = 1;
   cfg.gridDim = dim3(n_cl * kCl); cfg.blockDim = dim3(kClThreads); cfg.dynamicSmemBytes = cl_smem_bytes();
-  cfg.stream = s; cfg.attrs = at; cfg.numAttrs = 2;
+  // QP_CLUSTER_NO_COOP=1 drops the cooperative attribute (include/qp_debug.h): Nsight Compute
+  // rejects a cooperative launch with a cluster dimension.  Correctness does not rest on it:
+  // every wait is bounded and a cluster's CTAs are always scheduled together.
+  static const bool no_coop = [] {
+    const char* e = getenv("QP_CLUSTER_NO_COOP");
+    return e && e[0] == '1';
+  }();
+  cfg.stream = s; cfg.attrs = at; cfg.numAttrs = no_coop ? 1 : 2;
   // the build that shares loads pays off once every step's rows reach kClSplitRows
   const cudaError_t e = a.B >= kClSplitRows ? cudaLaunchKernelEx(&cfg, k_frames_cluster<true>, p)
                                                 : cudaLaunchKernelEx(&cfg, k_frames_cluster<false>, p);

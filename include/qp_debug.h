@@ -47,6 +47,14 @@ typedef enum {
   QP_ENGINE_CLUSTER = 3
 } qp_engine;
 
+/* The cluster engine is launched cooperatively (all clusters co-resident
+ * or the launch fails).  Nsight Compute rejects a cooperative launch with a
+ * cluster dimension; with the environment variable QP_CLUSTER_NO_COOP=1 set
+ * when the library is first used, the engine is launched without the
+ * cooperative attribute (the grid is still the number of clusters that fit
+ * at once, every wait stays bounded, and a cluster's CTAs are always
+ * scheduled together), so the profiler can capture it. */
+
 /* Select the engine for later calls on h.  A call the selected engine cannot
  * serve returns QP_ERR_ARG: with QP_ENGINE_SMALL more than 64 frames,
  * sampling over a vocabulary above 4096, or the deterministic schedule; with
