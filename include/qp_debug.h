@@ -76,7 +76,10 @@ qp_status qp_set_engine(qp_handle* h, int engine);
  *     completion count out, so the GEMM's consumers wait until the limit
  *     runs out.  The program's GEMMs are numbered in order: 0 is step 1's
  *     projection, then each step's GEMMs (4 per layer: QKV, O, gate/up,
- *     down; then the head).  -1 (the default) turns it off.
+ *     down; then the head).  The cluster engine, whose program is not a
+ *     list of GEMMs, takes any withhold_gemm >= 0 to mean: its first CTA
+ *     leaves out its count of step 1, layer 0's attention job, so every MLP
+ *     job waits until the limit runs out.  -1 (the default) turns it off.
  * QP_ERR_ARG for a null handle, wait_limit_us < 0 or withhold_gemm < -1. */
 qp_status qp_debug_waits(qp_handle* h, int wait_limit_us, int withhold_gemm);
 
