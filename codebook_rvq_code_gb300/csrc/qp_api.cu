@@ -109,7 +109,7 @@ qp_status run(qp_handle* h, const qp::RunArgs& a, cudaStream_t s) {
   if (h->engine == QP_ENGINE_CLUSTER || h->engine == QP_ENGINE_AUTO) {
     const bool cl = qp::cluster_supported(h, a);
     if (h->engine == QP_ENGINE_CLUSTER) return cl ? qp::run_frames_cluster(h, a, s) : QP_ERR_ARG;
-    if (cl) return qp::run_frames_cluster(h, a, s);
+    if (cl && (!qp::cluster_ext(h) || a.B >= qp::kClusterExtAutoFrames)) return qp::run_frames_cluster(h, a, s);
   }
   const bool sm = qp::small_supported(h, a);
   if (h->engine == QP_ENGINE_SMALL && !sm) return QP_ERR_ARG;

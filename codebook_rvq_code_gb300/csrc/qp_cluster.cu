@@ -91,7 +91,8 @@ struct CMisc {
 static_assert(kClOffMisc + sizeof(CMisc) + 1024 <= 227 * 1024, "shared memory layout too large");
 
 struct CLayer {
-  const uint16_t* w[4];    // qkv, o, gu, down: tile-packed f16 (qp_weights.cu)
+  const uint16_t* w[4];    // qkv, o, gu, down: tile-packed f16 (qp_weights.cu); a Q8_0 matrix's hi image
+  const uint16_t* wl[4];   // Q8_0 matrices: the lo image (hi + lo = d * q), else null
   const float* attn_norm; const float* q_norm; const float* k_norm; const float* ffn_norm;
 };
 
@@ -99,16 +100,18 @@ struct CParams {
   int d, qw, kvw, F, V, th, L, n_kv, n_steps, q0_vocab;
   float eps;
   bool embed_f16;
-  const uint16_t* w_proj; const float* b_proj; const uint16_t* e0;
+  const uint16_t* w_proj; const uint16_t* w_proj_lo; const float* b_proj; const uint16_t* e0;
+  bool proj_in;            // Talker-wide code tables: each step's input row is projected (a GEMM per step)
   CLayer layer[kMaxLayers];
   const float* out_norm;
   const uint16_t* embed[kMaxSteps];
   const uint16_t* w_head[kMaxSteps];
+  const uint16_t* w_head_lo[kMaxSteps];   // Q8_0 heads: the lo images, else null
   const float2* rope_cs;
   // scratch
   float* x;                // residual streams [step][2B][d], zeroed per call
   uint16_t* kv;            // f16 [layer][frame][pos][k|v][kv_width]
-  unsigned* proj_done;     // [1]: projection units finished
+  unsigned* proj_done;     // [step]: projection units finished (step 1; every step with Talker-wide tables)
   unsigned* att_done;      // [step][layer]: attention CTAs finished (O added)
   unsigned* mlp_done;      // [step][layer]: MLP CTAs finished (down added)
   unsigned* head_done;     // [step]: head CTAs finished (decisions folded in)
@@ -215,7 +218,7 @@ __device__ __forceinline__ int cl_proj_units(const CParams& p) {
   return g < p.n_proj ? (p.n_proj - 1 - g) / G + 1 : 0;
 }
 struct Prog {
-  int c, na, nm, nh, np, per_layer, per_step;
+  int c, na, nm, nh, np, per_layer, rest;   // rest: a step's tasks after its projection units
 };
 __device__ __forceinline__ Prog cl_prog(const CParams& p) {
   Prog g;
@@ -225,19 +228,41 @@ __device__ __forceinline__ Prog cl_prog(const CParams& p) {
   g.nh = n_mine(p.n_head, p.n_cl, g.c);
   g.np = cl_proj_units(p);
   g.per_layer = 2 * (g.na + g.nm);
-  g.per_step = p.L * g.per_layer + g.nh;
+  g.rest = p.L * g.per_layer + g.nh;
   return g;
 }
-__device__ __forceinline__ int cl_n_tasks(const CParams& p, const Prog& g) { return g.np + p.n_steps * g.per_step; }
+// EXT: the kernel instantiation that serves Q8_0 matrices (their hi and lo
+// images) and Talker-wide code tables (a projection GEMM per step); the
+// other one keeps the smaller code of 16-bit weights and unprojected tables.
+template <bool EXT>
+__device__ __forceinline__ bool cl_proj_in(const CParams& p) { return EXT && p.proj_in; }
+// Projection units of step k's inputs: step 1 always, later steps with Talker-wide tables.
+template <bool EXT>
+__device__ __forceinline__ int cl_step_proj(const CParams& p, const Prog& g, int k) {
+  return (k == 1 || cl_proj_in<EXT>(p)) ? g.np : 0;
+}
+template <bool EXT>
+__device__ __forceinline__ int cl_n_tasks(const CParams& p, const Prog& g) {
+  return g.np + g.rest + (p.n_steps - 1) * (cl_step_proj<EXT>(p, g, 2) + g.rest);
+}
+template <bool EXT>
 __device__ Task cl_task(const CParams& p, const Prog& g, int i) {
   Task t{};
-  if (i < g.np) {
-    t.kind = T_PROJ; t.k = 1; t.l = 0; t.job = int(blockIdx.x) + i * int(gridDim.x);
+  const int first = g.np + g.rest;
+  if (i < first) {
+    t.k = 1;
+  } else {
+    i -= first;
+    const int ps = cl_step_proj<EXT>(p, g, 2) + g.rest;
+    t.k = 2 + i / ps;
+    i %= ps;
+  }
+  const int pk = cl_step_proj<EXT>(p, g, t.k);
+  if (i < pk) {
+    t.kind = T_PROJ; t.l = 0; t.job = int(blockIdx.x) + i * int(gridDim.x);
     return t;
   }
-  i -= g.np;
-  t.k = 1 + i / g.per_step;
-  i %= g.per_step;
+  i -= pk;
   if (i >= p.L * g.per_layer) {
     t.kind = T_HEAD; t.l = p.L; t.job = g.c + (i - p.L * g.per_layer) * p.n_cl;
     return t;
@@ -271,37 +296,50 @@ __device__ __forceinline__ int cl_nsl(const CParams& p, const Task& t) {
     default: return p.d / 256;
   }
 }
-// Weight slice s of the task's unit: tile `mt` of the matrix, K slice `ks`.
-__device__ __forceinline__ const uint8_t* cl_slice(const CParams& p, const Task& t, int s) {
+// Images of each weight slice of the task: 2 for a Q8_0 matrix (hi, lo), else 1.
+template <bool EXT>
+__device__ __forceinline__ int cl_nimg(const CParams& p, const Task& t) {
+  if (!EXT) return 1;
+  switch (t.kind) {
+    case T_PROJ: return p.w_proj_lo ? 2 : 1;
+    case T_HEAD: return p.w_head_lo[t.k - 1] ? 2 : 1;
+    case T_QKV: return p.layer[t.l].wl[0] ? 2 : 1;
+    case T_O: return p.layer[t.l].wl[1] ? 2 : 1;
+    case T_GU: return p.layer[t.l].wl[2] ? 2 : 1;
+    default: return p.layer[t.l].wl[3] ? 2 : 1;
+  }
+}
+// Weight slice s of the task's unit, image img: tile `mt` of the matrix, K slice `ks`.
+__device__ __forceinline__ const uint8_t* cl_slice(const CParams& p, const Task& t, int s, int img) {
   const int r = int(cl_rank()), tq = r >> 1, h = r & 1, nkh = p.d / 256;
   const uint16_t* w;
   int mt, ks, K;
   switch (t.kind) {
     case T_PROJ: {
       const int nks = p.th / kKs;
-      w = p.w_proj; K = p.th; mt = t.job / nks; ks = t.job % nks;
+      w = img ? p.w_proj_lo : p.w_proj; K = p.th; mt = t.job / nks; ks = t.job % nks;
       break;
     }
     case T_QKV: {
       const int j = t.job;
       const int tiles[4] = {2 * j, 2 * j + 1, p.qw / kTileM + j, (p.qw + p.kvw) / kTileM + j};
-      w = p.layer[t.l].w[0]; K = p.d; mt = tiles[tq]; ks = h * nkh + s;
+      w = img ? p.layer[t.l].wl[0] : p.layer[t.l].w[0]; K = p.d; mt = tiles[tq]; ks = h * nkh + s;
       break;
     }
     case T_O:
-      w = p.layer[t.l].w[1]; K = p.qw; mt = r; ks = 2 * t.job + s;
+      w = img ? p.layer[t.l].wl[1] : p.layer[t.l].w[1]; K = p.qw; mt = r; ks = 2 * t.job + s;
       break;
     case T_GU: {
       const int m = t.job, fq = p.F / kTileM;
       const int tiles[4] = {2 * m, 2 * m + 1, fq + 2 * m, fq + 2 * m + 1};
-      w = p.layer[t.l].w[2]; K = p.d; mt = tiles[tq]; ks = h * nkh + s;
+      w = img ? p.layer[t.l].wl[2] : p.layer[t.l].w[2]; K = p.d; mt = tiles[tq]; ks = h * nkh + s;
       break;
     }
     case T_DOWN:
-      w = p.layer[t.l].w[3]; K = p.F; mt = r; ks = 2 * t.job + s;
+      w = img ? p.layer[t.l].wl[3] : p.layer[t.l].w[3]; K = p.F; mt = r; ks = 2 * t.job + s;
       break;
     default:   // T_HEAD
-      w = p.w_head[t.k - 1]; K = p.d; mt = 4 * t.job + tq; ks = h * nkh + s;
+      w = img ? p.w_head_lo[t.k - 1] : p.w_head[t.k - 1]; K = p.d; mt = 4 * t.job + tq; ks = h * nkh + s;
       break;
   }
   return reinterpret_cast<const uint8_t*>(w) + (size_t(mt) * K * kTileM + size_t(ks) * kTileM * kKs) * 2;
@@ -312,20 +350,23 @@ __device__ __forceinline__ uint32_t cl_op_off(const Task& t, int s, uint32_t ops
 }
 
 // ---------------------------------------------------------------- producer
+template <bool EXT>
 __device__ void cl_producer(const CParams& p, CMisc& ms, uint8_t* smem) {
   const uint64_t pol = policy_evict_first();
   const Prog g = cl_prog(p);
-  const int n = cl_n_tasks(p, g);
+  const int n = cl_n_tasks<EXT>(p, g);
   uint32_t it = 0;
   for (int i = 0; i < n; ++i) {
-    const Task t = cl_task(p, g, i);
-    const int nsl = cl_nsl(p, t);
+    const Task t = cl_task<EXT>(p, g, i);
+    const int nsl = cl_nsl(p, t), nimg = cl_nimg<EXT>(p, t);
     for (int s = 0; s < nsl; ++s) {
-      const uint32_t slot = it % kClNW, u = it / kClNW;
-      if (u > 0 && !mwait(p, &ms.wempty[slot], (u - 1) & 1)) goto drain;
-      mbar_expect_tx(&ms.wfull[slot], kClWSlot);
-      bulk_g2s_stream(smem + kClOffW + slot * kClWSlot, cl_slice(p, t, s), kClWSlot, &ms.wfull[slot], pol);
-      ++it;
+      for (int img = 0; img < nimg; ++img) {
+        const uint32_t slot = it % kClNW, u = it / kClNW;
+        if (u > 0 && !mwait(p, &ms.wempty[slot], (u - 1) & 1)) goto drain;
+        mbar_expect_tx(&ms.wfull[slot], kClWSlot);
+        bulk_g2s_stream(smem + kClOffW + slot * kClWSlot, cl_slice(p, t, s, img), kClWSlot, &ms.wfull[slot], pol);
+        ++it;
+      }
     }
   }
 drain:
@@ -333,48 +374,75 @@ drain:
 }
 
 // --------------------------------------------------------------- MMA warp
+__device__ bool cl_wait_slot(const CParams& p, CMisc& ms, uint32_t w, unsigned& evi, int i) {
+  if (mbar_try_wait(&ms.wfull[w % kClNW], (w / kClNW) & 1)) {
+    cl_ev(p, evi, 8192, CEV_WREADY, i);
+    return true;
+  }
+  if (!mwait(p, &ms.wfull[w % kClNW], (w / kClNW) & 1)) return false;
+  cl_ev(p, evi, 8192, CEV_WWAIT, i);
+  return true;
+}
+
+template <bool EXT>
 __device__ void cl_mma(const CParams& p, CMisc& ms, uint8_t* smem) {
   const Prog g = cl_prog(p);
-  const int n = cl_n_tasks(p, g);
+  const int n = cl_n_tasks<EXT>(p, g);
   uint32_t wit = 0, opseq = 0;
   unsigned evi = 0;
   for (int i = 0; i < n; ++i) {
-    const Task t = cl_task(p, g, i);
-    const int nsl = cl_nsl(p, t);
+    const Task t = cl_task<EXT>(p, g, i);
+    const int nsl = cl_nsl(p, t), nimg = cl_nimg<EXT>(p, t);
     if (nsl == 0) continue;
     const int np = cl_npad(cl_rows(p, t));
     const uint32_t idesc = idesc_f16(kTileM, np);
     const uint32_t blb = uint32_t(np / 8) * 128, opsz = uint32_t(np) * kKs * 2;
     // the task's weight slices first (usually there long before the operand):
-    // a wait between MMAs stalls the issuing thread while the tensor pipe drains
-    for (int s = 0; s < nsl; ++s) {
-      const uint32_t w = wit + uint32_t(s);
-      if (mbar_try_wait(&ms.wfull[w % kClNW], (w / kClNW) & 1)) {
-        cl_ev(p, evi, 8192, CEV_WREADY, i);
-      } else {
-        if (!mwait(p, &ms.wfull[w % kClNW], (w / kClNW) & 1)) goto out;
-        cl_ev(p, evi, 8192, CEV_WWAIT, i);
-      }
-    }
+    // a wait between MMAs stalls the issuing thread while the tensor pipe
+    // drains.  A task with more slices than the ring holds (Q8_0 images) waits
+    // for the rest as it goes.
+    const int nw = nsl * nimg, pre = nw <= kClNW ? nw : 0;
+    for (int s = 0; s < pre; ++s)
+      if (!cl_wait_slot(p, ms, wit + uint32_t(s), evi, i)) goto out;
     if (!mwait(p, &ms.opfull, opseq & 1)) goto out;
     cl_ev(p, evi, 8192, CEV_MOP, i);
     tc_fence_after();
-    for (int s = 0; s < nsl; ++s) {
-      const uint32_t ws = wit % kClNW;
-      const uint32_t a0 = smem_u32(smem + kClOffW + ws * kClWSlot);
-      const uint32_t b0 = smem_u32(smem + cl_op_off(t, s, opsz));
+    if (!EXT) {   // one image per slice, all of them already waited for
+      for (int s = 0; s < nsl; ++s) {
+        const uint32_t ws = wit % kClNW;
+        const uint32_t a0 = smem_u32(smem + kClOffW + ws * kClWSlot);
+        const uint32_t b0 = smem_u32(smem + cl_op_off(t, s, opsz));
 #pragma unroll
-      for (int j = 0; j < kKs / 16; ++j) {
-        const uint64_t ad = smem_desc(a0 + uint32_t(j) * 2 * (kTileM / 8) * 128, (kTileM / 8) * 128, 128);
-        const uint64_t bd = smem_desc(b0 + uint32_t(j) * 2 * blb, blb, 128);
-        mma_f16(ms.tmem_base, ad, bd, idesc, (s == 0 && j == 0) ? 0u : 1u);
+        for (int j = 0; j < kKs / 16; ++j) {
+          const uint64_t ad = smem_desc(a0 + uint32_t(j) * 2 * (kTileM / 8) * 128, (kTileM / 8) * 128, 128);
+          const uint64_t bd = smem_desc(b0 + uint32_t(j) * 2 * blb, blb, 128);
+          mma_f16(ms.tmem_base, ad, bd, idesc, (s == 0 && j == 0) ? 0u : 1u);
+        }
+        mma_commit(&ms.wempty[ws]);
+        ++wit;
       }
-      mma_commit(&ms.wempty[ws]);
-      ++wit;
+    } else
+    for (int s = 0; s < nsl; ++s) {
+      const uint32_t b0 = smem_u32(smem + cl_op_off(t, s, opsz));
+      for (int img = 0; img < nimg; ++img) {
+        const uint32_t ws = wit % kClNW;
+        if (!pre) {
+          if (!cl_wait_slot(p, ms, wit, evi, i)) goto out;
+          tc_fence_after();
+        }
+        const uint32_t a0 = smem_u32(smem + kClOffW + ws * kClWSlot);
+#pragma unroll
+        for (int j = 0; j < kKs / 16; ++j) {
+          const uint64_t ad = smem_desc(a0 + uint32_t(j) * 2 * (kTileM / 8) * 128, (kTileM / 8) * 128, 128);
+          const uint64_t bd = smem_desc(b0 + uint32_t(j) * 2 * blb, blb, 128);
+          mma_f16(ms.tmem_base, ad, bd, idesc, (s == 0 && img == 0 && j == 0) ? 0u : 1u);
+        }
+        mma_commit(&ms.wempty[ws]);
+        ++wit;
+      }
     }
     mma_commit(&ms.accfull);
     cl_ev(p, evi, 8192, CEV_COMMIT, i);
-
     ++opseq;
   }
 out:
@@ -722,28 +790,55 @@ __device__ bool cl_drain_resid(const CParams& p, CMisc& ms, CState& st, uint8_t*
 }
 
 // ------------------------------------------------------------ the tasks
-// Step 1's projection unit u (tile u / (th/128), K slice u % (th/128)):
-// rows 2b = H_b and 2b+1 = E0[q0_b], the first two positions of frame b (H
-// and q0 feed the residual loop: "拆解 Qwen3-TTS：OpenVINO 移植过程中的图分离
-// 与调度实践", section 1; their order is a reading).  Each row's slice is
-// scaled by 2^-e into f16's range (e from the slice's mean square) and the
-// partial product by 2^e; the K slice 0 unit adds the bias.
+__device__ __forceinline__ float* cl_x(const CParams& p, int k) { return p.x + size_t(k - 1) * 2 * p.B * p.d; }
+
+// The code each frame's step-k input embeds (k >= 2): the previous step's
+// decision, or the forced one; out of range latches QP_ERR_BAD_TOKEN and is
+// clamped.  Waits for the previous step's decisions first.
+__device__ bool cl_step_codes(const CParams& p, CMisc& ms, CState& st, int k) {
+  if (!cl_wait_ctr(p, ms, st, p.head_done + (k - 2), unsigned(p.n_head * kCl))) return false;
+  const int t = threadIdx.x;
+  if (t < p.B) {
+    int code = unpack_argmax_index(__ldcg(p.best + size_t(k - 2) * p.B + t));
+    if (p.forced) code = p.forced[size_t(t) * p.n_steps + (k - 2)];
+    if (code < 0 || code >= p.V) {
+      set_status(p.status, QP_ERR_BAD_TOKEN);
+      code = code < 0 ? 0 : p.V - 1;
+    }
+    ms.code[t] = code;
+  }
+  named_bar(CBAR_CONS, kClCons);
+  return true;
+}
+
+// Projection unit u of step k's inputs (tile u / (th/128), K slice u %
+// (th/128)).  Step 1: rows 2b = H_b and 2b+1 = E0[q0_b], the first two
+// positions of frame b (H and q0 feed the residual loop: "拆解 Qwen3-TTS：
+// OpenVINO 移植过程中的图分离与调度实践", section 1; their order is a reading).
+// Step k >= 2 with Talker-wide code tables: row b = E[k-2][the frame's
+// code].  Each row's slice is scaled by 2^-e into f16's range (e from the
+// slice's mean square) and the partial product by 2^e; the K slice 0 unit
+// adds the bias.
+template <bool EXT>
 __device__ bool cl_proj(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
-  const int t = threadIdx.x, R = 2 * p.B, np = cl_npad(R), n8 = np / 8;
+  const int k = EXT ? tk.k : 1;
+  if (k > 1 && !cl_step_codes(p, ms, st, k)) return false;
+  const int t = threadIdx.x, R = k == 1 ? 2 * p.B : p.B, np = cl_npad(R), n8 = np / 8;
   const int nks = p.th / kKs, mt = tk.job / nks, ks = tk.job % nks;
   uint16_t* op = reinterpret_cast<uint16_t*>(smem + kClOffOp);
   const int c = t & 15, kl = c * 8;
   for (int n = t >> 4; n < np; n += kClCons / 16) {   // warp-uniform: np is a multiple of 16
     float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
     if (n < R) {
-      const int b = n >> 1;
-      if ((n & 1) == 0) {
-        const float* hr = p.H + size_t(b) * p.th + ks * kKs + kl;
+      if (k > 1) {
+        ld8e(p.embed[k - 2] + size_t(ms.code[n]) * p.th + ks * kKs + kl, p.embed_f16, v);
+      } else if ((n & 1) == 0) {
+        const float* hr = p.H + size_t(n >> 1) * p.th + ks * kKs + kl;
         const float4 a = __ldg(reinterpret_cast<const float4*>(hr));
         const float4 e = __ldg(reinterpret_cast<const float4*>(hr + 4));
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = e.x; v[5] = e.y; v[6] = e.z; v[7] = e.w;
       } else {
-        int q = p.q0[b];
+        int q = p.q0[n >> 1];
         if (q < 0 || q >= p.q0_vocab) {
           if (c == 0 && mt == 0 && ks == 0) set_status(p.status, QP_ERR_BAD_TOKEN);
           q = q < 0 ? 0 : p.q0_vocab - 1;
@@ -769,41 +864,32 @@ __device__ bool cl_proj(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, 
   if (!cl_wait_acc(p, ms, st)) return false;
   const int warp = t >> 5, lane = t & 31, q = warp & 3, ch = warp >> 2, m = mt * kTileM + q * 32 + lane;
   const float bias = ks == 0 ? p.b_proj[m] : 0.f;
-  float* x1 = p.x;
+  float* xk = cl_x(p, k);
   for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {
     float v[8];
     tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      if (col + i < R) red_add_f32(x1 + size_t(col + i) * p.d + m, v[i] * ms.inv[col + i] + bias);
+      if (col + i < R) red_add_f32(xk + size_t(col + i) * p.d + m, v[i] * ms.inv[col + i] + bias);
   }
   tc_fence_before();
-  cl_publish(p, st, p.proj_done);
+  cl_publish(p, st, p.proj_done + (k - 1));
   return true;
 }
 
-__device__ __forceinline__ float* cl_x(const CParams& p, int k) { return p.x + size_t(k - 1) * 2 * p.B * p.d; }
 
 // The wait before a step's layer-l attention job and where its input rows
-// come from.  Step k >= 2, layer 0: the previous step's decisions (each
-// frame's code, or the forced one) select the code embedding rows.
+// come from.  Step k >= 2, layer 0: with code tables as wide as the hidden
+// size the previous step's decisions (each frame's code, or the forced one)
+// select the code embedding rows; with Talker-wide tables the step's
+// projection units wrote the rows.
+template <bool EXT>
 __device__ bool cl_att_input(const CParams& p, CMisc& ms, CState& st, const Task& tk, InSrc& in) {
   const int k = tk.k, l = tk.l;
   in.x = cl_x(p, k); in.emb = nullptr; in.row_mul = 1; in.row_add = 0;
   if (l > 0) return cl_wait_ctr(p, ms, st, p.mlp_done + (k - 1) * p.L + (l - 1), unsigned(p.n_mlp * kCl));
-  if (k == 1) return cl_wait_ctr(p, ms, st, p.proj_done, unsigned(p.n_proj));
-  if (!cl_wait_ctr(p, ms, st, p.head_done + (k - 2), unsigned(p.n_head * kCl))) return false;
-  const int t = threadIdx.x;
-  if (t < p.B) {
-    int code = unpack_argmax_index(__ldcg(p.best + size_t(k - 2) * p.B + t));
-    if (p.forced) code = p.forced[size_t(t) * p.n_steps + (k - 2)];
-    if (code < 0 || code >= p.V) {
-      set_status(p.status, QP_ERR_BAD_TOKEN);
-      code = code < 0 ? 0 : p.V - 1;
-    }
-    ms.code[t] = code;
-  }
-  named_bar(CBAR_CONS, kClCons);
+  if (k == 1 || cl_proj_in<EXT>(p)) return cl_wait_ctr(p, ms, st, p.proj_done + (k - 1), unsigned(p.n_proj));
+  if (!cl_step_codes(p, ms, st, k)) return false;
   in.x = nullptr;
   in.emb = p.embed[k - 2];
   return true;
@@ -817,11 +903,11 @@ __device__ bool cl_att_input(const CParams& p, CMisc& ms, CState& st, const Task
 // into every peer's O operand.  Lane l holds dims 4l..4l+3 of every
 // 128-vector; the scores of 16 positions are 16 partial dot products per
 // lane, summed by one reduce-scatter.
-template <bool SPLIT>
+template <bool SPLIT, bool EXT>
 __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
   const int k = tk.k, l = tk.l, j = tk.job, R = cl_rows(p, tk), np = cl_npad(R), n8 = np / 8;
   InSrc in;
-  if (!cl_att_input(p, ms, st, tk, in)) return false;
+  if (!cl_att_input<EXT>(p, ms, st, tk, in)) return false;
   if (!cl_build_norm<SPLIT>(p, ms, st, smem, in, p.layer[l].attn_norm, R)) return false;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, hh = warp & 1;
   const int P = k == 1 ? 2 : 1, ctx = p.n_steps + 1, pos0 = k == 1 ? 0 : k;
@@ -921,12 +1007,14 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
 
 // O projection of attention job j (after cl_qkv): tile r of W_o over the
 // group's 256 columns, added into the residual stream.
+template <bool EXT>
 __device__ bool cl_out(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
   const int R = cl_rows(p, tk);
   const bool mine = cl_nsl(p, tk) > 0;
   if (mine) {
     if (threadIdx.x == 0) mbar_arrive(&ms.opfull);   // the rows' writers fenced before the sync
-    const uint16_t* emb = (tk.kind == T_O && tk.k > 1 && tk.l == 0 && tk.job == 0) ? p.embed[tk.k - 2] : nullptr;
+    const uint16_t* emb =
+        (tk.kind == T_O && tk.k > 1 && tk.l == 0 && tk.job == 0 && !cl_proj_in<EXT>(p)) ? p.embed[tk.k - 2] : nullptr;
     if (!cl_drain_resid(p, ms, st, smem, cl_x(p, tk.k), R, st.r * kTileM, emb)) return false;
   }
   unsigned* ctr = tk.kind == T_O ? p.att_done + (tk.k - 1) * p.L + tk.l : p.mlp_done + (tk.k - 1) * p.L + tk.l;
@@ -1018,22 +1106,22 @@ __device__ bool cl_head(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, 
   return true;
 }
 
-template <bool SPLIT>
+template <bool SPLIT, bool EXT>
 __device__ void cl_consumer(const CParams& p, CMisc& ms, uint8_t* smem) {
   CState st{0u, 0u, 0u, int(cl_rank()), 0, 0u};
   const Prog g = cl_prog(p);
-  const int nt = cl_n_tasks(p, g);
+  const int nt = cl_n_tasks<EXT>(p, g);
   for (int i = 0; i < nt; ++i) {
-    const Task tk = cl_task(p, g, i);
+    const Task tk = cl_task<EXT>(p, g, i);
     st.task = i;
     cev(p, st, CEV_START);
     bool ok = true;
     switch (tk.kind) {
-      case T_PROJ: ok = cl_proj(p, ms, st, smem, tk); break;
-      case T_QKV: ok = cl_qkv<SPLIT>(p, ms, st, smem, tk); break;
+      case T_PROJ: ok = cl_proj<EXT>(p, ms, st, smem, tk); break;
+      case T_QKV: ok = cl_qkv<SPLIT, EXT>(p, ms, st, smem, tk); break;
       case T_GU: ok = cl_gu<SPLIT>(p, ms, st, smem, tk); break;
       case T_HEAD: ok = cl_head<SPLIT>(p, ms, st, smem, tk); break;
-      default: ok = cl_out(p, ms, st, smem, tk); break;   // T_O, T_DOWN
+      default: ok = cl_out<EXT>(p, ms, st, smem, tk); break;   // T_O, T_DOWN
     }
     if (!ok) return;
   }
@@ -1051,7 +1139,7 @@ __device__ void cl_consumer(const CParams& p, CMisc& ms, uint8_t* smem) {
 // compiled in (batches of kClSplitRows frames and more); without it the
 // kernel's code stays smaller, which shows at small batches (119.8 vs 125.0
 // us per step at one frame, measured).
-template <bool SPLIT>
+template <bool SPLIT, bool EXT>
 __global__ void __launch_bounds__(kClThreads, 1) k_frames_cluster(const CParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1072,12 +1160,12 @@ __global__ void __launch_bounds__(kClThreads, 1) k_frames_cluster(const CParams 
   tc_fence_after();
 
   if (warp < kClConsWarps) {
-    cl_consumer<SPLIT>(p, ms, smem);
+    cl_consumer<SPLIT, EXT>(p, ms, smem);
   } else if (warp == kClProdWarp) {
-    if ((t & 31) == 0) cl_producer(p, ms, smem);
+    if ((t & 31) == 0) cl_producer<EXT>(p, ms, smem);
     __syncwarp();
   } else if (warp == kClMmaWarp) {
-    if ((t & 31) == 0) cl_mma(p, ms, smem);
+    if ((t & 31) == 0) cl_mma<EXT>(p, ms, smem);
     __syncwarp();
   }
   tc_fence_before();
@@ -1098,7 +1186,7 @@ ClLayout cl_layout(const qp_geometry& g, int B) {
   const size_t steps = size_t(g.n_steps), L = size_t(g.layers);
   size_t o = 0;
   Lo.x = o;          o += cl_al256(steps * 2 * B * g.hidden * 4);
-  Lo.proj_done = o;  o += 256;
+  Lo.proj_done = o;  o += cl_al256(steps * 4);
   Lo.att_done = o;   o += cl_al256(steps * L * 4);
   Lo.mlp_done = o;   o += cl_al256(steps * L * 4);
   Lo.head_done = o;  o += cl_al256(steps * 4);
@@ -1123,8 +1211,10 @@ int cl_clusters(int dev) {
   int n = slot->load(std::memory_order_acquire);
   if (n != 0) return n;
   const int smem = int(cl_smem_bytes());
-  if (cudaFuncSetAttribute(k_frames_cluster<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
-      cudaFuncSetAttribute(k_frames_cluster<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
+  if (cudaFuncSetAttribute(k_frames_cluster<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_frames_cluster<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_frames_cluster<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_frames_cluster<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess) {
     cudaGetLastError();
     n = -1;
   } else {
@@ -1136,12 +1226,15 @@ int cl_clusters(int dev) {
     cfg.attrs = at; cfg.numAttrs = 1;
     int m = 0;
     int m2 = 0;
-    if (cudaOccupancyMaxActiveClusters(&m, k_frames_cluster<false>, &cfg) != cudaSuccess || m < 1 ||
-        cudaOccupancyMaxActiveClusters(&m2, k_frames_cluster<true>, &cfg) != cudaSuccess || m2 < 1) {
+    int m3 = 0, m4 = 0;
+    if (cudaOccupancyMaxActiveClusters(&m, k_frames_cluster<false, false>, &cfg) != cudaSuccess || m < 1 ||
+        cudaOccupancyMaxActiveClusters(&m2, k_frames_cluster<true, false>, &cfg) != cudaSuccess || m2 < 1 ||
+        cudaOccupancyMaxActiveClusters(&m3, k_frames_cluster<false, true>, &cfg) != cudaSuccess || m3 < 1 ||
+        cudaOccupancyMaxActiveClusters(&m4, k_frames_cluster<true, true>, &cfg) != cudaSuccess || m4 < 1) {
       cudaGetLastError();
       n = -1;
     } else {
-      n = std::min(m, m2);
+      n = std::min(std::min(m, m2), std::min(m3, m4));
     }
   }
   slot->store(n, std::memory_order_release);
@@ -1152,16 +1245,22 @@ int cl_clusters(int dev) {
 
 size_t cluster_scratch_bytes(const qp_geometry& g, int bmax) { return cl_layout(g, bmax).total; }
 
+bool cluster_ext(const qp_handle* h) {
+  return h->wfmt == WF_Q8_0 || h->hfmt == WF_Q8_0 || h->g.code_embed_dim != h->g.hidden;
+}
+
 bool cluster_geometry_ok(const qp_geometry& g) {
   return g.head_dim == kHeadDim && g.n_q_heads == 2 * g.n_kv_heads && g.hidden % 256 == 0 && g.hidden >= 512 &&
-         g.hidden <= 1024 &&
-         g.ffn % 256 == 0 && g.vocab % 512 == 0 && g.code_embed_dim == g.hidden && g.talker_hidden % kKs == 0 &&
+         g.hidden <= 1024 && g.ffn % 256 == 0 && g.vocab % 512 == 0 &&
+         (g.code_embed_dim == g.hidden || g.code_embed_dim == g.talker_hidden) && g.talker_hidden % kKs == 0 &&
          g.n_steps + 1 <= kMaxCtx && g.layers <= kMaxLayers;
 }
 
 bool cluster_supported(const qp_handle* h, const RunArgs& a) {
   if (!h->carena || !cluster_geometry_ok(h->g)) return false;
-  if (h->wfmt != WF_BF16 || h->hfmt != WF_BF16) return false;
+  // Q8_0 matrices (layers and projection, or heads) through their f16 hi and lo images
+  if (h->wfmt == WF_Q8_0 && !h->layer[0].qkv.w16[0]) return false;
+  if (h->hfmt == WF_Q8_0 && !h->head[0].w16[0]) return false;
   if (a.B < 1 || a.B > h->cmax_batch || a.B > kClusterMaxFrames) return false;
   if (a.temperature > 0.f) return false;
   return cl_clusters(h->device) > 0;
@@ -1179,20 +1278,27 @@ qp_status run_frames_cluster(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   p.th = g.talker_hidden; p.L = g.layers; p.n_kv = g.n_kv_heads; p.n_steps = g.n_steps; p.q0_vocab = g.q0_vocab;
   p.eps = g.rms_eps;
   p.embed_f16 = h->embed_f16;
-  p.w_proj = reinterpret_cast<const uint16_t*>(h->proj.w); p.b_proj = h->b_proj; p.e0 = h->e0;
+  // 16-bit matrices as packed; Q8_0 matrices through their f16 hi and lo images
+  auto hi = [](const PackedMat& m) {
+    return reinterpret_cast<const uint16_t*>(m.fmt == WF_Q8_0 ? m.w16[0] : m.w);
+  };
+  auto lo = [](const PackedMat& m) {
+    return m.fmt == WF_Q8_0 ? reinterpret_cast<const uint16_t*>(m.w16[1]) : nullptr;
+  };
+  p.w_proj = hi(h->proj); p.w_proj_lo = lo(h->proj); p.b_proj = h->b_proj; p.e0 = h->e0;
+  p.proj_in = g.code_embed_dim != g.hidden;
   for (int l = 0; l < g.layers; ++l) {
     const LayerW& Lw = h->layer[l];
-    p.layer[l].w[0] = reinterpret_cast<const uint16_t*>(Lw.qkv.w);
-    p.layer[l].w[1] = reinterpret_cast<const uint16_t*>(Lw.o.w);
-    p.layer[l].w[2] = reinterpret_cast<const uint16_t*>(Lw.gu.w);
-    p.layer[l].w[3] = reinterpret_cast<const uint16_t*>(Lw.down.w);
+    const PackedMat* mats[4] = {&Lw.qkv, &Lw.o, &Lw.gu, &Lw.down};
+    for (int i = 0; i < 4; ++i) { p.layer[l].w[i] = hi(*mats[i]); p.layer[l].wl[i] = lo(*mats[i]); }
     p.layer[l].attn_norm = Lw.attn_norm; p.layer[l].q_norm = Lw.q_norm;
     p.layer[l].k_norm = Lw.k_norm; p.layer[l].ffn_norm = Lw.ffn_norm;
   }
   p.out_norm = h->out_norm;
   for (int j = 0; j < g.n_steps; ++j) {
     p.embed[j] = h->embed[j];
-    p.w_head[j] = reinterpret_cast<const uint16_t*>(h->head[j].w);
+    p.w_head[j] = hi(h->head[j]);
+    p.w_head_lo[j] = lo(h->head[j]);
   }
   p.rope_cs = h->rope_cs;
   p.x = reinterpret_cast<float*>(base + Lo.x);
@@ -1232,8 +1338,11 @@ qp_status run_frames_cluster(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   }();
   cfg.stream = s; cfg.attrs = at; cfg.numAttrs = no_coop ? 1 : 2;
   // the build that shares loads pays off once every step's rows reach kClSplitRows
-  const cudaError_t e = a.B >= kClSplitRows ? cudaLaunchKernelEx(&cfg, k_frames_cluster<true>, p)
-                                                : cudaLaunchKernelEx(&cfg, k_frames_cluster<false>, p);
+  const bool split = a.B >= kClSplitRows, ext = cluster_ext(h);
+  const cudaError_t e = ext ? (split ? cudaLaunchKernelEx(&cfg, k_frames_cluster<true, true>, p)
+                                     : cudaLaunchKernelEx(&cfg, k_frames_cluster<false, true>, p))
+                            : (split ? cudaLaunchKernelEx(&cfg, k_frames_cluster<true, false>, p)
+                                     : cudaLaunchKernelEx(&cfg, k_frames_cluster<false, false>, p));
   if (e != cudaSuccess) {
     cudaGetLastError();
     return QP_ERR_CUDA;

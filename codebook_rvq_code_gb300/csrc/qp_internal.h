@@ -114,6 +114,10 @@ constexpr int kSmallAutoFrames = 40;
 // geometry, 119.8 vs 135.8 us per step at 1 frame (small-batch engine),
 // 128.2 vs 144.2 at 8, 157.5 vs 193.3 at 32.
 constexpr int kClusterMaxFrames = 32;
+// With Q8_0 matrices or Talker-wide code tables (the exporter's layout) the
+// cluster engine is the faster one from 16 frames (measured: 204.4 vs 212.1 us
+// per step at 32 frames, 166.3 vs 164.6 at 8, 159.2 vs 158.2 at 1).
+constexpr int kClusterExtAutoFrames = 16;
 
 }  // namespace qp
 
@@ -171,8 +175,10 @@ qp_status run_frames_static(qp_handle* h, const RunArgs& a, cudaStream_t s);
 size_t persistent_smem_bytes();
 // the Q8_0 build of the tile engine's kernel (qp_persistent_q8.cu)
 qp_status run_tile_q8(qp_handle* h, const RunArgs& a, uint8_t* scratch, const Scratch& L, int bmax, cudaStream_t s);
-// cluster engine (qp_cluster.cu): greedy frame loop, 16-bit weights, at most kClusterMaxFrames
+// cluster engine (qp_cluster.cu): greedy frame loop, at most kClusterMaxFrames
 size_t cluster_scratch_bytes(const qp_geometry& g, int bmax);
+// Q8_0 matrices or Talker-wide code tables: the engine's extended instantiation
+bool cluster_ext(const qp_handle* h);
 bool cluster_geometry_ok(const qp_geometry& g);
 bool cluster_supported(const qp_handle* h, const RunArgs& a);
 qp_status run_frames_cluster(qp_handle* h, const RunArgs& a, cudaStream_t s);

@@ -29,17 +29,19 @@ extern "C" {
  * unit) with at most 64 frames per call: partials go straight into their
  * destination and each consumer builds its operand slice from it, which
  * removes one dependent global round trip per GEMM.  The cluster engine
- * serves greedy calls of at most 32 frames with 16-bit weights, for
- * geometries with head_dim 128, two q heads per kv head, a hidden size of
- * 512 to 1024 (a multiple of 256), an FFN size a multiple of 256, a
- * vocabulary a multiple of 512 and code tables as wide as the hidden size
- * (the 1.7B predictor's): one 8-CTA thread-block cluster per kv head runs
+ * serves greedy calls of at most 32 frames, for geometries with head_dim
+ * 128, two q heads per kv head, a hidden size of 512 to 1024 (a multiple of
+ * 256), an FFN size a multiple of 256 and a vocabulary a multiple of 512
+ * (the 1.7B predictor's), with 16-bit or Q8_0 matrices (Q8_0 through their
+ * f16 hi + lo images) and code tables as wide as the hidden size or as the
+ * Talker state (then projected at every step): one 8-CTA thread-block cluster per kv head runs
  * QKV, attention and O, one per 256 FFN columns gate/up, SwiGLU and down,
  * partial products meeting in the cluster's shared memory, so a layer has two
  * grid-wide dependencies instead of five.  QP_ENGINE_AUTO (the default) takes
- * the cluster engine where it serves the call, else the small-batch engine
- * for calls of at most 40 frames, else the tile engine: the order of their
- * speed on GB300. */
+ * the cluster engine where it serves the call (with Q8_0 matrices or
+ * Talker-wide tables from 16 frames), else the small-batch engine for calls
+ * of at most 40 frames, else the tile engine: the order of their speed on
+ * GB300. */
 typedef enum {
   QP_ENGINE_AUTO = 0,
   QP_ENGINE_TILE = 1,

@@ -1,8 +1,10 @@
 """The cluster engine (QP_ENGINE_CLUSTER, include/qp_debug.h) against the
 oracle, through the C ABI: the greedy frame loop on 8-CTA clusters, for
 geometries with a hidden size of 512..1024 (multiple of 256), an FFN and a
-vocabulary that split into 256- and 512-wide jobs, 16-bit weights, and at
-most 32 frames.
+vocabulary that split into 256- and 512-wide jobs, and at most 32 frames;
+16-bit or Q8_0 matrices (through their exact f16 hi + lo images), code
+tables as wide as the hidden size or as the Talker state (projected at
+every step).
 """
 import dataclasses
 import time
@@ -133,14 +135,6 @@ def test_cluster_refuses_what_it_cannot_serve(qpk, cl_small):
             big.predict(H[:2], q0[:2], sampling=(0.8, 10, gum))   # sampling
     finally:
         big.close()
-    q8 = qpk.CodePredictor(CL, max_batch=4)
-    try:
-        q8.load_raw_weights(S.make_weights(CL, seed=87, gemm_format="q8_0"))
-        q8.set_engine("cluster")
-        with pytest.raises(qpk.QpError):
-            q8.predict(H[:2], q0[:2])                # Q8_0 matrices
-    finally:
-        q8.close()
     small_geo = dataclasses.replace(CL, hidden=256, code_embed_dim=256)   # hidden below 512
     sm = qpk.CodePredictor(small_geo, max_batch=4)
     try:
@@ -189,5 +183,63 @@ def test_cluster_withheld_count_times_out_and_the_handle_recovers(qpk):
         assert elapsed < 0.5, elapsed
         cp.debug_waits(0, -1)
         assert_parity(check_parity(cp, P, H, q0, np.arange(5)))
+    finally:
+        cp.close()
+
+
+@pytest.mark.parametrize("B", [1, 9, 32])
+def test_cluster_q8_0(qpk, B):
+    """Q8_0 matrices through their f16 hi + lo images (two slices per unit)
+    against the oracle's exact d*q weights."""
+    raw = S.make_weights(CL, seed=90 + B, gemm_format="q8_0", norm_mode="perturbed")
+    P = O.Predictor.from_raw(CL, raw)
+    cp = qpk.CodePredictor(CL, max_batch=B)
+    try:
+        cp.load_raw_weights(raw)
+        cp.set_engine("cluster")
+        H, q0 = S.toy_inputs(CL, B, seed=49 + B)
+        assert_parity(check_parity(cp, P, H, q0, np.arange(B)))
+    finally:
+        cp.close()
+
+
+CL_WIDE = dataclasses.replace(CL, code_embed_dim=CL.talker_hidden)
+
+
+@pytest.mark.parametrize("B,fmt", [(1, "bf16"), (17, "bf16"), (3, "q8_0"), (32, "q8_0")])
+def test_cluster_wide_tables(qpk, B, fmt):
+    """Talker-wide code tables: each step's input row is projected by a GEMM
+    spread over all CTAs; with Q8_0 the exporter's layout (f16 heads and
+    tables over Q8_0 matrices)."""
+    kw = {"gemm_format": fmt}
+    if fmt == "q8_0":
+        kw.update(head_format="f16", embed_format="f16")
+    raw = S.make_weights(CL_WIDE, seed=94 + B, norm_mode="perturbed", **kw)
+    P = O.Predictor.from_raw(CL_WIDE, raw)
+    cp = qpk.CodePredictor(CL_WIDE, max_batch=B)
+    try:
+        cp.load_raw_weights(raw)
+        cp.set_engine("cluster")
+        H, q0 = S.toy_inputs(CL_WIDE, B, seed=53 + B)
+        assert_parity(check_parity(cp, P, H, q0, np.arange(B)))
+    finally:
+        cp.close()
+
+
+@pytest.mark.parametrize("B", [1, 32])
+def test_cluster_exporter_layout_full_geometry(qpk, B):
+    """The exporter's real-model layout at the 1.7B geometry (2048-wide code
+    tables, Q8_0 matrices, f16 heads and tables), sampled frames against the
+    oracle."""
+    g = dataclasses.replace(S.Geometry(), code_embed_dim=S.Geometry().talker_hidden)
+    raw = S.make_weights(g, seed=97, gemm_format="q8_0", head_format="f16", embed_format="f16",
+                         norm_mode="perturbed")
+    P = O.Predictor.from_raw(g, raw)
+    cp = qpk.CodePredictor(g, max_batch=B)
+    try:
+        cp.load_raw_weights(raw)
+        cp.set_engine("cluster")
+        H, q0 = S.toy_inputs(g, B, seed=58 + B)
+        assert_parity(check_parity(cp, P, H, q0, sample_rows(B, 3)))
     finally:
         cp.close()
