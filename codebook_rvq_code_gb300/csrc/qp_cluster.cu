@@ -862,15 +862,31 @@ __device__ bool cl_proj(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, 
   }
   cl_op_ready(p, ms, st);
   if (!cl_wait_acc(p, ms, st)) return false;
-  const int warp = t >> 5, lane = t & 31, q = warp & 3, ch = warp >> 2, m = mt * kTileM + q * 32 + lane;
-  const float bias = ks == 0 ? p.b_proj[m] : 0.f;
+  // as the O and down drains: 32 features x 8 rows per warp through 1 KB of
+  // shared memory (the operand's, read by the finished MMAs), 4 features per
+  // reduction, each row scaled by its 2^e and the bias added by K slice 0
+  const int warp = t >> 5, lane = t & 31, q = warp & 3, ch = warp >> 2, mq = mt * kTileM + q * 32;
+  const int k4 = (lane & 7) * 4;
+  const float4 bias = ks == 0 ? __ldg(reinterpret_cast<const float4*>(p.b_proj + mq + k4)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  float* tp = reinterpret_cast<float*>(smem + kClOffOp) + warp * 256;   // [8 rows][32 features]
   float* xk = cl_x(p, k);
-  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {
+  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {   // warp-uniform
     float v[8];
     tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (col + i < R) red_add_f32(xk + size_t(col + i) * p.d + m, v[i] * ms.inv[col + i] + bias);
+    for (int i = 0; i < 8; ++i) tp[i * 32 + lane] = v[i];
+    __syncwarp();
+#pragma unroll
+    for (int pass = 0; pass < 2; ++pass) {
+      const int f = pass * 4 + (lane >> 3), n = col + f;
+      if (n < R) {
+        const float4 a = *reinterpret_cast<const float4*>(tp + f * 32 + k4);
+        const float sc = ms.inv[n];
+        red_add_v4_f32(xk + size_t(n) * p.d + mq + k4,
+                       make_float4(a.x * sc + bias.x, a.y * sc + bias.y, a.z * sc + bias.z, a.w * sc + bias.w));
+      }
+    }
+    __syncwarp();
   }
   tc_fence_before();
   cl_publish(p, st, p.proj_done + (k - 1));

@@ -243,3 +243,39 @@ def test_cluster_exporter_layout_full_geometry(qpk, B):
         assert_parity(check_parity(cp, P, H, q0, sample_rows(B, 3)))
     finally:
         cp.close()
+
+
+def test_cluster_bad_forced_code_is_reported(cl_small):
+    """A forced code outside [0, vocab) latches QP_ERR_BAD_TOKEN and is
+    clamped; the call still finishes."""
+    import torch
+    raw, P, cp = cl_small
+    H, q0 = S.toy_inputs(CL, 4, seed=61)
+    forced = np.zeros((4, CL.n_steps), np.int32)
+    forced[2, 5] = CL.vocab + 3
+    cp.predict(torch.from_numpy(H).cuda(), torch.from_numpy(q0).cuda(),
+               forced=torch.from_numpy(forced).cuda())
+    torch.cuda.synchronize()
+    assert cp.device_status() == 8    # QP_ERR_BAD_TOKEN
+    assert cp.device_status() == 0
+
+
+def test_cluster_deterministic_mode_goes_to_the_tile_engine(qpk, cl_small):
+    """The deterministic schedule is the tile engine's: forcing the cluster
+    engine with it is refused, AUTO serves it."""
+    import torch
+    raw, P, cp = cl_small
+    H, q0 = S.toy_inputs(CL, 3, seed=62)
+    tH, tq = torch.from_numpy(H).cuda(), torch.from_numpy(q0).cuda()
+    cp.set_deterministic(True)
+    try:
+        with pytest.raises(qpk.QpError) as e:
+            cp.predict(tH, tq)
+        assert e.value.code == 1
+        cp.set_engine("auto")
+        a = cp.predict(tH, tq).cpu().numpy()
+        b = cp.predict(tH, tq).cpu().numpy()
+        np.testing.assert_array_equal(a, b)
+    finally:
+        cp.set_deterministic(False)
+        cp.set_engine("cluster")
