@@ -279,3 +279,25 @@ def test_cluster_deterministic_mode_goes_to_the_tile_engine(qpk, cl_small):
     finally:
         cp.set_deterministic(False)
         cp.set_engine("cluster")
+
+
+def test_cluster_stress_random_batches(cl_small):
+    """Forty calls back to back with random batch sizes (both kernel
+    instantiations), teacher-forced to the tile engine's codes: every call's
+    logits match the tile engine's on the same inputs, so no buffer, counter
+    or cluster barrier of one call leaks into the next."""
+    import torch
+    raw, P, cp = cl_small
+    rng = np.random.default_rng(7)
+    for it in range(40):
+        B = int(rng.integers(1, 33))
+        H, q0 = S.toy_inputs(CL, B, seed=1000 + it)
+        try:
+            cp.set_engine("tile")
+            codes_t, logits_t = run_gpu(cp, H, q0)
+            cp.set_engine("cluster")
+            codes_c, logits_c = run_gpu(cp, H, q0, forced=codes_t)
+        finally:
+            cp.set_engine("cluster")
+        err = float(np.abs(logits_c - logits_t).max())
+        assert err <= 5e-3, (it, B, err)
