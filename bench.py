@@ -332,10 +332,10 @@ def whole_job(local_ms: float, frames_per_step: int, steps: int, world: int, dev
 
 def engine_of(B: int, gemm_format: str, sampled: bool = False) -> str:
     """The schedule QP_ENGINE_AUTO picks (include/qp_debug.h) at the 1.7B
-    geometry: the cluster engine for greedy calls of at most 32 frames with
-    16-bit weights, else the small-batch engine for calls of at most 40
-    frames (either weight format), else the tile engine."""
-    if gemm_format == "bf16" and not sampled and B <= 32:
+    geometry (either table width): the cluster engine for greedy calls of at
+    most 32 frames (either weight format), else the small-batch engine for
+    calls of at most 40 frames, else the tile engine."""
+    if not sampled and B <= 32:
         return "cluster"
     return "small" if B <= 40 else "tile"
 
@@ -473,9 +473,9 @@ def work_exporter(g, B: int):
 def exporter_rows(dev, stream, steps, hbm, tc):
     """The exporter's model layout (2048-wide code tables through small_to_mtp,
     Q8_0 matrices, f16 heads and tables), random weights, greedy, at one frame
-    (the small-batch engine, which streams each Q8_0 matrix as its f16 hi and
-    lo images: 4 B per weight against the blocks' 1.0625) and at 256 frames
-    (the tile engine, which streams the blocks and dequantises on chip)."""
+    (the cluster engine, which streams each Q8_0 matrix as its f16 hi and lo
+    images: 4 B per weight against the blocks' 1.0625) and at 256 frames (the
+    tile engine, which streams the blocks and dequantises on chip)."""
     import dataclasses
     import torch
     import codebook_rvq_code_gb300 as qpk

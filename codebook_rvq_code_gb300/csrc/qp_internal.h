@@ -115,9 +115,10 @@ constexpr int kSmallAutoFrames = 40;
 // 123.7 vs 144.2 at 8, 154.1 vs 193.7 at 32.
 constexpr int kClusterMaxFrames = 32;
 // With Q8_0 matrices or Talker-wide code tables (the exporter's layout) the
-// cluster engine is the faster one from 16 frames (measured: 204.4 vs 212.1 us
-// per step at 32 frames, 166.3 vs 164.6 at 8, 159.2 vs 158.2 at 1).
-constexpr int kClusterExtAutoFrames = 16;
+// cluster engine is the faster one at every batch it serves (measured, against
+// the small-batch engine: 155.8 vs 158.5 us per step at 1 frame, 162.7 vs 164.7
+// at 8, 171.1 vs 177.8 at 16, 201.3 vs 212.6 at 32).
+constexpr int kClusterExtAutoFrames = 1;
 
 }  // namespace qp
 

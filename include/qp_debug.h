@@ -38,10 +38,9 @@ extern "C" {
  * QKV, attention and O, one per 256 FFN columns gate/up, SwiGLU and down,
  * partial products meeting in the cluster's shared memory, so a layer has two
  * grid-wide dependencies instead of five.  QP_ENGINE_AUTO (the default) takes
- * the cluster engine where it serves the call (with Q8_0 matrices or
- * Talker-wide tables from 16 frames), else the small-batch engine for calls
- * of at most 40 frames, else the tile engine: the order of their speed on
- * GB300. */
+ * the cluster engine where it serves the call, else the small-batch engine
+ * for calls of at most 40 frames, else the tile engine: the order of their
+ * speed on GB300. */
 typedef enum {
   QP_ENGINE_AUTO = 0,
   QP_ENGINE_TILE = 1,
