@@ -65,6 +65,8 @@ constexpr uint32_t kClWSlot = kTileM * kKs * 2;       // one 128 x 128 f16 weigh
 // 116.6 us per step at one frame and 154.1 at 32, against 120.5 and 155.6
 // with five).
 constexpr int kClNW = 4;
+// the 16-bit MMA loop waits for all of a task's slices (up to four) before its first MMA
+static_assert(kClNW >= 4, "a 16-bit task's weight slices must all fit the ring");
 constexpr uint32_t kClOffW = 0;
 constexpr uint32_t kClOffOp = kClNW * kClWSlot;       // operand region (K half; then the partials)
 constexpr uint32_t kClOpBytes = 65536;
