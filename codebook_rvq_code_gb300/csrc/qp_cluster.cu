@@ -81,6 +81,7 @@ enum { T_PROJ = 0, T_QKV, T_O, T_GU, T_DOWN, T_HEAD };
 struct CMisc {
   uint64_t wfull[kClNW], wempty[kClNW];
   uint64_t opfull, accfull, mmadone;
+  uint64_t opx;                  // the O or down operand's rows, written by the peers, have landed
   uint64_t cbar[2];              // cluster syncs: one arrival from each CTA of the cluster
   uint32_t tmem_base;
   int flag[2];                   // a wait's outcome for all consumers (alternating: a fast thread's next
@@ -172,6 +173,13 @@ __device__ __forceinline__ float cl_ld1(uint32_t a) {
 }
 __device__ __forceinline__ void cl_st4(uint32_t a, uint4 v) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+// Asynchronous store into a peer's shared memory, counted in bytes on the
+// peer's mbarrier at cluster address `bar`.
+__device__ __forceinline__ void cl_st2_async(uint32_t a, uint2 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(a),
+               "r"(v.x), "r"(v.y), "r"(bar)
                : "memory");
 }
 __device__ __forceinline__ void cl_st2(uint32_t a, uint2 v) {
@@ -393,7 +401,7 @@ template <bool EXT>
 __device__ void cl_mma(const CParams& p, CMisc& ms, uint8_t* smem) {
   const Prog g = cl_prog(p);
   const int n = cl_n_tasks<EXT>(p, g);
-  uint32_t wit = 0, opseq = 0;
+  uint32_t wit = 0, opw = 0, xseq = 0;   // weight slots; phases of opfull and of opx waited for
   unsigned evi = 0;
   for (int i = 0; i < n; ++i) {
     const Task t = cl_task<EXT>(p, g, i);
@@ -409,7 +417,15 @@ __device__ void cl_mma(const CParams& p, CMisc& ms, uint8_t* smem) {
     const int nw = nsl * nimg, pre = nw <= kClNW ? nw : 0;
     for (int s = 0; s < pre; ++s)
       if (!cl_wait_slot(p, ms, wit + uint32_t(s), evi, i)) goto out;
-    if (!mwait(p, &ms.opfull, opseq & 1)) goto out;
+    if (t.kind == T_O || t.kind == T_DOWN) {
+      // the peers' asynchronous stores of the operand's rows, counted on opx
+      if (!mwait(p, &ms.opx, xseq & 1)) goto out;
+      ++xseq;
+      fence_proxy_async_shared();   // those generic-proxy writes, for the tensor cores' reads
+    } else {
+      if (!mwait(p, &ms.opfull, opw & 1)) goto out;
+      ++opw;
+    }
     cl_ev(p, evi, 8192, CEV_MOP, i);
     tc_fence_after();
     if (!EXT) {   // one image per slice, all of them already waited for
@@ -448,7 +464,6 @@ __device__ void cl_mma(const CParams& p, CMisc& ms, uint8_t* smem) {
     }
     mma_commit(&ms.accfull);
     cl_ev(p, evi, 8192, CEV_COMMIT, i);
-    ++opseq;
   }
 out:
   mma_commit(&ms.mmadone);
@@ -952,6 +967,10 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
 #pragma unroll
   for (int e = 0; e < 4; ++e) cs[e] = __ldg(p.rope_cs + pos0 * 64 + ((lane * 4 + e) & 63));
   if (!cl_drain_part(p, ms, st, smem, R)) return false;
+  // this CTA's O operand will hold R rows x 256 columns of f16, written by
+  // the peers' attention warps; the expectation is set before the sync that
+  // lets them write
+  if (threadIdx.x == 0 && st.r < p.d / kTileM) mbar_expect_tx(&ms.opx, uint32_t(R) * 512u);
   if (!cl_sync(p, ms, st)) return false;
   cev(p, st, CEV_S1);
   const float scale = rsqrtf(float(kHeadDim));
@@ -959,6 +978,7 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
   const uint32_t part0 = smem_u32(smem + kClOffOp) + uint32_t(lane) * 16;
   const uint32_t opsz = uint32_t(np) * kKs * 2;
   const uint32_t o0 = smem_u32(smem + kClOffOp2) + uint32_t(hh) * opsz;
+  const int n_dst = min(kCl, p.d / kTileM);   // the CTAs with an O tile
   if (b < p.B) {
     float4 kprev = z4, vprev = z4;   // step 1: position 0's k and v, for position 1
     for (int pp = 0; pp < P; ++pp) {
@@ -1014,16 +1034,14 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
       const uint2 hv = pack4_f16(o1.x, o1.y, o1.z, o1.w);
       const uint32_t a = o0 + op_idx(n, lane * 4, n8) * 2;
 #pragma unroll
-      for (int dst = 0; dst < kCl; ++dst) cl_st2(cl_map(a, uint32_t(dst)), hv);
+      const uint32_t xbar = smem_u32(&ms.opx);
+      for (int dst = 0; dst < n_dst; ++dst) cl_st2_async(cl_map(a, uint32_t(dst)), hv, cl_map(xbar, uint32_t(dst)));
       kprev = knew;
       vprev = vnew;
     }
-    fence_proxy_async_cluster();   // the rows written for the peers' tensor cores
   }
   cev(p, st, CEV_WORK);
-  const bool ok = cl_sync(p, ms, st);   // every O operand row is in place
-  cev(p, st, CEV_S3);
-  return ok;
+  return true;   // each peer's MMA warp waits until its O operand's rows have landed
 }
 
 // O projection of attention job j (after cl_qkv): tile r of W_o over the
@@ -1033,7 +1051,6 @@ __device__ bool cl_out(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
   const int R = cl_rows(p, tk);
   const bool mine = cl_nsl(p, tk) > 0;
   if (mine) {
-    if (threadIdx.x == 0) mbar_arrive(&ms.opfull);   // the rows' writers fenced before the sync
     const uint16_t* emb =
         (tk.kind == T_O && tk.k > 1 && tk.l == 0 && tk.job == 0 && !cl_proj_in<EXT>(p)) ? p.embed[tk.k - 2] : nullptr;
     if (!cl_drain_resid(p, ms, st, smem, cl_x(p, tk.k), R, st.r * kTileM, emb)) return false;
@@ -1057,6 +1074,8 @@ __device__ bool cl_gu(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, co
   InSrc in{cl_x(p, k), nullptr, 1, 0};
   if (!cl_build_norm<SPLIT>(p, ms, st, smem, in, p.layer[l].ffn_norm, R)) return false;
   if (!cl_drain_part(p, ms, st, smem, R)) return false;
+  // this CTA's down operand will hold R rows x 256 columns of f16, written by the peers
+  if (threadIdx.x == 0 && st.r < p.d / kTileM) mbar_expect_tx(&ms.opx, uint32_t(R) * 512u);
   if (!cl_sync(p, ms, st)) return false;
   cev(p, st, CEV_S1);
   const int t = threadIdx.x, c4 = t & 7, r = st.r;
@@ -1064,21 +1083,18 @@ __device__ bool cl_gu(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, co
   const uint32_t opsz = uint32_t(np) * kKs * 2;
   const uint32_t part0 = smem_u32(smem + kClOffOp) + uint32_t(m) * 4;
   const uint32_t o0 = smem_u32(smem + kClOffOp2) + uint32_t(tg) * opsz;   // slice c / 128 = r / 4
+  const int n_dst = min(kCl, p.d / kTileM);   // the CTAs with a down tile
   for (int n = t >> 3; n < R; n += kClCons / 8) {
     const uint32_t a = part0 + uint32_t(n) * kTileM * 4;
     const float4 g0 = cl_ld4(cl_map(a, uint32_t(2 * tg))), g1 = cl_ld4(cl_map(a, uint32_t(2 * tg + 1)));
     const float4 u0 = cl_ld4(cl_map(a, uint32_t(2 * tu))), u1 = cl_ld4(cl_map(a, uint32_t(2 * tu + 1)));
     const uint2 hv = pack4_f16(silu_f(g0.x + g1.x) * (u0.x + u1.x), silu_f(g0.y + g1.y) * (u0.y + u1.y),
                                silu_f(g0.z + g1.z) * (u0.z + u1.z), silu_f(g0.w + g1.w) * (u0.w + u1.w));
-    const uint32_t d = o0 + op_idx(n, m, n8) * 2;
-#pragma unroll
-    for (int dst = 0; dst < kCl; ++dst) cl_st2(cl_map(d, uint32_t(dst)), hv);
+    const uint32_t d = o0 + op_idx(n, m, n8) * 2, xbar = smem_u32(&ms.opx);
+    for (int dst = 0; dst < n_dst; ++dst) cl_st2_async(cl_map(d, uint32_t(dst)), hv, cl_map(xbar, uint32_t(dst)));
   }
-  if ((t >> 3) < R) fence_proxy_async_cluster();   // the rows written for the peers' tensor cores
   cev(p, st, CEV_WORK);
-  const bool ok = cl_sync(p, ms, st);   // every down operand row is in place
-  cev(p, st, CEV_S3);
-  return ok;
+  return true;   // each peer's MMA warp waits until its down operand's rows have landed
 }
 
 // Head job hj at step k: logits 512 hj .. 512 hj + 511 of the step's head
@@ -1171,6 +1187,7 @@ __global__ void __launch_bounds__(kClThreads, 1) k_frames_cluster(const CParams 
     mbar_init(&ms.opfull, 1);
     mbar_init(&ms.accfull, 1);
     mbar_init(&ms.mmadone, 1);
+    mbar_init(&ms.opx, 1);
     mbar_init(&ms.cbar[0], kCl);
     mbar_init(&ms.cbar[1], kCl);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
