@@ -71,7 +71,11 @@ constexpr uint32_t kClOffW = 0;
 constexpr uint32_t kClOffOp = kClNW * kClWSlot;       // operand region (K half; then the partials)
 constexpr uint32_t kClOpBytes = 65536;
 constexpr uint32_t kClOffOp2 = kClOffOp + 32768;      // O / down operand (second half of the region)
-constexpr uint32_t kClOffMisc = kClOffOp + kClOpBytes;
+// Partial products pushed here by the peers: an attention CTA's frames (q|k|v
+// tiles x K halves), or a SwiGLU CTA's 32 columns of gate and up.
+constexpr uint32_t kClOffRecv = kClOffOp + kClOpBytes;
+constexpr uint32_t kClRecvBytes = 32768;
+constexpr uint32_t kClOffMisc = kClOffRecv + kClRecvBytes;
 constexpr uint32_t kClTmemCols = 64;                  // one accumulator of up to 64 columns
 static_assert(kClusterMaxFrames <= kCl * kClConsWarps / 2, "attention: one (frame, q head) per warp");
 
@@ -82,6 +86,7 @@ struct CMisc {
   uint64_t wfull[kClNW], wempty[kClNW];
   uint64_t opfull, accfull, mmadone;
   uint64_t opx;                  // the O or down operand's rows, written by the peers, have landed
+  uint64_t prx;                  // the partial products this CTA consumes have landed
   uint64_t cbar[2];              // cluster syncs: one arrival from each CTA of the cluster
   uint32_t tmem_base;
   int flag[2];                   // a wait's outcome for all consumers (alternating: a fast thread's next
@@ -180,6 +185,11 @@ __device__ __forceinline__ void cl_st4(uint32_t a, uint4 v) {
 __device__ __forceinline__ void cl_st2_async(uint32_t a, uint2 v, uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(a),
                "r"(v.x), "r"(v.y), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void cl_st4_async(uint32_t a, float4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(a),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
                : "memory");
 }
 __device__ __forceinline__ void cl_st2(uint32_t a, uint2 v) {
@@ -475,6 +485,7 @@ struct CState {
   uint32_t opseq;   // tasks whose MMA ran
   uint32_t cseq;    // cluster syncs passed
   uint32_t fseq;    // waits whose outcome went through ms.flag
+  uint32_t rseq;    // phases of ms.prx
   int r;            // rank in the cluster
   int task;         // the task in progress (event log)
   unsigned evi;     // events logged (thread 0)
@@ -771,6 +782,73 @@ __device__ bool cl_drain_part(const CParams& p, CMisc& ms, CState& st, uint8_t* 
   return true;
 }
 
+// Frames b = r (mod 8) run attention in CTA r: activation row n (frame n /
+// P, position n % P) lands in CTA (n / P) % 8 as its local row
+// ((n / P) / 8) P + n % P.
+__device__ __forceinline__ int att_dst(int n, int P) { return (n / P) % kCl; }
+__device__ __forceinline__ int att_local(int n, int P) { return ((n / P) / kCl) * P + n % P; }
+__device__ __forceinline__ int att_rows(int B, int P, int r) { return r < B ? ((B - 1 - r) / kCl + 1) * P : 0; }
+
+// Drain the accumulator (128 weight rows x R activation rows, scaled by
+// ms.inv per row) straight into the consumers' receive buffers with
+// asynchronous stores counted on their ms.prx.  ATT: row n of tile tq, K
+// half h goes to the frame's attention CTA as recv[local row][tq][h][128];
+// otherwise (gate/up) rows m of tile tq go to the CTA that applies SwiGLU to
+// them, 4 (tq % 2) + m / 32, as recv[n][tq / 2][h][m % 32].  Each warp moves
+// 32 features x 8 rows at a time through 1 KB of its own (the operand region
+// is free once the MMAs are done), 8 consecutive features per lane.
+template <bool ATT>
+__device__ bool cl_drain_push(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, int R, int P) {
+  if (!cl_wait_acc(p, ms, st)) return false;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ch = warp >> 2;
+  const int tq = st.r >> 1, h = st.r & 1;
+  float* tp = reinterpret_cast<float*>(smem + kClOffOp) + warp * 256;   // [8 rows][32 features]
+  const uint32_t recv = smem_u32(smem + kClOffRecv), bar = smem_u32(&ms.prx);
+  const int f = lane >> 2, k8 = (lane & 3) * 8;   // this lane's row in the chunk and its features
+  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {   // warp-uniform
+    float v[8];
+    tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tp[i * 32 + lane] = v[i];
+    __syncwarp();
+    const int n = col + f;
+    if (n < R) {
+      const float sc = ms.inv[n];
+      const float4 a = *reinterpret_cast<const float4*>(tp + f * 32 + k8);
+      const float4 b = *reinterpret_cast<const float4*>(tp + f * 32 + k8 + 4);
+      int dst;
+      uint32_t off;   // byte offset in the destination's receive buffer
+      if (ATT) {
+        dst = att_dst(n, P);
+        off = uint32_t(((att_local(n, P) * 4 + tq) * 2 + h) * kTileM + q * 32 + k8) * 4;
+      } else {
+        dst = 4 * (tq & 1) + q;
+        off = uint32_t(((n * 2 + (tq >> 1)) * 2 + h) * 32 + k8) * 4;
+      }
+      const uint32_t da = cl_map(recv + off, uint32_t(dst)), db = cl_map(bar, uint32_t(dst));
+      cl_st4_async(da, make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc), db);
+      cl_st4_async(da + 16, make_float4(b.x * sc, b.y * sc, b.z * sc, b.w * sc), db);
+    }
+    __syncwarp();
+  }
+  tc_fence_before();
+  return true;
+}
+// Wait (all consumer threads) until this CTA's share of the pushed partial
+// products has landed: `bytes` of them (set here, before or after the peers'
+// stores: a phase needs this arrival as well as the bytes).
+__device__ bool cl_wait_recv(const CParams& p, CMisc& ms, CState& st, uint32_t bytes) {
+  if (bytes == 0) return true;
+  int* f = &ms.flag[st.fseq++ & 1];
+  if (threadIdx.x == 0) {
+    mbar_expect_tx(&ms.prx, bytes);
+    *f = cl_mwait(p, &ms.prx, st.rseq & 1);
+  }
+  ++st.rseq;
+  named_bar(CBAR_CONS, kClCons);
+  return *f != 0;
+}
+
 // Drain the accumulator of an O or down tile (rows m0 .. m0+127 of the
 // residual stream) into the residual rows n < R.  Each warp drains 32
 // features x 8 rows at a time, transposes them through 1 KB of shared
@@ -966,16 +1044,16 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
   float2 cs[4];   // position pos0's (step 1 reloads them for position 1)
 #pragma unroll
   for (int e = 0; e < 4; ++e) cs[e] = __ldg(p.rope_cs + pos0 * 64 + ((lane * 4 + e) & 63));
-  if (!cl_drain_part(p, ms, st, smem, R)) return false;
   // this CTA's O operand will hold R rows x 256 columns of f16, written by
-  // the peers' attention warps; the expectation is set before the sync that
-  // lets them write
+  // the peers' attention warps
   if (threadIdx.x == 0 && st.r < p.d / kTileM) mbar_expect_tx(&ms.opx, uint32_t(R) * 512u);
-  if (!cl_sync(p, ms, st)) return false;
+  if (!cl_drain_push<true>(p, ms, st, smem, R, P)) return false;
+  // this CTA's frames' q|k|v: 4 tiles x 2 K halves x 128 per row
+  if (!cl_wait_recv(p, ms, st, uint32_t(att_rows(p.B, P, st.r)) * 4096u)) return false;
   cev(p, st, CEV_S1);
   const float scale = rsqrtf(float(kHeadDim));
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-  const uint32_t part0 = smem_u32(smem + kClOffOp) + uint32_t(lane) * 16;
+  const float* recv = reinterpret_cast<const float*>(smem + kClOffRecv) + lane * 4;
   const uint32_t opsz = uint32_t(np) * kKs * 2;
   const uint32_t o0 = smem_u32(smem + kClOffOp2) + uint32_t(hh) * opsz;
   const int n_dst = min(kCl, p.d / kTileM);   // the CTAs with an O tile
@@ -985,12 +1063,12 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
       const int n = b * P + pp, pos = pos0 + pp;
       // the frame's q (head hh), k and v: the two K halves of tiles hh, 2 and 3
       float4 v4[3];
+      const int nl = att_local(n, P);
 #pragma unroll
       for (int i = 0; i < 3; ++i) {
         const int tq = i == 0 ? hh : i + 1;
-        const uint32_t a = part0 + uint32_t(n) * kTileM * 4;
-        const float4 h0 = cl_ld4(cl_map(a, uint32_t(2 * tq)));
-        const float4 h1 = cl_ld4(cl_map(a, uint32_t(2 * tq + 1)));
+        const float* a = recv + ((nl * 4 + tq) * 2) * kTileM;
+        const float4 h0 = *reinterpret_cast<const float4*>(a), h1 = *reinterpret_cast<const float4*>(a + kTileM);
         v4[i] = make_float4(h0.x + h1.x, h0.y + h1.y, h0.z + h1.z, h0.w + h1.w);
       }
       if (lane == 0 && threadIdx.x == 0) cl_ev(p, st.evi, 0, CEV_SUB, st.task);
@@ -1073,21 +1151,22 @@ __device__ bool cl_gu(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, co
   if (!cl_wait_ctr(p, ms, st, p.att_done + (k - 1) * p.L + l, unsigned(p.n_att * kCl))) return false;
   InSrc in{cl_x(p, k), nullptr, 1, 0};
   if (!cl_build_norm<SPLIT>(p, ms, st, smem, in, p.layer[l].ffn_norm, R)) return false;
-  if (!cl_drain_part(p, ms, st, smem, R)) return false;
   // this CTA's down operand will hold R rows x 256 columns of f16, written by the peers
   if (threadIdx.x == 0 && st.r < p.d / kTileM) mbar_expect_tx(&ms.opx, uint32_t(R) * 512u);
-  if (!cl_sync(p, ms, st)) return false;
+  if (!cl_drain_push<false>(p, ms, st, smem, R, 1)) return false;
+  // this CTA's 32 columns of gate and up, both K halves: 512 B per row
+  if (!cl_wait_recv(p, ms, st, uint32_t(R) * 512u)) return false;
   cev(p, st, CEV_S1);
   const int t = threadIdx.x, c4 = t & 7, r = st.r;
-  const int tg = r >> 2, tu = 2 + (r >> 2), m = 32 * (r & 3) + 4 * c4;   // tiles of gate and up, row in tile
+  const int tg = r >> 2, m = 32 * (r & 3) + 4 * c4;   // the gate (and up) tile of the columns, row in tile
   const uint32_t opsz = uint32_t(np) * kKs * 2;
-  const uint32_t part0 = smem_u32(smem + kClOffOp) + uint32_t(m) * 4;
+  const float* recv = reinterpret_cast<const float*>(smem + kClOffRecv) + 4 * c4;   // [n][gate|up][half][32]
   const uint32_t o0 = smem_u32(smem + kClOffOp2) + uint32_t(tg) * opsz;   // slice c / 128 = r / 4
   const int n_dst = min(kCl, p.d / kTileM);   // the CTAs with a down tile
   for (int n = t >> 3; n < R; n += kClCons / 8) {
-    const uint32_t a = part0 + uint32_t(n) * kTileM * 4;
-    const float4 g0 = cl_ld4(cl_map(a, uint32_t(2 * tg))), g1 = cl_ld4(cl_map(a, uint32_t(2 * tg + 1)));
-    const float4 u0 = cl_ld4(cl_map(a, uint32_t(2 * tu))), u1 = cl_ld4(cl_map(a, uint32_t(2 * tu + 1)));
+    const float* a = recv + n * 128;
+    const float4 g0 = *reinterpret_cast<const float4*>(a), g1 = *reinterpret_cast<const float4*>(a + 32);
+    const float4 u0 = *reinterpret_cast<const float4*>(a + 64), u1 = *reinterpret_cast<const float4*>(a + 96);
     const uint2 hv = pack4_f16(silu_f(g0.x + g1.x) * (u0.x + u1.x), silu_f(g0.y + g1.y) * (u0.y + u1.y),
                                silu_f(g0.z + g1.z) * (u0.z + u1.z), silu_f(g0.w + g1.w) * (u0.w + u1.w));
     const uint32_t d = o0 + op_idx(n, m, n8) * 2, xbar = smem_u32(&ms.opx);
@@ -1145,7 +1224,7 @@ __device__ bool cl_head(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, 
 
 template <bool SPLIT, bool EXT>
 __device__ void cl_consumer(const CParams& p, CMisc& ms, uint8_t* smem) {
-  CState st{0u, 0u, 0u, int(cl_rank()), 0, 0u};
+  CState st{0u, 0u, 0u, 0u, int(cl_rank()), 0, 0u};
   const Prog g = cl_prog(p);
   const int nt = cl_n_tasks<EXT>(p, g);
   for (int i = 0; i < nt; ++i) {
@@ -1188,6 +1267,7 @@ __global__ void __launch_bounds__(kClThreads, 1) k_frames_cluster(const CParams 
     mbar_init(&ms.accfull, 1);
     mbar_init(&ms.mmadone, 1);
     mbar_init(&ms.opx, 1);
+    mbar_init(&ms.prx, 1);
     mbar_init(&ms.cbar[0], kCl);
     mbar_init(&ms.cbar[1], kCl);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");

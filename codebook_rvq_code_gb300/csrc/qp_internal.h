@@ -111,8 +111,8 @@ constexpr int kSmallAutoFrames = 40;
 // Largest batch the cluster engine serves (2B <= 64 activation rows at step
 // 1: its operand and partial buffers share 64 KB of shared memory).  Where it
 // serves a call, QP_ENGINE_AUTO takes it: measured on GB300 at the 1.7B
-// geometry, 102.3 vs 135.8 us per step at 1 frame (small-batch engine),
-// 110.2 vs 144.0 at 8, 146.0 vs 193.5 at 32.
+// geometry, 92.3 vs 135.2 us per step at 1 frame (small-batch engine),
+// 101.0 vs 143.6 at 8, 140.6 vs 192.9 at 32.
 constexpr int kClusterMaxFrames = 32;
 // With Q8_0 matrices or Talker-wide code tables (the exporter's layout) the
 // cluster engine is the faster one at every batch it serves (measured, against
