@@ -165,12 +165,6 @@ __device__ __forceinline__ bool cl_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ float4 cl_ld4(uint32_t a) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(a)
-               : "memory");
-  return v;
-}
 __device__ __forceinline__ float cl_ld1(uint32_t a) {
   float v;
   asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
@@ -191,9 +185,6 @@ __device__ __forceinline__ void cl_st4_async(uint32_t a, float4 v, uint32_t bar)
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(a),
                "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar)
                : "memory");
-}
-__device__ __forceinline__ void cl_st2(uint32_t a, uint2 v) {
-  asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(a), "r"(v.x), "r"(v.y) : "memory");
 }
 // Hardware barrier of every thread of the cluster.
 __device__ __forceinline__ void cl_barrier_all() {
@@ -763,25 +754,6 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
   return true;
 }
 
-// Drain the accumulator (128 weight rows x R activation rows) into this
-// CTA's partial buffer part[n][m] (f32, at the start of the operand region,
-// whose operand the MMAs have finished reading), each activation row n
-// scaled by ms.inv[n].
-__device__ bool cl_drain_part(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, int R) {
-  if (!cl_wait_acc(p, ms, st)) return false;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ch = warp >> 2;
-  float* part = reinterpret_cast<float*>(smem + kClOffOp);
-  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {   // warp-uniform
-    float v[8];
-    tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      if (col + i < R) part[(col + i) * kTileM + q * 32 + lane] = v[i] * ms.inv[col + i];
-  }
-  tc_fence_before();
-  return true;
-}
-
 // Frames b = r (mod 8) run attention in CTA r: activation row n (frame n /
 // P, position n % P) lands in CTA (n / P) % 8 as its local row
 // ((n / P) / 8) P + n % P.
@@ -791,13 +763,16 @@ __device__ __forceinline__ int att_rows(int B, int P, int r) { return r < B ? ((
 
 // Drain the accumulator (128 weight rows x R activation rows, scaled by
 // ms.inv per row) straight into the consumers' receive buffers with
-// asynchronous stores counted on their ms.prx.  ATT: row n of tile tq, K
-// half h goes to the frame's attention CTA as recv[local row][tq][h][128];
-// otherwise (gate/up) rows m of tile tq go to the CTA that applies SwiGLU to
-// them, 4 (tq % 2) + m / 32, as recv[n][tq / 2][h][m % 32].  Each warp moves
-// 32 features x 8 rows at a time through 1 KB of its own (the operand region
-// is free once the MMAs are done), 8 consecutive features per lane.
-template <bool ATT>
+// asynchronous stores counted on their ms.prx.  PUSH_ATT: row n of tile tq,
+// K half h goes to the frame's attention CTA as recv[local row][tq][h][128];
+// PUSH_GU: rows m of gate/up tile tq go to the CTA that applies SwiGLU to
+// them, 4 (tq % 2) + m / 32, as recv[n][tq / 2][h][m % 32]; PUSH_HEAD: rows m
+// of the tile go to the member of the CTA pair that completes them (m < 64:
+// the K-half-0 CTA) as recv[n][h][m % 64].  Each warp moves 32 features x 8
+// rows at a time through 1 KB of its own (the operand region is free once
+// the MMAs are done), 8 consecutive features per lane.
+enum { PUSH_ATT = 0, PUSH_GU = 1, PUSH_HEAD = 2 };
+template <int MODE>
 __device__ bool cl_drain_push(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, int R, int P) {
   if (!cl_wait_acc(p, ms, st)) return false;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ch = warp >> 2;
@@ -818,12 +793,15 @@ __device__ bool cl_drain_push(const CParams& p, CMisc& ms, CState& st, uint8_t* 
       const float4 b = *reinterpret_cast<const float4*>(tp + f * 32 + k8 + 4);
       int dst;
       uint32_t off;   // byte offset in the destination's receive buffer
-      if (ATT) {
+      if (MODE == PUSH_ATT) {
         dst = att_dst(n, P);
         off = uint32_t(((att_local(n, P) * 4 + tq) * 2 + h) * kTileM + q * 32 + k8) * 4;
-      } else {
+      } else if (MODE == PUSH_GU) {
         dst = 4 * (tq & 1) + q;
         off = uint32_t(((n * 2 + (tq >> 1)) * 2 + h) * 32 + k8) * 4;
+      } else {
+        dst = (st.r & ~1) | (q >> 1);
+        off = uint32_t((n * 2 + h) * 64 + (q & 1) * 32 + k8) * 4;
       }
       const uint32_t da = cl_map(recv + off, uint32_t(dst)), db = cl_map(bar, uint32_t(dst));
       cl_st4_async(da, make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc), db);
@@ -1047,7 +1025,7 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
   // this CTA's O operand will hold R rows x 256 columns of f16, written by
   // the peers' attention warps
   if (threadIdx.x == 0 && st.r < p.d / kTileM) mbar_expect_tx(&ms.opx, uint32_t(R) * 512u);
-  if (!cl_drain_push<true>(p, ms, st, smem, R, P)) return false;
+  if (!cl_drain_push<PUSH_ATT>(p, ms, st, smem, R, P)) return false;
   // this CTA's frames' q|k|v: 4 tiles x 2 K halves x 128 per row
   if (!cl_wait_recv(p, ms, st, uint32_t(att_rows(p.B, P, st.r)) * 4096u)) return false;
   cev(p, st, CEV_S1);
@@ -1111,7 +1089,6 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
       // row n of the O operand (K = the group's 256 columns: head hh in slice hh) in every CTA
       const uint2 hv = pack4_f16(o1.x, o1.y, o1.z, o1.w);
       const uint32_t a = o0 + op_idx(n, lane * 4, n8) * 2;
-#pragma unroll
       const uint32_t xbar = smem_u32(&ms.opx);
       for (int dst = 0; dst < n_dst; ++dst) cl_st2_async(cl_map(a, uint32_t(dst)), hv, cl_map(xbar, uint32_t(dst)));
       kprev = knew;
@@ -1153,7 +1130,7 @@ __device__ bool cl_gu(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, co
   if (!cl_build_norm<SPLIT>(p, ms, st, smem, in, p.layer[l].ffn_norm, R)) return false;
   // this CTA's down operand will hold R rows x 256 columns of f16, written by the peers
   if (threadIdx.x == 0 && st.r < p.d / kTileM) mbar_expect_tx(&ms.opx, uint32_t(R) * 512u);
-  if (!cl_drain_push<false>(p, ms, st, smem, R, 1)) return false;
+  if (!cl_drain_push<PUSH_GU>(p, ms, st, smem, R, 1)) return false;
   // this CTA's 32 columns of gate and up, both K halves: 512 B per row
   if (!cl_wait_recv(p, ms, st, uint32_t(R) * 512u)) return false;
   cev(p, st, CEV_S1);
@@ -1186,17 +1163,17 @@ __device__ bool cl_head(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, 
   if (!cl_wait_ctr(p, ms, st, p.mlp_done + (k - 1) * p.L + (p.L - 1), unsigned(p.n_mlp * kCl))) return false;
   InSrc in{cl_x(p, k), nullptr, k == 1 ? 2 : 1, k == 1 ? 1 : 0};
   if (!cl_build_norm<SPLIT>(p, ms, st, smem, in, p.out_norm, R)) return false;
-  if (!cl_drain_part(p, ms, st, smem, R)) return false;
-  if (!cl_sync(p, ms, st)) return false;
+  if (!cl_drain_push<PUSH_HEAD>(p, ms, st, smem, R, 1)) return false;
+  // this CTA's 64 logits rows of the tile, both K halves: 512 B per frame
+  if (!cl_wait_recv(p, ms, st, uint32_t(R) * 512u)) return false;
   cev(p, st, CEV_S1);
   const int t = threadIdx.x, mg = t & 7, n = t >> 3, r = st.r;
   const int m = 64 * (r & 1) + 8 * mg;
   unsigned long long key = 0ull;
   if (n < R) {
-    const float* part = reinterpret_cast<const float*>(smem + kClOffOp) + n * kTileM + m;
-    const uint32_t pa = cl_map(smem_u32(part), uint32_t(r ^ 1));
+    const float* part = reinterpret_cast<const float*>(smem + kClOffRecv) + n * 128 + 8 * mg;   // [n][half][64]
     const float4 a0 = *reinterpret_cast<const float4*>(part), a1 = *reinterpret_cast<const float4*>(part + 4);
-    const float4 b0 = cl_ld4(pa), b1 = cl_ld4(pa + 16);
+    const float4 b0 = *reinterpret_cast<const float4*>(part + 64), b1 = *reinterpret_cast<const float4*>(part + 68);
     const float lg[8] = {a0.x + b0.x, a0.y + b0.y, a0.z + b0.z, a0.w + b0.w,
                          a1.x + b1.x, a1.y + b1.y, a1.z + b1.z, a1.w + b1.w};
     const int v0 = 512 * tk.job + kTileM * (r >> 1) + m;
