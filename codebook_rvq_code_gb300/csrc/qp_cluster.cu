@@ -87,12 +87,14 @@ struct CMisc {
   uint64_t opfull, accfull, mmadone;
   uint64_t opx;                  // the O or down operand's rows, written by the peers, have landed
   uint64_t prx;                  // the partial products this CTA consumes have landed
+  uint64_t psx;                  // the partner's sums of squares have landed
   uint64_t cbar[2];              // cluster syncs: one arrival from each CTA of the cluster
   uint32_t tmem_base;
   int flag[2];                   // a wait's outcome for all consumers (alternating: a fast thread's next
                                  // wait may write before a slow one has read the last)
   float ssw[kClConsWarps][kClMaxRows / 4];   // per-warp partial sums of squares of one pass's rows
   float ssx[kClMaxRows];         // this CTA's K-half sums of squares per row (its partner reads them)
+  float ssp[kClMaxRows];         // the partner's, stored here by the partner
   float inv[kClMaxRows];         // per row: the factor a drain applies (2^e / RMS, or 2^e for the projection)
   float rsc[kClMaxRows];         // per row: 2^-e, the operand's range scale
   int code[kClMaxRows];          // step k >= 2: the code each frame's input embeds
@@ -179,6 +181,10 @@ __device__ __forceinline__ void cl_st4(uint32_t a, uint4 v) {
 __device__ __forceinline__ void cl_st2_async(uint32_t a, uint2 v, uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(a),
                "r"(v.x), "r"(v.y), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void cl_st1_async(uint32_t a, float v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.f32 [%0], %1, [%2];" ::"r"(a), "f"(v), "r"(bar)
                : "memory");
 }
 __device__ __forceinline__ void cl_st4_async(uint32_t a, float4 v, uint32_t bar) {
@@ -477,6 +483,7 @@ struct CState {
   uint32_t cseq;    // cluster syncs passed
   uint32_t fseq;    // waits whose outcome went through ms.flag
   uint32_t rseq;    // phases of ms.prx
+  uint32_t pseq;    // phases of ms.psx
   int r;            // rank in the cluster
   int task;         // the task in progress (event log)
   unsigned evi;     // events logged (thread 0)
@@ -730,14 +737,23 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
   }
   if (!split) {
     cl_op_ready(p, ms, st);
-    // the rows' 1/RMS from both halves, while the MMAs run; the drain's
-    // barrier publishes ms.inv
-    if (!cl_sync(p, ms, st)) return false;
-    cev(p, st, CEV_SSYNC);
+    // the rows' 1/RMS from both halves, while the MMAs run: each CTA stores
+    // its half's sums of squares into its partner's ms.ssp (counted on the
+    // partner's ms.psx); the drain's barrier publishes ms.inv
     if (t < R) {
-      const float other = cl_ld1(cl_map(smem_u32(&ms.ssx[t]), uint32_t(st.r ^ 1)));
-      ms.inv[t] = rsqrtf((ms.ssx[t] + other) / float(p.d) + p.eps) / ms.rsc[t];
+      const uint32_t pr = uint32_t(st.r ^ 1);
+      cl_st1_async(cl_map(smem_u32(&ms.ssp[t]), pr), ms.ssx[t], cl_map(smem_u32(&ms.psx), pr));
     }
+    int* f = &ms.flag[st.fseq++ & 1];
+    if (t == 0) {
+      mbar_expect_tx(&ms.psx, uint32_t(R) * 4u);
+      *f = cl_mwait(p, &ms.psx, st.pseq & 1);
+    }
+    ++st.pseq;
+    named_bar(CBAR_CONS, kClCons);
+    if (!*f) return false;
+    cev(p, st, CEV_SSYNC);
+    if (t < R) ms.inv[t] = rsqrtf((ms.ssx[t] + ms.ssp[t]) / float(p.d) + p.eps) / ms.rsc[t];
     return true;
   }
   fence_proxy_async_cluster();   // the rows written for the four CTAs' tensor cores
@@ -1201,7 +1217,7 @@ __device__ bool cl_head(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, 
 
 template <bool SPLIT, bool EXT>
 __device__ void cl_consumer(const CParams& p, CMisc& ms, uint8_t* smem) {
-  CState st{0u, 0u, 0u, 0u, int(cl_rank()), 0, 0u};
+  CState st{0u, 0u, 0u, 0u, 0u, int(cl_rank()), 0, 0u};
   const Prog g = cl_prog(p);
   const int nt = cl_n_tasks<EXT>(p, g);
   for (int i = 0; i < nt; ++i) {
@@ -1245,6 +1261,7 @@ __global__ void __launch_bounds__(kClThreads, 1) k_frames_cluster(const CParams 
     mbar_init(&ms.mmadone, 1);
     mbar_init(&ms.opx, 1);
     mbar_init(&ms.prx, 1);
+    mbar_init(&ms.psx, 1);
     mbar_init(&ms.cbar[0], kCl);
     mbar_init(&ms.cbar[1], kCl);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
