@@ -87,16 +87,16 @@ struct CMisc {
   uint64_t opfull, accfull, mmadone;
   uint64_t opx;                  // the O or down operand's rows, written by the peers, have landed
   uint64_t prx;                  // the partial products this CTA consumes have landed
-  uint64_t psx;                  // the partner's sums of squares have landed
-  uint64_t cbar[2];              // cluster syncs: one arrival from each CTA of the cluster
+  uint64_t psx;                  // the partner's sums of squares have landed (split: the rows' statistics)
+  uint64_t nx;                   // split: the normalised operand's rows, written by the half's four CTAs, have landed
   uint32_t tmem_base;
   int flag[2];                   // a wait's outcome for all consumers (alternating: a fast thread's next
                                  // wait may write before a slow one has read the last)
   float ssw[kClConsWarps][kClMaxRows / 4];   // per-warp partial sums of squares of one pass's rows
-  float ssx[kClMaxRows];         // this CTA's K-half sums of squares per row (its partner reads them)
-  float ssp[kClMaxRows];         // the partner's, stored here by the partner
+  float ssx[kClMaxRows];         // per row: this K half's sum of squares (split: a peer's row stored by its builder)
+  float ssp[kClMaxRows];         // per row: the other K half's, stored by the partner (split: by the row's builder)
   float inv[kClMaxRows];         // per row: the factor a drain applies (2^e / RMS, or 2^e for the projection)
-  float rsc[kClMaxRows];         // per row: 2^-e, the operand's range scale
+  float rsc[kClMaxRows];         // per row: 2^-e, the operand's range scale (split: as ssx)
   int code[kClMaxRows];          // step k >= 2: the code each frame's input embeds
 };
 
@@ -153,9 +153,6 @@ __device__ __forceinline__ uint32_t cl_map(uint32_t a, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void cl_arrive_remote(uint32_t cl_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cl_addr) : "memory");
-}
 __device__ __forceinline__ bool cl_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -167,20 +164,16 @@ __device__ __forceinline__ bool cl_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ float cl_ld1(uint32_t a) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(a) : "memory");
-  return v;
-}
-__device__ __forceinline__ void cl_st4(uint32_t a, uint4 v) {
-  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(a), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-               : "memory");
-}
 // Asynchronous store into a peer's shared memory, counted in bytes on the
 // peer's mbarrier at cluster address `bar`.
 __device__ __forceinline__ void cl_st2_async(uint32_t a, uint2 v, uint32_t bar) {
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(a),
                "r"(v.x), "r"(v.y), "r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void cl_st4u_async(uint32_t a, uint4 v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(a),
+               "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(bar)
                : "memory");
 }
 __device__ __forceinline__ void cl_st1_async(uint32_t a, float v, uint32_t bar) {
@@ -195,11 +188,6 @@ __device__ __forceinline__ void cl_st4_async(uint32_t a, float4 v, uint32_t bar)
 // Hardware barrier of every thread of the cluster.
 __device__ __forceinline__ void cl_barrier_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-// Generic-proxy writes to shared memory of any CTA of the cluster made
-// visible to the tensor cores' reads.
-__device__ __forceinline__ void fence_proxy_async_cluster() {
-  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 
 // ------------------------------------------------------------ tracing
@@ -404,11 +392,11 @@ __device__ bool cl_wait_slot(const CParams& p, CMisc& ms, uint32_t w, unsigned& 
   return true;
 }
 
-template <bool EXT>
+template <bool SPLIT, bool EXT>
 __device__ void cl_mma(const CParams& p, CMisc& ms, uint8_t* smem) {
   const Prog g = cl_prog(p);
   const int n = cl_n_tasks<EXT>(p, g);
-  uint32_t wit = 0, opw = 0, xseq = 0;   // weight slots; phases of opfull and of opx waited for
+  uint32_t wit = 0, opw = 0, xseq = 0, nseq = 0;   // weight slots; phases of opfull, opx and nx waited for
   unsigned evi = 0;
   for (int i = 0; i < n; ++i) {
     const Task t = cl_task<EXT>(p, g, i);
@@ -429,6 +417,11 @@ __device__ void cl_mma(const CParams& p, CMisc& ms, uint8_t* smem) {
       if (!mwait(p, &ms.opx, xseq & 1)) goto out;
       ++xseq;
       fence_proxy_async_shared();   // those generic-proxy writes, for the tensor cores' reads
+    } else if (SPLIT && t.kind != T_PROJ && cl_rows(p, t) >= kClSplitRows) {
+      // a normalised operand built by the half's four CTAs, counted on nx
+      if (!mwait(p, &ms.nx, nseq & 1)) goto out;
+      ++nseq;
+      fence_proxy_async_shared();
     } else {
       if (!mwait(p, &ms.opfull, opw & 1)) goto out;
       ++opw;
@@ -480,7 +473,6 @@ out:
 // ------------------------------------------------------ consumer helpers
 struct CState {
   uint32_t opseq;   // tasks whose MMA ran
-  uint32_t cseq;    // cluster syncs passed
   uint32_t fseq;    // waits whose outcome went through ms.flag
   uint32_t rseq;    // phases of ms.prx
   uint32_t pseq;    // phases of ms.psx
@@ -492,7 +484,8 @@ __device__ __forceinline__ void cev(const CParams& p, CState& st, int code) {
   if (threadIdx.x == 0) cl_ev(p, st.evi, 0, code, st.task);
 }
 
-// Bounded wait for the cluster sync in flight (acquire at cluster scope).
+// Bounded wait for a phase of an mbarrier that peers complete (acquire at
+// cluster scope).
 template <class Par>
 __device__ bool cl_mwait(const Par& p, uint64_t* bar, uint32_t parity) {
   if (cl_try_wait(bar, parity)) return true;
@@ -505,23 +498,6 @@ __device__ bool cl_mwait(const Par& p, uint64_t* bar, uint32_t parity) {
     }
   }
 }
-// Every consumer thread of every CTA of the cluster reaches this point
-// before any goes on; the writes before it (shared memory of any CTA of the
-// cluster, and global memory) are visible after it.  Thread i < 8 arrives on
-// CTA i's barrier after this CTA's consumers meet; thread 0 waits on this
-// CTA's and the consumers meet again.
-__device__ bool cl_sync(const CParams& p, CMisc& ms, CState& st) {
-  named_bar(CBAR_CONS, kClCons);
-  const int t = threadIdx.x;
-  uint64_t* bar = &ms.cbar[st.cseq & 1];
-  if (t < kCl) cl_arrive_remote(cl_map(smem_u32(bar), uint32_t(t)));
-  int* f = &ms.flag[st.fseq++ & 1];
-  if (t == 0) *f = cl_mwait(p, bar, (st.cseq >> 1) & 1);
-  named_bar(CBAR_CONS, kClCons);
-  ++st.cseq;
-  return *f != 0;
-}
-
 // One thread waits on a global counter; the consumers meet and read after.
 __device__ bool cl_wait_ctr(const CParams& p, CMisc& ms, CState& st, const unsigned* ctr, unsigned want) {
   int* f = &ms.flag[st.fseq++ & 1];
@@ -635,12 +611,13 @@ __device__ __forceinline__ void in_load8(const CParams& p, const CMisc& ms, cons
 // 2^e / RMS to the partial products, the row's 1/RMS following from this
 // half's sum of squares and the partner's.
 //   * Up to kClSplitRows rows each CTA loads every row of its half, starts
-//     the MMAs, and exchanges the sums of squares (a cluster sync) while they
-//     run.
+//     the MMAs, and exchanges the sums of squares with its partner by
+//     asynchronous stores while they run.
 //   * From kClSplitRows rows the four CTAs of a half (ranks h, h+2, h+4,
 //     h+6) share the loads: CTA h+2g loads, scales and converts rows n = g
-//     (mod 4) and writes them into all four operands; one cluster sync then
-//     publishes the rows and the sums of squares before the MMAs start.
+//     (mod 4) and stores them asynchronously into all four operands, counted
+//     on each one's ms.nx, which the MMA warp waits for; the rows' sums of
+//     squares and scales go the same way to the eight CTAs (ms.psx).
 // Thread t takes column chunk t % CH (8 columns) of local rows t / CH + RP i.
 template <bool SPLIT>
 __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const InSrc& in,
@@ -654,6 +631,8 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
   const int passes = (RL + RP - 1) / RP;
   const int np = cl_npad(R), n8 = np / 8;
   const uint32_t opsz = uint32_t(np) * kKs * 2;
+  // split: all R rows of the half will land in this CTA's operand
+  if (split && t == 0) mbar_expect_tx(&ms.nx, uint32_t(R) * uint32_t(p.d));
   float hold[kClHold][8];
   // pass 1: sums of squares, the first kClHold chunks kept in registers
   // (their loads all in flight together); a warp's 32 lanes all belong to
@@ -691,8 +670,22 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
     const int slot = t % RP, i = t / RP, w0 = slot * CH / 32, n = g + G * t;
     float s = 0.f;
     for (int w = 0; w < CH / 32; ++w) s += ms.ssw[w0 + w][i];
+    const float rs = exp2i(-range_exp(s / float(half)));
     ms.ssx[n] = s;
-    ms.rsc[n] = exp2i(-range_exp(s / float(half)));
+    ms.rsc[n] = rs;
+    if (split) {   // the row's statistics to the other CTAs of both halves, ahead of the MMAs
+      const uint32_t xa = smem_u32(&ms.ssx[n]), ra = smem_u32(&ms.rsc[n]), pa = smem_u32(&ms.ssp[n]);
+      const uint32_t bar = smem_u32(&ms.psx);
+#pragma unroll
+      for (int gg = 0; gg < 4; ++gg) {
+        const uint32_t mate = uint32_t(h + 2 * gg), other = uint32_t((h ^ 1) + 2 * gg);
+        if (gg != g) {
+          cl_st1_async(cl_map(xa, mate), s, cl_map(bar, mate));
+          cl_st1_async(cl_map(ra, mate), rs, cl_map(bar, mate));
+        }
+        cl_st1_async(cl_map(pa, other), s, cl_map(bar, other));
+      }
+    }
   }
   named_bar(CBAR_CONS, kClCons);
   cev(p, st, CEV_BSUB);
@@ -707,9 +700,12 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
     if (!split) {
       *reinterpret_cast<uint4*>(op + op_idx(n, kk, n8)) = hv;
     } else {
-      const uint32_t a = smem_u32(op + op_idx(n, kk, n8));
+      const uint32_t a = smem_u32(op + op_idx(n, kk, n8)), bar = smem_u32(&ms.nx);
 #pragma unroll
-      for (int gg = 0; gg < 4; ++gg) cl_st4(cl_map(a, uint32_t(h + 2 * gg)), hv);
+      for (int gg = 0; gg < 4; ++gg) {
+        const uint32_t mate = uint32_t(h + 2 * gg);
+        cl_st4u_async(cl_map(a, mate), hv, cl_map(bar, mate));
+      }
     }
   };
 #pragma unroll
@@ -744,29 +740,22 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
       const uint32_t pr = uint32_t(st.r ^ 1);
       cl_st1_async(cl_map(smem_u32(&ms.ssp[t]), pr), ms.ssx[t], cl_map(smem_u32(&ms.psx), pr));
     }
-    int* f = &ms.flag[st.fseq++ & 1];
-    if (t == 0) {
-      mbar_expect_tx(&ms.psx, uint32_t(R) * 4u);
-      *f = cl_mwait(p, &ms.psx, st.pseq & 1);
-    }
-    ++st.pseq;
-    named_bar(CBAR_CONS, kClCons);
-    if (!*f) return false;
-    cev(p, st, CEV_SSYNC);
-    if (t < R) ms.inv[t] = rsqrtf((ms.ssx[t] + ms.ssp[t]) / float(p.d) + p.eps) / ms.rsc[t];
-    return true;
+  } else {
+    cev(p, st, CEV_OPREADY);
   }
-  fence_proxy_async_cluster();   // the rows written for the four CTAs' tensor cores
-  if (!cl_sync(p, ms, st)) return false;
-  cl_op_ready(p, ms, st);
+  // both halves' statistics of every row: the other half's R sums of
+  // squares, split also the sum of squares and scale of the own half's rows
+  // that the three other CTAs built
+  int* f = &ms.flag[st.fseq++ & 1];
+  if (t == 0) {
+    mbar_expect_tx(&ms.psx, uint32_t(R) * 4u + (split ? uint32_t(R - RL) * 8u : 0u));
+    *f = cl_mwait(p, &ms.psx, st.pseq & 1);
+  }
+  ++st.pseq;
+  named_bar(CBAR_CONS, kClCons);
+  if (!*f) return false;
   cev(p, st, CEV_SSYNC);
-  if (t < R) {   // row t's sums of squares and scale sit with the CTAs that built it
-    const uint32_t own = uint32_t(h + 2 * (t & 3)), other = uint32_t((h ^ 1) + 2 * (t & 3));
-    const float so = cl_ld1(cl_map(smem_u32(&ms.ssx[t]), own));
-    const float sp = cl_ld1(cl_map(smem_u32(&ms.ssx[t]), other));
-    const float rs = cl_ld1(cl_map(smem_u32(&ms.rsc[t]), own));
-    ms.inv[t] = rsqrtf((so + sp) / float(p.d) + p.eps) / rs;
-  }
+  if (t < R) ms.inv[t] = rsqrtf((ms.ssx[t] + ms.ssp[t]) / float(p.d) + p.eps) / ms.rsc[t];
   return true;
 }
 
@@ -846,8 +835,8 @@ __device__ bool cl_wait_recv(const CParams& p, CMisc& ms, CState& st, uint32_t b
 // Drain the accumulator of an O or down tile (rows m0 .. m0+127 of the
 // residual stream) into the residual rows n < R.  Each warp drains 32
 // features x 8 rows at a time, transposes them through 1 KB of shared
-// memory (the start of the operand region: the partials there were read
-// before the last cluster sync) and adds 4 consecutive features per thread
+// memory (the start of the operand region, whose normalised operand the
+// tensor cores read before any peer could reach the next one) and adds 4 consecutive features per thread
 // with one vector reduction.  emb: also add the frame's code embedding
 // (step k >= 2, layer 0, first kv group).
 __device__ bool cl_drain_resid(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, float* xrows, int R, int m0,
@@ -1217,7 +1206,7 @@ __device__ bool cl_head(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, 
 
 template <bool SPLIT, bool EXT>
 __device__ void cl_consumer(const CParams& p, CMisc& ms, uint8_t* smem) {
-  CState st{0u, 0u, 0u, 0u, 0u, int(cl_rank()), 0, 0u};
+  CState st{0u, 0u, 0u, 0u, int(cl_rank()), 0, 0u};
   const Prog g = cl_prog(p);
   const int nt = cl_n_tasks<EXT>(p, g);
   for (int i = 0; i < nt; ++i) {
@@ -1262,8 +1251,7 @@ __global__ void __launch_bounds__(kClThreads, 1) k_frames_cluster(const CParams 
     mbar_init(&ms.opx, 1);
     mbar_init(&ms.prx, 1);
     mbar_init(&ms.psx, 1);
-    mbar_init(&ms.cbar[0], kCl);
-    mbar_init(&ms.cbar[1], kCl);
+    mbar_init(&ms.nx, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 0) tmem_alloc(&ms.tmem_base, kClTmemCols);
@@ -1277,7 +1265,7 @@ __global__ void __launch_bounds__(kClThreads, 1) k_frames_cluster(const CParams 
     if ((t & 31) == 0) cl_producer<EXT>(p, ms, smem);
     __syncwarp();
   } else if (warp == kClMmaWarp) {
-    if ((t & 31) == 0) cl_mma<EXT>(p, ms, smem);
+    if ((t & 31) == 0) cl_mma<SPLIT, EXT>(p, ms, smem);
     __syncwarp();
   }
   tc_fence_before();
