@@ -633,6 +633,9 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
   const uint32_t opsz = uint32_t(np) * kKs * 2;
   // split: all R rows of the half will land in this CTA's operand
   if (split && t == 0) mbar_expect_tx(&ms.nx, uint32_t(R) * uint32_t(p.d));
+  // the norm's weights for this thread's 8 columns, in flight with the row loads
+  const float4 w0 = __ldg(reinterpret_cast<const float4*>(wn + col));
+  const float4 w1 = __ldg(reinterpret_cast<const float4*>(wn + col + 4));
   float hold[kClHold][8];
   // pass 1: sums of squares, the first kClHold chunks kept in registers
   // (their loads all in flight together); a warp's 32 lanes all belong to
@@ -690,8 +693,6 @@ __device__ bool cl_build_norm(const CParams& p, CMisc& ms, CState& st, uint8_t* 
   named_bar(CBAR_CONS, kClCons);
   cev(p, st, CEV_BSUB);
   // pass 2: f16(x * w * 2^-e) into the operand slices (of all four CTAs of the half, split)
-  const float4 w0 = __ldg(reinterpret_cast<const float4*>(wn + col));
-  const float4 w1 = __ldg(reinterpret_cast<const float4*>(wn + col + 4));
   const float w[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
   const int kl = c * 8, s = kl / kKs, kk = kl % kKs;
   uint16_t* op = reinterpret_cast<uint16_t*>(smem + kClOffOp + uint32_t(s) * opsz);
