@@ -111,13 +111,13 @@ constexpr int kSmallAutoFrames = 40;
 // Largest batch the cluster engine serves (2B <= 64 activation rows at step
 // 1: its operand and partial buffers share 64 KB of shared memory).  Where it
 // serves a call, QP_ENGINE_AUTO takes it: measured on GB300 at the 1.7B
-// geometry, 92.3 vs 135.2 us per step at 1 frame (small-batch engine),
-// 101.0 vs 143.6 at 8, 140.6 vs 192.9 at 32.
+// geometry, 91.4 vs 135.9 us per step at 1 frame (small-batch engine),
+// 99.8 vs 143.5 at 8, 138.3 vs 193.0 at 32.
 constexpr int kClusterMaxFrames = 32;
 // With Q8_0 matrices or Talker-wide code tables (the exporter's layout) the
 // cluster engine is the faster one at every batch it serves (measured, against
-// the small-batch engine: 155.8 vs 158.5 us per step at 1 frame, 162.7 vs 164.7
-// at 8, 171.1 vs 177.8 at 16, 201.3 vs 212.6 at 32).
+// the small-batch engine: 135.8 vs 158.4 us per step at 1 frame, 180.9 vs 212.1
+// at 32).
 constexpr int kClusterExtAutoFrames = 1;
 
 }  // namespace qp
