@@ -76,7 +76,16 @@ constexpr uint32_t kClOffOp2 = kClOffOp + 32768;      // O / down operand (secon
 constexpr uint32_t kClOffRecv = kClOffOp + kClOpBytes;
 constexpr uint32_t kClRecvBytes = 32768;
 constexpr uint32_t kClOffMisc = kClOffRecv + kClRecvBytes;
-constexpr uint32_t kClTmemCols = 64;                  // one accumulator of up to 64 columns
+// Tensor memory: the accumulator (up to 64 columns), then the KV cache of
+// the frames this CTA runs attention for.  Lane quarter q holds frame
+// r + 8q; per layer 64 columns: k of positions 0..15 in columns 2t, 2t + 1
+// (f16, dims 4l..4l+3 in lane l of the quarter), v in 32 + 2t, 33 + 2t.
+constexpr uint32_t kClTmemCols = 512;
+constexpr uint32_t kClKvCol = 64;
+constexpr uint32_t kClKvColsPerLayer = 4 * kMaxCtx;
+constexpr int kClMaxLayers = int((kClTmemCols - kClKvCol) / kClKvColsPerLayer);
+static_assert(kMaxCtx == 16, "the TMEM cache holds 16 positions per layer");
+static_assert(kClusterMaxFrames <= 4 * kCl, "one frame per lane quarter of each CTA");
 static_assert(kClusterMaxFrames <= kCl * kClConsWarps / 2, "attention: one (frame, q head) per warp");
 
 enum { CBAR_CONS = 1 };
@@ -123,7 +132,6 @@ struct CParams {
   const float2* rope_cs;
   // scratch
   float* x;                // residual streams [step][2B][d], zeroed per call
-  uint16_t* kv;            // f16 [layer][frame][pos][k|v][kv_width]
   unsigned* proj_done;     // [step]: projection units finished (step 1; every step with Talker-wide tables)
   unsigned* att_done;      // [step][layer]: attention CTAs finished (O added)
   unsigned* mlp_done;      // [step][layer]: MLP CTAs finished (down added)
@@ -566,11 +574,40 @@ __device__ __forceinline__ float4 ldv_f4(const void* src) {
   asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "l"(src));
   return v;
 }
-__device__ __forceinline__ uint2 ldv_u2(const void* src) {
-  uint2 v;
-  asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(src));
-  return v;
+// 32 lanes x 32 columns of 32-bit words from TMEM, issued only: tmem_wait_ld2
+// completes them.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,"
+      "%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
 }
+// Wait for this thread's TMEM loads; the registers pass through the wait so
+// that no use of them is scheduled ahead of it.
+__device__ __forceinline__ void tmem_regs_after_wait(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld2(uint32_t (&a)[32], uint32_t (&b)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  tmem_regs_after_wait(a);
+  tmem_regs_after_wait(b);
+}
+// Two 32-bit words into columns taddr, taddr + 1 of this thread's lane.
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint2 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(v.x), "r"(v.y) : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void ld8f(const float* src, float (&v)[8]) {
   const float4 a = ldv_f4(src), b = ldv_f4(src + 4);
   v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w; v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
@@ -997,29 +1034,33 @@ __device__ bool cl_att_input(const CParams& p, CMisc& ms, CState& st, const Task
 // GEMM over this CTA's tile and K half, then for the frames b = r (mod 8),
 // one warp per (frame, q head), the frame's q|k|v from the peers' partials,
 // per-head RMSNorm and RoPE of the new position(s), KV append (by the head-0
-// warp), causal softmax over positions 0..pos and the head's output written
+// warp, into this CTA's tensor memory), causal softmax over positions 0..pos and the head's output written
 // into every peer's O operand.  Lane l holds dims 4l..4l+3 of every
 // 128-vector; the scores of 16 positions are 16 partial dot products per
 // lane, summed by one reduce-scatter.
 template <bool SPLIT, bool EXT>
 __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, const Task& tk) {
-  const int k = tk.k, l = tk.l, j = tk.job, R = cl_rows(p, tk), np = cl_npad(R), n8 = np / 8;
+  const int k = tk.k, l = tk.l, R = cl_rows(p, tk), np = cl_npad(R), n8 = np / 8;
   InSrc in;
   if (!cl_att_input<EXT>(p, ms, st, tk, in)) return false;
   if (!cl_build_norm<SPLIT>(p, ms, st, smem, in, p.layer[l].attn_norm, R)) return false;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, hh = warp & 1;
-  const int P = k == 1 ? 2 : 1, ctx = p.n_steps + 1, pos0 = k == 1 ? 0 : k;
-  // warp w: q head hh = w % 2 of frame b = r + 8 (w / 2) (at most 32 frames: one per warp)
-  const int b = st.r + kCl * (warp >> 1);
-  uint16_t* kvb = p.kv + (size_t(l) * p.B + b) * ctx * 2 * p.kvw + j * kHeadDim + lane * 4;   // + (pos*2 + {0,1}) * kvw
-  // the positions of earlier steps, from the cache (written by this CTA's head-0 warps), loaded
-  // while the MMAs run
-  uint2 kh[kMaxCtx], vh[kMaxCtx];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, fq = warp & 3, hh = warp >> 2;
+  const int P = k == 1 ? 2 : 1, pos0 = k == 1 ? 0 : k;
+  // warp w: q head hh = w / 4 of frame b = r + 8 (w % 4), whose KV cache for
+  // kv head j sits in lane quarter w % 4 of this CTA's tensor memory (the
+  // cluster keeps kv head j at every layer and step)
+  const int b = st.r + kCl * fq;
+  const uint32_t kvt = ms.tmem_base + (uint32_t(fq * 32) << 16) + kClKvCol + uint32_t(l) * kClKvColsPerLayer;
+  // the positions of earlier steps (written by the head-0 warp), read while the MMAs run
+  uint32_t kc[2 * kMaxCtx], vc[2 * kMaxCtx];
+  const bool cached = b < p.B && pos0 > 0;   // warp-uniform
+  if (cached) {
+    tc_fence_after();
+    tmem_ld32(kvt, kc);
+    tmem_ld32(kvt + 2 * kMaxCtx, vc);
+  } else {
 #pragma unroll
-  for (int tt = 0; tt < kMaxCtx; ++tt) {
-    const bool c = b < p.B && tt < pos0;
-    kh[tt] = c ? ldv_u2(kvb + (size_t(tt) * 2 + 0) * p.kvw) : make_uint2(0, 0);
-    vh[tt] = c ? ldv_u2(kvb + (size_t(tt) * 2 + 1) * p.kvw) : make_uint2(0, 0);
+    for (int i = 0; i < 2 * kMaxCtx; ++i) kc[i] = vc[i] = 0u;
   }
   // the head norms' weights and the new positions' RoPE factors, also ahead of the sync
   const CLayer& L = p.layer[l];
@@ -1035,6 +1076,7 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
   // this CTA's frames' q|k|v: 4 tiles x 2 K halves x 128 per row
   if (!cl_wait_recv(p, ms, st, uint32_t(att_rows(p.B, P, st.r)) * 4096u)) return false;
   cev(p, st, CEV_S1);
+  if (cached) tmem_wait_ld2(kc, vc);
   const float scale = rsqrtf(float(kHeadDim));
   const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
   const float* recv = reinterpret_cast<const float*>(smem + kClOffRecv) + lane * 4;
@@ -1062,14 +1104,15 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
       float4 knew, qn;
       norm_rope_w2(v4[1], knw, v4[0], qnw, cs, p.eps, lane, knew, qn);
       const float4 vnew = v4[2];
-      if (hh == 0) {
-        *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 0) * p.kvw) = pack4_f16(knew.x, knew.y, knew.z, knew.w);
-        *reinterpret_cast<uint2*>(kvb + (size_t(pos) * 2 + 1) * p.kvw) = pack4_f16(vnew.x, vnew.y, vnew.z, vnew.w);
+      if (hh == 0) {   // the new position into the cache
+        tmem_st2(kvt + 2 * uint32_t(pos), pack4_f16(knew.x, knew.y, knew.z, knew.w));
+        tmem_st2(kvt + 2 * kMaxCtx + 2 * uint32_t(pos), pack4_f16(vnew.x, vnew.y, vnew.z, vnew.w));
       }
       float part[16];
 #pragma unroll
       for (int tt = 0; tt < kMaxCtx; ++tt) {
-        const float4 kk = tt < pos0 ? unpack4_f16(kh[tt]) : (tt == pos ? knew : (tt < pos ? kprev : z4));
+        const float4 kk = tt < pos0 ? unpack4_f16(make_uint2(kc[2 * tt], kc[2 * tt + 1]))
+                                    : (tt == pos ? knew : (tt < pos ? kprev : z4));
         part[tt] = qn.x * kk.x + qn.y * kk.y + qn.z * kk.z + qn.w * kk.w;
       }
       if (lane == 0 && threadIdx.x == 0) cl_ev(p, st.evi, 0, CEV_SUB, st.task);
@@ -1087,7 +1130,8 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
       float4 o1 = z4;
 #pragma unroll
       for (int tt = 0; tt < kMaxCtx; ++tt) {
-        const float4 vv = tt < pos0 ? unpack4_f16(vh[tt]) : (tt == pos ? vnew : (tt < pos ? vprev : z4));
+        const float4 vv = tt < pos0 ? unpack4_f16(make_uint2(vc[2 * tt], vc[2 * tt + 1]))
+                                    : (tt == pos ? vnew : (tt < pos ? vprev : z4));
         const float w = __shfl_sync(0xffffffffu, pr, 2 * tt);
         o1.x += w * vv.x; o1.y += w * vv.y; o1.z += w * vv.z; o1.w += w * vv.w;
       }
@@ -1099,6 +1143,10 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
       for (int dst = 0; dst < n_dst; ++dst) cl_st2_async(cl_map(a, uint32_t(dst)), hv, cl_map(xbar, uint32_t(dst)));
       kprev = knew;
       vprev = vnew;
+    }
+    if (hh == 0) {   // the cache stores done before the barriers that order the next step's loads
+      tmem_wait_st();
+      tc_fence_before();
     }
   }
   cev(p, st, CEV_WORK);
@@ -1294,7 +1342,6 @@ ClLayout cl_layout(const qp_geometry& g, int B) {
   Lo.best = o;       o += cl_al256(steps * B * 8);
   Lo.abort_flag = o; o += 256;
   Lo.zeroed = o;
-  Lo.kv = o;         o += cl_al256(L * B * (steps + 1) * 2 * size_t(g.n_kv_heads) * kHeadDim * 2);
   Lo.total = o;
   return Lo;
 }
@@ -1354,7 +1401,7 @@ bool cluster_geometry_ok(const qp_geometry& g) {
   return g.head_dim == kHeadDim && g.n_q_heads == 2 * g.n_kv_heads && g.hidden % 256 == 0 && g.hidden >= 512 &&
          g.hidden <= 1024 && g.ffn % 256 == 0 && g.vocab % 512 == 0 &&
          (g.code_embed_dim == g.hidden || g.code_embed_dim == g.talker_hidden) && g.talker_hidden % kKs == 0 &&
-         g.n_steps + 1 <= kMaxCtx && g.layers <= kMaxLayers;
+         g.n_steps + 1 <= kMaxCtx && g.layers <= kClMaxLayers;
 }
 
 bool cluster_supported(const qp_handle* h, const RunArgs& a) {
@@ -1403,7 +1450,6 @@ qp_status run_frames_cluster(qp_handle* h, const RunArgs& a, cudaStream_t s) {
   }
   p.rope_cs = h->rope_cs;
   p.x = reinterpret_cast<float*>(base + Lo.x);
-  p.kv = reinterpret_cast<uint16_t*>(base + Lo.kv);
   p.proj_done = reinterpret_cast<unsigned*>(base + Lo.proj_done);
   p.att_done = reinterpret_cast<unsigned*>(base + Lo.att_done);
   p.mlp_done = reinterpret_cast<unsigned*>(base + Lo.mlp_done);
