@@ -812,7 +812,8 @@ __device__ __forceinline__ int att_rows(int B, int P, int r) { return r < B ? ((
 // them, 4 (tq % 2) + m / 32, as recv[n][tq / 2][h][m % 32]; PUSH_HEAD: rows m
 // of the tile go to the member of the CTA pair that completes them (m < 64:
 // the K-half-0 CTA) as recv[n][h][m % 64].  Each warp moves 32 features x 8
-// rows at a time through 1 KB of its own (the operand region is free once
+// rows at a time (warps w and w + 4 share a lane quarter and take alternate
+// 8-row chunks) through 1 KB of its own (the operand region is free once
 // the MMAs are done), 8 consecutive features per lane.
 enum { PUSH_ATT = 0, PUSH_GU = 1, PUSH_HEAD = 2 };
 template <int MODE>
@@ -823,7 +824,7 @@ __device__ bool cl_drain_push(const CParams& p, CMisc& ms, CState& st, uint8_t* 
   float* tp = reinterpret_cast<float*>(smem + kClOffOp) + warp * 256;   // [8 rows][32 features]
   const uint32_t recv = smem_u32(smem + kClOffRecv), bar = smem_u32(&ms.prx);
   const int f = lane >> 2, k8 = (lane & 3) * 8;   // this lane's row in the chunk and its features
-  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {   // warp-uniform
+  for (int col = ch * 8; col < R; col += 16) {   // warp-uniform; the two warps of a lane quarter alternate
     float v[8];
     tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
 #pragma unroll
@@ -872,7 +873,8 @@ __device__ bool cl_wait_recv(const CParams& p, CMisc& ms, CState& st, uint32_t b
 
 // Drain the accumulator of an O or down tile (rows m0 .. m0+127 of the
 // residual stream) into the residual rows n < R.  Each warp drains 32
-// features x 8 rows at a time, transposes them through 1 KB of shared
+// features x 8 rows at a time (alternate chunks with the other warp of its
+// lane quarter), transposes them through 1 KB of shared
 // memory (the start of the operand region, whose normalised operand the
 // tensor cores read before any peer could reach the next one) and adds 4 consecutive features per thread
 // with one vector reduction.  emb: also add the frame's code embedding
@@ -883,7 +885,7 @@ __device__ bool cl_drain_resid(const CParams& p, CMisc& ms, CState& st, uint8_t*
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, q = warp & 3, ch = warp >> 2;
   float* tp = reinterpret_cast<float*>(smem + kClOffOp) + warp * 256;   // [8 rows][32 features]
   const int mq = m0 + q * 32;
-  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {   // warp-uniform
+  for (int col = ch * 8; col < R; col += 16) {   // warp-uniform; the two warps of a lane quarter alternate
     float v[8];
     tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
 #pragma unroll
@@ -989,7 +991,7 @@ __device__ bool cl_proj(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, 
   const float4 bias = ks == 0 ? __ldg(reinterpret_cast<const float4*>(p.b_proj + mq + k4)) : make_float4(0.f, 0.f, 0.f, 0.f);
   float* tp = reinterpret_cast<float*>(smem + kClOffOp) + warp * 256;   // [8 rows][32 features]
   float* xk = cl_x(p, k);
-  for (int col = ch * 32; col < ch * 32 + 32 && col < R; col += 8) {   // warp-uniform
+  for (int col = ch * 8; col < R; col += 16) {   // warp-uniform; the two warps of a lane quarter alternate
     float v[8];
     tmem_ld8(ms.tmem_base + (uint32_t(q * 32) << 16) + uint32_t(col), v);
 #pragma unroll
