@@ -70,7 +70,8 @@ def test_cluster_agrees_with_the_other_engines(cl_small):
 
 
 def test_cluster_repeated_calls(cl_small):
-    """Calls on one handle reuse the KV cache, counters and residual rows."""
+    """Calls on one handle reuse the counters and residual rows (the KV
+    cache lives in each CTA's tensor memory for the length of a call)."""
     raw, P, cp = cl_small
     H, q0 = S.toy_inputs(CL, 12, seed=43)
     a = run_gpu(cp, H, q0)
@@ -144,6 +145,41 @@ def test_cluster_refuses_what_it_cannot_serve(qpk, cl_small):
             sm.predict(torch.zeros((2, small_geo.talker_hidden), device="cuda"), q0[:2])
     finally:
         sm.close()
+
+
+@pytest.mark.parametrize("B", [3, 25])
+def test_cluster_seven_layers_fill_tensor_memory(qpk, B):
+    """Seven layers use all 512 tensor-memory columns (the 64-column
+    accumulator, then 64 columns of KV cache per layer): served and checked
+    against the oracle with the per-CTA and the shared-load operand builds;
+    an eighth layer is refused, and the automatic choice serves it on
+    another engine."""
+    import torch
+    g7 = dataclasses.replace(CL, layers=7)
+    raw = S.make_weights(g7, seed=93, norm_mode="perturbed")
+    cp = qpk.CodePredictor(g7, max_batch=B)
+    try:
+        cp.load_raw_weights(raw)
+        cp.set_engine("cluster")
+        H, q0 = S.toy_inputs(g7, B, seed=95 + B)
+        assert_parity(check_parity(cp, O.Predictor.from_raw(g7, raw), H, q0, sample_rows(B, 4)))
+    finally:
+        cp.close()
+    g8 = dataclasses.replace(CL, layers=8)
+    raw8 = S.make_weights(g8, seed=94, norm_mode="perturbed")
+    cp = qpk.CodePredictor(g8, max_batch=B)
+    try:
+        cp.load_raw_weights(raw8)
+        H, q0 = S.toy_inputs(g8, B, seed=97)
+        tH, tq = torch.from_numpy(H).cuda(), torch.from_numpy(q0.astype(np.int32)).cuda()
+        cp.set_engine("cluster")
+        with pytest.raises(qpk.QpError) as e:
+            cp.predict(tH, tq)
+        assert e.value.code == 1
+        cp.set_engine("auto")
+        assert_parity(check_parity(cp, O.Predictor.from_raw(g8, raw8), H, q0, sample_rows(B, 2)))
+    finally:
+        cp.close()
 
 
 def test_cluster_bad_first_code_is_reported(cl_small):
