@@ -111,12 +111,12 @@ constexpr int kSmallAutoFrames = 40;
 // Largest batch the cluster engine serves (2B <= 64 activation rows at step
 // 1: its operand and partial buffers share 64 KB of shared memory).  Where it
 // serves a call, QP_ENGINE_AUTO takes it: measured on GB300 at the 1.7B
-// geometry, 91.4 vs 135.9 us per step at 1 frame (small-batch engine),
-// 99.8 vs 143.5 at 8, 138.3 vs 193.0 at 32.
+// geometry, 90.0 vs 136.0 us per step at 1 frame (small-batch engine),
+// 99.2 vs 143.6 at 8, 135.6 vs 193.2 at 32.
 constexpr int kClusterMaxFrames = 32;
 // With Q8_0 matrices or Talker-wide code tables (the exporter's layout) the
 // cluster engine is the faster one at every batch it serves (measured, against
-// the small-batch engine: 135.8 vs 158.4 us per step at 1 frame, 180.9 vs 212.1
+// the small-batch engine: 133.7 vs 158.2 us per step at 1 frame, 179.3 vs 211.2
 // at 32).
 constexpr int kClusterExtAutoFrames = 1;
 
