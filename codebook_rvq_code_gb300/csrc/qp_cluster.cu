@@ -1400,8 +1400,10 @@ bool cluster_ext(const qp_handle* h) {
 }
 
 bool cluster_geometry_ok(const qp_geometry& g) {
-  return g.head_dim == kHeadDim && g.n_q_heads == 2 * g.n_kv_heads && g.hidden % 256 == 0 && g.hidden >= 512 &&
-         g.hidden <= 1024 && g.ffn % 256 == 0 && g.vocab % 512 == 0 &&
+  // hidden 512 or 1024: a row half of 256 or 512 columns is 32 or 64 chunks of 8, so each warp of an
+  // operand build holds chunks of one row and the consumers cover whole rows per pass
+  return g.head_dim == kHeadDim && g.n_q_heads == 2 * g.n_kv_heads && (g.hidden == 512 || g.hidden == 1024) &&
+         g.ffn % 256 == 0 && g.vocab % 512 == 0 &&
          (g.code_embed_dim == g.hidden || g.code_embed_dim == g.talker_hidden) && g.talker_hidden % kKs == 0 &&
          g.n_steps + 1 <= kMaxCtx && g.layers <= kClMaxLayers;
 }

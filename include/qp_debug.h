@@ -30,8 +30,8 @@ extern "C" {
  * destination and each consumer builds its operand slice from it, which
  * removes one dependent global round trip per GEMM.  The cluster engine
  * serves greedy calls of at most 32 frames, for geometries with head_dim
- * 128, two q heads per kv head, a hidden size of 512 to 1024 (a multiple of
- * 256), an FFN size a multiple of 256, a vocabulary a multiple of 512 and
+ * 128, two q heads per kv head, a hidden size of 512 or 1024, an FFN size a
+ * multiple of 256, a vocabulary a multiple of 512 and
  * at most 7 layers (the 1.7B predictor's: the KV cache of a CTA's frames
  * stays in its tensor memory), with 16-bit or Q8_0 matrices (Q8_0 through their
  * f16 hi + lo images) and code tables as wide as the hidden size or as the

@@ -1,6 +1,6 @@
 """The cluster engine (QP_ENGINE_CLUSTER, include/qp_debug.h) against the
 oracle, through the C ABI: the greedy frame loop on 8-CTA clusters, for
-geometries with a hidden size of 512..1024 (multiple of 256), an FFN and a
+geometries with a hidden size of 512 or 1024, an FFN and a
 vocabulary that split into 256- and 512-wide jobs, and at most 32 frames;
 16-bit or Q8_0 matrices (through their exact f16 hi + lo images), code
 tables as wide as the hidden size or as the Talker state (projected at
