@@ -1110,12 +1110,14 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
         tmem_st2(kvt + 2 * uint32_t(pos), pack4_f16(knew.x, knew.y, knew.z, knew.w));
         tmem_st2(kvt + 2 * kMaxCtx + 2 * uint32_t(pos), pack4_f16(vnew.x, vnew.y, vnew.z, vnew.w));
       }
-      float part[16];
+      float part[16];   // positions after pos (masked below) skipped: pos is the same in every lane
 #pragma unroll
       for (int tt = 0; tt < kMaxCtx; ++tt) {
-        const float4 kk = tt < pos0 ? unpack4_f16(make_uint2(kc[2 * tt], kc[2 * tt + 1]))
-                                    : (tt == pos ? knew : (tt < pos ? kprev : z4));
-        part[tt] = qn.x * kk.x + qn.y * kk.y + qn.z * kk.z + qn.w * kk.w;
+        part[tt] = 0.f;
+        if (tt <= pos) {
+          const float4 kk = tt < pos0 ? unpack4_f16(make_uint2(kc[2 * tt], kc[2 * tt + 1])) : (tt == pos ? knew : kprev);
+          part[tt] = qn.x * kk.x + qn.y * kk.y + qn.z * kk.z + qn.w * kk.w;
+        }
       }
       if (lane == 0 && threadIdx.x == 0) cl_ev(p, st.evi, 0, CEV_SUB, st.task);
       const float rsum = reduce_scatter16(part, lane);   // lanes 2t and 2t + 1: position t
@@ -1132,10 +1134,11 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
       float4 o1 = z4;
 #pragma unroll
       for (int tt = 0; tt < kMaxCtx; ++tt) {
-        const float4 vv = tt < pos0 ? unpack4_f16(make_uint2(vc[2 * tt], vc[2 * tt + 1]))
-                                    : (tt == pos ? vnew : (tt < pos ? vprev : z4));
-        const float w = __shfl_sync(0xffffffffu, pr, 2 * tt);
-        o1.x += w * vv.x; o1.y += w * vv.y; o1.z += w * vv.z; o1.w += w * vv.w;
+        if (tt <= pos) {   // warp-uniform
+          const float4 vv = tt < pos0 ? unpack4_f16(make_uint2(vc[2 * tt], vc[2 * tt + 1])) : (tt == pos ? vnew : vprev);
+          const float w = __shfl_sync(0xffffffffu, pr, 2 * tt);
+          o1.x += w * vv.x; o1.y += w * vv.y; o1.z += w * vv.z; o1.w += w * vv.w;
+        }
       }
       if (lane == 0 && threadIdx.x == 0) cl_ev(p, st.evi, 0, CEV_SUB, st.task);
       // row n of the O operand (K = the group's 256 columns: head hh in slice hh) in every CTA
