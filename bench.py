@@ -340,6 +340,25 @@ def engine_of(B: int, gemm_format: str, sampled: bool = False) -> str:
     return "small" if B <= 40 else "tile"
 
 
+def median_call_ms(fn, steps, flush, stream):
+    """Median CUDA-event time in ms of `steps` calls of fn, each after an L2
+    flush (the rows beside the headline: the median keeps one disturbed call,
+    another process's work or a clock dip, out of the figure)."""
+    import statistics
+    import torch
+    ts = []
+    for i in range(steps):
+        flush.fill_(float(i))
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
 def sweep(g, dev, stream, steps, hbm, tf):
     """Every batch configuration once more: ms per call, frames/s, us/step
     and roofline fraction (each call a full 15-step loop, L2 flushed)."""
@@ -362,17 +381,8 @@ def sweep(g, dev, stream, steps, hbm, tf):
         for _ in range(3):
             cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream)
         torch.cuda.synchronize()
-        tot = 0.0
-        for i in range(steps):
-            flush.fill_(float(i))
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream)
-            b.record(stream)
-            torch.cuda.synchronize()
-            tot += a.elapsed_time(b)
-        ms = tot / steps
+        ms = median_call_ms(lambda: cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream), steps, flush,
+                            stream)
         st = cp.device_status()
         cp.close()
         roof = roofline_of(g, w.B, w.gemm_format, samp is not None, ms, hbm, tf)
@@ -434,17 +444,8 @@ def deterministic_rows(g, dev, stream, steps, per_config):
         for _ in range(3):
             cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream)
         torch.cuda.synchronize()
-        tot = 0.0
-        for i in range(steps):
-            flush.fill_(float(i))
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream)
-            b.record(stream)
-            torch.cuda.synchronize()
-            tot += a.elapsed_time(b)
-        ms = tot / steps
+        ms = median_call_ms(lambda: cp.predict(H, q0, out_codes=codes, sampling=samp, stream=stream), steps, flush,
+                            stream)
         base = per_config.get(w.name, {}).get("ms_per_call")
         out[f"deterministic_{w.name}"] = {"ms_per_call": ms, "us_per_step": 1e3 * ms / g.n_steps,
                                           "frames_per_s": w.B / (ms / 1e3), "ordinary_ms_per_call": base,
@@ -494,17 +495,7 @@ def exporter_rows(dev, stream, steps, hbm, tc):
         for _ in range(3):
             cp.predict(tH, tq, out_codes=codes, stream=stream)
         torch.cuda.synchronize()
-        tot = 0.0
-        for i in range(steps):
-            flush.fill_(float(i))
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            cp.predict(tH, tq, out_codes=codes, stream=stream)
-            b.record(stream)
-            torch.cuda.synchronize()
-            tot += a.elapsed_time(b)
-        ms = tot / steps
+        ms = median_call_ms(lambda: cp.predict(tH, tq, out_codes=codes, stream=stream), steps, flush, stream)
         nbytes, flops = work_exporter(g, B)
         t_hbm, t_tc = nbytes / (hbm * 1e9), flops / (tc * 1e12)
         bound = "hbm" if t_hbm >= t_tc else "tensor"
@@ -551,17 +542,7 @@ def sched_rows(dev, stream, steps, hbm):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        tot = 0.0
-        for i in range(steps):
-            flush.fill_(float(i))
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            tot += a.elapsed_time(b)
-        return tot / steps
+        return median_call_ms(fn, steps, flush, stream)
 
     for B in (1, 32, 64):
         H, q0 = S.toy_inputs(g, B, seed=700 + B)
@@ -607,17 +588,7 @@ def rvq_rows(dev, stream, steps, hbm):
         for _ in range(3):
             fn()
         torch.cuda.synchronize()
-        tot = 0.0
-        for i in range(steps):
-            flush.fill_(float(i))
-            a = torch.cuda.Event(enable_timing=True)
-            b = torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            fn()
-            b.record(stream)
-            torch.cuda.synchronize()
-            tot += a.elapsed_time(b)
-        return tot / steps
+        return median_call_ms(fn, steps, flush, stream)
 
     # frame-feedback embeddings (qp_code_embeddings) of configuration 5's batch:
     # 1024 frames x 15 codes, bf16 rows in, f32 rows out

@@ -1105,10 +1105,13 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
         float part[32];
 #pragma unroll
         for (int t = 0; t < kMaxCtx; ++t) {
-          const float4 kk = t < pos ? unpack4_f16(kh[t]) : (t == pos ? knew : z4);
+          part[t] = part[16 + t] = 0.f;
+          if (t <= pos) {   // later positions are masked; pos is the same in every lane
+            const float4 kk = t < pos ? unpack4_f16(kh[t]) : knew;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh)
-            part[hh * 16 + t] = qn[hh].x * kk.x + qn[hh].y * kk.y + qn[hh].z * kk.z + qn[hh].w * kk.w;
+            for (int hh = 0; hh < 2; ++hh)
+              part[hh * 16 + t] = qn[hh].x * kk.x + qn[hh].y * kk.y + qn[hh].z * kk.z + qn[hh].w * kk.w;
+          }
         }
         const bool valid = (lane >> 4) < nh && (lane & 15) <= pos;
         const float rsum = reduce_scatter32(part, lane);   // all 32 lanes take part
@@ -1131,11 +1134,13 @@ __device__ bool sm_attn(const SParams& p, SMisc& ms, int k, int l) {
             vh[t] = t < pos ? __ldcg(reinterpret_cast<const uint2*>(kvb + (size_t(t) * 2 + 1) * p.kvw)) : make_uint2(0, 0);
 #pragma unroll
         for (int t = 0; t < kMaxCtx; ++t) {
-          const float4 vv = t < pos ? unpack4_f16(vh[t]) : (t == pos ? vnew : z4);
+          if (t <= pos) {
+            const float4 vv = t < pos ? unpack4_f16(vh[t]) : vnew;
 #pragma unroll
-          for (int hh = 0; hh < 2; ++hh) {
-            const float w = __shfl_sync(0xffffffffu, pr, hh * 16 + t);
-            o2[hh].x += w * vv.x; o2[hh].y += w * vv.y; o2[hh].z += w * vv.z; o2[hh].w += w * vv.w;
+            for (int hh = 0; hh < 2; ++hh) {
+              const float w = __shfl_sync(0xffffffffu, pr, hh * 16 + t);
+              o2[hh].x += w * vv.x; o2[hh].y += w * vv.y; o2[hh].z += w * vv.z; o2[hh].w += w * vv.w;
+            }
           }
         }
         for (int hh = 0; hh < nh; ++hh)
