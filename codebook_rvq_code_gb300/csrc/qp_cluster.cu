@@ -11,12 +11,14 @@
 //   * attention, one cluster per kv head j: its 8 CTAs multiply the group's
 //     512 q|k|v weight rows (q heads 2j and 2j+1, k head j, v head j: four
 //     128-row tiles) by the normalised input, CTA r taking tile r/2 over
-//     half r%2 of K.  The partial products stay in each CTA's shared memory;
-//     each CTA then adds a frame's two halves straight out of its peers'
-//     shared memory (distributed shared memory), runs that frame's
-//     attention and writes the frame's output row into every peer's operand
-//     of the O projection.  CTA r multiplies O's 128-row tile r over the
-//     group's 256 columns and adds the result into the residual stream;
+//     half r%2 of K.  Each drain stores its partial products, by
+//     asynchronous stores counted on the receiver's mbarrier, into the
+//     receive buffer of the CTA that owns the frame (frame b: CTA b mod 8),
+//     which adds the two halves, runs the frame's attention over the KV cache
+//     it keeps in its tensor memory and stores the frame's output row into
+//     every peer's operand of the O projection.  CTA r multiplies O's
+//     128-row tile r over the group's 256 columns and adds the result into
+//     the residual stream;
 //   * MLP, one cluster per 256 columns of the FFN: the gate and up tiles of
 //     those columns split the same way, SwiGLU from the peers' partials into
 //     every peer's down-projection operand, CTA r adds down's tile r over
@@ -26,13 +28,14 @@
 //     halves, writes them out if asked and folds their argmax into the
 //     frame's decision word with one 64-bit atomic max.
 //
-// A residual row's 1/RMS is known before its operand is built: each CTA
-// sums the squares of its K half and reads its partner's sum, so operands
-// are f16 of the normalised row (no range scaling needed there).  The only
-// grid-wide dependencies are the residual stream after O and after down
-// (counters in global memory, as in the other schedules) and the step's
-// decisions; cluster-local ones use an mbarrier in each CTA that every CTA
-// of the cluster arrives on.  Step 1's projection is spread over all CTAs
+// An operand row is f16(x * w_norm * 2^-e), e from the mean square of the
+// CTA's K half of the row; the drain applies 2^e / RMS, the exact RMS
+// following from this half's sum of squares and the partner's, which
+// arrives while the MMAs run.  The only grid-wide dependencies are the
+// residual stream after O and after down (counters in global memory, as in
+// the other schedules) and the step's decisions; inside a cluster every
+// exchange is an asynchronous store into a peer's shared memory, counted in
+// bytes on the peer's mbarrier.  Step 1's projection is spread over all CTAs
 // (partials added into the residual stream, each unit scaling its H slice
 // into f16's range by a power of two).
 //
