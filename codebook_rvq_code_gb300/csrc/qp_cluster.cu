@@ -1067,7 +1067,7 @@ __device__ bool cl_qkv(const CParams& p, CMisc& ms, CState& st, uint8_t* smem, c
 #pragma unroll
     for (int i = 0; i < 2 * kMaxCtx; ++i) kc[i] = vc[i] = 0u;
   }
-  // the head norms' weights and the new positions' RoPE factors, also ahead of the sync
+  // the head norms' weights and the new positions' RoPE factors, also while the MMAs run
   const CLayer& L = p.layer[l];
   const float4 qnw = __ldg(reinterpret_cast<const float4*>(L.q_norm + lane * 4));
   const float4 knw = __ldg(reinterpret_cast<const float4*>(L.k_norm + lane * 4));
