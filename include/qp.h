@@ -105,8 +105,9 @@ typedef struct qp_geometry {
  *         combination outside these is QP_ERR_WEIGHT_DTYPE.  A Q8_0
  *         matrix is kept twice on the device: as its blocks (the tile
  *         engine dequantises them on chip) and as two f16 images, hi =
- *         f16(d*q) and lo = f16(d*q - hi), for the small-batch engine (4
- *         more bytes per weight); hi + lo = d*q exactly for d >= 2^-14.
+ *         f16(d*q) and lo = f16(d*q - hi), for the small-batch and cluster
+ *         engines (4 more bytes per weight); hi + lo = d*q exactly for
+ *         d >= 2^-14.
  * dev_ptr: device memory, row-major HF layout [shape[0], shape[1]]; a Q8_0
  *         tensor is its raw block stream, shape[0] rows of shape[1]/32
  *         blocks.  Vectors use shape = {n, 0}. */
